@@ -1,0 +1,128 @@
+"""Seeded synthetic inputs: weights, prompts, tap rows, hc streams, KV.
+
+This module holds no arithmetic of the method: it only draws numbers.  It is
+the one module that both the CUDA path's callers and the CPU oracle's callers
+use, so that both see the same inputs.
+
+Every tensor is drawn from its own counter-keyed Philox stream (key = base
+seed, a stable id of the tensor's name, chunk index), so a tensor's values do
+not depend on which other tensors were drawn or in which order, and large
+tensors are drawn in parallel chunks.  Weights are N(0, std) in fp32, rounded
+to bf16 for bf16 models; norm weights are ones; prompts are uniform ids.
+"""
+
+from __future__ import annotations
+
+import os
+import zlib
+from concurrent.futures import ThreadPoolExecutor
+from typing import Dict, List, Sequence
+
+import numpy as np
+import torch
+
+_CHUNK = 1 << 22
+_THREADS = max(1, min(16, os.cpu_count() or 1))
+
+WEIGHT_SEED = 0
+PROMPT_SEED = 1
+TAP_SEED = 2
+KV_SEED = 3
+
+
+def _key(seed: int, name: str, chunk: int) -> int:
+    return (int(seed) << 64) | (zlib.crc32(name.encode()) << 32) | int(chunk)
+
+
+def _draw_chunk(args):
+    seed, name, chunk, count = args
+    rng = np.random.Generator(np.random.Philox(key=_key(seed, name, chunk)))
+    return rng.standard_normal(count, dtype=np.float32)
+
+
+def normal(shape: Sequence[int], std: float, seed: int, name: str) -> np.ndarray:
+    """N(0, std^2) fp32 array of `shape`, keyed by (seed, name)."""
+    total = int(np.prod(shape))
+    jobs = [(seed, name, c, min(_CHUNK, total - c * _CHUNK))
+            for c in range((total + _CHUNK - 1) // _CHUNK)]
+    if len(jobs) > 1:
+        with ThreadPoolExecutor(_THREADS) as ex:
+            parts = list(ex.map(_draw_chunk, jobs))
+    else:
+        parts = [_draw_chunk(j) for j in jobs] or [np.zeros(0, np.float32)]
+    out = np.concatenate(parts) if len(parts) > 1 else parts[0]
+    if std != 1.0:
+        out *= np.float32(std)
+    return out.reshape(shape)
+
+
+def as_torch(a: np.ndarray, dtype: torch.dtype) -> torch.Tensor:
+    return torch.from_numpy(a).to(dtype)
+
+
+def uniform_ids(n: int, vocab: int, seed: int = PROMPT_SEED, name: str = "prompt") -> np.ndarray:
+    rng = np.random.Generator(np.random.Philox(key=_key(seed, name, 0)))
+    return rng.integers(0, vocab, size=n, dtype=np.int64).astype(np.int32)
+
+
+LAYER_KEYS = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+NORM_KEYS = ("ln_attn", "ln_mlp", "q_norm", "k_norm")
+
+
+def layer_shapes(hidden: int, n_q: int, n_kv: int, head_dim: int, ffn: int) -> Dict[str, tuple]:
+    """nn.Linear layouts [out, in] of one Qwen3-shaped decoder layer."""
+    return {
+        "wq": (n_q * head_dim, hidden),
+        "wk": (n_kv * head_dim, hidden),
+        "wv": (n_kv * head_dim, hidden),
+        "wo": (hidden, n_q * head_dim),
+        "w_gate": (ffn, hidden),
+        "w_up": (ffn, hidden),
+        "w_down": (hidden, ffn),
+    }
+
+
+def decoder_layers(prefix: str, n_layers: int, hidden: int, n_q: int, n_kv: int,
+                   head_dim: int, ffn: int, dtype: torch.dtype, std: float = 0.02,
+                   seed: int = WEIGHT_SEED) -> List[Dict[str, torch.Tensor]]:
+    """Weights of n_layers decoder layers as CPU tensors.
+
+    Projections are N(0, std) drawn in fp32 and cast to `dtype` (fp32 or
+    bf16); norm weights (attention/MLP input norms, q/k head norms) are fp32
+    ones.
+    """
+    shapes = layer_shapes(hidden, n_q, n_kv, head_dim, ffn)
+    layers = []
+    for l in range(n_layers):
+        lw = {}
+        for k in LAYER_KEYS:
+            lw[k] = as_torch(normal(shapes[k], std, seed, f"{prefix}.{l}.{k}"), dtype)
+        lw["ln_attn"] = torch.ones(hidden, dtype=torch.float32)
+        lw["ln_mlp"] = torch.ones(hidden, dtype=torch.float32)
+        lw["q_norm"] = torch.ones(head_dim, dtype=torch.float32)
+        lw["k_norm"] = torch.ones(head_dim, dtype=torch.float32)
+        layers.append(lw)
+    return layers
+
+
+def matrix(name: str, rows: int, cols: int, dtype: torch.dtype, std: float = 0.02,
+           seed: int = WEIGHT_SEED) -> torch.Tensor:
+    return as_torch(normal((rows, cols), std, seed, name), dtype)
+
+
+def tap_rows(n_rows: int, width: int, dtype: torch.dtype = torch.bfloat16,
+             seed: int = TAP_SEED, name: str = "taps") -> torch.Tensor:
+    """N(0, 1) hidden rows standing in for target taps, [n_rows, width]."""
+    return as_torch(normal((n_rows, width), 1.0, seed, name), dtype)
+
+
+def hc_streams(n_layers: int, n_rows: int, hc: int, hidden: int,
+               dtype: torch.dtype = torch.bfloat16, seed: int = TAP_SEED) -> torch.Tensor:
+    """[n_layers, n_rows, hc * hidden] N(0, 1) hyper-connection streams."""
+    return as_torch(normal((n_layers, n_rows, hc * hidden), 1.0, seed, "hc"), dtype)
+
+
+def kv_rows(n_layers: int, n_kv: int, n_pos: int, head_dim: int,
+            dtype: torch.dtype = torch.bfloat16, seed: int = KV_SEED) -> torch.Tensor:
+    """[n_layers, 2, n_kv, n_pos, head_dim] N(0, 1) synthetic K/V."""
+    return as_torch(normal((n_layers, 2, n_kv, n_pos, head_dim), 1.0, seed, "kv"), dtype)
