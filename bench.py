@@ -1,0 +1,454 @@
+#!/usr/bin/env python3
+"""Throughput of the DFlash speculative round on GB300.
+
+One step = one full round of the hot path on the end-to-end workload
+(36-layer Qwen3-4B-shaped bf16 target, 5-layer drafter, block 16,
+1024-token seeded prompt): drafter forward over the masked block, batched
+verify forward of the 16 rows, first-mismatch acceptance with KV rollback,
+and the tap commit (fc + context K/V projection) of the accepted rows.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  `value` is rounds/s of device time (CUDA graph of
+one round, replayed K times, inputs resident in HBM; weights stream 9.9 GB
+per round, far larger than L2, so no flush is needed); `e2e` is the same
+workload driven through the public Python API from a host prompt to 512
+tokens on the host.  `--impl reference` times the CPU oracle on a bounded
+sample of the same round.  Under torchrun each rank runs an independent
+replica (the round does not shard).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DFlash draft+verify rounds/s and accepted tok/s at block 16; % of HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="(debug) override target layers; lines printed with it are not the workload")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.p:
+            self.p.terminate()
+            try:
+                self.p.wait(5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+
+    def summary(self):
+        self.f.flush()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons)}
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs_sustained", "hbm_gbs"):
+                if k in d and d[k]:
+                    return float(d[k]), f"measured ({k})"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
+
+
+def traffic_from_profiles():
+    """Per-launch DRAM bytes of the GEMM from the committed ncu summary, if any."""
+    p = os.path.join(ROOT, "profiles", "gemm_skinny_traffic.json")
+    if os.path.exists(p):
+        try:
+            return json.load(open(p))
+        except Exception:
+            return None
+    return None
+
+
+# ----------------------------------------------------------------- oracle sample
+
+class OracleRoundSample:
+    """The CPU oracle timed on a bounded sample of one speculative round of
+    workload `w`, extrapolated to the full round.
+
+    Pieces: the drafter's uncached context re-projection (fc over the
+    prompt's taps), one whole 1-layer drafter forward (fc + layer + LM head),
+    one target decoder layer verifying 16 rows over a synthetic
+    prompt-length KV cache, and one LM head over the full vocabulary.
+    Round time = t_fc + drf_layers * t_draft_layer + tgt_layers *
+    t_target_layer + 2 * t_head.  One untimed LM-head call warms the
+    allocator first.
+    """
+
+    PIECES = ("head", "fc", "draft", "target")
+
+    def __init__(self, w):
+        import numpy as np
+        import torch
+        from block_diffusion_speculative_gather_gb300 import synth
+        from oracle import dflash_oracle as O
+        self.O, self.np, self.w = O, np, w
+        H, B, n = w.hidden, w.block, w.prompt_len
+        self.cfg = O.OracleConfig(hidden=H, n_q=w.n_q, n_kv=w.n_kv, head_dim=w.head_dim,
+                                  ffn=w.ffn, vocab=w.vocab, tgt_layers=1, drf_layers=1,
+                                  tap_layers=[0], block=B, window=w.window)
+        np32 = lambda t: t.float().numpy()
+        layers = lambda prefix: [{k: np32(v) for k, v in lw.items()} for lw in
+                                 synth.decoder_layers(prefix, 1, H, w.n_q, w.n_kv, w.head_dim,
+                                                      w.ffn, torch.bfloat16)]
+        self.embed = np32(synth.matrix("embed", w.vocab, H, torch.bfloat16))
+        fc = np32(synth.matrix("fc", H, w.n_taps * H, torch.bfloat16))
+        self.taps = np32(synth.tap_rows(n, w.n_taps * H))
+        ones = np.ones(H, np.float32)
+        self.tl = layers("tgt")[0]
+        self.dw = O.DraftWeights(layers("drf"), fc, ones, ones)
+        kv = synth.kv_rows(1, w.n_kv, n, w.head_dim)
+        self.cache = O.KVCache(1, w.n_kv, w.head_dim)
+        self.cache.write(0, range(n), np.moveaxis(np32(kv[0, 0]), 0, 1),
+                         np.moveaxis(np32(kv[0, 1]), 0, 1))
+        self.h = np.random.default_rng(0).standard_normal((B, H))
+        O.linear(self.h, self.embed)                       # warm-up, untimed
+        self.t = {}
+
+    def time_piece(self, name: str) -> float:
+        O, w, n, B = self.O, self.w, self.w.prompt_len, self.w.block
+        tic = time.perf_counter()
+        if name == "head":
+            O.linear(self.h, self.embed)
+        elif name == "fc":
+            O.draft_context(self.dw, self.cfg, self.taps)
+        elif name == "draft":
+            O.draft_forward(self.dw, self.embed, self.cfg, self.taps, 17, n, B)
+        else:
+            x = self.embed[self.np.arange(1, B + 1)].astype(self.np.float64)
+            O.target_layer(x, self.tl, self.cfg, list(range(n, n + B)), self.cache, 0)
+        self.t[name] = time.perf_counter() - tic
+        return self.t[name]
+
+    def round_s(self) -> float:
+        t, w = self.t, self.w
+        t_draft_layer = max(0.0, t["draft"] - t["fc"] - t["head"])
+        return t["fc"] + w.drf_layers * t_draft_layer + w.tgt_layers * t["target"] + 2 * t["head"]
+
+    def describe(self) -> str:
+        t, w = self.t, self.w
+        return (f"timed pieces, fp64 numpy (OpenBLAS): fc context re-projection over "
+                f"{w.prompt_len} taps {t['fc']:.2f} s; 1-layer drafter forward {t['draft']:.2f} s; "
+                f"1 of {w.tgt_layers} target layers verifying {w.block} rows over a "
+                f"{w.prompt_len}-position cache {t['target']:.2f} s; one {w.vocab}-row LM head "
+                f"{t['head']:.2f} s; round extrapolated by layer count")
+
+
+def cpu_cores() -> int:
+    return int(os.environ.get("OPENBLAS_NUM_THREADS", 0) or os.cpu_count() or 1)
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from block_diffusion_speculative_gather_gb300 import build
+    build.build()
+    from block_diffusion_speculative_gather_gb300 import capi, synth
+    from block_diffusion_speculative_gather_gb300.configs import E2E_BF16
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+
+    rank, world, local = rank_info()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    w = E2E_BF16
+    if args.layers:
+        w = w.with_(tgt_layers=args.layers,
+                    tap_layers=tuple(min(t, args.layers - 1) for t in range(5)))
+    model = synth.ModelTensors(w)
+    dec = DFlash(w, model)
+    del model
+    prompt = torch.from_numpy(synth.uniform_ids(w.prompt_len, w.vocab))
+    B = w.block
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # launches per round
+    dec.prefill(prompt, w.n_new)
+    torch.cuda.synchronize()
+    l0 = capi.dflash_launch_count()
+    dec.verify(dec.draft())
+    torch.cuda.synchronize()
+    launches_per_round = capi.dflash_launch_count() - l0
+    for _ in range(args.warmup):
+        dec.verify(dec.draft())
+    dec.check()
+
+    # one round captured as a CUDA graph (state lives on the device)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dec.verify(dec.draft())
+    dec.prefill(prompt, w.n_new)
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    st0 = dec.stats()
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        start.record()
+        for _ in range(args.steps):
+            g.replay()
+        end.record()
+        torch.cuda.synchronize()
+        barrier()
+    ms = start.elapsed_time(end)
+    st1 = dec.stats()
+    dec.check()
+    clocks = clk.summary()
+    t_max = ms
+    rounds_total = args.steps * world
+    emitted = st1.emitted - st0.emitted
+    if world > 1:
+        tt = torch.tensor([ms, float(emitted)], device="cuda")
+        mx = tt.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        dist.all_reduce(tt, op=dist.ReduceOp.SUM)
+        t_max = float(mx[0])
+        emitted = float(tt[1])
+    value = rounds_total / (t_max / 1e3)
+
+    # GEMM timing: the same round captured with event nodes around each GEMM
+    capi.dflash_profile(dec.ctx, 1)
+    gp = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gp, stream=s):
+        dec.verify(dec.draft())
+    prof_ms, prof_bytes, prof_launch = 0.0, 0.0, 0
+    dec.prefill(prompt, w.n_new)
+    for _ in range(args.steps):
+        gp.replay()
+        p = capi.dflash_profile(dec.ctx, 2)
+        prof_ms += p.gemm_ms
+        prof_bytes += p.gemm_bytes
+        prof_launch += p.gemm_launches
+    capi.dflash_profile(dec.ctx, 0)
+    peak, peak_src = measured_peak()
+    achieved = prof_bytes / (prof_ms / 1e3) / 1e9 if prof_ms > 0 else None
+    traffic = traffic_from_profiles()
+
+    # verify cost against rows (plain greedy step = 1 row, round = 16 rows)
+    t1row = None
+    gg = torch.cuda.CUDAGraph()
+    dec.prefill(prompt, w.n_new)
+    with torch.cuda.graph(gg, stream=s):
+        dec.verify(None)
+    dec.prefill(prompt, w.n_new)
+    for _ in range(3):
+        gg.replay()
+    torch.cuda.synchronize()
+    start.record()
+    for _ in range(args.steps):
+        gg.replay()
+    end.record()
+    torch.cuda.synchronize()
+    t1row = start.elapsed_time(end) / args.steps
+
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": "rounds/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_max / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,0.02) random-init bf16 weights, uniform-random prompt",
+        "config": {
+            "workload": "e2e_bf16: 36-layer Qwen3-4B-shaped bf16 target (hidden 2560, 32q/8kv "
+                        "heads, SwiGLU 9728, vocab 151936) + 5-layer drafter, taps at "
+                        "{0,8,17,26,35}, block 16, 1024-token prompt, natural acceptance",
+            "block": B, "prompt_len": w.prompt_len,
+            "l2": "no flush: each round streams ~9.9 GB of weights, far larger than the 129 MB L2",
+            "timing": "CUDA graph of one round replayed K times, CUDA events on the replay stream",
+            "parallelism": f"replicas x{world}",
+        },
+        "accepted_tok_s": round(emitted / (t_max / 1e3), 3),
+        "tokens_per_round": round(emitted / rounds_total, 4),
+        "verify_ms_T1": round(t1row, 4),
+        "round_ms_T16": round(t_max / args.steps, 4),
+        "gpu_launches": launches_per_round * args.steps,
+        "clocks": clocks,
+        "roofline": {
+            "bound": "hbm", "kernel": "gemm_skinny_kernel (all weight-streaming GEMMs of a round)",
+            "achieved": round(achieved, 1) if achieved else None, "peak": peak,
+            "peak_source": peak_src, "unit": "GB/s",
+            "frac": round(achieved / peak, 4) if achieved else None,
+            "traffic": traffic.get("dram_bytes_per_launch") if traffic else None,
+            "gemm_share_of_round": round(prof_ms / ms, 4) if ms else None,
+            "bytes_per_round": prof_bytes / args.steps,
+        },
+    }
+    if args.layers:
+        result["config"]["workload"] += f" [DEBUG: target layers overridden to {args.layers}]"
+
+    if not args.no_e2e:
+        result["e2e"] = e2e_measure(dec, w, prompt)
+    if not args.no_cpu_baseline and rank == 0:
+        osmp = OracleRoundSample(E2E_BF16)
+        for piece in osmp.PIECES:
+            osmp.time_piece(piece)
+        result["cpu_baseline"] = {"value": round(1.0 / osmp.round_s(), 6), "unit": "rounds/s",
+                                  "cores": cpu_cores(), "kind": "oracle",
+                                  "sample": osmp.describe()}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    dec.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def e2e_measure(dec, w, prompt):
+    """Host prompt in pinned memory -> tokens on the host, through the public
+    Python API: H2D of the prompt, prefill, then rounds until w.n_new tokens,
+    each round reading the emitted tokens back to pinned host memory."""
+    import torch
+    host_prompt = prompt.to(torch.int32).pin_memory()
+    out_tok = torch.empty(w.block, dtype=torch.int32).pin_memory()
+    out_n = torch.empty(1, dtype=torch.int32).pin_memory()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    dev_prompt = host_prompt.to("cuda", non_blocking=True)
+    dec.prefill(dev_prompt, w.n_new)
+    st = dec.stats()
+    tokens = [st.t_n]
+    rounds = 0
+    while len(tokens) < w.n_new and not st.finished:
+        dec.verify(dec.draft())
+        out_tok.copy_(dec.tokens_out, non_blocking=True)
+        out_n.copy_(dec.n_emitted, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        n = int(out_n[0])
+        tokens.extend(out_tok[:n].tolist())
+        rounds += 1
+        st = dec.stats() if n == 0 else st
+        if n == 0:
+            break
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    return {"value": round(rounds / dt, 3), "unit": "rounds/s",
+            "tokens_per_s": round(len(tokens) / dt, 3), "rounds": rounds, "tokens": len(tokens),
+            "includes": "prompt H2D + 1024-token prefill + rounds to 512 tokens, per-round D2H",
+            "h2d_bytes_per_step": round(host_prompt.numel() * 4 / max(1, rounds), 2),
+            "d2h_bytes_per_step": (w.block + 1) * 4}
+
+
+# ----------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The oracle arm: each step times one piece of the round sample in
+    rotation (head, fc, draft, target); the reported round time is
+    re-extrapolated from the latest time of every piece after each step."""
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return
+    from block_diffusion_speculative_gather_gb300.configs import E2E_BF16
+    osmp = OracleRoundSample(E2E_BF16)
+    for piece in osmp.PIECES:              # every piece timed once before the steps
+        osmp.time_piece(piece)
+    rounds = []
+    for i in range(args.warmup + args.steps):
+        osmp.time_piece(osmp.PIECES[i % len(osmp.PIECES)])
+        if i >= args.warmup:
+            rounds.append(osmp.round_s())
+    mean = sum(rounds) / len(rounds)
+    v = 1.0 / mean
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "rounds/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(mean * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same generators as ours)",
+        "config": {"workload": "e2e_bf16 round on the CPU oracle, layer sample extrapolated"},
+        "cpu_baseline": {"value": round(v, 6), "unit": "rounds/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": osmp.describe()},
+        "e2e": {"value": round(v, 6), "unit": "rounds/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,809 @@
+// C ABI of the DFlash round (include/dflash.h): configuration guards,
+// workspace layout, TMA descriptors and the launch sequence of each call.
+//
+// The library never allocates device memory and never synchronises except
+// in dflash_stats / dflash_check; every launch goes to the caller's stream,
+// so the launches of a round can be captured in a CUDA graph.
+
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/dflash.h"
+#include "common.cuh"
+#include "gemm.cuh"
+#include "kernels.cuh"
+
+using namespace dfl;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+#define CUDA_TRY(x)                                                                   \
+    do {                                                                              \
+        cudaError_t e_ = (x);                                                         \
+        if (e_ != cudaSuccess)                                                        \
+            return fail(DFLASH_ERR_CUDA, "%s: %s", #x, cudaGetErrorString(e_));       \
+    } while (0)
+
+#define LAUNCH_TRY(x)                                                                 \
+    do {                                                                              \
+        if ((x) != 0) {                                                               \
+            cudaError_t e_ = cudaGetLastError();                                      \
+            return fail(DFLASH_ERR_CUDA, "%s failed: %s", #x, cudaGetErrorString(e_)); \
+        }                                                                             \
+    } while (0)
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int elem_size(int dtype) { return dtype == DFLASH_F32 ? 4 : 2; }
+
+int max_chunks(const dflash_config& c) { return (c.max_seq + ATTN_CHUNK - 1) / ATTN_CHUNK; }
+
+// ------------------------------------------------------------------ layout
+
+struct Layout {
+    size_t state, x, hn, qkv, qrot, attn, act, taps, cbuf, kvc, rcos, rsin, amax, part, slots,
+        counters, total;
+};
+
+constexpr int MAX_SMS = 256;
+constexpr int MAX_TILES = 8192;
+
+Layout make_layout(const dflash_config& c) {
+    Layout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 1024);
+        return o;
+    };
+    const size_t R = DFL_MAX_ROWS;
+    const int es = elem_size(c.dtype);
+    const int qd = c.n_q * c.head_dim, kvd = c.n_kv * c.head_dim;
+    L.state = take(sizeof(DevState));
+    L.x = take(R * c.hidden * 4);
+    L.hn = take(R * c.hidden * es);
+    L.qkv = take(R * (qd + 2 * kvd) * 4);
+    L.qrot = take(R * qd * es);
+    L.attn = take(R * qd * es);
+    L.act = take(R * c.ffn * es);
+    L.taps = take(R * (size_t)(c.n_taps > 0 ? c.n_taps : 1) * c.hidden * es);
+    L.cbuf = take(R * c.hidden * 4);
+    L.kvc = take(R * 2 * kvd * 4);
+    L.rcos = take(R * (c.head_dim / 2) * 4);
+    L.rsin = take(R * (c.head_dim / 2) * 4);
+    L.amax = take(R * 8);
+    L.part = take((size_t)max_chunks(c) * R * c.n_q * (c.head_dim + 2) * 4);
+    L.slots = take((size_t)MAX_SMS * 2 * GEMM_BN * R * 4);
+    L.counters = take((size_t)MAX_TILES * 4);
+    L.total = off;
+    return L;
+}
+
+// ------------------------------------------------------------------ validation
+
+int validate(const dflash_config* c) {
+    if (!c) return fail(DFLASH_ERR_ARG, "config is NULL");
+    if (c->hidden <= 0 || c->hidden % 64) return fail(DFLASH_ERR_CONFIG, "hidden %d: must be a positive multiple of 64", c->hidden);
+    if (c->head_dim != 64 && c->head_dim != 128) return fail(DFLASH_ERR_CONFIG, "head_dim %d: 64 or 128", c->head_dim);
+    if (c->n_q <= 0 || c->n_kv <= 0 || c->n_q % c->n_kv) return fail(DFLASH_ERR_CONFIG, "n_q %d / n_kv %d: n_q must be a multiple of n_kv", c->n_q, c->n_kv);
+    if ((c->n_q / c->n_kv) * DFL_MAX_ROWS > 256) return fail(DFLASH_ERR_CONFIG, "query group too large");
+    if ((c->n_q * c->head_dim) % 128 || (c->n_kv * c->head_dim) % 128) return fail(DFLASH_ERR_CONFIG, "n_q*head_dim and n_kv*head_dim must be multiples of 128");
+    if (c->ffn <= 0 || c->ffn % 64) return fail(DFLASH_ERR_CONFIG, "ffn %d: multiple of 64", c->ffn);
+    if (c->vocab <= 0 || c->vocab % 128) return fail(DFLASH_ERR_CONFIG, "vocab %d: multiple of 128", c->vocab);
+    if (c->vocab / 128 > MAX_TILES) return fail(DFLASH_ERR_CONFIG, "vocab too large");
+    if (c->block_max < 1 || c->block_max > DFLASH_MAX_BLOCK) return fail(DFLASH_ERR_CONFIG, "block_max %d: 1..16", c->block_max);
+    if (c->tgt_layers < 0 || c->drf_layers < 0 || (c->tgt_layers == 0 && c->drf_layers == 0)) return fail(DFLASH_ERR_CONFIG, "need a target or a drafter");
+    if (c->max_seq < 2) return fail(DFLASH_ERR_CONFIG, "max_seq %d", c->max_seq);
+    if (c->window < 0) return fail(DFLASH_ERR_CONFIG, "window %d", c->window);
+    if (c->dtype != DFLASH_F32 && c->dtype != DFLASH_BF16) return fail(DFLASH_ERR_CONFIG, "dtype %d: F32 or BF16", c->dtype);
+    if (c->drf_layers > 0) {
+        if (c->n_taps < 1 || c->n_taps > DFLASH_MAX_TAPS) return fail(DFLASH_ERR_CONFIG, "n_taps %d: 1..8", c->n_taps);
+        for (int i = 0; i < c->n_taps; ++i) {
+            if (c->tap_layer[i] < 0 || (c->tgt_layers > 0 && c->tap_layer[i] >= c->tgt_layers))
+                return fail(DFLASH_ERR_CONFIG, "tap layer %d out of range", c->tap_layer[i]);
+            if (i > 0 && c->tap_layer[i] <= c->tap_layer[i - 1]) return fail(DFLASH_ERR_CONFIG, "tap layers must increase");
+        }
+    }
+    auto fmt_ok = [&](int f) {
+        if (c->dtype == DFLASH_F32) return f == DFLASH_F32;
+        return f == DFLASH_BF16;   // INT4G64 is accepted once its GEMM is built
+    };
+    if (c->tgt_layers > 0 && !fmt_ok(c->tgt_wfmt)) return fail(DFLASH_ERR_CONFIG, "tgt_wfmt %d not supported with dtype %d", c->tgt_wfmt, c->dtype);
+    if (c->drf_layers > 0 && !fmt_ok(c->drf_wfmt)) return fail(DFLASH_ERR_CONFIG, "drf_wfmt %d not supported with dtype %d", c->drf_wfmt, c->dtype);
+    if (c->eos_id >= c->vocab) return fail(DFLASH_ERR_CONFIG, "eos_id %d >= vocab", c->eos_id);
+    if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return fail(DFLASH_ERR_CONFIG, "rms_eps / rope_theta must be positive");
+    return DFLASH_OK;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// ------------------------------------------------------------------ TMA maps
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encode() {
+    if (g_encode) return DFLASH_OK;
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return DFLASH_OK;
+}
+
+// 2D map over a row-major [rows][inner] matrix, 128-byte swizzled boxes of
+// [box_rows][128 bytes].
+int make_map(CUtensorMap* m, const void* base, int xt, uint64_t inner, uint64_t rows,
+             uint32_t box_rows) {
+    const int es = xt == XT_F32 ? 4 : 2;
+    CUtensorMapDataType dt = xt == XT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                           : xt == XT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (!aligned16(base)) return fail(DFLASH_ERR_ARG, "matrix %p is not 16-byte aligned", base);
+    if ((inner * es) % 16) return fail(DFLASH_ERR_ARG, "row of %llu elements is not a multiple of 16 bytes", (unsigned long long)inner);
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * es};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / es), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return DFLASH_OK;
+}
+
+// ------------------------------------------------------------------ plans
+
+struct GemmPlan {
+    GemmMaps maps;
+    GemmArgs args;   // pointers that vary per call are patched before launch
+    int wfmt, epi, xt, grid;
+    double wbytes;   // weight bytes streamed per launch
+    double abytes;   // algorithmic bytes per launch (weights + activations + outputs)
+};
+
+struct LayerPlans {
+    GemmPlan qkv, o, gateup, down, ctxkv;
+};
+
+}  // namespace
+
+struct dflash_ctx {
+    dflash_config cfg;
+    dflash_weights w;
+    std::vector<dflash_layer> tgt, drf;
+    Layout L;
+    uint8_t* ws;
+    void* kv_t;
+    void* kv_d;
+    int sms;
+    std::vector<LayerPlans> tplan, dplan;
+    GemmPlan lm, fc;
+    float* verify_logits = nullptr;
+    float* draft_logits = nullptr;
+    bool prefilled = false;
+    // dflash_profile state
+    bool prof = false;
+    std::vector<cudaEvent_t> ev;
+    size_t ev_used = 0;
+    long long prof_launches = 0;
+    double prof_bytes = 0, prof_wbytes = 0;
+
+    DevState* st() const { return reinterpret_cast<DevState*>(ws + L.state); }
+    template <typename T> T* buf(size_t off) const { return reinterpret_cast<T*>(ws + off); }
+    int act_xt() const { return cfg.dtype == DFLASH_F32 ? XT_F32 : XT_BF16; }
+    int wf(int f) const { return f == DFLASH_F32 ? WF_F32 : WF_BF16; }
+    size_t cache_layer_stride() const {   // elements per layer (K and V)
+        return (size_t)2 * cfg.n_kv * cfg.max_seq * cfg.head_dim;
+    }
+};
+
+namespace {
+
+int plan_gemm(dflash_ctx* c, GemmPlan* p, int wfmt, int epi, const void* const* w, const int* rows,
+              int nseg, int K, const void* x, int xt) {
+    memset(p, 0, sizeof *p);
+    p->wfmt = wfmt;
+    p->epi = epi;
+    p->xt = xt;
+    const int wxt = wfmt == WF_F32 ? XT_F32 : XT_BF16;
+    int N = 0;
+    for (int i = 0; i < nseg; ++i) {
+        int r = make_map(&p->maps.w[i], w[i], wxt, K, rows[i], epi == EPI_SWIGLU ? 64 : GEMM_BN);
+        if (r) return r;
+        p->args.seg_rows[i] = rows[i];
+        N += rows[i];
+    }
+    int r = make_map(&p->maps.x, x, xt, K, DFL_MAX_ROWS, DFL_MAX_ROWS);
+    if (r) return r;
+    GemmArgs& a = p->args;
+    a.n_seg = nseg;
+    a.K = K;
+    a.kb = K / (wfmt == WF_F32 ? 32 : 64);
+    if (epi == EPI_SWIGLU) {
+        a.N = rows[0];
+        a.n_tiles = rows[0] / 64;
+    } else {
+        a.N = N;
+        a.n_tiles = N / GEMM_BN;
+    }
+    if (a.n_tiles > MAX_TILES) return fail(DFLASH_ERR_CONFIG, "GEMM with %d tiles", a.n_tiles);
+    a.slots = c->buf<float>(c->L.slots);
+    a.counters = c->buf<int>(c->L.counters);
+    a.st = c->st();
+    const long long units = (long long)a.n_tiles * a.kb;
+    p->grid = (int)(units < c->sms ? units : c->sms);
+    const double wes = wfmt == WF_F32 ? 4.0 : 2.0, xes = xt == XT_F32 ? 4.0 : 2.0;
+    p->wbytes = (double)N * K * wes;
+    double outb = 0;
+    if (epi == EPI_STORE) outb = (double)DFL_MAX_ROWS * N * 4;
+    else if (epi == EPI_RESID) outb = 2.0 * DFL_MAX_ROWS * N * 4;
+    else if (epi == EPI_SWIGLU) outb = (double)DFL_MAX_ROWS * a.N * xes;
+    else outb = DFL_MAX_ROWS * 8.0;
+    p->abytes = p->wbytes + (double)DFL_MAX_ROWS * K * xes + outb;
+    return DFLASH_OK;
+}
+
+int run_gemm(dflash_ctx* c, const GemmPlan& p, const GemmArgs& a, cudaStream_t s) {
+    const bool timed = c->prof && c->ev_used + 2 <= c->ev.size();
+    if (timed) cudaEventRecordWithFlags(c->ev[c->ev_used], s, cudaEventRecordExternal);
+    if (launch_gemm(p.wfmt, p.epi, p.xt, p.maps, a, p.grid, s))
+        return fail(DFLASH_ERR_CUDA, "GEMM launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+    if (timed) {
+        cudaEventRecordWithFlags(c->ev[c->ev_used + 1], s, cudaEventRecordExternal);
+        c->ev_used += 2;
+        c->prof_launches += 1;
+        c->prof_bytes += p.abytes;
+        c->prof_wbytes += p.wbytes;
+    }
+    return DFLASH_OK;
+}
+
+int build_layer_plans(dflash_ctx* c, const dflash_layer& lw, int wfmt, bool draft, LayerPlans* lp) {
+    const dflash_config& g = c->cfg;
+    const int H = g.hidden, qd = g.n_q * g.head_dim, kvd = g.n_kv * g.head_dim;
+    const int wf = c->wf(wfmt), xt = c->act_xt();
+    const void* hn = c->ws + c->L.hn;
+    const void* wqkv[3] = {lw.wq, lw.wk, lw.wv};
+    const int rqkv[3] = {qd, kvd, kvd};
+    int r = plan_gemm(c, &lp->qkv, wf, EPI_STORE, wqkv, rqkv, 3, H, hn, xt);
+    if (r) return r;
+    const void* wo[1] = {lw.wo};
+    const int ro[1] = {H};
+    if ((r = plan_gemm(c, &lp->o, wf, EPI_RESID, wo, ro, 1, qd, c->ws + c->L.attn, xt))) return r;
+    const void* wgu[2] = {lw.w_gate, lw.w_up};
+    const int rgu[2] = {g.ffn, g.ffn};
+    if ((r = plan_gemm(c, &lp->gateup, wf, EPI_SWIGLU, wgu, rgu, 2, H, hn, xt))) return r;
+    const void* wd[1] = {lw.w_down};
+    if ((r = plan_gemm(c, &lp->down, wf, EPI_RESID, wd, ro, 1, g.ffn, c->ws + c->L.act, xt))) return r;
+    if (draft) {
+        const void* wkv[2] = {lw.wk, lw.wv};
+        const int rkv[2] = {kvd, kvd};
+        if ((r = plan_gemm(c, &lp->ctxkv, wf, EPI_STORE, wkv, rkv, 2, H, hn, xt))) return r;
+    }
+    return DFLASH_OK;
+}
+
+// ------------------------------------------------------------------ forward pieces
+
+int run_layers(dflash_ctx* c, bool target, cudaStream_t s) {
+    const dflash_config& g = c->cfg;
+    const int H = g.hidden, qd = g.n_q * g.head_dim, kvd = g.n_kv * g.head_dim;
+    const int xt = c->act_xt();
+    const int nl = target ? g.tgt_layers : g.drf_layers;
+    DevState* st = c->st();
+    float* x = c->buf<float>(c->L.x);
+    for (int l = 0; l < nl; ++l) {
+        const dflash_layer& lw = target ? c->tgt[l] : c->drf[l];
+        const LayerPlans& lp = target ? c->tplan[l] : c->dplan[l];
+        LAUNCH_TRY(launch_rmsnorm(x, lw.ln_attn, c->ws + c->L.hn, xt, H, g.rms_eps, ROWS_FWD, 1, st, s));
+        GemmArgs a = lp.qkv.args;
+        a.out = c->buf<float>(c->L.qkv);
+        a.ldo = qd + 2 * kvd;
+        int r = run_gemm(c, lp.qkv, a, s);
+        if (r) return r;
+        uint8_t* cache = reinterpret_cast<uint8_t*>(target ? c->kv_t : c->kv_d) +
+                         (size_t)l * c->cache_layer_stride() * elem_size(g.dtype);
+        const size_t vofs = (size_t)g.n_kv * g.max_seq * g.head_dim * elem_size(g.dtype);
+        QkvArgs q{};
+        q.in = c->buf<float>(c->L.qkv);
+        q.ld_in = qd + 2 * kvd;
+        q.n_q = g.n_q;
+        q.n_kv = g.n_kv;
+        q.head_dim = g.head_dim;
+        q.q_norm = lw.q_norm;
+        q.k_norm = lw.k_norm;
+        q.eps = g.rms_eps;
+        q.q_out = c->ws + c->L.qrot;
+        q.q_type = xt;
+        q.k_cache = cache;
+        q.v_cache = cache + vofs;
+        q.c_type = xt;
+        q.max_seq = g.max_seq;
+        q.row_sel = ROWS_FWD;
+        q.rope_cos = c->buf<float>(c->L.rcos);
+        q.rope_sin = c->buf<float>(c->L.rsin);
+        q.st = st;
+        LAUNCH_TRY(launch_qk_norm_rope(q, s));
+        AttnArgs at{};
+        at.q = c->ws + c->L.qrot;
+        at.k_cache = cache;
+        at.v_cache = cache + vofs;
+        at.kv_type = xt;
+        at.n_q = g.n_q;
+        at.n_kv = g.n_kv;
+        at.head_dim = g.head_dim;
+        at.max_seq = g.max_seq;
+        at.causal = target ? 1 : 0;
+        at.window = target ? 0 : g.window;
+        at.scale = 1.0f / sqrtf((float)g.head_dim);
+        at.part = c->buf<float>(c->L.part);
+        at.out = c->ws + c->L.attn;
+        at.out_type = xt;
+        at.max_chunks = max_chunks(g);
+        at.st = st;
+        LAUNCH_TRY(launch_attention(at, s));
+        a = lp.o.args;
+        a.out = x;
+        a.ldo = H;
+        if ((r = run_gemm(c, lp.o, a, s))) return r;
+        LAUNCH_TRY(launch_rmsnorm(x, lw.ln_mlp, c->ws + c->L.hn, xt, H, g.rms_eps, ROWS_FWD, 1, st, s));
+        a = lp.gateup.args;
+        a.out2 = c->ws + c->L.act;
+        a.ld2 = g.ffn;
+        a.x2t = xt;
+        if ((r = run_gemm(c, lp.gateup, a, s))) return r;
+        a = lp.down.args;
+        a.out = x;
+        a.ldo = H;
+        if (target && g.drf_layers > 0) {
+            for (int i = 0; i < g.n_taps; ++i)
+                if (g.tap_layer[i] == l) {
+                    a.out2 = c->ws + c->L.taps + (size_t)i * H * elem_size(g.dtype);
+                    a.ld2 = g.n_taps * H;
+                    a.x2t = xt;
+                }
+        }
+        if ((r = run_gemm(c, lp.down, a, s))) return r;
+    }
+    return DFLASH_OK;
+}
+
+int run_lm_head(dflash_ctx* c, const float* final_norm, float* logits, cudaStream_t s) {
+    const dflash_config& g = c->cfg;
+    LAUNCH_TRY(launch_rmsnorm(c->buf<float>(c->L.x), final_norm, c->ws + c->L.hn, c->act_xt(),
+                              g.hidden, g.rms_eps, ROWS_FWD, 1, c->st(), s));
+    GemmArgs a = c->lm.args;
+    a.amax = c->buf<unsigned long long>(c->L.amax);
+    a.logits = logits;
+    a.ldl = g.vocab;
+    return run_gemm(c, c->lm, a, s);
+}
+
+// fc -> ctx norm -> per draft layer k/v projection -> k-norm + RoPE -> draft cache,
+// for the rows the device state marks as committed.
+int run_ingest(dflash_ctx* c, cudaStream_t s) {
+    const dflash_config& g = c->cfg;
+    const int H = g.hidden, kvd = g.n_kv * g.head_dim;
+    DevState* st = c->st();
+    GemmArgs a = c->fc.args;
+    a.out = c->buf<float>(c->L.cbuf);
+    a.ldo = H;
+    int r = run_gemm(c, c->fc, a, s);
+    if (r) return r;
+    LAUNCH_TRY(launch_rmsnorm(c->buf<float>(c->L.cbuf), c->w.ctx_norm, c->ws + c->L.hn, c->act_xt(),
+                              H, g.rms_eps, ROWS_COMMIT, g.ctx_norm ? 1 : 0, st, s));
+    for (int l = 0; l < g.drf_layers; ++l) {
+        const LayerPlans& lp = c->dplan[l];
+        a = lp.ctxkv.args;
+        a.out = c->buf<float>(c->L.kvc);
+        a.ldo = 2 * kvd;
+        if ((r = run_gemm(c, lp.ctxkv, a, s))) return r;
+        uint8_t* cache = reinterpret_cast<uint8_t*>(c->kv_d) +
+                         (size_t)l * c->cache_layer_stride() * elem_size(g.dtype);
+        QkvArgs q{};
+        q.in = c->buf<float>(c->L.kvc);
+        q.ld_in = 2 * kvd;
+        q.n_q = 0;
+        q.n_kv = g.n_kv;
+        q.head_dim = g.head_dim;
+        q.k_norm = c->drf[l].k_norm;
+        q.eps = g.rms_eps;
+        q.k_cache = cache;
+        q.v_cache = cache + (size_t)g.n_kv * g.max_seq * g.head_dim * elem_size(g.dtype);
+        q.c_type = c->act_xt();
+        q.max_seq = g.max_seq;
+        q.row_sel = ROWS_COMMIT;
+        q.rope_cos = c->buf<float>(c->L.rcos);
+        q.rope_sin = c->buf<float>(c->L.rsin);
+        q.st = st;
+        LAUNCH_TRY(launch_qk_norm_rope(q, s));
+    }
+    return DFLASH_OK;
+}
+
+RowsArgs rows_args(dflash_ctx* c, int mode) {
+    const dflash_config& g = c->cfg;
+    RowsArgs a{};
+    a.mode = mode;
+    a.hidden = g.hidden;
+    a.vocab = g.vocab;
+    a.mask_id = g.vocab - 1;
+    a.embed = g.tgt_layers > 0 || g.drf_layers > 0 ? c->w.embed : nullptr;
+    a.embed_f32 = g.dtype == DFLASH_F32;
+    a.x = c->buf<float>(c->L.x);
+    a.rope_cos = c->buf<float>(c->L.rcos);
+    a.rope_sin = c->buf<float>(c->L.rsin);
+    a.head_dim = g.head_dim;
+    a.rope_theta = g.rope_theta;
+    a.amax = c->buf<unsigned long long>(c->L.amax);
+    a.st = c->st();
+    return a;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char* dflash_last_error(void) { return g_err.c_str(); }
+
+size_t dflash_workspace_bytes(const dflash_config* cfg) {
+    if (validate(cfg)) return 0;
+    return make_layout(*cfg).total;
+}
+
+size_t dflash_kv_target_bytes(const dflash_config* cfg) {
+    if (validate(cfg)) return 0;
+    return (size_t)cfg->tgt_layers * 2 * cfg->n_kv * cfg->max_seq * cfg->head_dim * elem_size(cfg->dtype);
+}
+
+size_t dflash_kv_draft_bytes(const dflash_config* cfg) {
+    if (validate(cfg)) return 0;
+    return (size_t)cfg->drf_layers * 2 * cfg->n_kv * cfg->max_seq * cfg->head_dim * elem_size(cfg->dtype);
+}
+
+int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_target, void* kv_draft,
+                void* workspace, size_t workspace_bytes, dflash_ctx** out) {
+    int r = validate(cfg);
+    if (r) return r;
+    if (!w || !out) return fail(DFLASH_ERR_ARG, "weights/out is NULL");
+    *out = nullptr;
+    const dflash_config& g = *cfg;
+    // every weight pointer is checked before any buffer is touched
+    if (!aligned16(w->embed)) return fail(DFLASH_ERR_ARG, "embed missing or misaligned");
+    if (g.tgt_layers > 0 && (!w->tgt || !w->final_norm_tgt)) return fail(DFLASH_ERR_ARG, "target weights missing");
+    if (g.drf_layers > 0 && (!w->drf || !w->final_norm_drf || !aligned16(w->fc) || !w->ctx_norm))
+        return fail(DFLASH_ERR_ARG, "draft weights missing");
+    auto check_layer = [&](const dflash_layer& l, const char* who, int i) -> int {
+        const void* ps[7] = {l.wq, l.wk, l.wv, l.wo, l.w_gate, l.w_up, l.w_down};
+        for (const void* p : ps)
+            if (!aligned16(p)) return fail(DFLASH_ERR_ARG, "%s layer %d: projection missing or misaligned", who, i);
+        if (!l.ln_attn || !l.ln_mlp || !l.q_norm || !l.k_norm)
+            return fail(DFLASH_ERR_ARG, "%s layer %d: norm weight missing", who, i);
+        return DFLASH_OK;
+    };
+    for (int i = 0; i < g.tgt_layers; ++i) if ((r = check_layer(w->tgt[i], "target", i))) return r;
+    for (int i = 0; i < g.drf_layers; ++i) if ((r = check_layer(w->drf[i], "draft", i))) return r;
+    const Layout L = make_layout(g);
+    if (!workspace || workspace_bytes < L.total)
+        return fail(DFLASH_ERR_ARG, "workspace %zu bytes < %zu", workspace_bytes, L.total);
+    if (!aligned16(workspace)) return fail(DFLASH_ERR_ARG, "workspace misaligned");
+    if (g.tgt_layers > 0 && !aligned16(kv_target)) return fail(DFLASH_ERR_ARG, "target KV cache missing");
+    if (g.drf_layers > 0 && !aligned16(kv_draft)) return fail(DFLASH_ERR_ARG, "draft KV cache missing");
+    if ((r = get_encode())) return r;
+    int dev = 0;
+    CUDA_TRY(cudaGetDevice(&dev));
+    int sms = 0;
+    CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    if (sms > MAX_SMS) sms = MAX_SMS;
+
+    dflash_ctx* c = new dflash_ctx();
+    c->cfg = g;
+    c->w = *w;
+    c->tgt.assign(w->tgt, w->tgt + g.tgt_layers);
+    c->drf.assign(w->drf, w->drf + g.drf_layers);
+    c->w.tgt = c->tgt.data();
+    c->w.drf = c->drf.data();
+    c->L = L;
+    c->ws = static_cast<uint8_t*>(workspace);
+    c->kv_t = kv_target;
+    c->kv_d = kv_draft;
+    c->sms = sms;
+    c->tplan.resize(g.tgt_layers);
+    c->dplan.resize(g.drf_layers);
+    for (int i = 0; i < g.tgt_layers && !r; ++i) r = build_layer_plans(c, c->tgt[i], g.tgt_wfmt, false, &c->tplan[i]);
+    for (int i = 0; i < g.drf_layers && !r; ++i) r = build_layer_plans(c, c->drf[i], g.drf_wfmt, true, &c->dplan[i]);
+    if (!r) {
+        const void* we[1] = {w->embed};
+        const int re[1] = {g.vocab};
+        r = plan_gemm(c, &c->lm, c->wf(g.dtype), EPI_ARGMAX, we, re, 1, g.hidden, c->ws + L.hn, c->act_xt());
+    }
+    if (!r && g.drf_layers > 0) {
+        const void* wfc[1] = {w->fc};
+        const int rfc[1] = {g.hidden};
+        r = plan_gemm(c, &c->fc, c->wf(g.dtype), EPI_STORE, wfc, rfc, 1, g.n_taps * g.hidden,
+                      c->ws + L.taps, c->act_xt());
+    }
+    if (r) {
+        delete c;
+        return r;
+    }
+    cudaError_t e = cudaMemset(workspace, 0, L.total);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        delete c;
+        return fail(DFLASH_ERR_CUDA, "workspace clear: %s", cudaGetErrorString(e));
+    }
+    *out = c;
+    return DFLASH_OK;
+}
+
+void dflash_destroy(dflash_ctx* ctx) {
+    if (!ctx) return;
+    for (cudaEvent_t e : ctx->ev) cudaEventDestroy(e);
+    delete ctx;
+}
+
+int64_t dflash_launch_count(void) { return g_launches; }
+
+int dflash_profile(dflash_ctx* c, int32_t mode, dflash_profile_t* out) {
+    if (!c) return fail(DFLASH_ERR_ARG, "ctx is NULL");
+    if (mode == 1) {
+        if (c->ev.empty()) {
+            c->ev.resize(1 << 16);
+            for (auto& e : c->ev) CUDA_TRY(cudaEventCreate(&e));
+        }
+        c->ev_used = 0;
+        c->prof_launches = 0;
+        c->prof_bytes = c->prof_wbytes = 0;
+        c->prof = true;
+        return DFLASH_OK;
+    }
+    if (mode == 0) c->prof = false;
+    double ms = 0;
+    for (size_t i = 0; i + 1 < c->ev_used; i += 2) {
+        CUDA_TRY(cudaEventSynchronize(c->ev[i + 1]));
+        float t = 0;
+        CUDA_TRY(cudaEventElapsedTime(&t, c->ev[i], c->ev[i + 1]));
+        ms += t;
+    }
+    if (out) {
+        out->gemm_launches = c->prof_launches;
+        out->gemm_ms = ms;
+        out->gemm_bytes = c->prof_bytes;
+        out->gemm_weight_bytes = c->prof_wbytes;
+    }
+    return DFLASH_OK;
+}
+
+int dflash_set_logits_out(dflash_ctx* ctx, float* verify_logits, float* draft_logits) {
+    if (!ctx) return fail(DFLASH_ERR_ARG, "ctx is NULL");
+    ctx->verify_logits = verify_logits;
+    ctx->draft_logits = draft_logits;
+    return DFLASH_OK;
+}
+
+int dflash_prefill_taps(dflash_ctx* c, const int32_t* prompt_ids, int32_t n_prompt,
+                        const void* ext_taps, int32_t n_ext, int32_t hc, int32_t first_token,
+                        int32_t max_new, dflash_stream_t stream) {
+    if (!c) return fail(DFLASH_ERR_ARG, "ctx is NULL");
+    const dflash_config& g = c->cfg;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (max_new < 1) return fail(DFLASH_ERR_ARG, "max_new %d < 1", max_new);
+    int r;
+    if (g.tgt_layers > 0) {
+        if (!prompt_ids || n_prompt < 1) return fail(DFLASH_ERR_ARG, "prompt missing");
+        if (n_prompt + 1 > g.max_seq) return fail(DFLASH_ERR_CAPACITY, "prompt of %d exceeds max_seq %d", n_prompt, g.max_seq);
+        const int commit_lo = g.window > 0 ? (n_prompt > g.window ? n_prompt - g.window : 0) : 0;
+        for (int p0 = 0; p0 < n_prompt; p0 += DFL_MAX_ROWS) {
+            const int T = n_prompt - p0 < DFL_MAX_ROWS ? n_prompt - p0 : DFL_MAX_ROWS;
+            RowsArgs ra = rows_args(c, FWD_PREFILL);
+            ra.pos0 = p0;
+            ra.T = T;
+            ra.tokens = prompt_ids;
+            LAUNCH_TRY(launch_prepare_rows(ra, s));
+            LAUNCH_TRY(launch_set_chunk(c->st(), p0, T, commit_lo, s));
+            if ((r = run_layers(c, true, s))) return r;
+            if (p0 + T == n_prompt) {
+                if ((r = run_lm_head(c, c->w.final_norm_tgt, c->verify_logits, s))) return r;
+                AcceptArgs aa{};
+                aa.mode = FWD_PREFILL;
+                aa.amax = c->buf<unsigned long long>(c->L.amax);
+                aa.block_max = g.block_max;
+                aa.max_seq = g.max_seq;
+                aa.eos_id = g.eos_id;
+                aa.max_new = max_new;
+                aa.prompt_len = n_prompt;
+                aa.st = c->st();
+                LAUNCH_TRY(launch_accept(aa, s));
+            }
+            if (g.drf_layers > 0 && p0 + T > commit_lo)
+                if ((r = run_ingest(c, s))) return r;
+        }
+    } else {
+        if (!ext_taps || n_ext < 1 || hc < 1) return fail(DFLASH_ERR_ARG, "external taps missing");
+        if (n_ext + g.block_max > g.max_seq) return fail(DFLASH_ERR_CAPACITY, "%d tap rows + block exceed max_seq %d", n_ext, g.max_seq);
+        if (first_token < 0 || first_token >= g.vocab) return fail(DFLASH_ERR_ARG, "first_token %d", first_token);
+        if (g.hidden % 8) return fail(DFLASH_ERR_CONFIG, "hidden must be a multiple of 8");
+        const int commit_lo = g.window > 0 ? (n_ext > g.window ? n_ext - g.window : 0) : 0;
+        const int es = elem_size(g.dtype);
+        for (int p0 = commit_lo / DFL_MAX_ROWS * DFL_MAX_ROWS; p0 < n_ext; p0 += DFL_MAX_ROWS) {
+            const int T = n_ext - p0 < DFL_MAX_ROWS ? n_ext - p0 : DFL_MAX_ROWS;
+            RowsArgs ra = rows_args(c, FWD_PREFILL);
+            ra.pos0 = p0;
+            ra.T = T;
+            ra.embed = nullptr;
+            ra.amax = nullptr;
+            LAUNCH_TRY(launch_prepare_rows(ra, s));
+            LAUNCH_TRY(launch_set_chunk(c->st(), p0, T, commit_lo, s));
+            TapArgs ta{};
+            for (int i = 0; i < g.n_taps; ++i)
+                ta.src[i] = static_cast<const uint8_t*>(ext_taps) +
+                            ((size_t)i * n_ext + p0) * hc * g.hidden * es;
+            ta.n_layers = g.n_taps;
+            ta.rows = T;
+            ta.hc = hc;
+            ta.hidden = g.hidden;
+            ta.in_type = c->act_xt();
+            ta.out = c->ws + c->L.taps;
+            ta.out_type = c->act_xt();
+            ta.out_row_stride = (long long)g.n_taps * g.hidden;
+            LAUNCH_TRY(launch_tap_reduce(ta, s));
+            if ((r = run_ingest(c, s))) return r;
+        }
+        LAUNCH_TRY(launch_set_ext_state(c->st(), n_ext, first_token, max_new, g.block_max, g.max_seq,
+                                        g.eos_id, s));
+    }
+    c->prefilled = true;
+    return DFLASH_OK;
+}
+
+int dflash_draft_block(dflash_ctx* c, int32_t* draft_ids, dflash_stream_t stream) {
+    if (!c) return fail(DFLASH_ERR_ARG, "ctx is NULL");
+    const dflash_config& g = c->cfg;
+    if (g.drf_layers == 0) return fail(DFLASH_ERR_STATE, "no drafter configured");
+    if (!c->prefilled) return fail(DFLASH_ERR_STATE, "draft before prefill");
+    if (!draft_ids) return fail(DFLASH_ERR_ARG, "draft_ids is NULL");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    LAUNCH_TRY(launch_prepare_rows(rows_args(c, FWD_DRAFT), s));
+    int r = run_layers(c, false, s);
+    if (r) return r;
+    if ((r = run_lm_head(c, c->w.final_norm_drf, c->draft_logits, s))) return r;
+    AcceptArgs aa{};
+    aa.mode = FWD_DRAFT;
+    aa.amax = c->buf<unsigned long long>(c->L.amax);
+    aa.draft_out = draft_ids;
+    aa.block_max = g.block_max;
+    aa.st = c->st();
+    LAUNCH_TRY(launch_accept(aa, s));
+    return DFLASH_OK;
+}
+
+int dflash_verify_accept(dflash_ctx* c, const int32_t* draft_ids, int32_t* tokens_out,
+                         int32_t* n_emitted, dflash_stream_t stream) {
+    if (!c) return fail(DFLASH_ERR_ARG, "ctx is NULL");
+    const dflash_config& g = c->cfg;
+    if (g.tgt_layers == 0) return fail(DFLASH_ERR_STATE, "no target configured");
+    if (!c->prefilled) return fail(DFLASH_ERR_STATE, "verify before prefill");
+    if (!tokens_out || !n_emitted) return fail(DFLASH_ERR_ARG, "tokens_out / n_emitted is NULL");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int mode = draft_ids ? FWD_VERIFY : FWD_GREEDY;
+    RowsArgs ra = rows_args(c, mode);
+    ra.tokens = draft_ids;
+    LAUNCH_TRY(launch_prepare_rows(ra, s));
+    int r = run_layers(c, true, s);
+    if (r) return r;
+    if ((r = run_lm_head(c, c->w.final_norm_tgt, c->verify_logits, s))) return r;
+    AcceptArgs aa{};
+    aa.mode = mode;
+    aa.amax = c->buf<unsigned long long>(c->L.amax);
+    aa.draft_ids = draft_ids;
+    aa.tokens_out = tokens_out;
+    aa.n_emitted = n_emitted;
+    aa.block_max = g.block_max;
+    aa.max_seq = g.max_seq;
+    aa.eos_id = g.eos_id;
+    aa.st = c->st();
+    LAUNCH_TRY(launch_accept(aa, s));
+    if (g.drf_layers > 0)
+        if ((r = run_ingest(c, s))) return r;
+    return DFLASH_OK;
+}
+
+int dflash_rollback(dflash_ctx* c, int64_t new_len, int32_t token, dflash_stream_t stream) {
+    if (!c) return fail(DFLASH_ERR_ARG, "ctx is NULL");
+    if (!c->prefilled) return fail(DFLASH_ERR_STATE, "rollback before prefill");
+    if (new_len < 1 || new_len >= c->cfg.max_seq) return fail(DFLASH_ERR_ARG, "new_len %lld", (long long)new_len);
+    if (token < 0 || token >= c->cfg.vocab) return fail(DFLASH_ERR_ARG, "token %d", token);
+    LAUNCH_TRY(launch_rollback(c->st(), (int)new_len, token, c->cfg.block_max, c->cfg.max_seq,
+                               reinterpret_cast<cudaStream_t>(stream)));
+    return DFLASH_OK;
+}
+
+int dflash_stats(dflash_ctx* c, dflash_stats_t* out, dflash_stream_t stream) {
+    if (!c || !out) return fail(DFLASH_ERR_ARG, "NULL argument");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    DevState h;
+    CUDA_TRY(cudaMemcpyAsync(&h, c->st(), sizeof h, cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    memset(out, 0, sizeof *out);
+    out->rounds = h.rounds;
+    out->emitted = h.emitted;
+    for (int j = 0; j < DFLASH_MAX_BLOCK; ++j) out->accept_hist[j] = h.accept_hist[j];
+    out->n = h.n;
+    out->t_n = h.t_n;
+    out->block_len = h.bl;
+    out->generated = h.generated;
+    out->max_new = h.max_new;
+    out->ctx_len = h.ctx_len;
+    out->finished = h.finished;
+    out->last_accept = h.last_a;
+    out->device_error = h.err;
+    return DFLASH_OK;
+}
+
+int dflash_check(dflash_ctx* c, dflash_stream_t stream) {
+    if (!c) return fail(DFLASH_ERR_ARG, "ctx is NULL");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    CUDA_TRY(cudaStreamSynchronize(s));
+    int err[2];
+    CUDA_TRY(cudaMemcpy(err, &c->st()->err, sizeof err, cudaMemcpyDeviceToHost));
+    if (err[0] == DERR_TIMEOUT) return fail(DFLASH_ERR_TIMEOUT, "bounded wait expired (site %d)", err[1]);
+    if (err[0] != DERR_NONE) return fail(DFLASH_ERR_DEVICE, "device error %d (info %d)", err[0], err[1]);
+    return DFLASH_OK;
+}
+
+int dflash_tap_reduce(const void* const* layer_streams, int32_t n_layers, int32_t rows, int32_t hc,
+                      int32_t hidden, float* out, dflash_stream_t stream) {
+    if (!layer_streams || !out) return fail(DFLASH_ERR_ARG, "NULL argument");
+    if (n_layers < 1 || n_layers > 8 || rows < 0 || hc < 1 || hidden < 8 || hidden % 8)
+        return fail(DFLASH_ERR_ARG, "bad shape (layers %d rows %d hc %d hidden %d)", n_layers, rows, hc, hidden);
+    if (rows == 0) return DFLASH_OK;
+    TapArgs ta{};
+    for (int i = 0; i < n_layers; ++i) {
+        if (!aligned16(layer_streams[i])) return fail(DFLASH_ERR_ARG, "stream %d misaligned", i);
+        ta.src[i] = layer_streams[i];
+    }
+    if (!aligned16(out)) return fail(DFLASH_ERR_ARG, "out misaligned");
+    ta.n_layers = n_layers;
+    ta.rows = rows;
+    ta.hc = hc;
+    ta.hidden = hidden;
+    ta.in_type = XT_BF16;
+    ta.out = out;
+    ta.out_type = XT_F32;
+    ta.out_row_stride = (long long)n_layers * hidden;
+    LAUNCH_TRY(launch_tap_reduce(ta, reinterpret_cast<cudaStream_t>(stream)));
+    return DFLASH_OK;
+}
+
+int dflash_quantize_int4g64(const float* w, int32_t n, int32_t k, uint8_t* packed, uint16_t* scales,
+                            dflash_stream_t stream) {
+    if (!w || !packed || !scales) return fail(DFLASH_ERR_ARG, "NULL argument");
+    if (n < 1 || k < 256 || k % 256) return fail(DFLASH_ERR_ARG, "n %d k %d: k must be a multiple of 256", n, k);
+    LAUNCH_TRY(launch_quantize_int4g64(w, n, k, packed, scales, reinterpret_cast<cudaStream_t>(stream)));
+    return DFLASH_OK;
+}
+
+}  // extern "C"

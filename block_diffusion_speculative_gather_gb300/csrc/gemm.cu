@@ -1,0 +1,376 @@
+// Skinny weight-streaming GEMM for the <= 16 rows of one DFlash forward.
+//
+// Y[t][n] = sum_k X[t][k] W[n][k], W in the nn.Linear layout [N][K].  The
+// rows t (block rows, verify rows or a prefill chunk) are few, so the work
+// is a stream of W from HBM: one pass over W per call is the whole cost.
+//
+// Design (sm_103a):
+//  * one persistent CTA per SM; the flattened (tile, k-block) space is split
+//    into equal contiguous ranges (stream-K), so every SM streams the same
+//    number of bytes whatever N and K are;
+//  * a producer warp issues TMA tile loads (cp.async.bulk.tensor, 128-byte
+//    swizzle) of the weight tile [128 rows x 128 B] and the matching
+//    activation tile [16 x 128 B] into an 8-deep shared-memory ring guarded
+//    by mbarriers; 8 consumer warps each own 16 weight rows;
+//  * bf16 weights: the weight rows are the M=16 side of mma.sync m16n8k16
+//    (swap-AB) and the <= 16 activation rows the N side (two n8 tiles);
+//    inside each 64-wide k-block every lane takes 16 consecutive k
+//    (one 32-byte run per row) and the same permutation of k is applied to
+//    both operands, so fragments come from plain 16-byte shared loads;
+//  * fp32 weights (the tiny fp32 workload) use CUDA-core FMAs in k order;
+//  * a tile whose k-range is split across CTAs is finished by the last CTA
+//    to arrive (atomic ticket, no waiting), which sums the parts in a fixed
+//    order: the result of a row never depends on how many rows the forward
+//    has, on timing, or on the other rows (batch invariance);
+//  * fused epilogues: store fp32, residual add (+ tap copy), SwiGLU of
+//    paired gate/up tiles, LM-head argmax with packed 64-bit atomicMax.
+//
+// Every mbarrier wait is bounded; an expired wait sets the device error
+// word, stops new copies and drains the copies already issued.
+
+#include "gemm.cuh"
+
+namespace dfl {
+
+long long g_launches = 0;
+
+namespace {
+
+__device__ __forceinline__ void consumer_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(GEMM_CONSUMERS * 32) : "memory");
+}
+
+__device__ __forceinline__ long long range_start(int b, long long U, int G) {
+    return (long long)b * U / G;
+}
+
+__device__ __forceinline__ int cta_of(long long u, long long U, int G) {
+    int b = (int)((u * G) / U);
+    while (b + 1 < G && range_start(b + 1, U, G) <= u) ++b;
+    while (b > 0 && range_start(b, U, G) > u) --b;
+    return b;
+}
+
+template <typename T>
+__device__ __forceinline__ void store_as(void* base, size_t idx, float v) {
+    reinterpret_cast<T*>(base)[idx] = from_f32<T>(v);
+}
+
+__device__ __forceinline__ void store_xt(void* base, int xt, size_t idx, float v) {
+    if (xt == XT_F32) store_as<float>(base, idx, v);
+    else if (xt == XT_BF16) store_as<__nv_bfloat16>(base, idx, v);
+    else store_as<__half>(base, idx, v);
+}
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+    return a > b ? a : b;
+}
+
+template <int WF, int EPI>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* Ws = smem;
+    uint8_t* Xs = Ws + GEMM_STAGES * GEMM_STAGE_W;
+    float* ctile = reinterpret_cast<float*>(Xs + GEMM_STAGES * GEMM_STAGE_X);  // [16][128]
+    uint64_t* full = reinterpret_cast<uint64_t*>(ctile + DFL_MAX_ROWS * GEMM_BN);
+    uint64_t* empty = full + GEMM_STAGES;
+    volatile int* s_flags = reinterpret_cast<volatile int*>(empty + GEMM_STAGES);
+    // s_flags[0]: abort, [1]: last-arriver, [2]: consumed stage count
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x;
+    const long long U = (long long)a.n_tiles * a.kb;
+    const long long u0 = range_start(blockIdx.x, U, G), u1 = range_start(blockIdx.x + 1, U, G);
+    constexpr int KBLK = (WF == WF_F32) ? 32 : 64;     // k per 128-byte row of a tile
+    constexpr uint32_t STAGE_BYTES = GEMM_STAGE_W + GEMM_STAGE_X;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < GEMM_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], GEMM_CONSUMERS);
+        }
+        s_flags[0] = 0;
+        s_flags[1] = 0;
+        s_flags[2] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == GEMM_CONSUMERS) {
+        // ------------------------------------------------ producer
+        if (lane == 0) {
+            for (int i = 0; i < a.n_seg; ++i) tma_prefetch_desc(&maps.w[i]);
+            tma_prefetch_desc(&maps.x);
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            for (long long u = u0; u < u1; ++u) {
+                if (s_flags[0]) break;
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u)) {
+                    s_flags[0] = 1;
+                    set_error(a.st, DERR_TIMEOUT, 100);
+                    break;
+                }
+                if (s_flags[0]) break;   // consumers gave up: issue nothing more
+                const int tile = (int)(u / a.kb), k = (int)(u % a.kb);
+                uint8_t* wdst = Ws + stage * GEMM_STAGE_W;
+                mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                if (EPI == EPI_SWIGLU) {
+                    tma_load_2d(wdst, &maps.w[0], &full[stage], k * KBLK, tile * 64);
+                    tma_load_2d(wdst + 64 * 128, &maps.w[1], &full[stage], k * KBLK, tile * 64);
+                } else {
+                    int row = tile * GEMM_BN, seg = 0;
+                    while (seg + 1 < a.n_seg && row >= a.seg_rows[seg]) {
+                        row -= a.seg_rows[seg];
+                        ++seg;
+                    }
+                    tma_load_2d(wdst, &maps.w[seg], &full[stage], k * KBLK, row);
+                }
+                tma_load_2d(Xs + stage * GEMM_STAGE_X, &maps.x, &full[stage], k * KBLK, 0);
+                ++issued;
+                if (++stage == GEMM_STAGES) { stage = 0; phase ^= 1u; }
+            }
+            // Wait (bounded) until the consumers have seen every issued copy
+            // land; after an abort, wait (bounded) for the copies still in
+            // flight so none lands after the CTA has exited.
+            const uint64_t t0 = globaltimer_ns();
+            while (s_flags[2] < issued && !s_flags[0]) {
+                if (globaltimer_ns() - t0 > 4000000000ull) {
+                    s_flags[0] = 1;
+                    set_error(a.st, DERR_TIMEOUT, 102);
+                    break;
+                }
+                __nanosleep(256);
+            }
+            if (s_flags[0]) {
+                for (long long j = s_flags[2]; j < issued; ++j)
+                    mbar_wait_bounded(&full[j % GEMM_STAGES], (uint32_t)((j / GEMM_STAGES) & 1),
+                                      100000000ull);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- consumers
+    const int tid = threadIdx.x;   // 0..255
+    const int g = lane >> 2, c = lane & 3;
+    int stage = 0;
+    uint32_t phase = 0;
+    float acc[8];
+    int first_tile_of_me = (int)(u0 / a.kb);
+
+    for (long long u = u0; u < u1; ++u) {
+        const int tile = (int)(u / a.kb), k = (int)(u % a.kb);
+        if (k == 0 || u == u0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        }
+        bool ok = false;
+        if (!s_flags[0]) {
+            ok = mbar_wait_bounded(&full[stage], phase);
+            if (!ok) {
+                s_flags[0] = 1;
+                set_error(a.st, DERR_TIMEOUT, 101);
+            }
+        }
+        if (ok) {
+            const uint8_t* Wt = Ws + stage * GEMM_STAGE_W;
+            const uint8_t* Xt = Xs + stage * GEMM_STAGE_X;
+            if (WF == WF_BF16) {
+                const int r0 = warp * 16 + g;
+                uint32_t ra[8], rb[8], xa[8], xb[8];
+                *reinterpret_cast<uint4*>(&ra[0]) = lds128(Wt + swz128(r0, 2 * c));
+                *reinterpret_cast<uint4*>(&ra[4]) = lds128(Wt + swz128(r0, 2 * c + 1));
+                *reinterpret_cast<uint4*>(&rb[0]) = lds128(Wt + swz128(r0 + 8, 2 * c));
+                *reinterpret_cast<uint4*>(&rb[4]) = lds128(Wt + swz128(r0 + 8, 2 * c + 1));
+                *reinterpret_cast<uint4*>(&xa[0]) = lds128(Xt + swz128(g, 2 * c));
+                *reinterpret_cast<uint4*>(&xa[4]) = lds128(Xt + swz128(g, 2 * c + 1));
+                *reinterpret_cast<uint4*>(&xb[0]) = lds128(Xt + swz128(g + 8, 2 * c));
+                *reinterpret_cast<uint4*>(&xb[4]) = lds128(Xt + swz128(g + 8, 2 * c + 1));
+                float(&d0)[4] = *reinterpret_cast<float(*)[4]>(&acc[0]);
+                float(&d1)[4] = *reinterpret_cast<float(*)[4]>(&acc[4]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t A[4] = {ra[2 * j], rb[2 * j], ra[2 * j + 1], rb[2 * j + 1]};
+                    const uint32_t B0[2] = {xa[2 * j], xa[2 * j + 1]};
+                    const uint32_t B1[2] = {xb[2 * j], xb[2 * j + 1]};
+                    mma_bf16_16816(d0, A, B0);
+                    mma_bf16_16816(d1, A, B1);
+                }
+            } else {  // WF_F32: CUDA-core FMAs, k in order
+                const int t = lane & 15, h = lane >> 4;
+                float xv[32];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 v = lds128(Xt + swz128(t, q));
+                    xv[4 * q + 0] = __uint_as_float(v.x);
+                    xv[4 * q + 1] = __uint_as_float(v.y);
+                    xv[4 * q + 2] = __uint_as_float(v.z);
+                    xv[4 * q + 3] = __uint_as_float(v.w);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = warp * 16 + 8 * h + i;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const uint4 v = lds128(Wt + swz128(row, q));
+                        acc[i] = fmaf(__uint_as_float(v.x), xv[4 * q + 0], acc[i]);
+                        acc[i] = fmaf(__uint_as_float(v.y), xv[4 * q + 1], acc[i]);
+                        acc[i] = fmaf(__uint_as_float(v.z), xv[4 * q + 2], acc[i]);
+                        acc[i] = fmaf(__uint_as_float(v.w), xv[4 * q + 3], acc[i]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+        if (tid == 0 && ok) s_flags[2] = s_flags[2] + 1;   // stages seen complete
+        if (++stage == GEMM_STAGES) { stage = 0; phase ^= 1u; }
+
+        if (!(k == a.kb - 1 || u == u1 - 1)) continue;
+
+        // ------------------------------------------ finish this tile
+        if (WF == WF_BF16) {
+            // C fragment: (row g, tokens 2c,2c+1), (row g+8, tokens 2c,2c+1) per n8 tile
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int t0 = nt * 8 + 2 * c, r = warp * 16 + g;
+                ctile[(t0 + 0) * GEMM_BN + r] = acc[nt * 4 + 0];
+                ctile[(t0 + 1) * GEMM_BN + r] = acc[nt * 4 + 1];
+                ctile[(t0 + 0) * GEMM_BN + r + 8] = acc[nt * 4 + 2];
+                ctile[(t0 + 1) * GEMM_BN + r + 8] = acc[nt * 4 + 3];
+            }
+        } else {
+            const int t = lane & 15, h = lane >> 4;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ctile[t * GEMM_BN + warp * 16 + 8 * h + i] = acc[i];
+        }
+        consumer_bar();
+
+        const long long ts = (long long)tile * a.kb;
+        const int i_first = cta_of(ts, U, G), i_last = cta_of(ts + a.kb - 1, U, G);
+        const bool aborted = s_flags[0] != 0;
+        bool do_epi = !aborted;
+        if (i_first != i_last) {
+            const int slot = (tile == first_tile_of_me) ? 0 : 1;
+            float* mine = a.slots + ((size_t)blockIdx.x * 2 + slot) * (GEMM_BN * DFL_MAX_ROWS);
+            for (int e = tid; e < GEMM_BN * DFL_MAX_ROWS; e += GEMM_CONSUMERS * 32)
+                __stcg(mine + e, ctile[e]);
+            __threadfence();
+            consumer_bar();
+            if (tid == 0) {
+                int last = 0;
+                if (!aborted) {
+                    const int old = atomicAdd(&a.counters[tile], 1);
+                    last = (old == i_last - i_first);
+                }
+                s_flags[1] = last;
+            }
+            consumer_bar();
+            do_epi = s_flags[1] != 0;
+            if (do_epi) {
+                __threadfence();
+                if (tid == 0) a.counters[tile] = 0;
+                for (int e = tid; e < GEMM_BN * DFL_MAX_ROWS; e += GEMM_CONSUMERS * 32) {
+                    float v = 0.f;
+                    for (int i = i_first; i <= i_last; ++i) {
+                        const int first_i = (int)(range_start(i, U, G) / a.kb);
+                        const int si = (tile == first_i) ? 0 : 1;
+                        v += __ldcg(a.slots + ((size_t)i * 2 + si) * (GEMM_BN * DFL_MAX_ROWS) + e);
+                    }
+                    ctile[e] = v;
+                }
+                consumer_bar();
+            }
+        }
+
+        if (do_epi) {
+            if (EPI == EPI_STORE || EPI == EPI_RESID) {
+                const int n0 = tile * GEMM_BN;
+                for (int e = tid; e < GEMM_BN * DFL_MAX_ROWS; e += GEMM_CONSUMERS * 32) {
+                    const int t = e / GEMM_BN, r = e % GEMM_BN;
+                    const size_t o = (size_t)t * a.ldo + n0 + r;
+                    if (EPI == EPI_STORE) {
+                        a.out[o] = ctile[e];
+                    } else {
+                        const float v = a.out[o] + ctile[e];
+                        a.out[o] = v;
+                        if (a.out2) store_xt(a.out2, a.x2t, (size_t)t * a.ld2 + n0 + r, v);
+                    }
+                }
+            } else if (EPI == EPI_SWIGLU) {
+                const int j0 = tile * 64;
+                for (int e = tid; e < 64 * DFL_MAX_ROWS; e += GEMM_CONSUMERS * 32) {
+                    const int t = e / 64, r = e % 64;
+                    const float gt = ctile[t * GEMM_BN + r], up = ctile[t * GEMM_BN + 64 + r];
+                    const float v = gt / (1.f + expf(-gt)) * up;
+                    store_xt(a.out2, a.x2t, (size_t)t * a.ld2 + j0 + r, v);
+                }
+            } else {  // EPI_ARGMAX: warp w reduces tokens 2w, 2w+1
+                const int n0 = tile * GEMM_BN;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int t = warp * 2 + q;
+                    unsigned long long best = 0ull;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = lane * 4 + i;
+                        const float v = ctile[t * GEMM_BN + r];
+                        best = umax64(best, argmax_key(v, n0 + r));
+                        if (a.logits) a.logits[(size_t)t * a.ldl + n0 + r] = v;
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
+                    if (lane == 0) atomicMax(a.amax + t, best);
+                }
+            }
+        }
+        consumer_bar();   // ctile is rewritten by the next tile
+    }
+}
+
+template <int WF, int EPI>
+int launch_one(const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t stream) {
+    constexpr size_t smem = 1024 + GEMM_STAGES * (GEMM_STAGE_W + GEMM_STAGE_X) +
+                            DFL_MAX_ROWS * GEMM_BN * 4 + 2 * GEMM_STAGES * 8 + 64;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(gemm_skinny_kernel<WF, EPI>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return -1;
+        attr_set = true;
+    }
+    gemm_skinny_kernel<WF, EPI><<<grid, GEMM_THREADS, smem, stream>>>(maps, args);
+    ++g_launches;
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace
+
+int launch_gemm(int wfmt, int epi, int xt, const GemmMaps& maps, const GemmArgs& args,
+                int grid, cudaStream_t stream) {
+    (void)xt;
+    if (wfmt == WF_BF16) {
+        switch (epi) {
+            case EPI_STORE: return launch_one<WF_BF16, EPI_STORE>(maps, args, grid, stream);
+            case EPI_RESID: return launch_one<WF_BF16, EPI_RESID>(maps, args, grid, stream);
+            case EPI_SWIGLU: return launch_one<WF_BF16, EPI_SWIGLU>(maps, args, grid, stream);
+            case EPI_ARGMAX: return launch_one<WF_BF16, EPI_ARGMAX>(maps, args, grid, stream);
+        }
+    } else if (wfmt == WF_F32) {
+        switch (epi) {
+            case EPI_STORE: return launch_one<WF_F32, EPI_STORE>(maps, args, grid, stream);
+            case EPI_RESID: return launch_one<WF_F32, EPI_RESID>(maps, args, grid, stream);
+            case EPI_SWIGLU: return launch_one<WF_F32, EPI_SWIGLU>(maps, args, grid, stream);
+            case EPI_ARGMAX: return launch_one<WF_F32, EPI_ARGMAX>(maps, args, grid, stream);
+        }
+    }
+    return -2;
+}
+
+}  // namespace dfl

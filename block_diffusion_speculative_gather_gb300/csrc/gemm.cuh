@@ -1,0 +1,52 @@
+// Skinny GEMM of the DFlash path: Y[t][n] = sum_k X[t][k] * W[n][k] for the
+// <= 16 rows t of one forward (draft block, verify batch or prefill chunk),
+// streaming the weight matrix W once from HBM.
+#pragma once
+
+#include "common.cuh"
+
+namespace dfl {
+
+enum WFmt : int { WF_F32 = 0, WF_BF16 = 1, WF_INT4 = 2 };
+enum Epi : int { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3 };
+enum XType : int { XT_F32 = 0, XT_BF16 = 1, XT_F16 = 2 };
+
+constexpr int GEMM_BN = 128;        // output rows (weight rows) per tile
+constexpr int GEMM_STAGES = 8;      // TMA ring depth
+constexpr int GEMM_CONSUMERS = 8;   // MMA warps, 16 weight rows each
+constexpr int GEMM_THREADS = (GEMM_CONSUMERS + 1) * 32;
+constexpr int GEMM_STAGE_W = GEMM_BN * 128;   // bytes of the weight tile per stage
+constexpr int GEMM_STAGE_X = DFL_MAX_ROWS * 128;  // bytes of the activation tile per stage (f32/bf16)
+
+struct GemmArgs {
+    int N;              // output width (SWIGLU: ffn)
+    int K;              // reduction length
+    int n_tiles;        // tiles of GEMM_BN output rows (SWIGLU: 64 outputs per tile)
+    int kb;             // k-blocks per tile
+    int seg_rows[3];    // rows of weight maps 0..2 (concatenated along N)
+    int n_seg;
+    // epilogue
+    float* out;         // STORE: fp32 [16][ldo]; RESID: residual x fp32 [16][ldo]
+    int ldo;
+    void* out2;         // SWIGLU: activation [16][ld2] (XType x2t); RESID: optional tap copy
+    int ld2;
+    int x2t;            // element type of out2
+    unsigned long long* amax;  // ARGMAX: packed keys [16]
+    float* logits;      // ARGMAX: optional fp32 dump [16][ldl]
+    int ldl;
+    // deterministic split-K across CTAs
+    float* slots;       // [grid][2][GEMM_BN * 16]
+    int* counters;      // [n_tiles], zero between launches
+    DevState* st;
+};
+
+struct GemmMaps {
+    CUtensorMap w[3];   // weight maps (SWIGLU: 0 = gate, 1 = up)
+    CUtensorMap x;      // activation map
+};
+
+// Host: enqueue one GEMM (fmt, epilogue and activation type fixed per call).
+int launch_gemm(int wfmt, int epi, int xt, const GemmMaps& maps, const GemmArgs& args,
+                int grid, cudaStream_t stream);
+
+}  // namespace dfl

@@ -1,0 +1,605 @@
+// Non-GEMM kernels of the DFlash round: row preparation (embedding gather,
+// RoPE angles), RMSNorm, per-head q/k norm + RoPE + KV-cache write, split-KV
+// attention with a fixed chunk size, acceptance / rollback bookkeeping, the
+// hc-stream tap reduce and the INT4 group-64 quantiser.
+//
+// All kernels read the forward's row count and position from the device
+// state, so a round needs no host round-trip; rows beyond the forward's
+// count are written as zeros, which keeps every padded GEMM column zero.
+
+#include "gemm.cuh"
+#include "kernels.cuh"
+
+namespace dfl {
+
+namespace {
+
+template <typename T>
+__device__ __forceinline__ void st_typed(void* base, size_t i, float v) {
+    reinterpret_cast<T*>(base)[i] = from_f32<T>(v);
+}
+
+__device__ __forceinline__ void st_any(void* base, int t, size_t i, float v) {
+    if (t == XT_F32) st_typed<float>(base, i, v);
+    else if (t == XT_BF16) st_typed<__nv_bfloat16>(base, i, v);
+    else st_typed<__half>(base, i, v);
+}
+
+__device__ __forceinline__ float ld_any(const void* base, int t, size_t i) {
+    if (t == XT_F32) return reinterpret_cast<const float*>(base)[i];
+    if (t == XT_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i]);
+    return __half2float(reinterpret_cast<const __half*>(base)[i]);
+}
+
+__device__ __forceinline__ int rows_of(const DevState* st, int sel, int* r0) {
+    if (sel == ROWS_COMMIT) {
+        *r0 = st->fwd_commit_r0;
+        return st->fwd_commit;
+    }
+    *r0 = 0;
+    return st->fwd_T;
+}
+
+// --------------------------------------------------------------- prepare rows
+
+// One CTA: sets the forward descriptor (thread 0), then every CTA gathers
+// its row of the embedding into the fp32 residual and fills the RoPE table.
+__global__ void prepare_rows_kernel(RowsArgs a) {
+    DevState* st = a.st;
+    __shared__ int s_T, s_pos0, s_tok;
+    const int t = blockIdx.x;   // row
+    if (threadIdx.x == 0) {
+        int T = 0, pos0 = 0;
+        if (a.mode == FWD_PREFILL) {
+            T = a.T;
+            pos0 = a.pos0;
+        } else if (!st->finished) {
+            pos0 = st->n;
+            if (a.mode == FWD_DRAFT) T = st->bl > 1 ? st->bl : 0;
+            else if (a.mode == FWD_VERIFY) T = st->bl;
+            else T = 1;   // FWD_GREEDY
+        }
+        int tok = 0;
+        if (t < T) {
+            if (a.mode == FWD_PREFILL) tok = a.tokens ? a.tokens[pos0 + t] : 0;
+            else if (t == 0) tok = st->t_n;
+            else if (a.mode == FWD_DRAFT) tok = a.mask_id;
+            else tok = a.tokens[t - 1];
+            if (tok < 0 || tok >= a.vocab) {
+                set_error(st, DERR_TOKEN, tok);
+                tok = 0;
+            }
+        }
+        s_T = T;
+        s_pos0 = pos0;
+        s_tok = tok;
+        if (t == 0) {
+            st->fwd_T = T;
+            st->fwd_pos0 = pos0;
+            st->fwd_commit = 0;
+            st->fwd_commit_r0 = 0;
+            if (a.mode == FWD_DRAFT) st->draft_bl = T;
+        }
+        if (a.amax) a.amax[t] = 0ull;
+    }
+    __syncthreads();
+    const int T = s_T;
+    float* xr = a.x + (size_t)t * a.hidden;
+    if (t < T && a.embed) {
+        for (int i = threadIdx.x; i < a.hidden; i += blockDim.x) {
+            const size_t e = (size_t)s_tok * a.hidden + i;
+            xr[i] = a.embed_f32 ? reinterpret_cast<const float*>(a.embed)[e]
+                                : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.embed)[e]);
+        }
+    } else if (a.embed) {
+        for (int i = threadIdx.x; i < a.hidden; i += blockDim.x) xr[i] = 0.f;
+    }
+    const int half = a.head_dim / 2;
+    for (int i = threadIdx.x; i < half; i += blockDim.x) {
+        // angle = pos * theta^(-2i/d), in double, rounded once to fp32
+        const double inv = pow((double)a.rope_theta, -2.0 * (double)i / (double)a.head_dim);
+        const double ang = (double)(s_pos0 + t) * inv;
+        a.rope_cos[t * half + i] = (float)cos(ang);
+        a.rope_sin[t * half + i] = (float)sin(ang);
+    }
+}
+
+// --------------------------------------------------------------- RMSNorm
+
+template <typename OT>
+__global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                               OT* __restrict__ out, int hidden, float eps, int row_sel,
+                               int apply, const DevState* st) {
+    const int t = blockIdx.x;
+    int r0;
+    const int n = rows_of(st, row_sel, &r0);
+    OT* o = out + (size_t)t * hidden;
+    if (t < r0 || t >= r0 + n) {
+        for (int i = threadIdx.x; i < hidden; i += blockDim.x) o[i] = from_f32<OT>(0.f);
+        return;
+    }
+    const float* xr = x + (size_t)t * hidden;
+    if (!apply) {
+        for (int i = threadIdx.x; i < hidden; i += blockDim.x) o[i] = from_f32<OT>(xr[i]);
+        return;
+    }
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < hidden; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+    __shared__ float red[32];
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+        v = warp_sum(v);
+        if (threadIdx.x == 0) red[0] = v;
+    }
+    __syncthreads();
+    const float inv = 1.0f / sqrtf(red[0] / (float)hidden + eps);
+    for (int i = threadIdx.x; i < hidden; i += blockDim.x) o[i] = from_f32<OT>(xr[i] * inv * w[i]);
+}
+
+// --------------------------------------------------------------- q/k norm + RoPE + KV write
+
+// One warp per (row, head): head-RMSNorm (q, k), rotate-half RoPE, then q to
+// the attention input and k, v to the cache at the row's absolute position.
+template <int HD>
+__global__ void qk_norm_rope_kernel(QkvArgs a) {
+    constexpr int PER = HD / 32;   // elements per lane; lane holds i = lane + 32 m
+    const int warps = blockDim.x >> 5;
+    const int gw = blockIdx.x * warps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int heads = a.n_q + 2 * a.n_kv;
+    const int t = gw / heads, h = gw % heads;
+    if (t >= DFL_MAX_ROWS) return;
+    int r0;
+    const int n = rows_of(a.st, a.row_sel, &r0);
+    if (t < r0 || t >= r0 + n) return;
+    const int pos = a.st->fwd_pos0 + t;
+    const float* src = a.in + (size_t)t * a.ld_in + (size_t)h * HD;
+    float v[PER];
+#pragma unroll
+    for (int m = 0; m < PER; ++m) v[m] = src[lane + 32 * m];
+    const bool is_q = h < a.n_q, is_k = !is_q && h < a.n_q + a.n_kv;
+    if (is_q || is_k) {
+        const float* nw = is_q ? a.q_norm : a.k_norm;
+        float ss = 0.f;
+#pragma unroll
+        for (int m = 0; m < PER; ++m) ss = fmaf(v[m], v[m], ss);
+        ss = warp_sum(ss);
+        const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
+#pragma unroll
+        for (int m = 0; m < PER; ++m) v[m] = v[m] * inv * nw[lane + 32 * m];
+        // rotate-half: element i pairs with i + HD/2 (same lane, m + PER/2)
+        const float* cs = a.rope_cos + t * (HD / 2);
+        const float* sn = a.rope_sin + t * (HD / 2);
+        float r[PER];
+#pragma unroll
+        for (int m = 0; m < PER / 2; ++m) {
+            const int i = lane + 32 * m;
+            const float c = cs[i], s = sn[i];
+            r[m] = v[m] * c - v[m + PER / 2] * s;
+            r[m + PER / 2] = v[m + PER / 2] * c + v[m] * s;
+        }
+#pragma unroll
+        for (int m = 0; m < PER; ++m) v[m] = r[m];
+    }
+    if (is_q) {
+        const size_t base = ((size_t)t * a.n_q + h) * HD;
+#pragma unroll
+        for (int m = 0; m < PER; ++m) st_any(a.q_out, a.q_type, base + lane + 32 * m, v[m]);
+        return;
+    }
+    if (pos < 0 || pos >= a.max_seq) {
+        set_error(a.st, DERR_INDEX, pos);
+        return;
+    }
+    const int kh = is_k ? h - a.n_q : h - a.n_q - a.n_kv;
+    void* cache = is_k ? a.k_cache : a.v_cache;
+    const size_t base = ((size_t)kh * a.max_seq + pos) * HD;
+#pragma unroll
+    for (int m = 0; m < PER; ++m) st_any(cache, a.c_type, base + lane + 32 * m, v[m]);
+}
+
+// --------------------------------------------------------------- attention
+
+__device__ __forceinline__ void attn_range(const AttnArgs& a, int* lo, int* hi, int* T, int* pos0) {
+    *T = a.st->fwd_T;
+    *pos0 = a.st->fwd_pos0;
+    *hi = *pos0 + *T;
+    *lo = (!a.causal && a.window > 0) ? max(0, *pos0 - a.window) : 0;
+}
+
+// One CTA per (kv head, chunk of ATTN_CHUNK keys): partial softmax state
+// (max m, sum l, unnormalised output o) of every query row of the kv head's
+// query-head group.  Keys outside the range, or after the query under the
+// causal rule, weigh exactly zero.
+template <int HD>
+__global__ void attn_partial_kernel(AttnArgs a) {
+    constexpr int C = ATTN_CHUNK;
+    const int kh = blockIdx.x, c = blockIdx.y;
+    int lo, hi, T, pos0;
+    attn_range(a, &lo, &hi, &T, &pos0);
+    if (T == 0) return;
+    const int k0 = c * C;
+    if (k0 >= hi || k0 + C <= lo) return;
+    extern __shared__ float sm[];
+    float* Ks = sm;                    // [C][HD]
+    float* Vs = Ks + C * HD;           // [C][HD]
+    float* Ps = Vs + C * HD;           // [warps][C]
+    float* Qs = Ps + (blockDim.x >> 5) * C;   // [warps][HD]
+    const int group = a.n_q / a.n_kv;
+    const size_t kbase = (size_t)kh * a.max_seq * HD;
+    for (int e = threadIdx.x; e < C * HD; e += blockDim.x) {
+        const int j = e / HD, d = e % HD;
+        const int key = k0 + j;
+        const bool in = key >= lo && key < hi;
+        Ks[e] = in ? ld_any(a.k_cache, a.kv_type, kbase + (size_t)key * HD + d) : 0.f;
+        Vs[e] = in ? ld_any(a.v_cache, a.kv_type, kbase + (size_t)key * HD + d) : 0.f;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, warps = blockDim.x >> 5;
+    const int nq = group * T;
+    for (int qi = warp; qi < nq; qi += warps) {
+        const int hq = kh * group + qi / T, t = qi % T;
+        const size_t qoff = ((size_t)t * a.n_q + hq) * HD;
+        for (int d = lane; d < HD; d += 32) Qs[warp * HD + d] = ld_any(a.q, a.kv_type, qoff + d);
+        __syncwarp();
+        float s[C / 32];
+        bool valid[C / 32];
+        float m = -INFINITY;
+#pragma unroll
+        for (int jj = 0; jj < C / 32; ++jj) {
+            const int j = lane + 32 * jj, key = k0 + j;
+            float acc = 0.f;
+            for (int d = 0; d < HD; ++d) acc = fmaf(Qs[warp * HD + d], Ks[j * HD + d], acc);
+            s[jj] = acc * a.scale;
+            valid[jj] = key >= lo && key < hi && (!a.causal || key <= pos0 + t);
+            if (valid[jj]) m = fmaxf(m, s[jj]);
+        }
+        m = warp_max(m);
+        float l = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < C / 32; ++jj) {
+            const float p = valid[jj] ? expf(s[jj] - m) : 0.f;
+            Ps[warp * C + lane + 32 * jj] = p;
+            l += p;
+        }
+        l = warp_sum(l);
+        __syncwarp();
+        float* dst = a.part + (((size_t)c * DFL_MAX_ROWS + t) * a.n_q + hq) * (HD + 2);
+        for (int d = lane; d < HD; d += 32) {
+            float o = 0.f;
+            for (int j = 0; j < C; ++j) o = fmaf(Ps[warp * C + j], Vs[j * HD + d], o);
+            dst[2 + d] = o;
+        }
+        if (lane == 0) {
+            dst[0] = m;
+            dst[1] = l;
+        }
+        __syncwarp();
+    }
+}
+
+// Folds the chunks of one (row, q head) in chunk order and normalises.
+template <int HD>
+__global__ void attn_combine_kernel(AttnArgs a) {
+    const int hq = blockIdx.x, t = blockIdx.y, d = threadIdx.x;
+    int lo, hi, T, pos0;
+    attn_range(a, &lo, &hi, &T, &pos0);
+    const size_t o = (size_t)t * a.n_q * HD + (size_t)hq * HD + d;
+    if (t >= T) {
+        st_any(a.out, a.out_type, o, 0.f);
+        return;
+    }
+    const int c_lo = lo / ATTN_CHUNK, c_hi = (hi - 1) / ATTN_CHUNK;
+    float M = -INFINITY;
+    for (int c = c_lo; c <= c_hi; ++c)
+        M = fmaxf(M, a.part[(((size_t)c * DFL_MAX_ROWS + t) * a.n_q + hq) * (HD + 2)]);
+    float L = 0.f, O = 0.f;
+    for (int c = c_lo; c <= c_hi; ++c) {
+        const float* p = a.part + (((size_t)c * DFL_MAX_ROWS + t) * a.n_q + hq) * (HD + 2);
+        const float w = (p[0] == -INFINITY) ? 0.f : expf(p[0] - M);
+        L = fmaf(p[1], w, L);
+        O = fmaf(p[2 + d], w, O);
+    }
+    st_any(a.out, a.out_type, o, O / L);
+}
+
+// --------------------------------------------------------------- acceptance
+
+__global__ void accept_kernel(AcceptArgs a) {
+    if (threadIdx.x != 0) return;
+    DevState* st = a.st;
+    const int T = st->fwd_T;
+    int y[DFL_MAX_ROWS];
+    for (int i = 0; i < DFL_MAX_ROWS; ++i) y[i] = argmax_key_index(a.amax[i]);
+    if (a.mode == FWD_DRAFT) {
+        for (int j = 0; j < a.block_max - 1; ++j)
+            a.draft_out[j] = (j + 1 < T) ? y[j + 1] : -1;
+        return;
+    }
+    const int B = a.block_max;
+    if (a.mode == FWD_PREFILL) {
+        st->t_n = y[T - 1];
+        st->n = a.prompt_len;
+        st->generated = 1;
+        st->max_new = a.max_new;
+        st->ctx_len = a.prompt_len;
+        st->rounds = 0;
+        st->emitted = 0;
+        for (int j = 0; j < 16; ++j) st->accept_hist[j] = 0;
+        st->last_a = 0;
+        st->finished = (a.eos_id >= 0 && st->t_n == a.eos_id) || a.max_new <= 1 ||
+                       st->n >= a.max_seq;
+        const int bl = min(B, min(a.max_new - 1, a.max_seq - st->n));
+        st->bl = st->finished ? 0 : bl;
+        return;
+    }
+    // VERIFY / GREEDY
+    if (T == 0) {
+        *a.n_emitted = 0;
+        for (int j = 0; j < B; ++j) a.tokens_out[j] = -1;
+        st->fwd_commit = 0;
+        return;
+    }
+    int acc = 0;
+    if (a.mode == FWD_VERIFY)
+        while (acc < T - 1 && a.draft_ids[acc] == y[acc]) ++acc;
+    int emit = acc + 1;
+    int fin = 0;
+    if (a.eos_id >= 0) {
+        for (int i = 0; i <= acc; ++i)
+            if (y[i] == a.eos_id) {
+                emit = i + 1;
+                fin = 1;
+                break;
+            }
+    }
+    for (int j = 0; j < B; ++j) a.tokens_out[j] = j < emit ? y[j] : -1;
+    *a.n_emitted = emit;
+    const int n_old = st->n;
+    st->n = n_old + emit;
+    st->t_n = y[emit - 1];
+    st->generated += emit;
+    st->ctx_len = st->n;
+    st->rounds += 1;
+    st->emitted += emit;
+    for (int j = 0; j < acc && j < 16; ++j) st->accept_hist[j] += 1;
+    st->last_a = acc;
+    fin |= st->generated >= st->max_new || st->n >= a.max_seq;
+    st->finished = fin;
+    st->bl = fin ? 0 : min(B, min(st->max_new - st->generated, a.max_seq - st->n));
+    st->fwd_commit_r0 = 0;
+    st->fwd_commit = emit;
+}
+
+__global__ void set_chunk_kernel(DevState* st, int pos0, int T, int commit_lo) {
+    st->fwd_pos0 = pos0;
+    st->fwd_T = T;
+    const int r0 = max(0, commit_lo - pos0);
+    st->fwd_commit_r0 = min(r0, T);
+    st->fwd_commit = max(0, T - st->fwd_commit_r0);
+}
+
+__global__ void rollback_kernel(DevState* st, int new_len, int token, int B, int max_seq) {
+    const int old = st->n;
+    st->n = new_len;
+    st->t_n = token;
+    if (st->ctx_len > new_len) st->ctx_len = new_len;
+    st->generated = max(1, st->generated - (old - new_len));
+    st->finished = st->generated >= st->max_new || new_len >= max_seq;
+    st->bl = st->finished ? 0 : min(B, min(st->max_new - st->generated, max_seq - new_len));
+}
+
+__global__ void set_ext_state_kernel(DevState* st, int n_ext, int tok, int max_new, int B,
+                                     int max_seq, int eos) {
+    st->n = n_ext;
+    st->t_n = tok;
+    st->generated = 1;
+    st->max_new = max_new;
+    st->ctx_len = n_ext;
+    st->rounds = 0;
+    st->emitted = 0;
+    for (int j = 0; j < 16; ++j) st->accept_hist[j] = 0;
+    st->last_a = 0;
+    st->finished = (eos >= 0 && tok == eos) || max_new <= 1 || n_ext >= max_seq;
+    st->bl = st->finished ? 0 : min(B, min(max_new - 1, max_seq - n_ext));
+    st->fwd_T = 0;
+    st->fwd_commit = 0;
+}
+
+// --------------------------------------------------------------- tap reduce
+
+// out[r][i*H + j] = (1/hc) * sum_{s=0..hc-1} src_i[r][s*H + j]; eight
+// consecutive columns per thread (16-byte loads of bf16 streams).
+template <typename IT, typename OT>
+__global__ void tap_reduce_kernel(TapArgs a) {
+    const long long per_row = (long long)a.n_layers * a.hidden / 8;
+    const long long total = per_row * a.rows;
+    const float inv = 1.0f / (float)a.hc;
+    for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < total;
+         v += (long long)gridDim.x * blockDim.x) {
+        const int r = (int)(v / per_row);
+        const int col = (int)(v % per_row) * 8;
+        const int layer = col / a.hidden, j = col % a.hidden;
+        const IT* src = reinterpret_cast<const IT*>(a.src[layer]) +
+                        (size_t)r * a.hc * a.hidden + j;
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        for (int s = 0; s < a.hc; ++s) {
+            if (sizeof(IT) == 2) {
+                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src + (size_t)s * a.hidden));
+                const IT* p = reinterpret_cast<const IT*>(&raw);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] += to_f32<IT>(p[e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] += to_f32<IT>(src[(size_t)s * a.hidden + e]);
+            }
+        }
+        OT* dst = reinterpret_cast<OT*>(a.out) + (size_t)r * a.out_row_stride + col;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dst[e] = from_f32<OT>(acc[e] * inv);
+    }
+}
+
+// --------------------------------------------------------------- INT4 quantiser
+
+// One warp per (row, 256 consecutive k): lane holds 8 consecutive values;
+// lanes 8q..8q+7 form group q.
+__global__ void quantize_int4g64_kernel(const float* __restrict__ w, int n, int k,
+                                        uint8_t* __restrict__ packed, uint16_t* __restrict__ scales) {
+    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int per_row = k / 256;
+    if (gw >= n * per_row) return;
+    const int row = gw / per_row, kb = gw % per_row;
+    const int k0 = kb * 256 + lane * 8;
+    const float* src = w + (size_t)row * k + k0;
+    float v[8];
+    float am = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        v[e] = src[e];
+        am = fmaxf(am, fabsf(v[e]));
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    const __nv_bfloat16 sb = __float2bfloat16_rn(__fdiv_rn(am, 7.0f));
+    const float s = __bfloat162float(sb);
+    uint32_t word = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        int q = 0;
+        if (s > 0.f) {
+            q = (int)rintf(__fdiv_rn(v[e], s));
+            q = max(-8, min(7, q));
+        }
+        word |= (uint32_t)(q + 8) << (4 * e);
+    }
+    *reinterpret_cast<uint32_t*>(packed + (size_t)row * (k / 2) + k0 / 2) = word;
+    if ((lane & 7) == 0) {
+        const int grp = (kb * 256 + lane * 8) / 64;
+        scales[(size_t)grp * n + row] = *reinterpret_cast<const uint16_t*>(&sb);
+    }
+}
+
+inline int ok_launch() {
+    ++g_launches;
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace
+
+int launch_prepare_rows(const RowsArgs& a, cudaStream_t s) {
+    prepare_rows_kernel<<<DFL_MAX_ROWS, 256, 0, s>>>(a);
+    return ok_launch();
+}
+
+int launch_rmsnorm(const float* x, const float* w, void* out, int out_type, int hidden,
+                   float eps, int row_sel, int apply, const DevState* st, cudaStream_t s) {
+    if (out_type == XT_F32)
+        rmsnorm_kernel<float><<<DFL_MAX_ROWS, 256, 0, s>>>(x, w, (float*)out, hidden, eps, row_sel,
+                                                           apply, st);
+    else if (out_type == XT_BF16)
+        rmsnorm_kernel<__nv_bfloat16><<<DFL_MAX_ROWS, 256, 0, s>>>(x, w, (__nv_bfloat16*)out, hidden,
+                                                                   eps, row_sel, apply, st);
+    else
+        rmsnorm_kernel<__half><<<DFL_MAX_ROWS, 256, 0, s>>>(x, w, (__half*)out, hidden, eps, row_sel,
+                                                            apply, st);
+    return ok_launch();
+}
+
+int launch_qk_norm_rope(const QkvArgs& a, cudaStream_t s) {
+    const int heads = a.n_q + 2 * a.n_kv;
+    const int warps = 8;
+    const int blocks = (DFL_MAX_ROWS * heads + warps - 1) / warps;
+    if (a.head_dim == 128) qk_norm_rope_kernel<128><<<blocks, warps * 32, 0, s>>>(a);
+    else if (a.head_dim == 64) qk_norm_rope_kernel<64><<<blocks, warps * 32, 0, s>>>(a);
+    else return -2;
+    return ok_launch();
+}
+
+int launch_attention(const AttnArgs& a, cudaStream_t s) {
+    const int threads = 256;
+    const size_t smem =
+        (size_t)(2 * ATTN_CHUNK * a.head_dim + (threads / 32) * (ATTN_CHUNK + a.head_dim)) * 4;
+    dim3 g1(a.n_kv, a.max_chunks), g2(a.n_q, DFL_MAX_ROWS);
+    if (a.head_dim == 128) {
+        static bool set = false;
+        if (!set) {
+            cudaFuncSetAttribute(attn_partial_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+            set = true;
+        }
+        attn_partial_kernel<128><<<g1, threads, smem, s>>>(a);
+        ++g_launches;
+        attn_combine_kernel<128><<<g2, 128, 0, s>>>(a);
+    } else if (a.head_dim == 64) {
+        static bool set = false;
+        if (!set) {
+            cudaFuncSetAttribute(attn_partial_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+            set = true;
+        }
+        attn_partial_kernel<64><<<g1, threads, smem, s>>>(a);
+        ++g_launches;
+        attn_combine_kernel<64><<<g2, 64, 0, s>>>(a);
+    } else {
+        return -2;
+    }
+    return ok_launch();
+}
+
+int launch_accept(const AcceptArgs& a, cudaStream_t s) {
+    accept_kernel<<<1, 32, 0, s>>>(a);
+    return ok_launch();
+}
+
+int launch_set_chunk(DevState* st, int pos0, int T, int commit_lo, cudaStream_t s) {
+    set_chunk_kernel<<<1, 1, 0, s>>>(st, pos0, T, commit_lo);
+    return ok_launch();
+}
+
+int launch_rollback(DevState* st, int new_len, int token, int block_max, int max_seq,
+                    cudaStream_t s) {
+    rollback_kernel<<<1, 1, 0, s>>>(st, new_len, token, block_max, max_seq);
+    return ok_launch();
+}
+
+int launch_set_ext_state(DevState* st, int n_ext, int first_token, int max_new, int block_max,
+                         int max_seq, int eos_id, cudaStream_t s) {
+    set_ext_state_kernel<<<1, 1, 0, s>>>(st, n_ext, first_token, max_new, block_max, max_seq,
+                                         eos_id);
+    return ok_launch();
+}
+
+int launch_tap_reduce(const TapArgs& a, cudaStream_t s) {
+    const long long vecs = (long long)a.rows * a.n_layers * a.hidden / 8;
+    const int threads = 256;
+    long long blocks = (vecs + threads - 1) / threads;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    if (a.in_type == XT_BF16 && a.out_type == XT_F32)
+        tap_reduce_kernel<__nv_bfloat16, float><<<(int)blocks, threads, 0, s>>>(a);
+    else if (a.in_type == XT_BF16 && a.out_type == XT_BF16)
+        tap_reduce_kernel<__nv_bfloat16, __nv_bfloat16><<<(int)blocks, threads, 0, s>>>(a);
+    else if (a.in_type == XT_F32 && a.out_type == XT_F32)
+        tap_reduce_kernel<float, float><<<(int)blocks, threads, 0, s>>>(a);
+    else
+        return -2;
+    return ok_launch();
+}
+
+int launch_quantize_int4g64(const float* w, int n, int k, uint8_t* packed, uint16_t* scales,
+                            cudaStream_t s) {
+    const long long warps = (long long)n * (k / 256);
+    const int per_block = 8;
+    quantize_int4g64_kernel<<<(int)((warps + per_block - 1) / per_block), per_block * 32, 0, s>>>(
+        w, n, k, packed, scales);
+    return ok_launch();
+}
+
+}  // namespace dfl

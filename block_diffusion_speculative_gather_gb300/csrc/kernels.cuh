@@ -1,0 +1,118 @@
+// Launchers of the non-GEMM kernels of the DFlash round.
+#pragma once
+
+#include "common.cuh"
+
+namespace dfl {
+
+enum FwdMode : int { FWD_PREFILL = 0, FWD_DRAFT = 1, FWD_VERIFY = 2, FWD_GREEDY = 3 };
+enum RowSel : int { ROWS_FWD = 0, ROWS_COMMIT = 1 };
+
+constexpr int ATTN_CHUNK = 64;   // keys per attention split (fixed: batch invariance)
+
+struct RowsArgs {
+    int mode;
+    int hidden, vocab, mask_id;
+    int pos0, T;                 // PREFILL only: chunk position and rows
+    const int32_t* tokens;       // PREFILL: prompt; VERIFY: draft ids; else unused
+    const void* embed;           // [vocab][hidden] (dtype)
+    int embed_f32;               // 1 = fp32 embedding, 0 = bf16
+    float* x;                    // fp32 [16][hidden]
+    float* rope_cos;             // [16][head_dim/2]
+    float* rope_sin;
+    int head_dim;
+    float rope_theta;
+    unsigned long long* amax;    // [16] reset to 0
+    DevState* st;
+};
+
+int launch_prepare_rows(const RowsArgs& a, cudaStream_t s);
+
+// out[t] = RMSNorm(x[t]) * w for the selected rows, zeros for the others.
+// apply = 0: plain conversion of the selected rows (no normalisation).
+int launch_rmsnorm(const float* x, const float* w, void* out, int out_type, int hidden,
+                   float eps, int row_sel, int apply, const DevState* st, cudaStream_t s);
+
+struct QkvArgs {
+    const float* in;        // fp32 [16][ld_in]: q heads, then k heads, then v heads
+    int ld_in;
+    int n_q, n_kv, head_dim;
+    const float* q_norm;    // [head_dim] (unused when n_q == 0)
+    const float* k_norm;
+    float eps;
+    void* q_out;            // [16][n_q][head_dim], type q_type
+    int q_type;
+    void* k_cache;          // layer base of K: [n_kv][max_seq][head_dim], type c_type
+    void* v_cache;
+    int c_type;
+    int max_seq;
+    int row_sel;            // ROWS_FWD: rows of the forward at fwd_pos0
+                            // ROWS_COMMIT: committed rows at fwd_commit_pos0
+    const float* rope_cos;  // [16][head_dim/2] (ROWS_FWD)
+    const float* rope_sin;
+    float rope_theta;       // (ROWS_COMMIT computes its own angles)
+    DevState* st;
+};
+
+int launch_qk_norm_rope(const QkvArgs& a, cudaStream_t s);
+
+struct AttnArgs {
+    const void* q;          // [16][n_q][head_dim]
+    const void* k_cache;    // layer base [n_kv][max_seq][head_dim]
+    const void* v_cache;
+    int kv_type;            // XT_F32 | XT_BF16 (q has the same type)
+    int n_q, n_kv, head_dim, max_seq;
+    int causal;             // 1: key pos <= query pos (verify/prefill); 0: draft block
+    int window;             // draft: context window (0 = all)
+    float scale;
+    float* part;            // [max_chunks][16][n_q][head_dim + 2]
+    void* out;              // [16][n_q * head_dim], type out_type
+    int out_type;
+    int max_chunks;
+    DevState* st;
+};
+
+int launch_attention(const AttnArgs& a, cudaStream_t s);
+
+struct AcceptArgs {
+    int mode;               // FWD_DRAFT | FWD_VERIFY | FWD_GREEDY | FWD_PREFILL (last chunk)
+    const unsigned long long* amax;
+    const int32_t* draft_ids;     // VERIFY
+    int32_t* draft_out;           // DRAFT: [block_max - 1]
+    int32_t* tokens_out;          // VERIFY/GREEDY: [block_max]
+    int32_t* n_emitted;
+    int block_max, max_seq, eos_id;
+    int max_new;                  // PREFILL
+    int prompt_len;               // PREFILL
+    int window;                   // PREFILL: tap rows committed = trailing window
+    DevState* st;
+};
+
+int launch_accept(const AcceptArgs& a, cudaStream_t s);
+
+// Prefill bookkeeping: forward descriptor of chunk (pos0, T) and the rows
+// of it whose taps are committed to the draft context.
+int launch_set_chunk(DevState* st, int pos0, int T, int commit_lo, cudaStream_t s);
+
+int launch_rollback(DevState* st, int new_len, int token, int block_max, int max_seq,
+                    cudaStream_t s);
+
+// Drafter-alone prefill: state after n_ext externally supplied tap rows.
+int launch_set_ext_state(DevState* st, int n_ext, int first_token, int max_new, int block_max,
+                         int max_seq, int eos_id, cudaStream_t s);
+
+struct TapArgs {
+    const void* src[8];   // per tap layer: [rows][hc * hidden] (in_type)
+    int n_layers, rows, hc, hidden;
+    int in_type;          // XT_F32 | XT_BF16
+    void* out;            // [rows][n_layers * hidden], out_type
+    int out_type;
+    long long out_row_stride;   // elements between output rows
+};
+
+int launch_tap_reduce(const TapArgs& a, cudaStream_t s);
+
+int launch_quantize_int4g64(const float* w, int n, int k, uint8_t* packed, uint16_t* scales,
+                            cudaStream_t s);
+
+}  // namespace dfl

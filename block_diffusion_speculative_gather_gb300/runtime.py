@@ -1,0 +1,192 @@
+"""Python harness over the C ABI: PyTorch owns the device memory and the
+stream, the library runs every step of the round in its own kernels.
+
+    dec = DFlash(workload, ModelTensors(workload))
+    dec.prefill(prompt)              # target prefill, or dec.prefill_taps(...)
+    d = dec.draft()                  # draft ids on the device
+    toks, n = dec.verify(d)          # accept + rollback + tap commit
+
+`DFlash.generate` is the speculative loop; `DFlash.greedy` runs the same
+verify kernels one row at a time (plain greedy decoding).
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+from typing import List, Optional
+
+import torch
+
+from . import capi
+from .configs import Workload
+
+
+def _dtype_code(w: Workload) -> int:
+    return capi.DFLASH_F32 if w.dtype == "f32" else capi.DFLASH_BF16
+
+
+def make_config(w: Workload, **over) -> capi.dflash_config:
+    cfg = capi.dflash_config()
+    cfg.hidden, cfg.n_q, cfg.n_kv, cfg.head_dim = w.hidden, w.n_q, w.n_kv, w.head_dim
+    cfg.ffn, cfg.vocab = w.ffn, w.vocab
+    cfg.tgt_layers, cfg.drf_layers = w.tgt_layers, w.drf_layers
+    cfg.n_taps = w.n_taps if w.drf_layers else 0
+    for i, l in enumerate(w.tap_layers[: capi.MAX_TAPS]):
+        cfg.tap_layer[i] = l
+    cfg.block_max, cfg.window, cfg.max_seq, cfg.eos_id = w.block, w.window, w.max_seq, w.eos_id
+    cfg.dtype = _dtype_code(w)
+    cfg.tgt_wfmt = _dtype_code(w)
+    cfg.drf_wfmt = capi.DFLASH_INT4G64 if w.drf_int4 else _dtype_code(w)
+    cfg.ctx_norm = 1 if w.ctx_norm else 0
+    cfg.rms_eps, cfg.rope_theta = w.rms_eps, w.rope_theta
+    for k, v in over.items():
+        setattr(cfg, k, v)
+    return cfg
+
+
+class DFlash:
+    """One generation context on one GPU."""
+
+    def __init__(self, w: Workload, model, device: str = "cuda", stream=None, **cfg_over):
+        self.w = w
+        self.device = torch.device(device)
+        self._stream = stream      # None: the current stream at each call
+        self.cfg = make_config(w, **cfg_over)
+        dev = lambda t: None if t is None else t.to(self.device).contiguous()
+        self.embed = dev(model.embed)
+        self.final_norm_t = dev(model.final_norm_t)
+        self.final_norm_d = dev(model.final_norm_d)
+        self.ctx_norm = dev(model.ctx_norm)
+        self.fc = dev(model.fc)
+        self.tgt = [{k: dev(v) for k, v in lw.items()} for lw in model.tgt]
+        self.drf = [{k: dev(v) for k, v in lw.items()} for lw in model.drf]
+        if w.drf_int4:
+            self._quantize_drafter()
+        kvt = capi.dflash_kv_target_bytes(self.cfg)
+        kvd = capi.dflash_kv_draft_bytes(self.cfg)
+        wsb = capi.dflash_workspace_bytes(self.cfg)
+        if wsb == 0:
+            capi.check(-1)
+        self.kv_target = torch.zeros(max(kvt, 16), dtype=torch.uint8, device=self.device)
+        self.kv_draft = torch.zeros(max(kvd, 16), dtype=torch.uint8, device=self.device)
+        self.workspace = torch.zeros(wsb, dtype=torch.uint8, device=self.device)
+        self._layers_t = (capi.dflash_layer * max(1, len(self.tgt)))(
+            *[self._layer(lw) for lw in self.tgt])
+        self._layers_d = (capi.dflash_layer * max(1, len(self.drf)))(
+            *[self._layer(lw) for lw in self.drf])
+        wts = capi.dflash_weights()
+        wts.embed = self.embed.data_ptr()
+        wts.final_norm_tgt = self.final_norm_t.data_ptr()
+        wts.final_norm_drf = self.final_norm_d.data_ptr()
+        wts.fc = self.fc.data_ptr() if self.fc is not None else None
+        wts.ctx_norm = self.ctx_norm.data_ptr()
+        wts.tgt = C.cast(self._layers_t, C.POINTER(capi.dflash_layer))
+        wts.drf = C.cast(self._layers_d, C.POINTER(capi.dflash_layer))
+        self._weights = wts
+        torch.cuda.synchronize(self.device)
+        self.ctx = capi.dflash_init(self.cfg, wts, self.kv_target, self.kv_draft, self.workspace)
+        B = w.block
+        self.draft_ids = torch.full((max(1, B - 1),), -1, dtype=torch.int32, device=self.device)
+        self.tokens_out = torch.full((B,), -1, dtype=torch.int32, device=self.device)
+        self.n_emitted = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    def _quantize_drafter(self):
+        for lw in self.drf:
+            for k in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down"):
+                wf = lw[k].float().contiguous()
+                n, kk = wf.shape
+                packed = torch.empty((n, kk // 2), dtype=torch.uint8, device=self.device)
+                scales = torch.empty((kk // 64, n), dtype=torch.int16, device=self.device)
+                capi.dflash_quantize_int4g64(wf, packed, scales, self.stream)
+                lw[k] = packed
+                lw["s" + k[1:]] = scales          # wq -> sq, w_gate -> s_gate
+
+    @staticmethod
+    def _layer(lw) -> capi.dflash_layer:
+        l = capi.dflash_layer()
+        for k in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "ln_attn", "ln_mlp",
+                  "q_norm", "k_norm"):
+            setattr(l, k, lw[k].data_ptr())
+        for k in ("sq", "sk", "sv", "so", "s_gate", "s_up", "s_down"):
+            if k in lw:
+                setattr(l, k, lw[k].data_ptr())
+        return l
+
+    @property
+    def stream(self):
+        return self._stream if self._stream is not None else torch.cuda.current_stream(self.device)
+
+    # ------------------------------------------------------------ the calls
+
+    def prefill(self, prompt: torch.Tensor, max_new: int):
+        self._prompt = prompt.to(self.device, torch.int32).contiguous()
+        capi.dflash_prefill_taps(self.ctx, self._prompt, None, 0, 1, 0, max_new, self.stream)
+
+    def prefill_taps(self, taps: torch.Tensor, hc: int, first_token: int, max_new: int):
+        """taps: [n_taps, n_ext, hc * hidden] in the workload dtype."""
+        self._taps = taps.to(self.device).contiguous()
+        capi.dflash_prefill_taps(self.ctx, None, self._taps, self._taps.shape[1], hc,
+                                 first_token, max_new, self.stream)
+
+    def draft(self, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        out = self.draft_ids if out is None else out
+        capi.dflash_draft_block(self.ctx, out, self.stream)
+        return out
+
+    def verify(self, draft_ids: Optional[torch.Tensor]):
+        capi.dflash_verify_accept(self.ctx, draft_ids, self.tokens_out, self.n_emitted,
+                                  self.stream)
+        return self.tokens_out, self.n_emitted
+
+    def rollback(self, new_len: int, token: int):
+        capi.dflash_rollback(self.ctx, new_len, token, self.stream)
+
+    def stats(self) -> capi.dflash_stats_t:
+        return capi.dflash_stats(self.ctx, self.stream)
+
+    def check(self):
+        capi.dflash_check(self.ctx, self.stream)
+
+    def set_logits_out(self, verify_logits=None, draft_logits=None):
+        capi.dflash_set_logits_out(self.ctx, verify_logits, draft_logits)
+
+    # ------------------------------------------------------------ loops
+
+    def _collect(self, out: List[int]):
+        n = int(self.n_emitted.item())
+        out.extend(self.tokens_out[:n].tolist())
+        return n
+
+    def generate(self, prompt: torch.Tensor, max_new: int, draft_fn=None) -> List[int]:
+        """Speculative decoding; draft_fn(dec) may replace the drafter's ids."""
+        self.prefill(prompt, max_new)
+        st = self.stats()
+        out = [st.t_n]
+        while not st.finished and len(out) < max_new:
+            d = draft_fn(self) if draft_fn is not None else self.draft()
+            self.verify(d)
+            self._collect(out)
+            st = self.stats()
+        return out
+
+    def greedy(self, prompt: torch.Tensor, max_new: int) -> List[int]:
+        """Plain greedy decoding through the same verify kernels, one row a step."""
+        self.prefill(prompt, max_new)
+        st = self.stats()
+        out = [st.t_n]
+        while not st.finished and len(out) < max_new:
+            self.verify(None)
+            self._collect(out)
+            st = self.stats()
+        return out
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            capi.dflash_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -126,3 +126,28 @@ def kv_rows(n_layers: int, n_kv: int, n_pos: int, head_dim: int,
             dtype: torch.dtype = torch.bfloat16, seed: int = KV_SEED) -> torch.Tensor:
     """[n_layers, 2, n_kv, n_pos, head_dim] N(0, 1) synthetic K/V."""
     return as_torch(normal((n_layers, 2, n_kv, n_pos, head_dim), 1.0, seed, "kv"), dtype)
+
+
+class ModelTensors:
+    """Every synthetic tensor of a workload (CPU tensors).
+
+    embed [vocab, H] (also the tied LM head), per-layer weights of the target
+    ("tgt") and the drafter ("drf"), fc [H, n_taps*H] and fp32 ones for the
+    final norms and the drafter's context norm.  Drafters stored as INT4 are
+    drawn in fp32; the quantiser of each side turns them into INT4.
+    """
+
+    def __init__(self, w, std: float = 0.02, seed: int = WEIGHT_SEED):
+        dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+        self.w = w
+        self.embed = matrix("embed", w.vocab, w.hidden, dt, std, seed)
+        self.final_norm_t = torch.ones(w.hidden, dtype=torch.float32)
+        self.final_norm_d = torch.ones(w.hidden, dtype=torch.float32)
+        self.ctx_norm = torch.ones(w.hidden, dtype=torch.float32)
+        self.tgt = decoder_layers("tgt", w.tgt_layers, w.hidden, w.n_q, w.n_kv, w.head_dim,
+                                  w.ffn, dt, std, seed)
+        ddt = torch.float32 if w.drf_int4 else dt
+        self.drf = decoder_layers("drf", w.drf_layers, w.hidden, w.n_q, w.n_kv, w.head_dim,
+                                  w.ffn, ddt, std, seed)
+        self.fc = matrix("fc", w.hidden, w.n_taps * w.hidden, dt, std, seed) \
+            if w.drf_layers else None

@@ -1,0 +1,269 @@
+/*
+ * dflash.h -- C ABI of the GB300 (sm_103a) DFlash block-diffusion
+ * speculative-decoding round.
+ *
+ * One round: (1) tap ingest -- target hidden-state taps are hc-mean-reduced,
+ * concatenated and fc-projected into the drafter's context K/V; (2) draft --
+ * one drafter forward over the masked block [t_n, MASK x (bl-1)] attending
+ * over [sliding context | bidirectional block], ending in an LM-head argmax;
+ * (3) verify -- one batched target forward over the 1+m rows
+ * [t_n, d_1..d_m]; (4) accept -- greedy first-mismatch acceptance, then the
+ * target KV positions and the draft context are rolled back to match.
+ *
+ * Sources: "[RFC] DFlash" (ExecuTorch PR #20840): "DFlash Overview", "Key
+ * Implementation Details" (Phase 1 taps, Phase 3 draft / verify /
+ * first-mismatch acceptance / KV-cache position rollback), review
+ * "Requested changes" 1 (dynamic block length), 3 (persistent draft KV
+ * cache) and 6 (acceptance cases); "feat: DFlash2 block-diffusion drafter
+ * for Qwen 3.8" (Mference PR #22): block attention over [sliding ctx |
+ * bidirectional block], fp32 residual stream, tap staging, config guards
+ * that fire before any buffer is built; "dflash: the chain verify builds
+ * pipelined ..." (mlx-serve PR #937), first commit: hc-stream mean taps.
+ *
+ * Memory.  The library allocates nothing.  Weights, both KV caches and one
+ * workspace are caller-owned device buffers (PyTorch tensors in the Python
+ * binding) that the caller keeps alive until dflash_destroy().  Every
+ * pointer is a DEVICE pointer unless marked (host).  Sizes come from
+ * dflash_workspace_bytes / dflash_kv_target_bytes / dflash_kv_draft_bytes.
+ *
+ * Streams.  Every call enqueues work on the given stream and returns without
+ * synchronising, except dflash_stats() and dflash_check(), which synchronise
+ * that stream.  The round's state (positions, next token, block length,
+ * budget, statistics) lives in device memory, so a round needs no host
+ * round-trip and the launches of a round can be captured in a CUDA graph.
+ * Calls on one context must not overlap on the GPU (one stream per context).
+ *
+ * Errors.  Every int-returning call returns DFLASH_OK (0) or a negative
+ * DFLASH_ERR_* code and never aborts; dflash_last_error() gives a message
+ * (thread-local).  Kernels never trap: an impossible index or an expired
+ * bounded wait sets a device error word that dflash_check() reports.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dflash_stream_t; /* a cudaStream_t; NULL = legacy default */
+
+enum {
+    DFLASH_OK = 0,
+    DFLASH_ERR_CONFIG = -1,   /* shape/format mismatch, rejected before any write */
+    DFLASH_ERR_CAPACITY = -2, /* max_seq / draft context capacity exceeded */
+    DFLASH_ERR_ARG = -3,      /* null pointer, size out of range, misaligned buffer */
+    DFLASH_ERR_CUDA = -4,     /* a CUDA runtime/driver call or launch failed */
+    DFLASH_ERR_DEVICE = -5,   /* a kernel set the device error word */
+    DFLASH_ERR_TIMEOUT = -6,  /* a kernel's bounded wait expired */
+    DFLASH_ERR_STATE = -7     /* call out of order (e.g. verify before prefill) */
+};
+
+enum { DFLASH_F32 = 0, DFLASH_BF16 = 1, DFLASH_INT4G64 = 2 };
+
+#define DFLASH_MAX_TAPS 8
+#define DFLASH_MAX_BLOCK 16
+
+/* Model and run configuration (Qwen3-shaped target and drafter). */
+typedef struct {
+    int32_t hidden, n_q, n_kv, head_dim, ffn, vocab;
+    int32_t tgt_layers;                 /* 0 = drafter alone (taps supplied by caller) */
+    int32_t drf_layers;                 /* 0 = target alone */
+    int32_t n_taps;                     /* tap layers; taps concatenate in this order */
+    int32_t tap_layer[DFLASH_MAX_TAPS]; /* strictly increasing target layer indices */
+    int32_t block_max;                  /* native block B, 1..16 */
+    int32_t window;                     /* drafter context window W; 0 = whole context */
+    int32_t max_seq;                    /* positions held by both caches */
+    int32_t eos_id;                     /* -1 = no EOS */
+    int32_t dtype;     /* DFLASH_F32 | DFLASH_BF16: embedding, fc, caches, activations */
+    int32_t tgt_wfmt;  /* projection format of target layers: F32 | BF16 (| INT4G64 not yet) */
+    int32_t drf_wfmt;  /* projection format of draft layers: F32 | BF16 | INT4G64 */
+    int32_t ctx_norm;  /* 1 = RMSNorm after fc (drafter context) */
+    float rms_eps, rope_theta;
+} dflash_config;
+
+/*
+ * One decoder layer.  Projections use the nn.Linear layout [out][in].
+ *   F32/BF16: element type as the format says.
+ *   INT4G64 : packed uint8 [out][in/2], low nibble = even input index,
+ *             code = nibble - 8; the scale pointer (s*) is bf16 [in/64][out]
+ *             (group-major); weight = code * scale.  Produced by
+ *             dflash_quantize_int4g64().
+ * Norm weights are fp32: ln_attn/ln_mlp [hidden], q_norm/k_norm [head_dim].
+ * All matrices must be 16-byte aligned with rows a multiple of 16 bytes.
+ */
+typedef struct {
+    const void *wq, *wk, *wv, *wo, *w_gate, *w_up, *w_down;
+    const void *sq, *sk, *sv, *so, *s_gate, *s_up, *s_down;
+    const float *ln_attn, *ln_mlp, *q_norm, *k_norm;
+} dflash_layer;
+
+typedef struct {
+    const void* embed;            /* [vocab][hidden] dtype; also the tied LM head */
+    const float* final_norm_tgt;  /* [hidden] */
+    const float* final_norm_drf;  /* [hidden] */
+    const void* fc;               /* [hidden][n_taps*hidden] dtype */
+    const float* ctx_norm;        /* [hidden] */
+    const dflash_layer* tgt;      /* (host) array [tgt_layers], copied by dflash_init */
+    const dflash_layer* drf;      /* (host) array [drf_layers], copied by dflash_init */
+} dflash_weights;
+
+/* Round counters kept on the device (per-draft-position accept profile). */
+typedef struct {
+    int64_t rounds;                      /* verify_accept calls that emitted */
+    int64_t emitted;                     /* tokens emitted by them */
+    int64_t accept_hist[DFLASH_MAX_BLOCK]; /* [j]: rounds in which draft j+1 was accepted */
+    int32_t n;          /* target KV length = position of the pending token */
+    int32_t t_n;        /* pending token (emitted, not yet forwarded) */
+    int32_t block_len;  /* block length of the next round */
+    int32_t generated;  /* tokens emitted so far, the prefill's first included */
+    int32_t max_new;    /* generation budget */
+    int32_t ctx_len;    /* committed draft context rows */
+    int32_t finished;   /* EOS or budget reached */
+    int32_t last_accept;/* a of the last round (accepted length - 1) */
+    int32_t device_error;
+    int32_t pad_;
+} dflash_stats_t;
+
+typedef struct dflash_ctx dflash_ctx;
+
+/* Bytes of the caller-owned buffers for a configuration (0 if invalid). */
+size_t dflash_workspace_bytes(const dflash_config* cfg /*host*/);
+/* Target KV cache: dtype [tgt_layers][2][n_kv][max_seq][head_dim]. */
+size_t dflash_kv_target_bytes(const dflash_config* cfg /*host*/);
+/* Draft context K/V: dtype [drf_layers][2][n_kv][max_seq][head_dim], indexed
+ * by absolute position (a persistent cache bounded by max_seq:
+ * "[RFC] DFlash", "Requested changes" 3 and the reply "3. Draft KV cache"). */
+size_t dflash_kv_draft_bytes(const dflash_config* cfg /*host*/);
+
+/*
+ * Validates cfg against the weights (hidden size, vocab, tap layers, formats,
+ * divisibility) BEFORE touching any buffer ("feat: DFlash2 ..." commit: the
+ * config guard fires before any buffer is built), builds the TMA
+ * descriptors, zeroes the workspace's counters on the legacy stream and
+ * returns a context in *out (host).  Borrowed buffers must outlive it.
+ */
+int dflash_init(const dflash_config* cfg /*host*/, const dflash_weights* w /*host*/,
+                void* kv_target, void* kv_draft, void* workspace, size_t workspace_bytes,
+                dflash_ctx** out /*host*/);
+
+/*
+ * Starts a generation.
+ * Target mode (tgt_layers > 0): prompt_ids [n_prompt] int32 run through the
+ *   target in 16-row chunks; K/V fill the target cache, tap rows of the
+ *   trailing context window are fc-projected into the draft context
+ *   ("feat: DFlash2 ...": prefill stages the prompt's trailing window of tap
+ *   rows), the argmax of the last row is the first generated token.
+ * Drafter-alone mode (tgt_layers == 0): ext_taps holds n_ext tap rows as
+ *   dtype [n_taps][n_ext][hc*hidden] (hc streams per tap layer, reduced by
+ *   their mean); rows are positions 0..n_ext-1 and first_token is the pending
+ *   token at position n_ext.
+ * max_new is the generation budget (the first token counts).  Errors:
+ * ARG, CAPACITY (n_prompt or n_ext + block > max_seq), STATE.
+ */
+int dflash_prefill_taps(dflash_ctx* ctx, const int32_t* prompt_ids, int32_t n_prompt,
+                        const void* ext_taps, int32_t n_ext, int32_t hc, int32_t first_token,
+                        int32_t max_new, dflash_stream_t stream);
+
+/*
+ * One drafter forward over the block of the device-held length bl at
+ * positions n..n+bl-1; writes draft_ids [block_max-1] int32 (entries
+ * >= bl-1 are -1).  bl <= 1 drafts nothing ("[RFC] DFlash", "Requested
+ * changes" 1: a one-token round is a target-only step).
+ */
+int dflash_draft_block(dflash_ctx* ctx, int32_t* draft_ids, dflash_stream_t stream);
+
+/*
+ * Verifies [t_n, draft_ids[0..bl-2]] in one target forward (draft_ids NULL:
+ * plain greedy step, one row), accepts the first-mismatch prefix plus the
+ * bonus token (EOS-truncated), writes tokens_out [block_max] (unused = -1)
+ * and *n_emitted, rolls the target KV length to n + n_emitted, commits the
+ * accepted rows' taps to the draft context and sets the next block length
+ * min(B, max_new - generated, max_seq - n).  A finished context emits 0.
+ */
+int dflash_verify_accept(dflash_ctx* ctx, const int32_t* draft_ids, int32_t* tokens_out,
+                         int32_t* n_emitted, dflash_stream_t stream);
+
+/*
+ * Rewinds the target KV length and the draft context to new_len (host),
+ * 1 <= new_len <= current length; the pending token becomes
+ * token_at_new_len (host).  Nothing is moved: positions >= new_len are
+ * overwritten by later rounds.  ("[RFC] DFlash", "Key Implementation
+ * Details": KV-cache position rollback; "feat: DFlash2 ...": continuity
+ * breaks reset the drafter with positions realigned.)
+ */
+int dflash_rollback(dflash_ctx* ctx, int64_t new_len, int32_t token_at_new_len,
+                    dflash_stream_t stream);
+
+/* Copies the device counters and state to *out (host); synchronises stream. */
+int dflash_stats(dflash_ctx* ctx, dflash_stats_t* out, dflash_stream_t stream);
+
+/* Synchronises stream, returns DEVICE/TIMEOUT if a kernel flagged an error. */
+int dflash_check(dflash_ctx* ctx, dflash_stream_t stream);
+
+/*
+ * Parity taps: while set (non-NULL), every target LM head (verify, and the
+ * last prefill chunk) writes its fp32 logits [16][vocab] to verify_logits
+ * (row i = forward row i) and every draft writes [16][vocab] to draft_logits
+ * (row j = block row j); rows past the forward's length hold padding.
+ * Costs one extra write of the logits; NULL switches it off.
+ */
+int dflash_set_logits_out(dflash_ctx* ctx, float* verify_logits, float* draft_logits);
+
+/*
+ * Kernel timing of the dominant kernel family (the weight-streaming GEMM).
+ * mode 1: start -- every later GEMM launch of this context is bracketed by
+ *   two CUDA events recorded on its stream (up to 1 << 15 launches; events
+ *   recorded during stream capture become event nodes of the graph, so a
+ *   captured round keeps timing itself on every replay);
+ * mode 2: read -- synchronise the bracketed events and sum them into *out;
+ * mode 0: read and stop.
+ * gemm_bytes counts algorithmic bytes: weights, the 16 activation rows read
+ * and the outputs written; gemm_weight_bytes the weights alone.
+ */
+typedef struct {
+    int64_t gemm_launches;
+    double gemm_ms;
+    double gemm_bytes;
+    double gemm_weight_bytes;
+} dflash_profile_t;
+
+int dflash_profile(dflash_ctx* ctx, int32_t mode, dflash_profile_t* out /*host*/);
+
+/* Kernels launched by this process through the library so far. */
+int64_t dflash_launch_count(void);
+
+void dflash_destroy(dflash_ctx* ctx);
+const char* dflash_last_error(void);
+
+/* ---- standalone operations ------------------------------------------- */
+
+/*
+ * hc-stream tap reduce ("dflash: the chain verify builds pipelined ...",
+ * first commit: per-token mean of the hyper-connection streams,
+ * unflatten(-1, (hc, hidden)).mean(-2)): layer_streams[i] (host array of
+ * n_layers device pointers) is bf16 [rows][hc*hidden] with stream s at
+ * columns s*hidden..; out is fp32 [rows][n_layers*hidden], tap layer i at
+ * columns i*hidden...  Streams are summed in order s = 0..hc-1 in fp32,
+ * then multiplied by 1/hc.  hidden must be a multiple of 8.
+ */
+int dflash_tap_reduce(const void* const* layer_streams /*host array*/, int32_t n_layers,
+                      int32_t rows, int32_t hc, int32_t hidden, float* out,
+                      dflash_stream_t stream);
+
+/*
+ * INT4 group-64 quantiser (the INT4G64 format above) of w fp32 [n][k]:
+ * per group of 64 consecutive k of one row, s = bf16(absmax / 7) (round to
+ * nearest even), code = clamp(rint(w / s), -8, 7) (0 where s == 0).  The
+ * scale and the division are fp32.  packed uint8 [n][k/2], scales bf16
+ * [k/64][n].  k must be a multiple of 256.
+ */
+int dflash_quantize_int4g64(const float* w, int32_t n, int32_t k, uint8_t* packed,
+                            uint16_t* scales, dflash_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H */

@@ -12,6 +12,7 @@ import numpy as np
 import torch
 
 from block_diffusion_speculative_gather_gb300 import synth
+from block_diffusion_speculative_gather_gb300.synth import ModelTensors  # noqa: F401
 from block_diffusion_speculative_gather_gb300.configs import Workload
 from oracle import dflash_oracle as O
 
@@ -34,26 +35,6 @@ def oracle_config(w: Workload, **kw) -> O.OracleConfig:
 
 def torch_dtype(w: Workload) -> torch.dtype:
     return torch.float32 if w.dtype == "f32" else torch.bfloat16
-
-
-class ModelTensors:
-    """All synthetic tensors of a workload, as CPU torch tensors."""
-
-    def __init__(self, w: Workload, std: float = 0.02):
-        dt = torch_dtype(w)
-        self.w = w
-        self.embed = synth.matrix("embed", w.vocab, w.hidden, dt, std)
-        self.final_norm_t = torch.ones(w.hidden, dtype=torch.float32)
-        self.final_norm_d = torch.ones(w.hidden, dtype=torch.float32)
-        self.ctx_norm = torch.ones(w.hidden, dtype=torch.float32)
-        self.tgt = synth.decoder_layers("tgt", w.tgt_layers, w.hidden, w.n_q, w.n_kv,
-                                        w.head_dim, w.ffn, dt, std)
-        # INT4 drafters are drawn in fp32; each side quantises them itself
-        ddt = torch.float32 if w.drf_int4 else dt
-        self.drf = synth.decoder_layers("drf", w.drf_layers, w.hidden, w.n_q, w.n_kv,
-                                        w.head_dim, w.ffn, ddt, std)
-        self.fc = synth.matrix("fc", w.hidden, w.n_taps * w.hidden, dt, std) \
-            if w.drf_layers else None
 
 
 def oracle_layers(layers: List[Dict[str, torch.Tensor]], int4: bool = False):

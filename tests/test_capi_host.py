@@ -1,0 +1,94 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+entry point include/dflash.h declares, and its configuration guards reject
+bad shapes before any buffer is touched."""
+
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def capi():
+    from block_diffusion_speculative_gather_gb300 import build
+    build.build()
+    from block_diffusion_speculative_gather_gb300 import capi as m
+    return m
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dflash.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dflash_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_symbols_exported(capi):
+    names = _declared()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(capi.lib, n), n
+    assert set(names) == set(capi.EXPORTED)
+
+
+def test_struct_sizes_match_header(capi):
+    # 17 int32 fields, the int32 tap array and 2 floats
+    assert C.sizeof(capi.dflash_config) == 4 * (17 + capi.MAX_TAPS + 2)
+    assert C.sizeof(capi.dflash_layer) == 18 * 8
+    assert C.sizeof(capi.dflash_stats_t) == 8 * (2 + capi.MAX_BLOCK) + 4 * 10
+
+
+def _cfg(capi, **kw):
+    from block_diffusion_speculative_gather_gb300.configs import TINY
+    from block_diffusion_speculative_gather_gb300.runtime import make_config
+    return make_config(TINY, **kw)
+
+
+def test_sizes_for_valid_config(capi):
+    cfg = _cfg(capi)
+    assert capi.dflash_workspace_bytes(cfg) > 0
+    assert capi.dflash_kv_target_bytes(cfg) == 2 * 2 * 2 * 256 * 64 * 4
+    assert capi.dflash_kv_draft_bytes(cfg) == 1 * 2 * 2 * 256 * 64 * 4
+
+
+@pytest.mark.parametrize("field,value", [
+    ("hidden", 200), ("head_dim", 96), ("n_kv", 3), ("vocab", 4000), ("block_max", 17),
+    ("block_max", 0), ("ffn", 1000), ("dtype", 7), ("drf_wfmt", 1), ("n_taps", 0),
+    ("eos_id", 4096), ("max_seq", 1),
+])
+def test_config_guard_rejects_before_buffers(capi, field, value):
+    cfg = _cfg(capi, **{field: value})
+    assert capi.dflash_workspace_bytes(cfg) == 0
+    out = C.c_void_p()
+    w = capi.dflash_weights()
+    rc = capi.lib.dflash_init(C.byref(cfg), C.byref(w), None, None, None, 0, C.byref(out))
+    assert rc == -1, capi.lib.dflash_last_error()
+    assert out.value is None
+
+
+def test_tap_layer_guard(capi):
+    cfg = _cfg(capi)
+    cfg.tap_layer[1] = 5            # beyond the 2-layer target
+    assert capi.dflash_workspace_bytes(cfg) == 0
+    cfg = _cfg(capi)
+    cfg.tap_layer[0], cfg.tap_layer[1] = 1, 0   # not increasing
+    assert capi.dflash_workspace_bytes(cfg) == 0
+
+
+def test_missing_weights_rejected(capi):
+    cfg = _cfg(capi)
+    out = C.c_void_p()
+    w = capi.dflash_weights()       # all NULL
+    rc = capi.lib.dflash_init(C.byref(cfg), C.byref(w), None, None, None, 0, C.byref(out))
+    assert rc == -3 and "embed" in capi.lib.dflash_last_error().decode()
+
+
+def test_null_context_calls_fail_cleanly(capi):
+    assert capi.lib.dflash_draft_block(None, None, None) == -3
+    assert capi.lib.dflash_verify_accept(None, None, None, None, None) == -3
+    assert capi.lib.dflash_rollback(None, 5, 0, None) == -3
+    assert capi.lib.dflash_prefill_taps(None, None, 0, None, 0, 1, 0, 1, None) == -3
+    assert capi.lib.dflash_quantize_int4g64(None, 1, 256, None, None, None) == -3
+    assert capi.lib.dflash_tap_reduce(None, 1, 1, 1, 8, None, None) == -3

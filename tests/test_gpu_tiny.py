@@ -1,0 +1,212 @@
+"""GPU parity on the tiny fp32 workload (2-layer target, 1-layer drafter,
+block 8, window 64, 32-token prompt, 64 tokens), through the C ABI.
+
+Tolerance: logits within rel 1e-4 of the fp64 oracle (per row, max abs
+difference over max |oracle|); token ids bit-exact wherever the oracle's
+top-2 margin exceeds twice that; GPU speculative output bit-identical to GPU
+plain greedy; acceptance lengths and rollback positions exact.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from block_diffusion_speculative_gather_gb300 import synth
+from block_diffusion_speculative_gather_gb300.configs import TINY
+from oracle import dflash_oracle as O
+from tests import gpu_common as G
+from tests.oracle_inputs import ModelTensors, oracle_config, oracle_draft, oracle_target
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module", params=[0.02, 0.1], ids=["std0.02", "std0.1"])
+def tiny(request):
+    G.build_lib()
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+    m = ModelTensors(TINY, std=request.param)
+    tw, dw, cfg = oracle_target(m), oracle_draft(m), oracle_config(TINY)
+    prompt = synth.uniform_ids(TINY.prompt_len, TINY.vocab)
+    cache = O.KVCache(len(tw.layers), cfg.n_kv, cfg.head_dim)
+    p_logits, p_taps = O.target_forward(tw, cfg, prompt.tolist(), 0, cache)
+    g = O.greedy(tw, cfg, prompt.tolist(), TINY.n_new)
+    # teacher-forced logits of every greedy step (row k predicts token k)
+    tf, _ = O.target_forward(tw, cfg, prompt.tolist() + g[:-1], 0,
+                             O.KVCache(len(tw.layers), cfg.n_kv, cfg.head_dim))
+    dec = DFlash(TINY, m)
+    return dict(m=m, tw=tw, dw=dw, cfg=cfg, prompt=torch.from_numpy(prompt), p_logits=p_logits,
+                p_taps=p_taps, greedy=g, greedy_logits=tf[len(prompt) - 1:], dec=dec)
+
+
+def test_prefill_logits_and_first_token(tiny):
+    dec = tiny["dec"]
+    vl = G.logits_buf(TINY.vocab)
+    dec.set_logits_out(vl, None)
+    dec.prefill(tiny["prompt"], TINY.n_new)
+    dec.check()
+    dec.set_logits_out(None, None)
+    st = dec.stats()
+    P = TINY.prompt_len
+    last_chunk = (P - 1) // 16 * 16
+    rows = P - last_chunk
+    err = G.rel_err_rows(vl[:rows].cpu().numpy(), tiny["p_logits"][last_chunk:P])
+    assert err.max() < TOL, err
+    assert st.n == P and st.generated == 1 and st.ctx_len == P
+    assert st.block_len == TINY.block
+    if G.decidable(tiny["p_logits"][P - 1], TOL):
+        assert st.t_n == int(np.argmax(tiny["p_logits"][P - 1]))
+
+
+def test_draft_matches_uncached_oracle(tiny):
+    """GPU drafter (persistent draft KV cache) vs the oracle drafter that
+    re-projects the context window from the raw taps."""
+    dec, P = tiny["dec"], TINY.prompt_len
+    dec.prefill(tiny["prompt"], TINY.n_new)
+    dl = G.logits_buf(TINY.vocab)
+    dec.set_logits_out(None, dl)
+    ids = dec.draft().cpu().numpy()
+    dec.check()
+    dec.set_logits_out(None, None)
+    t_n = dec.stats().t_n
+    ref_logits, ref_ids = O.draft_forward(tiny["dw"], tiny["tw"].embed, tiny["cfg"],
+                                          tiny["p_taps"], t_n, P, TINY.block)
+    err = G.rel_err_rows(dl[1:TINY.block].cpu().numpy(), ref_logits[1:])
+    assert err.max() < TOL, err
+    G.check_ids(ids[:TINY.block - 1], ref_logits[1:], TOL)
+
+
+@pytest.mark.parametrize("cut", [0, 3, 7])
+def test_verify_accept_rollback_match_oracle(tiny, cut):
+    """Drafts = the oracle's greedy continuation corrupted at position `cut`
+    (7 = not corrupted): acceptance length, emitted tokens, logits and the
+    rolled-back positions follow the oracle."""
+    dec, P, B = tiny["dec"], TINY.prompt_len, TINY.block
+    g = tiny["greedy"]
+    dec.prefill(tiny["prompt"], TINY.n_new)
+    st = dec.stats()
+    d = list(g[1:B])
+    if cut < B - 1:
+        d[cut] = (d[cut] + 1) % TINY.vocab
+    vl = G.logits_buf(TINY.vocab)
+    dec.set_logits_out(vl, None)
+    toks, n = dec.verify(torch.tensor(d, dtype=torch.int32, device="cuda"))
+    dec.check()
+    dec.set_logits_out(None, None)
+    cache = O.KVCache(len(tiny["tw"].layers), TINY.n_kv, TINY.head_dim)
+    O.target_forward(tiny["tw"], tiny["cfg"], tiny["prompt"].tolist(), 0, cache)
+    ref_logits, _ = O.target_forward(tiny["tw"], tiny["cfg"], [st.t_n] + d, P, cache)
+    err = G.rel_err_rows(vl[:B].cpu().numpy(), ref_logits)
+    assert err.max() < TOL, err
+    y = [int(np.argmax(r)) for r in ref_logits]
+    a, emitted, _ = O.accept(d, y, -1)
+    if all(G.decidable(r, TOL) for r in ref_logits[: a + 1]):
+        assert int(n.item()) == len(emitted)
+        assert toks[: len(emitted)].tolist() == emitted
+        assert all(t == -1 for t in toks[len(emitted):].tolist())
+        st2 = dec.stats()
+        assert st2.n == P + len(emitted) and st2.ctx_len == st2.n
+        assert st2.last_accept == a and st2.generated == 1 + len(emitted)
+
+
+def test_spec_equals_greedy_and_oracle(tiny):
+    dec = tiny["dec"]
+    gg = dec.greedy(tiny["prompt"], TINY.n_new)
+    sp = dec.generate(tiny["prompt"], TINY.n_new)
+    dec.check()
+    assert sp == gg, "GPU speculative output differs from GPU greedy"
+    st = dec.stats()
+    assert st.generated == TINY.n_new and st.n == TINY.prompt_len + TINY.n_new - 1
+    n = G.compared_prefix(gg, tiny["greedy"], tiny["greedy_logits"], TOL)
+    assert n >= 8, f"only {n} decidable tokens compared"
+
+
+def test_spec_with_adversarial_drafts_equals_greedy(tiny):
+    dec, B = tiny["dec"], TINY.block
+    gg = dec.greedy(tiny["prompt"], TINY.n_new)
+    rng = np.random.default_rng(3)
+
+    def oracle_like(d):        # the GPU greedy continuation: full acceptance
+        st = d.stats()
+        k = st.generated
+        ids = gg[k:k + B - 1] + [0] * (B - 1)
+        return torch.tensor(ids[:B - 1], dtype=torch.int32, device="cuda")
+
+    def random_ids(d):
+        return torch.from_numpy(rng.integers(0, TINY.vocab, B - 1).astype(np.int32)).cuda()
+
+    for fn in (oracle_like, random_ids):
+        out = dec.generate(tiny["prompt"], TINY.n_new, draft_fn=fn)
+        assert out == gg, fn.__name__
+        st = dec.stats()
+        assert 1 <= st.emitted / max(1, st.rounds) <= B
+        if fn is oracle_like:
+            assert st.accept_hist[B - 2] >= st.rounds - 2   # every draft position accepted
+
+
+def test_batch_invariance_rows_equal_single_row(tiny):
+    """Row i of a 8-row verify has the bit-identical logits of the i-th
+    one-row (greedy) step: the kernels never change with the row count."""
+    dec, P, B = tiny["dec"], TINY.prompt_len, TINY.block
+    gg = dec.greedy(tiny["prompt"], TINY.n_new)
+    dec.prefill(tiny["prompt"], TINY.n_new)
+    vl = G.logits_buf(TINY.vocab)
+    dec.set_logits_out(vl, None)
+    d = torch.tensor(gg[1:B], dtype=torch.int32, device="cuda")
+    dec.verify(d)
+    batch = vl[:B].clone()
+    dec.rollback(P, gg[0])
+    for i in range(B):
+        dec.verify(None)
+        assert torch.equal(vl[0], batch[i]), f"row {i} differs"
+    dec.set_logits_out(None, None)
+    dec.check()
+
+
+def test_eos_truncates_like_greedy(tiny):
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+    dec = tiny["dec"]
+    gg = dec.greedy(tiny["prompt"], TINY.n_new)
+    eos = gg[20]
+    de = DFlash(TINY.with_(eos_id=eos), tiny["m"])
+    ge = de.greedy(tiny["prompt"], TINY.n_new)
+    se = de.generate(tiny["prompt"], TINY.n_new)
+    assert ge == gg[: gg.index(eos) + 1]
+    assert se == ge
+    de.close()
+
+
+def test_budget_shrinks_last_round(tiny):
+    dec = tiny["dec"]
+    for n_new in (2, 9, 10, 17):
+        gg = dec.greedy(tiny["prompt"], n_new)
+        sp = dec.generate(tiny["prompt"], n_new)
+        assert len(gg) == n_new and sp == gg
+
+
+def test_tap_reduce_matches_oracle():
+    G.build_lib()
+    from block_diffusion_speculative_gather_gb300 import capi
+    for hc, H, rows in [(4, 64, 5), (4, 4096, 33), (1, 256, 16), (3, 128, 7)]:
+        streams = synth.hc_streams(4, rows, hc, H)
+        out = torch.empty((rows, 4 * H), dtype=torch.float32, device="cuda")
+        dev = [streams[i].cuda().contiguous() for i in range(4)]
+        capi.dflash_tap_reduce(dev, rows, hc, H, out)
+        torch.cuda.synchronize()
+        ref = O.tap_concat([streams[i].float().numpy() for i in range(4)], hc)
+        np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=2e-7, atol=1e-7)
+
+
+def test_quantizer_bit_exact_with_oracle():
+    G.build_lib()
+    from block_diffusion_speculative_gather_gb300 import capi
+    w = synth.normal((384, 512), 0.02, 0, "quant-test")
+    w[5, :64] = 0.0
+    wt = torch.from_numpy(w).cuda()
+    packed = torch.empty((384, 256), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((8, 384), dtype=torch.int16, device="cuda")
+    capi.dflash_quantize_int4g64(wt, packed, scales)
+    torch.cuda.synchronize()
+    ref_p, ref_s = O.quantize_int4_g64(w)
+    np.testing.assert_array_equal(packed.cpu().numpy(), ref_p)
+    np.testing.assert_array_equal(scales.cpu().numpy().view(np.uint16).T, ref_s)
