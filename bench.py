@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="(debug) override target layers; lines printed with it are not the workload")
+    ap.add_argument("--ncu-rounds", type=int, default=0,
+                    help="profiling mode: prefill, then N eager rounds inside the NVTX range "
+                         "'dflash_rounds', no timing and no JSON line")
     return ap.parse_args()
 
 
@@ -229,8 +232,9 @@ def run_ours(args):
     torch.cuda.set_device(local)
     w = E2E_BF16
     if args.layers:
+        from block_diffusion_speculative_gather_gb300.configs import evenly_spaced_taps
         w = w.with_(tgt_layers=args.layers,
-                    tap_layers=tuple(min(t, args.layers - 1) for t in range(5)))
+                    tap_layers=evenly_spaced_taps(args.layers, min(5, args.layers)))
     model = synth.ModelTensors(w)
     dec = DFlash(w, model)
     del model
@@ -240,6 +244,20 @@ def run_ours(args):
     def barrier():
         if world > 1:
             dist.barrier()
+
+    if args.ncu_rounds:
+        dec.prefill(prompt, w.n_new)
+        dec.verify(dec.draft())
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("dflash_rounds")
+        for _ in range(args.ncu_rounds):
+            dec.verify(dec.draft())
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+        dec.check()
+        print(f"ncu rounds done: {args.ncu_rounds}", flush=True)
+        dec.close()
+        return
 
     # launches per round
     dec.prefill(prompt, w.n_new)

@@ -266,8 +266,10 @@ int plan_gemm(dflash_ctx* c, GemmPlan* p, int wfmt, int epi, const void* const* 
 int run_gemm(dflash_ctx* c, const GemmPlan& p, const GemmArgs& a, cudaStream_t s) {
     const bool timed = c->prof && c->ev_used + 2 <= c->ev.size();
     if (timed) cudaEventRecordWithFlags(c->ev[c->ev_used], s, cudaEventRecordExternal);
-    if (launch_gemm(p.wfmt, p.epi, p.xt, p.maps, a, p.grid, s))
-        return fail(DFLASH_ERR_CUDA, "GEMM launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+    const int e = launch_gemm(p.wfmt, p.epi, p.xt, p.maps, a, p.grid, s);
+    if (e)
+        return fail(DFLASH_ERR_CUDA, "GEMM launch failed (fmt %d epi %d N %d K %d grid %d): %s",
+                    p.wfmt, p.epi, a.N, a.K, p.grid, cudaGetErrorString((cudaError_t)e));
     if (timed) {
         cudaEventRecordWithFlags(c->ev[c->ev_used + 1], s, cudaEventRecordExternal);
         c->ev_used += 2;

@@ -339,15 +339,15 @@ int launch_one(const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_
                             DFL_MAX_ROWS * GEMM_BN * 4 + 2 * GEMM_STAGES * 8 + 64;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(gemm_skinny_kernel<WF, EPI>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
-            return -1;
+        const cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<WF, EPI>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem);
+        if (e != cudaSuccess) return (int)e;
         attr_set = true;
     }
     gemm_skinny_kernel<WF, EPI><<<grid, GEMM_THREADS, smem, stream>>>(maps, args);
     ++g_launches;
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    return (int)cudaGetLastError();
 }
 
 }  // namespace
@@ -370,7 +370,7 @@ int launch_gemm(int wfmt, int epi, int xt, const GemmMaps& maps, const GemmArgs&
             case EPI_ARGMAX: return launch_one<WF_F32, EPI_ARGMAX>(maps, args, grid, stream);
         }
     }
-    return -2;
+    return (int)cudaErrorInvalidValue;
 }
 
 }  // namespace dfl

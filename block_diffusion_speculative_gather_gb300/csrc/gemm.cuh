@@ -46,6 +46,7 @@ struct GemmMaps {
 };
 
 // Host: enqueue one GEMM (fmt, epilogue and activation type fixed per call).
+// Returns 0 or the cudaError_t of the launch.
 int launch_gemm(int wfmt, int epi, int xt, const GemmMaps& maps, const GemmArgs& args,
                 int grid, cudaStream_t stream);
 
