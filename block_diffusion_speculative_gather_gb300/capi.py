@@ -94,6 +94,7 @@ def _load() -> C.CDLL:
         "dflash_quantize_int4g64": (C.c_int, [vp, i32, i32, vp, vp, vp]),
         "dflash_profile": (C.c_int, [vp, i32, C.POINTER(dflash_profile_t)]),
         "dflash_launch_count": (i64, []),
+        "dflash_selftest_timeout": (C.c_int, [vp, i64, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -108,7 +109,8 @@ EXPORTED = ("dflash_workspace_bytes", "dflash_kv_target_bytes", "dflash_kv_draft
             "dflash_init", "dflash_prefill_taps", "dflash_draft_block", "dflash_verify_accept",
             "dflash_rollback", "dflash_stats", "dflash_check", "dflash_set_logits_out",
             "dflash_destroy", "dflash_last_error", "dflash_tap_reduce",
-            "dflash_quantize_int4g64", "dflash_profile", "dflash_launch_count")
+            "dflash_quantize_int4g64", "dflash_profile", "dflash_launch_count",
+            "dflash_selftest_timeout")
 
 
 def check(rc: int) -> None:
@@ -204,3 +206,7 @@ def dflash_profile(ctx, mode: int) -> dflash_profile_t:
 
 def dflash_launch_count() -> int:
     return lib.dflash_launch_count()
+
+
+def dflash_selftest_timeout(ctx, limit_ns: int, stream=None):
+    check(lib.dflash_selftest_timeout(ctx, limit_ns, _stream(stream)))

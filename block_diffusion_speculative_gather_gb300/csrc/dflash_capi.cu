@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "../../include/dflash.h"
+#include "attention.cuh"
 #include "common.cuh"
 #include "gemm.cuh"
 #include "kernels.cuh"
@@ -53,7 +54,11 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 int elem_size(int dtype) { return dtype == DFLASH_F32 ? 4 : 2; }
 
-int max_chunks(const dflash_config& c) { return (c.max_seq + ATTN_CHUNK - 1) / ATTN_CHUNK; }
+// positions per (layer, K|V, head) run of a cache: max_seq rounded up to a
+// whole number of 64-key attention chunks
+int cache_cap(const dflash_config& c) { return (c.max_seq + 63) / 64 * 64; }
+
+int max_chunks(const dflash_config& c) { return cache_cap(c) / ATTN_CHUNK; }
 
 // ------------------------------------------------------------------ layout
 
@@ -123,10 +128,14 @@ int validate(const dflash_config* c) {
     }
     auto fmt_ok = [&](int f) {
         if (c->dtype == DFLASH_F32) return f == DFLASH_F32;
-        return f == DFLASH_BF16;   // INT4G64 is accepted once its GEMM is built
+        return f == DFLASH_BF16 || f == DFLASH_INT4G64;
     };
     if (c->tgt_layers > 0 && !fmt_ok(c->tgt_wfmt)) return fail(DFLASH_ERR_CONFIG, "tgt_wfmt %d not supported with dtype %d", c->tgt_wfmt, c->dtype);
     if (c->drf_layers > 0 && !fmt_ok(c->drf_wfmt)) return fail(DFLASH_ERR_CONFIG, "drf_wfmt %d not supported with dtype %d", c->drf_wfmt, c->dtype);
+    const bool int4 = (c->tgt_layers > 0 && c->tgt_wfmt == DFLASH_INT4G64) ||
+                      (c->drf_layers > 0 && c->drf_wfmt == DFLASH_INT4G64);
+    if (int4 && (c->hidden % 256 || (c->n_q * c->head_dim) % 256 || c->ffn % 256))
+        return fail(DFLASH_ERR_CONFIG, "INT4 projections need hidden, n_q*head_dim and ffn to be multiples of 256");
     if (c->eos_id >= c->vocab) return fail(DFLASH_ERR_CONFIG, "eos_id %d >= vocab", c->eos_id);
     if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return fail(DFLASH_ERR_CONFIG, "rms_eps / rope_theta must be positive");
     return DFLASH_OK;
@@ -150,25 +159,30 @@ int get_encode() {
     return DFLASH_OK;
 }
 
-// 2D map over a row-major [rows][inner] matrix, 128-byte swizzled boxes of
-// [box_rows][128 bytes].
+// 2D map over a row-major [rows][inner] matrix of es-byte elements.
+int make_map_raw(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es, uint64_t inner,
+                 uint64_t rows, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
+    if (!aligned16(base)) return fail(DFLASH_ERR_ARG, "matrix %p is not 16-byte aligned", base);
+    if ((inner * es) % 16) return fail(DFLASH_ERR_ARG, "row of %llu elements is not a multiple of 16 bytes", (unsigned long long)inner);
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * es};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return DFLASH_OK;
+}
+
+// 128-byte swizzled boxes of [box_rows][128 bytes] over an f32/bf16/f16 matrix.
 int make_map(CUtensorMap* m, const void* base, int xt, uint64_t inner, uint64_t rows,
              uint32_t box_rows) {
     const int es = xt == XT_F32 ? 4 : 2;
     CUtensorMapDataType dt = xt == XT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                            : xt == XT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if (!aligned16(base)) return fail(DFLASH_ERR_ARG, "matrix %p is not 16-byte aligned", base);
-    if ((inner * es) % 16) return fail(DFLASH_ERR_ARG, "row of %llu elements is not a multiple of 16 bytes", (unsigned long long)inner);
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {inner * es};
-    cuuint32_t box[2] = {(cuuint32_t)(128 / es), box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return DFLASH_OK;
+    return make_map_raw(m, base, dt, es, inner, rows, 128 / es, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // ------------------------------------------------------------------ plans
@@ -198,6 +212,7 @@ struct dflash_ctx {
     int sms;
     std::vector<LayerPlans> tplan, dplan;
     GemmPlan lm, fc;
+    AttnMaps amap_t{}, amap_d{};   // tensor-core attention maps (bf16 caches)
     float* verify_logits = nullptr;
     float* draft_logits = nullptr;
     bool prefilled = false;
@@ -211,24 +226,39 @@ struct dflash_ctx {
     DevState* st() const { return reinterpret_cast<DevState*>(ws + L.state); }
     template <typename T> T* buf(size_t off) const { return reinterpret_cast<T*>(ws + off); }
     int act_xt() const { return cfg.dtype == DFLASH_F32 ? XT_F32 : XT_BF16; }
-    int wf(int f) const { return f == DFLASH_F32 ? WF_F32 : WF_BF16; }
+    int wf(int f) const { return f == DFLASH_F32 ? WF_F32 : f == DFLASH_INT4G64 ? WF_INT4 : WF_BF16; }
     size_t cache_layer_stride() const {   // elements per layer (K and V)
-        return (size_t)2 * cfg.n_kv * cfg.max_seq * cfg.head_dim;
+        return (size_t)2 * cfg.n_kv * cache_cap(cfg) * cfg.head_dim;
+    }
+    size_t cache_kv_offset() const {      // elements from a layer's K to its V
+        return (size_t)cfg.n_kv * cache_cap(cfg) * cfg.head_dim;
     }
 };
 
 namespace {
 
 int plan_gemm(dflash_ctx* c, GemmPlan* p, int wfmt, int epi, const void* const* w, const int* rows,
-              int nseg, int K, const void* x, int xt) {
+              int nseg, int K, const void* x, int xt, const void* const* scales = nullptr) {
     memset(p, 0, sizeof *p);
     p->wfmt = wfmt;
     p->epi = epi;
     p->xt = xt;
     const int wxt = wfmt == WF_F32 ? XT_F32 : XT_BF16;
+    const uint32_t box_rows = epi == EPI_SWIGLU ? 64 : GEMM_BN;
     int N = 0;
     for (int i = 0; i < nseg; ++i) {
-        int r = make_map(&p->maps.w[i], w[i], wxt, K, rows[i], epi == EPI_SWIGLU ? 64 : GEMM_BN);
+        int r;
+        if (wfmt == WF_INT4) {
+            if (!scales || !aligned16(scales[i])) return fail(DFLASH_ERR_ARG, "INT4 scales missing or misaligned");
+            if (K % 256) return fail(DFLASH_ERR_CONFIG, "INT4 reduction length %d is not a multiple of 256", K);
+            r = make_map_raw(&p->maps.w[i], w[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, rows[i], 128,
+                             box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+            if (!r)
+                r = make_map_raw(&p->maps.s[i], scales[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, rows[i],
+                                 K / 64, box_rows, 4, CU_TENSOR_MAP_SWIZZLE_NONE);
+        } else {
+            r = make_map(&p->maps.w[i], w[i], wxt, K, rows[i], box_rows);
+        }
         if (r) return r;
         p->args.seg_rows[i] = rows[i];
         N += rows[i];
@@ -238,7 +268,7 @@ int plan_gemm(dflash_ctx* c, GemmPlan* p, int wfmt, int epi, const void* const* 
     GemmArgs& a = p->args;
     a.n_seg = nseg;
     a.K = K;
-    a.kb = K / (wfmt == WF_F32 ? 32 : 64);
+    a.kb = K / (wfmt == WF_F32 ? 32 : wfmt == WF_INT4 ? 256 : 64);
     if (epi == EPI_SWIGLU) {
         a.N = rows[0];
         a.n_tiles = rows[0] / 64;
@@ -252,8 +282,9 @@ int plan_gemm(dflash_ctx* c, GemmPlan* p, int wfmt, int epi, const void* const* 
     a.st = c->st();
     const long long units = (long long)a.n_tiles * a.kb;
     p->grid = (int)(units < c->sms ? units : c->sms);
-    const double wes = wfmt == WF_F32 ? 4.0 : 2.0, xes = xt == XT_F32 ? 4.0 : 2.0;
-    p->wbytes = (double)N * K * wes;
+    const double wes = wfmt == WF_F32 ? 4.0 : wfmt == WF_INT4 ? 0.5 : 2.0;
+    const double xes = xt == XT_F32 ? 4.0 : 2.0;
+    p->wbytes = (double)N * K * wes + (wfmt == WF_INT4 ? (double)N * (K / 64) * 2 : 0.0);
     double outb = 0;
     if (epi == EPI_STORE) outb = (double)DFL_MAX_ROWS * N * 4;
     else if (epi == EPI_RESID) outb = 2.0 * DFL_MAX_ROWS * N * 4;
@@ -286,21 +317,26 @@ int build_layer_plans(dflash_ctx* c, const dflash_layer& lw, int wfmt, bool draf
     const int wf = c->wf(wfmt), xt = c->act_xt();
     const void* hn = c->ws + c->L.hn;
     const void* wqkv[3] = {lw.wq, lw.wk, lw.wv};
+    const void* sqkv[3] = {lw.sq, lw.sk, lw.sv};
     const int rqkv[3] = {qd, kvd, kvd};
-    int r = plan_gemm(c, &lp->qkv, wf, EPI_STORE, wqkv, rqkv, 3, H, hn, xt);
+    int r = plan_gemm(c, &lp->qkv, wf, EPI_STORE, wqkv, rqkv, 3, H, hn, xt, sqkv);
     if (r) return r;
     const void* wo[1] = {lw.wo};
+    const void* so[1] = {lw.so};
     const int ro[1] = {H};
-    if ((r = plan_gemm(c, &lp->o, wf, EPI_RESID, wo, ro, 1, qd, c->ws + c->L.attn, xt))) return r;
+    if ((r = plan_gemm(c, &lp->o, wf, EPI_RESID, wo, ro, 1, qd, c->ws + c->L.attn, xt, so))) return r;
     const void* wgu[2] = {lw.w_gate, lw.w_up};
+    const void* sgu[2] = {lw.s_gate, lw.s_up};
     const int rgu[2] = {g.ffn, g.ffn};
-    if ((r = plan_gemm(c, &lp->gateup, wf, EPI_SWIGLU, wgu, rgu, 2, H, hn, xt))) return r;
+    if ((r = plan_gemm(c, &lp->gateup, wf, EPI_SWIGLU, wgu, rgu, 2, H, hn, xt, sgu))) return r;
     const void* wd[1] = {lw.w_down};
-    if ((r = plan_gemm(c, &lp->down, wf, EPI_RESID, wd, ro, 1, g.ffn, c->ws + c->L.act, xt))) return r;
+    const void* sd[1] = {lw.s_down};
+    if ((r = plan_gemm(c, &lp->down, wf, EPI_RESID, wd, ro, 1, g.ffn, c->ws + c->L.act, xt, sd))) return r;
     if (draft) {
         const void* wkv[2] = {lw.wk, lw.wv};
+        const void* skv[2] = {lw.sk, lw.sv};
         const int rkv[2] = {kvd, kvd};
-        if ((r = plan_gemm(c, &lp->ctxkv, wf, EPI_STORE, wkv, rkv, 2, H, hn, xt))) return r;
+        if ((r = plan_gemm(c, &lp->ctxkv, wf, EPI_STORE, wkv, rkv, 2, H, hn, xt, skv))) return r;
     }
     return DFLASH_OK;
 }
@@ -325,7 +361,7 @@ int run_layers(dflash_ctx* c, bool target, cudaStream_t s) {
         if (r) return r;
         uint8_t* cache = reinterpret_cast<uint8_t*>(target ? c->kv_t : c->kv_d) +
                          (size_t)l * c->cache_layer_stride() * elem_size(g.dtype);
-        const size_t vofs = (size_t)g.n_kv * g.max_seq * g.head_dim * elem_size(g.dtype);
+        const size_t vofs = c->cache_kv_offset() * elem_size(g.dtype);
         QkvArgs q{};
         q.in = c->buf<float>(c->L.qkv);
         q.ld_in = qd + 2 * kvd;
@@ -341,6 +377,7 @@ int run_layers(dflash_ctx* c, bool target, cudaStream_t s) {
         q.v_cache = cache + vofs;
         q.c_type = xt;
         q.max_seq = g.max_seq;
+        q.cap = cache_cap(g);
         q.row_sel = ROWS_FWD;
         q.rope_cos = c->buf<float>(c->L.rcos);
         q.rope_sin = c->buf<float>(c->L.rsin);
@@ -354,7 +391,7 @@ int run_layers(dflash_ctx* c, bool target, cudaStream_t s) {
         at.n_q = g.n_q;
         at.n_kv = g.n_kv;
         at.head_dim = g.head_dim;
-        at.max_seq = g.max_seq;
+        at.cap = cache_cap(g);
         at.causal = target ? 1 : 0;
         at.window = target ? 0 : g.window;
         at.scale = 1.0f / sqrtf((float)g.head_dim);
@@ -363,7 +400,24 @@ int run_layers(dflash_ctx* c, bool target, cudaStream_t s) {
         at.out_type = xt;
         at.max_chunks = max_chunks(g);
         at.st = st;
-        LAUNCH_TRY(launch_attention(at, s));
+        if (g.dtype == DFLASH_BF16) {
+            AttnMmaArgs am{};
+            am.n_q = g.n_q;
+            am.n_kv = g.n_kv;
+            am.head_dim = g.head_dim;
+            am.layer = l;
+            am.cap = cache_cap(g);
+            am.causal = at.causal;
+            am.window = at.window;
+            am.scale = at.scale;
+            am.part = at.part;
+            am.st = st;
+            const int e = launch_attention_mma(target ? c->amap_t : c->amap_d, am, at.max_chunks, s);
+            if (e) return fail(DFLASH_ERR_CUDA, "attention launch: %s", cudaGetErrorString((cudaError_t)e));
+            LAUNCH_TRY(launch_attention_combine(at, s));
+        } else {
+            LAUNCH_TRY(launch_attention(at, s));
+        }
         a = lp.o.args;
         a.out = x;
         a.ldo = H;
@@ -431,9 +485,10 @@ int run_ingest(dflash_ctx* c, cudaStream_t s) {
         q.k_norm = c->drf[l].k_norm;
         q.eps = g.rms_eps;
         q.k_cache = cache;
-        q.v_cache = cache + (size_t)g.n_kv * g.max_seq * g.head_dim * elem_size(g.dtype);
+        q.v_cache = cache + c->cache_kv_offset() * elem_size(g.dtype);
         q.c_type = c->act_xt();
         q.max_seq = g.max_seq;
+        q.cap = cache_cap(g);
         q.row_sel = ROWS_COMMIT;
         q.rope_cos = c->buf<float>(c->L.rcos);
         q.rope_sin = c->buf<float>(c->L.rsin);
@@ -477,12 +532,12 @@ size_t dflash_workspace_bytes(const dflash_config* cfg) {
 
 size_t dflash_kv_target_bytes(const dflash_config* cfg) {
     if (validate(cfg)) return 0;
-    return (size_t)cfg->tgt_layers * 2 * cfg->n_kv * cfg->max_seq * cfg->head_dim * elem_size(cfg->dtype);
+    return (size_t)cfg->tgt_layers * 2 * cfg->n_kv * cache_cap(*cfg) * cfg->head_dim * elem_size(cfg->dtype);
 }
 
 size_t dflash_kv_draft_bytes(const dflash_config* cfg) {
     if (validate(cfg)) return 0;
-    return (size_t)cfg->drf_layers * 2 * cfg->n_kv * cfg->max_seq * cfg->head_dim * elem_size(cfg->dtype);
+    return (size_t)cfg->drf_layers * 2 * cfg->n_kv * cache_cap(*cfg) * cfg->head_dim * elem_size(cfg->dtype);
 }
 
 int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_target, void* kv_draft,
@@ -497,16 +552,20 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
     if (g.tgt_layers > 0 && (!w->tgt || !w->final_norm_tgt)) return fail(DFLASH_ERR_ARG, "target weights missing");
     if (g.drf_layers > 0 && (!w->drf || !w->final_norm_drf || !aligned16(w->fc) || !w->ctx_norm))
         return fail(DFLASH_ERR_ARG, "draft weights missing");
-    auto check_layer = [&](const dflash_layer& l, const char* who, int i) -> int {
+    auto check_layer = [&](const dflash_layer& l, const char* who, int i, int fmt) -> int {
         const void* ps[7] = {l.wq, l.wk, l.wv, l.wo, l.w_gate, l.w_up, l.w_down};
         for (const void* p : ps)
             if (!aligned16(p)) return fail(DFLASH_ERR_ARG, "%s layer %d: projection missing or misaligned", who, i);
+        const void* ss[7] = {l.sq, l.sk, l.sv, l.so, l.s_gate, l.s_up, l.s_down};
+        if (fmt == DFLASH_INT4G64)
+            for (const void* p : ss)
+                if (!aligned16(p)) return fail(DFLASH_ERR_ARG, "%s layer %d: INT4 scales missing or misaligned", who, i);
         if (!l.ln_attn || !l.ln_mlp || !l.q_norm || !l.k_norm)
             return fail(DFLASH_ERR_ARG, "%s layer %d: norm weight missing", who, i);
         return DFLASH_OK;
     };
-    for (int i = 0; i < g.tgt_layers; ++i) if ((r = check_layer(w->tgt[i], "target", i))) return r;
-    for (int i = 0; i < g.drf_layers; ++i) if ((r = check_layer(w->drf[i], "draft", i))) return r;
+    for (int i = 0; i < g.tgt_layers; ++i) if ((r = check_layer(w->tgt[i], "target", i, g.tgt_wfmt))) return r;
+    for (int i = 0; i < g.drf_layers; ++i) if ((r = check_layer(w->drf[i], "draft", i, g.drf_wfmt))) return r;
     const Layout L = make_layout(g);
     if (!workspace || workspace_bytes < L.total)
         return fail(DFLASH_ERR_ARG, "workspace %zu bytes < %zu", workspace_bytes, L.total);
@@ -546,6 +605,19 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
         const int rfc[1] = {g.hidden};
         r = plan_gemm(c, &c->fc, c->wf(g.dtype), EPI_STORE, wfc, rfc, 1, g.n_taps * g.hidden,
                       c->ws + L.taps, c->act_xt());
+    }
+    if (!r && g.dtype == DFLASH_BF16) {
+        const int cap = cache_cap(g);
+        const int qrows = (g.n_q / g.n_kv) * DFL_MAX_ROWS;
+        r = make_map_raw(&c->amap_t.q, c->ws + L.qrot, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.head_dim,
+                         (uint64_t)g.n_q * DFL_MAX_ROWS, 64, qrows, CU_TENSOR_MAP_SWIZZLE_128B);
+        c->amap_d.q = c->amap_t.q;
+        if (!r && g.tgt_layers > 0)
+            r = make_map_raw(&c->amap_t.kv, kv_target, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.head_dim,
+                             (uint64_t)g.tgt_layers * 2 * g.n_kv * cap, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (!r && g.drf_layers > 0)
+            r = make_map_raw(&c->amap_d.kv, kv_draft, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.head_dim,
+                             (uint64_t)g.drf_layers * 2 * g.n_kv * cap, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     }
     if (r) {
         delete c;
@@ -771,8 +843,18 @@ int dflash_check(dflash_ctx* c, dflash_stream_t stream) {
     CUDA_TRY(cudaStreamSynchronize(s));
     int err[2];
     CUDA_TRY(cudaMemcpy(err, &c->st()->err, sizeof err, cudaMemcpyDeviceToHost));
+    if (err[0] == DERR_NONE) return DFLASH_OK;
+    const int zero[2] = {0, 0};   // report once, then clear
+    CUDA_TRY(cudaMemcpy(&c->st()->err, zero, sizeof zero, cudaMemcpyHostToDevice));
     if (err[0] == DERR_TIMEOUT) return fail(DFLASH_ERR_TIMEOUT, "bounded wait expired (site %d)", err[1]);
-    if (err[0] != DERR_NONE) return fail(DFLASH_ERR_DEVICE, "device error %d (info %d)", err[0], err[1]);
+    return fail(DFLASH_ERR_DEVICE, "device error %d (info %d)", err[0], err[1]);
+}
+
+int dflash_selftest_timeout(dflash_ctx* c, int64_t limit_ns, dflash_stream_t stream) {
+    if (!c) return fail(DFLASH_ERR_ARG, "ctx is NULL");
+    if (limit_ns < 0 || limit_ns > 2000000000LL) return fail(DFLASH_ERR_ARG, "limit %lld ns", (long long)limit_ns);
+    LAUNCH_TRY(launch_selftest_wait(c->st(), (unsigned long long)limit_ns,
+                                    reinterpret_cast<cudaStream_t>(stream)));
     return DFLASH_OK;
 }
 

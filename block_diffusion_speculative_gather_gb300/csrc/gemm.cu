@@ -72,23 +72,25 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    using CFG = GemmCfg<WF>;
+    constexpr int STAGES = CFG::STAGES, KBLK = CFG::KBLK, XB = CFG::XB, SB = CFG::SB;
     uint8_t* Ws = smem;
-    uint8_t* Xs = Ws + GEMM_STAGES * GEMM_STAGE_W;
-    float* ctile = reinterpret_cast<float*>(Xs + GEMM_STAGES * GEMM_STAGE_X);  // [16][128]
+    uint8_t* Xs = Ws + STAGES * GEMM_STAGE_W;
+    uint8_t* Ss = Xs + STAGES * XB;                                        // INT4 scales
+    float* ctile = reinterpret_cast<float*>(Ss + STAGES * SB);              // [16][128]
     uint64_t* full = reinterpret_cast<uint64_t*>(ctile + DFL_MAX_ROWS * GEMM_BN);
-    uint64_t* empty = full + GEMM_STAGES;
-    volatile int* s_flags = reinterpret_cast<volatile int*>(empty + GEMM_STAGES);
+    uint64_t* empty = full + STAGES;
+    volatile int* s_flags = reinterpret_cast<volatile int*>(empty + STAGES);
     // s_flags[0]: abort, [1]: last-arriver, [2]: consumed stage count
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
     const long long U = (long long)a.n_tiles * a.kb;
     const long long u0 = range_start(blockIdx.x, U, G), u1 = range_start(blockIdx.x + 1, U, G);
-    constexpr int KBLK = (WF == WF_F32) ? 32 : 64;     // k per 128-byte row of a tile
-    constexpr uint32_t STAGE_BYTES = GEMM_STAGE_W + GEMM_STAGE_X;
+    constexpr uint32_t STAGE_BYTES = GEMM_STAGE_W + XB + SB;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < GEMM_STAGES; ++s) {
+        for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], GEMM_CONSUMERS);
         }
@@ -102,7 +104,10 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     if (warp == GEMM_CONSUMERS) {
         // ------------------------------------------------ producer
         if (lane == 0) {
-            for (int i = 0; i < a.n_seg; ++i) tma_prefetch_desc(&maps.w[i]);
+            for (int i = 0; i < a.n_seg; ++i) {
+                tma_prefetch_desc(&maps.w[i]);
+                if (WF == WF_INT4) tma_prefetch_desc(&maps.s[i]);
+            }
             tma_prefetch_desc(&maps.x);
             int stage = 0;
             uint32_t phase = 0;
@@ -117,21 +122,36 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 if (s_flags[0]) break;   // consumers gave up: issue nothing more
                 const int tile = (int)(u / a.kb), k = (int)(u % a.kb);
                 uint8_t* wdst = Ws + stage * GEMM_STAGE_W;
+                uint8_t* sdst = Ss + stage * SB;
+                // weight x coordinate: elements for F32/BF16, bytes for packed INT4
+                const int wx = WF == WF_INT4 ? k * 128 : k * KBLK;
                 mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
                 if (EPI == EPI_SWIGLU) {
-                    tma_load_2d(wdst, &maps.w[0], &full[stage], k * KBLK, tile * 64);
-                    tma_load_2d(wdst + 64 * 128, &maps.w[1], &full[stage], k * KBLK, tile * 64);
+                    tma_load_2d(wdst, &maps.w[0], &full[stage], wx, tile * 64);
+                    tma_load_2d(wdst + 64 * 128, &maps.w[1], &full[stage], wx, tile * 64);
+                    if (WF == WF_INT4) {
+                        tma_load_2d(sdst, &maps.s[0], &full[stage], tile * 64, k * 4);
+                        tma_load_2d(sdst + SB / 2, &maps.s[1], &full[stage], tile * 64, k * 4);
+                    }
                 } else {
                     int row = tile * GEMM_BN, seg = 0;
                     while (seg + 1 < a.n_seg && row >= a.seg_rows[seg]) {
                         row -= a.seg_rows[seg];
                         ++seg;
                     }
-                    tma_load_2d(wdst, &maps.w[seg], &full[stage], k * KBLK, row);
+                    tma_load_2d(wdst, &maps.w[seg], &full[stage], wx, row);
+                    if (WF == WF_INT4) tma_load_2d(sdst, &maps.s[seg], &full[stage], row, k * 4);
                 }
-                tma_load_2d(Xs + stage * GEMM_STAGE_X, &maps.x, &full[stage], k * KBLK, 0);
+                if (WF == WF_INT4) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tma_load_2d(Xs + stage * XB + q * 2048, &maps.x, &full[stage],
+                                    k * KBLK + 64 * q, 0);
+                } else {
+                    tma_load_2d(Xs + stage * XB, &maps.x, &full[stage], k * KBLK, 0);
+                }
                 ++issued;
-                if (++stage == GEMM_STAGES) { stage = 0; phase ^= 1u; }
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
             // Wait (bounded) until the consumers have seen every issued copy
             // land; after an abort, wait (bounded) for the copies still in
@@ -147,7 +167,7 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             }
             if (s_flags[0]) {
                 for (long long j = s_flags[2]; j < issued; ++j)
-                    mbar_wait_bounded(&full[j % GEMM_STAGES], (uint32_t)((j / GEMM_STAGES) & 1),
+                    mbar_wait_bounded(&full[j % STAGES], (uint32_t)((j / STAGES) & 1),
                                       100000000ull);
             }
         }
@@ -178,8 +198,69 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         }
         if (ok) {
             const uint8_t* Wt = Ws + stage * GEMM_STAGE_W;
-            const uint8_t* Xt = Xs + stage * GEMM_STAGE_X;
-            if (WF == WF_BF16) {
+            const uint8_t* Xt = Xs + stage * XB;
+            if (WF == WF_INT4) {
+                // 4 scale groups of 64 k; inside group q a lane owns k 16c..16c+15
+                // of rows r0 and r0+8 (two interleaved 32-bit words each) and the
+                // same 16 k of tokens g and g+8; the group's partial sums are
+                // scaled per row in fp32 and added to the accumulators.
+                const int r0 = warp * 16 + g;
+                const __nv_bfloat16* St = reinterpret_cast<const __nv_bfloat16*>(Ss + stage * SB);
+                const __nv_bfloat162 bias = __floats2bfloat162_rn(136.f, 136.f);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t off = swz128(r0, 2 * q + (c >> 1)) + 8 * (c & 1);
+                    const uint2 wa = *reinterpret_cast<const uint2*>(Wt + off);
+                    const uint2 wb = *reinterpret_cast<const uint2*>(
+                        Wt + swz128(r0 + 8, 2 * q + (c >> 1)) + 8 * (c & 1));
+                    float sa, sb;
+                    if (EPI == EPI_SWIGLU) {
+                        sa = __bfloat162float(St[(r0 >> 6) * 256 + q * 64 + (r0 & 63)]);
+                        sb = __bfloat162float(St[((r0 + 8) >> 6) * 256 + q * 64 + ((r0 + 8) & 63)]);
+                    } else {
+                        sa = __bfloat162float(St[q * 128 + r0]);
+                        sb = __bfloat162float(St[q * 128 + r0 + 8]);
+                    }
+                    uint32_t xa[8], xb[8];
+                    const uint8_t* Xq = Xt + q * 2048;
+                    *reinterpret_cast<uint4*>(&xa[0]) = lds128(Xq + swz128(g, 2 * c));
+                    *reinterpret_cast<uint4*>(&xa[4]) = lds128(Xq + swz128(g, 2 * c + 1));
+                    *reinterpret_cast<uint4*>(&xb[0]) = lds128(Xq + swz128(g + 8, 2 * c));
+                    *reinterpret_cast<uint4*>(&xb[4]) = lds128(Xq + swz128(g + 8, 2 * c + 1));
+                    // dequantise: pair p_i of a word = nibbles (i, i+4) = k (2i, 2i+1)
+                    uint32_t pa[8], pb[8];
+                    const uint32_t wordsa[2] = {wa.x, wa.y}, wordsb[2] = {wb.x, wb.y};
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t ua = ((wordsa[m] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+                            uint32_t ub = ((wordsb[m] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+                            __nv_bfloat162 va = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&ua), bias);
+                            __nv_bfloat162 vb = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&ub), bias);
+                            pa[4 * m + i] = *reinterpret_cast<uint32_t*>(&va);
+                            pb[4 * m + i] = *reinterpret_cast<uint32_t*>(&vb);
+                        }
+                    }
+                    float g0[4] = {0.f, 0.f, 0.f, 0.f}, g1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t A[4] = {pa[2 * j], pb[2 * j], pa[2 * j + 1], pb[2 * j + 1]};
+                        const uint32_t B0[2] = {xa[2 * j], xa[2 * j + 1]};
+                        const uint32_t B1[2] = {xb[2 * j], xb[2 * j + 1]};
+                        mma_bf16_16816(g0, A, B0);
+                        mma_bf16_16816(g1, A, B1);
+                    }
+                    acc[0] = fmaf(sa, g0[0], acc[0]);
+                    acc[1] = fmaf(sa, g0[1], acc[1]);
+                    acc[2] = fmaf(sb, g0[2], acc[2]);
+                    acc[3] = fmaf(sb, g0[3], acc[3]);
+                    acc[4] = fmaf(sa, g1[0], acc[4]);
+                    acc[5] = fmaf(sa, g1[1], acc[5]);
+                    acc[6] = fmaf(sb, g1[2], acc[6]);
+                    acc[7] = fmaf(sb, g1[3], acc[7]);
+                }
+            } else if (WF == WF_BF16) {
                 const int r0 = warp * 16 + g;
                 uint32_t ra[8], rb[8], xa[8], xb[8];
                 *reinterpret_cast<uint4*>(&ra[0]) = lds128(Wt + swz128(r0, 2 * c));
@@ -228,12 +309,12 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stage]);
         if (tid == 0 && ok) s_flags[2] = s_flags[2] + 1;   // stages seen complete
-        if (++stage == GEMM_STAGES) { stage = 0; phase ^= 1u; }
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
 
         if (!(k == a.kb - 1 || u == u1 - 1)) continue;
 
         // ------------------------------------------ finish this tile
-        if (WF == WF_BF16) {
+        if (WF != WF_F32) {
             // C fragment: (row g, tokens 2c,2c+1), (row g+8, tokens 2c,2c+1) per n8 tile
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
@@ -335,8 +416,9 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
 
 template <int WF, int EPI>
 int launch_one(const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t stream) {
-    constexpr size_t smem = 1024 + GEMM_STAGES * (GEMM_STAGE_W + GEMM_STAGE_X) +
-                            DFL_MAX_ROWS * GEMM_BN * 4 + 2 * GEMM_STAGES * 8 + 64;
+    using CFG = GemmCfg<WF>;
+    constexpr size_t smem = 1024 + CFG::STAGES * (GEMM_STAGE_W + CFG::XB + CFG::SB) +
+                            DFL_MAX_ROWS * GEMM_BN * 4 + 2 * CFG::STAGES * 8 + 64;
     static bool attr_set = false;
     if (!attr_set) {
         const cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<WF, EPI>,
@@ -361,6 +443,13 @@ int launch_gemm(int wfmt, int epi, int xt, const GemmMaps& maps, const GemmArgs&
             case EPI_RESID: return launch_one<WF_BF16, EPI_RESID>(maps, args, grid, stream);
             case EPI_SWIGLU: return launch_one<WF_BF16, EPI_SWIGLU>(maps, args, grid, stream);
             case EPI_ARGMAX: return launch_one<WF_BF16, EPI_ARGMAX>(maps, args, grid, stream);
+        }
+    } else if (wfmt == WF_INT4) {
+        switch (epi) {
+            case EPI_STORE: return launch_one<WF_INT4, EPI_STORE>(maps, args, grid, stream);
+            case EPI_RESID: return launch_one<WF_INT4, EPI_RESID>(maps, args, grid, stream);
+            case EPI_SWIGLU: return launch_one<WF_INT4, EPI_SWIGLU>(maps, args, grid, stream);
+            case EPI_ARGMAX: return launch_one<WF_INT4, EPI_ARGMAX>(maps, args, grid, stream);
         }
     } else if (wfmt == WF_F32) {
         switch (epi) {

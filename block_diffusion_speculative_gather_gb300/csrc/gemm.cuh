@@ -12,11 +12,19 @@ enum Epi : int { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3 };
 enum XType : int { XT_F32 = 0, XT_BF16 = 1, XT_F16 = 2 };
 
 constexpr int GEMM_BN = 128;        // output rows (weight rows) per tile
-constexpr int GEMM_STAGES = 8;      // TMA ring depth
 constexpr int GEMM_CONSUMERS = 8;   // MMA warps, 16 weight rows each
 constexpr int GEMM_THREADS = (GEMM_CONSUMERS + 1) * 32;
 constexpr int GEMM_STAGE_W = GEMM_BN * 128;   // bytes of the weight tile per stage
-constexpr int GEMM_STAGE_X = DFL_MAX_ROWS * 128;  // bytes of the activation tile per stage (f32/bf16)
+
+// Per weight format: k per stage, activation bytes per stage, ring depth.
+//   F32 : 32 k  (one 128-byte weight row), X [16][32] fp32
+//   BF16: 64 k  (one 128-byte weight row), X [16][64] bf16
+//   INT4: 256 k (one 128-byte packed row = 4 scale groups), X 4 x [16][64] bf16,
+//         scales [4 groups][128 rows] bf16
+template <int WF> struct GemmCfg;
+template <> struct GemmCfg<0> { static constexpr int KBLK = 32, XB = 2048, SB = 0, STAGES = 8; };
+template <> struct GemmCfg<1> { static constexpr int KBLK = 64, XB = 2048, SB = 0, STAGES = 8; };
+template <> struct GemmCfg<2> { static constexpr int KBLK = 256, XB = 8192, SB = 1024, STAGES = 6; };
 
 struct GemmArgs {
     int N;              // output width (SWIGLU: ffn)
@@ -42,6 +50,7 @@ struct GemmArgs {
 
 struct GemmMaps {
     CUtensorMap w[3];   // weight maps (SWIGLU: 0 = gate, 1 = up)
+    CUtensorMap s[3];   // INT4 scale maps, one per weight map
     CUtensorMap x;      // activation map
 };
 

@@ -185,7 +185,7 @@ __global__ void qk_norm_rope_kernel(QkvArgs a) {
         for (int m = 0; m < PER; ++m) v[m] = r[m];
     }
     if (is_q) {
-        const size_t base = ((size_t)t * a.n_q + h) * HD;
+        const size_t base = ((size_t)h * DFL_MAX_ROWS + t) * HD;   // [n_q][16][HD]
 #pragma unroll
         for (int m = 0; m < PER; ++m) st_any(a.q_out, a.q_type, base + lane + 32 * m, v[m]);
         return;
@@ -196,7 +196,7 @@ __global__ void qk_norm_rope_kernel(QkvArgs a) {
     }
     const int kh = is_k ? h - a.n_q : h - a.n_q - a.n_kv;
     void* cache = is_k ? a.k_cache : a.v_cache;
-    const size_t base = ((size_t)kh * a.max_seq + pos) * HD;
+    const size_t base = ((size_t)kh * a.cap + pos) * HD;
 #pragma unroll
     for (int m = 0; m < PER; ++m) st_any(cache, a.c_type, base + lane + 32 * m, v[m]);
 }
@@ -229,7 +229,7 @@ __global__ void attn_partial_kernel(AttnArgs a) {
     float* Ps = Vs + C * HD;           // [warps][C]
     float* Qs = Ps + (blockDim.x >> 5) * C;   // [warps][HD]
     const int group = a.n_q / a.n_kv;
-    const size_t kbase = (size_t)kh * a.max_seq * HD;
+    const size_t kbase = (size_t)kh * a.cap * HD;
     for (int e = threadIdx.x; e < C * HD; e += blockDim.x) {
         const int j = e / HD, d = e % HD;
         const int key = k0 + j;
@@ -242,7 +242,7 @@ __global__ void attn_partial_kernel(AttnArgs a) {
     const int nq = group * T;
     for (int qi = warp; qi < nq; qi += warps) {
         const int hq = kh * group + qi / T, t = qi % T;
-        const size_t qoff = ((size_t)t * a.n_q + hq) * HD;
+        const size_t qoff = ((size_t)hq * DFL_MAX_ROWS + t) * HD;   // [n_q][16][HD]
         for (int d = lane; d < HD; d += 32) Qs[warp * HD + d] = ld_any(a.q, a.kv_type, qoff + d);
         __syncwarp();
         float s[C / 32];
@@ -469,6 +469,7 @@ __global__ void quantize_int4g64_kernel(const float* __restrict__ w, int n, int 
     for (int o = 4; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
     const __nv_bfloat16 sb = __float2bfloat16_rn(__fdiv_rn(am, 7.0f));
     const float s = __bfloat162float(sb);
+    // interleaved word: k0+2j at nibble j, k0+2j+1 at nibble j+4 (j = 0..3)
     uint32_t word = 0;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -477,13 +478,24 @@ __global__ void quantize_int4g64_kernel(const float* __restrict__ w, int n, int 
             q = (int)rintf(__fdiv_rn(v[e], s));
             q = max(-8, min(7, q));
         }
-        word |= (uint32_t)(q + 8) << (4 * e);
+        const int nib = (e & 1) ? 4 + (e >> 1) : (e >> 1);
+        word |= (uint32_t)(q + 8) << (4 * nib);
     }
     *reinterpret_cast<uint32_t*>(packed + (size_t)row * (k / 2) + k0 / 2) = word;
     if ((lane & 7) == 0) {
         const int grp = (kb * 256 + lane * 8) / 64;
         scales[(size_t)grp * n + row] = *reinterpret_cast<const uint16_t*>(&sb);
     }
+}
+
+// Self-test of the bounded wait: waits on an mbarrier that nothing arrives
+// on; the wait gives up after limit_ns and records DERR_TIMEOUT.
+__global__ void selftest_wait_kernel(DevState* st, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait_bounded(&bar, 0, limit_ns)) set_error(st, DERR_TIMEOUT, 300);
 }
 
 inline int ok_launch() {
@@ -553,6 +565,14 @@ int launch_attention(const AttnArgs& a, cudaStream_t s) {
     return ok_launch();
 }
 
+int launch_attention_combine(const AttnArgs& a, cudaStream_t s) {
+    dim3 g2(a.n_q, DFL_MAX_ROWS);
+    if (a.head_dim == 128) attn_combine_kernel<128><<<g2, 128, 0, s>>>(a);
+    else if (a.head_dim == 64) attn_combine_kernel<64><<<g2, 64, 0, s>>>(a);
+    else return -2;
+    return ok_launch();
+}
+
 int launch_accept(const AcceptArgs& a, cudaStream_t s) {
     accept_kernel<<<1, 32, 0, s>>>(a);
     return ok_launch();
@@ -590,6 +610,11 @@ int launch_tap_reduce(const TapArgs& a, cudaStream_t s) {
         tap_reduce_kernel<float, float><<<(int)blocks, threads, 0, s>>>(a);
     else
         return -2;
+    return ok_launch();
+}
+
+int launch_selftest_wait(DevState* st, unsigned long long limit_ns, cudaStream_t s) {
+    selftest_wait_kernel<<<1, 32, 0, s>>>(st, limit_ns);
     return ok_launch();
 }
 

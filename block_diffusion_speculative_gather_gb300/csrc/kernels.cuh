@@ -40,28 +40,28 @@ struct QkvArgs {
     const float* q_norm;    // [head_dim] (unused when n_q == 0)
     const float* k_norm;
     float eps;
-    void* q_out;            // [16][n_q][head_dim], type q_type
+    void* q_out;            // [n_q][16][head_dim] (head-major), type q_type
     int q_type;
-    void* k_cache;          // layer base of K: [n_kv][max_seq][head_dim], type c_type
+    void* k_cache;          // layer base of K: [n_kv][cap][head_dim], type c_type
     void* v_cache;
     int c_type;
-    int max_seq;
-    int row_sel;            // ROWS_FWD: rows of the forward at fwd_pos0
-                            // ROWS_COMMIT: committed rows at fwd_commit_pos0
-    const float* rope_cos;  // [16][head_dim/2] (ROWS_FWD)
+    int max_seq;            // positions allowed
+    int cap;                // positions per head run (max_seq rounded up to 64)
+    int row_sel;            // ROWS_FWD: the forward's rows; ROWS_COMMIT: the rows
+                            // committed to the draft context (both at fwd_pos0 + row)
+    const float* rope_cos;  // [16][head_dim/2] angles of the forward's rows
     const float* rope_sin;
-    float rope_theta;       // (ROWS_COMMIT computes its own angles)
     DevState* st;
 };
 
 int launch_qk_norm_rope(const QkvArgs& a, cudaStream_t s);
 
 struct AttnArgs {
-    const void* q;          // [16][n_q][head_dim]
-    const void* k_cache;    // layer base [n_kv][max_seq][head_dim]
+    const void* q;          // [n_q][16][head_dim]
+    const void* k_cache;    // layer base [n_kv][cap][head_dim]
     const void* v_cache;
     int kv_type;            // XT_F32 | XT_BF16 (q has the same type)
-    int n_q, n_kv, head_dim, max_seq;
+    int n_q, n_kv, head_dim, cap;
     int causal;             // 1: key pos <= query pos (verify/prefill); 0: draft block
     int window;             // draft: context window (0 = all)
     float scale;
@@ -72,7 +72,10 @@ struct AttnArgs {
     DevState* st;
 };
 
+// CUDA-core split-KV attention (the fp32 path) + the chunk-order combine.
 int launch_attention(const AttnArgs& a, cudaStream_t s);
+// The combine alone (after the tensor-core partial kernel).
+int launch_attention_combine(const AttnArgs& a, cudaStream_t s);
 
 struct AcceptArgs {
     int mode;               // FWD_DRAFT | FWD_VERIFY | FWD_GREEDY | FWD_PREFILL (last chunk)
@@ -111,6 +114,8 @@ struct TapArgs {
 };
 
 int launch_tap_reduce(const TapArgs& a, cudaStream_t s);
+
+int launch_selftest_wait(DevState* st, unsigned long long limit_ns, cudaStream_t s);
 
 int launch_quantize_int4g64(const float* w, int n, int k, uint8_t* packed, uint16_t* scales,
                             cudaStream_t s);

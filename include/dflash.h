@@ -78,7 +78,7 @@ typedef struct {
     int32_t max_seq;                    /* positions held by both caches */
     int32_t eos_id;                     /* -1 = no EOS */
     int32_t dtype;     /* DFLASH_F32 | DFLASH_BF16: embedding, fc, caches, activations */
-    int32_t tgt_wfmt;  /* projection format of target layers: F32 | BF16 (| INT4G64 not yet) */
+    int32_t tgt_wfmt;  /* projection format of target layers: F32 | BF16 | INT4G64 */
     int32_t drf_wfmt;  /* projection format of draft layers: F32 | BF16 | INT4G64 */
     int32_t ctx_norm;  /* 1 = RMSNorm after fc (drafter context) */
     float rms_eps, rope_theta;
@@ -87,10 +87,13 @@ typedef struct {
 /*
  * One decoder layer.  Projections use the nn.Linear layout [out][in].
  *   F32/BF16: element type as the format says.
- *   INT4G64 : packed uint8 [out][in/2], low nibble = even input index,
+ *   INT4G64 : packed [out][in/2] bytes read as little-endian 32-bit words,
+ *             each holding 8 consecutive inputs k0..k0+7 interleaved:
+ *             input k0+2j in nibble j, k0+2j+1 in nibble j+4 (j = 0..3);
  *             code = nibble - 8; the scale pointer (s*) is bf16 [in/64][out]
  *             (group-major); weight = code * scale.  Produced by
- *             dflash_quantize_int4g64().
+ *             dflash_quantize_int4g64().  The interleave lets one AND/OR per
+ *             pair of nibbles build a bf16 pair of adjacent inputs.
  * Norm weights are fp32: ln_attn/ln_mlp [hidden], q_norm/k_norm [head_dim].
  * All matrices must be 16-byte aligned with rows a multiple of 16 bytes.
  */
@@ -131,9 +134,10 @@ typedef struct dflash_ctx dflash_ctx;
 
 /* Bytes of the caller-owned buffers for a configuration (0 if invalid). */
 size_t dflash_workspace_bytes(const dflash_config* cfg /*host*/);
-/* Target KV cache: dtype [tgt_layers][2][n_kv][max_seq][head_dim]. */
+/* Target KV cache: dtype [tgt_layers][2][n_kv][cap][head_dim], cap = max_seq
+ * rounded up to a multiple of 64 (whole attention chunks). */
 size_t dflash_kv_target_bytes(const dflash_config* cfg /*host*/);
-/* Draft context K/V: dtype [drf_layers][2][n_kv][max_seq][head_dim], indexed
+/* Draft context K/V: dtype [drf_layers][2][n_kv][cap][head_dim], indexed
  * by absolute position (a persistent cache bounded by max_seq:
  * "[RFC] DFlash", "Requested changes" 3 and the reply "3. Draft KV cache"). */
 size_t dflash_kv_draft_bytes(const dflash_config* cfg /*host*/);
@@ -200,8 +204,15 @@ int dflash_rollback(dflash_ctx* ctx, int64_t new_len, int32_t token_at_new_len,
 /* Copies the device counters and state to *out (host); synchronises stream. */
 int dflash_stats(dflash_ctx* ctx, dflash_stats_t* out, dflash_stream_t stream);
 
-/* Synchronises stream, returns DEVICE/TIMEOUT if a kernel flagged an error. */
+/* Synchronises stream; returns DEVICE or TIMEOUT if a kernel flagged an
+ * error since the last check (and clears the flag), else OK.  After TIMEOUT
+ * the split-K tickets may be inconsistent: re-create the context. */
 int dflash_check(dflash_ctx* ctx, dflash_stream_t stream);
+
+/* Self-test of the kernels' bounded waits: launches one warp that waits on
+ * an mbarrier nothing arrives on, gives up after limit_ns (<= 2 s) and sets
+ * the device error word, so that the next dflash_check returns TIMEOUT. */
+int dflash_selftest_timeout(dflash_ctx* ctx, int64_t limit_ns, dflash_stream_t stream);
 
 /*
  * Parity taps: while set (non-NULL), every target LM head (verify, and the
@@ -257,8 +268,8 @@ int dflash_tap_reduce(const void* const* layer_streams /*host array*/, int32_t n
  * INT4 group-64 quantiser (the INT4G64 format above) of w fp32 [n][k]:
  * per group of 64 consecutive k of one row, s = bf16(absmax / 7) (round to
  * nearest even), code = clamp(rint(w / s), -8, 7) (0 where s == 0).  The
- * scale and the division are fp32.  packed uint8 [n][k/2], scales bf16
- * [k/64][n].  k must be a multiple of 256.
+ * scale and the division are fp32.  packed [n][k/2] bytes (interleaved
+ * words), scales bf16 [k/64][n].  k must be a multiple of 256.
  */
 int dflash_quantize_int4g64(const float* w, int32_t n, int32_t k, uint8_t* packed,
                             uint16_t* scales, dflash_stream_t stream);

@@ -208,5 +208,16 @@ def test_quantizer_bit_exact_with_oracle():
     capi.dflash_quantize_int4g64(wt, packed, scales)
     torch.cuda.synchronize()
     ref_p, ref_s = O.quantize_int4_g64(w)
-    np.testing.assert_array_equal(packed.cpu().numpy(), ref_p)
+    # the library's words interleave 8 consecutive inputs: k0+2j in nibble j,
+    # k0+2j+1 in nibble j+4; decode them back to the oracle's natural order
+    words = packed.cpu().numpy().view(np.uint32)                 # [384, 64]
+    nib = (words[..., None] >> (4 * np.arange(8, dtype=np.uint32))) & 0xF
+    codes = np.empty((384, 64, 8), np.uint8)
+    codes[..., 0::2] = nib[..., 0:4]
+    codes[..., 1::2] = nib[..., 4:8]
+    codes = codes.reshape(384, 512)
+    ref_codes = np.empty((384, 512), np.uint8)
+    ref_codes[:, 0::2] = ref_p & 0xF
+    ref_codes[:, 1::2] = ref_p >> 4
+    np.testing.assert_array_equal(codes, ref_codes)
     np.testing.assert_array_equal(scales.cpu().numpy().view(np.uint16).T, ref_s)
