@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the drafter-alone, INT4, hc-tap and verify-sweep measurements")
     ap.add_argument("--layers", type=int, default=0,
                     help="(debug) override target layers; lines printed with it are not the workload")
     ap.add_argument("--ncu-rounds", type=int, default=0,
@@ -237,6 +239,7 @@ def run_ours(args):
                     tap_layers=evenly_spaced_taps(args.layers, min(5, args.layers)))
     model = synth.ModelTensors(w)
     dec = DFlash(w, model)
+    model_for_sweep = model if not (args.no_workloads or args.layers) else None
     del model
     prompt = torch.from_numpy(synth.uniform_ids(w.prompt_len, w.vocab))
     B = w.block
@@ -309,12 +312,14 @@ def run_ours(args):
     value = rounds_total / (t_max / 1e3)
 
     # GEMM timing: the same round captured with event nodes around each GEMM
+    # (the prefill runs first, unprofiled; only the captured round is timed)
+    dec.prefill(prompt, w.n_new)
+    torch.cuda.synchronize()
     capi.dflash_profile(dec.ctx, 1)
     gp = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gp, stream=s):
         dec.verify(dec.draft())
     prof_ms, prof_bytes, prof_launch = 0.0, 0.0, 0
-    dec.prefill(prompt, w.n_new)
     for _ in range(args.steps):
         gp.replay()
         p = capi.dflash_profile(dec.ctx, 2)
@@ -378,6 +383,9 @@ def run_ours(args):
 
     if not args.no_e2e:
         result["e2e"] = e2e_measure(dec, w, prompt)
+    if not args.no_workloads and not args.layers:
+        dec.close()
+        result["workloads"] = measure_workloads(args.steps, args.warmup, model_for_sweep)
     if not args.no_cpu_baseline and rank == 0:
         osmp = OracleRoundSample(E2E_BF16)
         for piece in osmp.PIECES:
@@ -390,6 +398,119 @@ def run_ours(args):
     dec.close()
     if world > 1:
         dist.destroy_process_group()
+
+
+def _graph_time(fn, steps, warmup, stream=None):
+    """Captures fn() once as a CUDA graph; returns ms per replay (events)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, g
+
+
+def _gemm_bytes_per_call(dec, fn):
+    """Algorithmic GEMM bytes of one call of fn (library's own accounting)."""
+    import torch
+    from block_diffusion_speculative_gather_gb300 import capi
+    capi.dflash_profile(dec.ctx, 1)
+    fn()
+    torch.cuda.synchronize()
+    p = capi.dflash_profile(dec.ctx, 0)
+    return p.gemm_bytes, p.gemm_ms, p.gemm_launches
+
+
+def measure_workloads(steps, warmup, base_model):
+    """The other workloads, each reported beside the round: drafter alone
+    (bf16, 1024 tap rows, block 16), INT4 drafter (16384 tap rows, window
+    2048, block 8), hc tap reduce (4 x 4096 x hc 4 streams at 4 layers), and
+    the verify sweep T = 1..16 over a 16384-position synthetic KV cache."""
+    import torch
+    from block_diffusion_speculative_gather_gb300 import capi, synth
+    from block_diffusion_speculative_gather_gb300.configs import (DRAFT_BF16, DRAFT_INT4, HC_SWEEP,
+                                                                  HC_TAP)
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+    peak, _ = measured_peak()
+    out = {}
+    # --- drafter alone, bf16 and INT4
+    for w in (DRAFT_BF16, DRAFT_INT4):
+        m = synth.ModelTensors(w)
+        dec = DFlash(w, m)
+        del m
+        taps = synth.tap_rows(w.n_ctx, w.n_taps * w.hidden)
+        ext = taps.view(w.n_ctx, w.n_taps, w.hidden).permute(1, 0, 2).contiguous()
+        del taps
+        dec.prefill_taps(ext, hc=1, first_token=17, max_new=64)
+        del ext
+        dec.draft()
+        torch.cuda.synchronize()
+        gb, gms, gl = _gemm_bytes_per_call(dec, dec.draft)
+        ms, _ = _graph_time(dec.draft, steps, warmup)
+        ctx_rows = min(w.n_ctx, w.window) if w.window else w.n_ctx
+        kv_bytes = w.drf_layers * 2 * w.n_kv * (ctx_rows + w.block) * w.head_dim * 2
+        total = gb + kv_bytes
+        dec.check()
+        out[w.name] = {
+            "draft_rounds_s": round(1e3 / ms, 2), "ms_per_round": round(ms, 4),
+            "bytes_per_round": int(total), "hbm_gbs": round(total / (ms / 1e3) / 1e9, 1),
+            "frac_of_peak": round(total / (ms / 1e3) / 1e9 / peak, 4),
+            "gemm_gbs_event_timed": round(gb / (gms / 1e3) / 1e9, 1) if gms else None,
+            "gemm_launches": gl, "block": w.block, "context_rows": w.n_ctx, "window": w.window,
+            "weights": "INT4 g64 + bf16 scales (projections), bf16 LM head" if w.drf_int4
+                       else "bf16",
+        }
+        dec.close()
+        del dec
+        torch.cuda.empty_cache()
+    # --- hc tap reduce
+    hc = HC_TAP
+    rows_res = {}
+    for rows in hc["rows"]:
+        streams = [torch.randn(rows, hc["hc"] * hc["hidden"], device="cuda",
+                               generator=torch.Generator("cuda").manual_seed(2)).to(torch.bfloat16)
+                   for _ in range(hc["n_layers"])]
+        outb = torch.empty(rows, hc["n_layers"] * hc["hidden"], device="cuda")
+        fn = lambda: capi.dflash_tap_reduce(streams, rows, hc["hc"], hc["hidden"], outb)
+        ms, _ = _graph_time(fn, max(steps, 20), warmup)
+        nbytes = rows * hc["n_layers"] * hc["hidden"] * (hc["hc"] * 2 + 4)
+        rows_res[str(rows)] = {"us": round(ms * 1e3, 2), "bytes": nbytes,
+                               "gbs": round(nbytes / (ms / 1e3) / 1e9, 1)}
+    out["hc_tap"] = {"hc": hc["hc"], "hidden": hc["hidden"], "tap_layers": hc["n_layers"],
+                     "by_rows": rows_res}
+    # --- verify sweep over a 16384-position synthetic KV cache
+    w = HC_SWEEP
+    dec = DFlash(w, base_model)
+    kv = dec.kv_target.view(torch.bfloat16)
+    gen = torch.Generator("cuda").manual_seed(3)
+    chunk = 1 << 26
+    for i in range(0, kv.numel(), chunk):
+        kv[i:i + chunk].normal_(generator=gen)
+    n = w.prompt_len
+    sweep = {}
+    drafts = torch.randint(0, w.vocab, (w.block - 1,), dtype=torch.int32, device="cuda")
+    for T in (1, 2, 4, 8, 16):
+        def fn(T=T):
+            dec.adopt_kv(n, 17, T + 1)
+            dec.verify(drafts if T > 1 else None)
+        ms, _ = _graph_time(fn, steps, warmup)
+        sweep[str(T)] = round(ms, 4)
+    dec.check()
+    kvb = 36 * 2 * w.n_kv * n * w.head_dim * 2
+    out["verify_sweep_16k"] = {"ms_by_T": sweep, "T16_over_T1": round(sweep["16"] / sweep["1"], 3),
+                               "kv_positions": n, "kv_bytes": kvb}
+    dec.close()
+    return out
 
 
 def e2e_measure(dec, w, prompt):

@@ -95,6 +95,7 @@ def _load() -> C.CDLL:
         "dflash_profile": (C.c_int, [vp, i32, C.POINTER(dflash_profile_t)]),
         "dflash_launch_count": (i64, []),
         "dflash_selftest_timeout": (C.c_int, [vp, i64, vp]),
+        "dflash_adopt_kv": (C.c_int, [vp, i32, i32, i32, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -110,7 +111,7 @@ EXPORTED = ("dflash_workspace_bytes", "dflash_kv_target_bytes", "dflash_kv_draft
             "dflash_rollback", "dflash_stats", "dflash_check", "dflash_set_logits_out",
             "dflash_destroy", "dflash_last_error", "dflash_tap_reduce",
             "dflash_quantize_int4g64", "dflash_profile", "dflash_launch_count",
-            "dflash_selftest_timeout")
+            "dflash_selftest_timeout", "dflash_adopt_kv")
 
 
 def check(rc: int) -> None:
@@ -210,3 +211,7 @@ def dflash_launch_count() -> int:
 
 def dflash_selftest_timeout(ctx, limit_ns: int, stream=None):
     check(lib.dflash_selftest_timeout(ctx, limit_ns, _stream(stream)))
+
+
+def dflash_adopt_kv(ctx, n: int, pending_token: int, max_new: int, stream=None):
+    check(lib.dflash_adopt_kv(ctx, n, pending_token, max_new, _stream(stream)))

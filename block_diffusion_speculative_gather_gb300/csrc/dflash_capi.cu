@@ -753,6 +753,19 @@ int dflash_prefill_taps(dflash_ctx* c, const int32_t* prompt_ids, int32_t n_prom
     return DFLASH_OK;
 }
 
+int dflash_adopt_kv(dflash_ctx* c, int32_t n, int32_t pending_token, int32_t max_new,
+                    dflash_stream_t stream) {
+    if (!c) return fail(DFLASH_ERR_ARG, "ctx is NULL");
+    const dflash_config& g = c->cfg;
+    if (n < 1 || n + 1 > g.max_seq) return fail(DFLASH_ERR_CAPACITY, "n %d outside [1, max_seq)", n);
+    if (pending_token < 0 || pending_token >= g.vocab) return fail(DFLASH_ERR_ARG, "token %d", pending_token);
+    if (max_new < 1) return fail(DFLASH_ERR_ARG, "max_new %d < 1", max_new);
+    LAUNCH_TRY(launch_set_ext_state(c->st(), n, pending_token, max_new, g.block_max, g.max_seq,
+                                    g.eos_id, reinterpret_cast<cudaStream_t>(stream)));
+    c->prefilled = true;
+    return DFLASH_OK;
+}
+
 int dflash_draft_block(dflash_ctx* c, int32_t* draft_ids, dflash_stream_t stream) {
     if (!c) return fail(DFLASH_ERR_ARG, "ctx is NULL");
     const dflash_config& g = c->cfg;

@@ -128,6 +128,10 @@ class DFlash:
         capi.dflash_prefill_taps(self.ctx, None, self._taps, self._taps.shape[1], hc,
                                  first_token, max_new, self.stream)
 
+    def adopt_kv(self, n: int, pending_token: int, max_new: int):
+        """Continue from caches filled by the caller (positions [0, n))."""
+        capi.dflash_adopt_kv(self.ctx, n, pending_token, max_new, self.stream)
+
     def draft(self, out: Optional[torch.Tensor] = None) -> torch.Tensor:
         out = self.draft_ids if out is None else out
         capi.dflash_draft_block(self.ctx, out, self.stream)

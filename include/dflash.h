@@ -172,6 +172,17 @@ int dflash_prefill_taps(dflash_ctx* ctx, const int32_t* prompt_ids, int32_t n_pr
                         int32_t max_new, dflash_stream_t stream);
 
 /*
+ * Adopts caches the caller filled itself (e.g. by another prefill engine):
+ * the target cache, and the draft context cache if a drafter is configured,
+ * hold positions [0, n) in the layouts above; the generation continues from
+ * pending_token at position n with budget max_new (that token counts), as
+ * dflash_prefill_taps would leave it.  Errors: CAPACITY (n + 1 > max_seq),
+ * ARG.
+ */
+int dflash_adopt_kv(dflash_ctx* ctx, int32_t n, int32_t pending_token, int32_t max_new,
+                    dflash_stream_t stream);
+
+/*
  * One drafter forward over the block of the device-held length bl at
  * positions n..n+bl-1; writes draft_ids [block_max-1] int32 (entries
  * >= bl-1 are -1).  bl <= 1 drafts nothing ("[RFC] DFlash", "Requested
