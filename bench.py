@@ -383,6 +383,8 @@ def run_ours(args):
 
     if not args.no_e2e:
         result["e2e"] = e2e_measure(dec, w, prompt)
+    del g, gp, gg            # graphs hold event nodes of this context: drop them first
+    torch.cuda.synchronize()
     if not args.no_workloads and not args.layers:
         dec.close()
         result["workloads"] = measure_workloads(args.steps, args.warmup, model_for_sweep)
@@ -456,7 +458,8 @@ def measure_workloads(steps, warmup, base_model):
         dec.draft()
         torch.cuda.synchronize()
         gb, gms, gl = _gemm_bytes_per_call(dec, dec.draft)
-        ms, _ = _graph_time(dec.draft, steps, warmup)
+        ms, gdraft = _graph_time(dec.draft, steps, warmup)
+        del gdraft
         ctx_rows = min(w.n_ctx, w.window) if w.window else w.n_ctx
         kv_bytes = w.drf_layers * 2 * w.n_kv * (ctx_rows + w.block) * w.head_dim * 2
         total = gb + kv_bytes
@@ -482,7 +485,8 @@ def measure_workloads(steps, warmup, base_model):
                    for _ in range(hc["n_layers"])]
         outb = torch.empty(rows, hc["n_layers"] * hc["hidden"], device="cuda")
         fn = lambda: capi.dflash_tap_reduce(streams, rows, hc["hc"], hc["hidden"], outb)
-        ms, _ = _graph_time(fn, max(steps, 20), warmup)
+        ms, gtap = _graph_time(fn, max(steps, 20), warmup)
+        del gtap
         nbytes = rows * hc["n_layers"] * hc["hidden"] * (hc["hc"] * 2 + 4)
         rows_res[str(rows)] = {"us": round(ms * 1e3, 2), "bytes": nbytes,
                                "gbs": round(nbytes / (ms / 1e3) / 1e9, 1)}
@@ -503,7 +507,8 @@ def measure_workloads(steps, warmup, base_model):
         def fn(T=T):
             dec.adopt_kv(n, 17, T + 1)
             dec.verify(drafts if T > 1 else None)
-        ms, _ = _graph_time(fn, steps, warmup)
+        ms, gsw = _graph_time(fn, steps, warmup)
+        del gsw
         sweep[str(T)] = round(ms, 4)
     dec.check()
     kvb = 36 * 2 * w.n_kv * n * w.head_dim * 2

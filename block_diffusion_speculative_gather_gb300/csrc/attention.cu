@@ -53,6 +53,8 @@ attn_mma_kernel(const __grid_constant__ AttnMaps maps, const AttnMmaArgs a) {
     uint8_t* Vs = Ks + HALVES * C * 128;
     uint64_t* bar = reinterpret_cast<uint64_t*>(Vs + HALVES * C * 128);
 
+    pdl_trigger();
+    pdl_wait();
     const int kh = blockIdx.x, c = blockIdx.y;
     const int T = a.st->fwd_T, pos0 = a.st->fwd_pos0;
     const int hi = pos0 + T;
@@ -196,24 +198,23 @@ int launch_attention_mma(const AttnMaps& maps, const AttnMmaArgs& a, int max_chu
     if (a.head_dim == 128) {
         static bool set = false;
         if (!set) {
-            cudaFuncSetAttribute(attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+            const cudaError_t e = cudaFuncSetAttribute(
+                attn_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return (int)e;
             set = true;
         }
-        attn_mma_kernel<128><<<grid, 128, smem, s>>>(maps, a);
+        return (int)launch_k(attn_mma_kernel<128>, grid, dim3(128), smem, s, maps, a);
     } else if (a.head_dim == 64) {
         static bool set = false;
         if (!set) {
-            cudaFuncSetAttribute(attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+            const cudaError_t e = cudaFuncSetAttribute(
+                attn_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return (int)e;
             set = true;
         }
-        attn_mma_kernel<64><<<grid, 128, smem, s>>>(maps, a);
-    } else {
-        return (int)cudaErrorInvalidValue;
+        return (int)launch_k(attn_mma_kernel<64>, grid, dim3(128), smem, s, maps, a);
     }
-    ++g_launches;
-    return (int)cudaGetLastError();
+    return (int)cudaErrorInvalidValue;
 }
 
 }  // namespace dfl

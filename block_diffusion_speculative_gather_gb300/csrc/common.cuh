@@ -41,10 +41,41 @@ struct DevState {
     long long accept_hist[16];
 };
 
+#include <utility>
+
 namespace dfl {
 // Kernels launched through the library by this process (host counter).
 extern long long g_launches;
+// Programmatic dependent launch on (default) or off (environment DFLASH_PDL=0).
+extern bool g_pdl;
+
+// Launches a kernel on stream s with programmatic stream serialisation: the
+// kernel may be scheduled while its predecessor drains; every kernel of the
+// library calls pdl_wait() before it touches memory a predecessor writes.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    ++g_launches;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 }  // namespace dfl
+
+// Programmatic dependent launch: let the next kernel be scheduled now /
+// wait until every predecessor has finished and its writes are visible.
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void set_error(DevState* st, int code, int info) {
     if (atomicCAS(&st->err, 0, code) == 0) st->err_info = info;

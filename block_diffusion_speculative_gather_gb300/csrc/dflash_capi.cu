@@ -294,15 +294,26 @@ int plan_gemm(dflash_ctx* c, GemmPlan* p, int wfmt, int epi, const void* const* 
     return DFLASH_OK;
 }
 
+// Records a profiling event: as an event node when the stream is being
+// captured into a graph, as a plain record otherwise.
+cudaError_t record_event(cudaEvent_t e, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t r = cudaStreamIsCapturing(s, &cs);
+    if (r != cudaSuccess) return r;
+    return cs == cudaStreamCaptureStatusActive
+               ? cudaEventRecordWithFlags(e, s, cudaEventRecordExternal)
+               : cudaEventRecord(e, s);
+}
+
 int run_gemm(dflash_ctx* c, const GemmPlan& p, const GemmArgs& a, cudaStream_t s) {
     const bool timed = c->prof && c->ev_used + 2 <= c->ev.size();
-    if (timed) cudaEventRecordWithFlags(c->ev[c->ev_used], s, cudaEventRecordExternal);
+    if (timed) CUDA_TRY(record_event(c->ev[c->ev_used], s));
     const int e = launch_gemm(p.wfmt, p.epi, p.xt, p.maps, a, p.grid, s);
     if (e)
         return fail(DFLASH_ERR_CUDA, "GEMM launch failed (fmt %d epi %d N %d K %d grid %d): %s",
                     p.wfmt, p.epi, a.N, a.K, p.grid, cudaGetErrorString((cudaError_t)e));
     if (timed) {
-        cudaEventRecordWithFlags(c->ev[c->ev_used + 1], s, cudaEventRecordExternal);
+        CUDA_TRY(record_event(c->ev[c->ev_used + 1], s));
         c->ev_used += 2;
         c->prof_launches += 1;
         c->prof_bytes += p.abytes;
@@ -498,6 +509,16 @@ int run_ingest(dflash_ctx* c, cudaStream_t s) {
     return DFLASH_OK;
 }
 
+// A CUDA error left pending by the caller's own earlier calls would be
+// reported by our first launch check; surface it under its own name instead.
+int pending_error() {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(DFLASH_ERR_CUDA, "a CUDA error was pending before this call: %s",
+                    cudaGetErrorString(e));
+    return DFLASH_OK;
+}
+
 RowsArgs rows_args(dflash_ctx* c, int mode) {
     const dflash_config& g = c->cfg;
     RowsArgs a{};
@@ -685,6 +706,7 @@ int dflash_prefill_taps(dflash_ctx* c, const int32_t* prompt_ids, int32_t n_prom
     const dflash_config& g = c->cfg;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (max_new < 1) return fail(DFLASH_ERR_ARG, "max_new %d < 1", max_new);
+    if (int r0 = pending_error()) return r0;
     int r;
     if (g.tgt_layers > 0) {
         if (!prompt_ids || n_prompt < 1) return fail(DFLASH_ERR_ARG, "prompt missing");
@@ -768,6 +790,7 @@ int dflash_adopt_kv(dflash_ctx* c, int32_t n, int32_t pending_token, int32_t max
 
 int dflash_draft_block(dflash_ctx* c, int32_t* draft_ids, dflash_stream_t stream) {
     if (!c) return fail(DFLASH_ERR_ARG, "ctx is NULL");
+    if (int r0 = pending_error()) return r0;
     const dflash_config& g = c->cfg;
     if (g.drf_layers == 0) return fail(DFLASH_ERR_STATE, "no drafter configured");
     if (!c->prefilled) return fail(DFLASH_ERR_STATE, "draft before prefill");
@@ -794,6 +817,7 @@ int dflash_verify_accept(dflash_ctx* c, const int32_t* draft_ids, int32_t* token
     if (g.tgt_layers == 0) return fail(DFLASH_ERR_STATE, "no target configured");
     if (!c->prefilled) return fail(DFLASH_ERR_STATE, "verify before prefill");
     if (!tokens_out || !n_emitted) return fail(DFLASH_ERR_ARG, "tokens_out / n_emitted is NULL");
+    if (int r0 = pending_error()) return r0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int mode = draft_ids ? FWD_VERIFY : FWD_GREEDY;
     RowsArgs ra = rows_args(c, mode);

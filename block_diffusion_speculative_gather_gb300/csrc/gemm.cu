@@ -28,11 +28,17 @@
 // Every mbarrier wait is bounded; an expired wait sets the device error
 // word, stops new copies and drains the copies already issued.
 
+#include <cstdlib>
+
 #include "gemm.cuh"
 
 namespace dfl {
 
 long long g_launches = 0;
+bool g_pdl = [] {
+    const char* e = getenv("DFLASH_PDL");
+    return !(e && e[0] == '0');
+}();
 
 namespace {
 
@@ -89,6 +95,7 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     const long long u0 = range_start(blockIdx.x, U, G), u1 = range_start(blockIdx.x + 1, U, G);
     constexpr uint32_t STAGE_BYTES = GEMM_STAGE_W + XB + SB;
 
+    pdl_trigger();
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -109,23 +116,13 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 if (WF == WF_INT4) tma_prefetch_desc(&maps.s[i]);
             }
             tma_prefetch_desc(&maps.x);
-            int stage = 0;
-            uint32_t phase = 0;
-            long long issued = 0;
-            for (long long u = u0; u < u1; ++u) {
-                if (s_flags[0]) break;
-                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u)) {
-                    s_flags[0] = 1;
-                    set_error(a.st, DERR_TIMEOUT, 100);
-                    break;
-                }
-                if (s_flags[0]) break;   // consumers gave up: issue nothing more
+            // Stage loads: weight (+ INT4 scale) tiles, then activation tiles.
+            auto load_w = [&](long long u, int stage) {
                 const int tile = (int)(u / a.kb), k = (int)(u % a.kb);
                 uint8_t* wdst = Ws + stage * GEMM_STAGE_W;
                 uint8_t* sdst = Ss + stage * SB;
                 // weight x coordinate: elements for F32/BF16, bytes for packed INT4
                 const int wx = WF == WF_INT4 ? k * 128 : k * KBLK;
-                mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
                 if (EPI == EPI_SWIGLU) {
                     tma_load_2d(wdst, &maps.w[0], &full[stage], wx, tile * 64);
                     tma_load_2d(wdst + 64 * 128, &maps.w[1], &full[stage], wx, tile * 64);
@@ -142,6 +139,9 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     tma_load_2d(wdst, &maps.w[seg], &full[stage], wx, row);
                     if (WF == WF_INT4) tma_load_2d(sdst, &maps.s[seg], &full[stage], row, k * 4);
                 }
+            };
+            auto load_x = [&](long long u, int stage) {
+                const int k = (int)(u % a.kb);
                 if (WF == WF_INT4) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
@@ -150,6 +150,31 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 } else {
                     tma_load_2d(Xs + stage * XB, &maps.x, &full[stage], k * KBLK, 0);
                 }
+            };
+            // The weights do not depend on earlier kernels: fill the ring with
+            // them before waiting for the predecessor (programmatic dependent
+            // launch), then add the activation tiles.
+            const int npre = (int)((u1 - u0) < STAGES ? (u1 - u0) : STAGES);
+            for (int j = 0; j < npre; ++j) {
+                mbar_arrive_expect_tx(&full[j], STAGE_BYTES);
+                load_w(u0 + j, j);
+            }
+            pdl_wait();
+            for (int j = 0; j < npre; ++j) load_x(u0 + j, j);
+            long long issued = npre;
+            int stage = npre % STAGES;
+            uint32_t phase = npre == STAGES ? 1u : 0u;
+            for (long long u = u0 + npre; u < u1; ++u) {
+                if (s_flags[0]) break;
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u)) {
+                    s_flags[0] = 1;
+                    set_error(a.st, DERR_TIMEOUT, 100);
+                    break;
+                }
+                if (s_flags[0]) break;   // consumers gave up: issue nothing more
+                mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                load_w(u, stage);
+                load_x(u, stage);
                 ++issued;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
@@ -175,6 +200,7 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     }
 
     // ---------------------------------------------------- consumers
+    pdl_wait();    // the epilogues read and write buffers of earlier kernels
     const int tid = threadIdx.x;   // 0..255
     const int g = lane >> 2, c = lane & 3;
     int stage = 0;
@@ -427,9 +453,8 @@ int launch_one(const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_
         if (e != cudaSuccess) return (int)e;
         attr_set = true;
     }
-    gemm_skinny_kernel<WF, EPI><<<grid, GEMM_THREADS, smem, stream>>>(maps, args);
-    ++g_launches;
-    return (int)cudaGetLastError();
+    return (int)launch_k(gemm_skinny_kernel<WF, EPI>, dim3(grid), dim3(GEMM_THREADS), smem, stream,
+                         maps, args);
 }
 
 }  // namespace

@@ -45,6 +45,8 @@ __device__ __forceinline__ int rows_of(const DevState* st, int sel, int* r0) {
 // One CTA: sets the forward descriptor (thread 0), then every CTA gathers
 // its row of the embedding into the fp32 residual and fills the RoPE table.
 __global__ void prepare_rows_kernel(RowsArgs a) {
+    pdl_trigger();
+    pdl_wait();
     DevState* st = a.st;
     __shared__ int s_T, s_pos0, s_tok;
     const int t = blockIdx.x;   // row
@@ -110,6 +112,8 @@ template <typename OT>
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                OT* __restrict__ out, int hidden, float eps, int row_sel,
                                int apply, const DevState* st) {
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.x;
     int r0;
     const int n = rows_of(st, row_sel, &r0);
@@ -145,6 +149,8 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restr
 // the attention input and k, v to the cache at the row's absolute position.
 template <int HD>
 __global__ void qk_norm_rope_kernel(QkvArgs a) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int PER = HD / 32;   // elements per lane; lane holds i = lane + 32 m
     const int warps = blockDim.x >> 5;
     const int gw = blockIdx.x * warps + (threadIdx.x >> 5);
@@ -216,6 +222,8 @@ __device__ __forceinline__ void attn_range(const AttnArgs& a, int* lo, int* hi, 
 // causal rule, weigh exactly zero.
 template <int HD>
 __global__ void attn_partial_kernel(AttnArgs a) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int C = ATTN_CHUNK;
     const int kh = blockIdx.x, c = blockIdx.y;
     int lo, hi, T, pos0;
@@ -281,34 +289,71 @@ __global__ void attn_partial_kernel(AttnArgs a) {
     }
 }
 
-// Folds the chunks of one (row, q head) in chunk order and normalises.
+// Folds the chunks of one (row, q head) in chunk order and normalises.  The
+// chunk maxima and sums are staged in shared memory by all threads at once;
+// every thread then folds its output element over the chunks in chunk
+// order (fully masked chunks add exact zeros at the end, so a row's result
+// does not depend on the forward's row count).
 template <int HD>
 __global__ void attn_combine_kernel(AttnArgs a) {
+    pdl_trigger();
+    pdl_wait();
+    constexpr int MAXC = 512;
+    __shared__ float s_w[MAXC];
+    __shared__ float s_l[MAXC];
+    __shared__ float s_red[HD / 32];
     const int hq = blockIdx.x, t = blockIdx.y, d = threadIdx.x;
     int lo, hi, T, pos0;
     attn_range(a, &lo, &hi, &T, &pos0);
-    const size_t o = (size_t)t * a.n_q * HD + (size_t)hq * HD + d;
+    const size_t o = ((size_t)t * a.n_q + hq) * HD + d;
     if (t >= T) {
         st_any(a.out, a.out_type, o, 0.f);
         return;
     }
     const int c_lo = lo / ATTN_CHUNK, c_hi = (hi - 1) / ATTN_CHUNK;
-    float M = -INFINITY;
-    for (int c = c_lo; c <= c_hi; ++c)
-        M = fmaxf(M, a.part[(((size_t)c * DFL_MAX_ROWS + t) * a.n_q + hq) * (HD + 2)]);
-    float L = 0.f, O = 0.f;
-    for (int c = c_lo; c <= c_hi; ++c) {
-        const float* p = a.part + (((size_t)c * DFL_MAX_ROWS + t) * a.n_q + hq) * (HD + 2);
-        const float w = (p[0] == -INFINITY) ? 0.f : expf(p[0] - M);
-        L = fmaf(p[1], w, L);
-        O = fmaf(p[2 + d], w, O);
+    const int nc = c_hi - c_lo + 1;
+    const size_t cstride = (size_t)DFL_MAX_ROWS * a.n_q * (HD + 2);
+    const float* base = a.part + ((size_t)c_lo * DFL_MAX_ROWS + t) * a.n_q * (HD + 2) +
+                        (size_t)hq * (HD + 2);
+    if (nc > MAXC) {
+        if (d == 0) set_error(a.st, DERR_INDEX, nc);
+        return;
     }
+    float mx = -INFINITY;
+    for (int i = d; i < nc; i += HD) {
+        const float m = base[i * cstride];
+        s_w[i] = m;
+        s_l[i] = base[i * cstride + 1];
+        mx = fmaxf(mx, m);
+    }
+    mx = warp_max(mx);
+    if ((d & 31) == 0) s_red[d >> 5] = mx;
+    __syncthreads();
+    float M = s_red[0];
+#pragma unroll
+    for (int w = 1; w < HD / 32; ++w) M = fmaxf(M, s_red[w]);
+    for (int i = d; i < nc; i += HD) s_w[i] = (s_w[i] == -INFINITY) ? 0.f : expf(s_w[i] - M);
+    __syncthreads();
+    float L = 0.f, O = 0.f;
+    int i = 0;
+    for (; i + 4 <= nc; i += 4) {
+        const float o0 = base[(i + 0) * cstride + 2 + d], o1 = base[(i + 1) * cstride + 2 + d];
+        const float o2 = base[(i + 2) * cstride + 2 + d], o3 = base[(i + 3) * cstride + 2 + d];
+        O = fmaf(o0, s_w[i + 0], O);
+        O = fmaf(o1, s_w[i + 1], O);
+        O = fmaf(o2, s_w[i + 2], O);
+        O = fmaf(o3, s_w[i + 3], O);
+    }
+    for (; i < nc; ++i) O = fmaf(base[i * cstride + 2 + d], s_w[i], O);
+    for (int j = 0; j < nc; ++j) L = fmaf(s_l[j], s_w[j], L);
     st_any(a.out, a.out_type, o, O / L);
 }
 
 // --------------------------------------------------------------- acceptance
 
 __global__ void accept_kernel(AcceptArgs a) {
+    pdl_trigger();
+    pdl_wait();
     if (threadIdx.x != 0) return;
     DevState* st = a.st;
     const int T = st->fwd_T;
@@ -375,6 +420,8 @@ __global__ void accept_kernel(AcceptArgs a) {
 }
 
 __global__ void set_chunk_kernel(DevState* st, int pos0, int T, int commit_lo) {
+    pdl_trigger();
+    pdl_wait();
     st->fwd_pos0 = pos0;
     st->fwd_T = T;
     const int r0 = max(0, commit_lo - pos0);
@@ -383,6 +430,8 @@ __global__ void set_chunk_kernel(DevState* st, int pos0, int T, int commit_lo) {
 }
 
 __global__ void rollback_kernel(DevState* st, int new_len, int token, int B, int max_seq) {
+    pdl_trigger();
+    pdl_wait();
     const int old = st->n;
     st->n = new_len;
     st->t_n = token;
@@ -394,6 +443,8 @@ __global__ void rollback_kernel(DevState* st, int new_len, int token, int B, int
 
 __global__ void set_ext_state_kernel(DevState* st, int n_ext, int tok, int max_new, int B,
                                      int max_seq, int eos) {
+    pdl_trigger();
+    pdl_wait();
     st->n = n_ext;
     st->t_n = tok;
     st->generated = 1;
@@ -415,6 +466,8 @@ __global__ void set_ext_state_kernel(DevState* st, int n_ext, int tok, int max_n
 // consecutive columns per thread (16-byte loads of bf16 streams).
 template <typename IT, typename OT>
 __global__ void tap_reduce_kernel(TapArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const long long per_row = (long long)a.n_layers * a.hidden / 8;
     const long long total = per_row * a.rows;
     const float inv = 1.0f / (float)a.hc;
@@ -451,6 +504,8 @@ __global__ void tap_reduce_kernel(TapArgs a) {
 // lanes 8q..8q+7 form group q.
 __global__ void quantize_int4g64_kernel(const float* __restrict__ w, int n, int k,
                                         uint8_t* __restrict__ packed, uint16_t* __restrict__ scales) {
+    pdl_trigger();
+    pdl_wait();
     const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     const int per_row = k / 256;
@@ -491,6 +546,8 @@ __global__ void quantize_int4g64_kernel(const float* __restrict__ w, int n, int 
 // Self-test of the bounded wait: waits on an mbarrier that nothing arrives
 // on; the wait gives up after limit_ns and records DERR_TIMEOUT.
 __global__ void selftest_wait_kernel(DevState* st, unsigned long long limit_ns) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ uint64_t bar;
     if (threadIdx.x != 0) return;
     mbar_init(&bar, 1);
@@ -498,102 +555,92 @@ __global__ void selftest_wait_kernel(DevState* st, unsigned long long limit_ns) 
     if (!mbar_wait_bounded(&bar, 0, limit_ns)) set_error(st, DERR_TIMEOUT, 300);
 }
 
-inline int ok_launch() {
-    ++g_launches;
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
-}
+inline int ok(cudaError_t e) { return e == cudaSuccess ? 0 : -1; }
 
 }  // namespace
 
 int launch_prepare_rows(const RowsArgs& a, cudaStream_t s) {
-    prepare_rows_kernel<<<DFL_MAX_ROWS, 256, 0, s>>>(a);
-    return ok_launch();
+    return ok(launch_k(prepare_rows_kernel, dim3(DFL_MAX_ROWS), dim3(256), 0, s, a));
 }
 
 int launch_rmsnorm(const float* x, const float* w, void* out, int out_type, int hidden,
                    float eps, int row_sel, int apply, const DevState* st, cudaStream_t s) {
+    const dim3 g(DFL_MAX_ROWS), b(256);
     if (out_type == XT_F32)
-        rmsnorm_kernel<float><<<DFL_MAX_ROWS, 256, 0, s>>>(x, w, (float*)out, hidden, eps, row_sel,
-                                                           apply, st);
-    else if (out_type == XT_BF16)
-        rmsnorm_kernel<__nv_bfloat16><<<DFL_MAX_ROWS, 256, 0, s>>>(x, w, (__nv_bfloat16*)out, hidden,
-                                                                   eps, row_sel, apply, st);
-    else
-        rmsnorm_kernel<__half><<<DFL_MAX_ROWS, 256, 0, s>>>(x, w, (__half*)out, hidden, eps, row_sel,
-                                                            apply, st);
-    return ok_launch();
+        return ok(launch_k(rmsnorm_kernel<float>, g, b, 0, s, x, w, (float*)out, hidden, eps,
+                           row_sel, apply, st));
+    if (out_type == XT_BF16)
+        return ok(launch_k(rmsnorm_kernel<__nv_bfloat16>, g, b, 0, s, x, w, (__nv_bfloat16*)out,
+                           hidden, eps, row_sel, apply, st));
+    return ok(launch_k(rmsnorm_kernel<__half>, g, b, 0, s, x, w, (__half*)out, hidden, eps,
+                       row_sel, apply, st));
 }
 
 int launch_qk_norm_rope(const QkvArgs& a, cudaStream_t s) {
     const int heads = a.n_q + 2 * a.n_kv;
     const int warps = 8;
     const int blocks = (DFL_MAX_ROWS * heads + warps - 1) / warps;
-    if (a.head_dim == 128) qk_norm_rope_kernel<128><<<blocks, warps * 32, 0, s>>>(a);
-    else if (a.head_dim == 64) qk_norm_rope_kernel<64><<<blocks, warps * 32, 0, s>>>(a);
-    else return -2;
-    return ok_launch();
+    if (a.head_dim == 128)
+        return ok(launch_k(qk_norm_rope_kernel<128>, dim3(blocks), dim3(warps * 32), 0, s, a));
+    if (a.head_dim == 64)
+        return ok(launch_k(qk_norm_rope_kernel<64>, dim3(blocks), dim3(warps * 32), 0, s, a));
+    return -2;
 }
 
 int launch_attention(const AttnArgs& a, cudaStream_t s) {
     const int threads = 256;
     const size_t smem =
         (size_t)(2 * ATTN_CHUNK * a.head_dim + (threads / 32) * (ATTN_CHUNK + a.head_dim)) * 4;
-    dim3 g1(a.n_kv, a.max_chunks), g2(a.n_q, DFL_MAX_ROWS);
+    const dim3 g1(a.n_kv, a.max_chunks);
     if (a.head_dim == 128) {
         static bool set = false;
         if (!set) {
-            cudaFuncSetAttribute(attn_partial_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+            if (cudaFuncSetAttribute(attn_partial_kernel<128>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+                return -1;
             set = true;
         }
-        attn_partial_kernel<128><<<g1, threads, smem, s>>>(a);
-        ++g_launches;
-        attn_combine_kernel<128><<<g2, 128, 0, s>>>(a);
+        if (ok(launch_k(attn_partial_kernel<128>, g1, dim3(threads), smem, s, a))) return -1;
     } else if (a.head_dim == 64) {
         static bool set = false;
         if (!set) {
-            cudaFuncSetAttribute(attn_partial_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+            if (cudaFuncSetAttribute(attn_partial_kernel<64>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+                return -1;
             set = true;
         }
-        attn_partial_kernel<64><<<g1, threads, smem, s>>>(a);
-        ++g_launches;
-        attn_combine_kernel<64><<<g2, 64, 0, s>>>(a);
+        if (ok(launch_k(attn_partial_kernel<64>, g1, dim3(threads), smem, s, a))) return -1;
     } else {
         return -2;
     }
-    return ok_launch();
+    return launch_attention_combine(a, s);
 }
 
 int launch_attention_combine(const AttnArgs& a, cudaStream_t s) {
-    dim3 g2(a.n_q, DFL_MAX_ROWS);
-    if (a.head_dim == 128) attn_combine_kernel<128><<<g2, 128, 0, s>>>(a);
-    else if (a.head_dim == 64) attn_combine_kernel<64><<<g2, 64, 0, s>>>(a);
-    else return -2;
-    return ok_launch();
+    const dim3 g2(a.n_q, DFL_MAX_ROWS);
+    if (a.head_dim == 128) return ok(launch_k(attn_combine_kernel<128>, g2, dim3(128), 0, s, a));
+    if (a.head_dim == 64) return ok(launch_k(attn_combine_kernel<64>, g2, dim3(64), 0, s, a));
+    return -2;
 }
 
 int launch_accept(const AcceptArgs& a, cudaStream_t s) {
-    accept_kernel<<<1, 32, 0, s>>>(a);
-    return ok_launch();
+    return ok(launch_k(accept_kernel, dim3(1), dim3(32), 0, s, a));
 }
 
 int launch_set_chunk(DevState* st, int pos0, int T, int commit_lo, cudaStream_t s) {
-    set_chunk_kernel<<<1, 1, 0, s>>>(st, pos0, T, commit_lo);
-    return ok_launch();
+    return ok(launch_k(set_chunk_kernel, dim3(1), dim3(1), 0, s, st, pos0, T, commit_lo));
 }
 
 int launch_rollback(DevState* st, int new_len, int token, int block_max, int max_seq,
                     cudaStream_t s) {
-    rollback_kernel<<<1, 1, 0, s>>>(st, new_len, token, block_max, max_seq);
-    return ok_launch();
+    return ok(launch_k(rollback_kernel, dim3(1), dim3(1), 0, s, st, new_len, token, block_max,
+                       max_seq));
 }
 
 int launch_set_ext_state(DevState* st, int n_ext, int first_token, int max_new, int block_max,
                          int max_seq, int eos_id, cudaStream_t s) {
-    set_ext_state_kernel<<<1, 1, 0, s>>>(st, n_ext, first_token, max_new, block_max, max_seq,
-                                         eos_id);
-    return ok_launch();
+    return ok(launch_k(set_ext_state_kernel, dim3(1), dim3(1), 0, s, st, n_ext, first_token,
+                       max_new, block_max, max_seq, eos_id));
 }
 
 int launch_tap_reduce(const TapArgs& a, cudaStream_t s) {
@@ -602,29 +649,26 @@ int launch_tap_reduce(const TapArgs& a, cudaStream_t s) {
     long long blocks = (vecs + threads - 1) / threads;
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
+    const dim3 g((unsigned)blocks), b(threads);
     if (a.in_type == XT_BF16 && a.out_type == XT_F32)
-        tap_reduce_kernel<__nv_bfloat16, float><<<(int)blocks, threads, 0, s>>>(a);
-    else if (a.in_type == XT_BF16 && a.out_type == XT_BF16)
-        tap_reduce_kernel<__nv_bfloat16, __nv_bfloat16><<<(int)blocks, threads, 0, s>>>(a);
-    else if (a.in_type == XT_F32 && a.out_type == XT_F32)
-        tap_reduce_kernel<float, float><<<(int)blocks, threads, 0, s>>>(a);
-    else
-        return -2;
-    return ok_launch();
+        return ok(launch_k(tap_reduce_kernel<__nv_bfloat16, float>, g, b, 0, s, a));
+    if (a.in_type == XT_BF16 && a.out_type == XT_BF16)
+        return ok(launch_k(tap_reduce_kernel<__nv_bfloat16, __nv_bfloat16>, g, b, 0, s, a));
+    if (a.in_type == XT_F32 && a.out_type == XT_F32)
+        return ok(launch_k(tap_reduce_kernel<float, float>, g, b, 0, s, a));
+    return -2;
 }
 
 int launch_selftest_wait(DevState* st, unsigned long long limit_ns, cudaStream_t s) {
-    selftest_wait_kernel<<<1, 32, 0, s>>>(st, limit_ns);
-    return ok_launch();
+    return ok(launch_k(selftest_wait_kernel, dim3(1), dim3(32), 0, s, st, limit_ns));
 }
 
 int launch_quantize_int4g64(const float* w, int n, int k, uint8_t* packed, uint16_t* scales,
                             cudaStream_t s) {
     const long long warps = (long long)n * (k / 256);
     const int per_block = 8;
-    quantize_int4g64_kernel<<<(int)((warps + per_block - 1) / per_block), per_block * 32, 0, s>>>(
-        w, n, k, packed, scales);
-    return ok_launch();
+    return ok(launch_k(quantize_int4g64_kernel, dim3((unsigned)((warps + per_block - 1) / per_block)),
+                       dim3(per_block * 32), 0, s, w, n, k, packed, scales));
 }
 
 }  // namespace dfl
