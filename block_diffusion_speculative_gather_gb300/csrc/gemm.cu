@@ -80,10 +80,12 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     using CFG = GemmCfg<WF>;
     constexpr int STAGES = CFG::STAGES, KBLK = CFG::KBLK, XB = CFG::XB, SB = CFG::SB;
-    uint8_t* Ws = smem;
-    uint8_t* Xs = Ws + STAGES * GEMM_STAGE_W;
-    uint8_t* Ss = Xs + STAGES * XB;                                        // INT4 scales
-    float* ctile = reinterpret_cast<float*>(Ss + STAGES * SB);              // [16][128]
+    constexpr int CHUNK = CFG::CHUNK;
+    constexpr uint32_t KB_BYTES = GEMM_STAGE_W + XB + SB;     // bytes of one k-block
+    uint8_t* Ws = smem;                                        // [STAGES][CHUNK][128 x 128 B]
+    uint8_t* Xs = Ws + STAGES * CHUNK * GEMM_STAGE_W;          // [STAGES][CHUNK][XB]
+    uint8_t* Ss = Xs + STAGES * CHUNK * XB;                    // [STAGES][CHUNK][SB] (INT4)
+    float* ctile = reinterpret_cast<float*>(Ss + STAGES * CHUNK * SB);   // [16][128]
     uint64_t* full = reinterpret_cast<uint64_t*>(ctile + DFL_MAX_ROWS * GEMM_BN);
     uint64_t* empty = full + STAGES;
     volatile int* s_flags = reinterpret_cast<volatile int*>(empty + STAGES);
@@ -93,7 +95,14 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     const int G = gridDim.x;
     const long long U = (long long)a.n_tiles * a.kb;
     const long long u0 = range_start(blockIdx.x, U, G), u1 = range_start(blockIdx.x + 1, U, G);
-    constexpr uint32_t STAGE_BYTES = GEMM_STAGE_W + XB + SB;
+    // k-blocks in the stage that starts at unit u: never past the tile or the range
+    auto chunk_len = [&](long long u) {
+        long long n = CHUNK;
+        if (u1 - u < n) n = u1 - u;
+        const long long to_tile_end = a.kb - (u % a.kb);
+        if (to_tile_end < n) n = to_tile_end;
+        return (int)n;
+    };
 
     pdl_trigger();
     if (threadIdx.x == 0) {
@@ -116,11 +125,11 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 if (WF == WF_INT4) tma_prefetch_desc(&maps.s[i]);
             }
             tma_prefetch_desc(&maps.x);
-            // Stage loads: weight (+ INT4 scale) tiles, then activation tiles.
-            auto load_w = [&](long long u, int stage) {
+            // weight (+ INT4 scale) tile of unit u into slot j of a stage
+            auto load_w = [&](long long u, int stage, int j) {
                 const int tile = (int)(u / a.kb), k = (int)(u % a.kb);
-                uint8_t* wdst = Ws + stage * GEMM_STAGE_W;
-                uint8_t* sdst = Ss + stage * SB;
+                uint8_t* wdst = Ws + (stage * CHUNK + j) * GEMM_STAGE_W;
+                uint8_t* sdst = Ss + (stage * CHUNK + j) * SB;
                 // weight x coordinate: elements for F32/BF16, bytes for packed INT4
                 const int wx = WF == WF_INT4 ? k * 128 : k * KBLK;
                 if (EPI == EPI_SWIGLU) {
@@ -140,31 +149,41 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     if (WF == WF_INT4) tma_load_2d(sdst, &maps.s[seg], &full[stage], row, k * 4);
                 }
             };
-            auto load_x = [&](long long u, int stage) {
+            // activation tile(s) of unit u into slot j of a stage
+            auto load_x = [&](long long u, int stage, int j) {
                 const int k = (int)(u % a.kb);
+                uint8_t* xdst = Xs + (stage * CHUNK + j) * XB;
                 if (WF == WF_INT4) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        tma_load_2d(Xs + stage * XB + q * 2048, &maps.x, &full[stage],
-                                    k * KBLK + 64 * q, 0);
+                        tma_load_2d(xdst + q * 2048, &maps.x, &full[stage], k * KBLK + 64 * q, 0);
                 } else {
-                    tma_load_2d(Xs + stage * XB, &maps.x, &full[stage], k * KBLK, 0);
+                    tma_load_2d(xdst, &maps.x, &full[stage], k * KBLK, 0);
                 }
             };
             // The weights do not depend on earlier kernels: fill the ring with
             // them before waiting for the predecessor (programmatic dependent
             // launch), then add the activation tiles.
-            const int npre = (int)((u1 - u0) < STAGES ? (u1 - u0) : STAGES);
-            for (int j = 0; j < npre; ++j) {
-                mbar_arrive_expect_tx(&full[j], STAGE_BYTES);
-                load_w(u0 + j, j);
+            long long pu[STAGES];
+            int pl[STAGES];
+            int npre = 0;
+            long long u = u0;
+            while (u < u1 && npre < STAGES) {
+                const int len = chunk_len(u);
+                pu[npre] = u;
+                pl[npre] = len;
+                mbar_arrive_expect_tx(&full[npre], len * KB_BYTES);
+                for (int j = 0; j < len; ++j) load_w(u + j, npre, j);
+                u += len;
+                ++npre;
             }
             pdl_wait();
-            for (int j = 0; j < npre; ++j) load_x(u0 + j, j);
+            for (int i = 0; i < npre; ++i)
+                for (int j = 0; j < pl[i]; ++j) load_x(pu[i] + j, i, j);
             long long issued = npre;
             int stage = npre % STAGES;
             uint32_t phase = npre == STAGES ? 1u : 0u;
-            for (long long u = u0 + npre; u < u1; ++u) {
+            while (u < u1) {
                 if (s_flags[0]) break;
                 if (!mbar_wait_bounded(&empty[stage], phase ^ 1u)) {
                     s_flags[0] = 1;
@@ -172,9 +191,13 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     break;
                 }
                 if (s_flags[0]) break;   // consumers gave up: issue nothing more
-                mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                load_w(u, stage);
-                load_x(u, stage);
+                const int len = chunk_len(u);
+                mbar_arrive_expect_tx(&full[stage], len * KB_BYTES);
+                for (int j = 0; j < len; ++j) {
+                    load_w(u + j, stage, j);
+                    load_x(u + j, stage, j);
+                }
+                u += len;
                 ++issued;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
@@ -208,7 +231,8 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     float acc[8];
     int first_tile_of_me = (int)(u0 / a.kb);
 
-    for (long long u = u0; u < u1; ++u) {
+    for (long long u = u0; u < u1;) {
+        const int len = chunk_len(u);
         const int tile = (int)(u / a.kb), k = (int)(u % a.kb);
         if (k == 0 || u == u0) {
 #pragma unroll
@@ -223,15 +247,17 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             }
         }
         if (ok) {
-            const uint8_t* Wt = Ws + stage * GEMM_STAGE_W;
-            const uint8_t* Xt = Xs + stage * XB;
+            for (int jb = 0; jb < len; ++jb) {
+            const uint8_t* Wt = Ws + (stage * CHUNK + jb) * GEMM_STAGE_W;
+            const uint8_t* Xt = Xs + (stage * CHUNK + jb) * XB;
+            const uint8_t* Sb = Ss + (stage * CHUNK + jb) * SB;
             if (WF == WF_INT4) {
                 // 4 scale groups of 64 k; inside group q a lane owns k 16c..16c+15
                 // of rows r0 and r0+8 (two interleaved 32-bit words each) and the
                 // same 16 k of tokens g and g+8; the group's partial sums are
                 // scaled per row in fp32 and added to the accumulators.
                 const int r0 = warp * 16 + g;
-                const __nv_bfloat16* St = reinterpret_cast<const __nv_bfloat16*>(Ss + stage * SB);
+                const __nv_bfloat16* St = reinterpret_cast<const __nv_bfloat16*>(Sb);
                 const __nv_bfloat162 bias = __floats2bfloat162_rn(136.f, 136.f);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -331,13 +357,15 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     }
                 }
             }
+            }   // k-blocks of the stage
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stage]);
         if (tid == 0 && ok) s_flags[2] = s_flags[2] + 1;   // stages seen complete
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        u += len;
 
-        if (!(k == a.kb - 1 || u == u1 - 1)) continue;
+        if (!(k + len == a.kb || u == u1)) continue;
 
         // ------------------------------------------ finish this tile
         if (WF != WF_F32) {
@@ -381,15 +409,41 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             if (do_epi) {
                 __threadfence();
                 if (tid == 0) a.counters[tile] = 0;
-                for (int e = tid; e < GEMM_BN * DFL_MAX_ROWS; e += GEMM_CONSUMERS * 32) {
-                    float v = 0.f;
-                    for (int i = i_first; i <= i_last; ++i) {
-                        const int first_i = (int)(range_start(i, U, G) / a.kb);
-                        const int si = (tile == first_i) ? 0 : 1;
-                        v += __ldcg(a.slots + ((size_t)i * 2 + si) * (GEMM_BN * DFL_MAX_ROWS) + e);
-                    }
-                    ctile[e] = v;
+                // Sum the parts in CTA order.  Each thread owns 8 consecutive
+                // elements (two float4) and issues the loads of four parts at
+                // a time, so the L2 round trips overlap.
+                const int e0 = tid * 8;
+                float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+                auto part_ptr = [&](int i) {
+                    const int first_i = (int)(range_start(i, U, G) / a.kb);
+                    const int si = (tile == first_i) ? 0 : 1;
+                    return a.slots + ((size_t)i * 2 + si) * (GEMM_BN * DFL_MAX_ROWS) + e0;
+                };
+                auto add4 = [](float4& x, const float4& y) {
+                    x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+                };
+                int i = i_first;
+                for (; i + 3 <= i_last; i += 4) {
+                    const float4* p0 = reinterpret_cast<const float4*>(part_ptr(i));
+                    const float4* p1 = reinterpret_cast<const float4*>(part_ptr(i + 1));
+                    const float4* p2 = reinterpret_cast<const float4*>(part_ptr(i + 2));
+                    const float4* p3 = reinterpret_cast<const float4*>(part_ptr(i + 3));
+                    const float4 a0 = __ldcg(p0), b0 = __ldcg(p0 + 1);
+                    const float4 a1 = __ldcg(p1), b1 = __ldcg(p1 + 1);
+                    const float4 a2 = __ldcg(p2), b2 = __ldcg(p2 + 1);
+                    const float4 a3 = __ldcg(p3), b3 = __ldcg(p3 + 1);
+                    add4(acc0, a0); add4(acc1, b0);
+                    add4(acc0, a1); add4(acc1, b1);
+                    add4(acc0, a2); add4(acc1, b2);
+                    add4(acc0, a3); add4(acc1, b3);
                 }
+                for (; i <= i_last; ++i) {
+                    const float4* p0 = reinterpret_cast<const float4*>(part_ptr(i));
+                    add4(acc0, __ldcg(p0));
+                    add4(acc1, __ldcg(p0 + 1));
+                }
+                *reinterpret_cast<float4*>(ctile + e0) = acc0;
+                *reinterpret_cast<float4*>(ctile + e0 + 4) = acc1;
                 consumer_bar();
             }
         }
@@ -443,8 +497,9 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
 template <int WF, int EPI>
 int launch_one(const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_t stream) {
     using CFG = GemmCfg<WF>;
-    constexpr size_t smem = 1024 + CFG::STAGES * (GEMM_STAGE_W + CFG::XB + CFG::SB) +
+    constexpr size_t smem = 1024 + (size_t)CFG::STAGES * CFG::CHUNK * (GEMM_STAGE_W + CFG::XB + CFG::SB) +
                             DFL_MAX_ROWS * GEMM_BN * 4 + 2 * CFG::STAGES * 8 + 64;
+    static_assert(smem <= 232448, "GEMM shared memory exceeds the per-block limit");
     static bool attr_set = false;
     if (!attr_set) {
         const cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<WF, EPI>,

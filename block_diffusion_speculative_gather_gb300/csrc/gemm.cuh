@@ -16,15 +16,23 @@ constexpr int GEMM_CONSUMERS = 8;   // MMA warps, 16 weight rows each
 constexpr int GEMM_THREADS = (GEMM_CONSUMERS + 1) * 32;
 constexpr int GEMM_STAGE_W = GEMM_BN * 128;   // bytes of the weight tile per stage
 
-// Per weight format: k per stage, activation bytes per stage, ring depth.
-//   F32 : 32 k  (one 128-byte weight row), X [16][32] fp32
-//   BF16: 64 k  (one 128-byte weight row), X [16][64] bf16
-//   INT4: 256 k (one 128-byte packed row = 4 scale groups), X 4 x [16][64] bf16,
-//         scales [4 groups][128 rows] bf16
+// Per weight format: a k-block is one 128-byte row of a weight tile; a
+// pipeline stage holds CHUNK consecutive k-blocks of one tile, so every
+// weight row is fetched CHUNK x 128 contiguous bytes at a time.
+//   F32 : 32 k per k-block,  X [16][32] fp32,             1 k-block per stage, 8 stages
+//   BF16: 64 k per k-block,  X [16][64] bf16,             4 k-blocks per stage, 3 stages
+//   INT4: 256 k per k-block, X 4 x [16][64] bf16, scales [4 groups][128 rows] bf16,
+//         2 k-blocks per stage, 4 stages
 template <int WF> struct GemmCfg;
-template <> struct GemmCfg<0> { static constexpr int KBLK = 32, XB = 2048, SB = 0, STAGES = 8; };
-template <> struct GemmCfg<1> { static constexpr int KBLK = 64, XB = 2048, SB = 0, STAGES = 8; };
-template <> struct GemmCfg<2> { static constexpr int KBLK = 256, XB = 8192, SB = 1024, STAGES = 6; };
+template <> struct GemmCfg<0> {
+    static constexpr int KBLK = 32, XB = 2048, SB = 0, CHUNK = 1, STAGES = 8;
+};
+template <> struct GemmCfg<1> {
+    static constexpr int KBLK = 64, XB = 2048, SB = 0, CHUNK = 4, STAGES = 3;
+};
+template <> struct GemmCfg<2> {
+    static constexpr int KBLK = 256, XB = 8192, SB = 1024, CHUNK = 2, STAGES = 4;
+};
 
 struct GemmArgs {
     int N;              // output width (SWIGLU: ffn)
