@@ -44,6 +44,10 @@ struct DevState {
 #include <utility>
 
 namespace dfl {
+// Rows a kernel writes: the forward's rows, or the rows committed to the
+// draft context (both at absolute position fwd_pos0 + row).
+enum RowSel : int { ROWS_FWD = 0, ROWS_COMMIT = 1 };
+
 // Kernels launched through the library by this process (host counter).
 extern long long g_launches;
 // Programmatic dependent launch on (default) or off (environment DFLASH_PDL=0).
@@ -76,6 +80,18 @@ __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+namespace dfl {
+// Row range [*r0, *r0 + n) a kernel with row selection `sel` works on.
+__device__ __forceinline__ int rows_of(const DevState* st, int sel, int* r0) {
+    if (sel == ROWS_COMMIT) {
+        *r0 = st->fwd_commit_r0;
+        return st->fwd_commit;
+    }
+    *r0 = 0;
+    return st->fwd_T;
+}
+}  // namespace dfl
 
 __device__ __forceinline__ void set_error(DevState* st, int code, int info) {
     if (atomicCAS(&st->err, 0, code) == 0) st->err_info = info;

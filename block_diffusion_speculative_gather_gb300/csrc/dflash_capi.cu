@@ -63,13 +63,16 @@ int max_chunks(const dflash_config& c) { return cache_cap(c) / ATTN_CHUNK; }
 // ------------------------------------------------------------------ layout
 
 struct Layout {
-    size_t state, x, hn, qkv, qrot, attn, act, taps, cbuf, kvc, rcos, rsin, amax, part, slots,
-        counters, total;
+    size_t state, x, hn, ssq, qrot, attn, act, taps, rcos, rsin, amax, part, slots, counters,
+        total;
 };
 
 constexpr int MAX_SMS = 256;
 constexpr int MAX_TILES = 8192;
 
+// Workspace carving.  hn holds the next GEMM's normalised input rows
+// (x * w_norm, activation type) and ssq their per-128-column partial sums
+// of x^2, from which the consuming GEMM derives the RMSNorm row scale.
 Layout make_layout(const dflash_config& c) {
     Layout L{};
     size_t off = 0;
@@ -80,17 +83,15 @@ Layout make_layout(const dflash_config& c) {
     };
     const size_t R = DFL_MAX_ROWS;
     const int es = elem_size(c.dtype);
-    const int qd = c.n_q * c.head_dim, kvd = c.n_kv * c.head_dim;
+    const int qd = c.n_q * c.head_dim;
     L.state = take(sizeof(DevState));
     L.x = take(R * c.hidden * 4);
     L.hn = take(R * c.hidden * es);
-    L.qkv = take(R * (qd + 2 * kvd) * 4);
+    L.ssq = take(R * (c.hidden / 128 + 1) * 4);
     L.qrot = take(R * qd * es);
     L.attn = take(R * qd * es);
     L.act = take(R * c.ffn * es);
     L.taps = take(R * (size_t)(c.n_taps > 0 ? c.n_taps : 1) * c.hidden * es);
-    L.cbuf = take(R * c.hidden * 4);
-    L.kvc = take(R * 2 * kvd * 4);
     L.rcos = take(R * (c.head_dim / 2) * 4);
     L.rsin = take(R * (c.head_dim / 2) * 4);
     L.amax = take(R * 8);
@@ -105,7 +106,7 @@ Layout make_layout(const dflash_config& c) {
 
 int validate(const dflash_config* c) {
     if (!c) return fail(DFLASH_ERR_ARG, "config is NULL");
-    if (c->hidden <= 0 || c->hidden % 64) return fail(DFLASH_ERR_CONFIG, "hidden %d: must be a positive multiple of 64", c->hidden);
+    if (c->hidden <= 0 || c->hidden % 128) return fail(DFLASH_ERR_CONFIG, "hidden %d: must be a positive multiple of 128", c->hidden);
     if (c->head_dim != 64 && c->head_dim != 128) return fail(DFLASH_ERR_CONFIG, "head_dim %d: 64 or 128", c->head_dim);
     if (c->n_q <= 0 || c->n_kv <= 0 || c->n_q % c->n_kv) return fail(DFLASH_ERR_CONFIG, "n_q %d / n_kv %d: n_q must be a multiple of n_kv", c->n_q, c->n_kv);
     if ((c->n_q / c->n_kv) * DFL_MAX_ROWS > 256) return fail(DFLASH_ERR_CONFIG, "query group too large");
@@ -287,8 +288,10 @@ int plan_gemm(dflash_ctx* c, GemmPlan* p, int wfmt, int epi, const void* const* 
     p->wbytes = (double)N * K * wes + (wfmt == WF_INT4 ? (double)N * (K / 64) * 2 : 0.0);
     double outb = 0;
     if (epi == EPI_STORE) outb = (double)DFL_MAX_ROWS * N * 4;
-    else if (epi == EPI_RESID) outb = 2.0 * DFL_MAX_ROWS * N * 4;
+    else if (epi == EPI_RESID) outb = (double)DFL_MAX_ROWS * N * (8 + xes);
+    else if (epi == EPI_NORMOUT) outb = (double)DFL_MAX_ROWS * N * xes;
     else if (epi == EPI_SWIGLU) outb = (double)DFL_MAX_ROWS * a.N * xes;
+    else if (epi == EPI_QKV) outb = (double)DFL_MAX_ROWS * N * xes;
     else outb = DFL_MAX_ROWS * 8.0;
     p->abytes = p->wbytes + (double)DFL_MAX_ROWS * K * xes + outb;
     return DFLASH_OK;
@@ -330,7 +333,7 @@ int build_layer_plans(dflash_ctx* c, const dflash_layer& lw, int wfmt, bool draf
     const void* wqkv[3] = {lw.wq, lw.wk, lw.wv};
     const void* sqkv[3] = {lw.sq, lw.sk, lw.sv};
     const int rqkv[3] = {qd, kvd, kvd};
-    int r = plan_gemm(c, &lp->qkv, wf, EPI_STORE, wqkv, rqkv, 3, H, hn, xt, sqkv);
+    int r = plan_gemm(c, &lp->qkv, wf, EPI_QKV, wqkv, rqkv, 3, H, hn, xt, sqkv);
     if (r) return r;
     const void* wo[1] = {lw.wo};
     const void* so[1] = {lw.so};
@@ -347,57 +350,79 @@ int build_layer_plans(dflash_ctx* c, const dflash_layer& lw, int wfmt, bool draf
         const void* wkv[2] = {lw.wk, lw.wv};
         const void* skv[2] = {lw.sk, lw.sv};
         const int rkv[2] = {kvd, kvd};
-        if ((r = plan_gemm(c, &lp->ctxkv, wf, EPI_STORE, wkv, rkv, 2, H, hn, xt, skv))) return r;
+        if ((r = plan_gemm(c, &lp->ctxkv, wf, EPI_QKV, wkv, rkv, 2, H, hn, xt, skv))) return r;
     }
     return DFLASH_OK;
 }
 
 // ------------------------------------------------------------------ forward pieces
 
+// Folded-RMSNorm input of a GEMM: the partial sums written by the producer.
+void set_norm_in(const dflash_ctx* c, GemmArgs& a, bool on) {
+    a.ssq_in = on ? c->buf<float>(c->L.ssq) : nullptr;
+    a.ssq_parts = c->cfg.hidden / GEMM_BN;
+    a.inv_width = 1.0f / (float)c->cfg.hidden;
+    a.eps = c->cfg.rms_eps;
+}
+
+// Normalised-input output of a GEMM for the next folded RMSNorm.
+void set_norm_out(const dflash_ctx* c, GemmArgs& a, const float* w_next, bool with_ssq) {
+    a.xn_out = c->ws + c->L.hn;
+    a.xn_type = c->act_xt();
+    a.w_next = w_next;
+    a.ssq_out = with_ssq ? c->buf<float>(c->L.ssq) : nullptr;
+}
+
+QkvEpi qkv_epi(const dflash_ctx* c, const dflash_layer& lw, bool target, int layer, int n_q,
+               int row_sel) {
+    const dflash_config& g = c->cfg;
+    QkvEpi q{};
+    q.n_q = n_q;
+    q.n_kv = g.n_kv;
+    q.hd = g.head_dim;
+    q.q_norm = lw.q_norm;
+    q.k_norm = lw.k_norm;
+    q.rope_cos = c->buf<float>(c->L.rcos);
+    q.rope_sin = c->buf<float>(c->L.rsin);
+    q.q_out = c->ws + c->L.qrot;
+    q.q_type = c->act_xt();
+    uint8_t* cache = reinterpret_cast<uint8_t*>(target ? c->kv_t : c->kv_d) +
+                     (size_t)layer * c->cache_layer_stride() * elem_size(g.dtype);
+    q.k_cache = cache;
+    q.v_cache = cache + c->cache_kv_offset() * elem_size(g.dtype);
+    q.c_type = c->act_xt();
+    q.cap = cache_cap(g);
+    q.max_seq = g.max_seq;
+    q.row_sel = row_sel;
+    return q;
+}
+
+// One model's decoder layers over the forward's rows.  Per layer: q/k/v
+// GEMM (folded input norm, head norms, RoPE, K/V into the cache), attention,
+// o GEMM (+ residual, next folded norm), gate/up GEMM (+ SwiGLU), down GEMM
+// (+ residual, next folded norm, tap copy).
 int run_layers(dflash_ctx* c, bool target, cudaStream_t s) {
     const dflash_config& g = c->cfg;
-    const int H = g.hidden, qd = g.n_q * g.head_dim, kvd = g.n_kv * g.head_dim;
+    const int H = g.hidden;
     const int xt = c->act_xt();
     const int nl = target ? g.tgt_layers : g.drf_layers;
     DevState* st = c->st();
     float* x = c->buf<float>(c->L.x);
+    const float* final_norm = target ? c->w.final_norm_tgt : c->w.final_norm_drf;
     for (int l = 0; l < nl; ++l) {
         const dflash_layer& lw = target ? c->tgt[l] : c->drf[l];
         const LayerPlans& lp = target ? c->tplan[l] : c->dplan[l];
-        LAUNCH_TRY(launch_rmsnorm(x, lw.ln_attn, c->ws + c->L.hn, xt, H, g.rms_eps, ROWS_FWD, 1, st, s));
         GemmArgs a = lp.qkv.args;
-        a.out = c->buf<float>(c->L.qkv);
-        a.ldo = qd + 2 * kvd;
+        set_norm_in(c, a, true);
+        a.qkv = qkv_epi(c, lw, target, l, g.n_q, ROWS_FWD);
         int r = run_gemm(c, lp.qkv, a, s);
         if (r) return r;
+        AttnArgs at{};
         uint8_t* cache = reinterpret_cast<uint8_t*>(target ? c->kv_t : c->kv_d) +
                          (size_t)l * c->cache_layer_stride() * elem_size(g.dtype);
-        const size_t vofs = c->cache_kv_offset() * elem_size(g.dtype);
-        QkvArgs q{};
-        q.in = c->buf<float>(c->L.qkv);
-        q.ld_in = qd + 2 * kvd;
-        q.n_q = g.n_q;
-        q.n_kv = g.n_kv;
-        q.head_dim = g.head_dim;
-        q.q_norm = lw.q_norm;
-        q.k_norm = lw.k_norm;
-        q.eps = g.rms_eps;
-        q.q_out = c->ws + c->L.qrot;
-        q.q_type = xt;
-        q.k_cache = cache;
-        q.v_cache = cache + vofs;
-        q.c_type = xt;
-        q.max_seq = g.max_seq;
-        q.cap = cache_cap(g);
-        q.row_sel = ROWS_FWD;
-        q.rope_cos = c->buf<float>(c->L.rcos);
-        q.rope_sin = c->buf<float>(c->L.rsin);
-        q.st = st;
-        LAUNCH_TRY(launch_qk_norm_rope(q, s));
-        AttnArgs at{};
         at.q = c->ws + c->L.qrot;
         at.k_cache = cache;
-        at.v_cache = cache + vofs;
+        at.v_cache = cache + c->cache_kv_offset() * elem_size(g.dtype);
         at.kv_type = xt;
         at.n_q = g.n_q;
         at.n_kv = g.n_kv;
@@ -432,22 +457,25 @@ int run_layers(dflash_ctx* c, bool target, cudaStream_t s) {
         a = lp.o.args;
         a.out = x;
         a.ldo = H;
+        set_norm_out(c, a, lw.ln_mlp, true);
         if ((r = run_gemm(c, lp.o, a, s))) return r;
-        LAUNCH_TRY(launch_rmsnorm(x, lw.ln_mlp, c->ws + c->L.hn, xt, H, g.rms_eps, ROWS_FWD, 1, st, s));
         a = lp.gateup.args;
-        a.out2 = c->ws + c->L.act;
-        a.ld2 = g.ffn;
-        a.x2t = xt;
+        set_norm_in(c, a, true);
+        a.act = c->ws + c->L.act;
+        a.ld_act = g.ffn;
+        a.act_type = xt;
         if ((r = run_gemm(c, lp.gateup, a, s))) return r;
         a = lp.down.args;
         a.out = x;
         a.ldo = H;
+        const float* w_next = l + 1 < nl ? (target ? c->tgt[l + 1] : c->drf[l + 1]).ln_attn : final_norm;
+        set_norm_out(c, a, w_next, true);
         if (target && g.drf_layers > 0) {
             for (int i = 0; i < g.n_taps; ++i)
                 if (g.tap_layer[i] == l) {
-                    a.out2 = c->ws + c->L.taps + (size_t)i * H * elem_size(g.dtype);
-                    a.ld2 = g.n_taps * H;
-                    a.x2t = xt;
+                    a.tap_out = c->ws + c->L.taps + (size_t)i * H * elem_size(g.dtype);
+                    a.ld_tap = g.n_taps * H;
+                    a.tap_type = xt;
                 }
         }
         if ((r = run_gemm(c, lp.down, a, s))) return r;
@@ -455,56 +483,31 @@ int run_layers(dflash_ctx* c, bool target, cudaStream_t s) {
     return DFLASH_OK;
 }
 
-int run_lm_head(dflash_ctx* c, const float* final_norm, float* logits, cudaStream_t s) {
-    const dflash_config& g = c->cfg;
-    LAUNCH_TRY(launch_rmsnorm(c->buf<float>(c->L.x), final_norm, c->ws + c->L.hn, c->act_xt(),
-                              g.hidden, g.rms_eps, ROWS_FWD, 1, c->st(), s));
+// LM head over the final-norm input the last down projection wrote.
+int run_lm_head(dflash_ctx* c, float* logits, cudaStream_t s) {
     GemmArgs a = c->lm.args;
+    set_norm_in(c, a, true);
     a.amax = c->buf<unsigned long long>(c->L.amax);
     a.logits = logits;
-    a.ldl = g.vocab;
+    a.ldl = c->cfg.vocab;
     return run_gemm(c, c->lm, a, s);
 }
 
-// fc -> ctx norm -> per draft layer k/v projection -> k-norm + RoPE -> draft cache,
-// for the rows the device state marks as committed.
+// fc -> context norm -> per draft layer k/v projection with k-norm and
+// RoPE into the draft cache, for the rows the device state marks committed.
 int run_ingest(dflash_ctx* c, cudaStream_t s) {
     const dflash_config& g = c->cfg;
-    const int H = g.hidden, kvd = g.n_kv * g.head_dim;
-    DevState* st = c->st();
     GemmArgs a = c->fc.args;
-    a.out = c->buf<float>(c->L.cbuf);
-    a.ldo = H;
+    a.ldo = g.hidden;
+    set_norm_out(c, a, g.ctx_norm ? c->w.ctx_norm : nullptr, g.ctx_norm != 0);
     int r = run_gemm(c, c->fc, a, s);
     if (r) return r;
-    LAUNCH_TRY(launch_rmsnorm(c->buf<float>(c->L.cbuf), c->w.ctx_norm, c->ws + c->L.hn, c->act_xt(),
-                              H, g.rms_eps, ROWS_COMMIT, g.ctx_norm ? 1 : 0, st, s));
     for (int l = 0; l < g.drf_layers; ++l) {
         const LayerPlans& lp = c->dplan[l];
         a = lp.ctxkv.args;
-        a.out = c->buf<float>(c->L.kvc);
-        a.ldo = 2 * kvd;
+        set_norm_in(c, a, g.ctx_norm != 0);
+        a.qkv = qkv_epi(c, c->drf[l], false, l, 0, ROWS_COMMIT);
         if ((r = run_gemm(c, lp.ctxkv, a, s))) return r;
-        uint8_t* cache = reinterpret_cast<uint8_t*>(c->kv_d) +
-                         (size_t)l * c->cache_layer_stride() * elem_size(g.dtype);
-        QkvArgs q{};
-        q.in = c->buf<float>(c->L.kvc);
-        q.ld_in = 2 * kvd;
-        q.n_q = 0;
-        q.n_kv = g.n_kv;
-        q.head_dim = g.head_dim;
-        q.k_norm = c->drf[l].k_norm;
-        q.eps = g.rms_eps;
-        q.k_cache = cache;
-        q.v_cache = cache + c->cache_kv_offset() * elem_size(g.dtype);
-        q.c_type = c->act_xt();
-        q.max_seq = g.max_seq;
-        q.cap = cache_cap(g);
-        q.row_sel = ROWS_COMMIT;
-        q.rope_cos = c->buf<float>(c->L.rcos);
-        q.rope_sin = c->buf<float>(c->L.rsin);
-        q.st = st;
-        LAUNCH_TRY(launch_qk_norm_rope(q, s));
     }
     return DFLASH_OK;
 }
@@ -534,6 +537,13 @@ RowsArgs rows_args(dflash_ctx* c, int mode) {
     a.head_dim = g.head_dim;
     a.rope_theta = g.rope_theta;
     a.amax = c->buf<unsigned long long>(c->L.amax);
+    const bool draft = mode == FWD_DRAFT;
+    a.w0 = draft ? (g.drf_layers ? c->drf[0].ln_attn : nullptr)
+                 : (g.tgt_layers ? c->tgt[0].ln_attn : nullptr);
+    if (!a.w0) a.embed = nullptr;   // no model runs (drafter-alone tap staging)
+    a.xn = c->ws + c->L.hn;
+    a.xn_type = c->act_xt();
+    a.ssq = c->buf<float>(c->L.ssq);
     a.st = c->st();
     return a;
 }
@@ -624,7 +634,7 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
     if (!r && g.drf_layers > 0) {
         const void* wfc[1] = {w->fc};
         const int rfc[1] = {g.hidden};
-        r = plan_gemm(c, &c->fc, c->wf(g.dtype), EPI_STORE, wfc, rfc, 1, g.n_taps * g.hidden,
+        r = plan_gemm(c, &c->fc, c->wf(g.dtype), EPI_NORMOUT, wfc, rfc, 1, g.n_taps * g.hidden,
                       c->ws + L.taps, c->act_xt());
     }
     if (!r && g.dtype == DFLASH_BF16) {
@@ -722,7 +732,7 @@ int dflash_prefill_taps(dflash_ctx* c, const int32_t* prompt_ids, int32_t n_prom
             LAUNCH_TRY(launch_set_chunk(c->st(), p0, T, commit_lo, s));
             if ((r = run_layers(c, true, s))) return r;
             if (p0 + T == n_prompt) {
-                if ((r = run_lm_head(c, c->w.final_norm_tgt, c->verify_logits, s))) return r;
+                if ((r = run_lm_head(c, c->verify_logits, s))) return r;
                 AcceptArgs aa{};
                 aa.mode = FWD_PREFILL;
                 aa.amax = c->buf<unsigned long long>(c->L.amax);
@@ -799,7 +809,7 @@ int dflash_draft_block(dflash_ctx* c, int32_t* draft_ids, dflash_stream_t stream
     LAUNCH_TRY(launch_prepare_rows(rows_args(c, FWD_DRAFT), s));
     int r = run_layers(c, false, s);
     if (r) return r;
-    if ((r = run_lm_head(c, c->w.final_norm_drf, c->draft_logits, s))) return r;
+    if ((r = run_lm_head(c, c->draft_logits, s))) return r;
     AcceptArgs aa{};
     aa.mode = FWD_DRAFT;
     aa.amax = c->buf<unsigned long long>(c->L.amax);
@@ -825,7 +835,7 @@ int dflash_verify_accept(dflash_ctx* c, const int32_t* draft_ids, int32_t* token
     LAUNCH_TRY(launch_prepare_rows(ra, s));
     int r = run_layers(c, true, s);
     if (r) return r;
-    if ((r = run_lm_head(c, c->w.final_norm_tgt, c->verify_logits, s))) return r;
+    if ((r = run_lm_head(c, c->verify_logits, s))) return r;
     AcceptArgs aa{};
     aa.mode = mode;
     aa.amax = c->buf<unsigned long long>(c->L.amax);

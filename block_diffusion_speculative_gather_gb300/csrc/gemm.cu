@@ -223,6 +223,7 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     }
 
     // ---------------------------------------------------- consumers
+    __shared__ float s_rstd[DFL_MAX_ROWS];
     pdl_wait();    // the epilogues read and write buffers of earlier kernels
     const int tid = threadIdx.x;   // 0..255
     const int g = lane >> 2, c = lane & 3;
@@ -448,27 +449,108 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             }
         }
 
+        // Row scale of a folded RMSNorm: rstd[t] from the partial sums, summed
+        // in a fixed order (the same for every forward length).  Computed by
+        // all consumer threads, before the (barrier-free) epilogue.
+        if (EPI == EPI_SWIGLU || EPI == EPI_ARGMAX || EPI == EPI_QKV) {
+            if (tid < DFL_MAX_ROWS) {
+                float r = 1.f;
+                if (a.ssq_in) {
+                    float ss = 0.f;
+                    for (int p = 0; p < a.ssq_parts; ++p) ss += a.ssq_in[p * DFL_MAX_ROWS + tid];
+                    r = 1.0f / sqrtf(ss * a.inv_width + a.eps);
+                }
+                s_rstd[tid] = r;
+            }
+            consumer_bar();
+        }
         if (do_epi) {
-            if (EPI == EPI_STORE || EPI == EPI_RESID) {
+            if (EPI == EPI_STORE) {
                 const int n0 = tile * GEMM_BN;
                 for (int e = tid; e < GEMM_BN * DFL_MAX_ROWS; e += GEMM_CONSUMERS * 32) {
                     const int t = e / GEMM_BN, r = e % GEMM_BN;
-                    const size_t o = (size_t)t * a.ldo + n0 + r;
-                    if (EPI == EPI_STORE) {
-                        a.out[o] = ctile[e];
-                    } else {
-                        const float v = a.out[o] + ctile[e];
-                        a.out[o] = v;
-                        if (a.out2) store_xt(a.out2, a.x2t, (size_t)t * a.ld2 + n0 + r, v);
+                    a.out[(size_t)t * a.ldo + n0 + r] = ctile[e];
+                }
+            } else if (EPI == EPI_RESID || EPI == EPI_NORMOUT) {
+                // warp w: tokens 2w, 2w+1; lane: 4 consecutive columns
+                const int n0 = tile * GEMM_BN;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int t = warp * 2 + q;
+                    float ss = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = lane * 4 + i;
+                        float v = ctile[t * GEMM_BN + r];
+                        if (EPI == EPI_RESID) {
+                            const size_t o = (size_t)t * a.ldo + n0 + r;
+                            v += a.out[o];
+                            a.out[o] = v;
+                            if (a.tap_out) store_xt(a.tap_out, a.tap_type, (size_t)t * a.ld_tap + n0 + r, v);
+                        }
+                        ss = fmaf(v, v, ss);
+                        const float wn = a.w_next ? a.w_next[n0 + r] : 1.f;
+                        store_xt(a.xn_out, a.xn_type, (size_t)t * a.ldo + n0 + r, v * wn);
                     }
+                    ss = warp_sum(ss);
+                    if (a.ssq_out && lane == 0) a.ssq_out[tile * DFL_MAX_ROWS + t] = ss;
                 }
             } else if (EPI == EPI_SWIGLU) {
                 const int j0 = tile * 64;
                 for (int e = tid; e < 64 * DFL_MAX_ROWS; e += GEMM_CONSUMERS * 32) {
                     const int t = e / 64, r = e % 64;
-                    const float gt = ctile[t * GEMM_BN + r], up = ctile[t * GEMM_BN + 64 + r];
+                    const float gt = ctile[t * GEMM_BN + r] * s_rstd[t];
+                    const float up = ctile[t * GEMM_BN + 64 + r] * s_rstd[t];
                     const float v = gt / (1.f + expf(-gt)) * up;
-                    store_xt(a.out2, a.x2t, (size_t)t * a.ld2 + j0 + r, v);
+                    store_xt(a.act, a.act_type, (size_t)t * a.ld_act + j0 + r, v);
+                }
+            } else if (EPI == EPI_QKV) {
+                // the tile is 128 / hd whole heads; item = (token, head in tile)
+                const QkvEpi& qe = a.qkv;
+                int r0;
+                const int nrows = rows_of(a.st, qe.row_sel, &r0);
+                const int hd = qe.hd, hpt = GEMM_BN / hd, per = hd / 32;
+                const int h_first = tile * hpt;
+                for (int item = warp; item < DFL_MAX_ROWS * hpt; item += GEMM_CONSUMERS) {
+                    const int t = item / hpt, hi = item % hpt;
+                    if (t < r0 || t >= r0 + nrows) continue;
+                    const int h = h_first + hi;
+                    const bool is_q = h < qe.n_q, is_k = !is_q && h < qe.n_q + qe.n_kv;
+                    float v[4];
+                    for (int m = 0; m < per; ++m)
+                        v[m] = ctile[t * GEMM_BN + hi * hd + lane + 32 * m] * s_rstd[t];
+                    if (is_q || is_k) {
+                        const float* nw = is_q ? qe.q_norm : qe.k_norm;
+                        float ss = 0.f;
+                        for (int m = 0; m < per; ++m) ss = fmaf(v[m], v[m], ss);
+                        ss = warp_sum(ss);
+                        const float inv = 1.0f / sqrtf(ss / (float)hd + a.eps);
+                        for (int m = 0; m < per; ++m) v[m] = v[m] * inv * nw[lane + 32 * m];
+                        // rotate-half: element i pairs with i + hd/2 (same lane, m + per/2)
+                        const float* cs = qe.rope_cos + t * (hd / 2);
+                        const float* sn = qe.rope_sin + t * (hd / 2);
+                        float rr[4];
+                        for (int m = 0; m < per / 2; ++m) {
+                            const int i = lane + 32 * m;
+                            rr[m] = v[m] * cs[i] - v[m + per / 2] * sn[i];
+                            rr[m + per / 2] = v[m + per / 2] * cs[i] + v[m] * sn[i];
+                        }
+                        for (int m = 0; m < per; ++m) v[m] = rr[m];
+                    }
+                    if (is_q) {
+                        const size_t base = ((size_t)h * DFL_MAX_ROWS + t) * hd;   // [n_q][16][hd]
+                        for (int m = 0; m < per; ++m) store_xt(qe.q_out, qe.q_type, base + lane + 32 * m, v[m]);
+                        continue;
+                    }
+                    const int pos = a.st->fwd_pos0 + t;
+                    if (pos < 0 || pos >= qe.max_seq) {
+                        if (lane == 0) set_error(a.st, DERR_INDEX, pos);
+                        continue;
+                    }
+                    const int kh = is_k ? h - qe.n_q : h - qe.n_q - qe.n_kv;
+                    void* cache = is_k ? qe.k_cache : qe.v_cache;
+                    const size_t base = ((size_t)kh * qe.cap + pos) * hd;
+                    for (int m = 0; m < per; ++m) store_xt(cache, qe.c_type, base + lane + 32 * m, v[m]);
                 }
             } else {  // EPI_ARGMAX: warp w reduces tokens 2w, 2w+1
                 const int n0 = tile * GEMM_BN;
@@ -479,7 +561,7 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int r = lane * 4 + i;
-                        const float v = ctile[t * GEMM_BN + r];
+                        const float v = ctile[t * GEMM_BN + r] * s_rstd[t];
                         best = umax64(best, argmax_key(v, n0 + r));
                         if (a.logits) a.logits[(size_t)t * a.ldl + n0 + r] = v;
                     }
@@ -523,13 +605,15 @@ int launch_gemm(int wfmt, int epi, int xt, const GemmMaps& maps, const GemmArgs&
             case EPI_RESID: return launch_one<WF_BF16, EPI_RESID>(maps, args, grid, stream);
             case EPI_SWIGLU: return launch_one<WF_BF16, EPI_SWIGLU>(maps, args, grid, stream);
             case EPI_ARGMAX: return launch_one<WF_BF16, EPI_ARGMAX>(maps, args, grid, stream);
+            case EPI_QKV: return launch_one<WF_BF16, EPI_QKV>(maps, args, grid, stream);
+            case EPI_NORMOUT: return launch_one<WF_BF16, EPI_NORMOUT>(maps, args, grid, stream);
         }
     } else if (wfmt == WF_INT4) {
         switch (epi) {
             case EPI_STORE: return launch_one<WF_INT4, EPI_STORE>(maps, args, grid, stream);
             case EPI_RESID: return launch_one<WF_INT4, EPI_RESID>(maps, args, grid, stream);
             case EPI_SWIGLU: return launch_one<WF_INT4, EPI_SWIGLU>(maps, args, grid, stream);
-            case EPI_ARGMAX: return launch_one<WF_INT4, EPI_ARGMAX>(maps, args, grid, stream);
+            case EPI_QKV: return launch_one<WF_INT4, EPI_QKV>(maps, args, grid, stream);
         }
     } else if (wfmt == WF_F32) {
         switch (epi) {
@@ -537,6 +621,8 @@ int launch_gemm(int wfmt, int epi, int xt, const GemmMaps& maps, const GemmArgs&
             case EPI_RESID: return launch_one<WF_F32, EPI_RESID>(maps, args, grid, stream);
             case EPI_SWIGLU: return launch_one<WF_F32, EPI_SWIGLU>(maps, args, grid, stream);
             case EPI_ARGMAX: return launch_one<WF_F32, EPI_ARGMAX>(maps, args, grid, stream);
+            case EPI_QKV: return launch_one<WF_F32, EPI_QKV>(maps, args, grid, stream);
+            case EPI_NORMOUT: return launch_one<WF_F32, EPI_NORMOUT>(maps, args, grid, stream);
         }
     }
     return (int)cudaErrorInvalidValue;

@@ -8,7 +8,19 @@
 namespace dfl {
 
 enum WFmt : int { WF_F32 = 0, WF_BF16 = 1, WF_INT4 = 2 };
-enum Epi : int { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_ARGMAX = 3 };
+// Epilogues.  The RMSNorm that precedes a projection is folded into the
+// GEMMs around it: the producer of a normalised input (RESID, NORMOUT, the
+// row-preparation kernel) writes x * w_norm rounded to the GEMM input type
+// plus per-128-column partial sums of x^2; the consumer (QKV, SWIGLU,
+// ARGMAX) scales its rows by rstd = 1 / sqrt(sum / width + eps).
+enum Epi : int {
+    EPI_STORE = 0,    // fp32 store
+    EPI_RESID = 1,    // x += Y; next normalised input (+ partial sums) and tap copy
+    EPI_SWIGLU = 2,   // silu(rstd * gate) * (rstd * up) of paired tiles
+    EPI_ARGMAX = 3,   // LM head: rstd-scaled logits, packed argmax (+ optional dump)
+    EPI_QKV = 4,      // rstd, per-head q/k RMSNorm, RoPE, q out and K/V into the cache
+    EPI_NORMOUT = 5,  // Y * w_norm as the next normalised input (+ partial sums)
+};
 enum XType : int { XT_F32 = 0, XT_BF16 = 1, XT_F16 = 2 };
 
 constexpr int GEMM_BN = 128;        // output rows (weight rows) per tile
@@ -34,6 +46,22 @@ template <> struct GemmCfg<2> {
     static constexpr int KBLK = 256, XB = 8192, SB = 1024, CHUNK = 2, STAGES = 4;
 };
 
+// Per-head epilogue of the q/k/v projection (EPI_QKV).
+struct QkvEpi {
+    int n_q, n_kv, hd;          // heads in the tile order q.., k.., v..
+    const float* q_norm;        // [hd] (unused when n_q == 0)
+    const float* k_norm;        // [hd]
+    const float* rope_cos;      // [16][hd/2] angles of the forward's rows
+    const float* rope_sin;
+    void* q_out;                // [n_q][16][hd], q_type
+    int q_type;
+    void* k_cache;              // layer base [n_kv][cap][hd], c_type
+    void* v_cache;
+    int c_type;
+    int cap, max_seq;
+    int row_sel;                // rows written: ROWS_FWD (the forward's) or ROWS_COMMIT
+};
+
 struct GemmArgs {
     int N;              // output width (SWIGLU: ffn)
     int K;              // reduction length
@@ -41,15 +69,33 @@ struct GemmArgs {
     int kb;             // k-blocks per tile
     int seg_rows[3];    // rows of weight maps 0..2 (concatenated along N)
     int n_seg;
-    // epilogue
-    float* out;         // STORE: fp32 [16][ldo]; RESID: residual x fp32 [16][ldo]
+    // input row scale of a folded RMSNorm (QKV, SWIGLU, ARGMAX): NULL = 1
+    const float* ssq_in;    // [ssq_parts][16] partial sums of x^2
+    int ssq_parts;
+    float inv_width;        // 1 / normalised width
+    float eps;
+    // STORE: fp32 [16][ldo];  RESID: the fp32 residual x [16][ldo]
+    float* out;
     int ldo;
-    void* out2;         // SWIGLU: activation [16][ld2] (XType x2t); RESID: optional tap copy
-    int ld2;
-    int x2t;            // element type of out2
-    unsigned long long* amax;  // ARGMAX: packed keys [16]
-    float* logits;      // ARGMAX: optional fp32 dump [16][ldl]
+    // RESID / NORMOUT: next normalised input (x or Y) * w_next as xn_type
+    void* xn_out;
+    const float* w_next;    // NULL = ones
+    float* ssq_out;         // [n_tiles][16], or NULL
+    int xn_type;
+    // RESID: optional raw copy of the new x (target taps)
+    void* tap_out;
+    int ld_tap;
+    int tap_type;
+    // SWIGLU: activation [16][ld_act]
+    void* act;
+    int ld_act;
+    int act_type;
+    // ARGMAX
+    unsigned long long* amax;  // packed keys [16]
+    float* logits;             // optional fp32 dump [16][ldl]
     int ldl;
+    // QKV
+    QkvEpi qkv;
     // deterministic split-K across CTAs
     float* slots;       // [grid][2][GEMM_BN * 16]
     int* counters;      // [n_tiles], zero between launches

@@ -31,15 +31,6 @@ __device__ __forceinline__ float ld_any(const void* base, int t, size_t i) {
     return __half2float(reinterpret_cast<const __half*>(base)[i]);
 }
 
-__device__ __forceinline__ int rows_of(const DevState* st, int sel, int* r0) {
-    if (sel == ROWS_COMMIT) {
-        *r0 = st->fwd_commit_r0;
-        return st->fwd_commit;
-    }
-    *r0 = 0;
-    return st->fwd_T;
-}
-
 // --------------------------------------------------------------- prepare rows
 
 // One CTA: sets the forward descriptor (thread 0), then every CTA gathers
@@ -96,6 +87,23 @@ __global__ void prepare_rows_kernel(RowsArgs a) {
     } else if (a.embed) {
         for (int i = threadIdx.x; i < a.hidden; i += blockDim.x) xr[i] = 0.f;
     }
+    if (a.embed) {
+        // folded RMSNorm input of layer 0: xn = x * w0, per-128-column sums of x^2
+        __syncthreads();
+        for (int i = threadIdx.x; i < a.hidden; i += blockDim.x)
+            st_any(a.xn, a.xn_type, (size_t)t * a.hidden + i, xr[i] * a.w0[i]);
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        for (int b = warp; b < a.hidden / 128; b += blockDim.x >> 5) {
+            float ss = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float v = xr[b * 128 + lane * 4 + j];
+                ss = fmaf(v, v, ss);
+            }
+            ss = warp_sum(ss);
+            if (lane == 0) a.ssq[b * DFL_MAX_ROWS + t] = ss;
+        }
+    }
     const int half = a.head_dim / 2;
     for (int i = threadIdx.x; i < half; i += blockDim.x) {
         // angle = pos * theta^(-2i/d), in double, rounded once to fp32
@@ -104,107 +112,6 @@ __global__ void prepare_rows_kernel(RowsArgs a) {
         a.rope_cos[t * half + i] = (float)cos(ang);
         a.rope_sin[t * half + i] = (float)sin(ang);
     }
-}
-
-// --------------------------------------------------------------- RMSNorm
-
-template <typename OT>
-__global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ w,
-                               OT* __restrict__ out, int hidden, float eps, int row_sel,
-                               int apply, const DevState* st) {
-    pdl_trigger();
-    pdl_wait();
-    const int t = blockIdx.x;
-    int r0;
-    const int n = rows_of(st, row_sel, &r0);
-    OT* o = out + (size_t)t * hidden;
-    if (t < r0 || t >= r0 + n) {
-        for (int i = threadIdx.x; i < hidden; i += blockDim.x) o[i] = from_f32<OT>(0.f);
-        return;
-    }
-    const float* xr = x + (size_t)t * hidden;
-    if (!apply) {
-        for (int i = threadIdx.x; i < hidden; i += blockDim.x) o[i] = from_f32<OT>(xr[i]);
-        return;
-    }
-    float ss = 0.f;
-    for (int i = threadIdx.x; i < hidden; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
-    __shared__ float red[32];
-    ss = warp_sum(ss);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-        v = warp_sum(v);
-        if (threadIdx.x == 0) red[0] = v;
-    }
-    __syncthreads();
-    const float inv = 1.0f / sqrtf(red[0] / (float)hidden + eps);
-    for (int i = threadIdx.x; i < hidden; i += blockDim.x) o[i] = from_f32<OT>(xr[i] * inv * w[i]);
-}
-
-// --------------------------------------------------------------- q/k norm + RoPE + KV write
-
-// One warp per (row, head): head-RMSNorm (q, k), rotate-half RoPE, then q to
-// the attention input and k, v to the cache at the row's absolute position.
-template <int HD>
-__global__ void qk_norm_rope_kernel(QkvArgs a) {
-    pdl_trigger();
-    pdl_wait();
-    constexpr int PER = HD / 32;   // elements per lane; lane holds i = lane + 32 m
-    const int warps = blockDim.x >> 5;
-    const int gw = blockIdx.x * warps + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    const int heads = a.n_q + 2 * a.n_kv;
-    const int t = gw / heads, h = gw % heads;
-    if (t >= DFL_MAX_ROWS) return;
-    int r0;
-    const int n = rows_of(a.st, a.row_sel, &r0);
-    if (t < r0 || t >= r0 + n) return;
-    const int pos = a.st->fwd_pos0 + t;
-    const float* src = a.in + (size_t)t * a.ld_in + (size_t)h * HD;
-    float v[PER];
-#pragma unroll
-    for (int m = 0; m < PER; ++m) v[m] = src[lane + 32 * m];
-    const bool is_q = h < a.n_q, is_k = !is_q && h < a.n_q + a.n_kv;
-    if (is_q || is_k) {
-        const float* nw = is_q ? a.q_norm : a.k_norm;
-        float ss = 0.f;
-#pragma unroll
-        for (int m = 0; m < PER; ++m) ss = fmaf(v[m], v[m], ss);
-        ss = warp_sum(ss);
-        const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
-#pragma unroll
-        for (int m = 0; m < PER; ++m) v[m] = v[m] * inv * nw[lane + 32 * m];
-        // rotate-half: element i pairs with i + HD/2 (same lane, m + PER/2)
-        const float* cs = a.rope_cos + t * (HD / 2);
-        const float* sn = a.rope_sin + t * (HD / 2);
-        float r[PER];
-#pragma unroll
-        for (int m = 0; m < PER / 2; ++m) {
-            const int i = lane + 32 * m;
-            const float c = cs[i], s = sn[i];
-            r[m] = v[m] * c - v[m + PER / 2] * s;
-            r[m + PER / 2] = v[m + PER / 2] * c + v[m] * s;
-        }
-#pragma unroll
-        for (int m = 0; m < PER; ++m) v[m] = r[m];
-    }
-    if (is_q) {
-        const size_t base = ((size_t)h * DFL_MAX_ROWS + t) * HD;   // [n_q][16][HD]
-#pragma unroll
-        for (int m = 0; m < PER; ++m) st_any(a.q_out, a.q_type, base + lane + 32 * m, v[m]);
-        return;
-    }
-    if (pos < 0 || pos >= a.max_seq) {
-        set_error(a.st, DERR_INDEX, pos);
-        return;
-    }
-    const int kh = is_k ? h - a.n_q : h - a.n_q - a.n_kv;
-    void* cache = is_k ? a.k_cache : a.v_cache;
-    const size_t base = ((size_t)kh * a.cap + pos) * HD;
-#pragma unroll
-    for (int m = 0; m < PER; ++m) st_any(cache, a.c_type, base + lane + 32 * m, v[m]);
 }
 
 // --------------------------------------------------------------- attention
@@ -561,30 +468,6 @@ inline int ok(cudaError_t e) { return e == cudaSuccess ? 0 : -1; }
 
 int launch_prepare_rows(const RowsArgs& a, cudaStream_t s) {
     return ok(launch_k(prepare_rows_kernel, dim3(DFL_MAX_ROWS), dim3(256), 0, s, a));
-}
-
-int launch_rmsnorm(const float* x, const float* w, void* out, int out_type, int hidden,
-                   float eps, int row_sel, int apply, const DevState* st, cudaStream_t s) {
-    const dim3 g(DFL_MAX_ROWS), b(256);
-    if (out_type == XT_F32)
-        return ok(launch_k(rmsnorm_kernel<float>, g, b, 0, s, x, w, (float*)out, hidden, eps,
-                           row_sel, apply, st));
-    if (out_type == XT_BF16)
-        return ok(launch_k(rmsnorm_kernel<__nv_bfloat16>, g, b, 0, s, x, w, (__nv_bfloat16*)out,
-                           hidden, eps, row_sel, apply, st));
-    return ok(launch_k(rmsnorm_kernel<__half>, g, b, 0, s, x, w, (__half*)out, hidden, eps,
-                       row_sel, apply, st));
-}
-
-int launch_qk_norm_rope(const QkvArgs& a, cudaStream_t s) {
-    const int heads = a.n_q + 2 * a.n_kv;
-    const int warps = 8;
-    const int blocks = (DFL_MAX_ROWS * heads + warps - 1) / warps;
-    if (a.head_dim == 128)
-        return ok(launch_k(qk_norm_rope_kernel<128>, dim3(blocks), dim3(warps * 32), 0, s, a));
-    if (a.head_dim == 64)
-        return ok(launch_k(qk_norm_rope_kernel<64>, dim3(blocks), dim3(warps * 32), 0, s, a));
-    return -2;
 }
 
 int launch_attention(const AttnArgs& a, cudaStream_t s) {

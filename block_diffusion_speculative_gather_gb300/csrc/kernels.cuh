@@ -6,7 +6,6 @@
 namespace dfl {
 
 enum FwdMode : int { FWD_PREFILL = 0, FWD_DRAFT = 1, FWD_VERIFY = 2, FWD_GREEDY = 3 };
-enum RowSel : int { ROWS_FWD = 0, ROWS_COMMIT = 1 };
 
 constexpr int ATTN_CHUNK = 64;   // keys per attention split (fixed: batch invariance)
 
@@ -23,38 +22,15 @@ struct RowsArgs {
     int head_dim;
     float rope_theta;
     unsigned long long* amax;    // [16] reset to 0
+    // folded input norm of the first layer: xn = x * w0 and partial sums of x^2
+    const float* w0;             // [hidden] ln_attn of layer 0 of the model that runs
+    void* xn;                    // [16][hidden], xn_type
+    int xn_type;
+    float* ssq;                  // [hidden / 128][16]
     DevState* st;
 };
 
 int launch_prepare_rows(const RowsArgs& a, cudaStream_t s);
-
-// out[t] = RMSNorm(x[t]) * w for the selected rows, zeros for the others.
-// apply = 0: plain conversion of the selected rows (no normalisation).
-int launch_rmsnorm(const float* x, const float* w, void* out, int out_type, int hidden,
-                   float eps, int row_sel, int apply, const DevState* st, cudaStream_t s);
-
-struct QkvArgs {
-    const float* in;        // fp32 [16][ld_in]: q heads, then k heads, then v heads
-    int ld_in;
-    int n_q, n_kv, head_dim;
-    const float* q_norm;    // [head_dim] (unused when n_q == 0)
-    const float* k_norm;
-    float eps;
-    void* q_out;            // [n_q][16][head_dim] (head-major), type q_type
-    int q_type;
-    void* k_cache;          // layer base of K: [n_kv][cap][head_dim], type c_type
-    void* v_cache;
-    int c_type;
-    int max_seq;            // positions allowed
-    int cap;                // positions per head run (max_seq rounded up to 64)
-    int row_sel;            // ROWS_FWD: the forward's rows; ROWS_COMMIT: the rows
-                            // committed to the draft context (both at fwd_pos0 + row)
-    const float* rope_cos;  // [16][head_dim/2] angles of the forward's rows
-    const float* rope_sin;
-    DevState* st;
-};
-
-int launch_qk_norm_rope(const QkvArgs& a, cudaStream_t s);
 
 struct AttnArgs {
     const void* q;          // [n_q][16][head_dim]
