@@ -40,8 +40,13 @@ def _stale(obj: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra=(), out: str = None,
+          build_dir: str = None) -> str:
+    """Compiles (changed) sources and links the library; `extra` adds nvcc
+    flags, `out`/`build_dir` place a variant build elsewhere."""
+    lib_path = out or LIB
+    bdir = build_dir or BUILD
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [
@@ -49,7 +54,7 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     objs = []
     jobs = []
     for src in sources:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
             jobs.append([nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj])
@@ -64,13 +69,13 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
                 sys.stderr.write(r.stdout + r.stderr)
             if r.returncode:
                 raise RuntimeError(f"nvcc failed: {' '.join(cmd)}")
-    if jobs or force or _stale(LIB, objs):
-        cmd = [nvcc, *ARCH, "-shared", "-o", LIB, *objs, "-lcudart"]
+    if jobs or force or _stale(lib_path, objs):
+        cmd = [nvcc, *ARCH, "-shared", "-o", lib_path, *objs, "-lcudart"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("link failed")
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":

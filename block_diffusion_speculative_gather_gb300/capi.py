@@ -96,6 +96,8 @@ def _load() -> C.CDLL:
         "dflash_launch_count": (i64, []),
         "dflash_selftest_timeout": (C.c_int, [vp, i64, vp]),
         "dflash_adopt_kv": (C.c_int, [vp, i32, i32, i32, vp]),
+        "dflash_linear_workspace_bytes": (sz, [i32, i32]),
+        "dflash_linear": (C.c_int, [vp, vp, i32, i32, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -111,7 +113,8 @@ EXPORTED = ("dflash_workspace_bytes", "dflash_kv_target_bytes", "dflash_kv_draft
             "dflash_rollback", "dflash_stats", "dflash_check", "dflash_set_logits_out",
             "dflash_destroy", "dflash_last_error", "dflash_tap_reduce",
             "dflash_quantize_int4g64", "dflash_profile", "dflash_launch_count",
-            "dflash_selftest_timeout", "dflash_adopt_kv")
+            "dflash_selftest_timeout", "dflash_adopt_kv", "dflash_linear_workspace_bytes",
+            "dflash_linear")
 
 
 def check(rc: int) -> None:
@@ -215,3 +218,13 @@ def dflash_selftest_timeout(ctx, limit_ns: int, stream=None):
 
 def dflash_adopt_kv(ctx, n: int, pending_token: int, max_new: int, stream=None):
     check(lib.dflash_adopt_kv(ctx, n, pending_token, max_new, _stream(stream)))
+
+
+def dflash_linear_workspace_bytes(n: int, k: int) -> int:
+    return lib.dflash_linear_workspace_bytes(n, k)
+
+
+def dflash_linear(w, x, y, workspace, stream=None):
+    n, k = w.shape
+    check(lib.dflash_linear(_ptr(w), _ptr(x), n, k, _ptr(y), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream)))

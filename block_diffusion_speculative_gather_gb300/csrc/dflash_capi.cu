@@ -67,7 +67,7 @@ struct Layout {
         total;
 };
 
-constexpr int MAX_SMS = 256;
+constexpr int MAX_SMS = 256 * DFL_GEMM_CTAS_PER_SM;   // GEMM CTAs (split-K slots)
 constexpr int MAX_TILES = 8192;
 
 // Workspace carving.  hn holds the next GEMM's normalised input rows
@@ -169,8 +169,11 @@ int make_map_raw(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int e
     cuuint64_t strides[1] = {inner * es};
     cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t estr[2] = {1, 1};
+#ifndef DFL_L2_PROMOTION
+#define DFL_L2_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+#endif
     CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, DFL_L2_PROMOTION,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return DFLASH_OK;
@@ -282,7 +285,8 @@ int plan_gemm(dflash_ctx* c, GemmPlan* p, int wfmt, int epi, const void* const* 
     a.counters = c->buf<int>(c->L.counters);
     a.st = c->st();
     const long long units = (long long)a.n_tiles * a.kb;
-    p->grid = (int)(units < c->sms ? units : c->sms);
+    const int ctas = c->sms * DFL_GEMM_CTAS_PER_SM;
+    p->grid = (int)(units < ctas ? units : ctas);
     const double wes = wfmt == WF_F32 ? 4.0 : wfmt == WF_INT4 ? 0.5 : 2.0;
     const double xes = xt == XT_F32 ? 4.0 : 2.0;
     p->wbytes = (double)N * K * wes + (wfmt == WF_INT4 ? (double)N * (K / 64) * 2 : 0.0);
@@ -608,7 +612,7 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
     CUDA_TRY(cudaGetDevice(&dev));
     int sms = 0;
     CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    if (sms > MAX_SMS) sms = MAX_SMS;
+    if (sms > 256) sms = 256;
 
     dflash_ctx* c = new dflash_ctx();
     c->cfg = g;
@@ -926,6 +930,54 @@ int dflash_tap_reduce(const void* const* layer_streams, int32_t n_layers, int32_
     ta.out_type = XT_F32;
     ta.out_row_stride = (long long)n_layers * hidden;
     LAUNCH_TRY(launch_tap_reduce(ta, reinterpret_cast<cudaStream_t>(stream)));
+    return DFLASH_OK;
+}
+
+size_t dflash_linear_workspace_bytes(int32_t n, int32_t k) {
+    if (n < GEMM_BN || n % GEMM_BN || k < 64 || k % 64) return 0;
+    return align_up((size_t)MAX_SMS * 2 * GEMM_BN * DFL_MAX_ROWS * 4, 1024) +
+           align_up((size_t)(n / GEMM_BN) * 4, 256) + align_up(sizeof(DevState), 256);
+}
+
+int dflash_linear(const void* w, const void* x, int32_t n, int32_t k, float* y, void* workspace,
+                  size_t workspace_bytes, dflash_stream_t stream) {
+    if (!w || !x || !y || !workspace) return fail(DFLASH_ERR_ARG, "NULL argument");
+    const size_t need = dflash_linear_workspace_bytes(n, k);
+    if (need == 0) return fail(DFLASH_ERR_ARG, "n %d k %d: n a multiple of 128, k of 64", n, k);
+    if (workspace_bytes < need) return fail(DFLASH_ERR_ARG, "workspace %zu < %zu", workspace_bytes, need);
+    if (!aligned16(w) || !aligned16(x) || !aligned16(y) || !aligned16(workspace))
+        return fail(DFLASH_ERR_ARG, "misaligned buffer");
+    if (int r0 = get_encode()) return r0;
+    if (int r0 = pending_error()) return r0;
+    int dev = 0, sms = 0;
+    CUDA_TRY(cudaGetDevice(&dev));
+    CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    if (sms > 256) sms = 256;
+    GemmMaps maps;
+    memset(&maps, 0, sizeof maps);
+    int r = make_map(&maps.w[0], w, XT_BF16, k, n, GEMM_BN);
+    if (!r) r = make_map(&maps.x, x, XT_BF16, k, DFL_MAX_ROWS, DFL_MAX_ROWS);
+    if (r) return r;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    GemmArgs a;
+    memset(&a, 0, sizeof a);
+    a.N = n;
+    a.K = k;
+    a.n_tiles = n / GEMM_BN;
+    a.kb = k / 64;
+    a.seg_rows[0] = n;
+    a.n_seg = 1;
+    a.out = y;
+    a.ldo = n;
+    a.slots = reinterpret_cast<float*>(ws);
+    a.counters = reinterpret_cast<int*>(ws + align_up((size_t)MAX_SMS * 2 * GEMM_BN * DFL_MAX_ROWS * 4, 1024));
+    a.st = reinterpret_cast<DevState*>(ws + need - align_up(sizeof(DevState), 256));
+    const long long units = (long long)a.n_tiles * a.kb;
+    const int ctas = sms * DFL_GEMM_CTAS_PER_SM;
+    const int grid = (int)(units < ctas ? units : ctas);
+    const int e = launch_gemm(WF_BF16, EPI_STORE, XT_BF16, maps, a, grid,
+                              reinterpret_cast<cudaStream_t>(stream));
+    if (e) return fail(DFLASH_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString((cudaError_t)e));
     return DFLASH_OK;
 }
 

@@ -35,15 +35,33 @@ constexpr int GEMM_STAGE_W = GEMM_BN * 128;   // bytes of the weight tile per st
 //   BF16: 64 k per k-block,  X [16][64] bf16,             4 k-blocks per stage, 3 stages
 //   INT4: 256 k per k-block, X 4 x [16][64] bf16, scales [4 groups][128 rows] bf16,
 //         2 k-blocks per stage, 4 stages
+// Pipeline shape, overridable at build time for tuning sweeps.
+#ifndef DFL_BF16_CHUNK
+#define DFL_BF16_CHUNK 4
+#endif
+#ifndef DFL_BF16_STAGES
+#define DFL_BF16_STAGES 3
+#endif
+#ifndef DFL_INT4_CHUNK
+#define DFL_INT4_CHUNK 2
+#endif
+#ifndef DFL_INT4_STAGES
+#define DFL_INT4_STAGES 4
+#endif
+#ifndef DFL_GEMM_CTAS_PER_SM
+#define DFL_GEMM_CTAS_PER_SM 1
+#endif
+
 template <int WF> struct GemmCfg;
 template <> struct GemmCfg<0> {
     static constexpr int KBLK = 32, XB = 2048, SB = 0, CHUNK = 1, STAGES = 8;
 };
 template <> struct GemmCfg<1> {
-    static constexpr int KBLK = 64, XB = 2048, SB = 0, CHUNK = 4, STAGES = 3;
+    static constexpr int KBLK = 64, XB = 2048, SB = 0, CHUNK = DFL_BF16_CHUNK, STAGES = DFL_BF16_STAGES;
 };
 template <> struct GemmCfg<2> {
-    static constexpr int KBLK = 256, XB = 8192, SB = 1024, CHUNK = 2, STAGES = 4;
+    static constexpr int KBLK = 256, XB = 8192, SB = 1024, CHUNK = DFL_INT4_CHUNK,
+                         STAGES = DFL_INT4_STAGES;
 };
 
 // Per-head epilogue of the q/k/v projection (EPI_QKV).

@@ -285,6 +285,21 @@ int dflash_tap_reduce(const void* const* layer_streams /*host array*/, int32_t n
 int dflash_quantize_int4g64(const float* w, int32_t n, int32_t k, uint8_t* packed,
                             uint16_t* scales, dflash_stream_t stream);
 
+/*
+ * The round's weight-streaming GEMM as a standalone operation:
+ * y[t][j] = sum_k x[t][k] * w[j][k] for the 16 rows t of x, w bf16 [n][k]
+ * (nn.Linear layout), x bf16 [16][k] (rows the caller does not use are
+ * zero), y fp32 [16][n].  n a multiple of 128, k a multiple of 64; every
+ * buffer 16-byte aligned.  The workspace (dflash_linear_workspace_bytes)
+ * holds the split-K partial tiles and tickets; it must be zero-filled
+ * before its first use and is left zero-filled; calls sharing a workspace
+ * must not overlap on the GPU.  The result of a row depends only on that
+ * row (fixed reduction order).
+ */
+size_t dflash_linear_workspace_bytes(int32_t n, int32_t k);
+int dflash_linear(const void* w, const void* x, int32_t n, int32_t k, float* y, void* workspace,
+                  size_t workspace_bytes, dflash_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

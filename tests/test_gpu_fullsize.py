@@ -1,0 +1,114 @@
+"""Parity at the workloads' full sizes, in the launch configuration the bench
+times, on outputs the oracle can compute one by one:
+
+* drafter alone, bf16 (5 layers, 1024 tap rows, block 16): the block's 15
+  draft rows;
+* INT4 drafter (16384 tap rows, window 2048, block 8): the block's 7 rows;
+* 36-layer target verify of 16 rows over a 1024-position synthetic KV cache
+  (adopted through dflash_adopt_kv): logits, acceptance, rollback;
+* the same verify over a 16384-position cache at 1 and 16 rows: row 0 of the
+  16-row verify is bit-identical to the 1-row verify (batch invariance at
+  full size) and both follow the oracle.
+
+Tolerance rel 2e-2 (bf16/INT4 weights against the fp64 oracle); ids
+bit-exact on decidable rows.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from block_diffusion_speculative_gather_gb300 import synth
+from block_diffusion_speculative_gather_gb300.configs import DRAFT_BF16, DRAFT_INT4, E2E_BF16
+from oracle import dflash_oracle as O
+from tests import gpu_common as G
+from tests.oracle_inputs import ModelTensors, oracle_config, oracle_draft, oracle_target
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+
+
+def _ext(taps, w):
+    n = taps.shape[0]
+    return taps.view(n, w.n_taps, w.hidden).permute(1, 0, 2).contiguous()
+
+
+@pytest.mark.parametrize("w", [DRAFT_BF16, DRAFT_INT4], ids=["bf16", "int4"])
+def test_drafter_full_size(w):
+    G.build_lib()
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+    m = ModelTensors(w)
+    dec = DFlash(w, m)
+    taps = synth.tap_rows(w.n_ctx, w.n_taps * w.hidden)
+    dl = G.logits_buf(w.vocab)
+    dec.set_logits_out(None, dl)
+    dec.prefill_taps(_ext(taps, w), hc=1, first_token=4242, max_new=64)
+    ids = dec.draft().cpu().numpy()
+    dec.check()
+    st = dec.stats()
+    assert st.n == w.n_ctx and st.block_len == w.block
+    gpu = dl[1:w.block].cpu().numpy()
+    dec.close()
+    del dec
+    lo = max(0, w.n_ctx - w.window) if w.window else 0
+    taps_np = np.zeros((w.n_ctx, w.n_taps * w.hidden), np.float32)
+    taps_np[lo:] = taps[lo:].float().numpy()          # rows before the window are never read
+    ref, _ = O.draft_forward(oracle_draft(m), m.embed.float().numpy(), oracle_config(w),
+                             taps_np, 4242, w.n_ctx, w.block)
+    err = G.rel_err_rows(gpu, ref[1:])
+    assert err.max() < TOL, err
+    G.check_ids(ids[:w.block - 1], ref[1:], TOL)
+
+
+@pytest.fixture(scope="module")
+def target():
+    G.build_lib()
+    w = E2E_BF16.with_(drf_layers=0, max_seq=16384 + 64)
+    m = ModelTensors(w)
+    return w, m, oracle_target(m)
+
+
+def _synthetic_kv(dec, w, n):
+    """N(0,1) K/V at positions [0, n) of every layer, in the library's cache
+    layout [L][2][n_kv][cap][hd], and the same values for the oracle."""
+    kv = synth.kv_rows(w.tgt_layers, w.n_kv, n, w.head_dim)       # [L, 2, n_kv, n, hd] bf16
+    cap = (w.max_seq + 63) // 64 * 64
+    dev = dec.kv_target.view(torch.bfloat16).view(w.tgt_layers, 2, w.n_kv, cap, w.head_dim)
+    dev[:, :, :, :n, :] = kv.to("cuda")
+    cache = O.KVCache(w.tgt_layers, w.n_kv, w.head_dim)
+    kvf = kv.float().numpy()
+    for l in range(w.tgt_layers):
+        cache.write(l, range(n), np.moveaxis(kvf[l, 0], 0, 1), np.moveaxis(kvf[l, 1], 0, 1))
+    return cache
+
+
+@pytest.mark.parametrize("n", [1024, 16384])
+def test_verify_full_size_over_synthetic_cache(target, n):
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+    w, m, tw = target
+    dec = DFlash(w, m)
+    cache = _synthetic_kv(dec, w, n)
+    t_n = 31337
+    d = synth.uniform_ids(15, w.vocab, seed=5).tolist()
+    vl = G.logits_buf(w.vocab)
+    dec.set_logits_out(vl, None)
+    dec.adopt_kv(n, t_n, 64)
+    toks, ne = dec.verify(torch.tensor(d, dtype=torch.int32, device="cuda"))
+    dec.check()
+    batch = vl.clone()
+    toks, ne = toks.cpu().tolist(), int(ne.item())
+    st = dec.stats()
+    dec.adopt_kv(n, t_n, 64)
+    dec.verify(None)                    # one row: the plain greedy step
+    dec.check()
+    assert torch.equal(vl[0], batch[0]), "row 0 differs between a 16-row and a 1-row verify"
+    dec.close()
+    del dec
+    ref, _ = O.target_forward(tw, oracle_config(w), [t_n] + d, n, cache)
+    err = G.rel_err_rows(batch[:16].cpu().numpy(), ref)
+    assert err.max() < TOL, err
+    y = [int(np.argmax(r)) for r in ref]
+    a, emitted, _ = O.accept(d, y, -1)
+    if all(G.decidable(r, TOL) for r in ref[: a + 1]):
+        assert ne == len(emitted) and toks[:ne] == emitted
+        assert st.n == n + ne and st.last_accept == a
