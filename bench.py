@@ -495,7 +495,7 @@ def measure_workloads(steps, warmup, base_model):
     # --- verify sweep over a 16384-position synthetic KV cache
     w = HC_SWEEP
     dec = DFlash(w, base_model)
-    kv = dec.kv_target.view(torch.bfloat16)
+    kv = dec.kv_target.view(torch.float16)
     gen = torch.Generator("cuda").manual_seed(3)
     chunk = 1 << 26
     for i in range(0, kv.numel(), chunk):

@@ -1,4 +1,4 @@
-// Tensor-core split-KV attention (bf16 caches).
+// Tensor-core split-KV attention (fp16 q and caches).
 #pragma once
 
 #include "common.cuh"

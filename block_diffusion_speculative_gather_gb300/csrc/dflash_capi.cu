@@ -73,6 +73,8 @@ constexpr int MAX_TILES = 8192;
 // Workspace carving.  hn holds the next GEMM's normalised input rows
 // (x * w_norm, activation type) and ssq their per-128-column partial sums
 // of x^2, from which the consuming GEMM derives the RMSNorm row scale.
+// GEMM inputs (hn, attn, act, taps) take 4 bytes per (row, column): fp32
+// rows, or the [32][width] hi/lo bf16 planes of the bf16 models.
 Layout make_layout(const dflash_config& c) {
     Layout L{};
     size_t off = 0;
@@ -86,12 +88,12 @@ Layout make_layout(const dflash_config& c) {
     const int qd = c.n_q * c.head_dim;
     L.state = take(sizeof(DevState));
     L.x = take(R * c.hidden * 4);
-    L.hn = take(R * c.hidden * es);
+    L.hn = take(R * c.hidden * 4);
     L.ssq = take(R * (c.hidden / 128 + 1) * 4);
     L.qrot = take(R * qd * es);
-    L.attn = take(R * qd * es);
-    L.act = take(R * c.ffn * es);
-    L.taps = take(R * (size_t)(c.n_taps > 0 ? c.n_taps : 1) * c.hidden * es);
+    L.attn = take(R * qd * 4);
+    L.act = take(R * c.ffn * 4);
+    L.taps = take(R * (size_t)(c.n_taps > 0 ? c.n_taps : 1) * c.hidden * 4);
     L.rcos = take(R * (c.head_dim / 2) * 4);
     L.rsin = take(R * (c.head_dim / 2) * 4);
     L.amax = take(R * 8);
@@ -216,7 +218,7 @@ struct dflash_ctx {
     int sms;
     std::vector<LayerPlans> tplan, dplan;
     GemmPlan lm, fc;
-    AttnMaps amap_t{}, amap_d{};   // tensor-core attention maps (bf16 caches)
+    AttnMaps amap_t{}, amap_d{};   // tensor-core attention maps (fp16 q and caches)
     float* verify_logits = nullptr;
     float* draft_logits = nullptr;
     bool prefilled = false;
@@ -229,7 +231,10 @@ struct dflash_ctx {
 
     DevState* st() const { return reinterpret_cast<DevState*>(ws + L.state); }
     template <typename T> T* buf(size_t off) const { return reinterpret_cast<T*>(ws + off); }
-    int act_xt() const { return cfg.dtype == DFLASH_F32 ? XT_F32 : XT_BF16; }
+    // GEMM inputs: fp32, or hi/lo bf16 planes for the bf16 models
+    int act_xt() const { return cfg.dtype == DFLASH_F32 ? XT_F32 : XT_BF16S; }
+    // attention operands (q, K/V caches): fp32, or fp16 for the bf16 models
+    int kv_xt() const { return cfg.dtype == DFLASH_F32 ? XT_F32 : XT_F16; }
     int wf(int f) const { return f == DFLASH_F32 ? WF_F32 : f == DFLASH_INT4G64 ? WF_INT4 : WF_BF16; }
     size_t cache_layer_stride() const {   // elements per layer (K and V)
         return (size_t)2 * cfg.n_kv * cache_cap(cfg) * cfg.head_dim;
@@ -267,9 +272,11 @@ int plan_gemm(dflash_ctx* c, GemmPlan* p, int wfmt, int epi, const void* const* 
         p->args.seg_rows[i] = rows[i];
         N += rows[i];
     }
-    int r = make_map(&p->maps.x, x, xt, K, DFL_MAX_ROWS, DFL_MAX_ROWS);
+    const uint32_t xrows = xt == XT_BF16S ? 2 * DFL_MAX_ROWS : DFL_MAX_ROWS;
+    int r = make_map(&p->maps.x, x, xt == XT_BF16S ? XT_BF16 : xt, K, xrows, xrows);
     if (r) return r;
     GemmArgs& a = p->args;
+    a.x_split = xt == XT_BF16S ? 1 : 0;
     a.n_seg = nseg;
     a.K = K;
     a.kb = K / (wfmt == WF_F32 ? 32 : wfmt == WF_INT4 ? 256 : 64);
@@ -288,7 +295,7 @@ int plan_gemm(dflash_ctx* c, GemmPlan* p, int wfmt, int epi, const void* const* 
     const int ctas = c->sms * DFL_GEMM_CTAS_PER_SM;
     p->grid = (int)(units < ctas ? units : ctas);
     const double wes = wfmt == WF_F32 ? 4.0 : wfmt == WF_INT4 ? 0.5 : 2.0;
-    const double xes = xt == XT_F32 ? 4.0 : 2.0;
+    const double xes = (xt == XT_F32 || xt == XT_BF16S) ? 4.0 : 2.0;
     p->wbytes = (double)N * K * wes + (wfmt == WF_INT4 ? (double)N * (K / 64) * 2 : 0.0);
     double outb = 0;
     if (epi == EPI_STORE) outb = (double)DFL_MAX_ROWS * N * 4;
@@ -389,12 +396,12 @@ QkvEpi qkv_epi(const dflash_ctx* c, const dflash_layer& lw, bool target, int lay
     q.rope_cos = c->buf<float>(c->L.rcos);
     q.rope_sin = c->buf<float>(c->L.rsin);
     q.q_out = c->ws + c->L.qrot;
-    q.q_type = c->act_xt();
+    q.q_type = c->kv_xt();
     uint8_t* cache = reinterpret_cast<uint8_t*>(target ? c->kv_t : c->kv_d) +
                      (size_t)layer * c->cache_layer_stride() * elem_size(g.dtype);
     q.k_cache = cache;
     q.v_cache = cache + c->cache_kv_offset() * elem_size(g.dtype);
-    q.c_type = c->act_xt();
+    q.c_type = c->kv_xt();
     q.cap = cache_cap(g);
     q.max_seq = g.max_seq;
     q.row_sel = row_sel;
@@ -427,7 +434,7 @@ int run_layers(dflash_ctx* c, bool target, cudaStream_t s) {
         at.q = c->ws + c->L.qrot;
         at.k_cache = cache;
         at.v_cache = cache + c->cache_kv_offset() * elem_size(g.dtype);
-        at.kv_type = xt;
+        at.kv_type = c->kv_xt();
         at.n_q = g.n_q;
         at.n_kv = g.n_kv;
         at.head_dim = g.head_dim;
@@ -477,7 +484,7 @@ int run_layers(dflash_ctx* c, bool target, cudaStream_t s) {
         if (target && g.drf_layers > 0) {
             for (int i = 0; i < g.n_taps; ++i)
                 if (g.tap_layer[i] == l) {
-                    a.tap_out = c->ws + c->L.taps + (size_t)i * H * elem_size(g.dtype);
+                    a.tap_out = c->ws + c->L.taps + (size_t)i * H * elem_size(g.dtype);   // column i*H
                     a.ld_tap = g.n_taps * H;
                     a.tap_type = xt;
                 }
@@ -644,14 +651,14 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
     if (!r && g.dtype == DFLASH_BF16) {
         const int cap = cache_cap(g);
         const int qrows = (g.n_q / g.n_kv) * DFL_MAX_ROWS;
-        r = make_map_raw(&c->amap_t.q, c->ws + L.qrot, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.head_dim,
+        r = make_map_raw(&c->amap_t.q, c->ws + L.qrot, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.head_dim,
                          (uint64_t)g.n_q * DFL_MAX_ROWS, 64, qrows, CU_TENSOR_MAP_SWIZZLE_128B);
         c->amap_d.q = c->amap_t.q;
         if (!r && g.tgt_layers > 0)
-            r = make_map_raw(&c->amap_t.kv, kv_target, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.head_dim,
+            r = make_map_raw(&c->amap_t.kv, kv_target, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.head_dim,
                              (uint64_t)g.tgt_layers * 2 * g.n_kv * cap, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
         if (!r && g.drf_layers > 0)
-            r = make_map_raw(&c->amap_d.kv, kv_draft, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.head_dim,
+            r = make_map_raw(&c->amap_d.kv, kv_draft, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.head_dim,
                              (uint64_t)g.drf_layers * 2 * g.n_kv * cap, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     }
     if (r) {
@@ -775,7 +782,7 @@ int dflash_prefill_taps(dflash_ctx* c, const int32_t* prompt_ids, int32_t n_prom
             ta.rows = T;
             ta.hc = hc;
             ta.hidden = g.hidden;
-            ta.in_type = c->act_xt();
+            ta.in_type = g.dtype == DFLASH_F32 ? XT_F32 : XT_BF16;
             ta.out = c->ws + c->L.taps;
             ta.out_type = c->act_xt();
             ta.out_row_stride = (long long)g.n_taps * g.hidden;

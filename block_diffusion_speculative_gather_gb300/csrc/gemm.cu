@@ -9,9 +9,13 @@
 //    into equal contiguous ranges (stream-K), so every SM streams the same
 //    number of bytes whatever N and K are;
 //  * a producer warp issues TMA tile loads (cp.async.bulk.tensor, 128-byte
-//    swizzle) of the weight tile [128 rows x 128 B] and the matching
-//    activation tile [16 x 128 B] into an 8-deep shared-memory ring guarded
+//    swizzle) of consecutive weight tiles [128 rows x 128 B] and the
+//    matching activation tiles into a shared-memory ring of stages guarded
 //    by mbarriers; 8 consumer warps each own 16 weight rows;
+//  * the activations of the model's own forward are two bf16 planes (hi and
+//    the rounding remainder lo, rows 0..15 and 16..31 of the X tile): each
+//    weight fragment is multiplied by both, so the product carries the
+//    activation to about 16 mantissa bits while the weights stream once;
 //  * bf16 weights: the weight rows are the M=16 side of mma.sync m16n8k16
 //    (swap-AB) and the <= 16 activation rows the N side (two n8 tiles);
 //    inside each 64-wide k-block every lane takes 16 consecutive k
@@ -81,7 +85,8 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     using CFG = GemmCfg<WF>;
     constexpr int STAGES = CFG::STAGES, KBLK = CFG::KBLK, XB = CFG::XB, SB = CFG::SB;
     constexpr int CHUNK = CFG::CHUNK;
-    constexpr uint32_t KB_BYTES = GEMM_STAGE_W + XB + SB;     // bytes of one k-block
+    // bytes one k-block brings: an unsplit bf16 input fills half of its X slot
+    const uint32_t KB_BYTES = GEMM_STAGE_W + SB + ((WF == WF_F32 || a.x_split) ? XB : XB / 2);
     uint8_t* Ws = smem;                                        // [STAGES][CHUNK][128 x 128 B]
     uint8_t* Xs = Ws + STAGES * CHUNK * GEMM_STAGE_W;          // [STAGES][CHUNK][XB]
     uint8_t* Ss = Xs + STAGES * CHUNK * XB;                    // [STAGES][CHUNK][SB] (INT4)
@@ -156,7 +161,7 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 if (WF == WF_INT4) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        tma_load_2d(xdst + q * 2048, &maps.x, &full[stage], k * KBLK + 64 * q, 0);
+                        tma_load_2d(xdst + q * (XB / 4), &maps.x, &full[stage], k * KBLK + 64 * q, 0);
                 } else {
                     tma_load_2d(xdst, &maps.x, &full[stage], k * KBLK, 0);
                 }
@@ -275,7 +280,7 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                         sb = __bfloat162float(St[q * 128 + r0 + 8]);
                     }
                     uint32_t xa[8], xb[8];
-                    const uint8_t* Xq = Xt + q * 2048;
+                    const uint8_t* Xq = Xt + q * (XB / 4);
                     *reinterpret_cast<uint4*>(&xa[0]) = lds128(Xq + swz128(g, 2 * c));
                     *reinterpret_cast<uint4*>(&xa[4]) = lds128(Xq + swz128(g, 2 * c + 1));
                     *reinterpret_cast<uint4*>(&xb[0]) = lds128(Xq + swz128(g + 8, 2 * c));
@@ -303,6 +308,20 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                         const uint32_t B1[2] = {xb[2 * j], xb[2 * j + 1]};
                         mma_bf16_16816(g0, A, B0);
                         mma_bf16_16816(g1, A, B1);
+                    }
+                    if (a.x_split) {   // lo planes: tokens g, g + 8 at rows 16 + g, 24 + g
+                        *reinterpret_cast<uint4*>(&xa[0]) = lds128(Xq + swz128(16 + g, 2 * c));
+                        *reinterpret_cast<uint4*>(&xa[4]) = lds128(Xq + swz128(16 + g, 2 * c + 1));
+                        *reinterpret_cast<uint4*>(&xb[0]) = lds128(Xq + swz128(24 + g, 2 * c));
+                        *reinterpret_cast<uint4*>(&xb[4]) = lds128(Xq + swz128(24 + g, 2 * c + 1));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t A[4] = {pa[2 * j], pb[2 * j], pa[2 * j + 1], pb[2 * j + 1]};
+                            const uint32_t B0[2] = {xa[2 * j], xa[2 * j + 1]};
+                            const uint32_t B1[2] = {xb[2 * j], xb[2 * j + 1]};
+                            mma_bf16_16816(g0, A, B0);
+                            mma_bf16_16816(g1, A, B1);
+                        }
                     }
                     acc[0] = fmaf(sa, g0[0], acc[0]);
                     acc[1] = fmaf(sa, g0[1], acc[1]);
@@ -333,6 +352,20 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     const uint32_t B1[2] = {xb[2 * j], xb[2 * j + 1]};
                     mma_bf16_16816(d0, A, B0);
                     mma_bf16_16816(d1, A, B1);
+                }
+                if (a.x_split) {   // lo planes: tokens g, g + 8 at rows 16 + g, 24 + g
+                    *reinterpret_cast<uint4*>(&xa[0]) = lds128(Xt + swz128(16 + g, 2 * c));
+                    *reinterpret_cast<uint4*>(&xa[4]) = lds128(Xt + swz128(16 + g, 2 * c + 1));
+                    *reinterpret_cast<uint4*>(&xb[0]) = lds128(Xt + swz128(24 + g, 2 * c));
+                    *reinterpret_cast<uint4*>(&xb[4]) = lds128(Xt + swz128(24 + g, 2 * c + 1));
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t A[4] = {ra[2 * j], rb[2 * j], ra[2 * j + 1], rb[2 * j + 1]};
+                        const uint32_t B0[2] = {xa[2 * j], xa[2 * j + 1]};
+                        const uint32_t B1[2] = {xb[2 * j], xb[2 * j + 1]};
+                        mma_bf16_16816(d0, A, B0);
+                        mma_bf16_16816(d1, A, B1);
+                    }
                 }
             } else {  // WF_F32: CUDA-core FMAs, k in order
                 const int t = lane & 15, h = lane >> 4;
@@ -486,11 +519,11 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                             const size_t o = (size_t)t * a.ldo + n0 + r;
                             v += a.out[o];
                             a.out[o] = v;
-                            if (a.tap_out) store_xt(a.tap_out, a.tap_type, (size_t)t * a.ld_tap + n0 + r, v);
+                            if (a.tap_out) store_act(a.tap_out, a.tap_type, a.ld_tap, t, n0 + r, v);
                         }
                         ss = fmaf(v, v, ss);
                         const float wn = a.w_next ? a.w_next[n0 + r] : 1.f;
-                        store_xt(a.xn_out, a.xn_type, (size_t)t * a.ldo + n0 + r, v * wn);
+                        store_act(a.xn_out, a.xn_type, a.ldo, t, n0 + r, v * wn);
                     }
                     ss = warp_sum(ss);
                     if (a.ssq_out && lane == 0) a.ssq_out[tile * DFL_MAX_ROWS + t] = ss;
@@ -502,7 +535,7 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     const float gt = ctile[t * GEMM_BN + r] * s_rstd[t];
                     const float up = ctile[t * GEMM_BN + 64 + r] * s_rstd[t];
                     const float v = gt / (1.f + expf(-gt)) * up;
-                    store_xt(a.act, a.act_type, (size_t)t * a.ld_act + j0 + r, v);
+                    store_act(a.act, a.act_type, a.ld_act, t, j0 + r, v);
                 }
             } else if (EPI == EPI_QKV) {
                 // the tile is 128 / hd whole heads; item = (token, head in tile)

@@ -21,7 +21,28 @@ enum Epi : int {
     EPI_QKV = 4,      // rstd, per-head q/k RMSNorm, RoPE, q out and K/V into the cache
     EPI_NORMOUT = 5,  // Y * w_norm as the next normalised input (+ partial sums)
 };
-enum XType : int { XT_F32 = 0, XT_BF16 = 1, XT_F16 = 2 };
+// Activation element types.  XT_BF16S is a GEMM input kept to about 16
+// mantissa bits as two bf16 planes of one [32][ld] buffer: row t holds
+// hi = bf16(v) and row 16 + t holds lo = bf16(v - hi); the GEMM multiplies
+// both planes by the same weights and sums them in fp32.
+enum XType : int { XT_F32 = 0, XT_BF16 = 1, XT_F16 = 2, XT_BF16S = 3 };
+
+// Stores v as element (t, col) of a [rows][ld] activation of type xt (for
+// XT_BF16S: the hi plane at row t, the lo plane at row 16 + t).
+__device__ __forceinline__ void store_act(void* base, int xt, size_t ld, int t, size_t col, float v) {
+    const size_t i = (size_t)t * ld + col;
+    if (xt == XT_F32) {
+        reinterpret_cast<float*>(base)[i] = v;
+    } else if (xt == XT_F16) {
+        reinterpret_cast<__half*>(base)[i] = __float2half_rn(v);
+    } else {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        reinterpret_cast<__nv_bfloat16*>(base)[i] = hi;
+        if (xt == XT_BF16S)
+            reinterpret_cast<__nv_bfloat16*>(base)[i + DFL_MAX_ROWS * ld] =
+                __float2bfloat16_rn(v - __bfloat162float(hi));
+    }
+}
 
 constexpr int GEMM_BN = 128;        // output rows (weight rows) per tile
 constexpr int GEMM_CONSUMERS = 8;   // MMA warps, 16 weight rows each
@@ -31,13 +52,14 @@ constexpr int GEMM_STAGE_W = GEMM_BN * 128;   // bytes of the weight tile per st
 // Per weight format: a k-block is one 128-byte row of a weight tile; a
 // pipeline stage holds CHUNK consecutive k-blocks of one tile, so every
 // weight row is fetched CHUNK x 128 contiguous bytes at a time.
-//   F32 : 32 k per k-block,  X [16][32] fp32,             1 k-block per stage, 8 stages
-//   BF16: 64 k per k-block,  X [16][64] bf16,             4 k-blocks per stage, 3 stages
-//   INT4: 256 k per k-block, X 4 x [16][64] bf16, scales [4 groups][128 rows] bf16,
-//         2 k-blocks per stage, 4 stages
+//   F32 : 32 k per k-block,  X [16][32] fp32,                1 k-block per stage, 8 stages
+//   BF16: 64 k per k-block,  X [32][64] bf16 (hi/lo planes),  3 k-blocks per stage, 3 stages
+//   INT4: 256 k per k-block, X 4 x [32][64] bf16, scales [4 groups][128 rows] bf16,
+//         2 k-blocks per stage, 3 stages
+// (an unsplit bf16 input fills only the 16 hi rows of each X slot)
 // Pipeline shape, overridable at build time for tuning sweeps.
 #ifndef DFL_BF16_CHUNK
-#define DFL_BF16_CHUNK 4
+#define DFL_BF16_CHUNK 3
 #endif
 #ifndef DFL_BF16_STAGES
 #define DFL_BF16_STAGES 3
@@ -46,7 +68,7 @@ constexpr int GEMM_STAGE_W = GEMM_BN * 128;   // bytes of the weight tile per st
 #define DFL_INT4_CHUNK 2
 #endif
 #ifndef DFL_INT4_STAGES
-#define DFL_INT4_STAGES 4
+#define DFL_INT4_STAGES 3
 #endif
 #ifndef DFL_GEMM_CTAS_PER_SM
 #define DFL_GEMM_CTAS_PER_SM 1
@@ -57,10 +79,10 @@ template <> struct GemmCfg<0> {
     static constexpr int KBLK = 32, XB = 2048, SB = 0, CHUNK = 1, STAGES = 8;
 };
 template <> struct GemmCfg<1> {
-    static constexpr int KBLK = 64, XB = 2048, SB = 0, CHUNK = DFL_BF16_CHUNK, STAGES = DFL_BF16_STAGES;
+    static constexpr int KBLK = 64, XB = 4096, SB = 0, CHUNK = DFL_BF16_CHUNK, STAGES = DFL_BF16_STAGES;
 };
 template <> struct GemmCfg<2> {
-    static constexpr int KBLK = 256, XB = 8192, SB = 1024, CHUNK = DFL_INT4_CHUNK,
+    static constexpr int KBLK = 256, XB = 16384, SB = 1024, CHUNK = DFL_INT4_CHUNK,
                          STAGES = DFL_INT4_STAGES;
 };
 
@@ -87,6 +109,7 @@ struct GemmArgs {
     int kb;             // k-blocks per tile
     int seg_rows[3];    // rows of weight maps 0..2 (concatenated along N)
     int n_seg;
+    int x_split;        // 1: the activation is XT_BF16S (the x map's box is 32 rows)
     // input row scale of a folded RMSNorm (QKV, SWIGLU, ARGMAX): NULL = 1
     const float* ssq_in;    // [ssq_parts][16] partial sums of x^2
     int ssq_parts;

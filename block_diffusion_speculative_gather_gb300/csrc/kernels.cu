@@ -14,17 +14,6 @@ namespace dfl {
 
 namespace {
 
-template <typename T>
-__device__ __forceinline__ void st_typed(void* base, size_t i, float v) {
-    reinterpret_cast<T*>(base)[i] = from_f32<T>(v);
-}
-
-__device__ __forceinline__ void st_any(void* base, int t, size_t i, float v) {
-    if (t == XT_F32) st_typed<float>(base, i, v);
-    else if (t == XT_BF16) st_typed<__nv_bfloat16>(base, i, v);
-    else st_typed<__half>(base, i, v);
-}
-
 __device__ __forceinline__ float ld_any(const void* base, int t, size_t i) {
     if (t == XT_F32) return reinterpret_cast<const float*>(base)[i];
     if (t == XT_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[i]);
@@ -91,7 +80,7 @@ __global__ void prepare_rows_kernel(RowsArgs a) {
         // folded RMSNorm input of layer 0: xn = x * w0, per-128-column sums of x^2
         __syncthreads();
         for (int i = threadIdx.x; i < a.hidden; i += blockDim.x)
-            st_any(a.xn, a.xn_type, (size_t)t * a.hidden + i, xr[i] * a.w0[i]);
+            store_act(a.xn, a.xn_type, a.hidden, t, i, xr[i] * a.w0[i]);
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         for (int b = warp; b < a.hidden / 128; b += blockDim.x >> 5) {
             float ss = 0.f;
@@ -212,9 +201,9 @@ __global__ void attn_combine_kernel(AttnArgs a) {
     const int hq = blockIdx.x, t = blockIdx.y, d = threadIdx.x;
     int lo, hi, T, pos0;
     attn_range(a, &lo, &hi, &T, &pos0);
-    const size_t o = ((size_t)t * a.n_q + hq) * HD + d;
+    const size_t ld = (size_t)a.n_q * HD, col = (size_t)hq * HD + d;
     if (t >= T) {
-        st_any(a.out, a.out_type, o, 0.f);
+        store_act(a.out, a.out_type, ld, t, col, 0.f);
         return;
     }
     const int c_lo = lo / ATTN_CHUNK, c_hi = (hi - 1) / ATTN_CHUNK;
@@ -253,7 +242,7 @@ __global__ void attn_combine_kernel(AttnArgs a) {
     }
     for (; i < nc; ++i) O = fmaf(base[i * cstride + 2 + d], s_w[i], O);
     for (int j = 0; j < nc; ++j) L = fmaf(s_l[j], s_w[j], L);
-    st_any(a.out, a.out_type, o, O / L);
+    store_act(a.out, a.out_type, ld, t, col, O / L);
 }
 
 // --------------------------------------------------------------- acceptance
@@ -371,7 +360,7 @@ __global__ void set_ext_state_kernel(DevState* st, int n_ext, int tok, int max_n
 
 // out[r][i*H + j] = (1/hc) * sum_{s=0..hc-1} src_i[r][s*H + j]; eight
 // consecutive columns per thread (16-byte loads of bf16 streams).
-template <typename IT, typename OT>
+template <typename IT, typename OT, bool SPLIT = false>
 __global__ void tap_reduce_kernel(TapArgs a) {
     pdl_trigger();
     pdl_wait();
@@ -401,7 +390,13 @@ __global__ void tap_reduce_kernel(TapArgs a) {
         }
         OT* dst = reinterpret_cast<OT*>(a.out) + (size_t)r * a.out_row_stride + col;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) dst[e] = from_f32<OT>(acc[e] * inv);
+        for (int e = 0; e < 8; ++e) {
+            const float v = acc[e] * inv;
+            const OT hi = from_f32<OT>(v);
+            dst[e] = hi;
+            // XT_BF16S: the rounding remainder 16 rows further down
+            if (SPLIT) dst[e + DFL_MAX_ROWS * a.out_row_stride] = from_f32<OT>(v - to_f32<OT>(hi));
+        }
     }
 }
 
@@ -537,6 +532,10 @@ int launch_tap_reduce(const TapArgs& a, cudaStream_t s) {
         return ok(launch_k(tap_reduce_kernel<__nv_bfloat16, float>, g, b, 0, s, a));
     if (a.in_type == XT_BF16 && a.out_type == XT_BF16)
         return ok(launch_k(tap_reduce_kernel<__nv_bfloat16, __nv_bfloat16>, g, b, 0, s, a));
+    if (a.in_type == XT_BF16 && a.out_type == XT_BF16S) {
+        if (a.rows > DFL_MAX_ROWS) return -2;   // the lo plane sits 16 rows below
+        return ok(launch_k(tap_reduce_kernel<__nv_bfloat16, __nv_bfloat16, true>, g, b, 0, s, a));
+    }
     if (a.in_type == XT_F32 && a.out_type == XT_F32)
         return ok(launch_k(tap_reduce_kernel<float, float>, g, b, 0, s, a));
     return -2;

@@ -77,7 +77,8 @@ typedef struct {
     int32_t window;                     /* drafter context window W; 0 = whole context */
     int32_t max_seq;                    /* positions held by both caches */
     int32_t eos_id;                     /* -1 = no EOS */
-    int32_t dtype;     /* DFLASH_F32 | DFLASH_BF16: embedding, fc, caches, activations */
+    int32_t dtype;     /* DFLASH_F32 | DFLASH_BF16: embedding, fc, activations; the
+                        * caches are fp32 for F32 and fp16 for BF16 */
     int32_t tgt_wfmt;  /* projection format of target layers: F32 | BF16 | INT4G64 */
     int32_t drf_wfmt;  /* projection format of draft layers: F32 | BF16 | INT4G64 */
     int32_t ctx_norm;  /* 1 = RMSNorm after fc (drafter context) */
@@ -134,10 +135,12 @@ typedef struct dflash_ctx dflash_ctx;
 
 /* Bytes of the caller-owned buffers for a configuration (0 if invalid). */
 size_t dflash_workspace_bytes(const dflash_config* cfg /*host*/);
-/* Target KV cache: dtype [tgt_layers][2][n_kv][cap][head_dim], cap = max_seq
- * rounded up to a multiple of 64 (whole attention chunks). */
+/* Target KV cache: [tgt_layers][2][n_kv][cap][head_dim], cap = max_seq
+ * rounded up to a multiple of 64 (whole attention chunks); elements fp32
+ * when dtype is F32, fp16 (IEEE binary16) when dtype is BF16. */
 size_t dflash_kv_target_bytes(const dflash_config* cfg /*host*/);
-/* Draft context K/V: dtype [drf_layers][2][n_kv][cap][head_dim], indexed
+/* Draft context K/V: [drf_layers][2][n_kv][cap][head_dim] (elements as the
+ * target cache), indexed
  * by absolute position (a persistent cache bounded by max_seq:
  * "[RFC] DFlash", "Requested changes" 3 and the reply "3. Draft KV cache"). */
 size_t dflash_kv_draft_bytes(const dflash_config* cfg /*host*/);
@@ -291,10 +294,10 @@ int dflash_quantize_int4g64(const float* w, int32_t n, int32_t k, uint8_t* packe
  * (nn.Linear layout), x bf16 [16][k] (rows the caller does not use are
  * zero), y fp32 [16][n].  n a multiple of 128, k a multiple of 64; every
  * buffer 16-byte aligned.  The workspace (dflash_linear_workspace_bytes)
- * holds the split-K partial tiles and tickets; it must be zero-filled
- * before its first use and is left zero-filled; calls sharing a workspace
- * must not overlap on the GPU.  The result of a row depends only on that
- * row (fixed reduction order).
+ * holds the split-K partial tiles and tickets; zero-fill it before its
+ * first use (every completed call leaves the tickets at zero again); calls
+ * sharing a workspace must not overlap on the GPU.  The result of a row
+ * depends only on that row (fixed reduction order).
  */
 size_t dflash_linear_workspace_bytes(int32_t n, int32_t k);
 int dflash_linear(const void* w, const void* x, int32_t n, int32_t k, float* y, void* workspace,

@@ -70,10 +70,12 @@ def target():
 
 def _synthetic_kv(dec, w, n):
     """N(0,1) K/V at positions [0, n) of every layer, in the library's cache
-    layout [L][2][n_kv][cap][hd], and the same values for the oracle."""
-    kv = synth.kv_rows(w.tgt_layers, w.n_kv, n, w.head_dim)       # [L, 2, n_kv, n, hd] bf16
+    layout [L][2][n_kv][cap][hd] (fp16), and the same values for the oracle."""
+    # [L, 2, n_kv, n, hd], held as fp16 (the cache type of bf16 models);
+    # the oracle reads the same fp16 values
+    kv = synth.kv_rows(w.tgt_layers, w.n_kv, n, w.head_dim).to(torch.float16)
     cap = (w.max_seq + 63) // 64 * 64
-    dev = dec.kv_target.view(torch.bfloat16).view(w.tgt_layers, 2, w.n_kv, cap, w.head_dim)
+    dev = dec.kv_target.view(torch.float16).view(w.tgt_layers, 2, w.n_kv, cap, w.head_dim)
     dev[:, :, :, :n, :] = kv.to("cuda")
     cache = O.KVCache(w.tgt_layers, w.n_kv, w.head_dim)
     kvf = kv.float().numpy()
