@@ -98,6 +98,7 @@ def _load() -> C.CDLL:
         "dflash_adopt_kv": (C.c_int, [vp, i32, i32, i32, vp]),
         "dflash_linear_workspace_bytes": (sz, [i32, i32]),
         "dflash_linear": (C.c_int, [vp, vp, i32, i32, vp, vp, sz, vp]),
+        "dflash_linear_noalloc": (C.c_int, [vp, vp, i32, i32, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -114,7 +115,7 @@ EXPORTED = ("dflash_workspace_bytes", "dflash_kv_target_bytes", "dflash_kv_draft
             "dflash_destroy", "dflash_last_error", "dflash_tap_reduce",
             "dflash_quantize_int4g64", "dflash_profile", "dflash_launch_count",
             "dflash_selftest_timeout", "dflash_adopt_kv", "dflash_linear_workspace_bytes",
-            "dflash_linear")
+            "dflash_linear", "dflash_linear_noalloc")
 
 
 def check(rc: int) -> None:
@@ -228,3 +229,10 @@ def dflash_linear(w, x, y, workspace, stream=None):
     n, k = w.shape
     check(lib.dflash_linear(_ptr(w), _ptr(x), n, k, _ptr(y), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def dflash_linear_noalloc(w, x, y, stream=None):
+    """y = x w^T like dflash_linear, with the library's fixed scratch instead
+    of a caller workspace (for callers that cannot allocate device memory)."""
+    n, k = w.shape
+    check(lib.dflash_linear_noalloc(_ptr(w), _ptr(x), n, k, _ptr(y), _stream(stream)))

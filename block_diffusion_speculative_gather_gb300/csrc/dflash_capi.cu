@@ -561,6 +561,30 @@ RowsArgs rows_args(dflash_ctx* c, int mode) {
 
 }  // namespace
 
+// Host helpers shared with the other C-ABI source files.
+namespace dfl {
+
+int report_error(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int make_linear_maps(GemmMaps* maps, const void* w, const void* x, int n, int k) {
+    int r = get_encode();
+    if (r) return r;
+    memset(maps, 0, sizeof *maps);
+    r = make_map(&maps->w[0], w, XT_BF16, k, n, GEMM_BN);
+    if (!r) r = make_map(&maps->x, x, XT_BF16, k, DFL_MAX_ROWS, DFL_MAX_ROWS);
+    return r;
+}
+
+}  // namespace dfl
+
 // ====================================================================== C ABI
 
 extern "C" {

@@ -154,4 +154,10 @@ struct GemmMaps {
 int launch_gemm(int wfmt, int epi, int xt, const GemmMaps& maps, const GemmArgs& args,
                 int grid, cudaStream_t stream);
 
+// Host helpers of the C ABI (defined with it): record the message returned
+// by dflash_last_error and return code; build the bf16 weight and [16][k]
+// activation maps of a plain y = x w^T.
+int report_error(int code, const char* fmt, ...);
+int make_linear_maps(GemmMaps* maps, const void* w, const void* x, int n, int k);
+
 }  // namespace dfl

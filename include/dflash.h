@@ -303,6 +303,27 @@ size_t dflash_linear_workspace_bytes(int32_t n, int32_t k);
 int dflash_linear(const void* w, const void* x, int32_t n, int32_t k, float* y, void* workspace,
                   size_t workspace_bytes, dflash_stream_t stream);
 
+/*
+ * dflash_linear without a workspace, for callers that cannot allocate
+ * device memory: code that runs inside a host framework whose allocator
+ * owns the device memory, or in a latency-critical loop where cudaMalloc /
+ * cudaFree would synchronise the device.  No counterpart in the paper: the
+ * method itself has no such operation; this is a library convenience.
+ *
+ * Same operands, layout and result as dflash_linear (the same kernel and
+ * launch shape), with n at most 262144 output columns; larger n returns
+ * DFLASH_ERR_ARG before anything is launched.  The split-K scratch is one
+ * fixed 4 MiB + 9 KiB array in the library's device memory, held by every
+ * GPU that loads the library until the process exits.  The first call on a
+ * device looks up that array's device address (with the device current);
+ * make that first call before any stream capture.  Every call on a device
+ * shares the array: each clears the tickets it needs on its stream first,
+ * but calls that overlap on the GPU (unordered streams) race and may return
+ * wrong results.  The call allocates nothing.
+ */
+int dflash_linear_noalloc(const void* w, const void* x, int32_t n, int32_t k, float* y,
+                          dflash_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
