@@ -77,7 +77,7 @@ __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsig
 }
 
 template <int WF, int EPI>
-__global__ void __launch_bounds__(GEMM_THREADS, DFL_GEMM_CTAS_PER_SM)
+__global__ void __launch_bounds__(GEMM_THREADS, DFL_GEMM_MINBLOCKS)
 gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(

@@ -73,6 +73,11 @@ constexpr int GEMM_STAGE_W = GEMM_BN * 128;   // bytes of the weight tile per st
 #ifndef DFL_GEMM_CTAS_PER_SM
 #define DFL_GEMM_CTAS_PER_SM 1
 #endif
+// Register budget: a GEMM CTA sized to share its SM with one more CTA (the
+// next kernel's, under programmatic dependent launch) when set to 2.
+#ifndef DFL_GEMM_MINBLOCKS
+#define DFL_GEMM_MINBLOCKS DFL_GEMM_CTAS_PER_SM
+#endif
 
 template <int WF> struct GemmCfg;
 template <> struct GemmCfg<0> {
