@@ -56,9 +56,19 @@ extern bool g_pdl;
 // Launches a kernel on stream s with programmatic stream serialisation: the
 // kernel may be scheduled while its predecessor drains; every kernel of the
 // library calls pdl_wait() before it touches memory a predecessor writes.
+// Shared-memory carveout every kernel of the library asks for (percent of
+// the unified L1/shared array; -1 leaves the choice to the driver).  One
+// value for all kernels keeps the SMs from reconfiguring the split between
+// consecutive kernels of a round.
+#ifndef DFL_SMEM_CARVEOUT
+#define DFL_SMEM_CARVEOUT 100
+#endif
+void set_carveout_once(const void* kern);
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                             cudaStream_t s, Args&&... args) {
+    set_carveout_once(reinterpret_cast<const void*>(kern));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;

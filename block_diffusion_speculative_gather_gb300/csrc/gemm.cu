@@ -33,12 +33,28 @@
 // word, stops new copies and drains the copies already issued.
 
 #include <cstdlib>
+#include <mutex>
+#include <vector>
 
-#include "gemm.cuh"
+#include "gemm_dev.cuh"
 
 namespace dfl {
 
 long long g_launches = 0;
+
+void set_carveout_once(const void* kern) {
+    if (DFL_SMEM_CARVEOUT < 0) return;
+    static std::mutex mu;
+    static std::vector<const void*> done;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const void* k : done)
+        if (k == kern) return;
+    // a hint: on failure clear the error so it is not reported by a later check
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             DFL_SMEM_CARVEOUT) != cudaSuccess)
+        (void)cudaGetLastError();
+    done.push_back(kern);
+}
 bool g_pdl = [] {
     const char* e = getenv("DFLASH_PDL");
     return !(e && e[0] == '0');
@@ -46,35 +62,10 @@ bool g_pdl = [] {
 
 namespace {
 
-__device__ __forceinline__ void consumer_bar() {
-    asm volatile("bar.sync 1, %0;" ::"n"(GEMM_CONSUMERS * 32) : "memory");
-}
-
-__device__ __forceinline__ long long range_start(int b, long long U, int G) {
-    return (long long)b * U / G;
-}
-
-__device__ __forceinline__ int cta_of(long long u, long long U, int G) {
-    int b = (int)((u * G) / U);
-    while (b + 1 < G && range_start(b + 1, U, G) <= u) ++b;
-    while (b > 0 && range_start(b, U, G) > u) --b;
-    return b;
-}
-
-template <typename T>
-__device__ __forceinline__ void store_as(void* base, size_t idx, float v) {
-    reinterpret_cast<T*>(base)[idx] = from_f32<T>(v);
-}
-
-__device__ __forceinline__ void store_xt(void* base, int xt, size_t idx, float v) {
-    if (xt == XT_F32) store_as<float>(base, idx, v);
-    else if (xt == XT_BF16) store_as<__nv_bfloat16>(base, idx, v);
-    else store_as<__half>(base, idx, v);
-}
-
-__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
-    return a > b ? a : b;
-}
+using gdev::consumer_bar;
+using gdev::range_start;
+using gdev::mma_kblock;
+using gdev::finish_tile;
 
 template <int WF, int EPI>
 __global__ void __launch_bounds__(GEMM_THREADS, DFL_GEMM_MINBLOCKS)
@@ -231,7 +222,6 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     __shared__ float s_rstd[DFL_MAX_ROWS];
     pdl_wait();    // the epilogues read and write buffers of earlier kernels
     const int tid = threadIdx.x;   // 0..255
-    const int g = lane >> 2, c = lane & 3;
     int stage = 0;
     uint32_t phase = 0;
     float acc[8];
@@ -257,140 +247,7 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             const uint8_t* Wt = Ws + (stage * CHUNK + jb) * GEMM_STAGE_W;
             const uint8_t* Xt = Xs + (stage * CHUNK + jb) * XB;
             const uint8_t* Sb = Ss + (stage * CHUNK + jb) * SB;
-            if (WF == WF_INT4) {
-                // 4 scale groups of 64 k; inside group q a lane owns k 16c..16c+15
-                // of rows r0 and r0+8 (two interleaved 32-bit words each) and the
-                // same 16 k of tokens g and g+8; the group's partial sums are
-                // scaled per row in fp32 and added to the accumulators.
-                const int r0 = warp * 16 + g;
-                const __nv_bfloat16* St = reinterpret_cast<const __nv_bfloat16*>(Sb);
-                const __nv_bfloat162 bias = __floats2bfloat162_rn(136.f, 136.f);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t off = swz128(r0, 2 * q + (c >> 1)) + 8 * (c & 1);
-                    const uint2 wa = *reinterpret_cast<const uint2*>(Wt + off);
-                    const uint2 wb = *reinterpret_cast<const uint2*>(
-                        Wt + swz128(r0 + 8, 2 * q + (c >> 1)) + 8 * (c & 1));
-                    float sa, sb;
-                    if (EPI == EPI_SWIGLU) {
-                        sa = __bfloat162float(St[(r0 >> 6) * 256 + q * 64 + (r0 & 63)]);
-                        sb = __bfloat162float(St[((r0 + 8) >> 6) * 256 + q * 64 + ((r0 + 8) & 63)]);
-                    } else {
-                        sa = __bfloat162float(St[q * 128 + r0]);
-                        sb = __bfloat162float(St[q * 128 + r0 + 8]);
-                    }
-                    uint32_t xa[8], xb[8];
-                    const uint8_t* Xq = Xt + q * (XB / 4);
-                    *reinterpret_cast<uint4*>(&xa[0]) = lds128(Xq + swz128(g, 2 * c));
-                    *reinterpret_cast<uint4*>(&xa[4]) = lds128(Xq + swz128(g, 2 * c + 1));
-                    *reinterpret_cast<uint4*>(&xb[0]) = lds128(Xq + swz128(g + 8, 2 * c));
-                    *reinterpret_cast<uint4*>(&xb[4]) = lds128(Xq + swz128(g + 8, 2 * c + 1));
-                    // dequantise: pair p_i of a word = nibbles (i, i+4) = k (2i, 2i+1)
-                    uint32_t pa[8], pb[8];
-                    const uint32_t wordsa[2] = {wa.x, wa.y}, wordsb[2] = {wb.x, wb.y};
-#pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            uint32_t ua = ((wordsa[m] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-                            uint32_t ub = ((wordsb[m] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-                            __nv_bfloat162 va = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&ua), bias);
-                            __nv_bfloat162 vb = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&ub), bias);
-                            pa[4 * m + i] = *reinterpret_cast<uint32_t*>(&va);
-                            pb[4 * m + i] = *reinterpret_cast<uint32_t*>(&vb);
-                        }
-                    }
-                    float g0[4] = {0.f, 0.f, 0.f, 0.f}, g1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t A[4] = {pa[2 * j], pb[2 * j], pa[2 * j + 1], pb[2 * j + 1]};
-                        const uint32_t B0[2] = {xa[2 * j], xa[2 * j + 1]};
-                        const uint32_t B1[2] = {xb[2 * j], xb[2 * j + 1]};
-                        mma_bf16_16816(g0, A, B0);
-                        mma_bf16_16816(g1, A, B1);
-                    }
-                    if (a.x_split) {   // lo planes: tokens g, g + 8 at rows 16 + g, 24 + g
-                        *reinterpret_cast<uint4*>(&xa[0]) = lds128(Xq + swz128(16 + g, 2 * c));
-                        *reinterpret_cast<uint4*>(&xa[4]) = lds128(Xq + swz128(16 + g, 2 * c + 1));
-                        *reinterpret_cast<uint4*>(&xb[0]) = lds128(Xq + swz128(24 + g, 2 * c));
-                        *reinterpret_cast<uint4*>(&xb[4]) = lds128(Xq + swz128(24 + g, 2 * c + 1));
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint32_t A[4] = {pa[2 * j], pb[2 * j], pa[2 * j + 1], pb[2 * j + 1]};
-                            const uint32_t B0[2] = {xa[2 * j], xa[2 * j + 1]};
-                            const uint32_t B1[2] = {xb[2 * j], xb[2 * j + 1]};
-                            mma_bf16_16816(g0, A, B0);
-                            mma_bf16_16816(g1, A, B1);
-                        }
-                    }
-                    acc[0] = fmaf(sa, g0[0], acc[0]);
-                    acc[1] = fmaf(sa, g0[1], acc[1]);
-                    acc[2] = fmaf(sb, g0[2], acc[2]);
-                    acc[3] = fmaf(sb, g0[3], acc[3]);
-                    acc[4] = fmaf(sa, g1[0], acc[4]);
-                    acc[5] = fmaf(sa, g1[1], acc[5]);
-                    acc[6] = fmaf(sb, g1[2], acc[6]);
-                    acc[7] = fmaf(sb, g1[3], acc[7]);
-                }
-            } else if (WF == WF_BF16) {
-                const int r0 = warp * 16 + g;
-                uint32_t ra[8], rb[8], xa[8], xb[8];
-                *reinterpret_cast<uint4*>(&ra[0]) = lds128(Wt + swz128(r0, 2 * c));
-                *reinterpret_cast<uint4*>(&ra[4]) = lds128(Wt + swz128(r0, 2 * c + 1));
-                *reinterpret_cast<uint4*>(&rb[0]) = lds128(Wt + swz128(r0 + 8, 2 * c));
-                *reinterpret_cast<uint4*>(&rb[4]) = lds128(Wt + swz128(r0 + 8, 2 * c + 1));
-                *reinterpret_cast<uint4*>(&xa[0]) = lds128(Xt + swz128(g, 2 * c));
-                *reinterpret_cast<uint4*>(&xa[4]) = lds128(Xt + swz128(g, 2 * c + 1));
-                *reinterpret_cast<uint4*>(&xb[0]) = lds128(Xt + swz128(g + 8, 2 * c));
-                *reinterpret_cast<uint4*>(&xb[4]) = lds128(Xt + swz128(g + 8, 2 * c + 1));
-                float(&d0)[4] = *reinterpret_cast<float(*)[4]>(&acc[0]);
-                float(&d1)[4] = *reinterpret_cast<float(*)[4]>(&acc[4]);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t A[4] = {ra[2 * j], rb[2 * j], ra[2 * j + 1], rb[2 * j + 1]};
-                    const uint32_t B0[2] = {xa[2 * j], xa[2 * j + 1]};
-                    const uint32_t B1[2] = {xb[2 * j], xb[2 * j + 1]};
-                    mma_bf16_16816(d0, A, B0);
-                    mma_bf16_16816(d1, A, B1);
-                }
-                if (a.x_split) {   // lo planes: tokens g, g + 8 at rows 16 + g, 24 + g
-                    *reinterpret_cast<uint4*>(&xa[0]) = lds128(Xt + swz128(16 + g, 2 * c));
-                    *reinterpret_cast<uint4*>(&xa[4]) = lds128(Xt + swz128(16 + g, 2 * c + 1));
-                    *reinterpret_cast<uint4*>(&xb[0]) = lds128(Xt + swz128(24 + g, 2 * c));
-                    *reinterpret_cast<uint4*>(&xb[4]) = lds128(Xt + swz128(24 + g, 2 * c + 1));
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t A[4] = {ra[2 * j], rb[2 * j], ra[2 * j + 1], rb[2 * j + 1]};
-                        const uint32_t B0[2] = {xa[2 * j], xa[2 * j + 1]};
-                        const uint32_t B1[2] = {xb[2 * j], xb[2 * j + 1]};
-                        mma_bf16_16816(d0, A, B0);
-                        mma_bf16_16816(d1, A, B1);
-                    }
-                }
-            } else {  // WF_F32: CUDA-core FMAs, k in order
-                const int t = lane & 15, h = lane >> 4;
-                float xv[32];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint4 v = lds128(Xt + swz128(t, q));
-                    xv[4 * q + 0] = __uint_as_float(v.x);
-                    xv[4 * q + 1] = __uint_as_float(v.y);
-                    xv[4 * q + 2] = __uint_as_float(v.z);
-                    xv[4 * q + 3] = __uint_as_float(v.w);
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int row = warp * 16 + 8 * h + i;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const uint4 v = lds128(Wt + swz128(row, q));
-                        acc[i] = fmaf(__uint_as_float(v.x), xv[4 * q + 0], acc[i]);
-                        acc[i] = fmaf(__uint_as_float(v.y), xv[4 * q + 1], acc[i]);
-                        acc[i] = fmaf(__uint_as_float(v.z), xv[4 * q + 2], acc[i]);
-                        acc[i] = fmaf(__uint_as_float(v.w), xv[4 * q + 3], acc[i]);
-                    }
-                }
-            }
+            mma_kblock<WF, EPI>(Wt, Xt, Sb, a, warp, lane, acc);
             }   // k-blocks of the stage
         }
         __syncwarp();
@@ -401,211 +258,8 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
 
         if (!(k + len == a.kb || u == u1)) continue;
 
-        // ------------------------------------------ finish this tile
-        if (WF != WF_F32) {
-            // C fragment: (row g, tokens 2c,2c+1), (row g+8, tokens 2c,2c+1) per n8 tile
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int t0 = nt * 8 + 2 * c, r = warp * 16 + g;
-                ctile[(t0 + 0) * GEMM_BN + r] = acc[nt * 4 + 0];
-                ctile[(t0 + 1) * GEMM_BN + r] = acc[nt * 4 + 1];
-                ctile[(t0 + 0) * GEMM_BN + r + 8] = acc[nt * 4 + 2];
-                ctile[(t0 + 1) * GEMM_BN + r + 8] = acc[nt * 4 + 3];
-            }
-        } else {
-            const int t = lane & 15, h = lane >> 4;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ctile[t * GEMM_BN + warp * 16 + 8 * h + i] = acc[i];
-        }
-        consumer_bar();
-
-        const long long ts = (long long)tile * a.kb;
-        const int i_first = cta_of(ts, U, G), i_last = cta_of(ts + a.kb - 1, U, G);
-        const bool aborted = s_flags[0] != 0;
-        bool do_epi = !aborted;
-        if (i_first != i_last) {
-            const int slot = (tile == first_tile_of_me) ? 0 : 1;
-            float* mine = a.slots + ((size_t)blockIdx.x * 2 + slot) * (GEMM_BN * DFL_MAX_ROWS);
-            for (int e = tid; e < GEMM_BN * DFL_MAX_ROWS; e += GEMM_CONSUMERS * 32)
-                __stcg(mine + e, ctile[e]);
-            __threadfence();
-            consumer_bar();
-            if (tid == 0) {
-                int last = 0;
-                if (!aborted) {
-                    const int old = atomicAdd(&a.counters[tile], 1);
-                    last = (old == i_last - i_first);
-                }
-                s_flags[1] = last;
-            }
-            consumer_bar();
-            do_epi = s_flags[1] != 0;
-            if (do_epi) {
-                __threadfence();
-                if (tid == 0) a.counters[tile] = 0;
-                // Sum the parts in CTA order.  Each thread owns 8 consecutive
-                // elements (two float4) and issues the loads of four parts at
-                // a time, so the L2 round trips overlap.
-                const int e0 = tid * 8;
-                float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-                auto part_ptr = [&](int i) {
-                    const int first_i = (int)(range_start(i, U, G) / a.kb);
-                    const int si = (tile == first_i) ? 0 : 1;
-                    return a.slots + ((size_t)i * 2 + si) * (GEMM_BN * DFL_MAX_ROWS) + e0;
-                };
-                auto add4 = [](float4& x, const float4& y) {
-                    x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
-                };
-                int i = i_first;
-                for (; i + 3 <= i_last; i += 4) {
-                    const float4* p0 = reinterpret_cast<const float4*>(part_ptr(i));
-                    const float4* p1 = reinterpret_cast<const float4*>(part_ptr(i + 1));
-                    const float4* p2 = reinterpret_cast<const float4*>(part_ptr(i + 2));
-                    const float4* p3 = reinterpret_cast<const float4*>(part_ptr(i + 3));
-                    const float4 a0 = __ldcg(p0), b0 = __ldcg(p0 + 1);
-                    const float4 a1 = __ldcg(p1), b1 = __ldcg(p1 + 1);
-                    const float4 a2 = __ldcg(p2), b2 = __ldcg(p2 + 1);
-                    const float4 a3 = __ldcg(p3), b3 = __ldcg(p3 + 1);
-                    add4(acc0, a0); add4(acc1, b0);
-                    add4(acc0, a1); add4(acc1, b1);
-                    add4(acc0, a2); add4(acc1, b2);
-                    add4(acc0, a3); add4(acc1, b3);
-                }
-                for (; i <= i_last; ++i) {
-                    const float4* p0 = reinterpret_cast<const float4*>(part_ptr(i));
-                    add4(acc0, __ldcg(p0));
-                    add4(acc1, __ldcg(p0 + 1));
-                }
-                *reinterpret_cast<float4*>(ctile + e0) = acc0;
-                *reinterpret_cast<float4*>(ctile + e0 + 4) = acc1;
-                consumer_bar();
-            }
-        }
-
-        // Row scale of a folded RMSNorm: rstd[t] from the partial sums, summed
-        // in a fixed order (the same for every forward length).  Computed by
-        // all consumer threads, before the (barrier-free) epilogue.
-        if (EPI == EPI_SWIGLU || EPI == EPI_ARGMAX || EPI == EPI_QKV) {
-            if (tid < DFL_MAX_ROWS) {
-                float r = 1.f;
-                if (a.ssq_in) {
-                    float ss = 0.f;
-                    for (int p = 0; p < a.ssq_parts; ++p) ss += a.ssq_in[p * DFL_MAX_ROWS + tid];
-                    r = 1.0f / sqrtf(ss * a.inv_width + a.eps);
-                }
-                s_rstd[tid] = r;
-            }
-            consumer_bar();
-        }
-        if (do_epi) {
-            if (EPI == EPI_STORE) {
-                const int n0 = tile * GEMM_BN;
-                for (int e = tid; e < GEMM_BN * DFL_MAX_ROWS; e += GEMM_CONSUMERS * 32) {
-                    const int t = e / GEMM_BN, r = e % GEMM_BN;
-                    a.out[(size_t)t * a.ldo + n0 + r] = ctile[e];
-                }
-            } else if (EPI == EPI_RESID || EPI == EPI_NORMOUT) {
-                // warp w: tokens 2w, 2w+1; lane: 4 consecutive columns
-                const int n0 = tile * GEMM_BN;
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int t = warp * 2 + q;
-                    float ss = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int r = lane * 4 + i;
-                        float v = ctile[t * GEMM_BN + r];
-                        if (EPI == EPI_RESID) {
-                            const size_t o = (size_t)t * a.ldo + n0 + r;
-                            v += a.out[o];
-                            a.out[o] = v;
-                            if (a.tap_out) store_act(a.tap_out, a.tap_type, a.ld_tap, t, n0 + r, v);
-                        }
-                        ss = fmaf(v, v, ss);
-                        const float wn = a.w_next ? a.w_next[n0 + r] : 1.f;
-                        store_act(a.xn_out, a.xn_type, a.ldo, t, n0 + r, v * wn);
-                    }
-                    ss = warp_sum(ss);
-                    if (a.ssq_out && lane == 0) a.ssq_out[tile * DFL_MAX_ROWS + t] = ss;
-                }
-            } else if (EPI == EPI_SWIGLU) {
-                const int j0 = tile * 64;
-                for (int e = tid; e < 64 * DFL_MAX_ROWS; e += GEMM_CONSUMERS * 32) {
-                    const int t = e / 64, r = e % 64;
-                    const float gt = ctile[t * GEMM_BN + r] * s_rstd[t];
-                    const float up = ctile[t * GEMM_BN + 64 + r] * s_rstd[t];
-                    const float v = gt / (1.f + expf(-gt)) * up;
-                    store_act(a.act, a.act_type, a.ld_act, t, j0 + r, v);
-                }
-            } else if (EPI == EPI_QKV) {
-                // the tile is 128 / hd whole heads; item = (token, head in tile)
-                const QkvEpi& qe = a.qkv;
-                int r0;
-                const int nrows = rows_of(a.st, qe.row_sel, &r0);
-                const int hd = qe.hd, hpt = GEMM_BN / hd, per = hd / 32;
-                const int h_first = tile * hpt;
-                for (int item = warp; item < DFL_MAX_ROWS * hpt; item += GEMM_CONSUMERS) {
-                    const int t = item / hpt, hi = item % hpt;
-                    if (t < r0 || t >= r0 + nrows) continue;
-                    const int h = h_first + hi;
-                    const bool is_q = h < qe.n_q, is_k = !is_q && h < qe.n_q + qe.n_kv;
-                    float v[4];
-                    for (int m = 0; m < per; ++m)
-                        v[m] = ctile[t * GEMM_BN + hi * hd + lane + 32 * m] * s_rstd[t];
-                    if (is_q || is_k) {
-                        const float* nw = is_q ? qe.q_norm : qe.k_norm;
-                        float ss = 0.f;
-                        for (int m = 0; m < per; ++m) ss = fmaf(v[m], v[m], ss);
-                        ss = warp_sum(ss);
-                        const float inv = 1.0f / sqrtf(ss / (float)hd + a.eps);
-                        for (int m = 0; m < per; ++m) v[m] = v[m] * inv * nw[lane + 32 * m];
-                        // rotate-half: element i pairs with i + hd/2 (same lane, m + per/2)
-                        const float* cs = qe.rope_cos + t * (hd / 2);
-                        const float* sn = qe.rope_sin + t * (hd / 2);
-                        float rr[4];
-                        for (int m = 0; m < per / 2; ++m) {
-                            const int i = lane + 32 * m;
-                            rr[m] = v[m] * cs[i] - v[m + per / 2] * sn[i];
-                            rr[m + per / 2] = v[m + per / 2] * cs[i] + v[m] * sn[i];
-                        }
-                        for (int m = 0; m < per; ++m) v[m] = rr[m];
-                    }
-                    if (is_q) {
-                        const size_t base = ((size_t)h * DFL_MAX_ROWS + t) * hd;   // [n_q][16][hd]
-                        for (int m = 0; m < per; ++m) store_xt(qe.q_out, qe.q_type, base + lane + 32 * m, v[m]);
-                        continue;
-                    }
-                    const int pos = a.st->fwd_pos0 + t;
-                    if (pos < 0 || pos >= qe.max_seq) {
-                        if (lane == 0) set_error(a.st, DERR_INDEX, pos);
-                        continue;
-                    }
-                    const int kh = is_k ? h - qe.n_q : h - qe.n_q - qe.n_kv;
-                    void* cache = is_k ? qe.k_cache : qe.v_cache;
-                    const size_t base = ((size_t)kh * qe.cap + pos) * hd;
-                    for (int m = 0; m < per; ++m) store_xt(cache, qe.c_type, base + lane + 32 * m, v[m]);
-                }
-            } else {  // EPI_ARGMAX: warp w reduces tokens 2w, 2w+1
-                const int n0 = tile * GEMM_BN;
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int t = warp * 2 + q;
-                    unsigned long long best = 0ull;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int r = lane * 4 + i;
-                        const float v = ctile[t * GEMM_BN + r] * s_rstd[t];
-                        best = umax64(best, argmax_key(v, n0 + r));
-                        if (a.logits) a.logits[(size_t)t * a.ldl + n0 + r] = v;
-                    }
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1)
-                        best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
-                    if (lane == 0) atomicMax(a.amax + t, best);
-                }
-            }
-        }
-        consumer_bar();   // ctile is rewritten by the next tile
+        finish_tile<WF, EPI>(a, tile, acc, ctile, s_flags, s_rstd, U, G, blockIdx.x,
+                             first_tile_of_me, warp, lane, tid);
     }
 }
 

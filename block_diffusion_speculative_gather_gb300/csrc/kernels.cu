@@ -7,8 +7,7 @@
 // state, so a round needs no host round-trip; rows beyond the forward's
 // count are written as zeros, which keeps every padded GEMM column zero.
 
-#include "gemm.cuh"
-#include "kernels.cuh"
+#include "kernels_dev.cuh"
 
 namespace dfl {
 
@@ -24,93 +23,21 @@ __device__ __forceinline__ float ld_any(const void* base, int t, size_t i) {
 
 // One CTA: sets the forward descriptor (thread 0), then every CTA gathers
 // its row of the embedding into the fp32 residual and fills the RoPE table.
+struct BlockBar {
+    __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
+// One CTA per row (see kdev::prepare_row).
 __global__ void prepare_rows_kernel(RowsArgs a) {
     pdl_trigger();
     pdl_wait();
-    DevState* st = a.st;
-    __shared__ int s_T, s_pos0, s_tok;
-    const int t = blockIdx.x;   // row
-    if (threadIdx.x == 0) {
-        int T = 0, pos0 = 0;
-        if (a.mode == FWD_PREFILL) {
-            T = a.T;
-            pos0 = a.pos0;
-        } else if (!st->finished) {
-            pos0 = st->n;
-            if (a.mode == FWD_DRAFT) T = st->bl > 1 ? st->bl : 0;
-            else if (a.mode == FWD_VERIFY) T = st->bl;
-            else T = 1;   // FWD_GREEDY
-        }
-        int tok = 0;
-        if (t < T) {
-            if (a.mode == FWD_PREFILL) tok = a.tokens ? a.tokens[pos0 + t] : 0;
-            else if (t == 0) tok = st->t_n;
-            else if (a.mode == FWD_DRAFT) tok = a.mask_id;
-            else tok = a.tokens[t - 1];
-            if (tok < 0 || tok >= a.vocab) {
-                set_error(st, DERR_TOKEN, tok);
-                tok = 0;
-            }
-        }
-        s_T = T;
-        s_pos0 = pos0;
-        s_tok = tok;
-        if (t == 0) {
-            st->fwd_T = T;
-            st->fwd_pos0 = pos0;
-            st->fwd_commit = 0;
-            st->fwd_commit_r0 = 0;
-            if (a.mode == FWD_DRAFT) st->draft_bl = T;
-        }
-        if (a.amax) a.amax[t] = 0ull;
-    }
-    __syncthreads();
-    const int T = s_T;
-    float* xr = a.x + (size_t)t * a.hidden;
-    if (t < T && a.embed) {
-        for (int i = threadIdx.x; i < a.hidden; i += blockDim.x) {
-            const size_t e = (size_t)s_tok * a.hidden + i;
-            xr[i] = a.embed_f32 ? reinterpret_cast<const float*>(a.embed)[e]
-                                : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.embed)[e]);
-        }
-    } else if (a.embed) {
-        for (int i = threadIdx.x; i < a.hidden; i += blockDim.x) xr[i] = 0.f;
-    }
-    if (a.embed) {
-        // folded RMSNorm input of layer 0: xn = x * w0, per-128-column sums of x^2
-        __syncthreads();
-        for (int i = threadIdx.x; i < a.hidden; i += blockDim.x)
-            store_act(a.xn, a.xn_type, a.hidden, t, i, xr[i] * a.w0[i]);
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        for (int b = warp; b < a.hidden / 128; b += blockDim.x >> 5) {
-            float ss = 0.f;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float v = xr[b * 128 + lane * 4 + j];
-                ss = fmaf(v, v, ss);
-            }
-            ss = warp_sum(ss);
-            if (lane == 0) a.ssq[b * DFL_MAX_ROWS + t] = ss;
-        }
-    }
-    const int half = a.head_dim / 2;
-    for (int i = threadIdx.x; i < half; i += blockDim.x) {
-        // angle = pos * theta^(-2i/d), in double, rounded once to fp32
-        const double inv = pow((double)a.rope_theta, -2.0 * (double)i / (double)a.head_dim);
-        const double ang = (double)(s_pos0 + t) * inv;
-        a.rope_cos[t * half + i] = (float)cos(ang);
-        a.rope_sin[t * half + i] = (float)sin(ang);
-    }
+    __shared__ int sh[3];
+    kdev::prepare_row(a, blockIdx.x, threadIdx.x, blockDim.x, sh, BlockBar());
 }
 
 // --------------------------------------------------------------- attention
 
-__device__ __forceinline__ void attn_range(const AttnArgs& a, int* lo, int* hi, int* T, int* pos0) {
-    *T = a.st->fwd_T;
-    *pos0 = a.st->fwd_pos0;
-    *hi = *pos0 + *T;
-    *lo = (!a.causal && a.window > 0) ? max(0, *pos0 - a.window) : 0;
-}
+using kdev::attn_range;
 
 // One CTA per (kv head, chunk of ATTN_CHUNK keys): partial softmax state
 // (max m, sum l, unnormalised output o) of every query row of the kv head's
@@ -185,64 +112,15 @@ __global__ void attn_partial_kernel(AttnArgs a) {
     }
 }
 
-// Folds the chunks of one (row, q head) in chunk order and normalises.  The
-// chunk maxima and sums are staged in shared memory by all threads at once;
-// every thread then folds its output element over the chunks in chunk
-// order (fully masked chunks add exact zeros at the end, so a row's result
-// does not depend on the forward's row count).
+// One CTA per (q head, row) (see kdev::combine_item).
 template <int HD>
 __global__ void attn_combine_kernel(AttnArgs a) {
     pdl_trigger();
     pdl_wait();
-    constexpr int MAXC = 512;
-    __shared__ float s_w[MAXC];
-    __shared__ float s_l[MAXC];
+    __shared__ float s_w[kdev::COMBINE_MAXC];
+    __shared__ float s_l[kdev::COMBINE_MAXC];
     __shared__ float s_red[HD / 32];
-    const int hq = blockIdx.x, t = blockIdx.y, d = threadIdx.x;
-    int lo, hi, T, pos0;
-    attn_range(a, &lo, &hi, &T, &pos0);
-    const size_t ld = (size_t)a.n_q * HD, col = (size_t)hq * HD + d;
-    if (t >= T) {
-        store_act(a.out, a.out_type, ld, t, col, 0.f);
-        return;
-    }
-    const int c_lo = lo / ATTN_CHUNK, c_hi = (hi - 1) / ATTN_CHUNK;
-    const int nc = c_hi - c_lo + 1;
-    const size_t cstride = (size_t)DFL_MAX_ROWS * a.n_q * (HD + 2);
-    const float* base = a.part + ((size_t)c_lo * DFL_MAX_ROWS + t) * a.n_q * (HD + 2) +
-                        (size_t)hq * (HD + 2);
-    if (nc > MAXC) {
-        if (d == 0) set_error(a.st, DERR_INDEX, nc);
-        return;
-    }
-    float mx = -INFINITY;
-    for (int i = d; i < nc; i += HD) {
-        const float m = base[i * cstride];
-        s_w[i] = m;
-        s_l[i] = base[i * cstride + 1];
-        mx = fmaxf(mx, m);
-    }
-    mx = warp_max(mx);
-    if ((d & 31) == 0) s_red[d >> 5] = mx;
-    __syncthreads();
-    float M = s_red[0];
-#pragma unroll
-    for (int w = 1; w < HD / 32; ++w) M = fmaxf(M, s_red[w]);
-    for (int i = d; i < nc; i += HD) s_w[i] = (s_w[i] == -INFINITY) ? 0.f : expf(s_w[i] - M);
-    __syncthreads();
-    float L = 0.f, O = 0.f;
-    int i = 0;
-    for (; i + 4 <= nc; i += 4) {
-        const float o0 = base[(i + 0) * cstride + 2 + d], o1 = base[(i + 1) * cstride + 2 + d];
-        const float o2 = base[(i + 2) * cstride + 2 + d], o3 = base[(i + 3) * cstride + 2 + d];
-        O = fmaf(o0, s_w[i + 0], O);
-        O = fmaf(o1, s_w[i + 1], O);
-        O = fmaf(o2, s_w[i + 2], O);
-        O = fmaf(o3, s_w[i + 3], O);
-    }
-    for (; i < nc; ++i) O = fmaf(base[i * cstride + 2 + d], s_w[i], O);
-    for (int j = 0; j < nc; ++j) L = fmaf(s_l[j], s_w[j], L);
-    store_act(a.out, a.out_type, ld, t, col, O / L);
+    kdev::combine_item<HD>(a, blockIdx.x, blockIdx.y, threadIdx.x, s_w, s_l, s_red, BlockBar());
 }
 
 // --------------------------------------------------------------- acceptance
@@ -250,69 +128,7 @@ __global__ void attn_combine_kernel(AttnArgs a) {
 __global__ void accept_kernel(AcceptArgs a) {
     pdl_trigger();
     pdl_wait();
-    if (threadIdx.x != 0) return;
-    DevState* st = a.st;
-    const int T = st->fwd_T;
-    int y[DFL_MAX_ROWS];
-    for (int i = 0; i < DFL_MAX_ROWS; ++i) y[i] = argmax_key_index(a.amax[i]);
-    if (a.mode == FWD_DRAFT) {
-        for (int j = 0; j < a.block_max - 1; ++j)
-            a.draft_out[j] = (j + 1 < T) ? y[j + 1] : -1;
-        return;
-    }
-    const int B = a.block_max;
-    if (a.mode == FWD_PREFILL) {
-        st->t_n = y[T - 1];
-        st->n = a.prompt_len;
-        st->generated = 1;
-        st->max_new = a.max_new;
-        st->ctx_len = a.prompt_len;
-        st->rounds = 0;
-        st->emitted = 0;
-        for (int j = 0; j < 16; ++j) st->accept_hist[j] = 0;
-        st->last_a = 0;
-        st->finished = (a.eos_id >= 0 && st->t_n == a.eos_id) || a.max_new <= 1 ||
-                       st->n >= a.max_seq;
-        const int bl = min(B, min(a.max_new - 1, a.max_seq - st->n));
-        st->bl = st->finished ? 0 : bl;
-        return;
-    }
-    // VERIFY / GREEDY
-    if (T == 0) {
-        *a.n_emitted = 0;
-        for (int j = 0; j < B; ++j) a.tokens_out[j] = -1;
-        st->fwd_commit = 0;
-        return;
-    }
-    int acc = 0;
-    if (a.mode == FWD_VERIFY)
-        while (acc < T - 1 && a.draft_ids[acc] == y[acc]) ++acc;
-    int emit = acc + 1;
-    int fin = 0;
-    if (a.eos_id >= 0) {
-        for (int i = 0; i <= acc; ++i)
-            if (y[i] == a.eos_id) {
-                emit = i + 1;
-                fin = 1;
-                break;
-            }
-    }
-    for (int j = 0; j < B; ++j) a.tokens_out[j] = j < emit ? y[j] : -1;
-    *a.n_emitted = emit;
-    const int n_old = st->n;
-    st->n = n_old + emit;
-    st->t_n = y[emit - 1];
-    st->generated += emit;
-    st->ctx_len = st->n;
-    st->rounds += 1;
-    st->emitted += emit;
-    for (int j = 0; j < acc && j < 16; ++j) st->accept_hist[j] += 1;
-    st->last_a = acc;
-    fin |= st->generated >= st->max_new || st->n >= a.max_seq;
-    st->finished = fin;
-    st->bl = fin ? 0 : min(B, min(st->max_new - st->generated, a.max_seq - st->n));
-    st->fwd_commit_r0 = 0;
-    st->fwd_commit = emit;
+    if (threadIdx.x == 0) kdev::accept_run(a);
 }
 
 __global__ void set_chunk_kernel(DevState* st, int pos0, int T, int commit_lo) {
