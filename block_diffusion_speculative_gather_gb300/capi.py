@@ -99,6 +99,7 @@ def _load() -> C.CDLL:
         "dflash_linear_workspace_bytes": (sz, [i32, i32]),
         "dflash_linear": (C.c_int, [vp, vp, i32, i32, vp, vp, sz, vp]),
         "dflash_linear_noalloc": (C.c_int, [vp, vp, i32, i32, vp, vp]),
+        "dflash_profile_phases": (i32, [vp, i32, vp, i32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -115,7 +116,7 @@ EXPORTED = ("dflash_workspace_bytes", "dflash_kv_target_bytes", "dflash_kv_draft
             "dflash_destroy", "dflash_last_error", "dflash_tap_reduce",
             "dflash_quantize_int4g64", "dflash_profile", "dflash_launch_count",
             "dflash_selftest_timeout", "dflash_adopt_kv", "dflash_linear_workspace_bytes",
-            "dflash_linear", "dflash_linear_noalloc")
+            "dflash_linear", "dflash_linear_noalloc", "dflash_profile_phases")
 
 
 def check(rc: int) -> None:
@@ -236,3 +237,19 @@ def dflash_linear_noalloc(w, x, y, stream=None):
     of a caller workspace (for callers that cannot allocate device memory)."""
     n, k = w.shape
     check(lib.dflash_linear_noalloc(_ptr(w), _ptr(x), n, k, _ptr(y), _stream(stream)))
+
+
+def dflash_profile_phases(ctx, which: int):
+    """Start times (ns) of every phase of persistent program `which` (0 draft,
+    1 verify, 2 greedy) from its last profiled launch, plus the end time;
+    [] when the program is not in use."""
+    n = lib.dflash_profile_phases(ctx, which, None, 0)
+    if n < 0:
+        check(n)
+    if n == 0:
+        return []
+    buf = (C.c_uint64 * n)()
+    rc = lib.dflash_profile_phases(ctx, which, buf, n)
+    if rc < 0:
+        check(rc)
+    return list(buf)

@@ -225,7 +225,6 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     int stage = 0;
     uint32_t phase = 0;
     float acc[8];
-    int first_tile_of_me = (int)(u0 / a.kb);
 
     for (long long u = u0; u < u1;) {
         const int len = chunk_len(u);
@@ -258,8 +257,8 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
 
         if (!(k + len == a.kb || u == u1)) continue;
 
-        finish_tile<WF, EPI>(a, tile, acc, ctile, s_flags, s_rstd, U, G, blockIdx.x,
-                             first_tile_of_me, warp, lane, tid);
+        finish_tile<WF, EPI>(a, tile, acc, ctile, s_flags, s_rstd, U, G, blockIdx.x, warp, lane,
+                             tid);
     }
 }
 

@@ -38,6 +38,16 @@ __device__ __forceinline__ void store_xt(void* base, int xt, size_t idx, float v
     else store_as<__half>(base, idx, v);
 }
 
+__device__ __forceinline__ int ld_acquire_s32(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_add_s32(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
     return a > b ? a : b;
 }
@@ -188,14 +198,17 @@ __device__ __forceinline__ void mma_kblock(const uint8_t* Wt, const uint8_t* Xt,
     }
 }
 
-// Finish of a tile whose last k-block this CTA has just accumulated:
-// partial tiles of a split reduction go to this CTA's slot, the last CTA to
-// take the tile's ticket sums the parts in CTA order and runs the epilogue.
+// Finish of a tile whose last k-block this CTA has just accumulated.  A
+// tile split across CTAs is finished by its owner, the first CTA of the
+// split (it reaches the tile at the end of its range): the other CTAs
+// publish their parts and go on; the owner sums the parts in CTA order and
+// runs the epilogue, so a row's result never depends on timing or on the
+// other rows.
 template <int WF, int EPI>
 __device__ __forceinline__ void finish_tile(const GemmArgs& a, int tile, const float (&acc)[8],
                                             float* ctile, volatile int* s_flags, float* s_rstd,
-                                            long long U, int G, int cta, int first_tile_of_me,
-                                            int warp, int lane, int tid) {
+                                            long long U, int G, int cta, int warp, int lane,
+                                            int tid) {
     const int g = lane >> 2, c = lane & 3;
     // ------------------------------------------ finish this tile
     if (WF != WF_F32) {
@@ -219,45 +232,58 @@ __device__ __forceinline__ void finish_tile(const GemmArgs& a, int tile, const f
     const int i_first = cta_of(ts, U, G), i_last = cta_of(ts + a.kb - 1, U, G);
     const bool aborted = s_flags[0] != 0;
     bool do_epi = !aborted;
-    if (i_first != i_last) {
-        const int slot = (tile == first_tile_of_me) ? 0 : 1;
-        float* mine = a.slots + ((size_t)cta * 2 + slot) * (GEMM_BN * DFL_MAX_ROWS);
+    if (i_first != i_last && cta != i_first) {
+        // A later part of a split tile: the tile was this CTA's first, so its
+        // part goes to this CTA's slot; the tile's owner, CTA i_first (whose
+        // range ends in the tile, so it reaches the tile last), is told
+        // through the tile's counter and nothing here waits.
+        float* mine = a.slots + (size_t)cta * 2 * (GEMM_BN * DFL_MAX_ROWS);
         for (int e = tid; e < GEMM_BN * DFL_MAX_ROWS; e += GEMM_CONSUMERS * 32)
             __stcg(mine + e, ctile[e]);
         __threadfence();
         consumer_bar();
+        if (tid == 0) red_release_add_s32(&a.counters[tile], 1);
+        do_epi = false;
+    } else if (i_first != i_last) {
+        // The owner: wait (bounded) until the other parts are published,
+        // then sum all parts in CTA order, its own (still in ctile) first.
         if (tid == 0) {
-            int last = 0;
-            if (!aborted) {
-                const int old = atomicAdd(&a.counters[tile], 1);
-                last = (old == i_last - i_first);
+            const int need = i_last - i_first;
+            bool ok = ld_acquire_s32(&a.counters[tile]) >= need;
+            if (!ok && !aborted) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!(ok = ld_acquire_s32(&a.counters[tile]) >= need)) {
+                    if (globaltimer_ns() - t0 > 2000000000ull) {
+                        set_error(a.st, DERR_TIMEOUT, 105);
+                        break;
+                    }
+                }
             }
-            s_flags[1] = last;
+            if (ok) a.counters[tile] = 0;   // ready for the next launch
+            s_flags[1] = ok ? 1 : 0;
         }
         consumer_bar();
-        do_epi = s_flags[1] != 0;
+        do_epi = !aborted && s_flags[1] != 0;
         if (do_epi) {
             __threadfence();
-            if (tid == 0) a.counters[tile] = 0;
-            // Sum the parts in CTA order.  Each thread owns 8 consecutive
-            // elements (two float4) and issues the loads of four parts at
-            // a time, so the L2 round trips overlap.
+            // Each thread owns 8 consecutive elements (two float4) and issues
+            // the loads of four parts at a time, so the L2 round trips overlap.
             const int e0 = tid * 8;
-            float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+            float4 acc0 = *reinterpret_cast<const float4*>(ctile + e0);
+            float4 acc1 = *reinterpret_cast<const float4*>(ctile + e0 + 4);
             auto part_ptr = [&](int i) {
-                const int first_i = (int)(range_start(i, U, G) / a.kb);
-                const int si = (tile == first_i) ? 0 : 1;
-                return a.slots + ((size_t)i * 2 + si) * (GEMM_BN * DFL_MAX_ROWS) + e0;
+                return reinterpret_cast<const float4*>(
+                    a.slots + (size_t)i * 2 * (GEMM_BN * DFL_MAX_ROWS) + e0);
             };
             auto add4 = [](float4& x, const float4& y) {
                 x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
             };
-            int i = i_first;
+            int i = i_first + 1;
             for (; i + 3 <= i_last; i += 4) {
-                const float4* p0 = reinterpret_cast<const float4*>(part_ptr(i));
-                const float4* p1 = reinterpret_cast<const float4*>(part_ptr(i + 1));
-                const float4* p2 = reinterpret_cast<const float4*>(part_ptr(i + 2));
-                const float4* p3 = reinterpret_cast<const float4*>(part_ptr(i + 3));
+                const float4* p0 = part_ptr(i);
+                const float4* p1 = part_ptr(i + 1);
+                const float4* p2 = part_ptr(i + 2);
+                const float4* p3 = part_ptr(i + 3);
                 const float4 a0 = __ldcg(p0), b0 = __ldcg(p0 + 1);
                 const float4 a1 = __ldcg(p1), b1 = __ldcg(p1 + 1);
                 const float4 a2 = __ldcg(p2), b2 = __ldcg(p2 + 1);
@@ -268,11 +294,11 @@ __device__ __forceinline__ void finish_tile(const GemmArgs& a, int tile, const f
                 add4(acc0, a3); add4(acc1, b3);
             }
             for (; i <= i_last; ++i) {
-                const float4* p0 = reinterpret_cast<const float4*>(part_ptr(i));
+                const float4* p0 = part_ptr(i);
                 add4(acc0, __ldcg(p0));
                 add4(acc1, __ldcg(p0 + 1));
             }
-            *reinterpret_cast<float4*>(ctile + e0) = acc0;
+            *reinterpret_cast<float4*>(ctile + e0) = acc0;   // its own elements only
             *reinterpret_cast<float4*>(ctile + e0 + 4) = acc1;
             consumer_bar();
         }

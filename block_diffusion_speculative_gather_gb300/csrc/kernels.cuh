@@ -21,6 +21,7 @@ struct RowsArgs {
     float* rope_sin;
     int head_dim;
     float rope_theta;
+    const double* inv_freq;      // [head_dim/2] theta^(-2i/head_dim)
     unsigned long long* amax;    // [16] reset to 0
     // folded input norm of the first layer: xn = x * w0 and partial sums of x^2
     const float* w0;             // [hidden] ln_attn of layer 0 of the model that runs

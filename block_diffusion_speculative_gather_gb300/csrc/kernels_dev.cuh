@@ -92,11 +92,15 @@ __device__ __forceinline__ void prepare_row(const RowsArgs& a, int t, int tid, i
     }
     const int half = a.head_dim / 2;
     for (int i = tid; i < half; i += nthr) {
-        // angle = pos * theta^(-2i/d), in double, rounded once to fp32
-        const double inv = pow((double)a.rope_theta, -2.0 * (double)i / (double)a.head_dim);
-        const double ang = (double)(sh[1] + t) * inv;
-        a.rope_cos[t * half + i] = (float)cos(ang);
-        a.rope_sin[t * half + i] = (float)sin(ang);
+        // angle = pos * theta^(-2i/d) in double (the frequencies come from a
+        // table made on the host), reduced to [-pi, pi] with a two-part 2 pi,
+        // then cos / sin in double, rounded once to fp32
+        const double ang = (double)(sh[1] + t) * a.inv_freq[i];
+        const double k = rint(ang * 0.15915494309189535);          // 1 / (2 pi)
+        double r = fma(-k, 6.283185307179586, ang);                // 2 pi, high part
+        r = fma(-k, 2.4492935982947064e-16, r);                    // 2 pi, low part
+        a.rope_cos[t * half + i] = (float)cos(r);
+        a.rope_sin[t * half + i] = (float)sin(r);
     }
 }
 

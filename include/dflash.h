@@ -229,6 +229,17 @@ int dflash_check(dflash_ctx* ctx, dflash_stream_t stream);
 int dflash_selftest_timeout(dflash_ctx* ctx, int64_t limit_ns, dflash_stream_t stream);
 
 /*
+ * Profiling helper of the persistent round kernel: the device start times
+ * (ns, %globaltimer) of every phase of program `which` (0 draft, 1 verify,
+ * 2 greedy one-row step) recorded by its last launch made with profiling on
+ * (dflash_profile mode 1), plus the end time: up to `cap` values into ns
+ * (host).  Returns the number of values the program has (phases + 1), 0 if
+ * the program is not in use, or a negative DFLASH_ERR_*.  Synchronises the
+ * device.
+ */
+int32_t dflash_profile_phases(dflash_ctx* ctx, int32_t which, uint64_t* ns, int32_t cap);
+
+/*
  * Parity taps: while set (non-NULL), every target LM head (verify, and the
  * last prefill chunk) writes its fp32 logits [16][vocab] to verify_logits
  * (row i = forward row i) and every draft writes [16][vocab] to draft_logits
