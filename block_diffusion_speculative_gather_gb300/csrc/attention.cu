@@ -16,10 +16,21 @@
 // has (batch invariance) or on the chunks past its own causal limit.
 
 #include "attention_dev.cuh"
+#include "gemm.cuh"
 
 namespace dfl {
 
 namespace {
+
+__device__ __forceinline__ int ld_acquire_s32_(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_add_s32_(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 template <int HD>
 __global__ void __launch_bounds__(128)
@@ -76,6 +87,221 @@ attn_mma_kernel(const __grid_constant__ AttnMaps maps, const AttnMmaArgs a) {
     adev::chunk_partials<HD>(Qs, Ks, Vs, a, qrows, group, kh, c, T, pos0, lo, hi, warp, lane);
 }
 
+
+// Shared memory of the fused kernel: the q group, two K/V chunk buffers,
+// the split maxima / sums staged for the combine, mbarriers.
+template <int HD>
+constexpr size_t fused_smem(int qrows) {
+    return 1024 + (size_t)(HD / 64) * (qrows + 4 * ATTN_KEYS) * 128 + 2 * (16 * DFL_MAX_ROWS + 64) * 4 +
+           3 * 8 + 64;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(128)
+attn_fused_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) {
+    constexpr int C = ATTN_KEYS, HALVES = HD / 64;
+    constexpr int MAXS = 64;   // splits a combine folds (host guarantees max_splits <= 64)
+    constexpr int MAXP = 16 * DFL_MAX_ROWS;   // (q head, row) pairs of a group of <= 16 heads
+    constexpr int ENT = MAXP + MAXS;          // staged (pair, split) entries of one CTA
+    const AttnMmaArgs& a = f.m;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int group = a.n_q / a.n_kv, qrows = group * 16;
+    uint8_t* Qs = sm;                                   // [HALVES][qrows][128 B]
+    uint8_t* KV = Qs + HALVES * qrows * 128;            // 2 x (K, V) [HALVES][64][128 B]
+    constexpr int KVB = HALVES * C * 128;               // bytes of one K (or V) chunk
+    float* s_m = reinterpret_cast<float*>(KV + 4 * KVB);   // [ENT]
+    float* s_l = s_m + ENT;                                 // [ENT]
+    uint64_t* bar = reinterpret_cast<uint64_t*>(s_l + ENT);   // [0] q, [1..2] buffers
+
+    pdl_trigger();
+    pdl_wait();
+    const int kh = blockIdx.x, sp = blockIdx.y, tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int T = a.st->fwd_T, pos0 = a.st->fwd_pos0;
+    if (T == 0) return;
+    const int hi = pos0 + T;
+    const int lo = (!a.causal && a.window > 0) ? max(0, pos0 - a.window) : 0;
+    const int c_lo = lo / C, c_hi = (hi - 1) / C;
+    const int S = (c_hi - c_lo + f.split_chunks) / f.split_chunks;   // splits in use
+    if (sp >= S) return;
+    if (S > MAXS || S > f.max_splits) {
+        if (tid == 0) set_error(a.st, DERR_INDEX, S);
+        return;
+    }
+    const int c0 = c_lo + sp * f.split_chunks;
+    const int n_my = min(f.split_chunks, c_hi + 1 - c0);
+
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    auto load_chunk = [&](int i) {   // chunk c0 + i into buffer i & 1
+        uint8_t* Kb = KV + (i & 1) * 2 * KVB;
+        uint8_t* Vb = Kb + KVB;
+        const int c = c0 + i;
+        const int krow = ((a.layer * 2 + 0) * a.n_kv + kh) * a.cap + c * C;
+        const int vrow = ((a.layer * 2 + 1) * a.n_kv + kh) * a.cap + c * C;
+        mbar_arrive_expect_tx(&bar[1 + (i & 1)], 2 * KVB);
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h) {
+            tma_load_2d(Kb + h * C * 128, &maps.kv, &bar[1 + (i & 1)], 64 * h, krow);
+            tma_load_2d(Vb + h * C * 128, &maps.kv, &bar[1 + (i & 1)], 64 * h, vrow);
+        }
+    };
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar[0], HALVES * qrows * 128);
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h)
+            tma_load_2d(Qs + h * qrows * 128, &maps.q, &bar[0], 64 * h, kh * qrows);
+        load_chunk(0);
+        if (n_my > 1) load_chunk(1);
+    }
+    // every wait is voted on by the whole CTA, so all threads leave together
+    bool ok = __syncthreads_and(mbar_wait_bounded(&bar[0], 0)) != 0;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    float o[HD / 8][4];
+#pragma unroll
+    for (int dt = 0; dt < HD / 8; ++dt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[dt][e] = 0.f;
+    int issued = n_my > 1 ? 2 : 1;
+    for (int i = 0; i < n_my && ok; ++i) {
+        ok = __syncthreads_and(mbar_wait_bounded(&bar[1 + (i & 1)], (uint32_t)((i >> 1) & 1))) != 0;
+        if (ok && warp < group)
+            adev::chunk_online<HD>(Qs, KV + (i & 1) * 2 * KVB, KV + (i & 1) * 2 * KVB + KVB, a,
+                                   qrows, c0 + i, T, pos0, lo, hi, warp, lane, m, l, o);
+        __syncthreads();   // buffer i & 1 is free again
+        if (ok && tid == 0 && i + 2 < n_my) {
+            load_chunk(i + 2);
+            ++issued;
+        }
+    }
+    if (!ok) {
+        if (tid == 0) {
+            set_error(a.st, DERR_TIMEOUT, 210);
+            // let copies still in flight land before the CTA exits
+            mbar_wait_bounded(&bar[0], 0, 100000000ull);
+            for (int i = 0; i < issued; ++i)
+                mbar_wait_bounded(&bar[1 + (i & 1)], (uint32_t)((i >> 1) & 1), 100000000ull);
+        }
+        return;
+    }
+
+    // ---- publish this split's (max, sum, output) of rows t = g, g + 8
+    if (warp < group) {
+        const int g = lane >> 2, cq = lane & 3, hq = kh * group + warp;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int t = g + 8 * r;
+            float* dst = a.part + (((size_t)sp * DFL_MAX_ROWS + t) * a.n_q + hq) * (HD + 2);
+            if (cq == 0) {
+                dst[0] = m[r];
+                dst[1] = l[r];
+            }
+#pragma unroll
+            for (int dt = 0; dt < HD / 8; ++dt) {
+                dst[2 + dt * 8 + 2 * cq] = o[dt][2 * r];
+                dst[2 + dt * 8 + 2 * cq + 1] = o[dt][2 * r + 1];
+            }
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    __shared__ int s_ok;
+    if (tid == 0) {
+        red_release_add_s32_(&f.arrive[kh], 1);
+        bool got = ld_acquire_s32_(&f.arrive[kh]) >= S;
+        const uint64_t t0 = globaltimer_ns();
+        while (!got) {
+            got = ld_acquire_s32_(&f.arrive[kh]) >= S;
+            if (!got && globaltimer_ns() - t0 > 2000000000ull) {
+                set_error(a.st, DERR_TIMEOUT, 211);
+                break;
+            }
+        }
+        s_ok = got ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_ok) return;
+    __threadfence();
+
+    // ---- combine: pairs (q head of the group, row) p = sp, sp + S, ...
+    // Stage the splits' maxima and sums of all this CTA's pairs, turn them
+    // into weights w = exp(m - M) and per-pair sums L (split order), then
+    // every output element folds the splits in split order.
+    const int pairs = group * DFL_MAX_ROWS;
+    const int my_pairs = (pairs - sp + S - 1) / S;    // my_pairs * S < pairs + S <= ENT
+    float* s_w = s_m;                                 // weights overwrite the maxima
+    __shared__ float s_M[MAXP], s_L[MAXP];
+    auto pair_of = [&](int pi, int* hq, int* t) {
+        const int p = sp + pi * S;
+        *hq = kh * group + p / DFL_MAX_ROWS;
+        *t = p % DFL_MAX_ROWS;
+    };
+    for (int e = tid; e < my_pairs * S; e += blockDim.x) {
+        int hq, t;
+        pair_of(e / S, &hq, &t);
+        const float* src = a.part + (((size_t)(e % S) * DFL_MAX_ROWS + t) * a.n_q + hq) * (HD + 2);
+        s_m[e] = src[0];
+        s_l[e] = src[1];
+    }
+    __syncthreads();
+    for (int pi = tid; pi < my_pairs; pi += blockDim.x) {
+        float M = -INFINITY;
+        for (int j = 0; j < S; ++j) M = fmaxf(M, s_m[pi * S + j]);
+        s_M[pi] = M;
+    }
+    __syncthreads();
+    for (int e = tid; e < my_pairs * S; e += blockDim.x) {
+        const float mj = s_m[e];
+        s_w[e] = mj == -INFINITY ? 0.f : expf(mj - s_M[e / S]);
+    }
+    __syncthreads();
+    for (int pi = tid; pi < my_pairs; pi += blockDim.x) {
+        float L = 0.f;
+        for (int j = 0; j < S; ++j) L = fmaf(s_l[pi * S + j], s_w[pi * S + j], L);
+        s_L[pi] = L;
+    }
+    __syncthreads();
+    const size_t sstride = (size_t)DFL_MAX_ROWS * a.n_q * (HD + 2);
+    const size_t ld = (size_t)a.n_q * HD;
+    for (int e = tid; e < my_pairs * HD; e += blockDim.x) {
+        const int pi = e / HD, d = e % HD;
+        int hq, t;
+        pair_of(pi, &hq, &t);
+        const size_t col = (size_t)hq * HD + d;
+        if (t >= T) {
+            store_act(f.out, f.out_type, ld, t, col, 0.f);
+            continue;
+        }
+        const float* src = a.part + ((size_t)t * a.n_q + hq) * (HD + 2) + 2 + d;
+        const float* w = s_w + pi * S;
+        float O = 0.f;
+        int j = 0;
+        for (; j + 4 <= S; j += 4) {
+            const float o0 = src[(j + 0) * sstride], o1 = src[(j + 1) * sstride];
+            const float o2 = src[(j + 2) * sstride], o3 = src[(j + 3) * sstride];
+            O = fmaf(o0, w[j + 0], O);
+            O = fmaf(o1, w[j + 1], O);
+            O = fmaf(o2, w[j + 2], O);
+            O = fmaf(o3, w[j + 3], O);
+        }
+        for (; j < S; ++j) O = fmaf(src[j * sstride], w[j], O);
+        store_act(f.out, f.out_type, ld, t, col, O / s_L[pi]);
+    }
+    // the last split of the head to finish resets the head's counters
+    if (tid == 0) {
+        const int old = atomicAdd(&f.done[kh], 1);
+        if (old == S - 1) {
+            f.arrive[kh] = 0;
+            f.done[kh] = 0;
+        }
+    }
+}
+
 }  // namespace
 
 int launch_attention_mma(const AttnMaps& maps, const AttnMmaArgs& a, int max_chunks,
@@ -104,6 +330,43 @@ int launch_attention_mma(const AttnMaps& maps, const AttnMmaArgs& a, int max_chu
         return (int)launch_k(attn_mma_kernel<64>, grid, dim3(128), smem, s, maps, a);
     }
     return (int)cudaErrorInvalidValue;
+}
+
+
+template <int HD>
+int launch_fused_hd(const AttnMaps& maps, const AttnFusedArgs& f, cudaStream_t s) {
+    const int qrows = (f.m.n_q / f.m.n_kv) * 16;
+    const size_t smem = fused_smem<HD>(qrows);
+    static bool set = false;
+    if (!set) {
+        const cudaError_t e = cudaFuncSetAttribute(attn_fused_kernel<HD>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return (int)e;
+        set = true;
+    }
+    return (int)launch_k(attn_fused_kernel<HD>, dim3(f.m.n_kv, f.max_splits), dim3(128), smem, s, maps, f);
+}
+
+int launch_attention_fused(const AttnMaps& maps, const AttnFusedArgs& f, cudaStream_t s) {
+    if (f.m.head_dim == 128) return launch_fused_hd<128>(maps, f, s);
+    if (f.m.head_dim == 64) return launch_fused_hd<64>(maps, f, s);
+    return (int)cudaErrorInvalidValue;
+}
+
+int attention_fused_per_sm(int hd, int n_q, int n_kv, int* out) {
+    const int qrows = (n_q / n_kv) * 16;
+    *out = 0;
+    cudaError_t e;
+    if (hd == 128) {
+        const size_t smem = fused_smem<128>(qrows);
+        e = cudaFuncSetAttribute(attn_fused_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, attn_fused_kernel<128>, 128, smem);
+    } else {
+        const size_t smem = fused_smem<64>(qrows);
+        e = cudaFuncSetAttribute(attn_fused_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, attn_fused_kernel<64>, 128, smem);
+    }
+    return (int)e;
 }
 
 }  // namespace dfl

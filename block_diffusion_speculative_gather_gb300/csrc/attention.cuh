@@ -25,4 +25,25 @@ struct AttnMmaArgs {
 int launch_attention_mma(const AttnMaps& maps, const AttnMmaArgs& a, int max_chunks,
                          cudaStream_t s);
 
+// Split-KV attention with the combine in the same kernel.  CTA (kv head,
+// split) folds `split_chunks` consecutive 64-key chunks with an online
+// softmax, publishes its (max, sum, output) and, once every split of its kv
+// head has done so, normalises its share of the head group's (q head, row)
+// outputs over the splits in split order.  The splits of a kv head wait for
+// one another, so the launch must fit on the device at once: split_chunks is
+// chosen per configuration so that n_kv * max_splits CTAs are resident.
+struct AttnFusedArgs {
+    AttnMmaArgs m;      // shapes, layer, cap, mask rule, scale, partials, state
+    int split_chunks;   // chunks per split (fixed per configuration)
+    int max_splits;     // grid.y
+    void* out;          // [16][n_q * head_dim], out_type (hi/lo planes for XT_BF16S)
+    int out_type;
+    int* arrive;        // [n_kv] published splits, zero between launches
+    int* done;          // [n_kv] splits done combining, zero between launches
+};
+
+int launch_attention_fused(const AttnMaps& maps, const AttnFusedArgs& f, cudaStream_t s);
+// Host: CTAs of the fused attention kernel one SM holds, for head_dim hd.
+int attention_fused_per_sm(int hd, int n_q, int n_kv, int* out);
+
 }  // namespace dfl

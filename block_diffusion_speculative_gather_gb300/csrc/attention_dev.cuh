@@ -134,5 +134,99 @@ __device__ __forceinline__ void chunk_partials(const uint8_t* Qs, const uint8_t*
     }
 }
 
+// One 64-key chunk folded into a running softmax state (online softmax):
+// m[r], l[r] are the running max and sum of rows g, g + 8 of q head
+// kh * group + warp and o the unnormalised output.  A key that is masked
+// for a row weighs exactly 0, and a chunk masked entirely for a row leaves
+// that row's state bit-identical, so a row's result does not depend on how
+// many rows the forward has.
+template <int HD>
+__device__ __forceinline__ void chunk_online(const uint8_t* Qs, const uint8_t* Ks, const uint8_t* Vs,
+                                             const AttnMmaArgs& a, int qrows, int c, int T, int pos0,
+                                             int lo, int hi, int warp, int lane, float (&m)[2],
+                                             float (&l)[2], float (&o)[HD / 8][4]) {
+    constexpr int C = ATTN_KEYS;
+    const int k0 = c * C;
+    const int g = lane >> 2, cq = lane & 3;
+    float s[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+#pragma unroll
+    for (int kd = 0; kd < HD / 16; ++kd) {
+        uint32_t qa[4];
+        ldsm_x4(qa, tile_at<HD>(Qs, qrows, warp * 16 + (lane & 15), 2 * kd + (lane >> 4)));
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+            uint32_t kb[4];
+            const int key = np * 16 + (lane & 7) + 8 * (lane >> 4);
+            ldsm_x4(kb, tile_at<HD>(Ks, C, key, 2 * kd + ((lane >> 3) & 1)));
+            const uint32_t b0[2] = {kb[0], kb[1]}, b1[2] = {kb[2], kb[3]};
+            mma_f16_16816(s[2 * np], qa, b0);
+            mma_f16_16816(s[2 * np + 1], qa, b1);
+        }
+    }
+    float mc[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int t = g + 8 * (e >> 1);
+            const int key = k0 + nt * 8 + 2 * cq + (e & 1);
+            const bool valid = t < T && key >= lo && key < hi && (!a.causal || key <= pos0 + t);
+            s[nt][e] = valid ? s[nt][e] * a.scale : -INFINITY;
+            mc[e >> 1] = fmaxf(mc[e >> 1], s[nt][e]);
+        }
+    float mn[2], alpha[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        mc[r] = fmaxf(mc[r], __shfl_xor_sync(0xffffffffu, mc[r], 1));
+        mc[r] = fmaxf(mc[r], __shfl_xor_sync(0xffffffffu, mc[r], 2));
+        mn[r] = fmaxf(m[r], mc[r]);
+        alpha[r] = (mn[r] == m[r]) ? 1.f : expf(m[r] - mn[r]);   // m = -inf -> 0
+    }
+    float ls[2] = {0.f, 0.f};
+    uint32_t pa[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+        float p[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            p[e] = s[nt][e] == -INFINITY ? 0.f : expf(s[nt][e] - mn[e >> 1]);
+            ls[e >> 1] += p[e];
+        }
+        const int kk = nt >> 1, hi8 = nt & 1;
+        pa[kk][0 + 2 * hi8] = pack_f16x2(p[0], p[1]);
+        pa[kk][1 + 2 * hi8] = pack_f16x2(p[2], p[3]);
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        ls[r] += __shfl_xor_sync(0xffffffffu, ls[r], 1);
+        ls[r] += __shfl_xor_sync(0xffffffffu, ls[r], 2);
+        l[r] = l[r] * alpha[r] + ls[r];
+        m[r] = mn[r];
+    }
+#pragma unroll
+    for (int dt = 0; dt < HD / 8; ++dt) {
+        o[dt][0] *= alpha[0];
+        o[dt][1] *= alpha[0];
+        o[dt][2] *= alpha[1];
+        o[dt][3] *= alpha[1];
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+        for (int dp = 0; dp < HD / 16; ++dp) {
+            uint32_t vb[4];
+            const int key = kk * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+            ldsm_x4_trans(vb, tile_at<HD>(Vs, C, key, 2 * dp + (lane >> 4)));
+            const uint32_t b0[2] = {vb[0], vb[1]}, b1[2] = {vb[2], vb[3]};
+            mma_f16_16816(o[2 * dp], pa[kk], b0);
+            mma_f16_16816(o[2 * dp + 1], pa[kk], b1);
+        }
+    }
+}
+
 }  // namespace adev
 }  // namespace dfl

@@ -67,7 +67,7 @@ int max_chunks(const dflash_config& c) { return cache_cap(c) / ATTN_CHUNK; }
 
 struct Layout {
     size_t state, x, hn, ssq, qrot, attn, act, taps, rcos, rsin, invf, amax, part, slots, counters,
-        amaps, barc, prog[3], ns[3], total;
+        acnt, amaps, barc, prog[3], ns[3], total;
     int prog_n[3];
 };
 
@@ -127,6 +127,7 @@ Layout make_layout(const dflash_config& c) {
     L.part = take((size_t)max_chunks(c) * R * c.n_q * (c.head_dim + 2) * 4);
     L.slots = take((size_t)MAX_SMS * 2 * GEMM_BN * R * 4);
     L.counters = take((size_t)MAX_TILES * 4);
+    L.acnt = take((size_t)2 * c.n_kv * 4);
     L.amaps = take(2 * sizeof(AttnMaps));
     L.barc = take(256);
     for (int i = 0; i < 3; ++i) {
@@ -253,6 +254,10 @@ struct dflash_ctx {
     std::vector<LayerPlans> tplan, dplan;
     GemmPlan lm, fc;
     AttnMaps amap_t{}, amap_d{};   // tensor-core attention maps (fp16 q and caches)
+    // fused attention per model (0 target, 1 drafter): chunks per split and
+    // splits of a launch (0: two-kernel form)
+    int attn_split_chunks[2] = {0, 0};
+    int attn_max_splits[2] = {0, 0};
     float* verify_logits = nullptr;
     float* draft_logits = nullptr;
     bool prefilled = false;
@@ -530,7 +535,18 @@ int run_layers(dflash_ctx* c, bool target, Emit& em) {
             am.scale = at.scale;
             am.part = at.part;
             am.st = st;
-            if (em.rec) {
+            if (!em.rec && c->attn_split_chunks[target ? 0 : 1] > 0) {
+                AttnFusedArgs fa{};
+                fa.m = am;
+                fa.split_chunks = c->attn_split_chunks[target ? 0 : 1];
+                fa.max_splits = c->attn_max_splits[target ? 0 : 1];
+                fa.out = at.out;
+                fa.out_type = at.out_type;
+                fa.arrive = c->buf<int>(c->L.acnt);
+                fa.done = fa.arrive + g.n_kv;
+                const int e = launch_attention_fused(target ? c->amap_t : c->amap_d, fa, em.s);
+                if (e) return fail(DFLASH_ERR_CUDA, "attention launch: %s", cudaGetErrorString((cudaError_t)e));
+            } else if (em.rec) {
                 Phase& pa = record(em, PH_ATTN);
                 pa.am = am;
                 pa.target = target ? 1 : 0;
@@ -878,6 +894,31 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
             r = make_map_raw(&c->amap_d.kv, kv_draft, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.head_dim,
                              (uint64_t)g.drf_layers * 2 * g.n_kv * cap, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     }
+    if (!r && g.dtype == DFLASH_BF16) {
+        // fused attention: the splits of a kv head wait for one another, so
+        // every CTA of a launch must be resident at once
+        int per_sm = 0;
+        const int e = attention_fused_per_sm(g.head_dim, g.n_q, g.n_kv, &per_sm);
+        if (e) r = fail(DFLASH_ERR_CUDA, "attention occupancy: %s", cudaGetErrorString((cudaError_t)e));
+        const int capacity = per_sm * sms;
+        for (int mdl = 0; mdl < 2 && !r && capacity > 0; ++mdl) {
+            // chunks a forward can touch: the whole cache for the causal
+            // target, the window (+ block, + a partial chunk) for the drafter
+            int mc = max_chunks(g);
+            if (mdl == 1 && g.window > 0) {
+                const int wc = (g.window + g.block_max + 63) / 64 + 1;
+                if (wc < mc) mc = wc;
+            }
+            int q = (mc * g.n_kv + capacity - 1) / capacity;
+            if (q < (mc + 63) / 64) q = (mc + 63) / 64;
+            if (q < 1) q = 1;
+            const int smax = (mc + q - 1) / q;
+            if (g.n_kv * smax <= capacity && smax <= 64) {
+                c->attn_split_chunks[mdl] = q;
+                c->attn_max_splits[mdl] = smax;
+            }
+        }
+    }
     if (r) {
         delete c;
         return r;
@@ -1178,6 +1219,9 @@ int dflash_check(dflash_ctx* c, dflash_stream_t stream) {
     if (err[0] == DERR_NONE) return DFLASH_OK;
     const int zero[2] = {0, 0};   // report once, then clear
     CUDA_TRY(cudaMemcpy(&c->st()->err, zero, sizeof zero, cudaMemcpyHostToDevice));
+    // a kernel that gave up may have left split-K or attention counters set
+    CUDA_TRY(cudaMemset(c->ws + c->L.counters, 0, (size_t)MAX_TILES * 4));
+    CUDA_TRY(cudaMemset(c->ws + c->L.acnt, 0, (size_t)2 * c->cfg.n_kv * 4));
     if (err[0] == DERR_TIMEOUT) return fail(DFLASH_ERR_TIMEOUT, "bounded wait expired (site %d)", err[1]);
     return fail(DFLASH_ERR_DEVICE, "device error %d (info %d)", err[0], err[1]);
 }
