@@ -222,6 +222,7 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     __shared__ float s_rstd[DFL_MAX_ROWS];
     pdl_wait();    // the epilogues read and write buffers of earlier kernels
     const int tid = threadIdx.x;   // 0..255
+    gdev::compute_rstd<EPI>(a, s_rstd, tid);   // read after the first tile's barrier
     int stage = 0;
     uint32_t phase = 0;
     float acc[8];

@@ -198,6 +198,32 @@ __device__ __forceinline__ void mma_kblock(const uint8_t* Wt, const uint8_t* Xt,
     }
 }
 
+// Row scale of a folded RMSNorm, once per GEMM and CTA: rstd[t] from the
+// producer's per-128-column partial sums of x^2, summed in column order
+// (the same for every forward length).  Threads 0..15 load every part first
+// (independent loads, one round trip) and then add them in order; s_rstd is
+// read only after the next consumer barrier.
+template <int EPI>
+__device__ __forceinline__ void compute_rstd(const GemmArgs& a, float* s_rstd, int tid) {
+    if (!(EPI == EPI_SWIGLU || EPI == EPI_ARGMAX || EPI == EPI_QKV)) return;
+    if (tid >= DFL_MAX_ROWS) return;
+    float r = 1.f;
+    if (a.ssq_in) {
+        float ss = 0.f;
+        for (int p0 = 0; p0 < a.ssq_parts; p0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = p0 + j < a.ssq_parts ? a.ssq_in[(p0 + j) * DFL_MAX_ROWS + tid] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (p0 + j < a.ssq_parts) ss += v[j];
+        }
+        r = 1.0f / sqrtf(ss * a.inv_width + a.eps);
+    }
+    s_rstd[tid] = r;
+}
+
 // Finish of a tile whose last k-block this CTA has just accumulated.  A
 // tile split across CTAs is finished by its owner, the first CTA of the
 // split (it reaches the tile at the end of its range): the other CTAs
@@ -232,6 +258,22 @@ __device__ __forceinline__ void finish_tile(const GemmArgs& a, int tile, const f
     const int i_first = cta_of(ts, U, G), i_last = cta_of(ts + a.kb - 1, U, G);
     const bool aborted = s_flags[0] != 0;
     bool do_epi = !aborted;
+    // Epilogue operands from global memory, loaded now (independent loads,
+    // in flight while the parts of a split tile are gathered) by the CTA
+    // that runs the epilogue.
+    float pre_x[2][4], pre_w[4];
+    if ((EPI == EPI_RESID || EPI == EPI_NORMOUT) && (i_first == i_last || cta == i_first)) {
+        const int n0 = tile * GEMM_BN;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pre_w[i] = a.w_next ? a.w_next[n0 + lane * 4 + i] : 1.f;
+        if (EPI == EPI_RESID) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    pre_x[q][i] = a.out[(size_t)(warp * 2 + q) * a.ldo + n0 + lane * 4 + i];
+        }
+    }
     if (i_first != i_last && cta != i_first) {
         // A later part of a split tile: the tile was this CTA's first, so its
         // part goes to this CTA's slot; the tile's owner, CTA i_first (whose
@@ -266,8 +308,7 @@ __device__ __forceinline__ void finish_tile(const GemmArgs& a, int tile, const f
         do_epi = !aborted && s_flags[1] != 0;
         if (do_epi) {
             __threadfence();
-            // Each thread owns 8 consecutive elements (two float4) and issues
-            // the loads of four parts at a time, so the L2 round trips overlap.
+            // Each thread owns 8 consecutive elements (two float4).
             const int e0 = tid * 8;
             float4 acc0 = *reinterpret_cast<const float4*>(ctile + e0);
             float4 acc1 = *reinterpret_cast<const float4*>(ctile + e0 + 4);
@@ -278,25 +319,21 @@ __device__ __forceinline__ void finish_tile(const GemmArgs& a, int tile, const f
             auto add4 = [](float4& x, const float4& y) {
                 x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
             };
-            int i = i_first + 1;
-            for (; i + 3 <= i_last; i += 4) {
-                const float4* p0 = part_ptr(i);
-                const float4* p1 = part_ptr(i + 1);
-                const float4* p2 = part_ptr(i + 2);
-                const float4* p3 = part_ptr(i + 3);
-                const float4 a0 = __ldcg(p0), b0 = __ldcg(p0 + 1);
-                const float4 a1 = __ldcg(p1), b1 = __ldcg(p1 + 1);
-                const float4 a2 = __ldcg(p2), b2 = __ldcg(p2 + 1);
-                const float4 a3 = __ldcg(p3), b3 = __ldcg(p3 + 1);
-                add4(acc0, a0); add4(acc1, b0);
-                add4(acc0, a1); add4(acc1, b1);
-                add4(acc0, a2); add4(acc1, b2);
-                add4(acc0, a3); add4(acc1, b3);
-            }
-            for (; i <= i_last; ++i) {
-                const float4* p0 = part_ptr(i);
-                add4(acc0, __ldcg(p0));
-                add4(acc1, __ldcg(p0 + 1));
+            // up to 8 parts in flight at once (a tile of a 152-CTA split has <= 8)
+            for (int i0 = i_first + 1; i0 <= i_last; i0 += 8) {
+                float4 va[8], vb[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (i0 + j <= i_last) {
+                        va[j] = __ldcg(part_ptr(i0 + j));
+                        vb[j] = __ldcg(part_ptr(i0 + j) + 1);
+                    }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (i0 + j <= i_last) {
+                        add4(acc0, va[j]);
+                        add4(acc1, vb[j]);
+                    }
             }
             *reinterpret_cast<float4*>(ctile + e0) = acc0;   // its own elements only
             *reinterpret_cast<float4*>(ctile + e0 + 4) = acc1;
@@ -304,21 +341,6 @@ __device__ __forceinline__ void finish_tile(const GemmArgs& a, int tile, const f
         }
     }
 
-    // Row scale of a folded RMSNorm: rstd[t] from the partial sums, summed
-    // in a fixed order (the same for every forward length).  Computed by
-    // all consumer threads, before the (barrier-free) epilogue.
-    if (EPI == EPI_SWIGLU || EPI == EPI_ARGMAX || EPI == EPI_QKV) {
-        if (tid < DFL_MAX_ROWS) {
-            float r = 1.f;
-            if (a.ssq_in) {
-                float ss = 0.f;
-                for (int p = 0; p < a.ssq_parts; ++p) ss += a.ssq_in[p * DFL_MAX_ROWS + tid];
-                r = 1.0f / sqrtf(ss * a.inv_width + a.eps);
-            }
-            s_rstd[tid] = r;
-        }
-        consumer_bar();
-    }
     if (do_epi) {
         if (EPI == EPI_STORE) {
             const int n0 = tile * GEMM_BN;
@@ -338,14 +360,12 @@ __device__ __forceinline__ void finish_tile(const GemmArgs& a, int tile, const f
                     const int r = lane * 4 + i;
                     float v = ctile[t * GEMM_BN + r];
                     if (EPI == EPI_RESID) {
-                        const size_t o = (size_t)t * a.ldo + n0 + r;
-                        v += a.out[o];
-                        a.out[o] = v;
+                        v += pre_x[q][i];
+                        a.out[(size_t)t * a.ldo + n0 + r] = v;
                         if (a.tap_out) store_act(a.tap_out, a.tap_type, a.ld_tap, t, n0 + r, v);
                     }
                     ss = fmaf(v, v, ss);
-                    const float wn = a.w_next ? a.w_next[n0 + r] : 1.f;
-                    store_act(a.xn_out, a.xn_type, a.ldo, t, n0 + r, v * wn);
+                    store_act(a.xn_out, a.xn_type, a.ldo, t, n0 + r, v * pre_w[i]);
                 }
                 ss = warp_sum(ss);
                 if (a.ssq_out && lane == 0) a.ssq_out[tile * DFL_MAX_ROWS + t] = ss;
@@ -364,40 +384,63 @@ __device__ __forceinline__ void finish_tile(const GemmArgs& a, int tile, const f
             const QkvEpi& qe = a.qkv;
             int r0;
             const int nrows = rows_of(a.st, qe.row_sel, &r0);
+            const int pos0 = a.st->fwd_pos0;
             const int hd = qe.hd, hpt = GEMM_BN / hd, per = hd / 32;
             const int h_first = tile * hpt;
+            // head-norm weights of this lane (q and k), loaded once
+            float qn[4], kn[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                qn[m] = (m < per && qe.n_q > 0) ? qe.q_norm[lane + 32 * m] : 0.f;
+                kn[m] = m < per ? qe.k_norm[lane + 32 * m] : 0.f;
+            }
             for (int item = warp; item < DFL_MAX_ROWS * hpt; item += GEMM_CONSUMERS) {
                 const int t = item / hpt, hi = item % hpt;
                 if (t < r0 || t >= r0 + nrows) continue;
                 const int h = h_first + hi;
                 const bool is_q = h < qe.n_q, is_k = !is_q && h < qe.n_q + qe.n_kv;
+                // rotate-half pairs element i with i + hd/2 (same lane, m + per/2)
+                float cs[2], sn[2];
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    cs[m] = (m < per / 2 && (is_q || is_k)) ? qe.rope_cos[t * (hd / 2) + lane + 32 * m] : 0.f;
+                    sn[m] = (m < per / 2 && (is_q || is_k)) ? qe.rope_sin[t * (hd / 2) + lane + 32 * m] : 0.f;
+                }
                 float v[4];
-                for (int m = 0; m < per; ++m)
-                    v[m] = ctile[t * GEMM_BN + hi * hd + lane + 32 * m] * s_rstd[t];
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    v[m] = m < per ? ctile[t * GEMM_BN + hi * hd + lane + 32 * m] * s_rstd[t] : 0.f;
                 if (is_q || is_k) {
-                    const float* nw = is_q ? qe.q_norm : qe.k_norm;
                     float ss = 0.f;
-                    for (int m = 0; m < per; ++m) ss = fmaf(v[m], v[m], ss);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) ss = fmaf(v[m], v[m], ss);   // v[m >= per] = 0
                     ss = warp_sum(ss);
                     const float inv = 1.0f / sqrtf(ss / (float)hd + a.eps);
-                    for (int m = 0; m < per; ++m) v[m] = v[m] * inv * nw[lane + 32 * m];
-                    // rotate-half: element i pairs with i + hd/2 (same lane, m + per/2)
-                    const float* cs = qe.rope_cos + t * (hd / 2);
-                    const float* sn = qe.rope_sin + t * (hd / 2);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) v[m] = v[m] * inv * (is_q ? qn[m] : kn[m]);
                     float rr[4];
-                    for (int m = 0; m < per / 2; ++m) {
-                        const int i = lane + 32 * m;
-                        rr[m] = v[m] * cs[i] - v[m + per / 2] * sn[i];
-                        rr[m + per / 2] = v[m + per / 2] * cs[i] + v[m] * sn[i];
+                    if (per == 4) {
+#pragma unroll
+                        for (int m = 0; m < 2; ++m) {
+                            rr[m] = v[m] * cs[m] - v[m + 2] * sn[m];
+                            rr[m + 2] = v[m + 2] * cs[m] + v[m] * sn[m];
+                        }
+                    } else {
+                        rr[0] = v[0] * cs[0] - v[1] * sn[0];
+                        rr[1] = v[1] * cs[0] + v[0] * sn[0];
+                        rr[2] = rr[3] = 0.f;
                     }
-                    for (int m = 0; m < per; ++m) v[m] = rr[m];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) v[m] = rr[m];
                 }
                 if (is_q) {
                     const size_t base = ((size_t)h * DFL_MAX_ROWS + t) * hd;   // [n_q][16][hd]
-                    for (int m = 0; m < per; ++m) store_xt(qe.q_out, qe.q_type, base + lane + 32 * m, v[m]);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        if (m < per) store_xt(qe.q_out, qe.q_type, base + lane + 32 * m, v[m]);
                     continue;
                 }
-                const int pos = a.st->fwd_pos0 + t;
+                const int pos = pos0 + t;
                 if (pos < 0 || pos >= qe.max_seq) {
                     if (lane == 0) set_error(a.st, DERR_INDEX, pos);
                     continue;
@@ -405,7 +448,9 @@ __device__ __forceinline__ void finish_tile(const GemmArgs& a, int tile, const f
                 const int kh = is_k ? h - qe.n_q : h - qe.n_q - qe.n_kv;
                 void* cache = is_k ? qe.k_cache : qe.v_cache;
                 const size_t base = ((size_t)kh * qe.cap + pos) * hd;
-                for (int m = 0; m < per; ++m) store_xt(cache, qe.c_type, base + lane + 32 * m, v[m]);
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    if (m < per) store_xt(cache, qe.c_type, base + lane + 32 * m, v[m]);
             }
         } else {  // EPI_ARGMAX: warp w reduces tokens 2w, 2w+1
             const int n0 = tile * GEMM_BN;

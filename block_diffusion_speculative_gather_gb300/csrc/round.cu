@@ -258,6 +258,12 @@ __device__ __forceinline__ void gemm_phase(int epi, const GemmArgs& a, uint8_t* 
     const int G = gridDim.x, cta = blockIdx.x;
     const long long U = (long long)a.n_tiles * a.kb;
     const long long u0 = range_start(cta, U, G), u1 = range_start(cta + 1, U, G);
+    switch (epi) {   // rstd is read after the first tile's barrier
+        case EPI_SWIGLU: gdev::compute_rstd<EPI_SWIGLU>(a, s_rstd, tid); break;
+        case EPI_ARGMAX: gdev::compute_rstd<EPI_ARGMAX>(a, s_rstd, tid); break;
+        case EPI_QKV: gdev::compute_rstd<EPI_QKV>(a, s_rstd, tid); break;
+        default: break;
+    }
     float acc[8];
     for (long long u = u0; u < u1;) {
         const int len = chunk_len(u, u1, a.kb);
