@@ -100,6 +100,7 @@ def _load() -> C.CDLL:
         "dflash_linear": (C.c_int, [vp, vp, i32, i32, vp, vp, sz, vp]),
         "dflash_linear_noalloc": (C.c_int, [vp, vp, i32, i32, vp, vp]),
         "dflash_profile_phases": (i32, [vp, i32, vp, i32]),
+        "dflash_progress": (C.c_int, [vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -116,7 +117,8 @@ EXPORTED = ("dflash_workspace_bytes", "dflash_kv_target_bytes", "dflash_kv_draft
             "dflash_destroy", "dflash_last_error", "dflash_tap_reduce",
             "dflash_quantize_int4g64", "dflash_profile", "dflash_launch_count",
             "dflash_selftest_timeout", "dflash_adopt_kv", "dflash_linear_workspace_bytes",
-            "dflash_linear", "dflash_linear_noalloc", "dflash_profile_phases")
+            "dflash_linear", "dflash_linear_noalloc", "dflash_profile_phases",
+            "dflash_progress")
 
 
 def check(rc: int) -> None:
@@ -253,3 +255,9 @@ def dflash_profile_phases(ctx, which: int):
     if rc < 0:
         check(rc)
     return list(buf)
+
+
+def dflash_progress(ctx, out, stream=None):
+    """Enqueue the progress words (finished, generated, n, emitted) into the
+    int32[4] device tensor `out`."""
+    check(lib.dflash_progress(ctx, _ptr(out), _stream(stream)))

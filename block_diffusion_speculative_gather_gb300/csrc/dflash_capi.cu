@@ -1226,6 +1226,12 @@ int dflash_check(dflash_ctx* c, dflash_stream_t stream) {
     return fail(DFLASH_ERR_DEVICE, "device error %d (info %d)", err[0], err[1]);
 }
 
+int dflash_progress(dflash_ctx* c, int32_t* out, dflash_stream_t stream) {
+    if (!c || !out) return fail(DFLASH_ERR_ARG, "NULL argument");
+    LAUNCH_TRY(launch_progress(c->st(), out, reinterpret_cast<cudaStream_t>(stream)));
+    return DFLASH_OK;
+}
+
 int dflash_selftest_timeout(dflash_ctx* c, int64_t limit_ns, dflash_stream_t stream) {
     if (!c) return fail(DFLASH_ERR_ARG, "ctx is NULL");
     if (limit_ns < 0 || limit_ns > 2000000000LL) return fail(DFLASH_ERR_ARG, "limit %lld ns", (long long)limit_ns);

@@ -62,6 +62,16 @@ bool g_pdl = [] {
 
 namespace {
 
+// Build knob for latency studies: per-CTA %globaltimer stamps of the last
+// launch (entry, weights issued, producer released, consumers released,
+// first stage landed, last k-block done, tile finishes done, exit).
+#ifdef DFL_GEMM_TIMESTAMPS
+__device__ unsigned long long g_gemm_ts[256][8];
+#define GEMM_TS(i) (g_gemm_ts[blockIdx.x & 255][(i)] = globaltimer_ns())
+#else
+#define GEMM_TS(i) ((void)0)
+#endif
+
 using gdev::consumer_bar;
 using gdev::range_start;
 using gdev::mma_kblock;
@@ -101,6 +111,7 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     };
 
     pdl_trigger();
+    if (threadIdx.x == 0) GEMM_TS(0);
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -173,7 +184,9 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 u += len;
                 ++npre;
             }
+            GEMM_TS(1);
             pdl_wait();
+            GEMM_TS(2);
             for (int i = 0; i < npre; ++i)
                 for (int j = 0; j < pl[i]; ++j) load_x(pu[i] + j, i, j);
             long long issued = npre;
@@ -222,6 +235,8 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     __shared__ float s_rstd[DFL_MAX_ROWS];
     pdl_wait();    // the epilogues read and write buffers of earlier kernels
     const int tid = threadIdx.x;   // 0..255
+    if (tid == 0) GEMM_TS(3);
+    bool first_seen = false;
     gdev::compute_rstd<EPI>(a, s_rstd, tid);   // read after the first tile's barrier
     int stage = 0;
     uint32_t phase = 0;
@@ -241,6 +256,10 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                 s_flags[0] = 1;
                 set_error(a.st, DERR_TIMEOUT, 101);
             }
+            if (tid == 0 && !first_seen) {
+                first_seen = true;
+                GEMM_TS(4);
+            }
         }
         if (ok) {
             for (int jb = 0; jb < len; ++jb) {
@@ -257,10 +276,12 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
         u += len;
 
         if (!(k + len == a.kb || u == u1)) continue;
+        if (tid == 0 && u == u1) GEMM_TS(5);
 
         finish_tile<WF, EPI>(a, tile, acc, ctile, s_flags, s_rstd, U, G, blockIdx.x, warp, lane,
                              tid);
     }
+    if (tid == 0) GEMM_TS(7);
 }
 
 template <int WF, int EPI>
@@ -282,6 +303,12 @@ int launch_one(const GemmMaps& maps, const GemmArgs& args, int grid, cudaStream_
 }
 
 }  // namespace
+
+#ifdef DFL_GEMM_TIMESTAMPS
+extern "C" int dfl_gemm_timestamps(unsigned long long* out) {
+    return (int)cudaMemcpyFromSymbol(out, g_gemm_ts, sizeof(g_gemm_ts));
+}
+#endif
 
 int launch_gemm(int wfmt, int epi, int xt, const GemmMaps& maps, const GemmArgs& args,
                 int grid, cudaStream_t stream) {

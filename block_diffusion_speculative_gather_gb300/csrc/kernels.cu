@@ -273,6 +273,18 @@ __global__ void selftest_wait_kernel(DevState* st, unsigned long long limit_ns) 
     if (!mbar_wait_bounded(&bar, 0, limit_ns)) set_error(st, DERR_TIMEOUT, 300);
 }
 
+// Progress words of the round state: finished, tokens generated, KV length,
+// tokens emitted by rounds (low 32 bits).
+__global__ void progress_kernel(const DevState* st, int32_t* out) {
+    pdl_trigger();
+    pdl_wait();
+    if (threadIdx.x != 0) return;
+    out[0] = st->finished;
+    out[1] = st->generated;
+    out[2] = st->n;
+    out[3] = (int32_t)st->emitted;
+}
+
 inline int ok(cudaError_t e) { return e == cudaSuccess ? 0 : -1; }
 
 }  // namespace
@@ -355,6 +367,10 @@ int launch_tap_reduce(const TapArgs& a, cudaStream_t s) {
     if (a.in_type == XT_F32 && a.out_type == XT_F32)
         return ok(launch_k(tap_reduce_kernel<float, float>, g, b, 0, s, a));
     return -2;
+}
+
+int launch_progress(const DevState* st, int32_t* out, cudaStream_t s) {
+    return ok(launch_k(progress_kernel, dim3(1), dim3(32), 0, s, st, out));
 }
 
 int launch_selftest_wait(DevState* st, unsigned long long limit_ns, cudaStream_t s) {

@@ -94,6 +94,8 @@ int launch_tap_reduce(const TapArgs& a, cudaStream_t s);
 
 int launch_selftest_wait(DevState* st, unsigned long long limit_ns, cudaStream_t s);
 
+int launch_progress(const DevState* st, int32_t* out, cudaStream_t s);
+
 int launch_quantize_int4g64(const float* w, int n, int k, uint8_t* packed, uint16_t* scales,
                             cudaStream_t s);
 

@@ -173,6 +173,51 @@ class DFlash:
             st = self.stats()
         return out
 
+    def generate_graphed(self, prompt: torch.Tensor, max_new: int,
+                         rounds_per_replay: int = 16) -> List[int]:
+        """Speculative decoding with the rounds replayed from one CUDA graph of
+        `rounds_per_replay` rounds.  Each replay ends by copying its rounds'
+        emitted tokens and the progress words to pinned host memory; the
+        host waits once per replay, collects the tokens and stops when the
+        state says finished (rounds after that are empty on the device)."""
+        B, K = self.w.block, rounds_per_replay
+        self.prefill(prompt, max_new)
+        graph = getattr(self, "_round_graph", None)
+        if graph is None or graph[0] != K:
+            self._round_graph = None
+            stage = torch.zeros((K, B + 1), dtype=torch.int32, device=self.device)
+            prog = torch.zeros(4, dtype=torch.int32, device=self.device)
+            host_stage = torch.zeros((K, B + 1), dtype=torch.int32).pin_memory()
+            host_prog = torch.zeros(4, dtype=torch.int32).pin_memory()
+            s = torch.cuda.Stream(self.device)
+            s.wait_stream(torch.cuda.current_stream(self.device))
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for r in range(K):
+                    self.verify(self.draft())
+                    stage[r, :B].copy_(self.tokens_out)
+                    stage[r, B:].copy_(self.n_emitted)
+                capi.dflash_progress(self.ctx, prog, s)
+                host_stage.copy_(stage, non_blocking=True)
+                host_prog.copy_(prog, non_blocking=True)
+            self._round_graph = (K, g, stage, prog, host_stage, host_prog)
+            # the capture ran nothing; the prefill above still holds
+        _, g, stage, prog, host_stage, host_prog = self._round_graph
+        st = self.stats()
+        out = [st.t_n]
+        done = bool(st.finished)
+        ev = torch.cuda.Event()
+        while not done and len(out) < max_new:
+            g.replay()
+            ev.record()
+            ev.synchronize()
+            rows = host_stage.tolist()
+            for r in range(K):
+                n = rows[r][B]
+                out.extend(rows[r][:n])
+            done = bool(host_prog[0].item())
+        return out[:max_new]
+
     def greedy(self, prompt: torch.Tensor, max_new: int) -> List[int]:
         """Plain greedy decoding through the same verify kernels, one row a step."""
         self.prefill(prompt, max_new)
@@ -185,6 +230,7 @@ class DFlash:
         return out
 
     def close(self):
+        self._round_graph = None
         if getattr(self, "ctx", None):
             capi.dflash_destroy(self.ctx)
             self.ctx = None

@@ -151,6 +151,15 @@ size_t dflash_kv_draft_bytes(const dflash_config* cfg /*host*/);
  * config guard fires before any buffer is built), builds the TMA
  * descriptors, zeroes the workspace's counters on the legacy stream and
  * returns a context in *out (host).  Borrowed buffers must outlive it.
+ *
+ * Ordering: the calls on one context must be ordered on the GPU (one stream,
+ * or streams joined by events); they share the workspace.  The kernels also
+ * expect the device to themselves: inside a GEMM or attention launch some
+ * CTAs wait for others of the same launch, so kernels of another context or
+ * stream running at the same time on the same GPU can hold the SMs those
+ * waits need.  Every such wait is bounded: contention ends in
+ * DFLASH_ERR_TIMEOUT from dflash_check (which also resets the counters),
+ * never in a hang.
  */
 int dflash_init(const dflash_config* cfg /*host*/, const dflash_weights* w /*host*/,
                 void* kv_target, void* kv_draft, void* workspace, size_t workspace_bytes,
@@ -222,6 +231,17 @@ int dflash_stats(dflash_ctx* ctx, dflash_stats_t* out, dflash_stream_t stream);
  * error since the last check (and clears the flag), else OK.  After TIMEOUT
  * the split-K tickets may be inconsistent: re-create the context. */
 int dflash_check(dflash_ctx* ctx, dflash_stream_t stream);
+
+/*
+ * Enqueues a copy of the round state's progress words into out (device,
+ * int32[4]): finished (nonzero once the generation is done), tokens
+ * generated (the prefill's first included), KV length n, tokens emitted by
+ * rounds.  No synchronisation, so a host loop can run many rounds from a
+ * CUDA graph and read the progress once per replay (the host builds while
+ * the GPU runs: "dflash: the chain verify builds pipelined ...", the chain
+ * verify commit).  Errors: ARG.
+ */
+int dflash_progress(dflash_ctx* ctx, int32_t* out, dflash_stream_t stream);
 
 /* Self-test of the kernels' bounded waits: launches one warp that waits on
  * an mbarrier nothing arrives on, gives up after limit_ns (<= 2 s) and sets

@@ -121,6 +121,21 @@ def test_spec_equals_greedy_and_oracle(tiny):
     assert n >= 8, f"only {n} decidable tokens compared"
 
 
+@pytest.mark.parametrize("k", [1, 4])
+def test_graphed_loop_equals_greedy(tiny, k):
+    """Rounds replayed from a CUDA graph of k rounds (tokens and progress read
+    back once per replay) emit exactly the greedy stream, and stop at the
+    budget even when the last replay runs past the finish."""
+    dec = tiny["dec"]
+    gg = dec.greedy(tiny["prompt"], TINY.n_new)
+    gr = dec.generate_graphed(tiny["prompt"], TINY.n_new, rounds_per_replay=k)
+    dec.check()
+    assert gr == gg
+    st = dec.stats()
+    assert st.finished and st.generated == TINY.n_new
+    dec._round_graph = None
+
+
 def test_spec_with_adversarial_drafts_equals_greedy(tiny):
     dec, B = tiny["dec"], TINY.block
     gg = dec.greedy(tiny["prompt"], TINY.n_new)
