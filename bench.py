@@ -496,6 +496,30 @@ def measure_workloads(steps, warmup, base_model):
                                "gbs": round(nbytes / (ms / 1e3) / 1e9, 1)}
     out["hc_tap"] = {"hc": hc["hc"], "hidden": hc["hidden"], "tap_layers": hc["n_layers"],
                      "by_rows": rows_res}
+    # --- the e2e round with every model 4-bit: target layers, drafter layers
+    #     and the LM head in INT4 group-64 (quantised on the device from the
+    #     same bf16 draws), natural acceptance
+    from block_diffusion_speculative_gather_gb300.configs import E2E_BF16
+    w4 = E2E_BF16.with_(name="e2e_int4", tgt_int4=True, lm_int4=True, drf_int4=True)
+    dec = DFlash(w4, base_model)
+    prompt = torch.from_numpy(synth.uniform_ids(w4.prompt_len, w4.vocab))
+    dec.prefill(prompt, w4.n_new)
+    dec.verify(dec.draft())
+    torch.cuda.synchronize()
+    gb, _, gl = _gemm_bytes_per_call(dec, lambda: dec.verify(dec.draft()))
+    dec.prefill(prompt, w4.n_new)
+    ms, gr4 = _graph_time(lambda: dec.verify(dec.draft()), steps, warmup)
+    del gr4
+    dec.check()
+    kv_bytes = (w4.tgt_layers * w4.n_kv * 2 * (w4.prompt_len + w4.block) * w4.head_dim * 2 +
+                w4.drf_layers * w4.n_kv * 2 * (w4.prompt_len + w4.block) * w4.head_dim * 2)
+    out["e2e_int4"] = {"rounds_s": round(1e3 / ms, 2), "ms_per_round": round(ms, 4),
+                       "bytes_per_round": int(gb + kv_bytes), "gemm_launches": gl,
+                       "hbm_gbs": round((gb + kv_bytes) / (ms / 1e3) / 1e9, 1),
+                       "frac_of_peak": round((gb + kv_bytes) / (ms / 1e3) / 1e9 / peak, 4),
+                       "weights": "INT4 g64 + bf16 scales: target and drafter projections and "
+                                  "the LM head; embedding gather and fc bf16"}
+    dec.close()
     # --- verify sweep over a 16384-position synthetic KV cache
     w = HC_SWEEP
     dec = DFlash(w, base_model)

@@ -78,6 +78,7 @@ enum : int { PROG_DRAFT = 0, PROG_VERIFY = 1, PROG_GREEDY = 2 };
 // fits the kernel's slot.
 bool round_cfg_ok(const dflash_config& g, int which) {
     if (g.dtype != DFLASH_BF16 || (g.head_dim != 128 && g.head_dim != 64)) return false;
+    if (g.lm_wfmt != 0) return false;   // its GEMM phases are bf16 only
     if (round_attn_bytes(g.n_q, g.n_kv, g.head_dim) > ROUND_ATTN_BYTES) return false;
     if (which == PROG_DRAFT) return g.drf_layers > 0 && g.drf_wfmt == DFLASH_BF16;
     return g.tgt_layers > 0 && g.tgt_wfmt == DFLASH_BF16 &&
@@ -170,8 +171,11 @@ int validate(const dflash_config* c) {
     };
     if (c->tgt_layers > 0 && !fmt_ok(c->tgt_wfmt)) return fail(DFLASH_ERR_CONFIG, "tgt_wfmt %d not supported with dtype %d", c->tgt_wfmt, c->dtype);
     if (c->drf_layers > 0 && !fmt_ok(c->drf_wfmt)) return fail(DFLASH_ERR_CONFIG, "drf_wfmt %d not supported with dtype %d", c->drf_wfmt, c->dtype);
+    if (c->lm_wfmt != 0 && !(c->dtype == DFLASH_BF16 && c->lm_wfmt == DFLASH_INT4G64))
+        return fail(DFLASH_ERR_CONFIG, "lm_wfmt %d: 0 (tied embedding) or INT4G64 with dtype BF16", c->lm_wfmt);
     const bool int4 = (c->tgt_layers > 0 && c->tgt_wfmt == DFLASH_INT4G64) ||
-                      (c->drf_layers > 0 && c->drf_wfmt == DFLASH_INT4G64);
+                      (c->drf_layers > 0 && c->drf_wfmt == DFLASH_INT4G64) ||
+                      c->lm_wfmt == DFLASH_INT4G64;
     if (int4 && (c->hidden % 256 || (c->n_q * c->head_dim) % 256 || c->ffn % 256))
         return fail(DFLASH_ERR_CONFIG, "INT4 projections need hidden, n_q*head_dim and ffn to be multiples of 256");
     if (c->eos_id >= c->vocab) return fail(DFLASH_ERR_CONFIG, "eos_id %d >= vocab", c->eos_id);
@@ -824,6 +828,8 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
     const dflash_config& g = *cfg;
     // every weight pointer is checked before any buffer is touched
     if (!aligned16(w->embed)) return fail(DFLASH_ERR_ARG, "embed missing or misaligned");
+    if (g.lm_wfmt == DFLASH_INT4G64 && (!aligned16(w->lm_head) || !aligned16(w->lm_scales)))
+        return fail(DFLASH_ERR_ARG, "INT4 LM head or its scales missing or misaligned");
     if (g.tgt_layers > 0 && (!w->tgt || !w->final_norm_tgt)) return fail(DFLASH_ERR_ARG, "target weights missing");
     if (g.drf_layers > 0 && (!w->drf || !w->final_norm_drf || !aligned16(w->fc) || !w->ctx_norm))
         return fail(DFLASH_ERR_ARG, "draft weights missing");
@@ -871,9 +877,17 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
     for (int i = 0; i < g.tgt_layers && !r; ++i) r = build_layer_plans(c, c->tgt[i], g.tgt_wfmt, false, &c->tplan[i]);
     for (int i = 0; i < g.drf_layers && !r; ++i) r = build_layer_plans(c, c->drf[i], g.drf_wfmt, true, &c->dplan[i]);
     if (!r) {
-        const void* we[1] = {w->embed};
         const int re[1] = {g.vocab};
-        r = plan_gemm(c, &c->lm, c->wf(g.dtype), EPI_ARGMAX, we, re, 1, g.hidden, c->ws + L.hn, c->act_xt());
+        if (g.lm_wfmt == DFLASH_INT4G64) {
+            const void* wl[1] = {w->lm_head};
+            const void* sl[1] = {w->lm_scales};
+            r = plan_gemm(c, &c->lm, WF_INT4, EPI_ARGMAX, wl, re, 1, g.hidden, c->ws + L.hn,
+                          c->act_xt(), sl);
+        } else {
+            const void* we[1] = {w->embed};
+            r = plan_gemm(c, &c->lm, c->wf(g.dtype), EPI_ARGMAX, we, re, 1, g.hidden, c->ws + L.hn,
+                          c->act_xt());
+        }
     }
     if (!r && g.drf_layers > 0) {
         const void* wfc[1] = {w->fc};

@@ -327,6 +327,7 @@ int launch_gemm(int wfmt, int epi, int xt, const GemmMaps& maps, const GemmArgs&
             case EPI_STORE: return launch_one<WF_INT4, EPI_STORE>(maps, args, grid, stream);
             case EPI_RESID: return launch_one<WF_INT4, EPI_RESID>(maps, args, grid, stream);
             case EPI_SWIGLU: return launch_one<WF_INT4, EPI_SWIGLU>(maps, args, grid, stream);
+            case EPI_ARGMAX: return launch_one<WF_INT4, EPI_ARGMAX>(maps, args, grid, stream);
             case EPI_QKV: return launch_one<WF_INT4, EPI_QKV>(maps, args, grid, stream);
         }
     } else if (wfmt == WF_F32) {

@@ -37,6 +37,9 @@ def make_config(w: Workload, **over) -> capi.dflash_config:
     cfg.dtype = _dtype_code(w)
     cfg.tgt_wfmt = _dtype_code(w)
     cfg.drf_wfmt = capi.DFLASH_INT4G64 if w.drf_int4 else _dtype_code(w)
+    if w.tgt_int4:
+        cfg.tgt_wfmt = capi.DFLASH_INT4G64
+    cfg.lm_wfmt = capi.DFLASH_INT4G64 if w.lm_int4 else 0
     cfg.ctx_norm = 1 if w.ctx_norm else 0
     cfg.rms_eps, cfg.rope_theta = w.rms_eps, w.rope_theta
     for k, v in over.items():
@@ -61,7 +64,12 @@ class DFlash:
         self.tgt = [{k: dev(v) for k, v in lw.items()} for lw in model.tgt]
         self.drf = [{k: dev(v) for k, v in lw.items()} for lw in model.drf]
         if w.drf_int4:
-            self._quantize_drafter()
+            self._quantize_layers(self.drf)
+        if w.tgt_int4:
+            self._quantize_layers(self.tgt)
+        self.lm_head = self.lm_scales = None
+        if w.lm_int4:
+            self.lm_head, self.lm_scales = self._quantize(self.embed)
         kvt = capi.dflash_kv_target_bytes(self.cfg)
         kvd = capi.dflash_kv_draft_bytes(self.cfg)
         wsb = capi.dflash_workspace_bytes(self.cfg)
@@ -82,6 +90,9 @@ class DFlash:
         wts.ctx_norm = self.ctx_norm.data_ptr()
         wts.tgt = C.cast(self._layers_t, C.POINTER(capi.dflash_layer))
         wts.drf = C.cast(self._layers_d, C.POINTER(capi.dflash_layer))
+        if self.lm_head is not None:
+            wts.lm_head = self.lm_head.data_ptr()
+            wts.lm_scales = self.lm_scales.data_ptr()
         self._weights = wts
         torch.cuda.synchronize(self.device)
         self.ctx = capi.dflash_init(self.cfg, wts, self.kv_target, self.kv_draft, self.workspace)
@@ -90,16 +101,19 @@ class DFlash:
         self.tokens_out = torch.full((B,), -1, dtype=torch.int32, device=self.device)
         self.n_emitted = torch.zeros(1, dtype=torch.int32, device=self.device)
 
-    def _quantize_drafter(self):
-        for lw in self.drf:
+    def _quantize(self, w: torch.Tensor):
+        """INT4 group-64 (packed [n][k/2], bf16 scales [k/64][n]) of w [n][k]."""
+        wf = w.float().contiguous()
+        n, kk = wf.shape
+        packed = torch.empty((n, kk // 2), dtype=torch.uint8, device=self.device)
+        scales = torch.empty((kk // 64, n), dtype=torch.int16, device=self.device)
+        capi.dflash_quantize_int4g64(wf, packed, scales, self.stream)
+        return packed, scales
+
+    def _quantize_layers(self, layers):
+        for lw in layers:
             for k in ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down"):
-                wf = lw[k].float().contiguous()
-                n, kk = wf.shape
-                packed = torch.empty((n, kk // 2), dtype=torch.uint8, device=self.device)
-                scales = torch.empty((kk // 64, n), dtype=torch.int16, device=self.device)
-                capi.dflash_quantize_int4g64(wf, packed, scales, self.stream)
-                lw[k] = packed
-                lw["s" + k[1:]] = scales          # wq -> sq, w_gate -> s_gate
+                lw[k], lw["s" + k[1:]] = self._quantize(lw[k])   # wq -> sq, w_gate -> s_gate
 
     @staticmethod
     def _layer(lw) -> capi.dflash_layer:

@@ -133,8 +133,9 @@ class ModelTensors:
 
     embed [vocab, H] (also the tied LM head), per-layer weights of the target
     ("tgt") and the drafter ("drf"), fc [H, n_taps*H] and fp32 ones for the
-    final norms and the drafter's context norm.  Drafters stored as INT4 are
-    drawn in fp32; the quantiser of each side turns them into INT4.
+    final norms and the drafter's context norm.  Layers stored as INT4 (the
+    drafter's or the target's) are drawn in fp32; the quantiser of each side
+    turns them into INT4.
     """
 
     def __init__(self, w, std: float = 0.02, seed: int = WEIGHT_SEED):
@@ -144,8 +145,9 @@ class ModelTensors:
         self.final_norm_t = torch.ones(w.hidden, dtype=torch.float32)
         self.final_norm_d = torch.ones(w.hidden, dtype=torch.float32)
         self.ctx_norm = torch.ones(w.hidden, dtype=torch.float32)
+        tdt = torch.float32 if getattr(w, "tgt_int4", False) else dt
         self.tgt = decoder_layers("tgt", w.tgt_layers, w.hidden, w.n_q, w.n_kv, w.head_dim,
-                                  w.ffn, dt, std, seed)
+                                  w.ffn, tdt, std, seed)
         ddt = torch.float32 if w.drf_int4 else dt
         self.drf = decoder_layers("drf", w.drf_layers, w.hidden, w.n_q, w.n_kv, w.head_dim,
                                   w.ffn, ddt, std, seed)

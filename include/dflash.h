@@ -83,6 +83,9 @@ typedef struct {
     int32_t drf_wfmt;  /* projection format of draft layers: F32 | BF16 | INT4G64 */
     int32_t ctx_norm;  /* 1 = RMSNorm after fc (drafter context) */
     float rms_eps, rope_theta;
+    int32_t lm_wfmt;   /* LM head: 0 = the embedding itself (tied); INT4G64 = a
+                        * group-64 INT4 copy of it (dtype BF16 only; "[RFC] DFlash",
+                        * "Test Plan": target and drafter both run 4-bit) */
 } dflash_config;
 
 /*
@@ -112,6 +115,9 @@ typedef struct {
     const float* ctx_norm;        /* [hidden] */
     const dflash_layer* tgt;      /* (host) array [tgt_layers], copied by dflash_init */
     const dflash_layer* drf;      /* (host) array [drf_layers], copied by dflash_init */
+    const void* lm_head;          /* lm_wfmt INT4G64: packed [vocab][hidden/2] of the
+                                   * embedding (dflash_quantize_int4g64); else NULL */
+    const void* lm_scales;        /* lm_wfmt INT4G64: bf16 [hidden/64][vocab]; else NULL */
 } dflash_weights;
 
 /* Round counters kept on the device (per-draft-position accept profile). */

@@ -263,9 +263,16 @@ def target_layer(x: np.ndarray, lw, cfg: OracleConfig, positions: Sequence[int],
 
 @dataclass
 class TargetWeights:
-    embed: np.ndarray                      # [vocab, H] (also the LM head)
+    embed: np.ndarray                      # [vocab, H] (also the LM head when tied)
     layers: List[Dict[str, np.ndarray]]
     final_norm: np.ndarray
+    # LM head [vocab, H] when it is not the embedding itself: the 4-bit
+    # models of "[RFC] DFlash" ("Test Plan": target and draft both 4-bit)
+    # read the logits from an INT4 group-64 copy (dequantised values here)
+    lm_head: Optional[np.ndarray] = None
+
+    def head(self) -> np.ndarray:
+        return self.embed if self.lm_head is None else self.lm_head
 
 
 def target_forward(tw: TargetWeights, cfg: OracleConfig, tokens: Sequence[int],
@@ -285,7 +292,7 @@ def target_forward(tw: TargetWeights, cfg: OracleConfig, tokens: Sequence[int],
         if l in cfg.tap_layers:
             taps[l] = x.copy()
     h = rms_norm(x, tw.final_norm, cfg.rms_eps)
-    logits = linear(h, tw.embed)
+    logits = linear(h, tw.head())
     tap = np.concatenate([taps[l] for l in sorted(cfg.tap_layers)], axis=-1) \
         if cfg.tap_layers else np.zeros((len(tokens), 0))
     return logits, tap
@@ -401,7 +408,8 @@ def draft_context(dw: DraftWeights, cfg: OracleConfig, taps: np.ndarray) -> np.n
 
 
 def draft_forward(dw: DraftWeights, embed: np.ndarray, cfg: OracleConfig,
-                  taps_by_pos: np.ndarray, t_n: int, n: int, bl: int):
+                  taps_by_pos: np.ndarray, t_n: int, n: int, bl: int,
+                  lm_head: Optional[np.ndarray] = None):
     """One drafter forward over the masked block at positions n..n+bl-1.
 
     taps_by_pos[p] is the concatenated tap row of absolute position p (p < n).
@@ -412,6 +420,8 @@ def draft_forward(dw: DraftWeights, embed: np.ndarray, cfg: OracleConfig,
     [max(0, n-W), n) concatenated with the block's own.  The block attends
     bidirectionally.  Returns (logits [bl, vocab], draft ids [bl - 1]) where
     draft id j-1 = argmax of block row j, j = 1..bl-1 (row 0 is discarded).
+    The drafter shares the target's embedding and LM head (lm_head None: the
+    embedding itself).
     """
     ctx_pos = list(block_context_range(n, cfg.window))
     c = draft_context(dw, cfg, taps_by_pos[ctx_pos]) if ctx_pos else \
@@ -432,7 +442,8 @@ def draft_forward(dw: DraftWeights, embed: np.ndarray, cfg: OracleConfig,
         a = attention(q, K, V, vis, 1.0 / math.sqrt(d))
         x = x + linear(a.reshape(bl, -1), lw["wo"])
         x = x + mlp(x, lw, cfg)
-    logits = linear(rms_norm(x, dw.final_norm, cfg.rms_eps), embed)
+    logits = linear(rms_norm(x, dw.final_norm, cfg.rms_eps),
+                    embed if lm_head is None else lm_head)
     ids = [argmax_lowest(logits[j]) for j in range(1, bl)]
     return logits, ids
 
@@ -519,7 +530,8 @@ def spec_decode(tw: TargetWeights, dw: Optional[DraftWeights], cfg: OracleConfig
         elif draft_override is not None:
             d = list(draft_override(t_n, n, bl, list(prompt) + tr.tokens))
         else:
-            _, d = draft_forward(dw, tw.embed, cfg, np.stack(ctx_taps), t_n, n, bl)
+            _, d = draft_forward(dw, tw.embed, cfg, np.stack(ctx_taps), t_n, n, bl,
+                                 lm_head=tw.lm_head)
         logits, vtaps = target_forward(tw, cfg, [t_n] + d, n, cache)
         y = [argmax_lowest(logits[i]) for i in range(len(d) + 1)]
         a, emitted, finished = accept(d, y, cfg.eos_id)

@@ -51,9 +51,18 @@ def oracle_layers(layers: List[Dict[str, torch.Tensor]], int4: bool = False):
     return out
 
 
+def int4_roundtrip(w: np.ndarray) -> np.ndarray:
+    """The values an INT4 group-64 copy of w holds (the oracle's quantiser)."""
+    packed, s = O.quantize_int4_g64(w)
+    return O.dequant_int4_g64(packed, s)
+
+
 def oracle_target(m: ModelTensors) -> O.TargetWeights:
-    return O.TargetWeights(embed=np32(m.embed), layers=oracle_layers(m.tgt),
-                           final_norm=np32(m.final_norm_t))
+    w = m.w
+    embed = np32(m.embed)
+    return O.TargetWeights(embed=embed, layers=oracle_layers(m.tgt, getattr(w, "tgt_int4", False)),
+                           final_norm=np32(m.final_norm_t),
+                           lm_head=int4_roundtrip(embed) if getattr(w, "lm_int4", False) else None)
 
 
 def oracle_draft(m: ModelTensors) -> O.DraftWeights:

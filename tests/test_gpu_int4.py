@@ -40,3 +40,92 @@ def test_int4_drafter_matches_oracle(window, n_ext):
     assert err.max() < TOL, err
     G.check_ids(ids[:w.block - 1], ref[1:], TOL)
     dec.close()
+
+
+# ---------------------------------------------------------------- 4-bit target
+
+def _w4():
+    from block_diffusion_speculative_gather_gb300.configs import E2E_BF16
+    return E2E_BF16.with_(name="int4_target_2layer", tgt_layers=2, drf_layers=1, tap_layers=(0, 1),
+                          prompt_len=40, n_new=40, max_seq=256, tgt_int4=True, lm_int4=True,
+                          drf_int4=True)
+
+
+@pytest.fixture(scope="module")
+def int4_target():
+    G.build_lib()
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+    from tests.oracle_inputs import oracle_target
+    w = _w4()
+    m = ModelTensors(w)
+    return dict(w=w, m=m, tw=oracle_target(m), dw=oracle_draft(m), cfg=oracle_config(w),
+                prompt=torch.from_numpy(synth.uniform_ids(w.prompt_len, w.vocab)),
+                dec=DFlash(w, m))
+
+
+def test_int4_target_and_lm_head_verify_match_oracle(int4_target):
+    """Target layers and the LM head in INT4 group-64 (both models 4-bit):
+    the 16-row verify's logits within rel 2e-2 of the oracle's dequantised
+    fp64 target, acceptance and rollback exact where decidable."""
+    T = int4_target
+    w, dec, tw, cfg = T["w"], T["dec"], T["tw"], T["cfg"]
+    P, B = w.prompt_len, w.block
+    dec.prefill(T["prompt"], w.n_new)
+    t_n = dec.stats().t_n
+    d = synth.uniform_ids(B - 1, w.vocab, seed=21).tolist()
+    vl = G.logits_buf(w.vocab)
+    dec.set_logits_out(vl, None)
+    toks, n = dec.verify(torch.tensor(d, dtype=torch.int32, device="cuda"))
+    dec.check()
+    dec.set_logits_out(None, None)
+    cache = O.KVCache(2, w.n_kv, w.head_dim)
+    O.target_forward(tw, cfg, T["prompt"].tolist(), 0, cache)
+    ref, _ = O.target_forward(tw, cfg, [t_n] + d, P, cache)
+    err = G.rel_err_rows(vl[:B].cpu().numpy(), ref)
+    assert err.max() < TOL, err
+    y = [int(np.argmax(r)) for r in ref]
+    a, emitted, _ = O.accept(d, y, -1)
+    if all(G.decidable(r, TOL) for r in ref[: a + 1]):
+        assert toks[: n.item()].tolist() == emitted
+        assert dec.stats().n == P + len(emitted)
+
+
+def test_int4_target_draft_uses_int4_lm_head(int4_target):
+    """The drafter's logits come from the same INT4 LM head."""
+    T = int4_target
+    w, dec = T["w"], T["dec"]
+    dec.prefill(T["prompt"], w.n_new)
+    dl = G.logits_buf(w.vocab)
+    dec.set_logits_out(None, dl)
+    ids = dec.draft().cpu().numpy()
+    dec.check()
+    dec.set_logits_out(None, None)
+    t_n = dec.stats().t_n
+    cache = O.KVCache(2, w.n_kv, w.head_dim)
+    _, p_taps = O.target_forward(T["tw"], T["cfg"], T["prompt"].tolist(), 0, cache)
+    ref, _ = O.draft_forward(T["dw"], T["tw"].embed, T["cfg"], p_taps, t_n, w.prompt_len, w.block,
+                             lm_head=T["tw"].lm_head)
+    err = G.rel_err_rows(dl[1:w.block].cpu().numpy(), ref[1:])
+    assert err.max() < TOL, err
+    G.check_ids(ids[:w.block - 1], ref[1:], TOL)
+
+
+def test_int4_target_spec_equals_greedy_and_batch_invariant(int4_target):
+    T = int4_target
+    w, dec = T["w"], T["dec"]
+    gg = dec.greedy(T["prompt"], w.n_new)
+    sp = dec.generate(T["prompt"], w.n_new)
+    dec.check()
+    assert sp == gg
+    P, B = w.prompt_len, w.block
+    dec.prefill(T["prompt"], w.n_new)
+    vl = G.logits_buf(w.vocab)
+    dec.set_logits_out(vl, None)
+    dec.verify(torch.tensor(gg[1:B], dtype=torch.int32, device="cuda"))
+    batch = vl[:B].clone()
+    dec.rollback(P, gg[0])
+    for i in range(B):
+        dec.verify(None)
+        assert torch.equal(vl[0], batch[i]), f"row {i}"
+    dec.set_logits_out(None, None)
+    dec.close()

@@ -125,6 +125,23 @@ def test_draft_forward_matches_torch_composition(tiny):
     cfg.window = TINY.window
 
 
+def test_untied_lm_head_reads_only_the_logits(tiny):
+    """An untied LM head L replaces the embedding in the logits only: with
+    L = 2 E every logit doubles exactly (the embedding gather, hence every
+    hidden state, is unchanged), for the target and for the drafter."""
+    import dataclasses
+    tw, dw, cfg, prompt = tiny["tw"], tiny["dw"], tiny["cfg"], tiny["prompt"]
+    tw2 = dataclasses.replace(tw, lm_head=2.0 * tw.embed.astype(np.float64))
+    l1, t1 = O.target_forward(tw, cfg, prompt, 0, O.KVCache(len(tw.layers), cfg.n_kv, cfg.head_dim))
+    l2, t2 = O.target_forward(tw2, cfg, prompt, 0, O.KVCache(len(tw.layers), cfg.n_kv, cfg.head_dim))
+    np.testing.assert_array_equal(l2, 2.0 * l1)
+    np.testing.assert_array_equal(t2, t1)
+    taps = synth.tap_rows(40, cfg.n_taps * cfg.hidden, torch.float32).numpy()
+    d1, _ = O.draft_forward(dw, tw.embed, cfg, taps, 17, 40, 8)
+    d2, _ = O.draft_forward(dw, tw.embed, cfg, taps, 17, 40, 8, lm_head=tw2.lm_head)
+    np.testing.assert_array_equal(d2, 2.0 * d1)
+
+
 # ------------------------------------------------------- invariants
 
 def test_incremental_decoding_equals_full_forward(tiny):
