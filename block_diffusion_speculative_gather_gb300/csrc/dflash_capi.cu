@@ -95,6 +95,11 @@ int program_phases(const dflash_config& g, int which) {
 }
 
 constexpr int MAX_SMS = 256 * DFL_GEMM_CTAS_PER_SM;   // GEMM CTAs (split-K slots)
+
+// Fewest 64-key chunks one attention split folds (build knob).
+#ifndef DFL_ATTN_MIN_SPLIT
+#define DFL_ATTN_MIN_SPLIT 1
+#endif
 constexpr int MAX_TILES = 8192;
 
 // Workspace carving.  hn holds the next GEMM's normalised input rows
@@ -925,7 +930,7 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
             }
             int q = (mc * g.n_kv + capacity - 1) / capacity;
             if (q < (mc + 63) / 64) q = (mc + 63) / 64;
-            if (q < 1) q = 1;
+            if (q < DFL_ATTN_MIN_SPLIT) q = DFL_ATTN_MIN_SPLIT;
             const int smax = (mc + q - 1) / q;
             if (g.n_kv * smax <= capacity && smax <= 64) {
                 c->attn_split_chunks[mdl] = q;
