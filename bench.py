@@ -555,15 +555,21 @@ def measure_workloads(steps, warmup, base_model):
 ACCEPT_CONTINUE = 0.83
 
 
-def injected_schedule(g, n_new, B, prompt_len, max_seq, vocab, seed):
+def injected_schedule(g, n_new, B, prompt_len, max_seq, vocab, seed, adaptive=False):
     """Rounds of an injected run: (block length, draft row [B-1]) per round
-    and the tokens they emit, following the device's block-length rule."""
+    and the tokens they emit, following the device's block-length rule (with
+    `adaptive`, the device's cap: 4 / 8 / 16 rows from the halving average of
+    the accepted drafts, fp32)."""
     import numpy as np
     rng = np.random.default_rng(seed)
     gen, n = 1, prompt_len
     rows, emitted = [], []
+    ema = np.float32(B - 1)
     while gen < n_new and n < max_seq:
-        bl = min(B, n_new - gen, max_seq - n)
+        cap = B
+        if adaptive:
+            cap = min(B, 4 if ema < np.float32(1.5) else (8 if ema < np.float32(4.5) else 16))
+        bl = min(cap, n_new - gen, max_seq - n)
         a = 0
         while a < bl - 1 and rng.random() < ACCEPT_CONTINUE:
             a += 1
@@ -572,12 +578,13 @@ def injected_schedule(g, n_new, B, prompt_len, max_seq, vocab, seed):
             row[a] = (row[a] + 1) % vocab                                # first mismatch
         rows.append(row)
         emitted.append(a + 1)
+        ema = np.float32(0.5) * ema + np.float32(0.5) * np.float32(a)
         gen += a + 1
         n += a + 1
     return rows, emitted
 
 
-def measure_injected(w, model, blocks=(16, 8, 4), reps=3):
+def measure_injected(w, model, blocks=(16, 8, 4, "16a"), reps=3):
     """Rounds/s and accepted tok/s with injected acceptance at each block
     size, CUDA-graph timed; the emitted tokens must equal greedy decoding."""
     import torch
@@ -586,12 +593,15 @@ def measure_injected(w, model, blocks=(16, 8, 4), reps=3):
     prompt = torch.from_numpy(synth.uniform_ids(w.prompt_len, w.vocab))
     out = {"continue_prob": ACCEPT_CONTINUE, "by_block": {}}
     g = None
-    for B in blocks:
-        wb = w.with_(block=B)
+    for Bk in blocks:
+        adaptive = isinstance(Bk, str)                 # "16a": block 16, adaptive cap
+        B = int(str(Bk).rstrip("a"))
+        wb = w.with_(block=B, adaptive_block=adaptive)
         dec = DFlash(wb, model)
         if g is None:
             g = dec.greedy(prompt, w.n_new)           # the reference stream
-        rows, emitted = injected_schedule(g, w.n_new, B, w.prompt_len, w.max_seq, w.vocab, seed=7)
+        rows, emitted = injected_schedule(g, w.n_new, B, w.prompt_len, w.max_seq, w.vocab, seed=7,
+                                          adaptive=adaptive)
         R = len(rows)
         table = torch.tensor(rows, dtype=torch.int32, device="cuda")
         inj = torch.empty((1, B - 1), dtype=torch.int32, device="cuda")
@@ -640,7 +650,7 @@ def measure_injected(w, model, blocks=(16, 8, 4), reps=3):
             toks.extend(lt[r][:ln[r]])
         lossless = toks[:len(g)] == g[:len(toks)] and ln == emitted
         total = sum(ln)
-        out["by_block"][str(B)] = {
+        out["by_block"][str(Bk) if not adaptive else f"{B}_adaptive"] = {
             "rounds": R, "rounds_s": round(R / (best / 1e3), 2),
             "accepted_tok_s": round(total / (best / 1e3), 2),
             "tokens_per_round": round(total / R, 3), "ms_per_round": round(best / R, 4),

@@ -35,7 +35,7 @@ class dflash_config(C.Structure):
         ("block_max", C.c_int32), ("window", C.c_int32), ("max_seq", C.c_int32),
         ("eos_id", C.c_int32), ("dtype", C.c_int32), ("tgt_wfmt", C.c_int32),
         ("drf_wfmt", C.c_int32), ("ctx_norm", C.c_int32), ("rms_eps", C.c_float),
-        ("rope_theta", C.c_float), ("lm_wfmt", C.c_int32),
+        ("rope_theta", C.c_float), ("lm_wfmt", C.c_int32), ("adaptive_block", C.c_int32),
     ]
 
 

@@ -41,6 +41,7 @@ class Workload:
     drf_int4: bool = False
     tgt_int4: bool = False   # target q/k/v/o/gate/up/down in INT4 group-64
     lm_int4: bool = False    # LM head: INT4 group-64 copy of the embedding
+    adaptive_block: bool = False   # per-round block cap from recent acceptance
     prompt_len: int = 0
     n_new: int = 0
     n_ctx: int = 0           # externally supplied tap rows (drafter alone)

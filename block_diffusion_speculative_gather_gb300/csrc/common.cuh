@@ -39,6 +39,8 @@ struct DevState {
     int pad_;
     long long rounds, emitted;
     long long accept_hist[16];
+    float acc_ema;   // adaptive block: running average of accepted drafts
+    int adaptive;    // 1: the next block is capped from acc_ema
 };
 
 #include <utility>
@@ -102,6 +104,16 @@ __device__ __forceinline__ int rows_of(const DevState* st, int sel, int* r0) {
     return st->fwd_T;
 }
 }  // namespace dfl
+
+// Block length cap of the next round: the native block, or with the
+// adaptive policy 4 / 8 / 16 rows (3 / 7 / 15 drafts) from the running
+// average of accepted drafts (< 1.5, < 4.5, else).
+__device__ __forceinline__ int block_cap(const DevState* st, int B) {
+    if (!st->adaptive) return B;
+    const float e = st->acc_ema;
+    const int cap = e < 1.5f ? 4 : (e < 4.5f ? 8 : 16);
+    return cap < B ? cap : B;
+}
 
 __device__ __forceinline__ void set_error(DevState* st, int code, int info) {
     if (atomicCAS(&st->err, 0, code) == 0) st->err_info = info;

@@ -176,6 +176,8 @@ int validate(const dflash_config* c) {
     };
     if (c->tgt_layers > 0 && !fmt_ok(c->tgt_wfmt)) return fail(DFLASH_ERR_CONFIG, "tgt_wfmt %d not supported with dtype %d", c->tgt_wfmt, c->dtype);
     if (c->drf_layers > 0 && !fmt_ok(c->drf_wfmt)) return fail(DFLASH_ERR_CONFIG, "drf_wfmt %d not supported with dtype %d", c->drf_wfmt, c->dtype);
+    if (c->adaptive_block != 0 && c->adaptive_block != 1)
+        return fail(DFLASH_ERR_CONFIG, "adaptive_block %d: 0 or 1", c->adaptive_block);
     if (c->lm_wfmt != 0 && !(c->dtype == DFLASH_BF16 && c->lm_wfmt == DFLASH_INT4G64))
         return fail(DFLASH_ERR_CONFIG, "lm_wfmt %d: 0 (tied embedding) or INT4G64 with dtype BF16", c->lm_wfmt);
     const bool int4 = (c->tgt_layers > 0 && c->tgt_wfmt == DFLASH_INT4G64) ||
@@ -947,6 +949,14 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
     if (e != cudaSuccess) {
         delete c;
         return fail(DFLASH_ERR_CUDA, "workspace clear: %s", cudaGetErrorString(e));
+    }
+    if (g.adaptive_block) {
+        const int one = 1;
+        e = cudaMemcpy(&c->st()->adaptive, &one, sizeof one, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) {
+            delete c;
+            return fail(DFLASH_ERR_CUDA, "state init: %s", cudaGetErrorString(e));
+        }
     }
     {
         // RoPE frequencies theta^(-2i/d), in double

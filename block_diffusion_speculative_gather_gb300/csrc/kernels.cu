@@ -150,7 +150,7 @@ __global__ void rollback_kernel(DevState* st, int new_len, int token, int B, int
     if (st->ctx_len > new_len) st->ctx_len = new_len;
     st->generated = max(1, st->generated - (old - new_len));
     st->finished = st->generated >= st->max_new || new_len >= max_seq;
-    st->bl = st->finished ? 0 : min(B, min(st->max_new - st->generated, max_seq - new_len));
+    st->bl = st->finished ? 0 : min(block_cap(st, B), min(st->max_new - st->generated, max_seq - new_len));
 }
 
 __global__ void set_ext_state_kernel(DevState* st, int n_ext, int tok, int max_new, int B,
@@ -167,7 +167,8 @@ __global__ void set_ext_state_kernel(DevState* st, int n_ext, int tok, int max_n
     for (int j = 0; j < 16; ++j) st->accept_hist[j] = 0;
     st->last_a = 0;
     st->finished = (eos >= 0 && tok == eos) || max_new <= 1 || n_ext >= max_seq;
-    st->bl = st->finished ? 0 : min(B, min(max_new - 1, max_seq - n_ext));
+    st->acc_ema = (float)(B - 1);
+    st->bl = st->finished ? 0 : min(block_cap(st, B), min(max_new - 1, max_seq - n_ext));
     st->fwd_T = 0;
     st->fwd_commit = 0;
 }

@@ -186,7 +186,8 @@ __device__ __forceinline__ void accept_run(const AcceptArgs& a) {
         st->last_a = 0;
         st->finished = (a.eos_id >= 0 && st->t_n == a.eos_id) || a.max_new <= 1 ||
                        st->n >= a.max_seq;
-        const int bl = min(B, min(a.max_new - 1, a.max_seq - st->n));
+        st->acc_ema = (float)(B - 1);
+        const int bl = min(block_cap(st, B), min(a.max_new - 1, a.max_seq - st->n));
         st->bl = st->finished ? 0 : bl;
         return;
     }
@@ -221,9 +222,10 @@ __device__ __forceinline__ void accept_run(const AcceptArgs& a) {
     st->emitted += emit;
     for (int j = 0; j < acc && j < 16; ++j) st->accept_hist[j] += 1;
     st->last_a = acc;
+    st->acc_ema = 0.5f * st->acc_ema + 0.5f * (float)acc;
     fin |= st->generated >= st->max_new || st->n >= a.max_seq;
     st->finished = fin;
-    st->bl = fin ? 0 : min(B, min(st->max_new - st->generated, a.max_seq - st->n));
+    st->bl = fin ? 0 : min(block_cap(st, B), min(st->max_new - st->generated, a.max_seq - st->n));
     st->fwd_commit_r0 = 0;
     st->fwd_commit = emit;
 }

@@ -40,6 +40,7 @@ def make_config(w: Workload, **over) -> capi.dflash_config:
     if w.tgt_int4:
         cfg.tgt_wfmt = capi.DFLASH_INT4G64
     cfg.lm_wfmt = capi.DFLASH_INT4G64 if w.lm_int4 else 0
+    cfg.adaptive_block = 1 if w.adaptive_block else 0
     cfg.ctx_norm = 1 if w.ctx_norm else 0
     cfg.rms_eps, cfg.rope_theta = w.rms_eps, w.rope_theta
     for k, v in over.items():

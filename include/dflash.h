@@ -86,6 +86,11 @@ typedef struct {
     int32_t lm_wfmt;   /* LM head: 0 = the embedding itself (tied); INT4G64 = a
                         * group-64 INT4 copy of it (dtype BF16 only; "[RFC] DFlash",
                         * "Test Plan": target and drafter both run 4-bit) */
+    int32_t adaptive_block; /* 1: cap each round's block from recent acceptance:
+                        * ema <- ema/2 + a/2 (a = drafts accepted, fp32, from
+                        * block_max - 1), next block <= 4 rows if ema < 1.5, <= 8 if
+                        * ema < 4.5, else block_max (the round policy of "dflash: the
+                        * chain verify builds pipelined ...", first commit) */
 } dflash_config;
 
 /*

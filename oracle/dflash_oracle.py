@@ -80,6 +80,7 @@ class OracleConfig:
     rms_eps: float = 1e-6
     rope_theta: float = 1e6
     ctx_norm: bool = True
+    adaptive_block: bool = False   # per-round block cap from recent acceptance
 
     @property
     def mask_id(self) -> int:
@@ -488,6 +489,25 @@ def block_len(block: int, max_new: int, generated: int, max_seq: int, pos: int) 
     return min(block, max_new - generated, max_seq - pos)
 
 
+# Adaptive block length.  The mlx-serve page's round policy picks the block
+# size per round ("dflash: the chain verify builds pipelined ...", first
+# commit: the DFlash round policy drives the targets) without giving its
+# rule; reading taken: an exponential average of the accepted drafts a,
+# ema <- ema / 2 + a / 2 in fp32 (the precision the kernel decides in),
+# starting from block - 1, caps the next block at 4 rows (ema < 1.5),
+# 8 rows (ema < 4.5) or 16 rows: m in {3, 7, 15} drafts.
+
+def adaptive_block_cap(ema: float, block: int) -> int:
+    e = np.float32(ema)
+    cap = 4 if e < np.float32(1.5) else (8 if e < np.float32(4.5) else 16)
+    return min(block, cap)
+
+
+def adaptive_ema_update(ema: float, accepted: int) -> float:
+    half = np.float32(0.5)
+    return float(half * np.float32(ema) + half * np.float32(accepted))
+
+
 @dataclass
 class SpecTrace:
     tokens: List[int] = field(default_factory=list)
@@ -522,9 +542,11 @@ def spec_decode(tw: TargetWeights, dw: Optional[DraftWeights], cfg: OracleConfig
     tr = SpecTrace(tokens=[argmax_lowest(logits[-1])], accept_hist=[0] * (B - 1))
     n = len(prompt)
     finished = cfg.eos_id >= 0 and tr.tokens[0] == cfg.eos_id
+    ema = float(np.float32(B - 1))
     while len(tr.tokens) < n_new and not finished:
         t_n = tr.tokens[-1]
-        bl = block_len(B, n_new, len(tr.tokens), cfg.max_seq, n)
+        cap = adaptive_block_cap(ema, B) if cfg.adaptive_block else B
+        bl = block_len(cap, n_new, len(tr.tokens), cfg.max_seq, n)
         if bl <= 1:
             d = []
         elif draft_override is not None:
@@ -535,6 +557,7 @@ def spec_decode(tw: TargetWeights, dw: Optional[DraftWeights], cfg: OracleConfig
         logits, vtaps = target_forward(tw, cfg, [t_n] + d, n, cache)
         y = [argmax_lowest(logits[i]) for i in range(len(d) + 1)]
         a, emitted, finished = accept(d, y, cfg.eos_id)
+        ema = adaptive_ema_update(ema, a)
         for j in range(min(a, len(tr.accept_hist))):
             tr.accept_hist[j] += 1
         # rollback: positions n..n+#emitted-1 hold the confirmed inputs

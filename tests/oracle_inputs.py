@@ -27,7 +27,8 @@ def oracle_config(w: Workload, **kw) -> O.OracleConfig:
         vocab=w.vocab, tgt_layers=w.tgt_layers, drf_layers=w.drf_layers,
         tap_layers=list(w.tap_layers), block=w.block, window=w.window,
         max_seq=w.max_seq, eos_id=w.eos_id, rms_eps=w.rms_eps,
-        rope_theta=w.rope_theta, ctx_norm=w.ctx_norm)
+        rope_theta=w.rope_theta, ctx_norm=w.ctx_norm,
+        adaptive_block=getattr(w, "adaptive_block", False))
     for k, v in kw.items():
         setattr(cfg, k, v)
     return cfg

@@ -34,8 +34,8 @@ def test_header_symbols_exported(capi):
 
 
 def test_struct_sizes_match_header(capi):
-    # 18 int32 fields, the int32 tap array and 2 floats
-    assert C.sizeof(capi.dflash_config) == 4 * (18 + capi.MAX_TAPS + 2)
+    # 19 int32 fields, the int32 tap array and 2 floats
+    assert C.sizeof(capi.dflash_config) == 4 * (19 + capi.MAX_TAPS + 2)
     assert C.sizeof(capi.dflash_weights) == 9 * 8
     assert C.sizeof(capi.dflash_layer) == 18 * 8
     assert C.sizeof(capi.dflash_stats_t) == 8 * (2 + capi.MAX_BLOCK) + 4 * 10

@@ -136,6 +136,46 @@ def test_graphed_loop_equals_greedy(tiny, k):
     dec._round_graph = None
 
 
+def test_adaptive_block_follows_oracle_policy(tiny):
+    """The adaptive block cap on the device: every round's block length is
+    the oracle's policy (adaptive_block_cap / adaptive_ema_update) applied to
+    the acceptances the device saw, under drafts that are the GPU greedy
+    continuation wrong at their first position for the first ten positions
+    (so the cap falls to 4 rows and climbs back); the output is the greedy
+    stream."""
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+    w = TINY.with_(adaptive_block=True)
+    dec = DFlash(w, tiny["m"])
+    P = w.prompt_len
+    gg = dec.greedy(tiny["prompt"], w.n_new)
+    full = tiny["prompt"].tolist() + gg
+    rounds = []
+
+    def draft_fn(d):
+        st = d.stats()
+        if rounds:
+            rounds[-1]["a"] = st.last_accept
+        ids = full[st.n + 1:st.n + st.block_len]
+        if ids and st.n < P + 10:
+            ids[0] = (ids[0] + 1) % w.vocab
+        rounds.append(dict(n=st.n, gen=st.generated, bl=st.block_len))
+        ids = (ids + [0] * w.block)[:w.block - 1]
+        return torch.tensor(ids, dtype=torch.int32, device="cuda")
+
+    out = dec.generate(tiny["prompt"], w.n_new, draft_fn=draft_fn)
+    dec.check()
+    rounds[-1]["a"] = dec.stats().last_accept
+    assert out == gg
+    ema = float(w.block - 1)
+    for r in rounds:
+        want = min(O.adaptive_block_cap(ema, w.block), w.n_new - r["gen"], w.max_seq - r["n"])
+        assert r["bl"] == want, (r, ema)
+        ema = O.adaptive_ema_update(ema, r["a"])
+    bls = [r["bl"] for r in rounds]
+    assert 4 in bls and max(bls[bls.index(4):]) == w.block
+    dec.close()
+
+
 def test_spec_with_adversarial_drafts_equals_greedy(tiny):
     dec, B = tiny["dec"], TINY.block
     gg = dec.greedy(tiny["prompt"], TINY.n_new)

@@ -256,6 +256,38 @@ def test_spec_equals_greedy_with_adversarial_drafts(tiny):
                     assert r["a"] == cut[r["n"]]
 
 
+def test_adaptive_block_spec_equals_greedy_and_follows_the_policy(tiny):
+    """With the adaptive cap the loop stays lossless, and each round's block
+    is min(cap(ema), budget) with ema the halving average of the accepted
+    drafts so far (drafts copied from greedy, wrong at their first position
+    for the first ten positions and right afterwards, so the cap falls to 4
+    rows and climbs back)."""
+    import dataclasses
+    tw, dw, prompt = tiny["tw"], tiny["dw"], tiny["prompt"]
+    cfg = dataclasses.replace(tiny["cfg"], adaptive_block=True)
+    g = O.greedy(tw, cfg, prompt, TINY.n_new)
+    full = list(prompt) + g
+
+    def drafts(t_n, n, bl, hist):
+        d = full[n + 1:n + bl]
+        if d and n < len(prompt) + 10:
+            d[0] = (d[0] + 1) % cfg.vocab
+        return d
+
+    tr = O.spec_decode(tw, dw, cfg, prompt, TINY.n_new, draft_override=drafts)
+    assert tr.tokens == g
+    ema, B = 7.0, cfg.block
+    for r in tr.per_round:
+        gen = r["n"] - len(prompt) + 1
+        want = min(O.adaptive_block_cap(ema, B), TINY.n_new - gen, cfg.max_seq - r["n"])
+        assert r["bl"] == want
+        ema = O.adaptive_ema_update(ema, r["a"])
+    bls = [r["bl"] for r in tr.per_round]
+    assert 4 in bls and bls.index(4) < len(bls) - 1 and max(bls[bls.index(4):]) == cfg.block
+    tr2 = O.spec_decode(tw, dw, cfg, prompt, TINY.n_new)
+    assert tr2.tokens == g
+
+
 def test_spec_eos_and_budget(tiny):
     tw, cfg, prompt = tiny["tw"], tiny["cfg"], tiny["prompt"]
     g = O.greedy(tw, cfg, prompt, 30)

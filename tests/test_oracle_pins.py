@@ -140,3 +140,25 @@ def test_int4_round_trip_bound_and_code_range():
     assert np.all(deq[3, :64] == 0)
     # dequantised values are exact multiples of the bf16 scale
     np.testing.assert_array_equal(deq, codes * s)
+
+
+# ---------------------------------------------------------------- adaptive block
+
+def test_adaptive_block_cap_hand_cases():
+    cases = [(0.0, 16, 4), (1.49, 16, 4), (1.5, 16, 8), (4.49, 16, 8), (4.5, 16, 16),
+             (15.0, 16, 16), (15.0, 8, 8), (0.0, 2, 2)]
+    for ema, block, cap in cases:
+        assert O.adaptive_block_cap(ema, block) == cap, (ema, block)
+
+
+def test_adaptive_ema_is_the_halving_average():
+    """ema_k = ema_{k-1}/2 + a_k/2 from block-1, checked in exact rationals
+    over 20 rounds (every value is a dyadic rational fp32 holds exactly)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(3)
+    ema, exact = float(np.float32(15)), Fraction(15)
+    for _ in range(20):
+        a = int(rng.integers(0, 16))
+        ema = O.adaptive_ema_update(ema, a)
+        exact = exact / 2 + Fraction(a, 2)
+        assert Fraction(ema) == exact
