@@ -457,7 +457,11 @@ def measure_workloads(steps, warmup, base_model):
         taps = synth.tap_rows(w.n_ctx, w.n_taps * w.hidden)
         ext = taps.view(w.n_ctx, w.n_taps, w.hidden).permute(1, 0, 2).contiguous()
         del taps
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
         dec.prefill_taps(ext, hc=1, first_token=17, max_new=64)
+        torch.cuda.synchronize()
+        prefill_s = time.perf_counter() - t0
         del ext
         dec.draft()
         torch.cuda.synchronize()
@@ -468,7 +472,16 @@ def measure_workloads(steps, warmup, base_model):
         kv_bytes = w.drf_layers * 2 * w.n_kv * (ctx_rows + w.block) * w.head_dim * 2
         total = gb + kv_bytes
         dec.check()
+        # prefill of the committed context window: fc over the window's tap
+        # rows + context k/v of every draft layer (dense work, run here as
+        # 16-row chunks of the round's kernels)
+        win_rows = ctx_rows
+        prefill_flop = 2.0 * win_rows * (w.n_taps * w.hidden * w.hidden +
+                                         w.drf_layers * w.hidden * 2 * w.n_kv * w.head_dim)
         out[w.name] = {
+            "window_prefill": {"rows": win_rows, "s": round(prefill_s, 5),
+                               "tflops": round(prefill_flop / prefill_s / 1e12, 2),
+                               "path": "16-row chunks through the skinny GEMM"},
             "draft_rounds_s": round(1e3 / ms, 2), "ms_per_round": round(ms, 4),
             "bytes_per_round": int(total), "hbm_gbs": round(total / (ms / 1e3) / 1e9, 1),
             "frac_of_peak": round(total / (ms / 1e3) / 1e9 / peak, 4),
@@ -643,6 +656,8 @@ def measure_injected(w, model, blocks=(16, 8, 4, "16a"), reps=3):
             ms = a.elapsed_time(b)
             best = ms if best is None else min(best, ms)
         dec.check()
+        st = dec.stats()
+        profile = [round(st.accept_hist[j] / max(1, st.rounds), 3) for j in range(B - 1)]
         ln = log_n[:R, 0].cpu().tolist()
         lt = log_t[:R].cpu().tolist()
         toks = [g[0]]
@@ -654,7 +669,7 @@ def measure_injected(w, model, blocks=(16, 8, 4, "16a"), reps=3):
             "rounds": R, "rounds_s": round(R / (best / 1e3), 2),
             "accepted_tok_s": round(total / (best / 1e3), 2),
             "tokens_per_round": round(total / R, 3), "ms_per_round": round(best / R, 4),
-            "lossless_vs_greedy": bool(lossless)}
+            "accept_profile": profile, "lossless_vs_greedy": bool(lossless)}
         del gr
         dec.close()
     return out
