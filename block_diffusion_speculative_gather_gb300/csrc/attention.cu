@@ -89,11 +89,10 @@ attn_mma_kernel(const __grid_constant__ AttnMaps maps, const AttnMmaArgs a) {
 
 
 // Shared memory of the fused kernel: the q group, two K/V chunk buffers,
-// the split maxima / sums staged for the combine, mbarriers.
+// mbarriers.
 template <int HD>
 constexpr size_t fused_smem(int qrows) {
-    return 1024 + (size_t)(HD / 64) * (qrows + 4 * ATTN_KEYS) * 128 + 2 * (16 * DFL_MAX_ROWS + 64) * 4 +
-           3 * 8 + 64;
+    return 1024 + (size_t)(HD / 64) * (qrows + 4 * ATTN_KEYS) * 128 + 3 * 8 + 64;
 }
 
 template <int HD>
@@ -101,8 +100,6 @@ __global__ void __launch_bounds__(128)
 attn_fused_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) {
     constexpr int C = ATTN_KEYS, HALVES = HD / 64;
     constexpr int MAXS = 64;   // splits a combine folds (host guarantees max_splits <= 64)
-    constexpr int MAXP = 16 * DFL_MAX_ROWS;   // (q head, row) pairs of a group of <= 16 heads
-    constexpr int ENT = MAXP + MAXS;          // staged (pair, split) entries of one CTA
     const AttnMmaArgs& a = f.m;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -111,9 +108,7 @@ attn_fused_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) 
     uint8_t* Qs = sm;                                   // [HALVES][qrows][128 B]
     uint8_t* KV = Qs + HALVES * qrows * 128;            // 2 x (K, V) [HALVES][64][128 B]
     constexpr int KVB = HALVES * C * 128;               // bytes of one K (or V) chunk
-    float* s_m = reinterpret_cast<float*>(KV + 4 * KVB);   // [ENT]
-    float* s_l = s_m + ENT;                                 // [ENT]
-    uint64_t* bar = reinterpret_cast<uint64_t*>(s_l + ENT);   // [0] q, [1..2] buffers
+    uint64_t* bar = reinterpret_cast<uint64_t*>(KV + 4 * KVB);   // [0] q, [1..2] buffers
 
     pdl_trigger();
     pdl_wait();
@@ -190,22 +185,21 @@ attn_fused_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) 
         return;
     }
 
-    // ---- publish this split's (max, sum, output) of rows t = g, g + 8
+    // ---- publish this split's (max, sum) and unnormalised output of rows g, g + 8
+    // partials: outputs [max_splits][16][n_q][HD], then (max, sum) [max_splits][16][n_q]
+    const size_t osplit = (size_t)DFL_MAX_ROWS * a.n_q * HD;
+    float* Op = a.part;
+    float2* MLp = reinterpret_cast<float2*>(a.part + (size_t)f.max_splits * osplit);
     if (warp < group) {
         const int g = lane >> 2, cq = lane & 3, hq = kh * group + warp;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int t = g + 8 * r;
-            float* dst = a.part + (((size_t)sp * DFL_MAX_ROWS + t) * a.n_q + hq) * (HD + 2);
-            if (cq == 0) {
-                dst[0] = m[r];
-                dst[1] = l[r];
-            }
+            float* dst = Op + sp * osplit + ((size_t)t * a.n_q + hq) * HD + 2 * cq;
+            if (cq == 0) MLp[((size_t)sp * DFL_MAX_ROWS + t) * a.n_q + hq] = make_float2(m[r], l[r]);
 #pragma unroll
-            for (int dt = 0; dt < HD / 8; ++dt) {
-                dst[2 + dt * 8 + 2 * cq] = o[dt][2 * r];
-                dst[2 + dt * 8 + 2 * cq + 1] = o[dt][2 * r + 1];
-            }
+            for (int dt = 0; dt < HD / 8; ++dt)
+                *reinterpret_cast<float2*>(dst + dt * 8) = make_float2(o[dt][2 * r], o[dt][2 * r + 1]);
         }
     }
     __threadfence();
@@ -228,69 +222,72 @@ attn_fused_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) 
     if (!s_ok) return;
     __threadfence();
 
-    // ---- combine: pairs (q head of the group, row) p = sp, sp + S, ...
-    // Stage the splits' maxima and sums of all this CTA's pairs, turn them
-    // into weights w = exp(m - M) and per-pair sums L (split order), then
-    // every output element folds the splits in split order.
-    const int pairs = group * DFL_MAX_ROWS;
-    const int my_pairs = (pairs - sp + S - 1) / S;    // my_pairs * S < pairs + S <= ENT
-    float* s_w = s_m;                                 // weights overwrite the maxima
-    __shared__ float s_M[MAXP], s_L[MAXP];
-    auto pair_of = [&](int pi, int* hq, int* t) {
-        const int p = sp + pi * S;
-        *hq = kh * group + p / DFL_MAX_ROWS;
-        *t = p % DFL_MAX_ROWS;
-    };
-    for (int e = tid; e < my_pairs * S; e += blockDim.x) {
-        int hq, t;
-        pair_of(e / S, &hq, &t);
-        const float* src = a.part + (((size_t)(e % S) * DFL_MAX_ROWS + t) * a.n_q + hq) * (HD + 2);
-        s_m[e] = src[0];
-        s_l[e] = src[1];
-    }
-    __syncthreads();
-    for (int pi = tid; pi < my_pairs; pi += blockDim.x) {
-        float M = -INFINITY;
-        for (int j = 0; j < S; ++j) M = fmaxf(M, s_m[pi * S + j]);
-        s_M[pi] = M;
-    }
-    __syncthreads();
-    for (int e = tid; e < my_pairs * S; e += blockDim.x) {
-        const float mj = s_m[e];
-        s_w[e] = mj == -INFINITY ? 0.f : expf(mj - s_M[e / S]);
-    }
-    __syncthreads();
-    for (int pi = tid; pi < my_pairs; pi += blockDim.x) {
-        float L = 0.f;
-        for (int j = 0; j < S; ++j) L = fmaf(s_l[pi * S + j], s_w[pi * S + j], L);
-        s_L[pi] = L;
-    }
-    __syncthreads();
-    const size_t sstride = (size_t)DFL_MAX_ROWS * a.n_q * (HD + 2);
+    // ---- combine: this CTA's (q head of the group, row) pairs p = sp, sp + S, ...,
+    // one warp per pair.  Lane j holds split j's (and j + 32's) max and sum;
+    // with M the maximum, split j weighs w_j = exp(m_j - M), the row's sum is
+    // L = sum_j w_j l_j, and lane d folds output columns 4d..4d+3 over the
+    // splits in split order.  All loads of a batch are independent, so a
+    // pair costs about two L2 round trips whatever S is.
+    constexpr int NV = HD / 4;        // float4 columns of one output row
+    constexpr int BATCH = 8;          // splits loaded per batch
     const size_t ld = (size_t)a.n_q * HD;
-    for (int e = tid; e < my_pairs * HD; e += blockDim.x) {
-        const int pi = e / HD, d = e % HD;
-        int hq, t;
-        pair_of(pi, &hq, &t);
-        const size_t col = (size_t)hq * HD + d;
+    const int pairs = group * DFL_MAX_ROWS;
+    for (int p = sp + warp * S; p < pairs; p += 4 * S) {
+        const int hq = kh * group + p / DFL_MAX_ROWS, t = p % DFL_MAX_ROWS;
+        const size_t col = (size_t)hq * HD + 4 * lane;
         if (t >= T) {
-            store_act(f.out, f.out_type, ld, t, col, 0.f);
+            if (lane < NV)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) store_act(f.out, f.out_type, ld, t, col + e, 0.f);
             continue;
         }
-        const float* src = a.part + ((size_t)t * a.n_q + hq) * (HD + 2) + 2 + d;
-        const float* w = s_w + pi * S;
-        float O = 0.f;
-        int j = 0;
-        for (; j + 4 <= S; j += 4) {
-            const float o0 = src[(j + 0) * sstride], o1 = src[(j + 1) * sstride];
-            const float o2 = src[(j + 2) * sstride], o3 = src[(j + 3) * sstride];
-            O = fmaf(o0, w[j + 0], O);
-            O = fmaf(o1, w[j + 1], O);
-            O = fmaf(o2, w[j + 2], O);
-            O = fmaf(o3, w[j + 3], O);
+        const float2* ml = MLp + (size_t)t * a.n_q + hq;
+        const size_t mls = (size_t)DFL_MAX_ROWS * a.n_q;
+        const float2 ml0 = lane < S ? __ldcg(ml + lane * mls) : make_float2(-INFINITY, 0.f);
+        const float2 ml1 = lane + 32 < S ? __ldcg(ml + (lane + 32) * mls) : make_float2(-INFINITY, 0.f);
+        const float4* src = reinterpret_cast<const float4*>(Op + ((size_t)t * a.n_q + hq) * HD) + lane;
+        const size_t sst = osplit / 4;
+        float4 v[BATCH];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u)
+            v[u] = (u < S && lane < NV) ? __ldcg(src + u * sst) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float M = fmaxf(ml0.x, ml1.x);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float w0 = ml0.x == -INFINITY ? 0.f : expf(ml0.x - M);
+        const float w1 = ml1.x == -INFINITY ? 0.f : expf(ml1.x - M);
+        float L = fmaf(w1, ml1.y, w0 * ml0.y);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j0 = 0; j0 < S; j0 += BATCH) {
+            float4 nv[BATCH];
+            const int j1 = j0 + BATCH;
+#pragma unroll
+            for (int u = 0; u < BATCH; ++u)   // next batch in flight while this one folds
+                nv[u] = (j1 + u < S && lane < NV) ? __ldcg(src + (size_t)(j1 + u) * sst)
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < BATCH; ++u) {
+                const int j = j0 + u;
+                const float wa = __shfl_sync(0xffffffffu, w0, j & 31);
+                const float wb = __shfl_sync(0xffffffffu, w1, j & 31);
+                const float wj = j < 32 ? wa : wb;
+                O.x = fmaf(v[u].x, wj, O.x);
+                O.y = fmaf(v[u].y, wj, O.y);
+                O.z = fmaf(v[u].z, wj, O.z);
+                O.w = fmaf(v[u].w, wj, O.w);
+            }
+#pragma unroll
+            for (int u = 0; u < BATCH; ++u) v[u] = nv[u];
         }
-        for (; j < S; ++j) O = fmaf(src[j * sstride], w[j], O);
-        store_act(f.out, f.out_type, ld, t, col, O / s_L[pi]);
+        if (lane < NV) {
+            const float inv = 1.f / L;
+            store_act(f.out, f.out_type, ld, t, col + 0, O.x * inv);
+            store_act(f.out, f.out_type, ld, t, col + 1, O.y * inv);
+            store_act(f.out, f.out_type, ld, t, col + 2, O.z * inv);
+            store_act(f.out, f.out_type, ld, t, col + 3, O.w * inv);
+        }
     }
     // the last split of the head to finish resets the head's counters
     if (tid == 0) {
