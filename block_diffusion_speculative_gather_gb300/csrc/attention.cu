@@ -111,9 +111,26 @@ attn_fused_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) 
     uint64_t* bar = reinterpret_cast<uint64_t*>(KV + 4 * KVB);   // [0] q, [1..2] buffers
 
     pdl_trigger();
-    pdl_wait();
     const int kh = blockIdx.x, sp = blockIdx.y, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    // When the first visible key is 0 (causal, or no window) a split's chunks
+    // sit at fixed positions, so they can be brought into L2 while the
+    // predecessor still writes this forward's rows (L2 stays coherent with
+    // those writes; the copies into shared memory come after the wait).
+    if (tid == 0 && (a.causal || a.window <= 0)) {
+        const int np = min(f.split_chunks, 2);
+        for (int i = 0; i < np; ++i) {
+            const int c = sp * f.split_chunks + i;
+            const int krow = ((a.layer * 2 + 0) * a.n_kv + kh) * a.cap + c * C;
+            const int vrow = ((a.layer * 2 + 1) * a.n_kv + kh) * a.cap + c * C;
+#pragma unroll
+            for (int h = 0; h < HALVES; ++h) {
+                tma_prefetch_l2_2d(&maps.kv, 64 * h, krow);
+                tma_prefetch_l2_2d(&maps.kv, 64 * h, vrow);
+            }
+        }
+    }
+    pdl_wait();
     const int T = a.st->fwd_T, pos0 = a.st->fwd_pos0;
     if (T == 0) return;
     const int hi = pos0 + T;
@@ -202,7 +219,7 @@ attn_fused_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) 
                 *reinterpret_cast<float2*>(dst + dt * 8) = make_float2(o[dt][2 * r], o[dt][2 * r + 1]);
         }
     }
-    __threadfence();
+    // the barrier orders every thread's stores before thread 0's release add
     __syncthreads();
     __shared__ int s_ok;
     if (tid == 0) {
@@ -218,18 +235,17 @@ attn_fused_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) 
         }
         s_ok = got ? 1 : 0;
     }
-    __syncthreads();
+    __syncthreads();   // thread 0's acquire orders the partial loads below
     if (!s_ok) return;
-    __threadfence();
 
     // ---- combine: this CTA's (q head of the group, row) pairs p = sp, sp + S, ...,
     // one warp per pair.  Lane j holds split j's (and j + 32's) max and sum;
-    // with M the maximum, split j weighs w_j = exp(m_j - M), the row's sum is
+    // with M the maximum, split j weighs w_j = 2^(m_j - M), the row's sum is
     // L = sum_j w_j l_j, and lane d folds output columns 4d..4d+3 over the
     // splits in split order.  All loads of a batch are independent, so a
     // pair costs about two L2 round trips whatever S is.
     constexpr int NV = HD / 4;        // float4 columns of one output row
-    constexpr int BATCH = 8;          // splits loaded per batch
+    constexpr int BATCH = 16;         // splits loaded per batch
     const size_t ld = (size_t)a.n_q * HD;
     const int pairs = group * DFL_MAX_ROWS;
     for (int p = sp + warp * S; p < pairs; p += 4 * S) {
@@ -254,8 +270,8 @@ attn_fused_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) 
         float M = fmaxf(ml0.x, ml1.x);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        const float w0 = ml0.x == -INFINITY ? 0.f : expf(ml0.x - M);
-        const float w1 = ml1.x == -INFINITY ? 0.f : expf(ml1.x - M);
+        const float w0 = ml0.x == -INFINITY ? 0.f : exp2f(ml0.x - M);   // maxima are base-2
+        const float w1 = ml1.x == -INFINITY ? 0.f : exp2f(ml1.x - M);
         float L = fmaf(w1, ml1.y, w0 * ml0.y);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);

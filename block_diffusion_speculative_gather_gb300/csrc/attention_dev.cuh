@@ -136,10 +136,14 @@ __device__ __forceinline__ void chunk_partials(const uint8_t* Qs, const uint8_t*
 
 // One 64-key chunk folded into a running softmax state (online softmax):
 // m[r], l[r] are the running max and sum of rows g, g + 8 of q head
-// kh * group + warp and o the unnormalised output.  A key that is masked
-// for a row weighs exactly 0, and a chunk masked entirely for a row leaves
-// that row's state bit-identical, so a row's result does not depend on how
-// many rows the forward has.
+// kh * group + warp and o the unnormalised output.  Scores are kept in the
+// base-2 domain (scaled by scale * log2 e, so p = 2^(s - m)).  A key that is
+// masked for a row weighs exactly 0, and a chunk masked entirely for a row
+// leaves that row's state bit-identical, so a row's result does not depend
+// on how many rows the forward has.  A chunk every row sees whole (all its
+// keys inside the window and before the first query) skips the mask; for a
+// row that sees it whole the masked path computes the same values, and rows
+// t >= T are never read.
 template <int HD>
 __device__ __forceinline__ void chunk_online(const uint8_t* Qs, const uint8_t* Ks, const uint8_t* Vs,
                                              const AttnMmaArgs& a, int qrows, int c, int T, int pos0,
@@ -148,6 +152,7 @@ __device__ __forceinline__ void chunk_online(const uint8_t* Qs, const uint8_t* K
     constexpr int C = ATTN_KEYS;
     const int k0 = c * C;
     const int g = lane >> 2, cq = lane & 3;
+    const float sl2 = a.scale * 1.4426950408889634f;
     float s[8][4];
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt)
@@ -167,24 +172,35 @@ __device__ __forceinline__ void chunk_online(const uint8_t* Qs, const uint8_t* K
             mma_f16_16816(s[2 * np + 1], qa, b1);
         }
     }
+    const bool whole = k0 >= lo && (a.causal ? k0 + C - 1 <= pos0 : k0 + C <= hi);
     float mc[2] = {-INFINITY, -INFINITY};
+    if (whole) {
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int t = g + 8 * (e >> 1);
-            const int key = k0 + nt * 8 + 2 * cq + (e & 1);
-            const bool valid = t < T && key >= lo && key < hi && (!a.causal || key <= pos0 + t);
-            s[nt][e] = valid ? s[nt][e] * a.scale : -INFINITY;
-            mc[e >> 1] = fmaxf(mc[e >> 1], s[nt][e]);
-        }
+            for (int e = 0; e < 4; ++e) {
+                s[nt][e] *= sl2;
+                mc[e >> 1] = fmaxf(mc[e >> 1], s[nt][e]);
+            }
+    } else {
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int t = g + 8 * (e >> 1);
+                const int key = k0 + nt * 8 + 2 * cq + (e & 1);
+                const bool valid = t < T && key >= lo && key < hi && (!a.causal || key <= pos0 + t);
+                s[nt][e] = valid ? s[nt][e] * sl2 : -INFINITY;
+                mc[e >> 1] = fmaxf(mc[e >> 1], s[nt][e]);
+            }
+    }
     float mn[2], alpha[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         mc[r] = fmaxf(mc[r], __shfl_xor_sync(0xffffffffu, mc[r], 1));
         mc[r] = fmaxf(mc[r], __shfl_xor_sync(0xffffffffu, mc[r], 2));
         mn[r] = fmaxf(m[r], mc[r]);
-        alpha[r] = (mn[r] == m[r]) ? 1.f : expf(m[r] - mn[r]);   // m = -inf -> 0
+        alpha[r] = (mn[r] == m[r]) ? 1.f : exp2f(m[r] - mn[r]);   // m = -inf -> 0
     }
     float ls[2] = {0.f, 0.f};
     uint32_t pa[4][4];
@@ -193,7 +209,7 @@ __device__ __forceinline__ void chunk_online(const uint8_t* Qs, const uint8_t* K
         float p[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            p[e] = s[nt][e] == -INFINITY ? 0.f : expf(s[nt][e] - mn[e >> 1]);
+            p[e] = (!whole && s[nt][e] == -INFINITY) ? 0.f : exp2f(s[nt][e] - mn[e >> 1]);
             ls[e >> 1] += p[e];
         }
         const int kk = nt >> 1, hi8 = nt & 1;

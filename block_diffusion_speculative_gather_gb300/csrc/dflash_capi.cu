@@ -162,6 +162,8 @@ int validate(const dflash_config* c) {
     if (c->max_seq < 2) return fail(DFLASH_ERR_CONFIG, "max_seq %d", c->max_seq);
     if (c->window < 0) return fail(DFLASH_ERR_CONFIG, "window %d", c->window);
     if (c->dtype != DFLASH_F32 && c->dtype != DFLASH_BF16) return fail(DFLASH_ERR_CONFIG, "dtype %d: F32 or BF16", c->dtype);
+    if (c->dtype == DFLASH_BF16 && c->n_q / c->n_kv > 4)
+        return fail(DFLASH_ERR_CONFIG, "%d q heads per kv head: the BF16 attention takes at most 4", c->n_q / c->n_kv);
     if (c->drf_layers > 0) {
         if (c->n_taps < 1 || c->n_taps > DFLASH_MAX_TAPS) return fail(DFLASH_ERR_CONFIG, "n_taps %d: 1..8", c->n_taps);
         for (int i = 0; i < c->n_taps; ++i) {

@@ -68,7 +68,9 @@ enum { DFLASH_F32 = 0, DFLASH_BF16 = 1, DFLASH_INT4G64 = 2 };
 
 /* Model and run configuration (Qwen3-shaped target and drafter). */
 typedef struct {
-    int32_t hidden, n_q, n_kv, head_dim, ffn, vocab;
+    int32_t hidden, n_q, n_kv, head_dim, ffn, vocab;   /* n_q a multiple of n_kv; with
+                        * dtype BF16 at most 4 q heads per kv head (one warp of the
+                        * tensor-core attention per q head), else at most 16 */
     int32_t tgt_layers;                 /* 0 = drafter alone (taps supplied by caller) */
     int32_t drf_layers;                 /* 0 = target alone */
     int32_t n_taps;                     /* tap layers; taps concatenate in this order */

@@ -69,6 +69,15 @@ def test_config_guard_rejects_before_buffers(capi, field, value):
     assert out.value is None
 
 
+def test_bf16_query_group_guard(capi):
+    # the tensor-core attention gives one warp to each q head of a kv head's group
+    from block_diffusion_speculative_gather_gb300.configs import E2E_BF16
+    from block_diffusion_speculative_gather_gb300.runtime import make_config
+    assert capi.dflash_workspace_bytes(make_config(E2E_BF16)) > 0          # 32 / 8
+    assert capi.dflash_workspace_bytes(make_config(E2E_BF16, n_kv=4)) == 0  # 32 / 4
+    assert capi.dflash_workspace_bytes(_cfg(capi, n_q=16, n_kv=2)) > 0     # fp32: 8 per kv head
+
+
 def test_tap_layer_guard(capi):
     cfg = _cfg(capi)
     cfg.tap_layer[1] = 5            # beyond the 2-layer target
