@@ -17,6 +17,7 @@
 
 #include "attention_dev.cuh"
 #include "gemm.cuh"
+#include "tc_dev.cuh"
 
 namespace dfl {
 
@@ -87,6 +88,114 @@ attn_mma_kernel(const __grid_constant__ AttnMaps maps, const AttnMmaArgs a) {
     adev::chunk_partials<HD>(Qs, Ks, Vs, a, qrows, group, kh, c, T, pos0, lo, hi, warp, lane);
 }
 
+
+// Second half of a split-KV attention launch: once every split of kv head
+// kh has published its (max, sum) and unnormalised output into the partials
+// (outputs [max_splits][16][n_q][HD], then (max, sum) [max_splits][16][n_q],
+// maxima in the base-2 domain), CTA sp normalises its share of the group's
+// (q head, row) pairs.  Called by all threads after their stores.
+template <int HD>
+__device__ __forceinline__ void exchange_combine(const AttnFusedArgs& f, int kh, int sp, int S, int T,
+                                                 int group, int tid, int warp, int lane) {
+    const AttnMmaArgs& a = f.m;
+    const size_t osplit = (size_t)DFL_MAX_ROWS * a.n_q * HD;
+    const float* Op = a.part;
+    const float2* MLp = reinterpret_cast<const float2*>(a.part + (size_t)f.max_splits * osplit);
+    // the barrier orders every thread's stores before thread 0's release add
+    __syncthreads();
+    __shared__ int s_ok;
+    if (tid == 0) {
+        red_release_add_s32_(&f.arrive[kh], 1);
+        bool got = ld_acquire_s32_(&f.arrive[kh]) >= S;
+        const uint64_t t0 = globaltimer_ns();
+        while (!got) {
+            got = ld_acquire_s32_(&f.arrive[kh]) >= S;
+            if (!got && globaltimer_ns() - t0 > 2000000000ull) {
+                set_error(a.st, DERR_TIMEOUT, 211);
+                break;
+            }
+        }
+        s_ok = got ? 1 : 0;
+    }
+    __syncthreads();   // thread 0's acquire orders the partial loads below
+    if (!s_ok) return;
+
+    // ---- combine: this CTA's (q head of the group, row) pairs p = sp, sp + S, ...,
+    // one warp per pair.  Lane j holds split j's (and j + 32's) max and sum;
+    // with M the maximum, split j weighs w_j = 2^(m_j - M), the row's sum is
+    // L = sum_j w_j l_j, and lane d folds output columns 4d..4d+3 over the
+    // splits in split order.  All loads of a batch are independent, so a
+    // pair costs about two L2 round trips whatever S is.
+    constexpr int NV = HD / 4;        // float4 columns of one output row
+    constexpr int BATCH = 16;         // splits loaded per batch
+    const size_t ld = (size_t)a.n_q * HD;
+    const int pairs = group * DFL_MAX_ROWS;
+    for (int p = sp + warp * S; p < pairs; p += 4 * S) {
+        const int hq = kh * group + p / DFL_MAX_ROWS, t = p % DFL_MAX_ROWS;
+        const size_t col = (size_t)hq * HD + 4 * lane;
+        if (t >= T) {
+            if (lane < NV)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) store_act(f.out, f.out_type, ld, t, col + e, 0.f);
+            continue;
+        }
+        const float2* ml = MLp + (size_t)t * a.n_q + hq;
+        const size_t mls = (size_t)DFL_MAX_ROWS * a.n_q;
+        const float2 ml0 = lane < S ? __ldcg(ml + lane * mls) : make_float2(-INFINITY, 0.f);
+        const float2 ml1 = lane + 32 < S ? __ldcg(ml + (lane + 32) * mls) : make_float2(-INFINITY, 0.f);
+        const float4* src = reinterpret_cast<const float4*>(Op + ((size_t)t * a.n_q + hq) * HD) + lane;
+        const size_t sst = osplit / 4;
+        float4 v[BATCH];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u)
+            v[u] = (u < S && lane < NV) ? __ldcg(src + u * sst) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float M = fmaxf(ml0.x, ml1.x);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float w0 = ml0.x == -INFINITY ? 0.f : exp2f(ml0.x - M);   // maxima are base-2
+        const float w1 = ml1.x == -INFINITY ? 0.f : exp2f(ml1.x - M);
+        float L = fmaf(w1, ml1.y, w0 * ml0.y);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j0 = 0; j0 < S; j0 += BATCH) {
+            float4 nv[BATCH];
+            const int j1 = j0 + BATCH;
+#pragma unroll
+            for (int u = 0; u < BATCH; ++u)   // next batch in flight while this one folds
+                nv[u] = (j1 + u < S && lane < NV) ? __ldcg(src + (size_t)(j1 + u) * sst)
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < BATCH; ++u) {
+                const int j = j0 + u;
+                const float wa = __shfl_sync(0xffffffffu, w0, j & 31);
+                const float wb = __shfl_sync(0xffffffffu, w1, j & 31);
+                const float wj = j < 32 ? wa : wb;
+                O.x = fmaf(v[u].x, wj, O.x);
+                O.y = fmaf(v[u].y, wj, O.y);
+                O.z = fmaf(v[u].z, wj, O.z);
+                O.w = fmaf(v[u].w, wj, O.w);
+            }
+#pragma unroll
+            for (int u = 0; u < BATCH; ++u) v[u] = nv[u];
+        }
+        if (lane < NV) {
+            const float inv = 1.f / L;
+            store_act(f.out, f.out_type, ld, t, col + 0, O.x * inv);
+            store_act(f.out, f.out_type, ld, t, col + 1, O.y * inv);
+            store_act(f.out, f.out_type, ld, t, col + 2, O.z * inv);
+            store_act(f.out, f.out_type, ld, t, col + 3, O.w * inv);
+        }
+    }
+    // the last split of the head to finish resets the head's counters
+    if (tid == 0) {
+        const int old = atomicAdd(&f.done[kh], 1);
+        if (old == S - 1) {
+            f.arrive[kh] = 0;
+            f.done[kh] = 0;
+        }
+    }
+}
 
 // Shared memory of the fused kernel: the q group, two K/V chunk buffers,
 // mbarriers.
@@ -219,100 +328,221 @@ attn_fused_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) 
                 *reinterpret_cast<float2*>(dst + dt * 8) = make_float2(o[dt][2 * r], o[dt][2 * r + 1]);
         }
     }
-    // the barrier orders every thread's stores before thread 0's release add
-    __syncthreads();
-    __shared__ int s_ok;
-    if (tid == 0) {
-        red_release_add_s32_(&f.arrive[kh], 1);
-        bool got = ld_acquire_s32_(&f.arrive[kh]) >= S;
-        const uint64_t t0 = globaltimer_ns();
-        while (!got) {
-            got = ld_acquire_s32_(&f.arrive[kh]) >= S;
-            if (!got && globaltimer_ns() - t0 > 2000000000ull) {
-                set_error(a.st, DERR_TIMEOUT, 211);
-                break;
-            }
-        }
-        s_ok = got ? 1 : 0;
-    }
-    __syncthreads();   // thread 0's acquire orders the partial loads below
-    if (!s_ok) return;
+    exchange_combine<HD>(f, kh, sp, S, T, group, tid, warp, lane);
+}
 
-    // ---- combine: this CTA's (q head of the group, row) pairs p = sp, sp + S, ...,
-    // one warp per pair.  Lane j holds split j's (and j + 32's) max and sum;
-    // with M the maximum, split j weighs w_j = 2^(m_j - M), the row's sum is
-    // L = sum_j w_j l_j, and lane d folds output columns 4d..4d+3 over the
-    // splits in split order.  All loads of a batch are independent, so a
-    // pair costs about two L2 round trips whatever S is.
-    constexpr int NV = HD / 4;        // float4 columns of one output row
-    constexpr int BATCH = 16;         // splits loaded per batch
-    const size_t ld = (size_t)a.n_q * HD;
-    const int pairs = group * DFL_MAX_ROWS;
-    for (int p = sp + warp * S; p < pairs; p += 4 * S) {
-        const int hq = kh * group + p / DFL_MAX_ROWS, t = p % DFL_MAX_ROWS;
-        const size_t col = (size_t)hq * HD + 4 * lane;
-        if (t >= T) {
-            if (lane < NV)
+// Tensor-core (tcgen05) form of the fused attention for splits of one
+// 64-key chunk.  TMA brings each q head's 16 rows to tile rows 32h..32h+15
+// (so the score row of q head h, token t lands in tensor-memory lane 32h + t
+// and warp h owns head h), and the chunk's K and V.  One thread issues
+// S = Q K^T (M 128, N 64) into tensor memory while the CTA transposes V into
+// a K-major tile; each thread of a real row then reads its 64 scores, masks,
+// takes the row max and the base-2 exponentials in registers, and writes its
+// f16 probabilities as the A tile of O = P V (M 128, N head_dim), which the
+// tensor core accumulates in f32.  The rows' (max, sum, unnormalised
+// output) are published like the mma.sync form's and combined the same way.
+template <int HD>
+constexpr size_t tc_smem() {
+    return 1024 + (size_t)(HD / 64) * (128 + 2 * ATTN_KEYS) * 128 + (size_t)HD * 128 + 128 * 128 + 3 * 8 +
+           8 + 64;
+}
+template <int HD>
+constexpr uint32_t tc_cols() { return HD == 128 ? 256u : 128u; }   // S (64) + O (HD), power of two
+
+template <int HD>
+__global__ void __launch_bounds__(128)
+attn_tc_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) {
+    constexpr int C = ATTN_KEYS, HALVES = HD / 64;
+    constexpr int MAXS = 64;
+    constexpr uint32_t TCOLS = tc_cols<HD>();
+    const AttnMmaArgs& a = f.m;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* Qs = sm;                          // [HALVES][128 rows][128 B]
+    uint8_t* Ks = Qs + HALVES * 128 * 128;     // [HALVES][64 keys][128 B]
+    uint8_t* Vs = Ks + HALVES * C * 128;       // [HALVES][64 keys][128 B]
+    uint8_t* Vt = Vs + HALVES * C * 128;       // [HD][128 B]: V^T, 64 keys per row
+    uint8_t* Ps = Vt + HD * 128;               // [128 rows][128 B]: f16 probabilities
+    uint64_t* bar = reinterpret_cast<uint64_t*>(Ps + 128 * 128);   // [0] loads, [1] S, [2] O
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar + 3);
+
+    pdl_trigger();
+    const int kh = blockIdx.x, sp = blockIdx.y, tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    if (tid == 0 && (a.causal || a.window <= 0)) {   // split sp is chunk sp (see the mma.sync form)
+        const int krow = ((a.layer * 2 + 0) * a.n_kv + kh) * a.cap + sp * C;
+        const int vrow = ((a.layer * 2 + 1) * a.n_kv + kh) * a.cap + sp * C;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) store_act(f.out, f.out_type, ld, t, col + e, 0.f);
-            continue;
-        }
-        const float2* ml = MLp + (size_t)t * a.n_q + hq;
-        const size_t mls = (size_t)DFL_MAX_ROWS * a.n_q;
-        const float2 ml0 = lane < S ? __ldcg(ml + lane * mls) : make_float2(-INFINITY, 0.f);
-        const float2 ml1 = lane + 32 < S ? __ldcg(ml + (lane + 32) * mls) : make_float2(-INFINITY, 0.f);
-        const float4* src = reinterpret_cast<const float4*>(Op + ((size_t)t * a.n_q + hq) * HD) + lane;
-        const size_t sst = osplit / 4;
-        float4 v[BATCH];
-#pragma unroll
-        for (int u = 0; u < BATCH; ++u)
-            v[u] = (u < S && lane < NV) ? __ldcg(src + u * sst) : make_float4(0.f, 0.f, 0.f, 0.f);
-        float M = fmaxf(ml0.x, ml1.x);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        const float w0 = ml0.x == -INFINITY ? 0.f : exp2f(ml0.x - M);   // maxima are base-2
-        const float w1 = ml1.x == -INFINITY ? 0.f : exp2f(ml1.x - M);
-        float L = fmaf(w1, ml1.y, w0 * ml0.y);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j0 = 0; j0 < S; j0 += BATCH) {
-            float4 nv[BATCH];
-            const int j1 = j0 + BATCH;
-#pragma unroll
-            for (int u = 0; u < BATCH; ++u)   // next batch in flight while this one folds
-                nv[u] = (j1 + u < S && lane < NV) ? __ldcg(src + (size_t)(j1 + u) * sst)
-                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int u = 0; u < BATCH; ++u) {
-                const int j = j0 + u;
-                const float wa = __shfl_sync(0xffffffffu, w0, j & 31);
-                const float wb = __shfl_sync(0xffffffffu, w1, j & 31);
-                const float wj = j < 32 ? wa : wb;
-                O.x = fmaf(v[u].x, wj, O.x);
-                O.y = fmaf(v[u].y, wj, O.y);
-                O.z = fmaf(v[u].z, wj, O.z);
-                O.w = fmaf(v[u].w, wj, O.w);
-            }
-#pragma unroll
-            for (int u = 0; u < BATCH; ++u) v[u] = nv[u];
-        }
-        if (lane < NV) {
-            const float inv = 1.f / L;
-            store_act(f.out, f.out_type, ld, t, col + 0, O.x * inv);
-            store_act(f.out, f.out_type, ld, t, col + 1, O.y * inv);
-            store_act(f.out, f.out_type, ld, t, col + 2, O.z * inv);
-            store_act(f.out, f.out_type, ld, t, col + 3, O.w * inv);
+        for (int h = 0; h < HALVES; ++h) {
+            tma_prefetch_l2_2d(&maps.kv, 64 * h, krow);
+            tma_prefetch_l2_2d(&maps.kv, 64 * h, vrow);
         }
     }
-    // the last split of the head to finish resets the head's counters
+    pdl_wait();
+    const int T = a.st->fwd_T, pos0 = a.st->fwd_pos0;
+    if (T == 0) return;
+    const int hi = pos0 + T;
+    const int lo = (!a.causal && a.window > 0) ? max(0, pos0 - a.window) : 0;
+    const int c_lo = lo / C, c_hi = (hi - 1) / C;
+    const int S = c_hi - c_lo + 1;   // one chunk per split
+    if (sp >= S) return;
+    if (S > MAXS || S > f.max_splits) {
+        if (tid == 0) set_error(a.st, DERR_INDEX, S);
+        return;
+    }
+    const int k0 = (c_lo + sp) * C;
+    const int group = a.n_q / a.n_kv;
+
     if (tid == 0) {
-        const int old = atomicAdd(&f.done[kh], 1);
-        if (old == S - 1) {
-            f.arrive[kh] = 0;
-            f.done[kh] = 0;
+        for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tc::tmem_alloc(s_tmem, TCOLS);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = *s_tmem;
+    if (tid == 0) {
+        const int krow = ((a.layer * 2 + 0) * a.n_kv + kh) * a.cap + k0;
+        const int vrow = ((a.layer * 2 + 1) * a.n_kv + kh) * a.cap + k0;
+        mbar_arrive_expect_tx(&bar[0], HALVES * (group * 16 + 2 * C) * 128);
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h) {
+            for (int q = 0; q < group; ++q)
+                tma_load_2d(Qs + h * 128 * 128 + q * 32 * 128, &maps.q16, &bar[0], 64 * h,
+                            (kh * group + q) * 16);
+            tma_load_2d(Ks + h * C * 128, &maps.kv, &bar[0], 64 * h, krow);
+            tma_load_2d(Vs + h * C * 128, &maps.kv, &bar[0], 64 * h, vrow);
         }
     }
+    // every wait is voted on by the whole CTA, so all threads leave together
+    bool ok = __syncthreads_and(mbar_wait_bounded(&bar[0], 0)) != 0;
+    const bool s_issued = ok;
+    if (ok && tid == 0) {   // S = Q K^T while the CTA transposes V
+        tc::fence_after_sync();
+        constexpr uint32_t IS = tc::idesc_f16_f32(128, C);
+#pragma unroll
+        for (int kd = 0; kd < HD / 16; ++kd) {
+            const int h = kd >> 2, ko = (kd & 3) * 32;
+            tc::mma_f16(tm, tc::desc_sw128(Qs + h * 128 * 128 + ko), tc::desc_sw128(Ks + h * C * 128 + ko),
+                        IS, kd > 0 ? 1u : 0u);
+        }
+        tc::commit(&bar[1]);
+    }
+    if (ok && tid < HD) {   // V^T row d = tid: the chunk's 64 keys of column d
+        const int h = tid >> 6, dd = tid & 63, ch = dd >> 3;
+        const uint8_t* vb = Vs + h * C * 128 + (dd & 7) * 2;
+        uint32_t w[32];
+#pragma unroll
+        for (int k2 = 0; k2 < 32; ++k2) {
+            const int k = 2 * k2;
+            const uint32_t x0 = *reinterpret_cast<const uint16_t*>(vb + k * 128 + ((ch ^ (k & 7)) << 4));
+            const uint32_t x1 =
+                *reinterpret_cast<const uint16_t*>(vb + (k + 1) * 128 + ((ch ^ ((k + 1) & 7)) << 4));
+            w[k2] = x0 | (x1 << 16);
+        }
+        uint8_t* row = Vt + tid * 128;
+#pragma unroll
+        for (int kc = 0; kc < 8; ++kc)
+            *reinterpret_cast<uint4*>(row + ((kc ^ (tid & 7)) << 4)) =
+                make_uint4(w[4 * kc], w[4 * kc + 1], w[4 * kc + 2], w[4 * kc + 3]);
+    }
+    tc::fence_async_smem();   // V^T visible to the tensor core
+    if (ok) ok = __syncthreads_and(mbar_wait_bounded(&bar[1], 0)) != 0;
+    tc::fence_after_sync();
+
+    // ---- softmax of this thread's score row (q head `warp`, token `lane`)
+    const bool mine = warp < group && lane < 16;
+    float m_r = -INFINITY, l_r = 0.f;
+    if (ok && warp < group) {
+        float s0[32], s1[32];
+        const uint32_t trow = tm + ((uint32_t)(warp * 32) << 16);
+        tc::ld_x32(trow, s0);
+        tc::ld_x32(trow + 32, s1);
+        if (mine) {
+            const int t = lane;
+            const float sl2 = a.scale * 1.4426950408889634f;
+            const int kmax = a.causal ? min(hi - 1, pos0 + t) : hi - 1;
+            const bool whole = t < T && k0 >= lo && k0 + C - 1 <= kmax;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < C; ++j) {
+                float v = (j < 32 ? s0[j & 31] : s1[j & 31]) * sl2;
+                if (!whole) {
+                    const int key = k0 + j;
+                    if (!(t < T && key >= lo && key <= kmax)) v = -INFINITY;
+                }
+                if (j < 32) s0[j & 31] = v; else s1[j & 31] = v;
+                mx = fmaxf(mx, v);
+            }
+            float sum = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int j2 = 0; j2 < 32; ++j2) {
+                const float v0 = j2 < 16 ? s0[(2 * j2) & 31] : s1[(2 * j2) & 31];
+                const float v1 = j2 < 16 ? s0[(2 * j2 + 1) & 31] : s1[(2 * j2 + 1) & 31];
+                const float p0 = v0 == -INFINITY ? 0.f : exp2f(v0 - mx);
+                const float p1 = v1 == -INFINITY ? 0.f : exp2f(v1 - mx);
+                sum += p0;
+                sum += p1;
+                pk[j2] = pack_f16x2(p0, p1);
+            }
+            uint8_t* prow = Ps + tid * 128;
+#pragma unroll
+            for (int kc = 0; kc < 8; ++kc)
+                *reinterpret_cast<uint4*>(prow + ((kc ^ (tid & 7)) << 4)) =
+                    make_uint4(pk[4 * kc], pk[4 * kc + 1], pk[4 * kc + 2], pk[4 * kc + 3]);
+            m_r = mx;
+            l_r = sum;
+        }
+    }
+    tc::fence_async_smem();   // P visible to the tensor core
+    tc::fence_before_sync();
+    __syncthreads();
+    const bool o_issued = ok;
+    if (ok && tid == 0) {   // O = P V
+        tc::fence_after_sync();
+        constexpr uint32_t IO = tc::idesc_f16_f32(128, HD);
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)
+            tc::mma_f16(tm + C, tc::desc_sw128(Ps + kk * 32), tc::desc_sw128(Vt + kk * 32), IO,
+                        kk > 0 ? 1u : 0u);
+        tc::commit(&bar[2]);
+    }
+    if (ok) ok = __syncthreads_and(mbar_wait_bounded(&bar[2], 0)) != 0;
+    tc::fence_after_sync();
+
+    // ---- publish (max, sum) and the unnormalised output row
+    const size_t osplit = (size_t)DFL_MAX_ROWS * a.n_q * HD;
+    float* Op = a.part;
+    float2* MLp = reinterpret_cast<float2*>(a.part + (size_t)f.max_splits * osplit);
+    if (ok && warp < group) {
+        const int t = lane, hq = kh * group + warp;
+        float* dst = Op + sp * osplit + ((size_t)t * a.n_q + hq) * HD;
+        const uint32_t trow = tm + ((uint32_t)(warp * 32) << 16) + C;
+#pragma unroll
+        for (int q = 0; q < HD / 32; ++q) {
+            float v[32];
+            tc::ld_x32(trow + 32 * q, v);
+            if (mine)
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                    *reinterpret_cast<float4*>(dst + 32 * q + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        }
+        if (mine) MLp[((size_t)sp * DFL_MAX_ROWS + t) * a.n_q + hq] = make_float2(m_r, l_r);
+    }
+    if (!ok) {   // copies and MMAs still in flight finish before tensor memory is freed
+        if (tid == 0) set_error(a.st, DERR_TIMEOUT, 212);
+        mbar_wait_bounded(&bar[0], 0, 100000000ull);
+        if (s_issued) mbar_wait_bounded(&bar[1], 0, 100000000ull);
+        if (o_issued) mbar_wait_bounded(&bar[2], 0, 100000000ull);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tm, TCOLS);
+    if (!ok) return;
+    exchange_combine<HD>(f, kh, sp, S, T, group, tid, warp, lane);
 }
 
 }  // namespace
@@ -357,6 +587,18 @@ int launch_fused_hd(const AttnMaps& maps, const AttnFusedArgs& f, cudaStream_t s
         if (e != cudaSuccess) return (int)e;
         set = true;
     }
+    if (f.tc) {
+        if (f.split_chunks != 1) return (int)cudaErrorInvalidValue;
+        constexpr size_t tsmem = tc_smem<HD>();
+        static bool tset = false;
+        if (!tset) {
+            const cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tsmem);
+            if (e != cudaSuccess) return (int)e;
+            tset = true;
+        }
+        return (int)launch_k(attn_tc_kernel<HD>, dim3(f.m.n_kv, f.max_splits), dim3(128), tsmem, s, maps, f);
+    }
     return (int)launch_k(attn_fused_kernel<HD>, dim3(f.m.n_kv, f.max_splits), dim3(128), smem, s, maps, f);
 }
 
@@ -378,6 +620,25 @@ int attention_fused_per_sm(int hd, int n_q, int n_kv, int* out) {
         const size_t smem = fused_smem<64>(qrows);
         e = cudaFuncSetAttribute(attn_fused_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, attn_fused_kernel<64>, 128, smem);
+    }
+    return (int)e;
+}
+
+int attention_tc_per_sm(int hd, int* out, int* tmem_cols) {
+    *out = 0;
+    cudaError_t e;
+    if (hd == 128) {
+        *tmem_cols = (int)tc_cols<128>();
+        e = cudaFuncSetAttribute(attn_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)tc_smem<128>());
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, attn_tc_kernel<128>, 128, tc_smem<128>());
+    } else {
+        *tmem_cols = (int)tc_cols<64>();
+        e = cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)tc_smem<64>());
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, attn_tc_kernel<64>, 128, tc_smem<64>());
     }
     return (int)e;
 }

@@ -8,8 +8,9 @@ namespace dfl {
 constexpr int ATTN_KEYS = 64;   // keys per chunk; equals the fp32 path's chunk
 
 struct AttnMaps {
-    CUtensorMap q;    // q rows [n_q * 16][head_dim] (head-major, 16 rows per head)
+    CUtensorMap q;    // q rows [n_q * 16][head_dim] (head-major, 16 rows per head), box = the group
     CUtensorMap kv;   // whole cache [layers * 2 * n_kv * cap][head_dim]
+    CUtensorMap q16;  // the q rows again, box = one head's 16 rows
 };
 
 struct AttnMmaArgs {
@@ -40,10 +41,14 @@ struct AttnFusedArgs {
     int out_type;
     int* arrive;        // [n_kv] published splits, zero between launches
     int* done;          // [n_kv] splits done combining, zero between launches
+    int tc;             // 1: tensor-core (tcgen05) form; needs split_chunks == 1
 };
 
 int launch_attention_fused(const AttnMaps& maps, const AttnFusedArgs& f, cudaStream_t s);
 // Host: CTAs of the fused attention kernel one SM holds, for head_dim hd.
 int attention_fused_per_sm(int hd, int n_q, int n_kv, int* out);
+// Host: the same for the tcgen05 form, and the tensor-memory columns one of
+// its CTAs allocates.
+int attention_tc_per_sm(int hd, int* out, int* tmem_cols);
 
 }  // namespace dfl

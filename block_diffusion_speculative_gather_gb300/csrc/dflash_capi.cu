@@ -271,6 +271,7 @@ struct dflash_ctx {
     // splits of a launch (0: two-kernel form)
     int attn_split_chunks[2] = {0, 0};
     int attn_max_splits[2] = {0, 0};
+    int attn_tc[2] = {0, 0};   // tcgen05 form of the fused attention
     float* verify_logits = nullptr;
     float* draft_logits = nullptr;
     bool prefilled = false;
@@ -553,6 +554,7 @@ int run_layers(dflash_ctx* c, bool target, Emit& em) {
                 fa.m = am;
                 fa.split_chunks = c->attn_split_chunks[target ? 0 : 1];
                 fa.max_splits = c->attn_max_splits[target ? 0 : 1];
+                fa.tc = c->attn_tc[target ? 0 : 1];
                 fa.out = at.out;
                 fa.out_type = at.out_type;
                 fa.arrive = c->buf<int>(c->L.acnt);
@@ -909,7 +911,11 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
         const int qrows = (g.n_q / g.n_kv) * DFL_MAX_ROWS;
         r = make_map_raw(&c->amap_t.q, c->ws + L.qrot, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.head_dim,
                          (uint64_t)g.n_q * DFL_MAX_ROWS, 64, qrows, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (!r)
+            r = make_map_raw(&c->amap_t.q16, c->ws + L.qrot, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.head_dim,
+                             (uint64_t)g.n_q * DFL_MAX_ROWS, 64, DFL_MAX_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
         c->amap_d.q = c->amap_t.q;
+        c->amap_d.q16 = c->amap_t.q16;
         if (!r && g.tgt_layers > 0)
             r = make_map_raw(&c->amap_t.kv, kv_target, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.head_dim,
                              (uint64_t)g.tgt_layers * 2 * g.n_kv * cap, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -940,6 +946,19 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
                 c->attn_split_chunks[mdl] = q;
                 c->attn_max_splits[mdl] = smax;
             }
+        }
+        // tcgen05 form for splits of one chunk: every CTA of a launch resident,
+        // and the tensor memory of the CTAs one SM holds within its 512 columns
+        // (DFLASH_ATTN_TC=0 keeps the mma.sync form)
+        const char* tc_env = getenv("DFLASH_ATTN_TC");
+        if (!r && !(tc_env && tc_env[0] == '0')) {
+            int tc_per_sm = 0, tc_cols = 0;
+            const int e2 = attention_tc_per_sm(g.head_dim, &tc_per_sm, &tc_cols);
+            if (e2) r = fail(DFLASH_ERR_CUDA, "attention occupancy: %s", cudaGetErrorString((cudaError_t)e2));
+            for (int mdl = 0; mdl < 2 && !r; ++mdl)
+                c->attn_tc[mdl] = c->attn_split_chunks[mdl] == 1 &&
+                                  g.n_kv * c->attn_max_splits[mdl] <= tc_per_sm * sms &&
+                                  tc_per_sm * tc_cols <= 512;
         }
     }
     if (r) {

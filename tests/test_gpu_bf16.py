@@ -136,3 +136,30 @@ def test_drafter_alone_ext_taps(qwen):
     assert err.max() < TOL, err
     G.check_ids(ids[:W.block - 1], ref[1:], TOL)
     dec.close()
+
+
+def test_attention_forms_agree(qwen, monkeypatch):
+    """The tcgen05 attention (splits of one chunk, the default here) and the
+    mma.sync form (DFLASH_ATTN_TC=0) give the same prefill and verify logits
+    within the parity tolerance, and the same greedy tokens where decidable;
+    each form reproduces itself bit-for-bit."""
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+    dec, P = qwen["dec"], W.prompt_len
+    monkeypatch.setenv("DFLASH_ATTN_TC", "0")
+    ref = DFlash(W, qwen["m"])
+    monkeypatch.delenv("DFLASH_ATTN_TC")
+    out = []
+    for d in (dec, ref, dec):
+        vl = G.logits_buf(W.vocab)
+        d.set_logits_out(vl, None)
+        d.prefill(qwen["prompt"], W.n_new)
+        first = vl[:P % 16 or 16].clone()
+        d.verify(torch.arange(1, W.block, dtype=torch.int32, device="cuda") * 97)
+        out.append((first, vl[:W.block].clone()))
+        d.set_logits_out(None, None)
+        d.check()
+    ref.close()
+    assert torch.equal(out[0][0], out[2][0]) and torch.equal(out[0][1], out[2][1])
+    for a, b in zip(out[0], out[1]):
+        err = G.rel_err_rows(a.cpu().numpy(), b.cpu().numpy())
+        assert err.max() < TOL / 4, err
