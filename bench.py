@@ -367,6 +367,8 @@ def run_ours(args):
         "verify_ms_T1": round(t1row, 4),
         "round_ms_T16": round(t_max / args.steps, 4),
         "gpu_launches": launches_per_round * args.steps,
+        "attention_form": {m: {2: "tcgen05", 1: "mma.sync split-KV", 0: "partial + combine"}[
+            capi.dflash_attention_form(dec.ctx, i)] for i, m in ((0, "target"), (1, "drafter"))},
         "clocks": clocks,
         "roofline": {
             "bound": "hbm", "kernel": "gemm_skinny_kernel (all weight-streaming GEMMs of a round)",
@@ -532,6 +534,24 @@ def measure_workloads(steps, warmup, base_model):
                        "frac_of_peak": round((gb + kv_bytes) / (ms / 1e3) / 1e9 / peak, 4),
                        "weights": "INT4 g64 + bf16 scales: target and drafter projections and "
                                   "the LM head; embedding gather and fc bf16"}
+    dec.close()
+    # --- the e2e bf16 round with the opt-in tcgen05 attention (tensor-memory
+    #     accumulators; splits of two chunks at this cache size)
+    os.environ["DFLASH_ATTN_TC"] = "1"
+    try:
+        dec = DFlash(E2E_BF16, base_model)
+    finally:
+        del os.environ["DFLASH_ATTN_TC"]
+    dec.prefill(prompt, E2E_BF16.n_new)
+    dec.verify(dec.draft())
+    dec.prefill(prompt, E2E_BF16.n_new)
+    ms, gtc = _graph_time(lambda: dec.verify(dec.draft()), steps, warmup)
+    del gtc
+    dec.check()
+    out["e2e_bf16_attention_tcgen05"] = {
+        "rounds_s": round(1e3 / ms, 2), "ms_per_round": round(ms, 4),
+        "attention_form": {1: "mma.sync split-KV", 2: "tcgen05"}.get(capi.dflash_attention_form(dec.ctx, 0)),
+        "note": "same round as the headline line with DFLASH_ATTN_TC=1"}
     dec.close()
     # --- verify sweep over a 16384-position synthetic KV cache
     w = HC_SWEEP

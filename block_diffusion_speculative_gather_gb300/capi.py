@@ -102,6 +102,7 @@ def _load() -> C.CDLL:
         "dflash_linear_noalloc": (C.c_int, [vp, vp, i32, i32, vp, vp]),
         "dflash_profile_phases": (i32, [vp, i32, vp, i32]),
         "dflash_progress": (C.c_int, [vp, vp, vp]),
+        "dflash_attention_form": (C.c_int, [vp, i32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -119,7 +120,7 @@ EXPORTED = ("dflash_workspace_bytes", "dflash_kv_target_bytes", "dflash_kv_draft
             "dflash_quantize_int4g64", "dflash_profile", "dflash_launch_count",
             "dflash_selftest_timeout", "dflash_adopt_kv", "dflash_linear_workspace_bytes",
             "dflash_linear", "dflash_linear_noalloc", "dflash_profile_phases",
-            "dflash_progress")
+            "dflash_progress", "dflash_attention_form")
 
 
 def check(rc: int) -> None:
@@ -262,3 +263,11 @@ def dflash_progress(ctx, out, stream=None):
     """Enqueue the progress words (finished, generated, n, emitted) into the
     int32[4] device tensor `out`."""
     check(lib.dflash_progress(ctx, _ptr(out), _stream(stream)))
+
+
+def dflash_attention_form(ctx, model: int) -> int:
+    """Attention form of the target (model 0) or drafter (model 1):
+    2 tcgen05, 1 mma.sync split-KV, 0 separate partial/combine kernels."""
+    r = lib.dflash_attention_form(ctx, model)
+    check(min(r, 0))
+    return r

@@ -331,52 +331,66 @@ attn_fused_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) 
     exchange_combine<HD>(f, kh, sp, S, T, group, tid, warp, lane);
 }
 
-// Tensor-core (tcgen05) form of the fused attention for splits of one
-// 64-key chunk.  TMA brings each q head's 16 rows to tile rows 32h..32h+15
-// (so the score row of q head h, token t lands in tensor-memory lane 32h + t
-// and warp h owns head h), and the chunk's K and V.  One thread issues
-// S = Q K^T (M 128, N 64) into tensor memory while the CTA transposes V into
-// a K-major tile; each thread of a real row then reads its 64 scores, masks,
-// takes the row max and the base-2 exponentials in registers, and writes its
-// f16 probabilities as the A tile of O = P V (M 128, N head_dim), which the
-// tensor core accumulates in f32.  The rows' (max, sum, unnormalised
-// output) are published like the mma.sync form's and combined the same way.
-template <int HD>
+// Tensor-core (tcgen05) form of the fused attention for splits of NC = 1 or
+// 2 consecutive 64-key chunks (KEYS = 64 NC keys).  TMA brings each q
+// head's 16 rows to tile rows 32h..32h+15 (so the score row of q head h,
+// token t lands in tensor-memory lane 32h + t and warp h owns head h), and
+// the split's K and V.  One thread issues S = Q K^T (M 128, N KEYS) into
+// tensor memory while the CTA transposes V into a K-major tile; each thread
+// of a real row then reads its scores, masks, takes the row max and the
+// base-2 exponentials in registers, and writes its f16 probabilities as the
+// A tile of O = P V (M 128, N head_dim, K KEYS), which the tensor core
+// accumulates in f32.  The rows' (max, sum, unnormalised output) are
+// published like the mma.sync form's and combined the same way.  A kernel
+// that allocates tensor memory holds one CTA per SM here, so a launch has
+// at most one CTA per SM and NC = 2 serves the longer caches.
+template <int HD, int NC>
 constexpr size_t tc_smem() {
-    return 1024 + (size_t)(HD / 64) * (128 + 2 * ATTN_KEYS) * 128 + (size_t)HD * 128 + 128 * 128 + 3 * 8 +
-           8 + 64;
+    // Q [HD/64][128 rows][128 B], V and K [HD/64][KEYS][128 B] each,
+    // V^T [NC][HD][128 B]; P [NC][128][128 B] over K (as large for head_dim
+    // 128, twice as large for 64), barriers and the tensor-memory address
+    constexpr size_t q = (size_t)(HD / 64) * 128 * 128, kv = (size_t)(HD / 64) * NC * ATTN_KEYS * 128;
+    constexpr size_t vt = (size_t)NC * HD * 128, pk = (size_t)NC * 128 * 128;
+    return 1024 + q + kv + vt + (kv > pk ? kv : pk) + 3 * 8 + 8 + 64;
 }
-template <int HD>
-constexpr uint32_t tc_cols() { return HD == 128 ? 256u : 128u; }   // S (64) + O (HD), power of two
+template <int HD, int NC>
+constexpr uint32_t tc_cols() {   // S (KEYS columns) + O (HD), rounded up to a power of two
+    return NC * ATTN_KEYS + HD <= 128 ? 128u : NC * ATTN_KEYS + HD <= 256 ? 256u : 512u;
+}
 
-template <int HD>
+template <int HD, int NC>
 __global__ void __launch_bounds__(128)
 attn_tc_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) {
-    constexpr int C = ATTN_KEYS, HALVES = HD / 64;
+    constexpr int C = ATTN_KEYS, HALVES = HD / 64, KEYS = NC * C;
     constexpr int MAXS = 64;
-    constexpr uint32_t TCOLS = tc_cols<HD>();
+    constexpr uint32_t TCOLS = tc_cols<HD, NC>();
     const AttnMmaArgs& a = f.m;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int KVH = KEYS * 128;            // bytes of one 64-column half of K (or V)
     uint8_t* Qs = sm;                          // [HALVES][128 rows][128 B]
-    uint8_t* Ks = Qs + HALVES * 128 * 128;     // [HALVES][64 keys][128 B]
-    uint8_t* Vs = Ks + HALVES * C * 128;       // [HALVES][64 keys][128 B]
-    uint8_t* Vt = Vs + HALVES * C * 128;       // [HD][128 B]: V^T, 64 keys per row
-    uint8_t* Ps = Vt + HD * 128;               // [128 rows][128 B]: f16 probabilities
-    uint64_t* bar = reinterpret_cast<uint64_t*>(Ps + 128 * 128);   // [0] loads, [1] S, [2] O
+    uint8_t* Vs = Qs + HALVES * 128 * 128;     // [HALVES][KEYS][128 B]
+    uint8_t* Vt = Vs + HALVES * KVH;           // [NC][HD][128 B]: V^T, 64 keys per 128-byte row
+    uint8_t* Ks = Vt + NC * HD * 128;          // [HALVES][KEYS][128 B]
+    uint8_t* Ps = Ks;                          // [NC][128 rows][128 B] over K once S is done
+    constexpr int KP = HALVES * KVH > NC * 128 * 128 ? HALVES * KVH : NC * 128 * 128;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(Ks + KP);   // [0] loads, [1] S, [2] O
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar + 3);
 
     pdl_trigger();
     const int kh = blockIdx.x, sp = blockIdx.y, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    if (tid == 0 && (a.causal || a.window <= 0)) {   // split sp is chunk sp (see the mma.sync form)
-        const int krow = ((a.layer * 2 + 0) * a.n_kv + kh) * a.cap + sp * C;
-        const int vrow = ((a.layer * 2 + 1) * a.n_kv + kh) * a.cap + sp * C;
+    if (tid == 0 && (a.causal || a.window <= 0)) {   // the split's chunks sit at fixed positions
 #pragma unroll
-        for (int h = 0; h < HALVES; ++h) {
-            tma_prefetch_l2_2d(&maps.kv, 64 * h, krow);
-            tma_prefetch_l2_2d(&maps.kv, 64 * h, vrow);
+        for (int j = 0; j < NC; ++j) {
+            const int krow = ((a.layer * 2 + 0) * a.n_kv + kh) * a.cap + (sp * NC + j) * C;
+            const int vrow = ((a.layer * 2 + 1) * a.n_kv + kh) * a.cap + (sp * NC + j) * C;
+#pragma unroll
+            for (int h = 0; h < HALVES; ++h) {
+                tma_prefetch_l2_2d(&maps.kv, 64 * h, krow);
+                tma_prefetch_l2_2d(&maps.kv, 64 * h, vrow);
+            }
         }
     }
     pdl_wait();
@@ -385,117 +399,127 @@ attn_tc_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) {
     const int hi = pos0 + T;
     const int lo = (!a.causal && a.window > 0) ? max(0, pos0 - a.window) : 0;
     const int c_lo = lo / C, c_hi = (hi - 1) / C;
-    const int S = c_hi - c_lo + 1;   // one chunk per split
+    const int S = (c_hi - c_lo + NC) / NC;   // splits in use
     if (sp >= S) return;
     if (S > MAXS || S > f.max_splits) {
         if (tid == 0) set_error(a.st, DERR_INDEX, S);
         return;
     }
-    const int k0 = (c_lo + sp) * C;
+    const int k0 = (c_lo + sp * NC) * C;   // first key of the split
     const int group = a.n_q / a.n_kv;
 
+    // the loads first, so the tensor-memory allocation overlaps them
     if (tid == 0) {
         for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
-    }
-    if (warp == 0) tc::tmem_alloc(s_tmem, TCOLS);
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tm = *s_tmem;
-    if (tid == 0) {
-        const int krow = ((a.layer * 2 + 0) * a.n_kv + kh) * a.cap + k0;
-        const int vrow = ((a.layer * 2 + 1) * a.n_kv + kh) * a.cap + k0;
-        mbar_arrive_expect_tx(&bar[0], HALVES * (group * 16 + 2 * C) * 128);
+        mbar_arrive_expect_tx(&bar[0], HALVES * (group * 16 + 2 * KEYS) * 128);
 #pragma unroll
         for (int h = 0; h < HALVES; ++h) {
             for (int q = 0; q < group; ++q)
                 tma_load_2d(Qs + h * 128 * 128 + q * 32 * 128, &maps.q16, &bar[0], 64 * h,
                             (kh * group + q) * 16);
-            tma_load_2d(Ks + h * C * 128, &maps.kv, &bar[0], 64 * h, krow);
-            tma_load_2d(Vs + h * C * 128, &maps.kv, &bar[0], 64 * h, vrow);
+#pragma unroll
+            for (int j = 0; j < NC; ++j) {
+                const int krow = ((a.layer * 2 + 0) * a.n_kv + kh) * a.cap + k0 + j * C;
+                const int vrow = ((a.layer * 2 + 1) * a.n_kv + kh) * a.cap + k0 + j * C;
+                tma_load_2d(Ks + h * KVH + j * C * 128, &maps.kv, &bar[0], 64 * h, krow);
+                tma_load_2d(Vs + h * KVH + j * C * 128, &maps.kv, &bar[0], 64 * h, vrow);
+            }
         }
     }
+    __syncwarp();
+    if (warp == 0) tc::tmem_alloc(s_tmem, TCOLS);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = *s_tmem;
     // every wait is voted on by the whole CTA, so all threads leave together
     bool ok = __syncthreads_and(mbar_wait_bounded(&bar[0], 0)) != 0;
     const bool s_issued = ok;
     if (ok && tid == 0) {   // S = Q K^T while the CTA transposes V
         tc::fence_after_sync();
-        constexpr uint32_t IS = tc::idesc_f16_f32(128, C);
+        constexpr uint32_t IS = tc::idesc_f16_f32(128, KEYS);
 #pragma unroll
         for (int kd = 0; kd < HD / 16; ++kd) {
             const int h = kd >> 2, ko = (kd & 3) * 32;
-            tc::mma_f16(tm, tc::desc_sw128(Qs + h * 128 * 128 + ko), tc::desc_sw128(Ks + h * C * 128 + ko),
-                        IS, kd > 0 ? 1u : 0u);
+            tc::mma_f16(tm, tc::desc_sw128(Qs + h * 128 * 128 + ko), tc::desc_sw128(Ks + h * KVH + ko), IS,
+                        kd > 0 ? 1u : 0u);
         }
         tc::commit(&bar[1]);
     }
-    if (ok && tid < HD) {   // V^T row d = tid: the chunk's 64 keys of column d
-        const int h = tid >> 6, dd = tid & 63, ch = dd >> 3;
-        const uint8_t* vb = Vs + h * C * 128 + (dd & 7) * 2;
-        uint32_t w[32];
-#pragma unroll
-        for (int k2 = 0; k2 < 32; ++k2) {
-            const int k = 2 * k2;
-            const uint32_t x0 = *reinterpret_cast<const uint16_t*>(vb + k * 128 + ((ch ^ (k & 7)) << 4));
-            const uint32_t x1 =
-                *reinterpret_cast<const uint16_t*>(vb + (k + 1) * 128 + ((ch ^ ((k + 1) & 7)) << 4));
-            w[k2] = x0 | (x1 << 16);
+    if (ok) {   // V^T by 8x8 transposes: ldmatrix a [keys][d] block, store it as [d][keys]
+        const int r8 = lane & 7, m = lane >> 3;
+#pragma unroll 1
+        for (int o = warp; o < NC * HALVES * 16; o += 4) {
+            const int j = o / (HALVES * 16), h = (o / 16) % HALVES;
+            const int kb = (o & 15) >> 1, db = ((o & 1) << 2) + m;   // key block, d block of matrix m
+            const int key = 8 * kb + r8, d = 64 * h + 8 * db + r8;
+            uint32_t r[4];
+            adev::ldsm_x4(r, Vs + h * KVH + j * C * 128 + key * 128 + ((db ^ (key & 7)) << 4));
+            adev::stsm_x4_trans(Vt + j * HD * 128 + d * 128 + ((kb ^ (d & 7)) << 4), r);
         }
-        uint8_t* row = Vt + tid * 128;
-#pragma unroll
-        for (int kc = 0; kc < 8; ++kc)
-            *reinterpret_cast<uint4*>(row + ((kc ^ (tid & 7)) << 4)) =
-                make_uint4(w[4 * kc], w[4 * kc + 1], w[4 * kc + 2], w[4 * kc + 3]);
     }
     tc::fence_async_smem();   // V^T visible to the tensor core
     if (ok) ok = __syncthreads_and(mbar_wait_bounded(&bar[1], 0)) != 0;
     tc::fence_after_sync();
 
-    // ---- softmax of this thread's score row (q head `warp`, token `lane`)
+    // ---- softmax of this thread's score row (q head `warp`, token `lane`),
+    // 32 scores at a time: the row max first, then the probabilities
     const bool mine = warp < group && lane < 16;
     float m_r = -INFINITY, l_r = 0.f;
     if (ok && warp < group) {
-        float s0[32], s1[32];
         const uint32_t trow = tm + ((uint32_t)(warp * 32) << 16);
-        tc::ld_x32(trow, s0);
-        tc::ld_x32(trow + 32, s1);
-        if (mine) {
-            const int t = lane;
-            const float sl2 = a.scale * 1.4426950408889634f;
-            const int kmax = a.causal ? min(hi - 1, pos0 + t) : hi - 1;
-            const bool whole = t < T && k0 >= lo && k0 + C - 1 <= kmax;
-            float mx = -INFINITY;
+        const int t = lane;
+        const float sl2 = a.scale * 1.4426950408889634f;
+        const int kmax = a.causal ? min(hi - 1, pos0 + t) : hi - 1;
+        const bool whole = t < T && k0 >= lo && k0 + KEYS - 1 <= kmax;
+        // scaled, masked scores of keys k0 + 32 b + j.  The load is warp-wide;
+        // lanes 16..31 hold the tile's padding rows (never-written shared
+        // memory, any bit pattern) and do no arithmetic on them.
+        auto scores = [&](int b, float (&sv)[32]) {
 #pragma unroll
-            for (int j = 0; j < C; ++j) {
-                float v = (j < 32 ? s0[j & 31] : s1[j & 31]) * sl2;
-                if (!whole) {
-                    const int key = k0 + j;
-                    if (!(t < T && key >= lo && key <= kmax)) v = -INFINITY;
+            for (int j = 0; j < 32; ++j) sv[j] *= sl2;
+            if (!whole) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int key = k0 + 32 * b + j;
+                    if (!(t < T && key >= lo && key <= kmax)) sv[j] = -INFINITY;
                 }
-                if (j < 32) s0[j & 31] = v; else s1[j & 31] = v;
-                mx = fmaxf(mx, v);
             }
-            float sum = 0.f;
-            uint32_t pk[32];
+        };
+        float mx = -INFINITY, sum = 0.f;
+#pragma unroll 1
+        for (int b = 0; b < KEYS / 32; ++b) {
+            float sv[32];
+            tc::ld_x32(trow + 32 * b, sv);
+            if (mine) {
+                scores(b, sv);
 #pragma unroll
-            for (int j2 = 0; j2 < 32; ++j2) {
-                const float v0 = j2 < 16 ? s0[(2 * j2) & 31] : s1[(2 * j2) & 31];
-                const float v1 = j2 < 16 ? s0[(2 * j2 + 1) & 31] : s1[(2 * j2 + 1) & 31];
-                const float p0 = v0 == -INFINITY ? 0.f : exp2f(v0 - mx);
-                const float p1 = v1 == -INFINITY ? 0.f : exp2f(v1 - mx);
-                sum += p0;
-                sum += p1;
-                pk[j2] = pack_f16x2(p0, p1);
+                for (int j = 0; j < 32; ++j) mx = fmaxf(mx, sv[j]);
             }
-            uint8_t* prow = Ps + tid * 128;
-#pragma unroll
-            for (int kc = 0; kc < 8; ++kc)
-                *reinterpret_cast<uint4*>(prow + ((kc ^ (tid & 7)) << 4)) =
-                    make_uint4(pk[4 * kc], pk[4 * kc + 1], pk[4 * kc + 2], pk[4 * kc + 3]);
-            m_r = mx;
-            l_r = sum;
         }
+#pragma unroll 1
+        for (int b = 0; b < KEYS / 32; ++b) {
+            float sv[32];
+            tc::ld_x32(trow + 32 * b, sv);
+            if (mine) {   // keys 32b.. : chunk b/2 of P, 16-byte groups 4(b&1)..4(b&1)+3
+                scores(b, sv);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sv[j] = sv[j] == -INFINITY ? 0.f : exp2f(sv[j] - mx);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sum += sv[j];
+                uint8_t* prow = Ps + (b >> 1) * 128 * 128 + tid * 128;
+#pragma unroll
+                for (int g4 = 0; g4 < 4; ++g4) {
+                    const int kc = 4 * (b & 1) + g4;
+                    *reinterpret_cast<uint4*>(prow + ((kc ^ (tid & 7)) << 4)) = make_uint4(
+                        pack_f16x2(sv[8 * g4 + 0], sv[8 * g4 + 1]), pack_f16x2(sv[8 * g4 + 2], sv[8 * g4 + 3]),
+                        pack_f16x2(sv[8 * g4 + 4], sv[8 * g4 + 5]), pack_f16x2(sv[8 * g4 + 6], sv[8 * g4 + 7]));
+                }
+            }
+        }
+        m_r = mx;
+        l_r = sum;
     }
     tc::fence_async_smem();   // P visible to the tensor core
     tc::fence_before_sync();
@@ -505,9 +529,11 @@ attn_tc_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) {
         tc::fence_after_sync();
         constexpr uint32_t IO = tc::idesc_f16_f32(128, HD);
 #pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)
-            tc::mma_f16(tm + C, tc::desc_sw128(Ps + kk * 32), tc::desc_sw128(Vt + kk * 32), IO,
-                        kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < KEYS / 16; ++kk) {
+            const int j = kk >> 2, ko = (kk & 3) * 32;
+            tc::mma_f16(tm + KEYS, tc::desc_sw128(Ps + j * 128 * 128 + ko),
+                        tc::desc_sw128(Vt + j * HD * 128 + ko), IO, kk > 0 ? 1u : 0u);
+        }
         tc::commit(&bar[2]);
     }
     if (ok) ok = __syncthreads_and(mbar_wait_bounded(&bar[2], 0)) != 0;
@@ -520,8 +546,8 @@ attn_tc_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) {
     if (ok && warp < group) {
         const int t = lane, hq = kh * group + warp;
         float* dst = Op + sp * osplit + ((size_t)t * a.n_q + hq) * HD;
-        const uint32_t trow = tm + ((uint32_t)(warp * 32) << 16) + C;
-#pragma unroll
+        const uint32_t trow = tm + ((uint32_t)(warp * 32) << 16) + KEYS;
+#pragma unroll 1
         for (int q = 0; q < HD / 32; ++q) {
             float v[32];
             tc::ld_x32(trow + 32 * q, v);
@@ -576,6 +602,30 @@ int launch_attention_mma(const AttnMaps& maps, const AttnMmaArgs& a, int max_chu
 }
 
 
+template <int HD, int NC>
+int launch_tc(const AttnMaps& maps, const AttnFusedArgs& f, cudaStream_t s) {
+    constexpr size_t smem = tc_smem<HD, NC>();
+    static bool set = false;
+    if (!set) {
+        const cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, NC>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return (int)e;
+        set = true;
+    }
+    return (int)launch_k(attn_tc_kernel<HD, NC>, dim3(f.m.n_kv, f.max_splits), dim3(128), smem, s, maps, f);
+}
+
+template <int HD, int NC>
+int tc_per_sm(int* out, int* tmem_cols) {
+    *tmem_cols = (int)tc_cols<HD, NC>();
+    set_carveout_once(reinterpret_cast<const void*>(attn_tc_kernel<HD, NC>));
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tc_smem<HD, NC>());
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, attn_tc_kernel<HD, NC>, 128, tc_smem<HD, NC>());
+    return (int)e;
+}
+
 template <int HD>
 int launch_fused_hd(const AttnMaps& maps, const AttnFusedArgs& f, cudaStream_t s) {
     const int qrows = (f.m.n_q / f.m.n_kv) * 16;
@@ -588,16 +638,9 @@ int launch_fused_hd(const AttnMaps& maps, const AttnFusedArgs& f, cudaStream_t s
         set = true;
     }
     if (f.tc) {
-        if (f.split_chunks != 1) return (int)cudaErrorInvalidValue;
-        constexpr size_t tsmem = tc_smem<HD>();
-        static bool tset = false;
-        if (!tset) {
-            const cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tsmem);
-            if (e != cudaSuccess) return (int)e;
-            tset = true;
-        }
-        return (int)launch_k(attn_tc_kernel<HD>, dim3(f.m.n_kv, f.max_splits), dim3(128), tsmem, s, maps, f);
+        if (f.split_chunks == 1) return launch_tc<HD, 1>(maps, f, s);
+        if (f.split_chunks == 2) return launch_tc<HD, 2>(maps, f, s);
+        return (int)cudaErrorInvalidValue;
     }
     return (int)launch_k(attn_fused_kernel<HD>, dim3(f.m.n_kv, f.max_splits), dim3(128), smem, s, maps, f);
 }
@@ -614,33 +657,23 @@ int attention_fused_per_sm(int hd, int n_q, int n_kv, int* out) {
     cudaError_t e;
     if (hd == 128) {
         const size_t smem = fused_smem<128>(qrows);
+        set_carveout_once(reinterpret_cast<const void*>(attn_fused_kernel<128>));
         e = cudaFuncSetAttribute(attn_fused_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, attn_fused_kernel<128>, 128, smem);
     } else {
         const size_t smem = fused_smem<64>(qrows);
+        set_carveout_once(reinterpret_cast<const void*>(attn_fused_kernel<64>));
         e = cudaFuncSetAttribute(attn_fused_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, attn_fused_kernel<64>, 128, smem);
     }
     return (int)e;
 }
 
-int attention_tc_per_sm(int hd, int* out, int* tmem_cols) {
+int attention_tc_per_sm(int hd, int nc, int* out, int* tmem_cols) {
     *out = 0;
-    cudaError_t e;
-    if (hd == 128) {
-        *tmem_cols = (int)tc_cols<128>();
-        e = cudaFuncSetAttribute(attn_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)tc_smem<128>());
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, attn_tc_kernel<128>, 128, tc_smem<128>());
-    } else {
-        *tmem_cols = (int)tc_cols<64>();
-        e = cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)tc_smem<64>());
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, attn_tc_kernel<64>, 128, tc_smem<64>());
-    }
-    return (int)e;
+    if (nc == 1) return hd == 128 ? tc_per_sm<128, 1>(out, tmem_cols) : tc_per_sm<64, 1>(out, tmem_cols);
+    if (nc == 2) return hd == 128 ? tc_per_sm<128, 2>(out, tmem_cols) : tc_per_sm<64, 2>(out, tmem_cols);
+    return (int)cudaErrorInvalidValue;
 }
 
 }  // namespace dfl

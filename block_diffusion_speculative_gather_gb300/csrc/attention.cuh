@@ -41,14 +41,14 @@ struct AttnFusedArgs {
     int out_type;
     int* arrive;        // [n_kv] published splits, zero between launches
     int* done;          // [n_kv] splits done combining, zero between launches
-    int tc;             // 1: tensor-core (tcgen05) form; needs split_chunks == 1
+    int tc;             // 1: tensor-core (tcgen05) form; split_chunks 1 or 2
 };
 
 int launch_attention_fused(const AttnMaps& maps, const AttnFusedArgs& f, cudaStream_t s);
 // Host: CTAs of the fused attention kernel one SM holds, for head_dim hd.
 int attention_fused_per_sm(int hd, int n_q, int n_kv, int* out);
-// Host: the same for the tcgen05 form, and the tensor-memory columns one of
-// its CTAs allocates.
-int attention_tc_per_sm(int hd, int* out, int* tmem_cols);
+// Host: the same for the tcgen05 form with nc (1 or 2) chunks per split,
+// and the tensor-memory columns one of its CTAs allocates.
+int attention_tc_per_sm(int hd, int nc, int* out, int* tmem_cols);
 
 }  // namespace dfl

@@ -19,6 +19,14 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* p) {
                  : "r"(smem_u32(p)));
 }
 
+// Four 8x8 b16 matrices from registers (ldmatrix fragment layout) to shared
+// memory, each transposed; lane l gives the address of row l % 8 of matrix l / 8.
+__device__ __forceinline__ void stsm_x4_trans(void* p, const uint32_t (&r)[4]) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};"
+                 ::"r"(smem_u32(p)), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
 // Byte address of (row, 16-byte chunk) in a tile made of HD/64 swizzled
 // halves of [rows][128 B] (d 0..63 in half 0, 64..127 in half 1).
 template <int HD>

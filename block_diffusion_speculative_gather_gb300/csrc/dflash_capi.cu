@@ -930,14 +930,18 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
         const int e = attention_fused_per_sm(g.head_dim, g.n_q, g.n_kv, &per_sm);
         if (e) r = fail(DFLASH_ERR_CUDA, "attention occupancy: %s", cudaGetErrorString((cudaError_t)e));
         const int capacity = per_sm * sms;
-        for (int mdl = 0; mdl < 2 && !r && capacity > 0; ++mdl) {
-            // chunks a forward can touch: the whole cache for the causal
-            // target, the window (+ block, + a partial chunk) for the drafter
+        // chunks a forward can touch: the whole cache for the causal target,
+        // the window (+ block, + a partial chunk) for the drafter
+        auto model_chunks = [&](int mdl) {
             int mc = max_chunks(g);
             if (mdl == 1 && g.window > 0) {
                 const int wc = (g.window + g.block_max + 63) / 64 + 1;
                 if (wc < mc) mc = wc;
             }
+            return mc;
+        };
+        for (int mdl = 0; mdl < 2 && !r && capacity > 0; ++mdl) {
+            const int mc = model_chunks(mdl);
             int q = (mc * g.n_kv + capacity - 1) / capacity;
             if (q < (mc + 63) / 64) q = (mc + 63) / 64;
             if (q < DFL_ATTN_MIN_SPLIT) q = DFL_ATTN_MIN_SPLIT;
@@ -947,18 +951,30 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
                 c->attn_max_splits[mdl] = smax;
             }
         }
-        // tcgen05 form for splits of one chunk: every CTA of a launch resident,
-        // and the tensor memory of the CTAs one SM holds within its 512 columns
-        // (DFLASH_ATTN_TC=0 keeps the mma.sync form)
+        // tcgen05 form (opt-in, DFLASH_ATTN_TC=1: measured slower than the
+        // mma.sync form on the 16-row round) with splits of 1 or 2 chunks,
+        // where every CTA of a launch is resident at once and the tensor
+        // memory of the CTAs one SM holds fits its 512 columns
         const char* tc_env = getenv("DFLASH_ATTN_TC");
-        if (!r && !(tc_env && tc_env[0] == '0')) {
-            int tc_per_sm = 0, tc_cols = 0;
-            const int e2 = attention_tc_per_sm(g.head_dim, &tc_per_sm, &tc_cols);
-            if (e2) r = fail(DFLASH_ERR_CUDA, "attention occupancy: %s", cudaGetErrorString((cudaError_t)e2));
-            for (int mdl = 0; mdl < 2 && !r; ++mdl)
-                c->attn_tc[mdl] = c->attn_split_chunks[mdl] == 1 &&
-                                  g.n_kv * c->attn_max_splits[mdl] <= tc_per_sm * sms &&
-                                  tc_per_sm * tc_cols <= 512;
+        for (int mdl = 0; mdl < 2 && !r && tc_env && tc_env[0] == '1'; ++mdl) {
+            if (c->attn_split_chunks[mdl] <= 0) continue;
+            const int mc = model_chunks(mdl);
+            for (int nc = 1; nc <= 2 && !r; ++nc) {
+                int tc_per_sm = 0, tc_cols = 0;
+                const int e2 = attention_tc_per_sm(g.head_dim, nc, &tc_per_sm, &tc_cols);
+                if (e2) {
+                    r = fail(DFLASH_ERR_CUDA, "attention occupancy: %s", cudaGetErrorString((cudaError_t)e2));
+                    break;
+                }
+                const int smax = (mc + nc - 1) / nc;
+                if (tc_per_sm > 0 && g.n_kv * smax <= tc_per_sm * sms && smax <= 64 &&
+                    tc_per_sm * tc_cols <= 512) {
+                    c->attn_split_chunks[mdl] = nc;
+                    c->attn_max_splits[mdl] = smax;
+                    c->attn_tc[mdl] = 1;
+                    break;
+                }
+            }
         }
     }
     if (r) {
@@ -1274,6 +1290,13 @@ int dflash_check(dflash_ctx* c, dflash_stream_t stream) {
     CUDA_TRY(cudaMemset(c->ws + c->L.acnt, 0, (size_t)2 * c->cfg.n_kv * 4));
     if (err[0] == DERR_TIMEOUT) return fail(DFLASH_ERR_TIMEOUT, "bounded wait expired (site %d)", err[1]);
     return fail(DFLASH_ERR_DEVICE, "device error %d (info %d)", err[0], err[1]);
+}
+
+int dflash_attention_form(const dflash_ctx* c, int32_t model) {
+    if (!c || (model != 0 && model != 1)) return fail(DFLASH_ERR_ARG, "NULL context or model %d", model);
+    const bool persistent = c->prog[model == 0 ? PROG_VERIFY : PROG_DRAFT].on;
+    if (c->cfg.dtype != DFLASH_BF16 || persistent || c->attn_split_chunks[model] <= 0) return 0;
+    return c->attn_tc[model] ? 2 : 1;
 }
 
 int dflash_progress(dflash_ctx* c, int32_t* out, dflash_stream_t stream) {

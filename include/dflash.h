@@ -256,6 +256,20 @@ int dflash_check(dflash_ctx* ctx, dflash_stream_t stream);
  */
 int dflash_progress(dflash_ctx* ctx, int32_t* out, dflash_stream_t stream);
 
+/*
+ * The attention form a context's forwards run for the target (model 0) or
+ * the drafter (model 1), fixed at dflash_init from the configuration and
+ * the device: 2 = split-KV on the fifth-generation tensor cores (tcgen05),
+ * splits of one 64-key chunk; 1 = split-KV on mma.sync tensor cores, splits
+ * of several chunks; 0 = the separate partial and combine kernels (fp32
+ * models, the persistent schedule).  Form 2 is opt-in: environment
+ * DFLASH_ATTN_TC=1 at init (on the 16-row round it measured slower than
+ * form 1).  No counterpart in the pages: an implementation choice
+ * of this library.  Returns the form, or ARG for a NULL context or a model
+ * other than 0 and 1.
+ */
+int dflash_attention_form(const dflash_ctx* ctx, int32_t model);
+
 /* Self-test of the kernels' bounded waits: launches one warp that waits on
  * an mbarrier nothing arrives on, gives up after limit_ns (<= 2 s) and sets
  * the device error word, so that the next dflash_check returns TIMEOUT. */

@@ -99,6 +99,7 @@ def test_null_context_calls_fail_cleanly(capi):
     assert capi.lib.dflash_draft_block(None, None, None) == -3
     assert capi.lib.dflash_verify_accept(None, None, None, None, None) == -3
     assert capi.lib.dflash_rollback(None, 5, 0, None) == -3
+    assert capi.lib.dflash_attention_form(None, 0) == -3
     assert capi.lib.dflash_prefill_taps(None, None, 0, None, 0, 1, 0, 1, None) == -3
     assert capi.lib.dflash_quantize_int4g64(None, 1, 256, None, None, None) == -3
     assert capi.lib.dflash_tap_reduce(None, 1, 1, 1, 8, None, None) == -3

@@ -138,16 +138,23 @@ def test_drafter_alone_ext_taps(qwen):
     dec.close()
 
 
-def test_attention_forms_agree(qwen, monkeypatch):
-    """The tcgen05 attention (splits of one chunk, the default here) and the
-    mma.sync form (DFLASH_ATTN_TC=0) give the same prefill and verify logits
-    within the parity tolerance, and the same greedy tokens where decidable;
-    each form reproduces itself bit-for-bit."""
+@pytest.mark.parametrize("max_seq,chunks", [(256, 1), (1280, 2)], ids=["1chunk", "2chunk"])
+def test_attention_forms_agree(qwen, monkeypatch, max_seq, chunks):
+    """The tcgen05 attention (DFLASH_ATTN_TC=1; splits of one chunk for a
+    256-position cache, of two for 1280 positions, where 8 kv heads x 20
+    one-chunk splits would exceed one CTA per SM) and the default mma.sync
+    form give the same prefill and verify logits within the parity
+    tolerance; each form reproduces itself bit-for-bit."""
+    from block_diffusion_speculative_gather_gb300 import capi
     from block_diffusion_speculative_gather_gb300.runtime import DFlash
-    dec, P = qwen["dec"], W.prompt_len
-    monkeypatch.setenv("DFLASH_ATTN_TC", "0")
-    ref = DFlash(W, qwen["m"])
+    P = W.prompt_len
+    Wm = W.with_(max_seq=max_seq)
+    ref = DFlash(Wm, qwen["m"])
+    monkeypatch.setenv("DFLASH_ATTN_TC", "1")
+    dec = DFlash(Wm, qwen["m"])
     monkeypatch.delenv("DFLASH_ATTN_TC")
+    assert [capi.dflash_attention_form(dec.ctx, i) for i in (0, 1)] == [2, 2]
+    assert [capi.dflash_attention_form(ref.ctx, i) for i in (0, 1)] == [1, 1]
     out = []
     for d in (dec, ref, dec):
         vl = G.logits_buf(W.vocab)
@@ -159,6 +166,7 @@ def test_attention_forms_agree(qwen, monkeypatch):
         d.set_logits_out(None, None)
         d.check()
     ref.close()
+    dec.close()
     assert torch.equal(out[0][0], out[2][0]) and torch.equal(out[0][1], out[2][1])
     for a, b in zip(out[0], out[1]):
         err = G.rel_err_rows(a.cpu().numpy(), b.cpu().numpy())

@@ -84,11 +84,22 @@ def _synthetic_kv(dec, w, n):
     return cache
 
 
-@pytest.mark.parametrize("n", [1024, 16384])
-def test_verify_full_size_over_synthetic_cache(target, n):
+@pytest.mark.parametrize("n,max_seq,form", [(1024, 1600, 2), (1024, 1600, 1), (16384, 16448, 1)],
+                         ids=["1k-tcgen05", "1k-mma", "16k-mma"])
+def test_verify_full_size_over_synthetic_cache(target, n, max_seq, form, monkeypatch):
+    """36-layer verify over an n-token cache, with the tcgen05 attention
+    (opt-in; a 1600-position cache, the end-to-end workload's, gives splits
+    of two chunks) and with the default mma.sync form (one chunk per split
+    at 1600 positions, several at 16448)."""
+    from block_diffusion_speculative_gather_gb300 import capi
     from block_diffusion_speculative_gather_gb300.runtime import DFlash
     w, m, tw = target
+    w = w.with_(max_seq=max_seq)
+    if form == 2:
+        monkeypatch.setenv("DFLASH_ATTN_TC", "1")
     dec = DFlash(w, m)
+    monkeypatch.delenv("DFLASH_ATTN_TC", raising=False)
+    assert capi.dflash_attention_form(dec.ctx, 0) == form
     cache = _synthetic_kv(dec, w, n)
     t_n = 31337
     d = synth.uniform_ids(15, w.vocab, seed=5).tolist()
