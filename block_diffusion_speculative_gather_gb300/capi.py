@@ -103,6 +103,7 @@ def _load() -> C.CDLL:
         "dflash_profile_phases": (i32, [vp, i32, vp, i32]),
         "dflash_progress": (C.c_int, [vp, vp, vp]),
         "dflash_attention_form": (C.c_int, [vp, i32]),
+        "dflash_linear_dense": (C.c_int, [vp, vp, vp, i32, i32, i32, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -120,7 +121,7 @@ EXPORTED = ("dflash_workspace_bytes", "dflash_kv_target_bytes", "dflash_kv_draft
             "dflash_quantize_int4g64", "dflash_profile", "dflash_launch_count",
             "dflash_selftest_timeout", "dflash_adopt_kv", "dflash_linear_workspace_bytes",
             "dflash_linear", "dflash_linear_noalloc", "dflash_profile_phases",
-            "dflash_progress", "dflash_attention_form")
+            "dflash_progress", "dflash_attention_form", "dflash_linear_dense")
 
 
 def check(rc: int) -> None:
@@ -271,3 +272,12 @@ def dflash_attention_form(ctx, model: int) -> int:
     r = lib.dflash_attention_form(ctx, model)
     check(min(r, 0))
     return r
+
+
+def dflash_linear_dense(w, x, y, err, x_lo=None, stream=None):
+    """y[m][n] = x[m] . w[n] (+ x_lo[m] . w[n]) on the tcgen05 dense GEMM:
+    x, x_lo bf16 [M][K], w bf16 [N][K], y fp32 [M][N], err int32[2] zeros."""
+    m, k = x.shape
+    n = w.shape[0]
+    check(lib.dflash_linear_dense(_ptr(w), _ptr(x), _ptr(x_lo), m, n, k, _ptr(y), _ptr(err),
+                                  _stream(stream)))

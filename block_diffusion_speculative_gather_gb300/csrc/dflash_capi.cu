@@ -17,6 +17,7 @@
 
 #include "../../include/dflash.h"
 #include "attention.cuh"
+#include "gemm_tc.cuh"
 #include "common.cuh"
 #include "gemm.cuh"
 #include "kernels.cuh"
@@ -1341,6 +1342,41 @@ size_t dflash_linear_workspace_bytes(int32_t n, int32_t k) {
     if (n < GEMM_BN || n % GEMM_BN || k < 64 || k % 64) return 0;
     return align_up((size_t)MAX_SMS * 2 * GEMM_BN * DFL_MAX_ROWS * 4, 1024) +
            align_up((size_t)(n / GEMM_BN) * 4, 256) + align_up(sizeof(DevState), 256);
+}
+
+int dflash_linear_dense(const void* w, const void* x, const void* x_lo, int32_t m, int32_t n, int32_t k,
+                        float* y, int32_t* err, dflash_stream_t stream) {
+    if (!w || !x || !y || !err) return fail(DFLASH_ERR_ARG, "NULL argument");
+    if (m < 1 || n < 1 || k < DT_BK || k % DT_BK)
+        return fail(DFLASH_ERR_ARG, "m %d n %d k %d: m, n >= 1, k a multiple of 64", m, n, k);
+    if (!aligned16(w) || !aligned16(x) || !aligned16(y) || !aligned16(err) || (x_lo && !aligned16(x_lo)))
+        return fail(DFLASH_ERR_ARG, "misaligned buffer");
+    if (n % 4) return fail(DFLASH_ERR_ARG, "n %d: rows of y must stay 16-byte aligned (n a multiple of 4)", n);
+    if (int r0 = get_encode()) return r0;
+    if (int r0 = pending_error()) return r0;
+    DenseMaps maps;
+    memset(&maps, 0, sizeof maps);
+    int r = make_map_raw(&maps.x, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, m, DT_BK, DT_BM,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!r && x_lo)
+        r = make_map_raw(&maps.x_lo, x_lo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, m, DT_BK, DT_BM,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!r)
+        r = make_map_raw(&maps.w[0], w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, n, DT_BK, DT_BN,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r) return r;
+    DenseArgs a{};
+    a.M = m;
+    a.N = n;
+    a.K = k;
+    a.n_seg0 = (n + DT_BN - 1) / DT_BN * DT_BN;
+    a.x_split = x_lo ? 1 : 0;
+    a.y = y;
+    a.ldy = n;
+    a.err = err;
+    const int e = launch_dense(maps, a, reinterpret_cast<cudaStream_t>(stream));
+    if (e) return fail(DFLASH_ERR_CUDA, "dense GEMM launch: %s", cudaGetErrorString((cudaError_t)e));
+    return DFLASH_OK;
 }
 
 int dflash_linear(const void* w, const void* x, int32_t n, int32_t k, float* y, void* workspace,

@@ -1,0 +1,174 @@
+// Dense many-row GEMM on tcgen05 (see gemm_tc.cuh).
+//
+// One CTA per 128 x 256 output tile, 128 threads.  Thread 0 is the TMA
+// producer: a ring of k-blocks (the x tile [128][64] bf16, its low plane
+// when x_split, and the w tile [256][64] bf16, all 128-byte swizzled,
+// K-major).  Thread 32 issues tcgen05.mma (M 128, N 256, K 16, f32
+// accumulators in 256 tensor-memory columns) four times per k-block (twice
+// that with the low plane) and commits each stage back to the producer
+// through its "empty" mbarrier.  After the last k-block every warp reads
+// its 32 tensor-memory lanes (rows) with tcgen05.ld and stores fp32 rows;
+// rows past M and columns past N are not stored (TMA fills the missing x
+// and w rows with zeros).  Every wait is bounded; a wait that times out
+// sets the device error word, and the MMA thread still commits, so the
+// tensor memory is freed only after the MMAs it issued have finished.
+
+#include "gemm_tc.cuh"
+#include "tc_dev.cuh"
+
+namespace dfl {
+
+namespace {
+
+__device__ __forceinline__ void dense_error(int* err, int site) {
+    if (atomicCAS(&err[0], 0, DERR_TIMEOUT) == 0) err[1] = site;
+}
+
+template <bool SPLIT>
+struct DenseCfg {
+    static constexpr uint32_t XB = DT_BM * 128;                    // x tile bytes (64 k)
+    static constexpr uint32_t WB = DT_BN * 128;                    // w tile bytes
+    static constexpr uint32_t STAGE = (SPLIT ? 2 : 1) * XB + WB;
+    static constexpr int STAGES = SPLIT ? 3 : 4;
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + (2 * STAGES + 1) * 8 + 16;
+};
+
+template <bool SPLIT>
+__global__ void __launch_bounds__(128, 1)
+gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
+    using CFG = DenseCfg<SPLIT>;
+    constexpr int STAGES = CFG::STAGES;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + STAGES * CFG::STAGE);
+    uint64_t* empty = full + STAGES;
+    uint64_t* done = empty + STAGES;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
+    __shared__ int s_fail;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * DT_BM, n0 = blockIdx.y * DT_BN;
+    const int nkb = a.K / DT_BK;
+    const int seg = n0 >= a.n_seg0 ? 1 : 0;
+    const int wrow = n0 - seg * a.n_seg0;
+
+    pdl_trigger();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(done, 1);
+        fence_mbar_init();
+        s_fail = 0;
+        tma_prefetch_desc(&maps.x);
+        if (SPLIT) tma_prefetch_desc(&maps.x_lo);
+        tma_prefetch_desc(&maps.w[seg]);
+    }
+    if (warp == 1) tc::tmem_alloc(s_tmem, DT_BN);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = *s_tmem;
+    pdl_wait();   // x may come from the previous kernel
+
+    if (threadIdx.x == 0) {   // ---- TMA producer
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % STAGES;
+            if (kb >= STAGES && !mbar_wait_bounded(&empty[s], (uint32_t)((kb / STAGES - 1) & 1))) {
+                s_fail = 1;
+                dense_error(a.err, 300);
+                break;
+            }
+            uint8_t* st = ring + s * CFG::STAGE;
+            mbar_arrive_expect_tx(&full[s], CFG::STAGE);
+            tma_load_2d(st, &maps.x, &full[s], kb * DT_BK, m0);
+            if (SPLIT) tma_load_2d(st + CFG::XB, &maps.x_lo, &full[s], kb * DT_BK, m0);
+            tma_load_2d(st + (SPLIT ? 2 : 1) * CFG::XB, &maps.w[seg], &full[s], kb * DT_BK, wrow);
+        }
+    } else if (threadIdx.x == 32) {   // ---- MMA issuer
+        constexpr uint32_t ID = tc::idesc_bf16_f32(DT_BM, DT_BN);
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % STAGES;
+            if (!mbar_wait_bounded(&full[s], (uint32_t)((kb / STAGES) & 1))) {
+                s_fail = 1;
+                dense_error(a.err, 301);
+                break;
+            }
+            tc::fence_after_sync();
+            const uint8_t* st = ring + s * CFG::STAGE;
+            const uint8_t* wt = st + (SPLIT ? 2 : 1) * CFG::XB;
+#pragma unroll
+            for (int k = 0; k < DT_BK / 16; ++k) {
+                const uint64_t bd = tc::desc_sw128(wt + 32 * k);
+                tc::mma_f16(tm, tc::desc_sw128(st + 32 * k), bd, ID, (kb | k) != 0 ? 1u : 0u);
+                if (SPLIT) tc::mma_f16(tm, tc::desc_sw128(st + CFG::XB + 32 * k), bd, ID, 1u);
+            }
+            tc::commit(&empty[s]);   // the stage is free once these MMAs are done
+        }
+        tc::commit(done);   // always: the epilogue (and the free) waits on it
+    }
+    __syncwarp();
+
+    // ---- epilogue: warp w holds rows m0 + 32 w + lane in its tensor-memory lanes
+    bool ok = mbar_wait_bounded(done, 0);
+    ok = __syncthreads_and(ok) != 0;   // the barrier also orders the s_fail writes
+    ok = ok && s_fail == 0;
+    tc::fence_after_sync();
+    if (ok) {
+        const int row = m0 + 32 * warp + lane;
+        const uint32_t trow = tm + ((uint32_t)(32 * warp) << 16);
+#pragma unroll 1
+        for (int c = 0; c < DT_BN / 32; ++c) {
+            float v[32];
+            tc::ld_x32(trow + 32 * c, v);
+            const int col = n0 + 32 * c;
+            if (row < a.M && col < a.N) {
+                float* dst = a.y + (size_t)row * a.ldy + col;
+                if (col + 32 <= a.N) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (col + i < a.N) dst[i] = v[i];
+                }
+            }
+        }
+    } else if (threadIdx.x == 0 && s_fail == 0) {
+        dense_error(a.err, 302);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) tc::tmem_dealloc(tm, DT_BN);
+}
+
+template <bool SPLIT>
+int launch_one(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
+    constexpr size_t smem = DenseCfg<SPLIT>::SMEM;
+    static_assert(smem <= 232448, "dense GEMM shared memory exceeds the per-block limit");
+    static bool set = false;
+    if (!set) {
+        const cudaError_t e = cudaFuncSetAttribute(gemm_dense_kernel<SPLIT>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return (int)e;
+        set = true;
+    }
+    const dim3 grid((unsigned)((a.M + DT_BM - 1) / DT_BM), (unsigned)((a.N + DT_BN - 1) / DT_BN));
+    return (int)launch_k(gemm_dense_kernel<SPLIT>, grid, dim3(128), smem, s, maps, a);
+}
+
+}  // namespace
+
+size_t dense_smem(bool split) { return split ? DenseCfg<true>::SMEM : DenseCfg<false>::SMEM; }
+
+int launch_dense(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
+    if (a.M < 1 || a.N < 1 || a.K < DT_BK || a.K % DT_BK || a.ldy < a.N || a.ldy % 4 ||
+        a.n_seg0 % DT_BN)
+        return (int)cudaErrorInvalidValue;
+    return a.x_split ? launch_one<true>(maps, a, s) : launch_one<false>(maps, a, s);
+}
+
+}  // namespace dfl

@@ -1,0 +1,37 @@
+// Dense many-row GEMM on the fifth-generation tensor cores:
+// y[m][n] = sum_k x[m][k] * w[n][k], x and w bf16 (w in nn.Linear layout),
+// y fp32, accumulated in tensor memory.  Serves the dense part of the
+// round's pipeline, the drafter's context-window ingest (fc over the
+// window's tap rows, then every draft layer's context K/V), where the rows
+// number hundreds to thousands and the work is a real contraction.
+#pragma once
+
+#include "common.cuh"
+
+namespace dfl {
+
+constexpr int DT_BM = 128;   // rows of x per CTA (tensor-memory lanes)
+constexpr int DT_BN = 256;   // output columns per CTA (tensor-memory columns)
+constexpr int DT_BK = 64;    // k per pipeline stage (one 128-byte swizzled row)
+
+struct DenseMaps {
+    CUtensorMap x;      // [M][K] bf16, box [128 rows][64]
+    CUtensorMap x_lo;   // low plane of x when x_split (same shape)
+    CUtensorMap w[2];   // [N_i][K] bf16 segments concatenated along n, box [256 rows][64]
+};
+
+struct DenseArgs {
+    int M, N, K;        // K a multiple of 64
+    int n_seg0;         // columns of w[0] (a multiple of 256); n >= n_seg0 reads w[1]
+    int x_split;        // 1: x = x (hi) + x_lo, two MMAs per k step
+    float* y;           // [M][ldy] fp32
+    int ldy;            // a multiple of 4
+    int* err;           // device [code, site]: a wait that timed out sets it (code 0 before)
+};
+
+// Host: dynamic shared memory of the kernel (x_split or not), the launch
+// (grid ceil(M/128) x ceil(N/256), 128 threads).  Returns 0 or a cudaError_t.
+size_t dense_smem(bool split);
+int launch_dense(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s);
+
+}  // namespace dfl

@@ -382,6 +382,24 @@ int dflash_linear(const void* w, const void* x, int32_t n, int32_t k, float* y, 
 int dflash_linear_noalloc(const void* w, const void* x, int32_t n, int32_t k, float* y,
                           dflash_stream_t stream);
 
+/*
+ * Dense many-row GEMM on the fifth-generation tensor cores (tcgen05, f32
+ * accumulators in tensor memory): y[m][j] = sum_i x[m][i] * w[j][i] (+ the
+ * same with x_lo) for m < M, j < N.  x bf16 row-major [M][K]; x_lo a second
+ * bf16 plane of x added to it (the low part of an fp32 activation split
+ * into bf16 hi + lo), or NULL; w bf16 [N][K] (nn.Linear layout); y fp32
+ * [M][N].  M >= 1, N >= 1, K a multiple of 64, every pointer 16-byte
+ * aligned.  err: device int32[2], zero before the call; a kernel wait that
+ * timed out writes 1 and a site number there (kernels never trap).  The library's
+ * kernel for the dense step of the round's pipeline: the drafter's
+ * context-window ingest (the fc re-projection of the window's tap rows and
+ * each draft layer's context K/V, "[RFC] DFlash", "Requested changes" 3,
+ * the persistent draft KV cache), where the rows number in the hundreds or
+ * thousands.  Errors: ARG, CUDA.
+ */
+int dflash_linear_dense(const void* w, const void* x, const void* x_lo, int32_t m, int32_t n, int32_t k,
+                        float* y, int32_t* err, dflash_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
