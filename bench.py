@@ -483,7 +483,7 @@ def measure_workloads(steps, warmup, base_model):
         out[w.name] = {
             "window_prefill": {"rows": win_rows, "s": round(prefill_s, 5),
                                "tflops": round(prefill_flop / prefill_s / 1e12, 2),
-                               "path": "16-row chunks through the skinny GEMM"},
+                               "path": "dense tcgen05 GEMM (fc, bf16 context K/V) in 1024-row passes" if not w.drf_int4 else "16-row chunks through the skinny GEMM (INT4 drafter)"},
             "draft_rounds_s": round(1e3 / ms, 2), "ms_per_round": round(ms, 4),
             "bytes_per_round": int(total), "hbm_gbs": round(total / (ms / 1e3) / 1e9, 1),
             "frac_of_peak": round(total / (ms / 1e3) / 1e9 / peak, 4),
@@ -553,6 +553,36 @@ def measure_workloads(steps, warmup, base_model):
         "attention_form": {1: "mma.sync split-KV", 2: "tcgen05"}.get(capi.dflash_attention_form(dec.ctx, 0)),
         "note": "same round as the headline line with DFLASH_ATTN_TC=1"}
     dec.close()
+    # --- the dense tcgen05 GEMM alone, at the window-ingest shapes
+    bf16_peak, bf16_src = 1900.0, "fallback"
+    try:
+        pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        if pk.get("bf16_tflops"):
+            bf16_peak, bf16_src = float(pk["bf16_tflops"]), "measured (bf16_tflops, burst)"
+    except Exception:
+        pass
+    dense = {}
+    for m, n, k, split, what in [(2048, 2560, 12800, False, "fc over a 2048-row window (5 taps)"),
+                                 (2048, 2048, 2560, True, "context K/V of one draft layer, hi + lo input")]:
+        gen = torch.Generator(device="cuda").manual_seed(9)
+        wd = (torch.randn(n, k, device="cuda", generator=gen) * 0.02).to(torch.bfloat16)
+        xd = torch.randn(m, k, device="cuda", generator=gen).to(torch.bfloat16)
+        xl = (torch.randn(m, k, device="cuda", generator=gen) * 2 ** -9).to(torch.bfloat16) if split else None
+        yd = torch.empty(m, n, device="cuda")
+        errw = torch.zeros(2, dtype=torch.int32, device="cuda")
+        ms, gd = _graph_time(lambda: capi.dflash_linear_dense(wd, xd, yd, errw, x_lo=xl), max(steps, 20),
+                             warmup)
+        del gd
+        assert errw.tolist() == [0, 0]
+        flop = 2.0 * m * n * k * (2 if split else 1)
+        tf = flop / (ms / 1e3) / 1e12
+        dense[f"{m}x{n}x{k}" + ("_hilo" if split else "")] = {
+            "what": what, "us": round(ms * 1e3, 2), "tflops": round(tf, 1),
+            "frac_of_bf16_peak": round(tf / bf16_peak, 4)}
+        del wd, xd, xl, yd
+    out["dense_gemm_tcgen05"] = {"peak_tflops": bf16_peak, "peak_source": bf16_src,
+                                 "note": "inputs stay in L2 across replays; the kernel is tensor-bound",
+                                 "by_shape": dense}
     # --- verify sweep over a 16384-position synthetic KV cache
     w = HC_SWEEP
     dec = DFlash(w, base_model)

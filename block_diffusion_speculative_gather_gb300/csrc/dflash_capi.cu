@@ -68,7 +68,7 @@ int max_chunks(const dflash_config& c) { return cache_cap(c) / ATTN_CHUNK; }
 
 struct Layout {
     size_t state, x, hn, ssq, qrot, attn, act, taps, rcos, rsin, invf, amax, part, slots, counters,
-        acnt, amaps, barc, prog[3], ns[3], total;
+        acnt, amaps, barc, prog[3], ns[3], pf_x, pf_y, pf_chi, pf_clo, total;
     int prog_n[3];
 };
 
@@ -102,6 +102,14 @@ constexpr int MAX_SMS = 256 * DFL_GEMM_CTAS_PER_SM;   // GEMM CTAs (split-K slot
 #define DFL_ATTN_MIN_SPLIT 1
 #endif
 constexpr int MAX_TILES = 8192;
+
+// Window ingest on the dense tcgen05 GEMM: rows per pass, and whether the
+// configuration has it (bf16 drafter, shapes the GEMM's tiles cover).
+constexpr int PF_ROWS = 1024;
+bool dense_ingest_ok(const dflash_config& c) {
+    return c.dtype == DFLASH_BF16 && c.drf_layers > 0 && c.drf_wfmt == DFLASH_BF16 && c.n_taps > 0 &&
+           c.hidden % 64 == 0 && (c.n_kv * c.head_dim) % 256 == 0 && c.hidden % 4 == 0;
+}
 
 // Workspace carving.  hn holds the next GEMM's normalised input rows
 // (x * w_norm, activation type) and ssq their per-128-column partial sums
@@ -137,6 +145,13 @@ Layout make_layout(const dflash_config& c) {
     L.acnt = take((size_t)2 * c.n_kv * 4);
     L.amaps = take(2 * sizeof(AttnMaps));
     L.barc = take(256);
+    if (dense_ingest_ok(c)) {   // [PF_ROWS] rows: taps bf16, GEMM out fp32, context rows hi/lo bf16
+        const size_t kv = (size_t)2 * c.n_kv * c.head_dim;
+        L.pf_x = take((size_t)PF_ROWS * c.n_taps * c.hidden * 2);
+        L.pf_y = take((size_t)PF_ROWS * (kv > (size_t)c.hidden ? kv : (size_t)c.hidden) * 4);
+        L.pf_chi = take((size_t)PF_ROWS * c.hidden * 2);
+        L.pf_clo = take((size_t)PF_ROWS * c.hidden * 2);
+    }
     for (int i = 0; i < 3; ++i) {
         L.prog_n[i] = program_phases(c, i);
         L.prog[i] = take((size_t)L.prog_n[i] * sizeof(Phase));
@@ -273,6 +288,9 @@ struct dflash_ctx {
     int attn_split_chunks[2] = {0, 0};
     int attn_max_splits[2] = {0, 0};
     int attn_tc[2] = {0, 0};   // tcgen05 form of the fused attention
+    bool dense_ingest = false;  // window ingest on the dense tcgen05 GEMM
+    DenseMaps d_fc{};           // fc over the window's tap rows
+    std::vector<DenseMaps> d_kv;   // per draft layer: context K/V from the context rows
     float* verify_logits = nullptr;
     float* draft_logits = nullptr;
     bool prefilled = false;
@@ -978,6 +996,25 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
             }
         }
     }
+    // window ingest on the dense tcgen05 GEMM (DFLASH_DENSE_INGEST=0 keeps
+    // the 16-row chunks through the round's kernels)
+    const char* di_env = getenv("DFLASH_DENSE_INGEST");
+    if (!r && dense_ingest_ok(g) && !(di_env && di_env[0] == '0')) {
+        const uint64_t K1 = (uint64_t)g.n_taps * g.hidden, kvr = (uint64_t)g.n_kv * g.head_dim;
+        const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+        r = make_map_raw(&c->d_fc.x, c->ws + L.pf_x, bf, 2, K1, PF_ROWS, DT_BK, DT_BM, sw);
+        if (!r) r = make_map_raw(&c->d_fc.w[0], w->fc, bf, 2, K1, g.hidden, DT_BK, DT_BN, sw);
+        c->d_kv.resize(g.drf_layers);
+        for (int l = 0; l < g.drf_layers && !r; ++l) {
+            DenseMaps& m = c->d_kv[l];
+            r = make_map_raw(&m.x, c->ws + L.pf_chi, bf, 2, g.hidden, PF_ROWS, DT_BK, DT_BM, sw);
+            if (!r) r = make_map_raw(&m.x_lo, c->ws + L.pf_clo, bf, 2, g.hidden, PF_ROWS, DT_BK, DT_BM, sw);
+            if (!r) r = make_map_raw(&m.w[0], c->drf[l].wk, bf, 2, g.hidden, kvr, DT_BK, DT_BN, sw);
+            if (!r) r = make_map_raw(&m.w[1], c->drf[l].wv, bf, 2, g.hidden, kvr, DT_BK, DT_BN, sw);
+        }
+        c->dense_ingest = !r;
+    }
     if (r) {
         delete c;
         return r;
@@ -1093,6 +1130,84 @@ int dflash_set_logits_out(dflash_ctx* ctx, float* verify_logits, float* draft_lo
     return DFLASH_OK;
 }
 
+namespace {
+
+// The drafter's context-window ingest as dense work, PF_ROWS rows per pass
+// (positions p0..p0+R-1 of the external tap rows): tap rows (bf16) -> fc on
+// the dense GEMM -> context RMSNorm into bf16 hi/lo rows -> per draft layer
+// [W_k; W_v] on the dense GEMM (hi + lo) -> k-norm, RoPE and the cache rows.
+int run_dense_ingest(dflash_ctx* c, const void* ext_taps, int n_ext, int commit_lo, cudaStream_t s) {
+    const dflash_config& g = c->cfg;
+    const int kvr = g.n_kv * g.head_dim;
+    int* err = &c->st()->err;
+    for (int p0 = commit_lo; p0 < n_ext; p0 += PF_ROWS) {
+        const int R = n_ext - p0 < PF_ROWS ? n_ext - p0 : PF_ROWS;
+        TapArgs ta{};
+        for (int i = 0; i < g.n_taps; ++i)
+            ta.src[i] = static_cast<const uint8_t*>(ext_taps) + ((size_t)i * n_ext + p0) * g.hidden * 2;
+        ta.n_layers = g.n_taps;
+        ta.rows = R;
+        ta.hc = 1;
+        ta.hidden = g.hidden;
+        ta.in_type = XT_BF16;
+        ta.out = c->ws + c->L.pf_x;
+        ta.out_type = XT_BF16;
+        ta.out_row_stride = (long long)g.n_taps * g.hidden;
+        LAUNCH_TRY(launch_tap_reduce(ta, s));
+        DenseArgs fa{};
+        fa.M = R;
+        fa.N = g.hidden;
+        fa.K = g.n_taps * g.hidden;
+        fa.n_seg0 = (g.hidden + DT_BN - 1) / DT_BN * DT_BN;
+        fa.y = c->buf<float>(c->L.pf_y);
+        fa.ldy = g.hidden;
+        fa.err = err;
+        LAUNCH_TRY(launch_dense(c->d_fc, fa, s));
+        CtxRowsArgs ra{};
+        ra.y = fa.y;
+        ra.rows = R;
+        ra.hidden = g.hidden;
+        ra.w = g.ctx_norm ? c->w.ctx_norm : nullptr;
+        ra.norm = g.ctx_norm ? 1 : 0;
+        ra.eps = g.rms_eps;
+        ra.c_hi = c->ws + c->L.pf_chi;
+        ra.c_lo = c->ws + c->L.pf_clo;
+        LAUNCH_TRY(launch_ctx_rows(ra, s));
+        for (int l = 0; l < g.drf_layers; ++l) {
+            DenseArgs ka{};
+            ka.M = R;
+            ka.N = 2 * kvr;
+            ka.K = g.hidden;
+            ka.n_seg0 = kvr;
+            ka.x_split = 1;
+            ka.y = c->buf<float>(c->L.pf_y);
+            ka.ldy = 2 * kvr;
+            ka.err = err;
+            LAUNCH_TRY(launch_dense(c->d_kv[l], ka, s));
+            const QkvEpi q = qkv_epi(c, c->drf[l], false, l, 0, ROWS_COMMIT);
+            CtxKvArgs ca{};
+            ca.y = ka.y;
+            ca.rows = R;
+            ca.pos0 = p0;
+            ca.n_kv = g.n_kv;
+            ca.head_dim = g.head_dim;
+            ca.cap = q.cap;
+            ca.max_seq = g.max_seq;
+            ca.k_norm = c->drf[l].k_norm;
+            ca.eps = g.rms_eps;
+            ca.inv_freq = c->buf<double>(c->L.invf);
+            ca.k_cache = q.k_cache;
+            ca.v_cache = q.v_cache;
+            ca.c_type = q.c_type;
+            ca.st = c->st();
+            LAUNCH_TRY(launch_ctx_kv_store(ca, s));
+        }
+    }
+    return DFLASH_OK;
+}
+
+}  // namespace
+
 int dflash_prefill_taps(dflash_ctx* c, const int32_t* prompt_ids, int32_t n_prompt,
                         const void* ext_taps, int32_t n_ext, int32_t hc, int32_t first_token,
                         int32_t max_new, dflash_stream_t stream) {
@@ -1140,6 +1255,9 @@ int dflash_prefill_taps(dflash_ctx* c, const int32_t* prompt_ids, int32_t n_prom
         if (g.hidden % 8) return fail(DFLASH_ERR_CONFIG, "hidden must be a multiple of 8");
         const int commit_lo = g.window > 0 ? (n_ext > g.window ? n_ext - g.window : 0) : 0;
         const int es = elem_size(g.dtype);
+        if (c->dense_ingest && hc == 1) {
+            if ((r = run_dense_ingest(c, ext_taps, n_ext, commit_lo, s))) return r;
+        } else
         for (int p0 = commit_lo / DFL_MAX_ROWS * DFL_MAX_ROWS; p0 < n_ext; p0 += DFL_MAX_ROWS) {
             const int T = n_ext - p0 < DFL_MAX_ROWS ? n_ext - p0 : DFL_MAX_ROWS;
             RowsArgs ra = rows_args(c, FWD_PREFILL);

@@ -211,9 +211,113 @@ __global__ void tap_reduce_kernel(TapArgs a) {
             const float v = acc[e] * inv;
             const OT hi = from_f32<OT>(v);
             dst[e] = hi;
-            // XT_BF16S: the rounding remainder 16 rows further down
-            if (SPLIT) dst[e + DFL_MAX_ROWS * a.out_row_stride] = from_f32<OT>(v - to_f32<OT>(hi));
+            // XT_BF16S: the rounding remainder 16 rows further down, or lo_offset away
+            if (SPLIT)
+                dst[e + (a.lo_offset ? a.lo_offset : DFL_MAX_ROWS * a.out_row_stride)] =
+                    from_f32<OT>(v - to_f32<OT>(hi));
         }
+    }
+}
+
+// --------------------------------------------------------------- window ingest
+
+// One CTA of 256 threads per row: sum of squares in a fixed order (per
+// thread, then the warp tree, then the warps in order), then the row.
+__global__ void ctx_rows_kernel(CtxRowsArgs a) {
+    pdl_trigger();
+    pdl_wait();
+    const int r = blockIdx.x, tid = threadIdx.x;
+    const float* y = a.y + (size_t)r * a.hidden;
+    __shared__ float s_part[8];
+    float rstd = 1.f;
+    if (a.norm) {
+        float ss = 0.f;
+        for (int j = tid; j < a.hidden; j += 256) ss = fmaf(y[j], y[j], ss);
+        ss = warp_sum(ss);
+        if ((tid & 31) == 0) s_part[tid >> 5] = ss;
+        __syncthreads();
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) tot += s_part[w];
+        rstd = 1.0f / sqrtf(tot / (float)a.hidden + a.eps);
+    }
+    __nv_bfloat16* hi = reinterpret_cast<__nv_bfloat16*>(a.c_hi) + (size_t)r * a.hidden;
+    __nv_bfloat16* lo = reinterpret_cast<__nv_bfloat16*>(a.c_lo) + (size_t)r * a.hidden;
+    for (int j = tid; j < a.hidden; j += 256) {
+        const float v = a.norm ? y[j] * a.w[j] * rstd : y[j];
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        hi[j] = h;
+        lo[j] = __float2bfloat16_rn(v - __bfloat162float(h));
+    }
+}
+
+// One warp per (row, kv head, K or V); lane l holds elements l + 32 m.
+__global__ void ctx_kv_store_kernel(CtxKvArgs a) {
+    pdl_trigger();
+    pdl_wait();
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    const int items = a.rows * a.n_kv * 2;
+    if (warp >= items) return;
+    const int r = warp / (2 * a.n_kv), rem = warp % (2 * a.n_kv);
+    const bool is_k = rem < a.n_kv;
+    const int kh = is_k ? rem : rem - a.n_kv;
+    const int hd = a.head_dim, per = hd / 32;
+    const int pos = a.pos0 + r;
+    if (pos < 0 || pos >= a.max_seq || pos >= a.cap) {
+        if (lane == 0) set_error(a.st, DERR_INDEX, pos);
+        return;
+    }
+    const float* src = a.y + (size_t)r * 2 * a.n_kv * hd + (size_t)rem * hd;
+    float v[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) v[m] = m < per ? src[lane + 32 * m] : 0.f;
+    if (is_k) {
+        float ss = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) ss = fmaf(v[m], v[m], ss);
+        ss = warp_sum(ss);
+        const float inv = 1.0f / sqrtf(ss / (float)hd + a.eps);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) v[m] = m < per ? v[m] * inv * a.k_norm[lane + 32 * m] : 0.f;
+        // rotate-half RoPE at `pos`: element i pairs with i + hd/2 (m and m + per/2)
+        float cs[2], sn[2];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            cs[m] = 1.f;
+            sn[m] = 0.f;
+            if (m < per / 2) {
+                const double ang = (double)pos * a.inv_freq[lane + 32 * m];
+                const double k = rint(ang * 0.15915494309189535);
+                double rr = fma(-k, 6.283185307179586, ang);
+                rr = fma(-k, 2.4492935982947064e-16, rr);
+                cs[m] = (float)cos(rr);
+                sn[m] = (float)sin(rr);
+            }
+        }
+        float o[4];
+        if (per == 4) {
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                o[m] = v[m] * cs[m] - v[m + 2] * sn[m];
+                o[m + 2] = v[m + 2] * cs[m] + v[m] * sn[m];
+            }
+        } else {
+            o[0] = v[0] * cs[0] - v[1] * sn[0];
+            o[1] = v[1] * cs[0] + v[0] * sn[0];
+            o[2] = o[3] = 0.f;
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) v[m] = o[m];
+    }
+    void* cache = is_k ? a.k_cache : a.v_cache;
+    const size_t base = ((size_t)kh * a.cap + pos) * hd;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        if (m >= per) continue;
+        const size_t i = base + lane + 32 * m;
+        if (a.c_type == XT_F32) reinterpret_cast<float*>(cache)[i] = v[m];
+        else if (a.c_type == XT_BF16) reinterpret_cast<__nv_bfloat16*>(cache)[i] = __float2bfloat16_rn(v[m]);
+        else reinterpret_cast<__half*>(cache)[i] = __float2half_rn(v[m]);
     }
 }
 
@@ -362,12 +466,23 @@ int launch_tap_reduce(const TapArgs& a, cudaStream_t s) {
     if (a.in_type == XT_BF16 && a.out_type == XT_BF16)
         return ok(launch_k(tap_reduce_kernel<__nv_bfloat16, __nv_bfloat16>, g, b, 0, s, a));
     if (a.in_type == XT_BF16 && a.out_type == XT_BF16S) {
-        if (a.rows > DFL_MAX_ROWS) return -2;   // the lo plane sits 16 rows below
+        if (a.rows > DFL_MAX_ROWS && !a.lo_offset) return -2;   // the lo plane sits 16 rows below
         return ok(launch_k(tap_reduce_kernel<__nv_bfloat16, __nv_bfloat16, true>, g, b, 0, s, a));
     }
     if (a.in_type == XT_F32 && a.out_type == XT_F32)
         return ok(launch_k(tap_reduce_kernel<float, float>, g, b, 0, s, a));
     return -2;
+}
+
+int launch_ctx_rows(const CtxRowsArgs& a, cudaStream_t s) {
+    if (a.rows < 1) return 0;
+    return ok(launch_k(ctx_rows_kernel, dim3((unsigned)a.rows), dim3(256), 0, s, a));
+}
+
+int launch_ctx_kv_store(const CtxKvArgs& a, cudaStream_t s) {
+    if (a.rows < 1) return 0;
+    const long long warps = (long long)a.rows * a.n_kv * 2;
+    return ok(launch_k(ctx_kv_store_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, a));
 }
 
 int launch_progress(const DevState* st, int32_t* out, cudaStream_t s) {

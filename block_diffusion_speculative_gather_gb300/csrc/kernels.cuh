@@ -88,9 +88,41 @@ struct TapArgs {
     void* out;            // [rows][n_layers * hidden], out_type
     int out_type;
     long long out_row_stride;   // elements between output rows
+    long long lo_offset;        // XT_BF16S: elements from a value to its low part (0: 16 rows below)
 };
 
 int launch_tap_reduce(const TapArgs& a, cudaStream_t s);
+
+// Context rows of a window ingest (many rows at once): c = RMSNorm(y) * w
+// (or c = y without the norm), y fp32 [rows][hidden], written as bf16 hi
+// and lo planes [rows][hidden] (c = hi + lo to 16 bits).
+struct CtxRowsArgs {
+    const float* y;
+    int rows, hidden;
+    const float* w;       // [hidden] ctx norm weight; NULL with norm = 0
+    int norm;
+    float eps;
+    void* c_hi;
+    void* c_lo;
+};
+int launch_ctx_rows(const CtxRowsArgs& a, cudaStream_t s);
+
+// Context K/V of a window ingest for one draft layer: y fp32 [rows][2 n_kv
+// hd] (K heads, then V heads) of rows at positions pos0 + r; K gets the
+// per-head k RMSNorm and RoPE at its position, both go to the layer's cache
+// rows ([n_kv][cap][hd], c_type) as the round's q/k/v epilogue writes them.
+struct CtxKvArgs {
+    const float* y;
+    int rows, pos0, n_kv, head_dim, cap, max_seq;
+    const float* k_norm;    // [head_dim]
+    float eps;
+    const double* inv_freq; // [head_dim / 2]
+    void* k_cache;
+    void* v_cache;
+    int c_type;
+    DevState* st;
+};
+int launch_ctx_kv_store(const CtxKvArgs& a, cudaStream_t s);
 
 int launch_selftest_wait(DevState* st, unsigned long long limit_ns, cudaStream_t s);
 

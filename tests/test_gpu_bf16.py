@@ -171,3 +171,36 @@ def test_attention_forms_agree(qwen, monkeypatch, max_seq, chunks):
     for a, b in zip(out[0], out[1]):
         err = G.rel_err_rows(a.cpu().numpy(), b.cpu().numpy())
         assert err.max() < TOL / 4, err
+
+
+def test_dense_ingest_matches_chunked(qwen, monkeypatch):
+    """The context-window ingest on the dense tcgen05 GEMM (default for bf16
+    drafters) writes the same draft K/V cache rows as the 16-row chunks
+    through the round's kernels (DFLASH_DENSE_INGEST=0) up to fp16 rounding
+    of the cache, and the next draft's logits agree within the parity
+    tolerance.  300 tap rows: two 128-row tiles and a ragged third."""
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+    Wd = W.with_(tgt_layers=0, tap_layers=(0, 8, 17, 26, 35)[:2], max_seq=512)
+    n = 300
+    taps = synth.tap_rows(n, Wd.n_taps * W.hidden)
+    ext = taps.view(n, Wd.n_taps, W.hidden).permute(1, 0, 2).contiguous()
+    out = []
+    for env in (None, "0"):
+        if env is not None:
+            monkeypatch.setenv("DFLASH_DENSE_INGEST", env)
+        dec = DFlash(Wd, qwen["m"])
+        monkeypatch.delenv("DFLASH_DENSE_INGEST", raising=False)
+        dl = G.logits_buf(W.vocab)
+        dec.set_logits_out(None, dl)
+        dec.prefill_taps(ext, hc=1, first_token=321, max_new=32)
+        dec.draft()
+        dec.check()
+        cap = (Wd.max_seq + 63) // 64 * 64
+        kv = dec.kv_draft.view(torch.float16).view(Wd.drf_layers, 2, Wd.n_kv, cap, W.head_dim)
+        out.append((kv[:, :, :, :n].float().clone(), dl[1:W.block].clone()))
+        dec.close()
+    (kv_d, lg_d), (kv_c, lg_c) = out
+    scale = kv_c.abs().amax(dim=-1, keepdim=True).clamp_min(1e-6)
+    assert ((kv_d - kv_c).abs() / scale).max().item() < 2.0 ** -9
+    err = G.rel_err_rows(lg_d.cpu().numpy(), lg_c.cpu().numpy())
+    assert err.max() < TOL / 4, err
