@@ -483,7 +483,8 @@ def measure_workloads(steps, warmup, base_model):
         out[w.name] = {
             "window_prefill": {"rows": win_rows, "s": round(prefill_s, 5),
                                "tflops": round(prefill_flop / prefill_s / 1e12, 2),
-                               "path": "dense tcgen05 GEMM (fc, bf16 context K/V) in 1024-row passes" if not w.drf_int4 else "16-row chunks through the skinny GEMM (INT4 drafter)"},
+                               "path": "dense tcgen05 GEMM in 1024-row passes (fc bf16; context K/V " +
+                                       ("f16 from the INT4 weights dequantised)" if w.drf_int4 else "bf16)")},
             "draft_rounds_s": round(1e3 / ms, 2), "ms_per_round": round(ms, 4),
             "bytes_per_round": int(total), "hbm_gbs": round(total / (ms / 1e3) / 1e9, 1),
             "frac_of_peak": round(total / (ms / 1e3) / 1e9 / peak, 4),

@@ -68,7 +68,7 @@ int max_chunks(const dflash_config& c) { return cache_cap(c) / ATTN_CHUNK; }
 
 struct Layout {
     size_t state, x, hn, ssq, qrot, attn, act, taps, rcos, rsin, invf, amax, part, slots, counters,
-        acnt, amaps, barc, prog[3], ns[3], pf_x, pf_y, pf_chi, pf_clo, total;
+        acnt, amaps, barc, prog[3], ns[3], pf_x, pf_y, pf_chi, pf_clo, pf_w, total;
     int prog_n[3];
 };
 
@@ -107,8 +107,9 @@ constexpr int MAX_TILES = 8192;
 // configuration has it (bf16 drafter, shapes the GEMM's tiles cover).
 constexpr int PF_ROWS = 1024;
 bool dense_ingest_ok(const dflash_config& c) {
-    return c.dtype == DFLASH_BF16 && c.drf_layers > 0 && c.drf_wfmt == DFLASH_BF16 && c.n_taps > 0 &&
-           c.hidden % 64 == 0 && (c.n_kv * c.head_dim) % 256 == 0 && c.hidden % 4 == 0;
+    return c.dtype == DFLASH_BF16 && c.drf_layers > 0 && c.n_taps > 0 &&
+           (c.drf_wfmt == DFLASH_BF16 || c.drf_wfmt == DFLASH_INT4G64) && c.hidden % 64 == 0 &&
+           (c.n_kv * c.head_dim) % 256 == 0 && c.hidden % 4 == 0;
 }
 
 // Workspace carving.  hn holds the next GEMM's normalised input rows
@@ -151,6 +152,8 @@ Layout make_layout(const dflash_config& c) {
         L.pf_y = take((size_t)PF_ROWS * (kv > (size_t)c.hidden ? kv : (size_t)c.hidden) * 4);
         L.pf_chi = take((size_t)PF_ROWS * c.hidden * 2);
         L.pf_clo = take((size_t)PF_ROWS * c.hidden * 2);
+        if (c.drf_wfmt == DFLASH_INT4G64)   // one layer's [W_k; W_v] dequantised to f16
+            L.pf_w = take(kv * c.hidden * 2);
     }
     for (int i = 0; i < 3; ++i) {
         L.prog_n[i] = program_phases(c, i);
@@ -1006,12 +1009,16 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
         r = make_map_raw(&c->d_fc.x, c->ws + L.pf_x, bf, 2, K1, PF_ROWS, DT_BK, DT_BM, sw);
         if (!r) r = make_map_raw(&c->d_fc.w[0], w->fc, bf, 2, K1, g.hidden, DT_BK, DT_BN, sw);
         c->d_kv.resize(g.drf_layers);
+        const bool q4 = g.drf_wfmt == DFLASH_INT4G64;   // f16 operands: rows and dequantised weights
+        const CUtensorMapDataType xt = q4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : bf;
         for (int l = 0; l < g.drf_layers && !r; ++l) {
             DenseMaps& m = c->d_kv[l];
-            r = make_map_raw(&m.x, c->ws + L.pf_chi, bf, 2, g.hidden, PF_ROWS, DT_BK, DT_BM, sw);
-            if (!r) r = make_map_raw(&m.x_lo, c->ws + L.pf_clo, bf, 2, g.hidden, PF_ROWS, DT_BK, DT_BM, sw);
-            if (!r) r = make_map_raw(&m.w[0], c->drf[l].wk, bf, 2, g.hidden, kvr, DT_BK, DT_BN, sw);
-            if (!r) r = make_map_raw(&m.w[1], c->drf[l].wv, bf, 2, g.hidden, kvr, DT_BK, DT_BN, sw);
+            r = make_map_raw(&m.x, c->ws + L.pf_chi, xt, 2, g.hidden, PF_ROWS, DT_BK, DT_BM, sw);
+            if (!r) r = make_map_raw(&m.x_lo, c->ws + L.pf_clo, xt, 2, g.hidden, PF_ROWS, DT_BK, DT_BM, sw);
+            if (!r && q4)
+                r = make_map_raw(&m.w[0], c->ws + L.pf_w, xt, 2, g.hidden, 2 * kvr, DT_BK, DT_BN, sw);
+            if (!r && !q4) r = make_map_raw(&m.w[0], c->drf[l].wk, bf, 2, g.hidden, kvr, DT_BK, DT_BN, sw);
+            if (!r && !q4) r = make_map_raw(&m.w[1], c->drf[l].wv, bf, 2, g.hidden, kvr, DT_BK, DT_BN, sw);
         }
         c->dense_ingest = !r;
     }
@@ -1134,8 +1141,11 @@ namespace {
 
 // The drafter's context-window ingest as dense work, PF_ROWS rows per pass
 // (positions p0..p0+R-1 of the external tap rows): tap rows (bf16) -> fc on
-// the dense GEMM -> context RMSNorm into bf16 hi/lo rows -> per draft layer
+// the dense GEMM -> context RMSNorm into hi/lo rows -> per draft layer
 // [W_k; W_v] on the dense GEMM (hi + lo) -> k-norm, RoPE and the cache rows.
+// bf16 drafters use bf16 rows and weights; INT4 drafters f16 rows and the
+// layer's W_k, W_v dequantised exactly to f16 first (the tensor core takes
+// one type for both operands).
 int run_dense_ingest(dflash_ctx* c, const void* ext_taps, int n_ext, int commit_lo, cudaStream_t s) {
     const dflash_config& g = c->cfg;
     const int kvr = g.n_kv * g.head_dim;
@@ -1172,13 +1182,25 @@ int run_dense_ingest(dflash_ctx* c, const void* ext_taps, int n_ext, int commit_
         ra.eps = g.rms_eps;
         ra.c_hi = c->ws + c->L.pf_chi;
         ra.c_lo = c->ws + c->L.pf_clo;
+        const bool q4 = g.drf_wfmt == DFLASH_INT4G64;
+        ra.f16 = q4 ? 1 : 0;
         LAUNCH_TRY(launch_ctx_rows(ra, s));
         for (int l = 0; l < g.drf_layers; ++l) {
+            if (q4) {   // this layer's W_k and W_v, dequantised (exactly) to f16
+                uint8_t* wq = c->ws + c->L.pf_w;
+                LAUNCH_TRY(launch_dequant_int4g64_f16(static_cast<const uint8_t*>(c->drf[l].wk),
+                                                      static_cast<const uint16_t*>(c->drf[l].sk), kvr,
+                                                      g.hidden, wq, s));
+                LAUNCH_TRY(launch_dequant_int4g64_f16(static_cast<const uint8_t*>(c->drf[l].wv),
+                                                      static_cast<const uint16_t*>(c->drf[l].sv), kvr,
+                                                      g.hidden, wq + (size_t)kvr * g.hidden * 2, s));
+            }
             DenseArgs ka{};
             ka.M = R;
             ka.N = 2 * kvr;
             ka.K = g.hidden;
-            ka.n_seg0 = kvr;
+            ka.n_seg0 = q4 ? (2 * kvr + DT_BN - 1) / DT_BN * DT_BN : kvr;
+            ka.f16 = q4 ? 1 : 0;
             ka.x_split = 1;
             ka.y = c->buf<float>(c->L.pf_y);
             ka.ldy = 2 * kvr;

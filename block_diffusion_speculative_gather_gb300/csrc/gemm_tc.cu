@@ -1,8 +1,8 @@
 // Dense many-row GEMM on tcgen05 (see gemm_tc.cuh).
 //
 // One CTA per 128 x 256 output tile, 128 threads.  Thread 0 is the TMA
-// producer: a ring of k-blocks (the x tile [128][64] bf16, its low plane
-// when x_split, and the w tile [256][64] bf16, all 128-byte swizzled,
+// producer: a ring of k-blocks (the x tile [128][64], its low plane when
+// x_split, and the w tile [256][64], bf16 or all f16, 128-byte swizzled,
 // K-major).  Thread 32 issues tcgen05.mma (M 128, N 256, K 16, f32
 // accumulators in 256 tensor-memory columns) four times per k-block (twice
 // that with the low plane) and commits each stage back to the producer
@@ -33,7 +33,7 @@ struct DenseCfg {
     static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + (2 * STAGES + 1) * 8 + 16;
 };
 
-template <bool SPLIT>
+template <bool SPLIT, bool F16>
 __global__ void __launch_bounds__(128, 1)
 gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
     using CFG = DenseCfg<SPLIT>;
@@ -88,7 +88,7 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
             tma_load_2d(st + (SPLIT ? 2 : 1) * CFG::XB, &maps.w[seg], &full[s], kb * DT_BK, wrow);
         }
     } else if (threadIdx.x == 32) {   // ---- MMA issuer
-        constexpr uint32_t ID = tc::idesc_bf16_f32(DT_BM, DT_BN);
+        constexpr uint32_t ID = F16 ? tc::idesc_f16_f32(DT_BM, DT_BN) : tc::idesc_bf16_f32(DT_BM, DT_BN);
         for (int kb = 0; kb < nkb; ++kb) {
             const int s = kb % STAGES;
             if (!mbar_wait_bounded(&full[s], (uint32_t)((kb / STAGES) & 1))) {
@@ -145,19 +145,19 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
     if (warp == 1) tc::tmem_dealloc(tm, DT_BN);
 }
 
-template <bool SPLIT>
+template <bool SPLIT, bool F16>
 int launch_one(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
     constexpr size_t smem = DenseCfg<SPLIT>::SMEM;
     static_assert(smem <= 232448, "dense GEMM shared memory exceeds the per-block limit");
     static bool set = false;
     if (!set) {
-        const cudaError_t e = cudaFuncSetAttribute(gemm_dense_kernel<SPLIT>,
+        const cudaError_t e = cudaFuncSetAttribute(gemm_dense_kernel<SPLIT, F16>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return (int)e;
         set = true;
     }
     const dim3 grid((unsigned)((a.M + DT_BM - 1) / DT_BM), (unsigned)((a.N + DT_BN - 1) / DT_BN));
-    return (int)launch_k(gemm_dense_kernel<SPLIT>, grid, dim3(128), smem, s, maps, a);
+    return (int)launch_k(gemm_dense_kernel<SPLIT, F16>, grid, dim3(128), smem, s, maps, a);
 }
 
 }  // namespace
@@ -168,7 +168,8 @@ int launch_dense(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
     if (a.M < 1 || a.N < 1 || a.K < DT_BK || a.K % DT_BK || a.ldy < a.N || a.ldy % 4 ||
         a.n_seg0 % DT_BN)
         return (int)cudaErrorInvalidValue;
-    return a.x_split ? launch_one<true>(maps, a, s) : launch_one<false>(maps, a, s);
+    if (a.f16) return a.x_split ? launch_one<true, true>(maps, a, s) : launch_one<false, true>(maps, a, s);
+    return a.x_split ? launch_one<true, false>(maps, a, s) : launch_one<false, false>(maps, a, s);
 }
 
 }  // namespace dfl

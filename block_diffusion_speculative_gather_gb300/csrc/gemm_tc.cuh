@@ -1,5 +1,5 @@
 // Dense many-row GEMM on the fifth-generation tensor cores:
-// y[m][n] = sum_k x[m][k] * w[n][k], x and w bf16 (w in nn.Linear layout),
+// y[m][n] = sum_k x[m][k] * w[n][k], x and w bf16 or both f16 (w in nn.Linear layout),
 // y fp32, accumulated in tensor memory.  Serves the dense part of the
 // round's pipeline, the drafter's context-window ingest (fc over the
 // window's tap rows, then every draft layer's context K/V), where the rows
@@ -24,6 +24,7 @@ struct DenseArgs {
     int M, N, K;        // K a multiple of 64
     int n_seg0;         // columns of w[0] (a multiple of 256); n >= n_seg0 reads w[1]
     int x_split;        // 1: x = x (hi) + x_lo, two MMAs per k step
+    int f16;            // 1: x and w are f16 (else bf16); both operands always share one type
     float* y;           // [M][ldy] fp32
     int ldy;            // a multiple of 4
     int* err;           // device [code, site]: a wait that timed out sets it (code 0 before)

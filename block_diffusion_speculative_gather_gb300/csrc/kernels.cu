@@ -241,13 +241,40 @@ __global__ void ctx_rows_kernel(CtxRowsArgs a) {
         for (int w = 0; w < 8; ++w) tot += s_part[w];
         rstd = 1.0f / sqrtf(tot / (float)a.hidden + a.eps);
     }
-    __nv_bfloat16* hi = reinterpret_cast<__nv_bfloat16*>(a.c_hi) + (size_t)r * a.hidden;
-    __nv_bfloat16* lo = reinterpret_cast<__nv_bfloat16*>(a.c_lo) + (size_t)r * a.hidden;
     for (int j = tid; j < a.hidden; j += 256) {
         const float v = a.norm ? y[j] * a.w[j] * rstd : y[j];
-        const __nv_bfloat16 h = __float2bfloat16_rn(v);
-        hi[j] = h;
-        lo[j] = __float2bfloat16_rn(v - __bfloat162float(h));
+        const size_t i = (size_t)r * a.hidden + j;
+        if (a.f16) {
+            const __half h = __float2half_rn(v);
+            reinterpret_cast<__half*>(a.c_hi)[i] = h;
+            reinterpret_cast<__half*>(a.c_lo)[i] = __float2half_rn(v - __half2float(h));
+        } else {
+            const __nv_bfloat16 h = __float2bfloat16_rn(v);
+            reinterpret_cast<__nv_bfloat16*>(a.c_hi)[i] = h;
+            reinterpret_cast<__nv_bfloat16*>(a.c_lo)[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+        }
+    }
+}
+
+// One thread per 32-bit word of the packed rows (8 consecutive inputs).
+__global__ void dequant_int4g64_f16_kernel(const uint32_t* __restrict__ packed,
+                                           const uint16_t* __restrict__ scales, int n, int k,
+                                           __half* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
+    const long long words = (long long)n * (k / 8);
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < words;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int row = (int)(i / (k / 8)), k0 = (int)(i % (k / 8)) * 8;
+        const uint32_t wv = packed[i];
+        const float sc = __uint_as_float((uint32_t)scales[(size_t)(k0 / 64) * n + row] << 16);
+        __half h[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            h[2 * j] = __float2half_rn((float)((int)((wv >> (4 * j)) & 15u) - 8) * sc);
+            h[2 * j + 1] = __float2half_rn((float)((int)((wv >> (4 * j + 16)) & 15u) - 8) * sc);
+        }
+        *reinterpret_cast<uint4*>(out + (size_t)row * k + k0) = *reinterpret_cast<const uint4*>(h);
     }
 }
 
@@ -477,6 +504,16 @@ int launch_tap_reduce(const TapArgs& a, cudaStream_t s) {
 int launch_ctx_rows(const CtxRowsArgs& a, cudaStream_t s) {
     if (a.rows < 1) return 0;
     return ok(launch_k(ctx_rows_kernel, dim3((unsigned)a.rows), dim3(256), 0, s, a));
+}
+
+int launch_dequant_int4g64_f16(const uint8_t* packed, const uint16_t* scales, int n, int k, void* out,
+                               cudaStream_t s) {
+    const long long words = (long long)n * (k / 8);
+    long long blocks = (words + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    return ok(launch_k(dequant_int4g64_f16_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
+                       reinterpret_cast<const uint32_t*>(packed), scales, n, k,
+                       reinterpret_cast<__half*>(out)));
 }
 
 int launch_ctx_kv_store(const CtxKvArgs& a, cudaStream_t s) {

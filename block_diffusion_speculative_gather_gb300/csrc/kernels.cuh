@@ -104,8 +104,15 @@ struct CtxRowsArgs {
     float eps;
     void* c_hi;
     void* c_lo;
+    int f16;              // 1: the planes are f16 (else bf16)
 };
 int launch_ctx_rows(const CtxRowsArgs& a, cudaStream_t s);
+
+// INT4G64 weights [n][k] (packed [n][k/2], scales bf16 [k/64][n]) to f16
+// [n][k]: code * scale has at most 11 significant bits, so the f16 value is
+// exact (inside f16's normal range).
+int launch_dequant_int4g64_f16(const uint8_t* packed, const uint16_t* scales, int n, int k, void* out,
+                               cudaStream_t s);
 
 // Context K/V of a window ingest for one draft layer: y fp32 [rows][2 n_kv
 // hd] (K heads, then V heads) of rows at positions pos0 + r; K gets the

@@ -173,14 +173,17 @@ def test_attention_forms_agree(qwen, monkeypatch, max_seq, chunks):
         assert err.max() < TOL / 4, err
 
 
-def test_dense_ingest_matches_chunked(qwen, monkeypatch):
+@pytest.mark.parametrize("int4", [False, True], ids=["bf16", "int4"])
+def test_dense_ingest_matches_chunked(qwen, monkeypatch, int4):
     """The context-window ingest on the dense tcgen05 GEMM (default for bf16
     drafters) writes the same draft K/V cache rows as the 16-row chunks
     through the round's kernels (DFLASH_DENSE_INGEST=0) up to fp16 rounding
     of the cache, and the next draft's logits agree within the parity
-    tolerance.  300 tap rows: two 128-row tiles and a ragged third."""
+    tolerance.  300 tap rows: two 128-row tiles and a ragged third.  With an
+    INT4 drafter the dense path multiplies f16 rows by the exactly
+    dequantised f16 weights."""
     from block_diffusion_speculative_gather_gb300.runtime import DFlash
-    Wd = W.with_(tgt_layers=0, tap_layers=(0, 8, 17, 26, 35)[:2], max_seq=512)
+    Wd = W.with_(tgt_layers=0, tap_layers=(0, 8, 17, 26, 35)[:2], max_seq=512, drf_int4=int4)
     n = 300
     taps = synth.tap_rows(n, Wd.n_taps * W.hidden)
     ext = taps.view(n, Wd.n_taps, W.hidden).permute(1, 0, 2).contiguous()
