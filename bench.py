@@ -48,6 +48,8 @@ def parse():
                     help="skip the drafter-alone, INT4, hc-tap and verify-sweep measurements")
     ap.add_argument("--layers", type=int, default=0,
                     help="(debug) override target layers; lines printed with it are not the workload")
+    ap.add_argument("--ncu-dense", type=int, nargs=3, metavar=("M", "N", "K"), default=None,
+                    help="profiling mode: three dense tcgen05 GEMMs of M x N x K, no JSON line")
     ap.add_argument("--ncu-rounds", type=int, default=0,
                     help="profiling mode: prefill, then N eager rounds inside the NVTX range "
                          "'dflash_rounds', no timing and no JSON line")
@@ -232,6 +234,19 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
+    if args.ncu_dense:
+        m, n, k = args.ncu_dense
+        gen = torch.Generator(device="cuda").manual_seed(9)
+        wd = (torch.randn(n, k, device="cuda", generator=gen) * 0.02).to(torch.bfloat16)
+        xd = torch.randn(m, k, device="cuda", generator=gen).to(torch.bfloat16)
+        yd = torch.empty(m, n, device="cuda")
+        errw = torch.zeros(2, dtype=torch.int32, device="cuda")
+        for _ in range(3):
+            capi.dflash_linear_dense(wd, xd, yd, errw)
+        torch.cuda.synchronize()
+        assert errw.tolist() == [0, 0]
+        print(f"ncu dense done: {m} x {n} x {k}", flush=True)
+        return
     w = E2E_BF16
     if args.layers:
         from block_diffusion_speculative_gather_gb300.configs import evenly_spaced_taps

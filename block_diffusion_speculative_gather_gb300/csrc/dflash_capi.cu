@@ -1007,7 +1007,7 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
         const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
         r = make_map_raw(&c->d_fc.x, c->ws + L.pf_x, bf, 2, K1, PF_ROWS, DT_BK, DT_BM, sw);
-        if (!r) r = make_map_raw(&c->d_fc.w[0], w->fc, bf, 2, K1, g.hidden, DT_BK, DT_BN, sw);
+        if (!r) r = make_map_raw(&c->d_fc.w[0], w->fc, bf, 2, K1, g.hidden, DT_BK, DT_WBOX, sw);
         c->d_kv.resize(g.drf_layers);
         const bool q4 = g.drf_wfmt == DFLASH_INT4G64;   // f16 operands: rows and dequantised weights
         const CUtensorMapDataType xt = q4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : bf;
@@ -1016,9 +1016,9 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
             r = make_map_raw(&m.x, c->ws + L.pf_chi, xt, 2, g.hidden, PF_ROWS, DT_BK, DT_BM, sw);
             if (!r) r = make_map_raw(&m.x_lo, c->ws + L.pf_clo, xt, 2, g.hidden, PF_ROWS, DT_BK, DT_BM, sw);
             if (!r && q4)
-                r = make_map_raw(&m.w[0], c->ws + L.pf_w, xt, 2, g.hidden, 2 * kvr, DT_BK, DT_BN, sw);
-            if (!r && !q4) r = make_map_raw(&m.w[0], c->drf[l].wk, bf, 2, g.hidden, kvr, DT_BK, DT_BN, sw);
-            if (!r && !q4) r = make_map_raw(&m.w[1], c->drf[l].wv, bf, 2, g.hidden, kvr, DT_BK, DT_BN, sw);
+                r = make_map_raw(&m.w[0], c->ws + L.pf_w, xt, 2, g.hidden, 2 * kvr, DT_BK, DT_WBOX, sw);
+            if (!r && !q4) r = make_map_raw(&m.w[0], c->drf[l].wk, bf, 2, g.hidden, kvr, DT_BK, DT_WBOX, sw);
+            if (!r && !q4) r = make_map_raw(&m.w[1], c->drf[l].wv, bf, 2, g.hidden, kvr, DT_BK, DT_WBOX, sw);
         }
         c->dense_ingest = !r;
     }
@@ -1502,7 +1502,7 @@ int dflash_linear_dense(const void* w, const void* x, const void* x_lo, int32_t 
         r = make_map_raw(&maps.x_lo, x_lo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, m, DT_BK, DT_BM,
                          CU_TENSOR_MAP_SWIZZLE_128B);
     if (!r)
-        r = make_map_raw(&maps.w[0], w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, n, DT_BK, DT_BN,
+        r = make_map_raw(&maps.w[0], w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, n, DT_BK, DT_WBOX,
                          CU_TENSOR_MAP_SWIZZLE_128B);
     if (r) return r;
     DenseArgs a{};

@@ -1,10 +1,11 @@
 // Dense many-row GEMM on tcgen05 (see gemm_tc.cuh).
 //
-// One CTA per 128 x 256 output tile, 128 threads.  Thread 0 is the TMA
+// One CTA per 128 x BN output tile (BN 256, or 128 where that balances
+// the waves over the SMs better), 128 threads.  Thread 0 is the TMA
 // producer: a ring of k-blocks (the x tile [128][64], its low plane when
 // x_split, and the w tile [256][64], bf16 or all f16, 128-byte swizzled,
-// K-major).  Thread 32 issues tcgen05.mma (M 128, N 256, K 16, f32
-// accumulators in 256 tensor-memory columns) four times per k-block (twice
+// K-major).  Thread 32 issues tcgen05.mma (M 128, N BN, K 16, f32
+// accumulators in BN tensor-memory columns) four times per k-block (twice
 // that with the low plane) and commits each stage back to the producer
 // through its "empty" mbarrier.  After the last k-block every warp reads
 // its 32 tensor-memory lanes (rows) with tcgen05.ld and stores fp32 rows;
@@ -24,19 +25,19 @@ __device__ __forceinline__ void dense_error(int* err, int site) {
     if (atomicCAS(&err[0], 0, DERR_TIMEOUT) == 0) err[1] = site;
 }
 
-template <bool SPLIT>
+template <bool SPLIT, int BN>
 struct DenseCfg {
     static constexpr uint32_t XB = DT_BM * 128;                    // x tile bytes (64 k)
-    static constexpr uint32_t WB = DT_BN * 128;                    // w tile bytes
+    static constexpr uint32_t WB = BN * 128;                       // w tile bytes
     static constexpr uint32_t STAGE = (SPLIT ? 2 : 1) * XB + WB;
-    static constexpr int STAGES = SPLIT ? 3 : 4;
+    static constexpr int STAGES = (int)((192u * 1024u) / STAGE);   // 192 KB of ring
     static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + (2 * STAGES + 1) * 8 + 16;
 };
 
-template <bool SPLIT, bool F16>
+template <bool SPLIT, bool F16, int BN>
 __global__ void __launch_bounds__(128, 1)
 gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
-    using CFG = DenseCfg<SPLIT>;
+    using CFG = DenseCfg<SPLIT, BN>;
     constexpr int STAGES = CFG::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>(
@@ -48,7 +49,7 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
     __shared__ int s_fail;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * DT_BM, n0 = blockIdx.y * DT_BN;
+    const int m0 = blockIdx.x * DT_BM, n0 = blockIdx.y * BN;
     const int nkb = a.K / DT_BK;
     const int seg = n0 >= a.n_seg0 ? 1 : 0;
     const int wrow = n0 - seg * a.n_seg0;
@@ -66,7 +67,7 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
         if (SPLIT) tma_prefetch_desc(&maps.x_lo);
         tma_prefetch_desc(&maps.w[seg]);
     }
-    if (warp == 1) tc::tmem_alloc(s_tmem, DT_BN);
+    if (warp == 1) tc::tmem_alloc(s_tmem, BN);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -85,10 +86,13 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
             mbar_arrive_expect_tx(&full[s], CFG::STAGE);
             tma_load_2d(st, &maps.x, &full[s], kb * DT_BK, m0);
             if (SPLIT) tma_load_2d(st + CFG::XB, &maps.x_lo, &full[s], kb * DT_BK, m0);
-            tma_load_2d(st + (SPLIT ? 2 : 1) * CFG::XB, &maps.w[seg], &full[s], kb * DT_BK, wrow);
+#pragma unroll
+            for (int b = 0; b < BN / DT_WBOX; ++b)
+                tma_load_2d(st + (SPLIT ? 2 : 1) * CFG::XB + b * DT_WBOX * 128, &maps.w[seg], &full[s],
+                            kb * DT_BK, wrow + b * DT_WBOX);
         }
     } else if (threadIdx.x == 32) {   // ---- MMA issuer
-        constexpr uint32_t ID = F16 ? tc::idesc_f16_f32(DT_BM, DT_BN) : tc::idesc_bf16_f32(DT_BM, DT_BN);
+        constexpr uint32_t ID = F16 ? tc::idesc_f16_f32(DT_BM, BN) : tc::idesc_bf16_f32(DT_BM, BN);
         for (int kb = 0; kb < nkb; ++kb) {
             const int s = kb % STAGES;
             if (!mbar_wait_bounded(&full[s], (uint32_t)((kb / STAGES) & 1))) {
@@ -120,7 +124,7 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
         const int row = m0 + 32 * warp + lane;
         const uint32_t trow = tm + ((uint32_t)(32 * warp) << 16);
 #pragma unroll 1
-        for (int c = 0; c < DT_BN / 32; ++c) {
+        for (int c = 0; c < BN / 32; ++c) {
             float v[32];
             tc::ld_x32(trow + 32 * c, v);
             const int col = n0 + 32 * c;
@@ -142,34 +146,53 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 1) tc::tmem_dealloc(tm, DT_BN);
+    if (warp == 1) tc::tmem_dealloc(tm, BN);
 }
 
-template <bool SPLIT, bool F16>
+template <bool SPLIT, bool F16, int BN>
 int launch_one(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
-    constexpr size_t smem = DenseCfg<SPLIT>::SMEM;
+    constexpr size_t smem = DenseCfg<SPLIT, BN>::SMEM;
     static_assert(smem <= 232448, "dense GEMM shared memory exceeds the per-block limit");
     static bool set = false;
     if (!set) {
-        const cudaError_t e = cudaFuncSetAttribute(gemm_dense_kernel<SPLIT, F16>,
+        const cudaError_t e = cudaFuncSetAttribute(gemm_dense_kernel<SPLIT, F16, BN>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return (int)e;
         set = true;
     }
-    const dim3 grid((unsigned)((a.M + DT_BM - 1) / DT_BM), (unsigned)((a.N + DT_BN - 1) / DT_BN));
-    return (int)launch_k(gemm_dense_kernel<SPLIT, F16>, grid, dim3(128), smem, s, maps, a);
+    const dim3 grid((unsigned)((a.M + DT_BM - 1) / DT_BM), (unsigned)((a.N + BN - 1) / BN));
+    return (int)launch_k(gemm_dense_kernel<SPLIT, F16, BN>, grid, dim3(128), smem, s, maps, a);
+}
+
+template <bool SPLIT, bool F16>
+int launch_bn(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
+    // one CTA per SM; a 128-column tile costs about 0.8 of a 256-column one
+    // (measured: the x tile streams once per column tile either way), so
+    // the narrow tile wins only where it saves a whole wave
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+            sms = 1;
+    }
+    const long long mt = (a.M + DT_BM - 1) / DT_BM;
+    const long long w256 = (mt * ((a.N + 255) / 256) + sms - 1) / sms;
+    const long long w128 = (mt * ((a.N + 127) / 128) + sms - 1) / sms;
+    if (w128 * 4 < w256 * 5) return launch_one<SPLIT, F16, 128>(maps, a, s);
+    return launch_one<SPLIT, F16, 256>(maps, a, s);
 }
 
 }  // namespace
 
-size_t dense_smem(bool split) { return split ? DenseCfg<true>::SMEM : DenseCfg<false>::SMEM; }
+size_t dense_smem(bool split) { return split ? DenseCfg<true, DT_BN>::SMEM : DenseCfg<false, DT_BN>::SMEM; }
 
 int launch_dense(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
     if (a.M < 1 || a.N < 1 || a.K < DT_BK || a.K % DT_BK || a.ldy < a.N || a.ldy % 4 ||
         a.n_seg0 % DT_BN)
         return (int)cudaErrorInvalidValue;
-    if (a.f16) return a.x_split ? launch_one<true, true>(maps, a, s) : launch_one<false, true>(maps, a, s);
-    return a.x_split ? launch_one<true, false>(maps, a, s) : launch_one<false, false>(maps, a, s);
+    if (a.f16) return a.x_split ? launch_bn<true, true>(maps, a, s) : launch_bn<false, true>(maps, a, s);
+    return a.x_split ? launch_bn<true, false>(maps, a, s) : launch_bn<false, false>(maps, a, s);
 }
 
 }  // namespace dfl

@@ -11,13 +11,14 @@
 namespace dfl {
 
 constexpr int DT_BM = 128;   // rows of x per CTA (tensor-memory lanes)
-constexpr int DT_BN = 256;   // output columns per CTA (tensor-memory columns)
+constexpr int DT_BN = 256;   // widest output tile (tensor-memory columns); 128 where it balances better
+constexpr int DT_WBOX = 128; // rows of one weight TMA box (a 256-column tile loads two)
 constexpr int DT_BK = 64;    // k per pipeline stage (one 128-byte swizzled row)
 
 struct DenseMaps {
     CUtensorMap x;      // [M][K] bf16, box [128 rows][64]
     CUtensorMap x_lo;   // low plane of x when x_split (same shape)
-    CUtensorMap w[2];   // [N_i][K] bf16 segments concatenated along n, box [256 rows][64]
+    CUtensorMap w[2];   // [N_i][K] segments concatenated along n, box [128 rows][64]
 };
 
 struct DenseArgs {
@@ -31,7 +32,8 @@ struct DenseArgs {
 };
 
 // Host: dynamic shared memory of the kernel (x_split or not), the launch
-// (grid ceil(M/128) x ceil(N/256), 128 threads).  Returns 0 or a cudaError_t.
+// (grid ceil(M/128) x ceil(N/BN), 128 threads; BN 256, or 128 where that
+// saves a wave of CTAs over the SMs).  Returns 0 or a cudaError_t.
 size_t dense_smem(bool split);
 int launch_dense(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s);
 
