@@ -571,6 +571,128 @@ attn_tc_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) {
     exchange_combine<HD>(f, kh, sp, S, T, group, tid, warp, lane);
 }
 
+struct PrefillMaps {
+    CUtensorMap q, kv;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(128)
+prefill_attn_kernel(const __grid_constant__ PrefillMaps maps, const PrefillAttnArgs p) {
+    constexpr int C = ATTN_KEYS, HALVES = HD / 64;
+    const AttnMmaArgs& a = p.m;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int group = a.n_q / a.n_kv, qrows = group * 16;
+    uint8_t* Qs = sm;                                   // [HALVES][qrows][128 B]
+    uint8_t* KV = Qs + HALVES * qrows * 128;            // 2 x (K, V) [HALVES][64][128 B]
+    constexpr int KVB = HALVES * C * 128;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(KV + 4 * KVB);   // [0] q, [1..2] buffers
+
+    pdl_trigger();
+    pdl_wait();
+    const int kh = blockIdx.x, z = blockIdx.y, tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int T = min(16, p.rows - 16 * z);
+    if (T <= 0) return;
+    const int pos0 = p.pos0 + 16 * z, hi = pos0 + T;
+    const int n_my = (hi - 1) / C + 1;   // chunks 0 .. (hi - 1) / 64
+
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    auto load_chunk = [&](int i) {   // chunk i into buffer i & 1
+        uint8_t* Kb = KV + (i & 1) * 2 * KVB;
+        uint8_t* Vb = Kb + KVB;
+        const int krow = ((a.layer * 2 + 0) * a.n_kv + kh) * a.cap + i * C;
+        const int vrow = ((a.layer * 2 + 1) * a.n_kv + kh) * a.cap + i * C;
+        mbar_arrive_expect_tx(&bar[1 + (i & 1)], 2 * KVB);
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h) {
+            tma_load_2d(Kb + h * C * 128, &maps.kv, &bar[1 + (i & 1)], 64 * h, krow);
+            tma_load_2d(Vb + h * C * 128, &maps.kv, &bar[1 + (i & 1)], 64 * h, vrow);
+        }
+    };
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar[0], HALVES * qrows * 128);
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h)
+            tma_load_2d(Qs + h * qrows * 128, &maps.q, &bar[0], 64 * h, (z * a.n_q + kh * group) * 16);
+        load_chunk(0);
+        if (n_my > 1) load_chunk(1);
+    }
+    bool ok = __syncthreads_and(mbar_wait_bounded(&bar[0], 0)) != 0;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    float o[HD / 8][4];
+#pragma unroll
+    for (int dt = 0; dt < HD / 8; ++dt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[dt][e] = 0.f;
+    int issued = n_my > 1 ? 2 : 1;
+    for (int i = 0; i < n_my && ok; ++i) {
+        ok = __syncthreads_and(mbar_wait_bounded(&bar[1 + (i & 1)], (uint32_t)((i >> 1) & 1))) != 0;
+        if (ok && warp < group)
+            adev::chunk_online<HD>(Qs, KV + (i & 1) * 2 * KVB, KV + (i & 1) * 2 * KVB + KVB, a, qrows, i, T,
+                                   pos0, 0, hi, warp, lane, m, l, o);
+        __syncthreads();   // buffer i & 1 is free again
+        if (ok && tid == 0 && i + 2 < n_my) {
+            load_chunk(i + 2);
+            ++issued;
+        }
+    }
+    if (!ok) {
+        if (tid == 0) {
+            set_error(a.st, DERR_TIMEOUT, 220);
+            mbar_wait_bounded(&bar[0], 0, 100000000ull);
+            for (int i = 0; i < issued; ++i)
+                mbar_wait_bounded(&bar[1 + (i & 1)], (uint32_t)((i >> 1) & 1), 100000000ull);
+        }
+        return;
+    }
+    if (warp < group) {
+        const int g = lane >> 2, cq = lane & 3, hq = kh * group + warp;
+        const size_t ld = (size_t)a.n_q * HD;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int t = g + 8 * r;
+            if (t >= T) continue;
+            const float inv = 1.f / l[r];
+            const size_t row = (size_t)(16 * z + t) * ld + (size_t)hq * HD + 2 * cq;
+#pragma unroll
+            for (int dt = 0; dt < HD / 8; ++dt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float v = o[dt][2 * r + e] * inv;
+                    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+                    reinterpret_cast<__nv_bfloat16*>(p.out_hi)[row + dt * 8 + e] = h;
+                    reinterpret_cast<__nv_bfloat16*>(p.out_lo)[row + dt * 8 + e] =
+                        __float2bfloat16_rn(v - __bfloat162float(h));
+                }
+        }
+    }
+}
+
+template <int HD>
+int launch_prefill_hd(const CUtensorMap& q_map, const CUtensorMap& kv_map, const PrefillAttnArgs& p,
+                      cudaStream_t s) {
+    const int qrows = (p.m.n_q / p.m.n_kv) * 16;
+    const size_t smem = 1024 + (size_t)(HD / 64) * (qrows + 4 * ATTN_KEYS) * 128 + 3 * 8 + 64;
+    static bool set = false;
+    if (!set) {
+        const cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel<HD>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return (int)e;
+        set = true;
+    }
+    PrefillMaps maps;
+    maps.q = q_map;
+    maps.kv = kv_map;
+    return (int)launch_k(prefill_attn_kernel<HD>, dim3((unsigned)p.m.n_kv, (unsigned)((p.rows + 15) / 16)),
+                         dim3(128), smem, s, maps, p);
+}
+
 }  // namespace
 
 int launch_attention_mma(const AttnMaps& maps, const AttnMmaArgs& a, int max_chunks,
@@ -643,6 +765,14 @@ int launch_fused_hd(const AttnMaps& maps, const AttnFusedArgs& f, cudaStream_t s
         return (int)cudaErrorInvalidValue;
     }
     return (int)launch_k(attn_fused_kernel<HD>, dim3(f.m.n_kv, f.max_splits), dim3(128), smem, s, maps, f);
+}
+
+int launch_prefill_attention(const CUtensorMap& q_map, const CUtensorMap& kv_map, const PrefillAttnArgs& p,
+                             cudaStream_t s) {
+    if (p.rows < 1) return 0;
+    if (p.m.head_dim == 128) return launch_prefill_hd<128>(q_map, kv_map, p, s);
+    if (p.m.head_dim == 64) return launch_prefill_hd<64>(q_map, kv_map, p, s);
+    return (int)cudaErrorInvalidValue;
 }
 
 int launch_attention_fused(const AttnMaps& maps, const AttnFusedArgs& f, cudaStream_t s) {

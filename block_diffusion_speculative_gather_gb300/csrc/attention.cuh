@@ -45,6 +45,21 @@ struct AttnFusedArgs {
 };
 
 int launch_attention_fused(const AttnMaps& maps, const AttnFusedArgs& f, cudaStream_t s);
+
+// Causal attention of a dense prompt prefill: rows pos0 .. pos0 + rows - 1,
+// q from q_map ([rows/16][n_q][16][hd] f16, box = one kv head's q group),
+// K/V from the target cache map; one CTA per (kv head, 16-row block) folds
+// every visible 64-key chunk with the online softmax of the round's
+// attention and writes the normalised rows as bf16 hi/lo planes
+// [rows][n_q * hd].
+struct PrefillAttnArgs {
+    AttnMmaArgs m;      // shapes, layer, cap, scale (causal, no window), state
+    int rows, pos0;
+    void* out_hi;
+    void* out_lo;
+};
+int launch_prefill_attention(const CUtensorMap& q_map, const CUtensorMap& kv_map, const PrefillAttnArgs& p,
+                             cudaStream_t s);
 // Host: CTAs of the fused attention kernel one SM holds, for head_dim hd.
 int attention_fused_per_sm(int hd, int n_q, int n_kv, int* out);
 // Host: the same for the tcgen05 form with nc (1 or 2) chunks per split,

@@ -68,7 +68,8 @@ int max_chunks(const dflash_config& c) { return cache_cap(c) / ATTN_CHUNK; }
 
 struct Layout {
     size_t state, x, hn, ssq, qrot, attn, act, taps, rcos, rsin, invf, amax, part, slots, counters,
-        acnt, amaps, barc, prog[3], ns[3], pf_x, pf_y, pf_chi, pf_clo, pf_w, total;
+        acnt, amaps, barc, prog[3], ns[3], pf_x, pf_y, pf_chi, pf_clo, pf_w, pp_x, pp_y, pp_hi, pp_lo, pp_q,
+        pp_thi, pp_tlo, total;
     int prog_n[3];
 };
 
@@ -102,6 +103,16 @@ constexpr int MAX_SMS = 256 * DFL_GEMM_CTAS_PER_SM;   // GEMM CTAs (split-K slot
 #define DFL_ATTN_MIN_SPLIT 1
 #endif
 constexpr int MAX_TILES = 8192;
+
+// Dense prompt prefill of a bf16 target (every prompt row before the last
+// 16-row chunk): the shapes the dense GEMM's tiles and segments cover.
+bool dense_ingest_ok(const dflash_config& c);
+bool dense_prefill_ok(const dflash_config& c) {
+    const int qd = c.n_q * c.head_dim, kvd = c.n_kv * c.head_dim;
+    return c.dtype == DFLASH_BF16 && c.tgt_layers > 0 && c.tgt_wfmt == DFLASH_BF16 &&
+           (c.drf_layers == 0 || dense_ingest_ok(c)) && c.hidden % 256 == 0 && qd % 256 == 0 &&
+           kvd % 256 == 0 && c.ffn % 256 == 0 && (c.head_dim == 128 || c.head_dim == 64);
+}
 
 // Window ingest on the dense tcgen05 GEMM: rows per pass, and whether the
 // configuration has it (bf16 drafter, shapes the GEMM's tiles cover).
@@ -154,6 +165,24 @@ Layout make_layout(const dflash_config& c) {
         L.pf_clo = take((size_t)PF_ROWS * c.hidden * 2);
         if (c.drf_wfmt == DFLASH_INT4G64)   // one layer's [W_k; W_v] dequantised to f16
             L.pf_w = take(kv * c.hidden * 2);
+    }
+    if (dense_prefill_ok(c)) {   // [PF_ROWS] rows of a dense target forward
+        const size_t qd = (size_t)c.n_q * c.head_dim, kvd = (size_t)c.n_kv * c.head_dim;
+        size_t ywide = qd + 2 * kvd;
+        if ((size_t)2 * c.ffn > ywide) ywide = (size_t)2 * c.ffn;
+        if ((size_t)c.hidden > ywide) ywide = c.hidden;
+        size_t xwide = c.hidden;
+        if (qd > xwide) xwide = qd;
+        if ((size_t)c.ffn > xwide) xwide = c.ffn;
+        L.pp_x = take((size_t)PF_ROWS * c.hidden * 4);
+        L.pp_y = take((size_t)PF_ROWS * ywide * 4);
+        L.pp_hi = take((size_t)PF_ROWS * xwide * 2);
+        L.pp_lo = take((size_t)PF_ROWS * xwide * 2);
+        L.pp_q = take((size_t)PF_ROWS * qd * 2);
+        if (c.drf_layers > 0) {
+            L.pp_thi = take((size_t)PF_ROWS * c.n_taps * c.hidden * 2);
+            L.pp_tlo = take((size_t)PF_ROWS * c.n_taps * c.hidden * 2);
+        }
     }
     for (int i = 0; i < 3; ++i) {
         L.prog_n[i] = program_phases(c, i);
@@ -294,6 +323,11 @@ struct dflash_ctx {
     bool dense_ingest = false;  // window ingest on the dense tcgen05 GEMM
     DenseMaps d_fc{};           // fc over the window's tap rows
     std::vector<DenseMaps> d_kv;   // per draft layer: context K/V from the context rows
+    bool dense_prefill = false;    // prompt rows before the last chunk on the dense GEMM
+    struct PrefillLayer { DenseMaps qkv, o, gu, down; };
+    std::vector<PrefillLayer> d_pp;
+    DenseMaps d_fc_pp{};           // fc over the prefill's hi/lo tap rows
+    CUtensorMap pp_qmap{};         // q rows of the prefill attention
     float* verify_logits = nullptr;
     float* draft_logits = nullptr;
     bool prefilled = false;
@@ -1022,6 +1056,44 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
         }
         c->dense_ingest = !r;
     }
+    // dense prompt prefill (DFLASH_DENSE_PREFILL=0 keeps 16-row forwards)
+    const char* dp_env = getenv("DFLASH_DENSE_PREFILL");
+    if (!r && dense_prefill_ok(g) && (g.drf_layers == 0 || c->dense_ingest) && !(dp_env && dp_env[0] == '0')) {
+        const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+        const uint64_t qd = (uint64_t)g.n_q * g.head_dim, kvd = (uint64_t)g.n_kv * g.head_dim;
+        auto xmaps = [&](DenseMaps& m, uint64_t width) {
+            int e = make_map_raw(&m.x, c->ws + L.pp_hi, bf, 2, width, PF_ROWS, DT_BK, DT_BM, sw);
+            if (!e) e = make_map_raw(&m.x_lo, c->ws + L.pp_lo, bf, 2, width, PF_ROWS, DT_BK, DT_BM, sw);
+            return e;
+        };
+        c->d_pp.resize(g.tgt_layers);
+        for (int l = 0; l < g.tgt_layers && !r; ++l) {
+            const dflash_layer& lw = c->tgt[l];
+            dflash_ctx::PrefillLayer& P = c->d_pp[l];
+            r = xmaps(P.qkv, g.hidden);
+            if (!r) r = make_map_raw(&P.qkv.w[0], lw.wq, bf, 2, g.hidden, qd, DT_BK, DT_WBOX, sw);
+            if (!r) r = make_map_raw(&P.qkv.w[1], lw.wk, bf, 2, g.hidden, kvd, DT_BK, DT_WBOX, sw);
+            if (!r) r = make_map_raw(&P.qkv.w[2], lw.wv, bf, 2, g.hidden, kvd, DT_BK, DT_WBOX, sw);
+            if (!r) r = xmaps(P.o, qd);
+            if (!r) r = make_map_raw(&P.o.w[0], lw.wo, bf, 2, qd, g.hidden, DT_BK, DT_WBOX, sw);
+            if (!r) r = xmaps(P.gu, g.hidden);
+            if (!r) r = make_map_raw(&P.gu.w[0], lw.w_gate, bf, 2, g.hidden, g.ffn, DT_BK, DT_WBOX, sw);
+            if (!r) r = make_map_raw(&P.gu.w[1], lw.w_up, bf, 2, g.hidden, g.ffn, DT_BK, DT_WBOX, sw);
+            if (!r) r = xmaps(P.down, g.ffn);
+            if (!r) r = make_map_raw(&P.down.w[0], lw.w_down, bf, 2, g.ffn, g.hidden, DT_BK, DT_WBOX, sw);
+        }
+        if (!r)
+            r = make_map_raw(&c->pp_qmap, c->ws + L.pp_q, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.head_dim,
+                             (uint64_t)PF_ROWS * g.n_q, 64, (g.n_q / g.n_kv) * DFL_MAX_ROWS, sw);
+        if (!r && g.drf_layers > 0) {
+            const uint64_t K1 = (uint64_t)g.n_taps * g.hidden;
+            r = make_map_raw(&c->d_fc_pp.x, c->ws + L.pp_thi, bf, 2, K1, PF_ROWS, DT_BK, DT_BM, sw);
+            if (!r) r = make_map_raw(&c->d_fc_pp.x_lo, c->ws + L.pp_tlo, bf, 2, K1, PF_ROWS, DT_BK, DT_BM, sw);
+            if (!r) r = make_map_raw(&c->d_fc_pp.w[0], w->fc, bf, 2, K1, g.hidden, DT_BK, DT_WBOX, sw);
+        }
+        c->dense_prefill = !r;
+    }
     if (r) {
         delete c;
         return r;
@@ -1146,10 +1218,81 @@ namespace {
 // bf16 drafters use bf16 rows and weights; INT4 drafters f16 rows and the
 // layer's W_k, W_v dequantised exactly to f16 first (the tensor core takes
 // one type for both operands).
-int run_dense_ingest(dflash_ctx* c, const void* ext_taps, int n_ext, int commit_lo, cudaStream_t s) {
+// fc over R context rows already in place (x rows m_off .. m_off + R - 1 of
+// fc's maps), then the context norm, K/V and cache rows at pos0 ...
+int ingest_rows(dflash_ctx* c, const DenseMaps& fcm, int x_split, int m_off, int R, int pos0, cudaStream_t s) {
     const dflash_config& g = c->cfg;
     const int kvr = g.n_kv * g.head_dim;
     int* err = &c->st()->err;
+    DenseArgs fa{};
+    fa.M = R;
+    fa.N = g.hidden;
+    fa.K = g.n_taps * g.hidden;
+    fa.n_seg0 = (g.hidden + DT_BN - 1) / DT_BN * DT_BN;
+    fa.n_seg1 = 1 << 30;
+    fa.m_off = m_off;
+    fa.x_split = x_split;
+    fa.y = c->buf<float>(c->L.pf_y);
+    fa.ldy = g.hidden;
+    fa.err = err;
+    LAUNCH_TRY(launch_dense(fcm, fa, s));
+    CtxRowsArgs ra{};
+    ra.y = fa.y;
+    ra.rows = R;
+    ra.hidden = g.hidden;
+    ra.w = g.ctx_norm ? c->w.ctx_norm : nullptr;
+    ra.norm = g.ctx_norm ? 1 : 0;
+    ra.eps = g.rms_eps;
+    ra.c_hi = c->ws + c->L.pf_chi;
+    ra.c_lo = c->ws + c->L.pf_clo;
+    const bool q4 = g.drf_wfmt == DFLASH_INT4G64;
+    ra.f16 = q4 ? 1 : 0;
+    LAUNCH_TRY(launch_ctx_rows(ra, s));
+    for (int l = 0; l < g.drf_layers; ++l) {
+        if (q4) {   // this layer's W_k and W_v, dequantised (exactly) to f16
+            uint8_t* wq = c->ws + c->L.pf_w;
+            LAUNCH_TRY(launch_dequant_int4g64_f16(static_cast<const uint8_t*>(c->drf[l].wk),
+                                                  static_cast<const uint16_t*>(c->drf[l].sk), kvr, g.hidden,
+                                                  wq, s));
+            LAUNCH_TRY(launch_dequant_int4g64_f16(static_cast<const uint8_t*>(c->drf[l].wv),
+                                                  static_cast<const uint16_t*>(c->drf[l].sv), kvr, g.hidden,
+                                                  wq + (size_t)kvr * g.hidden * 2, s));
+        }
+        DenseArgs ka{};
+        ka.M = R;
+        ka.N = 2 * kvr;
+        ka.K = g.hidden;
+        ka.n_seg0 = q4 ? (2 * kvr + DT_BN - 1) / DT_BN * DT_BN : kvr;
+        ka.n_seg1 = 1 << 30;
+        ka.f16 = q4 ? 1 : 0;
+        ka.x_split = 1;
+        ka.y = c->buf<float>(c->L.pf_y);
+        ka.ldy = 2 * kvr;
+        ka.err = err;
+        LAUNCH_TRY(launch_dense(c->d_kv[l], ka, s));
+        const QkvEpi q = qkv_epi(c, c->drf[l], false, l, 0, ROWS_COMMIT);
+        CtxKvArgs ca{};
+        ca.y = ka.y;
+        ca.rows = R;
+        ca.pos0 = pos0;
+        ca.n_kv = g.n_kv;
+        ca.head_dim = g.head_dim;
+        ca.cap = q.cap;
+        ca.max_seq = g.max_seq;
+        ca.k_norm = c->drf[l].k_norm;
+        ca.eps = g.rms_eps;
+        ca.inv_freq = c->buf<double>(c->L.invf);
+        ca.k_cache = q.k_cache;
+        ca.v_cache = q.v_cache;
+        ca.c_type = q.c_type;
+        ca.st = c->st();
+        LAUNCH_TRY(launch_ctx_kv_store(ca, s));
+    }
+    return DFLASH_OK;
+}
+
+int run_dense_ingest(dflash_ctx* c, const void* ext_taps, int n_ext, int commit_lo, cudaStream_t s) {
+    const dflash_config& g = c->cfg;
     for (int p0 = commit_lo; p0 < n_ext; p0 += PF_ROWS) {
         const int R = n_ext - p0 < PF_ROWS ? n_ext - p0 : PF_ROWS;
         TapArgs ta{};
@@ -1164,65 +1307,119 @@ int run_dense_ingest(dflash_ctx* c, const void* ext_taps, int n_ext, int commit_
         ta.out_type = XT_BF16;
         ta.out_row_stride = (long long)g.n_taps * g.hidden;
         LAUNCH_TRY(launch_tap_reduce(ta, s));
-        DenseArgs fa{};
-        fa.M = R;
-        fa.N = g.hidden;
-        fa.K = g.n_taps * g.hidden;
-        fa.n_seg0 = (g.hidden + DT_BN - 1) / DT_BN * DT_BN;
-        fa.y = c->buf<float>(c->L.pf_y);
-        fa.ldy = g.hidden;
-        fa.err = err;
-        LAUNCH_TRY(launch_dense(c->d_fc, fa, s));
-        CtxRowsArgs ra{};
-        ra.y = fa.y;
-        ra.rows = R;
-        ra.hidden = g.hidden;
-        ra.w = g.ctx_norm ? c->w.ctx_norm : nullptr;
-        ra.norm = g.ctx_norm ? 1 : 0;
-        ra.eps = g.rms_eps;
-        ra.c_hi = c->ws + c->L.pf_chi;
-        ra.c_lo = c->ws + c->L.pf_clo;
-        const bool q4 = g.drf_wfmt == DFLASH_INT4G64;
-        ra.f16 = q4 ? 1 : 0;
-        LAUNCH_TRY(launch_ctx_rows(ra, s));
-        for (int l = 0; l < g.drf_layers; ++l) {
-            if (q4) {   // this layer's W_k and W_v, dequantised (exactly) to f16
-                uint8_t* wq = c->ws + c->L.pf_w;
-                LAUNCH_TRY(launch_dequant_int4g64_f16(static_cast<const uint8_t*>(c->drf[l].wk),
-                                                      static_cast<const uint16_t*>(c->drf[l].sk), kvr,
-                                                      g.hidden, wq, s));
-                LAUNCH_TRY(launch_dequant_int4g64_f16(static_cast<const uint8_t*>(c->drf[l].wv),
-                                                      static_cast<const uint16_t*>(c->drf[l].sv), kvr,
-                                                      g.hidden, wq + (size_t)kvr * g.hidden * 2, s));
-            }
-            DenseArgs ka{};
-            ka.M = R;
-            ka.N = 2 * kvr;
-            ka.K = g.hidden;
-            ka.n_seg0 = q4 ? (2 * kvr + DT_BN - 1) / DT_BN * DT_BN : kvr;
-            ka.f16 = q4 ? 1 : 0;
-            ka.x_split = 1;
-            ka.y = c->buf<float>(c->L.pf_y);
-            ka.ldy = 2 * kvr;
-            ka.err = err;
-            LAUNCH_TRY(launch_dense(c->d_kv[l], ka, s));
-            const QkvEpi q = qkv_epi(c, c->drf[l], false, l, 0, ROWS_COMMIT);
-            CtxKvArgs ca{};
-            ca.y = ka.y;
-            ca.rows = R;
-            ca.pos0 = p0;
-            ca.n_kv = g.n_kv;
-            ca.head_dim = g.head_dim;
-            ca.cap = q.cap;
-            ca.max_seq = g.max_seq;
-            ca.k_norm = c->drf[l].k_norm;
-            ca.eps = g.rms_eps;
-            ca.inv_freq = c->buf<double>(c->L.invf);
-            ca.k_cache = q.k_cache;
-            ca.v_cache = q.v_cache;
-            ca.c_type = q.c_type;
-            ca.st = c->st();
-            LAUNCH_TRY(launch_ctx_kv_store(ca, s));
+        if (int r = ingest_rows(c, c->d_fc, 0, 0, R, p0, s)) return r;
+    }
+    return DFLASH_OK;
+}
+
+// Dense forward of prompt rows [0, P) of the target (P a multiple of 16,
+// the rows before the prompt's last chunk), PF_ROWS rows per pass: per
+// layer RMSNorm -> [W_q; W_k; W_v] -> q/k norms, RoPE, cache rows -> causal
+// attention -> W_o -> residual + RMSNorm -> [W_gate; W_up] -> SwiGLU ->
+// W_down -> residual; the tap layers' outputs of the committed rows then go
+// through the dense window ingest.  The prompt's last chunk runs the round's
+// 16-row forward, which also takes the LM head and sets the state.
+int run_dense_prefill(dflash_ctx* c, const int32_t* tokens, int P, int commit_lo, cudaStream_t s) {
+    const dflash_config& g = c->cfg;
+    const int qd = g.n_q * g.head_dim, kvd = g.n_kv * g.head_dim;
+    int* err = &c->st()->err;
+    float* x = c->buf<float>(c->L.pp_x);
+    float* y = c->buf<float>(c->L.pp_y);
+    void* hi = c->ws + c->L.pp_hi;
+    void* lo = c->ws + c->L.pp_lo;
+    const long long tap_ld = (long long)g.n_taps * g.hidden;
+    auto dense = [&](const DenseMaps& m, int R, int N, int K, int seg0, int seg1) {
+        DenseArgs d{};
+        d.M = R;
+        d.N = N;
+        d.K = K;
+        d.n_seg0 = seg0;
+        d.n_seg1 = seg1;
+        d.x_split = 1;
+        d.y = y;
+        d.ldy = N;
+        d.err = err;
+        return launch_dense(m, d, s);
+    };
+    for (int p0 = 0; p0 < P; p0 += PF_ROWS) {
+        const int R = P - p0 < PF_ROWS ? P - p0 : PF_ROWS;
+        LAUNCH_TRY(launch_embed_rows(tokens + p0, R, c->w.embed, g.hidden, g.vocab, x, c->st(), s));
+        for (int l = 0; l <= g.tgt_layers; ++l) {
+            // residual of layer l - 1's down projection, then layer l's input norm
+            // (after the last layer: the final norm, whose rows nothing reads)
+            ResidNormArgs rn{};
+            rn.x = x;
+            rn.y = l > 0 ? y : nullptr;
+            rn.rows = R;
+            rn.hidden = g.hidden;
+            rn.w = l < g.tgt_layers ? c->tgt[l].ln_attn : c->w.final_norm_tgt;
+            rn.eps = g.rms_eps;
+            rn.hi = hi;
+            rn.lo = lo;
+            for (int i = 0; i < g.n_taps && l > 0 && g.drf_layers > 0; ++i)
+                if (g.tap_layer[i] == l - 1) {
+                    rn.tap_hi = c->ws + c->L.pp_thi;
+                    rn.tap_lo = c->ws + c->L.pp_tlo;
+                    rn.tap_ld = tap_ld;
+                    rn.tap_col = i * g.hidden;
+                }
+            LAUNCH_TRY(launch_resid_norm(rn, s));
+            if (l == g.tgt_layers) break;
+            const dflash_ctx::PrefillLayer& PL = c->d_pp[l];
+            LAUNCH_TRY(dense(PL.qkv, R, qd + 2 * kvd, g.hidden, qd, qd + kvd));
+            const QkvEpi q = qkv_epi(c, c->tgt[l], true, l, g.n_q, ROWS_FWD);
+            QkvRowsArgs qa{};
+            qa.y = y;
+            qa.rows = R;
+            qa.pos0 = p0;
+            qa.n_q = g.n_q;
+            qa.n_kv = g.n_kv;
+            qa.head_dim = g.head_dim;
+            qa.cap = q.cap;
+            qa.max_seq = g.max_seq;
+            qa.q_norm = c->tgt[l].q_norm;
+            qa.k_norm = c->tgt[l].k_norm;
+            qa.eps = g.rms_eps;
+            qa.inv_freq = c->buf<double>(c->L.invf);
+            qa.q_out = c->ws + c->L.pp_q;
+            qa.k_cache = q.k_cache;
+            qa.v_cache = q.v_cache;
+            qa.c_type = q.c_type;
+            qa.st = c->st();
+            LAUNCH_TRY(launch_qkv_rows(qa, s));
+            PrefillAttnArgs pa{};
+            pa.m.n_q = g.n_q;
+            pa.m.n_kv = g.n_kv;
+            pa.m.head_dim = g.head_dim;
+            pa.m.layer = l;
+            pa.m.cap = cache_cap(g);
+            pa.m.causal = 1;
+            pa.m.window = 0;
+            pa.m.scale = 1.0f / sqrtf((float)g.head_dim);
+            pa.m.st = c->st();
+            pa.rows = R;
+            pa.pos0 = p0;
+            pa.out_hi = hi;
+            pa.out_lo = lo;
+            LAUNCH_TRY(launch_prefill_attention(c->pp_qmap, c->amap_t.kv, pa, s));
+            LAUNCH_TRY(dense(PL.o, R, g.hidden, qd, (g.hidden + DT_BN - 1) / DT_BN * DT_BN, 1 << 30));
+            rn = ResidNormArgs{};
+            rn.x = x;
+            rn.y = y;
+            rn.rows = R;
+            rn.hidden = g.hidden;
+            rn.w = c->tgt[l].ln_mlp;
+            rn.eps = g.rms_eps;
+            rn.hi = hi;
+            rn.lo = lo;
+            LAUNCH_TRY(launch_resid_norm(rn, s));
+            LAUNCH_TRY(dense(PL.gu, R, 2 * g.ffn, g.hidden, g.ffn, 1 << 30));
+            LAUNCH_TRY(launch_swiglu_rows(y, R, g.ffn, hi, lo, s));
+            LAUNCH_TRY(dense(PL.down, R, g.hidden, g.ffn, (g.hidden + DT_BN - 1) / DT_BN * DT_BN, 1 << 30));
+        }
+        if (g.drf_layers > 0 && p0 + R > commit_lo) {   // the committed rows of this pass
+            const int r0 = commit_lo > p0 ? commit_lo - p0 : 0;
+            if (int r = ingest_rows(c, c->d_fc_pp, 1, r0, R - r0, p0 + r0, s)) return r;
         }
     }
     return DFLASH_OK;
@@ -1245,7 +1442,12 @@ int dflash_prefill_taps(dflash_ctx* c, const int32_t* prompt_ids, int32_t n_prom
         if (!prompt_ids || n_prompt < 1) return fail(DFLASH_ERR_ARG, "prompt missing");
         if (n_prompt + 1 > g.max_seq) return fail(DFLASH_ERR_CAPACITY, "prompt of %d exceeds max_seq %d", n_prompt, g.max_seq);
         const int commit_lo = g.window > 0 ? (n_prompt > g.window ? n_prompt - g.window : 0) : 0;
-        for (int p0 = 0; p0 < n_prompt; p0 += DFL_MAX_ROWS) {
+        int p_first = 0;
+        if (c->dense_prefill && n_prompt > DFL_MAX_ROWS) {   // rows before the last chunk, dense
+            p_first = (n_prompt - 1) / DFL_MAX_ROWS * DFL_MAX_ROWS;
+            if ((r = run_dense_prefill(c, prompt_ids, p_first, commit_lo, s))) return r;
+        }
+        for (int p0 = p_first; p0 < n_prompt; p0 += DFL_MAX_ROWS) {
             const int T = n_prompt - p0 < DFL_MAX_ROWS ? n_prompt - p0 : DFL_MAX_ROWS;
             RowsArgs ra = rows_args(c, FWD_PREFILL);
             ra.pos0 = p0;
@@ -1510,6 +1712,7 @@ int dflash_linear_dense(const void* w, const void* x, const void* x_lo, int32_t 
     a.N = n;
     a.K = k;
     a.n_seg0 = (n + DT_BN - 1) / DT_BN * DT_BN;
+    a.n_seg1 = 1 << 30;
     a.x_split = x_lo ? 1 : 0;
     a.y = y;
     a.ldy = n;

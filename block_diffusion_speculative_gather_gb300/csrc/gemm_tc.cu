@@ -51,8 +51,8 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * DT_BM, n0 = blockIdx.y * BN;
     const int nkb = a.K / DT_BK;
-    const int seg = n0 >= a.n_seg0 ? 1 : 0;
-    const int wrow = n0 - seg * a.n_seg0;
+    const int seg = n0 >= a.n_seg1 ? 2 : n0 >= a.n_seg0 ? 1 : 0;
+    const int wrow = n0 - (seg == 2 ? a.n_seg1 : seg == 1 ? a.n_seg0 : 0);
 
     pdl_trigger();
     if (threadIdx.x == 0) {
@@ -84,8 +84,8 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
             }
             uint8_t* st = ring + s * CFG::STAGE;
             mbar_arrive_expect_tx(&full[s], CFG::STAGE);
-            tma_load_2d(st, &maps.x, &full[s], kb * DT_BK, m0);
-            if (SPLIT) tma_load_2d(st + CFG::XB, &maps.x_lo, &full[s], kb * DT_BK, m0);
+            tma_load_2d(st, &maps.x, &full[s], kb * DT_BK, a.m_off + m0);
+            if (SPLIT) tma_load_2d(st + CFG::XB, &maps.x_lo, &full[s], kb * DT_BK, a.m_off + m0);
 #pragma unroll
             for (int b = 0; b < BN / DT_WBOX; ++b)
                 tma_load_2d(st + (SPLIT ? 2 : 1) * CFG::XB + b * DT_WBOX * 128, &maps.w[seg], &full[s],
@@ -189,7 +189,7 @@ size_t dense_smem(bool split) { return split ? DenseCfg<true, DT_BN>::SMEM : Den
 
 int launch_dense(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
     if (a.M < 1 || a.N < 1 || a.K < DT_BK || a.K % DT_BK || a.ldy < a.N || a.ldy % 4 ||
-        a.n_seg0 % DT_BN)
+        a.n_seg0 % DT_BN || (a.n_seg1 < a.N && (a.n_seg1 % DT_BN || a.n_seg1 < a.n_seg0)) || a.m_off < 0)
         return (int)cudaErrorInvalidValue;
     if (a.f16) return a.x_split ? launch_bn<true, true>(maps, a, s) : launch_bn<false, true>(maps, a, s);
     return a.x_split ? launch_bn<true, false>(maps, a, s) : launch_bn<false, false>(maps, a, s);

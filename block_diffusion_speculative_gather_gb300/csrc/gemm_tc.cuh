@@ -18,12 +18,14 @@ constexpr int DT_BK = 64;    // k per pipeline stage (one 128-byte swizzled row)
 struct DenseMaps {
     CUtensorMap x;      // [M][K] bf16, box [128 rows][64]
     CUtensorMap x_lo;   // low plane of x when x_split (same shape)
-    CUtensorMap w[2];   // [N_i][K] segments concatenated along n, box [128 rows][64]
+    CUtensorMap w[3];   // [N_i][K] segments concatenated along n, box [128 rows][64]
 };
 
 struct DenseArgs {
     int M, N, K;        // K a multiple of 64
-    int n_seg0;         // columns of w[0] (a multiple of 256); n >= n_seg0 reads w[1]
+    int n_seg0;         // columns of w[0] (a multiple of 256); n >= n_seg0 reads w[1] ...
+    int n_seg1;         // ... up to n_seg1 (a multiple of 256, or >= N), then w[2]
+    int m_off;          // rows of x to skip: output row m reads x row m_off + m
     int x_split;        // 1: x = x (hi) + x_lo, two MMAs per k step
     int f16;            // 1: x and w are f16 (else bf16); both operands always share one type
     float* y;           // [M][ldy] fp32

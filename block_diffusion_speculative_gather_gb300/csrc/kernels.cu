@@ -256,6 +256,147 @@ __global__ void ctx_rows_kernel(CtxRowsArgs a) {
     }
 }
 
+// ---- dense prompt prefill
+
+__global__ void embed_rows_kernel(const int32_t* tokens, int rows, const __nv_bfloat16* embed, int hidden,
+                                  int vocab, float* x, DevState* st) {
+    pdl_trigger();
+    pdl_wait();
+    const int r = blockIdx.x;
+    int tok = tokens[r];
+    if (tok < 0 || tok >= vocab) {
+        if (threadIdx.x == 0) set_error(st, DERR_TOKEN, tok);
+        tok = -1;
+    }
+    for (int j = threadIdx.x; j < hidden; j += blockDim.x)
+        x[(size_t)r * hidden + j] = tok < 0 ? 0.f : __bfloat162float(embed[(size_t)tok * hidden + j]);
+}
+
+__device__ __forceinline__ void store_hilo(void* hi, void* lo, size_t i, float v) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    reinterpret_cast<__nv_bfloat16*>(hi)[i] = h;
+    reinterpret_cast<__nv_bfloat16*>(lo)[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
+// One CTA of 256 threads per row; sum of squares in a fixed order.
+__global__ void resid_norm_kernel(ResidNormArgs a) {
+    pdl_trigger();
+    pdl_wait();
+    const int r = blockIdx.x, tid = threadIdx.x;
+    float* x = a.x + (size_t)r * a.hidden;
+    __shared__ float s_part[8];
+    float ss = 0.f;
+    for (int j = tid; j < a.hidden; j += 256) {
+        float v = x[j];
+        if (a.y) {
+            v += a.y[(size_t)r * a.hidden + j];
+            x[j] = v;
+        }
+        if (a.tap_hi) store_hilo(a.tap_hi, a.tap_lo, (size_t)r * a.tap_ld + a.tap_col + j, v);
+        ss = fmaf(v, v, ss);
+    }
+    ss = warp_sum(ss);
+    if ((tid & 31) == 0) s_part[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += s_part[w];
+    const float rstd = 1.0f / sqrtf(tot / (float)a.hidden + a.eps);
+    for (int j = tid; j < a.hidden; j += 256)
+        store_hilo(a.hi, a.lo, (size_t)r * a.hidden + j, x[j] * a.w[j] * rstd);
+}
+
+// One warp per (row, head) over the q, k and v heads; lane l holds
+// elements l + 32 m (rotate-half pairs m with m + per/2 in the same lane).
+__global__ void qkv_rows_kernel(QkvRowsArgs a) {
+    pdl_trigger();
+    pdl_wait();
+    const int heads = a.n_q + 2 * a.n_kv;
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= a.rows * heads) return;
+    const int r = warp / heads, h = warp % heads;
+    const bool is_q = h < a.n_q, is_k = !is_q && h < a.n_q + a.n_kv;
+    const int hd = a.head_dim, per = hd / 32;
+    const int pos = a.pos0 + r;
+    const float* src = a.y + (size_t)r * heads * hd + (size_t)h * hd;
+    float v[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) v[m] = m < per ? src[lane + 32 * m] : 0.f;
+    if (is_q || is_k) {
+        const float* nw = is_q ? a.q_norm : a.k_norm;
+        float ss = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) ss = fmaf(v[m], v[m], ss);
+        ss = warp_sum(ss);
+        const float inv = 1.0f / sqrtf(ss / (float)hd + a.eps);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) v[m] = m < per ? v[m] * inv * nw[lane + 32 * m] : 0.f;
+        float cs[2], sn[2];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            cs[m] = 1.f;
+            sn[m] = 0.f;
+            if (m < per / 2) {
+                const double ang = (double)pos * a.inv_freq[lane + 32 * m];
+                const double k = rint(ang * 0.15915494309189535);
+                double rr = fma(-k, 6.283185307179586, ang);
+                rr = fma(-k, 2.4492935982947064e-16, rr);
+                cs[m] = (float)cos(rr);
+                sn[m] = (float)sin(rr);
+            }
+        }
+        float o[4];
+        if (per == 4) {
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                o[m] = v[m] * cs[m] - v[m + 2] * sn[m];
+                o[m + 2] = v[m + 2] * cs[m] + v[m] * sn[m];
+            }
+        } else {
+            o[0] = v[0] * cs[0] - v[1] * sn[0];
+            o[1] = v[1] * cs[0] + v[0] * sn[0];
+            o[2] = o[3] = 0.f;
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) v[m] = o[m];
+    }
+    if (is_q) {
+        __half* q = reinterpret_cast<__half*>(a.q_out) +
+                    (((size_t)(r >> 4) * a.n_q + h) * DFL_MAX_ROWS + (r & 15)) * hd;
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            if (m < per) q[lane + 32 * m] = __float2half_rn(v[m]);
+        return;
+    }
+    if (pos < 0 || pos >= a.max_seq || pos >= a.cap) {
+        if (lane == 0) set_error(a.st, DERR_INDEX, pos);
+        return;
+    }
+    const int kh = is_k ? h - a.n_q : h - a.n_q - a.n_kv;
+    void* cache = is_k ? a.k_cache : a.v_cache;
+    const size_t base = ((size_t)kh * a.cap + pos) * hd;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        if (m >= per) continue;
+        const size_t i = base + lane + 32 * m;
+        if (a.c_type == XT_F32) reinterpret_cast<float*>(cache)[i] = v[m];
+        else if (a.c_type == XT_BF16) reinterpret_cast<__nv_bfloat16*>(cache)[i] = __float2bfloat16_rn(v[m]);
+        else reinterpret_cast<__half*>(cache)[i] = __float2half_rn(v[m]);
+    }
+}
+
+__global__ void swiglu_rows_kernel(const float* y, int rows, int ffn, void* hi, void* lo) {
+    pdl_trigger();
+    pdl_wait();
+    const long long n = (long long)rows * ffn;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long r = i / ffn, j = i % ffn;
+        const float g = y[r * 2 * ffn + j], u = y[r * 2 * ffn + ffn + j];
+        store_hilo(hi, lo, (size_t)i, g / (1.f + expf(-g)) * u);
+    }
+}
+
 // One thread per 32-bit word of the packed rows (8 consecutive inputs).
 __global__ void dequant_int4g64_f16_kernel(const uint32_t* __restrict__ packed,
                                            const uint16_t* __restrict__ scales, int n, int k,
@@ -514,6 +655,31 @@ int launch_dequant_int4g64_f16(const uint8_t* packed, const uint16_t* scales, in
     return ok(launch_k(dequant_int4g64_f16_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
                        reinterpret_cast<const uint32_t*>(packed), scales, n, k,
                        reinterpret_cast<__half*>(out)));
+}
+
+int launch_embed_rows(const int32_t* tokens, int rows, const void* embed, int hidden, int vocab, float* x,
+                      DevState* st, cudaStream_t s) {
+    if (rows < 1) return 0;
+    return ok(launch_k(embed_rows_kernel, dim3((unsigned)rows), dim3(256), 0, s, tokens, rows,
+                       reinterpret_cast<const __nv_bfloat16*>(embed), hidden, vocab, x, st));
+}
+
+int launch_resid_norm(const ResidNormArgs& a, cudaStream_t s) {
+    if (a.rows < 1) return 0;
+    return ok(launch_k(resid_norm_kernel, dim3((unsigned)a.rows), dim3(256), 0, s, a));
+}
+
+int launch_qkv_rows(const QkvRowsArgs& a, cudaStream_t s) {
+    if (a.rows < 1) return 0;
+    const long long warps = (long long)a.rows * (a.n_q + 2 * a.n_kv);
+    return ok(launch_k(qkv_rows_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, a));
+}
+
+int launch_swiglu_rows(const float* y, int rows, int ffn, void* hi, void* lo, cudaStream_t s) {
+    if (rows < 1) return 0;
+    long long blocks = ((long long)rows * ffn + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    return ok(launch_k(swiglu_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, s, y, rows, ffn, hi, lo));
 }
 
 int launch_ctx_kv_store(const CtxKvArgs& a, cudaStream_t s) {

@@ -108,6 +108,55 @@ struct CtxRowsArgs {
 };
 int launch_ctx_rows(const CtxRowsArgs& a, cudaStream_t s);
 
+// ---- dense prompt prefill (many rows at once; the same formulas as the
+// round's 16-row kernels and epilogues)
+
+// x[r] = embedding row of tokens[r] (bf16 -> fp32); an id outside [0, vocab)
+// sets the error word and gives a zero row.
+int launch_embed_rows(const int32_t* tokens, int rows, const void* embed, int hidden, int vocab, float* x,
+                      DevState* st, cudaStream_t s);
+
+// x += y (y may be NULL), then RMSNorm(x) * w as bf16 hi/lo planes; with
+// tap_hi, x itself (after the add) also goes to tap_hi/tap_lo rows
+// [rows][tap_ld] at column tap_col.
+struct ResidNormArgs {
+    float* x;
+    const float* y;
+    int rows, hidden;
+    const float* w;
+    float eps;
+    void* hi;
+    void* lo;
+    void* tap_hi;
+    void* tap_lo;
+    long long tap_ld;
+    int tap_col;
+};
+int launch_resid_norm(const ResidNormArgs& a, cudaStream_t s);
+
+// q/k/v rows of a dense forward: y fp32 [rows][(n_q + 2 n_kv) hd] (q heads,
+// k heads, v heads) of rows at positions pos0 + r; q gets q-norm and RoPE
+// and goes to q_out f16 [rows/16][n_q][16][hd]; k gets k-norm and RoPE, k
+// and v go to the layer's cache rows [n_kv][cap][hd] (c_type).
+struct QkvRowsArgs {
+    const float* y;
+    int rows, pos0, n_q, n_kv, head_dim, cap, max_seq;
+    const float* q_norm;
+    const float* k_norm;
+    float eps;
+    const double* inv_freq;
+    void* q_out;
+    void* k_cache;
+    void* v_cache;
+    int c_type;
+    DevState* st;
+};
+int launch_qkv_rows(const QkvRowsArgs& a, cudaStream_t s);
+
+// h = silu(gate) * up from y fp32 [rows][2 ffn] (gate columns, then up), as
+// bf16 hi/lo planes [rows][ffn].
+int launch_swiglu_rows(const float* y, int rows, int ffn, void* hi, void* lo, cudaStream_t s);
+
 // INT4G64 weights [n][k] (packed [n][k/2], scales bf16 [k/64][n]) to f16
 // [n][k]: code * scale has at most 11 significant bits, so the f16 value is
 // exact (inside f16's normal range).

@@ -207,3 +207,46 @@ def test_dense_ingest_matches_chunked(qwen, monkeypatch, int4):
     assert ((kv_d - kv_c).abs() / scale).max().item() < 2.0 ** -9
     err = G.rel_err_rows(lg_d.cpu().numpy(), lg_c.cpu().numpy())
     assert err.max() < TOL / 4, err
+
+
+def test_dense_prefill_matches_chunked_and_oracle(qwen, monkeypatch):
+    """The dense prompt prefill of the bf16 target (default: every prompt row
+    before the last 16-row chunk through the dense tcgen05 GEMM and the
+    many-row causal attention, 1024 rows per pass) against 16-row forwards
+    (DFLASH_DENSE_PREFILL=0) on an 1100-token prompt (two passes, 1024 + 64
+    rows, then the last 12-row chunk): target and draft cache rows agree to
+    fp16 rounding, the last chunk's logits within the parity tolerance of
+    each other and of the oracle."""
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+    Wp = W.with_(max_seq=1280)
+    P = 1100
+    prompt = torch.from_numpy(synth.uniform_ids(P, W.vocab, seed=11))
+    cap = (Wp.max_seq + 63) // 64 * 64
+    out = []
+    for env in (None, "0"):
+        if env is not None:
+            monkeypatch.setenv("DFLASH_DENSE_PREFILL", env)
+        dec = DFlash(Wp, qwen["m"])
+        monkeypatch.delenv("DFLASH_DENSE_PREFILL", raising=False)
+        vl = G.logits_buf(W.vocab)
+        dec.set_logits_out(vl, None)
+        dec.prefill(prompt, 8)
+        dec.check()
+        kt = dec.kv_target.view(torch.float16).view(Wp.tgt_layers, 2, W.n_kv, cap, W.head_dim)
+        kd = dec.kv_draft.view(torch.float16).view(Wp.drf_layers, 2, W.n_kv, cap, W.head_dim)
+        out.append((kt[:, :, :, :P].float().clone(), kd[:, :, :, :P].float().clone(),
+                    vl[:P % 16 or 16].clone(), dec.stats().t_n))
+        dec.close()
+    (kt_d, kd_d, lg_d, tn_d), (kt_c, kd_c, lg_c, tn_c) = out
+    for a, b in ((kt_d, kt_c), (kd_d, kd_c)):
+        scale = b.abs().amax(dim=-1, keepdim=True).clamp_min(1e-6)
+        assert ((a - b).abs() / scale).max().item() < 2.0 ** -8
+    err = G.rel_err_rows(lg_d.cpu().numpy(), lg_c.cpu().numpy())
+    assert err.max() < TOL / 4, err
+    cache = O.KVCache(2, W.n_kv, W.head_dim)
+    ref, _ = O.target_forward(qwen["tw"], qwen["cfg"], prompt.tolist(), 0, cache)
+    last = (P - 1) // 16 * 16
+    err = G.rel_err_rows(lg_d.cpu().numpy(), ref[last:P])
+    assert err.max() < TOL, err
+    if G.decidable(ref[P - 1], TOL):
+        assert tn_d == int(np.argmax(ref[P - 1]))
