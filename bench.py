@@ -277,6 +277,17 @@ def run_ours(args):
         dec.close()
         return
 
+    # prompt prefill (dense: every row before the last 16-row chunk on the
+    # dense tcgen05 GEMM), CUDA events on the launching stream, after a warm-up
+    dec.prefill(prompt, w.n_new)
+    torch.cuda.synchronize()
+    pe0, pe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pe0.record()
+    dec.prefill(prompt, w.n_new)
+    pe1.record()
+    torch.cuda.synchronize()
+    prefill_ms = pe0.elapsed_time(pe1)
+
     # launches per round
     dec.prefill(prompt, w.n_new)
     torch.cuda.synchronize()
@@ -381,6 +392,9 @@ def run_ours(args):
         "tokens_per_round": round(emitted / rounds_total, 4),
         "verify_ms_T1": round(t1row, 4),
         "round_ms_T16": round(t_max / args.steps, 4),
+        "prefill": {"prompt_tokens": w.prompt_len, "ms": round(prefill_ms, 3),
+                    "path": "dense tcgen05 forward of rows before the last 16-row chunk"
+                            if w.prompt_len > 16 else "16-row forwards"},
         "gpu_launches": launches_per_round * args.steps,
         "attention_form": {m: {2: "tcgen05", 1: "mma.sync split-KV", 0: "partial + combine"}[
             capi.dflash_attention_form(dec.ctx, i)] for i, m in ((0, "target"), (1, "drafter"))},
@@ -592,6 +606,24 @@ def measure_workloads(steps, warmup, base_model):
     ms, gtc = _graph_time(lambda: dec.verify(dec.draft()), steps, warmup)
     del gtc
     dec.check()
+    # the same prompt prefill as 16-row forwards of the round's kernels
+    os.environ["DFLASH_DENSE_PREFILL"] = "0"
+    try:
+        dpc = DFlash(E2E_BF16, base_model)
+    finally:
+        del os.environ["DFLASH_DENSE_PREFILL"]
+    dpc.prefill(prompt, E2E_BF16.n_new)
+    torch.cuda.synchronize()
+    pe0, pe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pe0.record()
+    dpc.prefill(prompt, E2E_BF16.n_new)
+    pe1.record()
+    torch.cuda.synchronize()
+    out["e2e_bf16_prefill_16_row_forwards"] = {"prompt_tokens": E2E_BF16.prompt_len,
+                                               "ms": round(pe0.elapsed_time(pe1), 3)}
+    dpc.check()
+    dpc.close()
+    del dpc
     out["e2e_bf16_attention_tcgen05"] = {
         "rounds_s": round(1e3 / ms, 2), "ms_per_round": round(ms, 4),
         "attention_form": {1: "mma.sync split-KV", 2: "tcgen05"}.get(capi.dflash_attention_form(dec.ctx, 0)),

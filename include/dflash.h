@@ -180,15 +180,21 @@ int dflash_init(const dflash_config* cfg /*host*/, const dflash_weights* w /*hos
 
 /*
  * Starts a generation.
- * Target mode (tgt_layers > 0): prompt_ids [n_prompt] int32 run through the
- *   target in 16-row chunks; K/V fill the target cache, tap rows of the
- *   trailing context window are fc-projected into the draft context
- *   ("feat: DFlash2 ...": prefill stages the prompt's trailing window of tap
- *   rows), the argmax of the last row is the first generated token.
+ * Target mode (tgt_layers > 0): prompt_ids [n_prompt] int32 (device) run
+ *   through the target; K/V fill the target cache, tap rows of the trailing
+ *   context window are fc-projected into the draft context ("feat: DFlash2
+ *   ...": prefill stages the prompt's trailing window of tap rows), the
+ *   argmax of the last row is the first generated token.  With a bf16
+ *   target every row before the prompt's last 16-row chunk runs as a dense
+ *   forward (tcgen05 GEMMs over up to 1024 rows at a time; environment
+ *   DFLASH_DENSE_PREFILL=0 at dflash_init runs 16-row chunks instead); the
+ *   last chunk runs the round's 16-row forward.
  * Drafter-alone mode (tgt_layers == 0): ext_taps holds n_ext tap rows as
  *   dtype [n_taps][n_ext][hc*hidden] (hc streams per tap layer, reduced by
  *   their mean); rows are positions 0..n_ext-1 and first_token is the pending
- *   token at position n_ext.
+ *   token at position n_ext.  With a bf16 or INT4 drafter and hc = 1 the
+ *   window's rows are ingested on the dense tcgen05 GEMM
+ *   (DFLASH_DENSE_INGEST=0 at dflash_init: 16-row chunks).
  * max_new is the generation budget (the first token counts).  Errors:
  * ARG, CAPACITY (n_prompt or n_ext + block > max_seq), STATE.
  */
