@@ -50,6 +50,9 @@ def parse():
                     help="(debug) override target layers; lines printed with it are not the workload")
     ap.add_argument("--ncu-dense", type=int, nargs=3, metavar=("M", "N", "K"), default=None,
                     help="profiling mode: three dense tcgen05 GEMMs of M x N x K, no JSON line")
+    ap.add_argument("--ncu-prefill", action="store_true",
+                    help="profiling mode: one warm-up prefill, then one inside the NVTX range "
+                         "'dflash_prefill', no JSON line")
     ap.add_argument("--ncu-rounds", type=int, default=0,
                     help="profiling mode: prefill, then N eager rounds inside the NVTX range "
                          "'dflash_rounds', no timing and no JSON line")
@@ -263,6 +266,17 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
+    if args.ncu_prefill:
+        dec.prefill(prompt, w.n_new)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("dflash_prefill")
+        dec.prefill(prompt, w.n_new)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+        dec.check()
+        print("ncu prefill done", flush=True)
+        dec.close()
+        return
     if args.ncu_rounds:
         dec.prefill(prompt, w.n_new)
         dec.verify(dec.draft())

@@ -69,7 +69,7 @@ int max_chunks(const dflash_config& c) { return cache_cap(c) / ATTN_CHUNK; }
 struct Layout {
     size_t state, x, hn, ssq, qrot, attn, act, taps, rcos, rsin, invf, amax, part, slots, counters,
         acnt, amaps, barc, prog[3], ns[3], pf_x, pf_y, pf_chi, pf_clo, pf_w, pp_x, pp_y, pp_hi, pp_lo, pp_q,
-        pp_thi, pp_tlo, total;
+        pp_thi, pp_tlo, pf_rope, total;
     int prog_n[3];
 };
 
@@ -165,6 +165,7 @@ Layout make_layout(const dflash_config& c) {
         L.pf_clo = take((size_t)PF_ROWS * c.hidden * 2);
         if (c.drf_wfmt == DFLASH_INT4G64)   // one layer's [W_k; W_v] dequantised to f16
             L.pf_w = take(kv * c.hidden * 2);
+        L.pf_rope = take((size_t)PF_ROWS * c.head_dim * 4);   // cos, sin [PF_ROWS][head_dim / 2]
     }
     if (dense_prefill_ok(c)) {   // [PF_ROWS] rows of a dense target forward
         const size_t qd = (size_t)c.n_q * c.head_dim, kvd = (size_t)c.n_kv * c.head_dim;
@@ -179,6 +180,7 @@ Layout make_layout(const dflash_config& c) {
         L.pp_hi = take((size_t)PF_ROWS * xwide * 2);
         L.pp_lo = take((size_t)PF_ROWS * xwide * 2);
         L.pp_q = take((size_t)PF_ROWS * qd * 2);
+        if (!L.pf_rope) L.pf_rope = take((size_t)PF_ROWS * c.head_dim * 4);
         if (c.drf_layers > 0) {
             L.pp_thi = take((size_t)PF_ROWS * c.n_taps * c.hidden * 2);
             L.pp_tlo = take((size_t)PF_ROWS * c.n_taps * c.hidden * 2);
@@ -1248,6 +1250,9 @@ int ingest_rows(dflash_ctx* c, const DenseMaps& fcm, int x_split, int m_off, int
     const bool q4 = g.drf_wfmt == DFLASH_INT4G64;
     ra.f16 = q4 ? 1 : 0;
     LAUNCH_TRY(launch_ctx_rows(ra, s));
+    float* rcos = c->buf<float>(c->L.pf_rope);
+    float* rsin = rcos + (size_t)PF_ROWS * (g.head_dim / 2);
+    LAUNCH_TRY(launch_rope_rows(pos0, R, g.head_dim / 2, c->buf<double>(c->L.invf), rcos, rsin, s));
     for (int l = 0; l < g.drf_layers; ++l) {
         if (q4) {   // this layer's W_k and W_v, dequantised (exactly) to f16
             uint8_t* wq = c->ws + c->L.pf_w;
@@ -1282,6 +1287,8 @@ int ingest_rows(dflash_ctx* c, const DenseMaps& fcm, int x_split, int m_off, int
         ca.k_norm = c->drf[l].k_norm;
         ca.eps = g.rms_eps;
         ca.inv_freq = c->buf<double>(c->L.invf);
+        ca.rope_cos = rcos;
+        ca.rope_sin = rsin;
         ca.k_cache = q.k_cache;
         ca.v_cache = q.v_cache;
         ca.c_type = q.c_type;
@@ -1344,6 +1351,9 @@ int run_dense_prefill(dflash_ctx* c, const int32_t* tokens, int P, int commit_lo
     for (int p0 = 0; p0 < P; p0 += PF_ROWS) {
         const int R = P - p0 < PF_ROWS ? P - p0 : PF_ROWS;
         LAUNCH_TRY(launch_embed_rows(tokens + p0, R, c->w.embed, g.hidden, g.vocab, x, c->st(), s));
+        float* rcos = c->buf<float>(c->L.pf_rope);
+        float* rsin = rcos + (size_t)PF_ROWS * (g.head_dim / 2);
+        LAUNCH_TRY(launch_rope_rows(p0, R, g.head_dim / 2, c->buf<double>(c->L.invf), rcos, rsin, s));
         for (int l = 0; l <= g.tgt_layers; ++l) {
             // residual of layer l - 1's down projection, then layer l's input norm
             // (after the last layer: the final norm, whose rows nothing reads)
@@ -1381,6 +1391,8 @@ int run_dense_prefill(dflash_ctx* c, const int32_t* tokens, int P, int commit_lo
             qa.k_norm = c->tgt[l].k_norm;
             qa.eps = g.rms_eps;
             qa.inv_freq = c->buf<double>(c->L.invf);
+            qa.rope_cos = rcos;
+            qa.rope_sin = rsin;
             qa.q_out = c->ws + c->L.pp_q;
             qa.k_cache = q.k_cache;
             qa.v_cache = q.v_cache;

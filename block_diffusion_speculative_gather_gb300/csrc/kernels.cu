@@ -337,12 +337,17 @@ __global__ void qkv_rows_kernel(QkvRowsArgs a) {
             cs[m] = 1.f;
             sn[m] = 0.f;
             if (m < per / 2) {
-                const double ang = (double)pos * a.inv_freq[lane + 32 * m];
-                const double k = rint(ang * 0.15915494309189535);
-                double rr = fma(-k, 6.283185307179586, ang);
-                rr = fma(-k, 2.4492935982947064e-16, rr);
-                cs[m] = (float)cos(rr);
-                sn[m] = (float)sin(rr);
+                if (a.rope_cos) {
+                    cs[m] = a.rope_cos[(size_t)r * (hd / 2) + lane + 32 * m];
+                    sn[m] = a.rope_sin[(size_t)r * (hd / 2) + lane + 32 * m];
+                } else {
+                    const double ang = (double)pos * a.inv_freq[lane + 32 * m];
+                    const double k = rint(ang * 0.15915494309189535);
+                    double rr = fma(-k, 6.283185307179586, ang);
+                    rr = fma(-k, 2.4492935982947064e-16, rr);
+                    cs[m] = (float)cos(rr);
+                    sn[m] = (float)sin(rr);
+                }
             }
         }
         float o[4];
@@ -382,6 +387,23 @@ __global__ void qkv_rows_kernel(QkvRowsArgs a) {
         if (a.c_type == XT_F32) reinterpret_cast<float*>(cache)[i] = v[m];
         else if (a.c_type == XT_BF16) reinterpret_cast<__nv_bfloat16*>(cache)[i] = __float2bfloat16_rn(v[m]);
         else reinterpret_cast<__half*>(cache)[i] = __float2half_rn(v[m]);
+    }
+}
+
+__global__ void rope_rows_kernel(int pos0, int rows, int half, const double* inv_freq, float* cs,
+                                 float* sn) {
+    pdl_trigger();
+    pdl_wait();
+    const long long n = (long long)rows * half;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int r = (int)(e / half), i = (int)(e % half);
+        const double ang = (double)(pos0 + r) * inv_freq[i];
+        const double k = rint(ang * 0.15915494309189535);
+        double rr = fma(-k, 6.283185307179586, ang);
+        rr = fma(-k, 2.4492935982947064e-16, rr);
+        cs[e] = (float)cos(rr);
+        sn[e] = (float)sin(rr);
     }
 }
 
@@ -454,12 +476,17 @@ __global__ void ctx_kv_store_kernel(CtxKvArgs a) {
             cs[m] = 1.f;
             sn[m] = 0.f;
             if (m < per / 2) {
-                const double ang = (double)pos * a.inv_freq[lane + 32 * m];
-                const double k = rint(ang * 0.15915494309189535);
-                double rr = fma(-k, 6.283185307179586, ang);
-                rr = fma(-k, 2.4492935982947064e-16, rr);
-                cs[m] = (float)cos(rr);
-                sn[m] = (float)sin(rr);
+                if (a.rope_cos) {
+                    cs[m] = a.rope_cos[(size_t)r * (hd / 2) + lane + 32 * m];
+                    sn[m] = a.rope_sin[(size_t)r * (hd / 2) + lane + 32 * m];
+                } else {
+                    const double ang = (double)pos * a.inv_freq[lane + 32 * m];
+                    const double k = rint(ang * 0.15915494309189535);
+                    double rr = fma(-k, 6.283185307179586, ang);
+                    rr = fma(-k, 2.4492935982947064e-16, rr);
+                    cs[m] = (float)cos(rr);
+                    sn[m] = (float)sin(rr);
+                }
             }
         }
         float o[4];
@@ -673,6 +700,15 @@ int launch_qkv_rows(const QkvRowsArgs& a, cudaStream_t s) {
     if (a.rows < 1) return 0;
     const long long warps = (long long)a.rows * (a.n_q + 2 * a.n_kv);
     return ok(launch_k(qkv_rows_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, a));
+}
+
+int launch_rope_rows(int pos0, int rows, int half, const double* inv_freq, float* cos_out, float* sin_out,
+                     cudaStream_t s) {
+    if (rows < 1) return 0;
+    long long blocks = ((long long)rows * half + 255) / 256;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    return ok(launch_k(rope_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, s, pos0, rows, half, inv_freq,
+                       cos_out, sin_out));
 }
 
 int launch_swiglu_rows(const float* y, int rows, int ffn, void* hi, void* lo, cudaStream_t s) {

@@ -145,6 +145,8 @@ struct QkvRowsArgs {
     const float* k_norm;
     float eps;
     const double* inv_freq;
+    const float* rope_cos;  // [rows][head_dim / 2] table, or NULL: from inv_freq
+    const float* rope_sin;
     void* q_out;
     void* k_cache;
     void* v_cache;
@@ -156,6 +158,12 @@ int launch_qkv_rows(const QkvRowsArgs& a, cudaStream_t s);
 // h = silu(gate) * up from y fp32 [rows][2 ffn] (gate columns, then up), as
 // bf16 hi/lo planes [rows][ffn].
 int launch_swiglu_rows(const float* y, int rows, int ffn, void* hi, void* lo, cudaStream_t s);
+
+// RoPE table of positions pos0 .. pos0 + rows - 1: cos and sin [rows][half]
+// of pos * inv_freq[i] (angle reduced and evaluated in double, rounded once
+// to fp32: the round's table), for the many-row kernels above.
+int launch_rope_rows(int pos0, int rows, int half, const double* inv_freq, float* cos_out, float* sin_out,
+                     cudaStream_t s);
 
 // INT4G64 weights [n][k] (packed [n][k/2], scales bf16 [k/64][n]) to f16
 // [n][k]: code * scale has at most 11 significant bits, so the f16 value is
@@ -173,6 +181,8 @@ struct CtxKvArgs {
     const float* k_norm;    // [head_dim]
     float eps;
     const double* inv_freq; // [head_dim / 2]
+    const float* rope_cos;  // [rows][head_dim / 2] table (launch_rope_rows), or NULL: from inv_freq
+    const float* rope_sin;
     void* k_cache;
     void* v_cache;
     int c_type;

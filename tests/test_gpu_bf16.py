@@ -250,3 +250,29 @@ def test_dense_prefill_matches_chunked_and_oracle(qwen, monkeypatch):
     assert err.max() < TOL, err
     if G.decidable(ref[P - 1], TOL):
         assert tn_d == int(np.argmax(ref[P - 1]))
+
+
+@pytest.mark.parametrize("P", [17, 1040], ids=["one-block", "one-full-pass"])
+def test_dense_prefill_edges(qwen, monkeypatch, P):
+    """Dense prefill at its edges: 17 tokens (one 16-row dense block before a
+    1-row last chunk) and 1040 (exactly one full 1024-row pass): the last
+    chunk's logits and the first token match the 16-row forwards."""
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+    Wp = W.with_(max_seq=1280)
+    prompt = torch.from_numpy(synth.uniform_ids(P, W.vocab, seed=13))
+    out = []
+    for env in (None, "0"):
+        if env is not None:
+            monkeypatch.setenv("DFLASH_DENSE_PREFILL", env)
+        dec = DFlash(Wp, qwen["m"])
+        monkeypatch.delenv("DFLASH_DENSE_PREFILL", raising=False)
+        vl = G.logits_buf(W.vocab)
+        dec.set_logits_out(vl, None)
+        dec.prefill(prompt, 8)
+        dec.check()
+        out.append((vl[:P % 16 or 16].clone(), dec.stats().t_n))
+        dec.close()
+    err = G.rel_err_rows(out[0][0].cpu().numpy(), out[1][0].cpu().numpy())
+    assert err.max() < TOL / 4, err
+    if G.decidable(out[1][0][-1].double().cpu().numpy(), TOL):
+        assert out[0][1] == out[1][1]
