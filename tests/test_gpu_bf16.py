@@ -276,3 +276,40 @@ def test_dense_prefill_edges(qwen, monkeypatch, P):
     assert err.max() < TOL / 4, err
     if G.decidable(out[1][0][-1].double().cpu().numpy(), TOL):
         assert out[0][1] == out[1][1]
+
+
+@pytest.mark.parametrize("int4", [False, True], ids=["bf16-drafter", "int4-drafter"])
+def test_dense_prefill_window_commit(qwen, monkeypatch, int4):
+    """Dense prefill with a drafter window of 64 positions on a 300-token
+    prompt: only rows 236..299 enter the draft context — rows 236..287 from
+    the middle of the dense pass (the fc reads the tap rows from row 236 on),
+    288..299 from the last 16-row chunk.  Draft cache rows match the 16-row
+    forwards to fp16 rounding, rows before the window stay untouched, and
+    the first draft after the prefill gives the same logits."""
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+    Wp = W.with_(max_seq=512, window=64, drf_int4=int4)
+    P, lo = 300, 300 - 64
+    prompt = torch.from_numpy(synth.uniform_ids(P, W.vocab, seed=17))
+    cap = (Wp.max_seq + 63) // 64 * 64
+    out = []
+    for env in (None, "0"):
+        if env is not None:
+            monkeypatch.setenv("DFLASH_DENSE_PREFILL", env)
+        dec = DFlash(Wp, qwen["m"])
+        monkeypatch.delenv("DFLASH_DENSE_PREFILL", raising=False)
+        dl = G.logits_buf(W.vocab)
+        dec.set_logits_out(None, dl)
+        dec.prefill(prompt, 64)        # a budget that leaves the first block its 16 rows
+        dec.draft()
+        dec.check()
+        kd = dec.kv_draft.view(torch.float16).view(Wp.drf_layers, 2, W.n_kv, cap, W.head_dim)
+        out.append((kd[:, :, :, :P].float().clone(), dl[1:W.block].clone()))
+        dec.close()
+    (kd_d, dl_d), (kd_c, dl_c) = out
+    assert kd_d[:, :, :, :lo].abs().max().item() == 0.0
+    assert kd_c[:, :, :, :lo].abs().max().item() == 0.0
+    a, b = kd_d[:, :, :, lo:], kd_c[:, :, :, lo:]
+    scale = b.abs().amax(dim=-1, keepdim=True).clamp_min(1e-6)
+    assert ((a - b).abs() / scale).max().item() < 2.0 ** -8
+    err = G.rel_err_rows(dl_d.cpu().numpy(), dl_c.cpu().numpy())
+    assert err.max() < TOL / 4, err
