@@ -20,7 +20,7 @@ Sources (three pull-request pages on one subject):
   * "dflash: the chain verify builds pipelined and defers the qwen4 PLE
     gather" -- mlx-serve PR #937 (first commit message: hcStreamMean).
 
-Readings where the pages are silent (each is also listed in the design doc):
+Readings where the pages are silent:
   * decoder layer = Qwen3: pre-norm RMSNorm (eps 1e-6), per-head q/k RMSNorm
     before rotate-half RoPE (theta 1e6), GQA, SwiGLU MLP, no biases, final
     RMSNorm, LM head tied to the embedding;
