@@ -665,10 +665,16 @@ prefill_attn_kernel(const __grid_constant__ PrefillMaps maps, const PrefillAttnA
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const float v = o[dt][2 * r + e] * inv;
-                    const __nv_bfloat16 h = __float2bfloat16_rn(v);
-                    reinterpret_cast<__nv_bfloat16*>(p.out_hi)[row + dt * 8 + e] = h;
-                    reinterpret_cast<__nv_bfloat16*>(p.out_lo)[row + dt * 8 + e] =
-                        __float2bfloat16_rn(v - __bfloat162float(h));
+                    if (p.f16) {
+                        const __half h = __float2half_rn(v);
+                        reinterpret_cast<__half*>(p.out_hi)[row + dt * 8 + e] = h;
+                        reinterpret_cast<__half*>(p.out_lo)[row + dt * 8 + e] = __float2half_rn(v - __half2float(h));
+                    } else {
+                        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+                        reinterpret_cast<__nv_bfloat16*>(p.out_hi)[row + dt * 8 + e] = h;
+                        reinterpret_cast<__nv_bfloat16*>(p.out_lo)[row + dt * 8 + e] =
+                            __float2bfloat16_rn(v - __bfloat162float(h));
+                    }
                 }
         }
     }

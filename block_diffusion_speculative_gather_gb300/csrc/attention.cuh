@@ -57,6 +57,7 @@ struct PrefillAttnArgs {
     int rows, pos0;
     void* out_hi;
     void* out_lo;
+    int f16;            // 1: f16 planes (else bf16)
 };
 int launch_prefill_attention(const CUtensorMap& q_map, const CUtensorMap& kv_map, const PrefillAttnArgs& p,
                              cudaStream_t s);

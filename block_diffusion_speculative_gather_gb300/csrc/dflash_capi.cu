@@ -69,7 +69,7 @@ int max_chunks(const dflash_config& c) { return cache_cap(c) / ATTN_CHUNK; }
 struct Layout {
     size_t state, x, hn, ssq, qrot, attn, act, taps, rcos, rsin, invf, amax, part, slots, counters,
         acnt, amaps, barc, prog[3], ns[3], pf_x, pf_y, pf_chi, pf_clo, pf_w, pp_x, pp_y, pp_hi, pp_lo, pp_q,
-        pp_thi, pp_tlo, pf_rope, total;
+        pp_thi, pp_tlo, pf_rope, pp_w, total;
     int prog_n[3];
 };
 
@@ -109,7 +109,8 @@ constexpr int MAX_TILES = 8192;
 bool dense_ingest_ok(const dflash_config& c);
 bool dense_prefill_ok(const dflash_config& c) {
     const int qd = c.n_q * c.head_dim, kvd = c.n_kv * c.head_dim;
-    return c.dtype == DFLASH_BF16 && c.tgt_layers > 0 && c.tgt_wfmt == DFLASH_BF16 &&
+    return c.dtype == DFLASH_BF16 && c.tgt_layers > 0 &&
+           (c.tgt_wfmt == DFLASH_BF16 || c.tgt_wfmt == DFLASH_INT4G64) &&
            (c.drf_layers == 0 || dense_ingest_ok(c)) && c.hidden % 256 == 0 && qd % 256 == 0 &&
            kvd % 256 == 0 && c.ffn % 256 == 0 && (c.head_dim == 128 || c.head_dim == 64);
 }
@@ -181,6 +182,11 @@ Layout make_layout(const dflash_config& c) {
         L.pp_lo = take((size_t)PF_ROWS * xwide * 2);
         L.pp_q = take((size_t)PF_ROWS * qd * 2);
         if (!L.pf_rope) L.pf_rope = take((size_t)PF_ROWS * c.head_dim * 4);
+        if (c.tgt_wfmt == DFLASH_INT4G64) {   // the largest of a layer's matrices, dequantised to f16
+            size_t wmax = (qd + 2 * kvd) * c.hidden;
+            if ((size_t)2 * c.ffn * c.hidden > wmax) wmax = (size_t)2 * c.ffn * c.hidden;
+            L.pp_w = take(wmax * 2);
+        }
         if (c.drf_layers > 0) {
             L.pp_thi = take((size_t)PF_ROWS * c.n_taps * c.hidden * 2);
             L.pp_tlo = take((size_t)PF_ROWS * c.n_taps * c.hidden * 2);
@@ -1064,13 +1070,27 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
         const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
         const uint64_t qd = (uint64_t)g.n_q * g.head_dim, kvd = (uint64_t)g.n_kv * g.head_dim;
+        const bool q4 = g.tgt_wfmt == DFLASH_INT4G64;   // f16 rows times exactly dequantised f16 weights
+        const CUtensorMapDataType xt = q4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : bf;
         auto xmaps = [&](DenseMaps& m, uint64_t width) {
-            int e = make_map_raw(&m.x, c->ws + L.pp_hi, bf, 2, width, PF_ROWS, DT_BK, DT_BM, sw);
-            if (!e) e = make_map_raw(&m.x_lo, c->ws + L.pp_lo, bf, 2, width, PF_ROWS, DT_BK, DT_BM, sw);
+            int e = make_map_raw(&m.x, c->ws + L.pp_hi, xt, 2, width, PF_ROWS, DT_BK, DT_BM, sw);
+            if (!e) e = make_map_raw(&m.x_lo, c->ws + L.pp_lo, xt, 2, width, PF_ROWS, DT_BK, DT_BM, sw);
             return e;
         };
         c->d_pp.resize(g.tgt_layers);
-        for (int l = 0; l < g.tgt_layers && !r; ++l) {
+        for (int l = 0; l < g.tgt_layers && !r && q4; ++l) {   // every layer's GEMMs read the scratch
+            dflash_ctx::PrefillLayer& P = c->d_pp[l];
+            uint8_t* pw = c->ws + L.pp_w;
+            r = xmaps(P.qkv, g.hidden);
+            if (!r) r = make_map_raw(&P.qkv.w[0], pw, xt, 2, g.hidden, qd + 2 * kvd, DT_BK, DT_WBOX, sw);
+            if (!r) r = xmaps(P.o, qd);
+            if (!r) r = make_map_raw(&P.o.w[0], pw, xt, 2, qd, g.hidden, DT_BK, DT_WBOX, sw);
+            if (!r) r = xmaps(P.gu, g.hidden);
+            if (!r) r = make_map_raw(&P.gu.w[0], pw, xt, 2, g.hidden, 2 * (uint64_t)g.ffn, DT_BK, DT_WBOX, sw);
+            if (!r) r = xmaps(P.down, g.ffn);
+            if (!r) r = make_map_raw(&P.down.w[0], pw, xt, 2, g.ffn, g.hidden, DT_BK, DT_WBOX, sw);
+        }
+        for (int l = 0; l < g.tgt_layers && !r && !q4; ++l) {
             const dflash_layer& lw = c->tgt[l];
             dflash_ctx::PrefillLayer& P = c->d_pp[l];
             r = xmaps(P.qkv, g.hidden);
@@ -1335,13 +1355,21 @@ int run_dense_prefill(dflash_ctx* c, const int32_t* tokens, int P, int commit_lo
     void* hi = c->ws + c->L.pp_hi;
     void* lo = c->ws + c->L.pp_lo;
     const long long tap_ld = (long long)g.n_taps * g.hidden;
+    const bool q4 = g.tgt_wfmt == DFLASH_INT4G64;
+    uint8_t* pw = c->ws + c->L.pp_w;
+    auto deq = [&](const void* packed, const void* scales, int n, int k, size_t row_off) {
+        return launch_dequant_int4g64_f16(static_cast<const uint8_t*>(packed),
+                                          static_cast<const uint16_t*>(scales), n, k,
+                                          pw + row_off * k * 2, s);
+    };
     auto dense = [&](const DenseMaps& m, int R, int N, int K, int seg0, int seg1) {
         DenseArgs d{};
         d.M = R;
         d.N = N;
         d.K = K;
-        d.n_seg0 = seg0;
-        d.n_seg1 = seg1;
+        d.n_seg0 = q4 ? 1 << 30 : seg0;   // INT4: one dequantised matrix
+        d.n_seg1 = q4 ? 1 << 30 : seg1;
+        d.f16 = q4 ? 1 : 0;
         d.x_split = 1;
         d.y = y;
         d.ldy = N;
@@ -1366,6 +1394,7 @@ int run_dense_prefill(dflash_ctx* c, const int32_t* tokens, int P, int commit_lo
             rn.eps = g.rms_eps;
             rn.hi = hi;
             rn.lo = lo;
+            rn.f16 = q4 ? 1 : 0;
             for (int i = 0; i < g.n_taps && l > 0 && g.drf_layers > 0; ++i)
                 if (g.tap_layer[i] == l - 1) {
                     rn.tap_hi = c->ws + c->L.pp_thi;
@@ -1376,6 +1405,12 @@ int run_dense_prefill(dflash_ctx* c, const int32_t* tokens, int P, int commit_lo
             LAUNCH_TRY(launch_resid_norm(rn, s));
             if (l == g.tgt_layers) break;
             const dflash_ctx::PrefillLayer& PL = c->d_pp[l];
+            const dflash_layer& lw = c->tgt[l];
+            if (q4) {
+                LAUNCH_TRY(deq(lw.wq, lw.sq, qd, g.hidden, 0));
+                LAUNCH_TRY(deq(lw.wk, lw.sk, kvd, g.hidden, qd));
+                LAUNCH_TRY(deq(lw.wv, lw.sv, kvd, g.hidden, qd + kvd));
+            }
             LAUNCH_TRY(dense(PL.qkv, R, qd + 2 * kvd, g.hidden, qd, qd + kvd));
             const QkvEpi q = qkv_epi(c, c->tgt[l], true, l, g.n_q, ROWS_FWD);
             QkvRowsArgs qa{};
@@ -1413,7 +1448,9 @@ int run_dense_prefill(dflash_ctx* c, const int32_t* tokens, int P, int commit_lo
             pa.pos0 = p0;
             pa.out_hi = hi;
             pa.out_lo = lo;
+            pa.f16 = q4 ? 1 : 0;
             LAUNCH_TRY(launch_prefill_attention(c->pp_qmap, c->amap_t.kv, pa, s));
+            if (q4) LAUNCH_TRY(deq(lw.wo, lw.so, g.hidden, qd, 0));
             LAUNCH_TRY(dense(PL.o, R, g.hidden, qd, (g.hidden + DT_BN - 1) / DT_BN * DT_BN, 1 << 30));
             rn = ResidNormArgs{};
             rn.x = x;
@@ -1424,9 +1461,15 @@ int run_dense_prefill(dflash_ctx* c, const int32_t* tokens, int P, int commit_lo
             rn.eps = g.rms_eps;
             rn.hi = hi;
             rn.lo = lo;
+            rn.f16 = q4 ? 1 : 0;
             LAUNCH_TRY(launch_resid_norm(rn, s));
+            if (q4) {
+                LAUNCH_TRY(deq(lw.w_gate, lw.s_gate, g.ffn, g.hidden, 0));
+                LAUNCH_TRY(deq(lw.w_up, lw.s_up, g.ffn, g.hidden, g.ffn));
+            }
             LAUNCH_TRY(dense(PL.gu, R, 2 * g.ffn, g.hidden, g.ffn, 1 << 30));
-            LAUNCH_TRY(launch_swiglu_rows(y, R, g.ffn, hi, lo, s));
+            LAUNCH_TRY(launch_swiglu_rows(y, R, g.ffn, hi, lo, q4 ? 1 : 0, s));
+            if (q4) LAUNCH_TRY(deq(lw.w_down, lw.s_down, g.hidden, g.ffn, 0));
             LAUNCH_TRY(dense(PL.down, R, g.hidden, g.ffn, (g.hidden + DT_BN - 1) / DT_BN * DT_BN, 1 << 30));
         }
         if (g.drf_layers > 0 && p0 + R > commit_lo) {   // the committed rows of this pass

@@ -272,7 +272,13 @@ __global__ void embed_rows_kernel(const int32_t* tokens, int rows, const __nv_bf
         x[(size_t)r * hidden + j] = tok < 0 ? 0.f : __bfloat162float(embed[(size_t)tok * hidden + j]);
 }
 
-__device__ __forceinline__ void store_hilo(void* hi, void* lo, size_t i, float v) {
+__device__ __forceinline__ void store_hilo(void* hi, void* lo, size_t i, float v, int f16 = 0) {
+    if (f16) {
+        const __half h = __float2half_rn(v);
+        reinterpret_cast<__half*>(hi)[i] = h;
+        reinterpret_cast<__half*>(lo)[i] = __float2half_rn(v - __half2float(h));
+        return;
+    }
     const __nv_bfloat16 h = __float2bfloat16_rn(v);
     reinterpret_cast<__nv_bfloat16*>(hi)[i] = h;
     reinterpret_cast<__nv_bfloat16*>(lo)[i] = __float2bfloat16_rn(v - __bfloat162float(h));
@@ -303,7 +309,7 @@ __global__ void resid_norm_kernel(ResidNormArgs a) {
     for (int w = 0; w < 8; ++w) tot += s_part[w];
     const float rstd = 1.0f / sqrtf(tot / (float)a.hidden + a.eps);
     for (int j = tid; j < a.hidden; j += 256)
-        store_hilo(a.hi, a.lo, (size_t)r * a.hidden + j, x[j] * a.w[j] * rstd);
+        store_hilo(a.hi, a.lo, (size_t)r * a.hidden + j, x[j] * a.w[j] * rstd, a.f16);
 }
 
 // One warp per (row, head) over the q, k and v heads; lane l holds
@@ -407,7 +413,7 @@ __global__ void rope_rows_kernel(int pos0, int rows, int half, const double* inv
     }
 }
 
-__global__ void swiglu_rows_kernel(const float* y, int rows, int ffn, void* hi, void* lo) {
+__global__ void swiglu_rows_kernel(const float* y, int rows, int ffn, void* hi, void* lo, int f16) {
     pdl_trigger();
     pdl_wait();
     const long long n = (long long)rows * ffn;
@@ -415,7 +421,7 @@ __global__ void swiglu_rows_kernel(const float* y, int rows, int ffn, void* hi, 
          i += (long long)gridDim.x * blockDim.x) {
         const long long r = i / ffn, j = i % ffn;
         const float g = y[r * 2 * ffn + j], u = y[r * 2 * ffn + ffn + j];
-        store_hilo(hi, lo, (size_t)i, g / (1.f + expf(-g)) * u);
+        store_hilo(hi, lo, (size_t)i, g / (1.f + expf(-g)) * u, f16);
     }
 }
 
@@ -711,11 +717,12 @@ int launch_rope_rows(int pos0, int rows, int half, const double* inv_freq, float
                        cos_out, sin_out));
 }
 
-int launch_swiglu_rows(const float* y, int rows, int ffn, void* hi, void* lo, cudaStream_t s) {
+int launch_swiglu_rows(const float* y, int rows, int ffn, void* hi, void* lo, int f16, cudaStream_t s) {
     if (rows < 1) return 0;
     long long blocks = ((long long)rows * ffn + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
-    return ok(launch_k(swiglu_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, s, y, rows, ffn, hi, lo));
+    return ok(launch_k(swiglu_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, s, y, rows, ffn, hi, lo,
+                       f16));
 }
 
 int launch_ctx_kv_store(const CtxKvArgs& a, cudaStream_t s) {

@@ -184,9 +184,10 @@ int dflash_init(const dflash_config* cfg /*host*/, const dflash_weights* w /*hos
  *   through the target; K/V fill the target cache, tap rows of the trailing
  *   context window are fc-projected into the draft context ("feat: DFlash2
  *   ...": prefill stages the prompt's trailing window of tap rows), the
- *   argmax of the last row is the first generated token.  With a bf16
- *   target every row before the prompt's last 16-row chunk runs as a dense
- *   forward (tcgen05 GEMMs over up to 1024 rows at a time; environment
+ *   argmax of the last row is the first generated token.  With a bf16 or
+ *   INT4 target every row before the prompt's last 16-row chunk runs as a
+ *   dense forward (tcgen05 GEMMs over up to 1024 rows at a time; INT4
+ *   matrices dequantised exactly to f16 layer by layer; environment
  *   DFLASH_DENSE_PREFILL=0 at dflash_init runs 16-row chunks instead); the
  *   last chunk runs the round's 16-row forward.
  * Drafter-alone mode (tgt_layers == 0): ext_taps holds n_ext tap rows as

@@ -129,3 +129,41 @@ def test_int4_target_spec_equals_greedy_and_batch_invariant(int4_target):
         assert torch.equal(vl[0], batch[i]), f"row {i}"
     dec.set_logits_out(None, None)
     dec.close()
+
+
+def test_int4_target_dense_prefill_matches_chunked_and_oracle(int4_target, monkeypatch):
+    """The dense prefill of an INT4 target (f16 rows times each layer's
+    matrices dequantised exactly to f16) against the 16-row forwards
+    (DFLASH_DENSE_PREFILL=0) on a 300-token prompt: target and draft cache
+    rows to fp16 rounding, the last chunk's logits within the tolerance of
+    each other and of the oracle's dequantised fp64 target."""
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+    T = int4_target
+    w = T["w"].with_(max_seq=512)
+    P = 300
+    prompt = torch.from_numpy(synth.uniform_ids(P, w.vocab, seed=23))
+    cap = (w.max_seq + 63) // 64 * 64
+    out = []
+    for env in (None, "0"):
+        if env is not None:
+            monkeypatch.setenv("DFLASH_DENSE_PREFILL", env)
+        dec = DFlash(w, T["m"])
+        monkeypatch.delenv("DFLASH_DENSE_PREFILL", raising=False)
+        vl = G.logits_buf(w.vocab)
+        dec.set_logits_out(vl, None)
+        dec.prefill(prompt, 8)
+        dec.check()
+        kt = dec.kv_target.view(torch.float16).view(w.tgt_layers, 2, w.n_kv, cap, w.head_dim)
+        kd = dec.kv_draft.view(torch.float16).view(w.drf_layers, 2, w.n_kv, cap, w.head_dim)
+        out.append((kt[:, :, :, :P].float().clone(), kd[:, :, :, :P].float().clone(), vl[:P % 16 or 16].clone()))
+        dec.close()
+    (kt_d, kd_d, lg_d), (kt_c, kd_c, lg_c) = out
+    for a, b in ((kt_d, kt_c), (kd_d, kd_c)):
+        scale = b.abs().amax(dim=-1, keepdim=True).clamp_min(1e-6)
+        assert ((a - b).abs() / scale).max().item() < 2.0 ** -8
+    err = G.rel_err_rows(lg_d.cpu().numpy(), lg_c.cpu().numpy())
+    assert err.max() < TOL / 4, err
+    ref, _ = O.target_forward(T["tw"], T["cfg"], prompt.tolist(), 0, O.KVCache(2, w.n_kv, w.head_dim))
+    last = (P - 1) // 16 * 16
+    err = G.rel_err_rows(lg_d.cpu().numpy(), ref[last:P])
+    assert err.max() < TOL, err
