@@ -591,6 +591,13 @@ def measure_workloads(steps, warmup, base_model):
     dec = DFlash(w4, base_model)
     prompt = torch.from_numpy(synth.uniform_ids(w4.prompt_len, w4.vocab))
     dec.prefill(prompt, w4.n_new)
+    torch.cuda.synchronize()
+    pe0, pe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pe0.record()
+    dec.prefill(prompt, w4.n_new)   # dense: INT4 matrices dequantised to f16 layer by layer
+    pe1.record()
+    torch.cuda.synchronize()
+    prefill4_ms = pe0.elapsed_time(pe1)
     dec.verify(dec.draft())
     torch.cuda.synchronize()
     gb, _, gl = _gemm_bytes_per_call(dec, lambda: dec.verify(dec.draft()))
@@ -601,6 +608,7 @@ def measure_workloads(steps, warmup, base_model):
     kv_bytes = (w4.tgt_layers * w4.n_kv * 2 * (w4.prompt_len + w4.block) * w4.head_dim * 2 +
                 w4.drf_layers * w4.n_kv * 2 * (w4.prompt_len + w4.block) * w4.head_dim * 2)
     out["e2e_int4"] = {"rounds_s": round(1e3 / ms, 2), "ms_per_round": round(ms, 4),
+                       "prefill_ms": round(prefill4_ms, 3),
                        "bytes_per_round": int(gb + kv_bytes), "gemm_launches": gl,
                        "hbm_gbs": round((gb + kv_bytes) / (ms / 1e3) / 1e9, 1),
                        "frac_of_peak": round((gb + kv_bytes) / (ms / 1e3) / 1e9 / peak, 4),
