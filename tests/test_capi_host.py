@@ -100,6 +100,20 @@ def test_null_context_calls_fail_cleanly(capi):
     assert capi.lib.dflash_verify_accept(None, None, None, None, None) == -3
     assert capi.lib.dflash_rollback(None, 5, 0, None) == -3
     assert capi.lib.dflash_attention_form(None, 0) == -3
+    assert capi.lib.dflash_linear_dense(None, None, None, 1, 4, 64, None, None, None) == -3
+
+
+def test_dense_linear_argument_guards(capi):
+    # rejected before anything touches the device: the pointers are never read
+    p = C.c_void_p(1 << 20)                       # 16-byte aligned, never dereferenced
+    bad = [(1, 4, 96),     # k not a multiple of 64
+           (1, 6, 64),     # n not a multiple of 4 (rows of y stay 16-byte aligned)
+           (0, 4, 64),     # no rows
+           (1, 4, 0)]      # no k
+    for m, n, k in bad:
+        assert capi.lib.dflash_linear_dense(p, p, None, m, n, k, p, p, None) == -3, (m, n, k)
+    q = C.c_void_p((1 << 20) + 8)                 # misaligned
+    assert capi.lib.dflash_linear_dense(q, p, None, 1, 4, 64, p, p, None) == -3
     assert capi.lib.dflash_prefill_taps(None, None, 0, None, 0, 1, 0, 1, None) == -3
     assert capi.lib.dflash_quantize_int4g64(None, 1, 256, None, None, None) == -3
     assert capi.lib.dflash_tap_reduce(None, 1, 1, 1, 8, None, None) == -3
