@@ -70,3 +70,42 @@ def test_dequantised_f16_equals_the_oracle_dequantisation():
     assert ((s == 0) | ((s >= LO) & (s <= HI))).all()
     deq = O.dequant_int4_g64(packed, s_bits)
     np.testing.assert_array_equal(deq.astype(np.float16).astype(np.float64), deq)
+
+
+def _wide_fp32(n, seed, lo_exp, hi_exp):
+    rng = np.random.default_rng(seed)
+    mant = rng.uniform(1.0, 2.0, n)
+    exp = rng.integers(lo_exp, hi_exp, n)
+    sign = rng.choice([-1.0, 1.0], n)
+    return (sign * mant * np.exp2(exp)).astype(np.float32)
+
+
+def test_bf16_hi_lo_planes_carry_16_bits():
+    # GEMM inputs go in as hi = bf16(v), lo = bf16(v - hi): the fp32
+    # difference is exact and hi + lo is within 2^-16 of v (two roundings
+    # of an 8-bit significand), which is what puts the GEMM-input share of
+    # the logits' error near 2e-5 instead of the ~1 % of plain bf16 inputs
+    import torch
+    v = _wide_fp32(200_000, 3, -60, 60)
+    hi = torch.from_numpy(v).to(torch.bfloat16).float().numpy()
+    r = v - hi                                              # fp32, as the kernel
+    np.testing.assert_array_equal(r.astype(np.float64), v.astype(np.float64) - hi.astype(np.float64))
+    lo = torch.from_numpy(r).to(torch.bfloat16).float().numpy()
+    err = np.abs(v.astype(np.float64) - hi.astype(np.float64) - lo.astype(np.float64))
+    assert (err <= 2.0 ** -16 * np.abs(v.astype(np.float64))).all()
+    # plain bf16 is 2^8 times coarser: the bound is reached, not loose
+    rel_hi = np.abs(v.astype(np.float64) - hi) / np.abs(v.astype(np.float64))
+    assert rel_hi.max() > 2.0 ** -9.5 and (err / np.abs(v.astype(np.float64))).max() > 2.0 ** -18
+
+
+def test_f16_hi_lo_planes_inside_their_range():
+    # the INT4 dense paths carry activations as f16 hi/lo: within 2^-22
+    # relative plus the subnormal floor 2^-25, for |v| up to 65504
+    v = _wide_fp32(200_000, 4, -12, 16)
+    v = v[np.abs(v) <= 65504]
+    hi = v.astype(np.float16).astype(np.float32)
+    r = v - hi
+    np.testing.assert_array_equal(r.astype(np.float64), v.astype(np.float64) - hi.astype(np.float64))
+    lo = r.astype(np.float16).astype(np.float64)
+    err = np.abs(v.astype(np.float64) - hi.astype(np.float64) - lo)
+    assert (err <= 2.0 ** -22 * np.abs(v.astype(np.float64)) + 2.0 ** -25).all()
