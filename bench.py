@@ -66,6 +66,21 @@ def rank_info():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def reduce_over_ranks(world, device, t_ms, *counts):
+    """Replicas: the whole job's time is the slowest rank's timed region and
+    each count (rounds, tokens) is summed over the ranks.  Returns
+    (max t_ms, [sum of each count]); with one rank, the inputs unchanged."""
+    if world == 1:
+        return t_ms, list(counts)
+    import torch
+    import torch.distributed as dist
+    mx = torch.tensor([float(t_ms)], dtype=torch.float64, device=device)
+    sm = torch.tensor([float(c) for c in counts], dtype=torch.float64, device=device)
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return float(mx[0]), [float(v) for v in sm.tolist()]
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
 
@@ -339,16 +354,8 @@ def run_ours(args):
     st1 = dec.stats()
     dec.check()
     clocks = clk.summary()
-    t_max = ms
     rounds_total = args.steps * world
-    emitted = st1.emitted - st0.emitted
-    if world > 1:
-        tt = torch.tensor([ms, float(emitted)], device="cuda")
-        mx = tt.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        dist.all_reduce(tt, op=dist.ReduceOp.SUM)
-        t_max = float(mx[0])
-        emitted = float(tt[1])
+    t_max, (emitted,) = reduce_over_ranks(world, "cuda", ms, st1.emitted - st0.emitted)
     value = rounds_total / (t_max / 1e3)
 
     # GEMM timing: the same round captured with event nodes around each GEMM
@@ -427,7 +434,7 @@ def run_ours(args):
         result["config"]["workload"] += f" [DEBUG: target layers overridden to {args.layers}]"
 
     if not args.no_e2e:
-        result["e2e"] = e2e_measure(dec, w, prompt)
+        result["e2e"] = e2e_measure(dec, w, prompt, world, barrier)
     del g, gp, gg            # graphs hold event nodes of this context: drop them first
     torch.cuda.synchronize()
     if not args.no_workloads and not args.layers:
@@ -826,28 +833,32 @@ def measure_injected(w, model, blocks=(16, 8, 4, "16a"), reps=3):
 E2E_ROUNDS_PER_REPLAY = 16
 
 
-def e2e_measure(dec, w, prompt):
+def e2e_measure(dec, w, prompt, world=1, barrier=lambda: None):
     """Host prompt in pinned memory -> tokens on the host, through the public
     Python API (DFlash.generate_graphed): H2D of the prompt, prefill, then
     rounds replayed from a CUDA graph of 16 rounds until w.n_new tokens; every
     round's emitted tokens and the progress words come back to pinned host
-    memory with each replay (one host wait per replay)."""
+    memory with each replay (one host wait per replay).  With several
+    replicas: the rounds and tokens of all ranks over the slowest rank's time."""
     import torch
     host_prompt = prompt.to(torch.int32).pin_memory()
     dec.generate_graphed(host_prompt.to("cuda"), w.n_new, E2E_ROUNDS_PER_REPLAY)   # capture
     torch.cuda.synchronize()
+    barrier()
     t0 = time.perf_counter()
     dev_prompt = host_prompt.to("cuda", non_blocking=True)
     tokens = dec.generate_graphed(dev_prompt, w.n_new, E2E_ROUNDS_PER_REPLAY)
     torch.cuda.synchronize()
     dt = time.perf_counter() - t0
-    st = dec.stats()
-    rounds = int(st.rounds)
+    rounds_rank = int(dec.stats().rounds)
+    dt_ms, (rounds, n_tok) = reduce_over_ranks(world, "cuda", dt * 1e3, rounds_rank, len(tokens))
+    dt = dt_ms / 1e3
+    rounds, n_tok = int(rounds), int(n_tok)
     return {"value": round(rounds / dt, 3), "unit": "rounds/s",
-            "tokens_per_s": round(len(tokens) / dt, 3), "rounds": rounds, "tokens": len(tokens),
+            "tokens_per_s": round(n_tok / dt, 3), "rounds": rounds, "tokens": n_tok,
             "includes": "prompt H2D + 1024-token prefill + rounds to 512 tokens; each round's "
                         "tokens and the progress words D2H per 16-round graph replay",
-            "h2d_bytes_per_step": round(host_prompt.numel() * 4 / max(1, rounds), 2),
+            "h2d_bytes_per_step": round(host_prompt.numel() * 4 / max(1, rounds_rank), 2),
             "d2h_bytes_per_step": (w.block + 1) * 4 + round(16 / E2E_ROUNDS_PER_REPLAY, 2)}
 
 
