@@ -428,6 +428,12 @@ def run_ours(args):
             "traffic": traffic.get("dram_bytes_per_launch") if traffic else None,
             "gemm_share_of_round": round(prof_ms / ms, 4) if ms else None,
             "bytes_per_round": prof_bytes / args.steps,
+            "round_bound_gbs": round(prof_bytes / (ms / 1e3) / 1e9, 1) if ms else None,
+            "note": "achieved: each GEMM timed by CUDA event nodes in a captured round; the "
+                    "events break the programmatic-dependent-launch overlap, so each GEMM's "
+                    "duration also holds its start-up behind the previous kernel (the sum can "
+                    "exceed the round: gemm_share_of_round > 1) and achieved is a lower bound; "
+                    "round_bound_gbs (the GEMMs' bytes over the whole round's time) is another",
         },
     }
     if args.layers:
