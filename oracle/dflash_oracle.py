@@ -519,10 +519,12 @@ class SpecTrace:
 DraftFn = Callable[[int, int, int, List[int]], List[int]]
 
 
-def spec_decode(tw: TargetWeights, dw: Optional[DraftWeights], cfg: OracleConfig,
+def spec_rounds(tw: TargetWeights, dw: Optional[DraftWeights], cfg: OracleConfig,
                 prompt: Sequence[int], n_new: int,
-                draft_override: Optional[DraftFn] = None) -> SpecTrace:
-    """The speculative loop: draft -> verify -> accept -> roll back.
+                draft_override: Optional[DraftFn] = None):
+    """The speculative loop: draft -> verify -> accept -> roll back, as a
+    generator: yields (trace, 0) after the prompt's forward and (trace, bl)
+    after every round, bl = the rows that round's verify ran.
 
     Per round ([RFC] DFlash, "Key Implementation Details" Phase 3, and
     "Requested changes" 1 and 3):
@@ -543,6 +545,7 @@ def spec_decode(tw: TargetWeights, dw: Optional[DraftWeights], cfg: OracleConfig
     n = len(prompt)
     finished = cfg.eos_id >= 0 and tr.tokens[0] == cfg.eos_id
     ema = float(np.float32(B - 1))
+    yield tr, 0
     while len(tr.tokens) < n_new and not finished:
         t_n = tr.tokens[-1]
         cap = adaptive_block_cap(ema, B) if cfg.adaptive_block else B
@@ -569,4 +572,57 @@ def spec_decode(tw: TargetWeights, dw: Optional[DraftWeights], cfg: OracleConfig
         tr.tokens.extend(emitted)
         tr.rounds += 1
         n = n_new_len
+        yield tr, bl
+
+
+def spec_decode(tw: TargetWeights, dw: Optional[DraftWeights], cfg: OracleConfig,
+                prompt: Sequence[int], n_new: int,
+                draft_override: Optional[DraftFn] = None) -> SpecTrace:
+    """The whole speculative loop of one sequence (spec_rounds run out)."""
+    tr = None
+    for tr, _ in spec_rounds(tw, dw, cfg, prompt, n_new, draft_override):
+        pass
     return tr
+
+
+@dataclass
+class BatchTrace:
+    traces: List[SpecTrace]
+    rounds: int = 0                                            # batched rounds
+    rows_per_round: List[int] = field(default_factory=list)   # verify rows, all sequences
+
+
+def spec_decode_batch(tw: TargetWeights, dw: Optional[DraftWeights], cfg: OracleConfig,
+                      prompts: Sequence[Sequence[int]], n_new,
+                      draft_overrides: Optional[Sequence[Optional[DraftFn]]] = None) -> BatchTrace:
+    """Several independent sequences decoded in lockstep rounds.
+
+    The pages verify one sequence's 1+m rows per forward ([RFC] DFlash,
+    "Key Implementation Details" Phase 3: a [1, 1+m] batch).  Batching
+    sequences is this library's extension (a reading): in each batched
+    round every unfinished sequence takes its own round (its own block
+    length, drafts, acceptance and rollback), and the batched verify runs
+    the sum of their rows.  Sequences share only the weights, so each
+    sequence's result is its single-sequence speculative decode.  n_new is
+    one budget for all sequences or one per sequence; draft_overrides, one
+    per sequence, as spec_decode's draft_override.
+    """
+    budgets = list(n_new) if isinstance(n_new, (list, tuple)) else [n_new] * len(prompts)
+    fns = list(draft_overrides) if draft_overrides is not None else [None] * len(prompts)
+    gens = [spec_rounds(tw, dw, cfg, p, b, f) for p, b, f in zip(prompts, budgets, fns)]
+    bt = BatchTrace(traces=[next(g)[0] for g in gens])
+    active = list(range(len(gens)))
+    while active:
+        rows, still = 0, []
+        for i in active:
+            step = next(gens[i], None)
+            if step is None:
+                continue
+            bt.traces[i], bl = step
+            rows += bl
+            still.append(i)
+        if still:
+            bt.rounds += 1
+            bt.rows_per_round.append(rows)
+        active = still
+    return bt

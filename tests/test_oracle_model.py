@@ -310,6 +310,44 @@ def test_spec_eos_and_budget(tiny):
             r["emitted"] for r in tr.per_round[:-1]))
 
 
+def test_batch_of_sequences_equals_each_sequence_alone(tiny):
+    """Lockstep multi-sequence rounds: every sequence's tokens are its own
+    greedy decoding and its rounds those of its single-sequence run; the
+    batched round count is the longest sequence's, each batched round's
+    verify rows are the block lengths of the sequences still running, and
+    reordering the batch reorders the results."""
+    tw, dw, cfg = tiny["tw"], tiny["dw"], tiny["cfg"]
+    prompts = [tiny["prompt"], synth.uniform_ids(20, TINY.vocab, seed=5).tolist(),
+               synth.uniform_ids(27, TINY.vocab, seed=6).tolist()]
+    budgets = [24, 9, 16]
+    greedy = [O.greedy(tw, cfg, p, b) for p, b in zip(prompts, budgets)]
+
+    def copy_of(i):   # drafts copied from greedy, wrong at every third round
+        def fn(t_n, n, bl, hist):
+            k = len(hist) - len(prompts[i])
+            d = greedy[i][k:k + bl - 1]
+            if d and (n // 2) % 3 == 0:
+                d[-1] = (d[-1] + 1) % cfg.vocab
+            return d
+        return fn
+
+    for overrides in (None, [copy_of(0), None, copy_of(2)]):
+        bt = O.spec_decode_batch(tw, dw, cfg, prompts, budgets, overrides)
+        for i, tr in enumerate(bt.traces):
+            assert tr.tokens == greedy[i]
+            f = overrides[i] if overrides else None
+            assert tr.per_round == O.spec_decode(tw, dw, cfg, prompts[i], budgets[i], f).per_round
+        assert bt.rounds == max(tr.rounds for tr in bt.traces)
+        assert len({tr.rounds for tr in bt.traces}) > 1          # sequences leave at different rounds
+        for r in range(bt.rounds):
+            assert bt.rows_per_round[r] == sum(tr.per_round[r]["bl"] for tr in bt.traces
+                                               if r < tr.rounds)
+        rev = O.spec_decode_batch(tw, dw, cfg, prompts[::-1], budgets[::-1],
+                                  overrides[::-1] if overrides else None)
+        assert [t.tokens for t in rev.traces] == [t.tokens for t in bt.traces][::-1]
+        assert rev.rows_per_round == bt.rows_per_round
+
+
 def test_tap_is_residual_after_layer(tiny):
     """A tap at the last layer is the stream the final norm reads: the logits
     follow from it through final RMSNorm and the tied LM head."""
