@@ -133,6 +133,39 @@ def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+DFLASH_ERR_ARG = -3
+
+
+def _need(t, name: str, dtypes, shape) -> None:
+    """Binding-side argument check of a standalone operation's tensor (the C
+    ABI sees only pointers and sizes): dtype, shape (None = any extent) and
+    row-major contiguity.  Raises DFlashError(ARG) before any device work."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise DFlashError(DFLASH_ERR_ARG, f"{name}: a torch tensor is required")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise DFlashError(DFLASH_ERR_ARG, f"{name}: dtype {t.dtype}, expected one of {dtypes}")
+    if shape is not None and (t.dim() != len(shape) or
+                              any(e is not None and e != d for e, d in zip(shape, t.shape))):
+        raise DFlashError(DFLASH_ERR_ARG, f"{name}: shape {tuple(t.shape)}, expected {shape}")
+    if not t.is_contiguous():
+        raise DFlashError(DFLASH_ERR_ARG, f"{name}: must be contiguous (row-major)")
+
+
+def _on_gpu(**tensors) -> None:
+    """Every tensor on one CUDA device: the library reads device pointers and
+    has no CPU path."""
+    devs = set()
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise DFlashError(DFLASH_ERR_ARG, f"{name}: a CUDA tensor is required (no CPU path)")
+        devs.add(t.device)
+    if len(devs) > 1:
+        raise DFlashError(DFLASH_ERR_ARG, f"tensors on several devices: {sorted(map(str, devs))}")
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         import torch
@@ -198,13 +231,24 @@ def dflash_destroy(ctx):
 
 
 def dflash_tap_reduce(layer_streams, rows: int, hc: int, hidden: int, out, stream=None):
+    import torch
+    for i, t in enumerate(layer_streams):
+        _need(t, f"layer_streams[{i}]", (torch.bfloat16,), (rows, hc * hidden))
+    _need(out, "out", (torch.float32,), (rows, len(layer_streams) * hidden))
+    _on_gpu(out=out, **{f"layer_streams[{i}]": t for i, t in enumerate(layer_streams)})
     arr = (C.c_void_p * len(layer_streams))(*[t.data_ptr() for t in layer_streams])
     check(lib.dflash_tap_reduce(arr, len(layer_streams), rows, hc, hidden, _ptr(out),
                                 _stream(stream)))
 
 
 def dflash_quantize_int4g64(w, packed, scales, stream=None):
+    import torch
+    _need(w, "w", (torch.float32,), (None, None))
     n, k = w.shape
+    _need(packed, "packed", (torch.uint8,), (n, k // 2))
+    two_byte = tuple(d for d in (torch.int16, getattr(torch, "uint16", None)) if d is not None)
+    _need(scales, "scales", two_byte, (k // 64, n))
+    _on_gpu(w=w, packed=packed, scales=scales)
     check(lib.dflash_quantize_int4g64(_ptr(w), n, k, _ptr(packed), _ptr(scales), _stream(stream)))
 
 
@@ -231,8 +275,19 @@ def dflash_linear_workspace_bytes(n: int, k: int) -> int:
     return lib.dflash_linear_workspace_bytes(n, k)
 
 
-def dflash_linear(w, x, y, workspace, stream=None):
+def _linear_operands(w, x, y):
+    import torch
+    _need(w, "w", (torch.bfloat16,), (None, None))
     n, k = w.shape
+    _need(x, "x", (torch.bfloat16,), (MAX_BLOCK, k))
+    _need(y, "y", (torch.float32,), (MAX_BLOCK, n))
+    return n, k
+
+
+def dflash_linear(w, x, y, workspace, stream=None):
+    n, k = _linear_operands(w, x, y)
+    _need(workspace, "workspace", None, None)
+    _on_gpu(w=w, x=x, y=y, workspace=workspace)
     check(lib.dflash_linear(_ptr(w), _ptr(x), n, k, _ptr(y), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(stream)))
 
@@ -240,7 +295,8 @@ def dflash_linear(w, x, y, workspace, stream=None):
 def dflash_linear_noalloc(w, x, y, stream=None):
     """y = x w^T like dflash_linear, with the library's fixed scratch instead
     of a caller workspace (for callers that cannot allocate device memory)."""
-    n, k = w.shape
+    n, k = _linear_operands(w, x, y)
+    _on_gpu(w=w, x=x, y=y)
     check(lib.dflash_linear_noalloc(_ptr(w), _ptr(x), n, k, _ptr(y), _stream(stream)))
 
 
@@ -277,7 +333,17 @@ def dflash_attention_form(ctx, model: int) -> int:
 def dflash_linear_dense(w, x, y, err, x_lo=None, stream=None):
     """y[m][n] = x[m] . w[n] (+ x_lo[m] . w[n]) on the tcgen05 dense GEMM:
     x, x_lo bf16 [M][K], w bf16 [N][K], y fp32 [M][N], err int32[2] zeros."""
+    import torch
+    _need(x, "x", (torch.bfloat16,), (None, None))
     m, k = x.shape
+    _need(w, "w", (torch.bfloat16,), (None, k))
     n = w.shape[0]
+    _need(y, "y", (torch.float32,), (m, n))
+    if x_lo is not None:
+        _need(x_lo, "x_lo", (torch.bfloat16,), (m, k))
+    _need(err, "err", (torch.int32,), (None,))
+    if err.numel() < 2:
+        raise DFlashError(DFLASH_ERR_ARG, "err: int32[2] required")
+    _on_gpu(w=w, x=x, x_lo=x_lo, y=y, err=err)
     check(lib.dflash_linear_dense(_ptr(w), _ptr(x), _ptr(x_lo), m, n, k, _ptr(y), _ptr(err),
                                   _stream(stream)))

@@ -117,3 +117,40 @@ def test_dense_linear_argument_guards(capi):
     assert capi.lib.dflash_prefill_taps(None, None, 0, None, 0, 1, 0, 1, None) == -3
     assert capi.lib.dflash_quantize_int4g64(None, 1, 256, None, None, None) == -3
     assert capi.lib.dflash_tap_reduce(None, 1, 1, 1, 8, None, None) == -3
+
+
+def test_binding_checks_standalone_operands_before_the_library(capi):
+    """The bindings of the standalone operations check dtype, shape,
+    contiguity and device before calling the library (which sees only
+    pointers): mismatches raise DFlashError(ARG) on the host, and host tensors
+    are refused (the library has no CPU path)."""
+    import torch
+    bf, f32 = torch.bfloat16, torch.float32
+    e = lambda: torch.zeros(2, dtype=torch.int32)
+    cases = [
+        ("w", lambda: capi.dflash_linear_dense(torch.zeros(8, 128, dtype=bf), torch.zeros(4, 64, dtype=bf),
+                                               torch.zeros(4, 8), e())),
+        ("y", lambda: capi.dflash_linear_dense(torch.zeros(8, 64, dtype=bf), torch.zeros(4, 64, dtype=bf),
+                                               torch.zeros(8, 4), e())),
+        ("x_lo", lambda: capi.dflash_linear_dense(torch.zeros(8, 64, dtype=bf), torch.zeros(4, 64, dtype=bf),
+                                                  torch.zeros(4, 8), e(),
+                                                  x_lo=torch.zeros(4, 64, dtype=f32))),
+        ("err", lambda: capi.dflash_linear_dense(torch.zeros(8, 64, dtype=bf), torch.zeros(4, 64, dtype=bf),
+                                                 torch.zeros(4, 8), torch.zeros(1, dtype=torch.int32))),
+        ("x", lambda: capi.dflash_linear(torch.zeros(128, 64, dtype=bf), torch.zeros(8, 64, dtype=bf),
+                                         torch.zeros(16, 128), torch.zeros(64, dtype=torch.uint8))),
+        ("x", lambda: capi.dflash_linear_noalloc(torch.zeros(128, 64, dtype=bf),
+                                                 torch.zeros(128, 16, dtype=bf).t(), torch.zeros(16, 128))),
+        ("scales", lambda: capi.dflash_quantize_int4g64(torch.zeros(4, 256), torch.zeros(4, 128, dtype=torch.uint8),
+                                                        torch.zeros(2, 4, dtype=torch.int16))),
+        ("out", lambda: capi.dflash_tap_reduce([torch.zeros(3, 4 * 64, dtype=bf)] * 2, 3, 4, 64,
+                                               torch.zeros(3, 64))),
+        ("CUDA", lambda: capi.dflash_linear_dense(torch.zeros(8, 64, dtype=bf), torch.zeros(4, 64, dtype=bf),
+                                                  torch.zeros(4, 8), e())),
+        ("CUDA", lambda: capi.dflash_tap_reduce([torch.zeros(3, 4 * 64, dtype=bf)] * 2, 3, 4, 64,
+                                                torch.zeros(3, 128))),
+    ]
+    for word, call in cases:
+        with pytest.raises(capi.DFlashError) as exc:
+            call()
+        assert exc.value.code == -3 and word in str(exc.value), (word, str(exc.value))
