@@ -514,6 +514,7 @@ class SpecTrace:
     rounds: int = 0
     accept_hist: List[int] = field(default_factory=list)   # per draft position
     per_round: List[dict] = field(default_factory=list)
+    ctx_taps: List[np.ndarray] = field(default_factory=list)  # draft context, by position
 
 
 DraftFn = Callable[[int, int, int, List[int]], List[int]]
@@ -541,7 +542,8 @@ def spec_rounds(tw: TargetWeights, dw: Optional[DraftWeights], cfg: OracleConfig
     cache = KVCache(len(tw.layers), cfg.n_kv, cfg.head_dim)
     logits, taps = target_forward(tw, cfg, prompt, 0, cache)
     ctx_taps = [row for row in taps]                  # position p -> tap row
-    tr = SpecTrace(tokens=[argmax_lowest(logits[-1])], accept_hist=[0] * (B - 1))
+    tr = SpecTrace(tokens=[argmax_lowest(logits[-1])], accept_hist=[0] * (B - 1),
+                   ctx_taps=ctx_taps)
     n = len(prompt)
     finished = cfg.eos_id >= 0 and tr.tokens[0] == cfg.eos_id
     ema = float(np.float32(B - 1))

@@ -310,6 +310,30 @@ def test_spec_eos_and_budget(tiny):
             r["emitted"] for r in tr.per_round[:-1]))
 
 
+def test_tap_commit_holds_the_full_forward_taps(tiny):
+    """After the loop, the draft context's tap row at every position p is the
+    target's tap row of a single forward over the whole confirmed sequence
+    at p: rounds commit exactly the taps of the accepted verify rows (the
+    pending token's row is not committed)."""
+    tw, dw, cfg, prompt = tiny["tw"], tiny["dw"], tiny["cfg"], tiny["prompt"]
+    g = O.greedy(tw, cfg, prompt, 40)
+
+    def drafts(t_n, n, bl, hist):   # right for most rows, wrong at every third round
+        k = len(hist) - len(prompt)
+        d = g[k:k + bl - 1]
+        if d and (n % 3) == 0:
+            d[len(d) // 2] = (d[len(d) // 2] + 1) % cfg.vocab
+        return d
+
+    for fn in (drafts, None):
+        tr = O.spec_decode(tw, dw, cfg, prompt, 40, draft_override=fn)
+        assert tr.tokens == g
+        seq = list(prompt) + tr.tokens[:-1]
+        _, full = O.target_forward(tw, cfg, seq, 0, O.KVCache(len(tw.layers), cfg.n_kv, cfg.head_dim))
+        assert len(tr.ctx_taps) == len(seq)
+        np.testing.assert_allclose(np.stack(tr.ctx_taps), full, rtol=1e-10, atol=1e-10)
+
+
 def test_batch_of_sequences_equals_each_sequence_alone(tiny):
     """Lockstep multi-sequence rounds: every sequence's tokens are its own
     greedy decoding and its rounds those of its single-sequence run; the
