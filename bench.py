@@ -66,6 +66,20 @@ def rank_info():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def workload_config(w, world, timing, l2):
+    """The `config` object both arms print: the same workload, with the
+    arm's own timing method and cache treatment."""
+    return {
+        "workload": "e2e_bf16: 36-layer Qwen3-4B-shaped bf16 target (hidden 2560, 32q/8kv "
+                    "heads, SwiGLU 9728, vocab 151936) + 5-layer drafter, taps at "
+                    "{0,8,17,26,35}, block 16, 1024-token prompt, natural acceptance",
+        "block": w.block, "prompt_len": w.prompt_len,
+        "l2": l2,
+        "timing": timing,
+        "parallelism": f"replicas x{world}",
+    }
+
+
 def reduce_over_ranks(world, device, t_ms, *counts):
     """Replicas: the whole job's time is the slowest rank's timed region and
     each count (rounds, tokens) is summed over the ranks.  Returns
@@ -400,15 +414,10 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_max / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded N(0,0.02) random-init bf16 weights, uniform-random prompt",
-        "config": {
-            "workload": "e2e_bf16: 36-layer Qwen3-4B-shaped bf16 target (hidden 2560, 32q/8kv "
-                        "heads, SwiGLU 9728, vocab 151936) + 5-layer drafter, taps at "
-                        "{0,8,17,26,35}, block 16, 1024-token prompt, natural acceptance",
-            "block": B, "prompt_len": w.prompt_len,
-            "l2": "no flush: each round streams ~9.9 GB of weights, far larger than the 129 MB L2",
-            "timing": "CUDA graph of one round replayed K times, CUDA events on the replay stream",
-            "parallelism": f"replicas x{world}",
-        },
+        "config": workload_config(
+            w, world,
+            timing="CUDA graph of one round replayed K times, CUDA events on the replay stream",
+            l2="no flush: each round streams ~9.9 GB of weights, far larger than the 129 MB L2"),
         "accepted_tok_s": round(emitted / (t_max / 1e3), 3),
         "tokens_per_round": round(emitted / rounds_total, 4),
         "verify_ms_T1": round(t1row, 4),
@@ -893,7 +902,11 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(mean * 1e3, 1), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same generators as ours)",
-        "config": {"workload": "e2e_bf16 round on the CPU oracle, layer sample extrapolated"},
+        "config": workload_config(
+            E2E_BF16, world,
+            timing="CPU oracle (fp64) on the host cores: each step times one piece of a layer "
+                   "sample of the round, the round extrapolated by layer count",
+            l2="not applicable (host run)"),
         "cpu_baseline": {"value": round(v, 6), "unit": "rounds/s", "cores": cpu_cores(),
                          "kind": "oracle", "sample": osmp.describe()},
         "e2e": {"value": round(v, 6), "unit": "rounds/s", "h2d_bytes_per_step": 0,
