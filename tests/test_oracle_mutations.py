@@ -9,7 +9,10 @@ a causal mask off by one, the sliding window's anchor off by one, argmax ties
 to the highest index, acceptance or rollback off by one, the bonus token
 dropped, taps committed from the wrong rows or taken before the layer, the
 hc layout interleaved, INT4 nibbles or scale wrong, drafts read from block
-row 0, a causal draft block.  Every case must make at least one pin of the
+row 0, a causal draft block, the drafter's context keys and values built
+wrong, the mask token replaced, the attention scale or residual wrong, the
+untied LM head ignored, EOS truncation or the hc scale wrong, the adaptive
+average or the batched row count wrong.  Every case must make at least one pin of the
 oracle test modules fail an assertion; the unmutated oracle passes them all.
 """
 
@@ -74,6 +77,24 @@ MUTATIONS = [
      "vis[:, :len(ctx_pos)] = ctx_ok[None, :]\n"
      "    vis[:, len(ctx_pos):] = np.tril(np.ones((bl, bl), dtype=bool))"),
     ("adaptive_threshold_inclusive", "adaptive_block_cap", "e < np.float32(1.5)", "e <= np.float32(1.5)"),
+    ("adaptive_average_weights", "adaptive_ema_update",
+     "half * np.float32(ema) + half * np.float32(accepted)",
+     "np.float32(0.75) * np.float32(ema) + np.float32(0.25) * np.float32(accepted)"),
+    ("ctx_rope_positions_shifted", "draft_forward", "ctx_pos,\n                              cfg.rope_theta",
+     "[p + 1 for p in ctx_pos],\n                              cfg.rope_theta"),
+    ("ctx_k_norm_dropped", "draft_forward", 'rope_rotate_half(rms_norm(kc, lw["k_norm"], cfg.rms_eps), ctx_pos,',
+     "rope_rotate_half(kc, ctx_pos,"),
+    ("ctx_values_from_w_k", "draft_forward", 'vc = linear(c, lw["wv"])', 'vc = linear(c, lw["wk"])'),
+    ("mask_token_replaced", "draft_forward", "[t_n] + [cfg.mask_id] * (bl - 1)", "[t_n] * bl"),
+    ("attention_scale", "target_layer", "1.0 / math.sqrt(cfg.head_dim)", "1.0 / cfg.head_dim"),
+    ("attention_residual_dropped", "target_layer", 'x = x + linear(a.reshape(x.shape[0], -1), lw["wo"])',
+     'x = linear(a.reshape(x.shape[0], -1), lw["wo"])'),
+    ("untied_lm_head_ignored", "target_forward", "logits = linear(h, tw.head())",
+     "logits = linear(h, tw.embed)"),
+    ("eos_dropped_from_output", "accept", "emitted = emitted[: emitted.index(eos_id) + 1]",
+     "emitted = emitted[: max(emitted.index(eos_id), 1)]"),
+    ("hc_mean_scale", "hc_mean", "acc * (1.0 / hc)", "acc * (1.0 / max(hc - 1, 1))"),
+    ("batch_rows_counted_per_sequence", "spec_decode_batch", "rows += bl", "rows += 1"),
 ]
 
 
