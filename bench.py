@@ -217,9 +217,11 @@ class OracleRoundSample:
         self.h = np.random.default_rng(0).standard_normal((B, H))
         O.linear(self.h, self.embed)                       # warm-up, untimed
         self.t = {}
+        self.wall = self.cpu = 0.0                         # over every timed piece
 
     def time_piece(self, name: str) -> float:
         O, w, n, B = self.O, self.w, self.w.prompt_len, self.w.block
+        c0 = os.times()
         tic = time.perf_counter()
         if name == "head":
             O.linear(self.h, self.embed)
@@ -231,7 +233,15 @@ class OracleRoundSample:
             x = self.embed[self.np.arange(1, B + 1)].astype(self.np.float64)
             O.target_layer(x, self.tl, self.cfg, list(range(n, n + B)), self.cache, 0)
         self.t[name] = time.perf_counter() - tic
+        c1 = os.times()
+        self.wall += self.t[name]
+        self.cpu += (c1.user - c0.user) + (c1.system - c0.system)
         return self.t[name]
+
+    def threads_used(self) -> float:
+        """Process CPU time over wall time of the timed pieces: the number of
+        host threads the oracle kept busy on average (BLAS threads included)."""
+        return self.cpu / self.wall if self.wall > 0 else 0.0
 
     def round_s(self) -> float:
         t, w = self.t, self.w
@@ -244,7 +254,8 @@ class OracleRoundSample:
                 f"{w.prompt_len} taps {t['fc']:.2f} s; 1-layer drafter forward {t['draft']:.2f} s; "
                 f"1 of {w.tgt_layers} target layers verifying {w.block} rows over a "
                 f"{w.prompt_len}-position cache {t['target']:.2f} s; one {w.vocab}-row LM head "
-                f"{t['head']:.2f} s; round extrapolated by layer count")
+                f"{t['head']:.2f} s; round extrapolated by layer count; {self.threads_used():.1f} "
+                f"host threads busy on average (CPU time / wall time)")
 
 
 def cpu_cores() -> int:
