@@ -1,5 +1,15 @@
 // Split-KV attention on tensor cores for the bf16 models (verify, prefill
-// and the drafter's block attention).  q and the K/V caches are fp16 (11
+// and the drafter's block attention).
+//
+// What it computes, by page: the drafter's block rows attend to the sliding
+// context window and to every row of their own block, with no causal order
+// inside the block ("feat: DFlash2 block-diffusion drafter for Qwen 3.8",
+// first commit: block attention over [sliding ctx | bidirectional block];
+// "[RFC] DFlash", "Requested changes" 2: the draft block is non-causal); the
+// target's verify and prefill rows attend causally over the KV cache ("[RFC]
+// DFlash", "Key Implementation Details", Phase 3).  Only the valid part of a
+// cache is read, never the whole buffer (the RFC author's reply, "3. Draft
+// KV cache": a masked full-buffer attention cost tracked the buffer size).  q and the K/V caches are fp16 (11
 // mantissa bits, against bf16's 8: the scores of a 36-layer stack stay
 // within the logit tolerance), P is rounded to fp16 for the P V product.
 //

@@ -1,6 +1,14 @@
 // C ABI of the DFlash round (include/dflash.h): configuration guards,
 // workspace layout, TMA descriptors and the launch sequence of each call.
 //
+// The guards check the drafter against the target (hidden size, vocabulary,
+// tap layers) before any buffer is touched ("feat: DFlash2 block-diffusion
+// drafter for Qwen 3.8", the config-guard commit: a checkpoint with the
+// right vocabulary and layer count but another hidden size had been
+// accepted).  The calls follow the round of "[RFC] DFlash", "Key
+// Implementation Details": taps (Phase 1), draft, batched verify,
+// first-mismatch acceptance and KV-cache rollback (Phase 3).
+//
 // The library never allocates device memory and never synchronises except
 // in dflash_stats / dflash_check; every launch goes to the caller's stream,
 // so the launches of a round can be captured in a CUDA graph.

@@ -1,5 +1,16 @@
 // Skinny weight-streaming GEMM for the <= 16 rows of one DFlash forward.
 //
+// By page: the drafter's projections stream each weight once for all the
+// block's rows ("feat: DFlash2 block-diffusion drafter for Qwen 3.8", first
+// commit: the multi-x BF16 GEMV; third commit: projections quantised at
+// load into the multi-x INT4 format); the verify runs the 1+m rows in one
+// forward ("dflash: the chain verify builds pipelined ...", fourth commit:
+// the [1, 1+m] verify forward; "[RFC] DFlash", "Key Implementation Details",
+// Phase 3); the residual stream stays fp32 (DFlash2 page, first commit: the
+// o/down projections overflow fp16 on outlier channels).  A row's result
+// never depends on how many rows the call has (the RFC author's reply, the
+// aside on a quantised-matmul kernel switch at batch 6 that flipped argmaxes).
+//
 // Y[t][n] = sum_k X[t][k] W[n][k], W in the nn.Linear layout [N][K].  The
 // rows t (block rows, verify rows or a prefill chunk) are few, so the work
 // is a stream of W from HBM: one pass over W per call is the whole cost.

@@ -1,4 +1,10 @@
-// Dense many-row GEMM on the fifth-generation tensor cores:
+// Dense many-row GEMM on the fifth-generation tensor cores (by page: the
+// drafter's context ingest stages the prompt's trailing window of tap rows,
+// "feat: DFlash2 block-diffusion drafter for Qwen 3.8", third commit, into
+// the persistent draft KV cache of "[RFC] DFlash", "Requested changes" 3;
+// and the target's prompt forward, which returns logits and tap rows,
+// "[RFC] DFlash", "Key Implementation Details", Phase 1, target hidden-state
+// export):
 // y[m][n] = sum_k x[m][k] * w[n][k], x and w bf16 or both f16 (w in nn.Linear layout),
 // y fp32, accumulated in tensor memory.  Serves the dense part of the
 // round's pipeline, the drafter's context-window ingest (fc over the

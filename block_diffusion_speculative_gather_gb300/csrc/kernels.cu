@@ -3,6 +3,16 @@
 // attention with a fixed chunk size, acceptance / rollback bookkeeping, the
 // hc-stream tap reduce and the INT4 group-64 quantiser.
 //
+// By page: the block [t_n, MASK...] drafted in one forward ("[RFC] DFlash",
+// "DFlash Overview"); first-mismatch acceptance with the bonus token and
+// KV-cache position rollback ("[RFC] DFlash", "Key Implementation Details",
+// Phase 3), the dynamic block length ("Requested changes" 1), EOS keeping
+// the first EOS (the second review); the per-token mean over the
+// hyper-connection streams ("dflash: the chain verify builds pipelined ...",
+// first commit); projections quantised to INT4 at load ("feat: DFlash2
+// block-diffusion drafter for Qwen 3.8", third commit), here the group-64
+// symmetric format with bf16 scales of the long-context drafter workload.
+//
 // All kernels read the forward's row count and position from the device
 // state, so a round needs no host round-trip; rows beyond the forward's
 // count are written as zeros, which keeps every padded GEMM column zero.
