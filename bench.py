@@ -216,7 +216,7 @@ class OracleRoundSample:
                          np.moveaxis(np32(kv[0, 1]), 0, 1))
         self.h = np.random.default_rng(0).standard_normal((B, H))
         O.linear(self.h, self.embed)                       # warm-up, untimed
-        self.t = {}
+        self.t = {}                                        # piece -> every timed run (s)
         self.wall = self.cpu = 0.0                         # over every timed piece
 
     def time_piece(self, name: str) -> float:
@@ -232,11 +232,24 @@ class OracleRoundSample:
         else:
             x = self.embed[self.np.arange(1, B + 1)].astype(self.np.float64)
             O.target_layer(x, self.tl, self.cfg, list(range(n, n + B)), self.cache, 0)
-        self.t[name] = time.perf_counter() - tic
+        dt = time.perf_counter() - tic
         c1 = os.times()
-        self.wall += self.t[name]
+        self.t.setdefault(name, []).append(dt)
+        self.wall += dt
         self.cpu += (c1.user - c0.user) + (c1.system - c0.system)
-        return self.t[name]
+        return dt
+
+    def time_for(self, seconds: float, max_sets: int = 40) -> None:
+        """Times every piece in turn, set after set, until `seconds` of wall
+        time have gone into the timed pieces (at least two sets)."""
+        sets = 0
+        while sets < 2 or (self.wall < seconds and sets < max_sets):
+            for piece in self.PIECES:
+                self.time_piece(piece)
+            sets += 1
+
+    def _med(self, name: str) -> float:
+        return statistics.median(self.t[name])
 
     def threads_used(self) -> float:
         """Process CPU time over wall time of the timed pieces: the number of
@@ -244,13 +257,18 @@ class OracleRoundSample:
         return self.cpu / self.wall if self.wall > 0 else 0.0
 
     def round_s(self) -> float:
-        t, w = self.t, self.w
+        """Round time from the median of each piece's runs so far."""
+        w = self.w
+        t = {k: self._med(k) for k in self.PIECES}
         t_draft_layer = max(0.0, t["draft"] - t["fc"] - t["head"])
         return t["fc"] + w.drf_layers * t_draft_layer + w.tgt_layers * t["target"] + 2 * t["head"]
 
     def describe(self) -> str:
-        t, w = self.t, self.w
-        return (f"timed pieces, fp64 numpy (OpenBLAS): fc context re-projection over "
+        w = self.w
+        t = {k: self._med(k) for k in self.PIECES}
+        runs = min(len(v) for v in self.t.values())
+        return (f"timed pieces (median of >= {runs} runs each, {self.wall:.1f} s of timed wall "
+                f"time in all), fp64 numpy (OpenBLAS): fc context re-projection over "
                 f"{w.prompt_len} taps {t['fc']:.2f} s; 1-layer drafter forward {t['draft']:.2f} s; "
                 f"1 of {w.tgt_layers} target layers verifying {w.block} rows over a "
                 f"{w.prompt_len}-position cache {t['target']:.2f} s; one {w.vocab}-row LM head "
@@ -472,8 +490,7 @@ def run_ours(args):
         result["workloads"] = measure_workloads(args.steps, args.warmup, model_for_sweep)
     if not args.no_cpu_baseline and rank == 0:
         osmp = OracleRoundSample(E2E_BF16)
-        for piece in osmp.PIECES:
-            osmp.time_piece(piece)
+        osmp.time_for(12.0)
         result["cpu_baseline"] = {"value": round(1.0 / osmp.round_s(), 6), "unit": "rounds/s",
                                   "cores": cpu_cores(), "kind": "oracle",
                                   "sample": osmp.describe()}
