@@ -3,7 +3,8 @@
 The round does not shard: under torchrun each rank runs an independent
 replica, and the whole job's figure is the rounds (and tokens) of all ranks
 over the slowest rank's timed region.  These tests run that reduction on two
-CPU processes, and check that the reference arm prints from rank 0 only.
+CPU processes, check that the reference arm prints from rank 0 only, and
+that its one JSON line keeps the bench contract.
 """
 
 import json
@@ -61,3 +62,27 @@ def test_reference_arm_other_ranks_exit_without_work():
                        timeout=120)
     assert p.returncode == 0, p.stderr
     assert p.stdout.strip() == ""
+
+
+def test_reference_arm_line_keeps_the_contract():
+    # one step of the oracle arm on this host: the JSON line's keys, the
+    # cpu_baseline describing this run and e2e equal to the line's own value
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert p.returncode == 0, p.stderr
+    lines = [l for l in p.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["steps"] == 1 and d["warmup"] == 0
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["unit"] == "rounds/s"
+    assert d["config"]["workload"].startswith("e2e_bf16")
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
