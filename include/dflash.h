@@ -398,11 +398,13 @@ int dflash_linear_noalloc(const void* w, const void* x, int32_t n, int32_t k, fl
  * [M][N].  M >= 1, N >= 1, K a multiple of 64, every pointer 16-byte
  * aligned.  err: device int32[2], zero before the call; a kernel wait that
  * timed out writes 1 and a site number there (kernels never trap).  The library's
- * kernel for the dense step of the round's pipeline: the drafter's
- * context-window ingest (the fc re-projection of the window's tap rows and
- * each draft layer's context K/V, "[RFC] DFlash", "Requested changes" 3,
- * the persistent draft KV cache), where the rows number in the hundreds or
- * thousands.  Errors: ARG, CUDA.
+ * kernel for the dense steps of the pipeline, where the rows number in the
+ * hundreds or thousands: the drafter's context-window ingest (the fc
+ * re-projection of the window's tap rows and each draft layer's context
+ * K/V, "[RFC] DFlash", "Requested changes" 3, the persistent draft KV
+ * cache) and the target's prompt prefill (every projection of the prompt
+ * rows before the last 16-row chunk).  The binding checks dtypes, shapes
+ * and devices before the call.  Errors: ARG, CUDA.
  */
 int dflash_linear_dense(const void* w, const void* x, const void* x_lo, int32_t m, int32_t n, int32_t k,
                         float* y, int32_t* err, dflash_stream_t stream);
