@@ -488,7 +488,7 @@ def run_ours(args):
         if inj16:
             result["accepted_tok_s_injected"] = inj16["accepted_tok_s"]
         result["workloads"] = measure_workloads(args.steps, args.warmup, model_for_sweep)
-    if not args.no_cpu_baseline and rank == 0:
+    if not args.no_cpu_baseline and rank == 0 and world == 1:   # the oracle baseline: N = 1 only
         osmp = OracleRoundSample(E2E_BF16)
         osmp.time_for(12.0)
         result["cpu_baseline"] = {"value": round(1.0 / osmp.round_s(), 6), "unit": "rounds/s",
