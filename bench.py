@@ -42,6 +42,12 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--ncu-tap", type=int, default=0, metavar="ROWS",
+                    help="run the hc tap reduce (4 layers, hc 4, hidden 4096) at ROWS rows, "
+                         "3 launches, for an ncu capture")
+    ap.add_argument("--int4", action="store_true",
+                    help="with --ncu-rounds: the e2e workload with every model in INT4 group-64")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
@@ -162,122 +168,247 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
 
 
+def gemm_source_sha() -> str:
+    """Hash of the skinny GEMM's sources: a committed traffic figure counts
+    only while the kernel it was captured on is unchanged."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "gemm_dev.cuh", "gemm.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "block_diffusion_speculative_gather_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_from_profiles():
-    """Per-launch DRAM bytes of the GEMM from the committed ncu summary, if any."""
+    """Per-launch DRAM bytes of the GEMM from the committed ncu summary, if it
+    was captured on the current kernel sources."""
     p = os.path.join(ROOT, "profiles", "gemm_skinny_traffic.json")
     if os.path.exists(p):
         try:
-            return json.load(open(p))
+            d = json.load(open(p))
         except Exception:
             return None
+        if d.get("kernel_sha") == gemm_source_sha():
+            return d
     return None
 
 
-# ----------------------------------------------------------------- oracle sample
+# ----------------------------------------------------------------- the oracle on the host
 
-class OracleRoundSample:
-    """The CPU oracle timed on a bounded sample of one speculative round of
-    workload `w`, extrapolated to the full round.
+def _np32(t):
+    return t.detach().float().numpy()
 
-    Pieces: the drafter's uncached context re-projection (fc over the
-    prompt's taps), one whole 1-layer drafter forward (fc + layer + LM head),
-    one target decoder layer verifying 16 rows over a synthetic
-    prompt-length KV cache, and one LM head over the full vocabulary.
-    Round time = t_fc + drf_layers * t_draft_layer + tgt_layers *
-    t_target_layer + 2 * t_head.  One untimed LM-head call warms the
-    allocator first.
-    """
 
-    PIECES = ("head", "fc", "draft", "target")
+def oracle_weights(w, model=None):
+    """The oracle's weights of workload w, from the seeded generators (the
+    values the GPU arm streams): target layers and drafter, INT4 layers as
+    the oracle's own quantise-dequantise of the same fp32 draws."""
+    from block_diffusion_speculative_gather_gb300 import synth
+    from oracle import dflash_oracle as O
+    m = model if model is not None else synth.ModelTensors(w)
 
-    def __init__(self, w):
+    def layers(ls, int4):
+        out = []
+        for lw in ls:
+            d = {}
+            for k, t in lw.items():
+                a = _np32(t)
+                if int4 and k in synth.LAYER_KEYS:
+                    a = O.dequant_int4_g64(*O.quantize_int4_g64(a))
+                d[k] = a
+            out.append(d)
+        return out
+
+    embed = _np32(m.embed)
+    tw = O.TargetWeights(embed, layers(m.tgt, w.tgt_int4), _np32(m.final_norm_t)) \
+        if w.tgt_layers else None
+    dw = O.DraftWeights(layers(m.drf, w.drf_int4), _np32(m.fc), _np32(m.ctx_norm),
+                        _np32(m.final_norm_d)) if w.drf_layers else None
+    cfg = O.OracleConfig(hidden=w.hidden, n_q=w.n_q, n_kv=w.n_kv, head_dim=w.head_dim, ffn=w.ffn,
+                         vocab=w.vocab, tgt_layers=w.tgt_layers, drf_layers=w.drf_layers,
+                         tap_layers=list(w.tap_layers), block=w.block, window=w.window,
+                         max_seq=w.max_seq, eos_id=w.eos_id, rms_eps=w.rms_eps,
+                         rope_theta=w.rope_theta, ctx_norm=w.ctx_norm)
+    return tw, dw, cfg, embed
+
+
+def synthetic_cache(n_layers, n_kv, n_pos, head_dim, name):
+    """The oracle's KV cache holding N(0,1) K/V (rounded to fp16, the GPU
+    caches' type) at positions [0, n_pos) of every layer."""
+    import numpy as np
+    from block_diffusion_speculative_gather_gb300 import synth
+    from oracle import dflash_oracle as O
+    cache = O.KVCache(n_layers, n_kv, head_dim)
+    for l in range(n_layers):
+        kv = synth.normal((2, n_kv, n_pos, head_dim), 1.0, synth.KV_SEED, f"{name}.{l}")
+        kv = kv.astype(np.float16).astype(np.float32)
+        cache.write(l, range(n_pos), np.moveaxis(kv[0], 0, 1), np.moveaxis(kv[1], 0, 1))
+    return cache
+
+
+class OracleRounds:
+    """Real speculative rounds of the CPU oracle from a synthetic state: the
+    target's cache holds N(0,1) K/V at positions [0, n) and the drafter's
+    context N(0,1) tap rows there (a 1024-token prefill through the oracle
+    would take hours), the pending token a seeded id.  One round is what the
+    oracle's own loop (spec_rounds) does per round: draft_forward over the
+    tap context, target_forward of [t_n, d_1..d_m], argmax, accept, KV
+    rollback and the tap rows of the emitted tokens appended to the
+    context."""
+
+    def __init__(self, tw, dw, cfg, n):
         import numpy as np
-        import torch
         from block_diffusion_speculative_gather_gb300 import synth
         from oracle import dflash_oracle as O
-        self.O, self.np, self.w = O, np, w
-        H, B, n = w.hidden, w.block, w.prompt_len
-        self.cfg = O.OracleConfig(hidden=H, n_q=w.n_q, n_kv=w.n_kv, head_dim=w.head_dim,
-                                  ffn=w.ffn, vocab=w.vocab, tgt_layers=1, drf_layers=1,
-                                  tap_layers=[0], block=B, window=w.window)
-        np32 = lambda t: t.float().numpy()
-        layers = lambda prefix: [{k: np32(v) for k, v in lw.items()} for lw in
-                                 synth.decoder_layers(prefix, 1, H, w.n_q, w.n_kv, w.head_dim,
-                                                      w.ffn, torch.bfloat16)]
-        self.embed = np32(synth.matrix("embed", w.vocab, H, torch.bfloat16))
-        fc = np32(synth.matrix("fc", H, w.n_taps * H, torch.bfloat16))
-        self.taps = np32(synth.tap_rows(n, w.n_taps * H))
-        ones = np.ones(H, np.float32)
-        self.tl = layers("tgt")[0]
-        self.dw = O.DraftWeights(layers("drf"), fc, ones, ones)
-        kv = synth.kv_rows(1, w.n_kv, n, w.head_dim)
-        self.cache = O.KVCache(1, w.n_kv, w.head_dim)
-        self.cache.write(0, range(n), np.moveaxis(np32(kv[0, 0]), 0, 1),
-                         np.moveaxis(np32(kv[0, 1]), 0, 1))
-        self.h = np.random.default_rng(0).standard_normal((B, H))
-        O.linear(self.h, self.embed)                       # warm-up, untimed
-        self.t = {}                                        # piece -> every timed run (s)
-        self.wall = self.cpu = 0.0                         # over every timed piece
+        self.O, self.np = O, np
+        self.tw, self.dw, self.cfg, self.n = tw, dw, cfg, n
+        taps = synth.tap_rows(n, cfg.n_taps * cfg.hidden)
+        self.taps = list(_np32(taps))
+        self.cache = synthetic_cache(len(tw.layers), cfg.n_kv, n, cfg.head_dim, "oracle-e2e-kv")
+        self.t_n = int(synth.uniform_ids(1, cfg.vocab, seed=synth.PROMPT_SEED, name="t_n")[0])
+        self.emitted = 0
+        self.rounds = 0
 
-    def time_piece(self, name: str) -> float:
-        O, w, n, B = self.O, self.w, self.w.prompt_len, self.w.block
-        c0 = os.times()
+    def round(self) -> float:
+        O, np = self.O, self.np
         tic = time.perf_counter()
-        if name == "head":
-            O.linear(self.h, self.embed)
-        elif name == "fc":
-            O.draft_context(self.dw, self.cfg, self.taps)
-        elif name == "draft":
-            O.draft_forward(self.dw, self.embed, self.cfg, self.taps, 17, n, B)
-        else:
-            x = self.embed[self.np.arange(1, B + 1)].astype(self.np.float64)
-            O.target_layer(x, self.tl, self.cfg, list(range(n, n + B)), self.cache, 0)
-        dt = time.perf_counter() - tic
-        c1 = os.times()
-        self.t.setdefault(name, []).append(dt)
-        self.wall += dt
-        self.cpu += (c1.user - c0.user) + (c1.system - c0.system)
-        return dt
+        _, d = O.draft_forward(self.dw, self.tw.embed, self.cfg, np.stack(self.taps), self.t_n,
+                               self.n, self.cfg.block, lm_head=self.tw.lm_head)
+        logits, vtaps = O.target_forward(self.tw, self.cfg, [self.t_n] + d, self.n, self.cache)
+        y = [O.argmax_lowest(logits[i]) for i in range(len(d) + 1)]
+        a, emitted, _ = O.accept(d, y, self.cfg.eos_id)
+        self.cache.truncate(self.n + len(emitted))
+        self.taps.extend(vtaps[i] for i in range(len(emitted)))
+        self.n += len(emitted)
+        self.t_n = emitted[-1]
+        self.emitted += len(emitted)
+        self.rounds += 1
+        return time.perf_counter() - tic
 
-    def time_for(self, seconds: float, max_sets: int = 40) -> None:
-        """Times every piece in turn, set after set, until `seconds` of wall
-        time have gone into the timed pieces (at least two sets)."""
-        sets = 0
-        while sets < 2 or (self.wall < seconds and sets < max_sets):
-            for piece in self.PIECES:
-                self.time_piece(piece)
-            sets += 1
 
-    def _med(self, name: str) -> float:
-        return statistics.median(self.t[name])
-
-    def threads_used(self) -> float:
-        """Process CPU time over wall time of the timed pieces: the number of
-        host threads the oracle kept busy on average (BLAS threads included)."""
-        return self.cpu / self.wall if self.wall > 0 else 0.0
-
-    def round_s(self) -> float:
-        """Round time from the median of each piece's runs so far."""
-        w = self.w
-        t = {k: self._med(k) for k in self.PIECES}
-        t_draft_layer = max(0.0, t["draft"] - t["fc"] - t["head"])
-        return t["fc"] + w.drf_layers * t_draft_layer + w.tgt_layers * t["target"] + 2 * t["head"]
-
-    def describe(self) -> str:
-        w = self.w
-        t = {k: self._med(k) for k in self.PIECES}
-        runs = min(len(v) for v in self.t.values())
-        return (f"timed pieces (median of >= {runs} runs each, {self.wall:.1f} s of timed wall "
-                f"time in all), fp64 numpy (OpenBLAS): fc context re-projection over "
-                f"{w.prompt_len} taps {t['fc']:.2f} s; 1-layer drafter forward {t['draft']:.2f} s; "
-                f"1 of {w.tgt_layers} target layers verifying {w.block} rows over a "
-                f"{w.prompt_len}-position cache {t['target']:.2f} s; one {w.vocab}-row LM head "
-                f"{t['head']:.2f} s; round extrapolated by layer count; {self.threads_used():.1f} "
-                f"host threads busy on average (CPU time / wall time)")
+def host_cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 def cpu_cores() -> int:
-    return int(os.environ.get("OPENBLAS_NUM_THREADS", 0) or os.cpu_count() or 1)
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def cpu_baseline_worker():
+    """The cpu_baseline leg, run as its own process with one BLAS thread:
+    prepares the workloads' oracle weights and synthetic states, waits for
+    a line on stdin (the GPU measurements are over), then pins itself to one
+    core and times one real unit of each workload, printing one JSON line."""
+    import numpy as np
+    from block_diffusion_speculative_gather_gb300 import synth
+    from block_diffusion_speculative_gather_gb300.configs import DRAFT_INT4, E2E_BF16, HC_SWEEP
+    from oracle import dflash_oracle as O
+    prep0 = time.perf_counter()
+    w = E2E_BF16
+    tw, dw, cfg, embed = oracle_weights(w)
+    rounds = OracleRounds(tw, dw, cfg, w.prompt_len)
+    ctx = np.stack(rounds.taps)
+    # the INT4 drafter (long-context workload): the same draws quantised
+    w4 = DRAFT_INT4
+    m4 = synth.ModelTensors(w4.with_(tgt_layers=0))
+    _, dw4, cfg4, _ = oracle_weights(w4, m4)
+    del m4
+    lo = w4.n_ctx - w4.window
+    taps4 = np.zeros((w4.n_ctx, cfg4.n_taps * cfg4.hidden), np.float32)
+    taps4[lo:] = _np32(synth.tap_rows(w4.window, cfg4.n_taps * cfg4.hidden, name="taps-window"))
+    # the verify sweep's 16384-position synthetic cache
+    n16 = HC_SWEEP.prompt_len
+    cache16 = synthetic_cache(len(tw.layers), cfg.n_kv, n16, cfg.head_dim, "oracle-16k-kv")
+    cfg16 = O.OracleConfig(**{**cfg.__dict__, "max_seq": HC_SWEEP.max_seq})
+    drafts = synth.uniform_ids(15, cfg.vocab, seed=5).tolist()
+    prep_s = time.perf_counter() - prep0
+    sys.stdout.write(json.dumps({"ready": True, "prep_s": round(prep_s, 1)}) + "\n")
+    sys.stdout.flush()
+    sys.stdin.readline()                          # the GPU measurements are over
+    core = max(os.sched_getaffinity(0))
+    os.sched_setaffinity(0, {core})
+    res, cpu0, wall0 = {}, os.times(), time.perf_counter()
+
+    def timed(fn):
+        t = time.perf_counter()
+        fn()
+        return time.perf_counter() - t
+
+    res["e2e_bf16_round_s"] = rounds.round()
+    res["draft_bf16_round_s"] = timed(lambda: O.draft_forward(dw, embed, cfg, ctx, 4242, w.prompt_len,
+                                                              16))
+    res["draft_int4_round_s"] = timed(lambda: O.draft_forward(dw4, embed, cfg4, taps4, 4242,
+                                                              w4.n_ctx, w4.block))
+    sweep = {}
+    for T in (1, 16):
+        sweep[str(T)] = timed(lambda: O.target_forward(tw, cfg16, [17] + drafts[:T - 1], n16, cache16))
+        cache16.truncate(n16)
+    res["verify_16k_s_by_T"] = sweep
+    cpu1, wall = os.times(), time.perf_counter() - wall0
+    res["threads_busy"] = round(((cpu1.user - cpu0.user) + (cpu1.system - cpu0.system)) / wall, 2)
+    res["core"] = core
+    res["prep_s"] = round(prep_s, 1)
+    sys.stdout.write(json.dumps(res) + "\n")
+    sys.stdout.flush()
+
+
+class CpuBaseline:
+    """Starts the cpu_baseline worker (one BLAS thread) so that its
+    preparation overlaps the GPU measurements; finish() lets it time its
+    units with the GPU work over and returns the cpu_baseline object."""
+
+    def __init__(self):
+        env = dict(os.environ)
+        for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+            env[k] = "1"
+        env["CUDA_VISIBLE_DEVICES"] = ""          # the worker never touches a GPU
+        self.p = subprocess.Popen([sys.executable, os.path.abspath(__file__), "--cpu-baseline-worker"],
+                                  stdin=subprocess.PIPE, stdout=subprocess.PIPE, text=True, env=env,
+                                  cwd=ROOT)
+
+    def finish(self, timeout_s=900.0):
+        try:
+            ready = json.loads(self.p.stdout.readline() or "{}")
+            if not ready.get("ready"):
+                raise RuntimeError("worker not ready")
+            self.p.stdin.write("go\n")
+            self.p.stdin.flush()
+            line = self.p.stdout.readline()
+            self.p.wait(timeout=timeout_s)
+            r = json.loads(line)
+        except Exception as e:                    # pragma: no cover
+            self.p.kill()
+            return {"value": None, "unit": "rounds/s", "cores": 1, "kind": "oracle",
+                    "sample": f"the oracle worker failed: {e}"}
+        e2e = r["e2e_bf16_round_s"]
+        return {
+            "value": round(1.0 / e2e, 6), "unit": "rounds/s", "cores": 1, "kind": "oracle",
+            "sample": ("one real round of the e2e workload (drafter forward re-projecting the "
+                       "1024-row tap context, 16-row verify of the 36-layer target over a "
+                       "1024-position synthetic cache, acceptance, rollback, tap commit) from a "
+                       f"synthetic state: {e2e:.2f} s; fp64 numpy, one BLAS thread, pinned to "
+                       f"core {r['core']} ({r['threads_busy']} threads busy)"),
+            "host_cpu": host_cpu_model(), "host_cores": os.cpu_count(),
+            "per_config": {
+                "draft_bf16": {"unit": "draft rounds/s", "value": round(1.0 / r["draft_bf16_round_s"], 5),
+                               "s": round(r["draft_bf16_round_s"], 3),
+                               "what": "one drafter forward, block 16, 1024 context tap rows"},
+                "draft_int4": {"unit": "draft rounds/s", "value": round(1.0 / r["draft_int4_round_s"], 5),
+                               "s": round(r["draft_int4_round_s"], 3),
+                               "what": "one INT4 drafter forward, block 8, window 2048 of 16384 tap rows"},
+                "verify_sweep_16k": {"unit": "ms per verify", "by_T": {
+                    T: round(v * 1e3, 1) for T, v in r["verify_16k_s_by_T"].items()},
+                    "what": "one 36-layer verify of T rows over a 16384-position synthetic cache"},
+            },
+        }
 
 
 # ----------------------------------------------------------------- our arm
@@ -292,9 +423,26 @@ def run_ours(args):
     from block_diffusion_speculative_gather_gb300.runtime import DFlash
 
     rank, world, local = rank_info()
+    # the oracle baseline (N = 1 only): its worker prepares while the GPU runs
+    cpu_leg = None
+    if not (args.no_cpu_baseline or args.ncu_dense or args.ncu_prefill or args.ncu_rounds
+            or args.ncu_tap or args.layers) and rank == 0 and world == 1:
+        cpu_leg = CpuBaseline()
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
+    if args.ncu_tap:
+        from block_diffusion_speculative_gather_gb300.configs import HC_TAP
+        hc, rows = HC_TAP, args.ncu_tap
+        gen = torch.Generator("cuda").manual_seed(2)
+        streams = [torch.randn(rows, hc["hc"] * hc["hidden"], device="cuda", generator=gen)
+                   .to(torch.bfloat16) for _ in range(hc["n_layers"])]
+        outb = torch.empty(rows, hc["n_layers"] * hc["hidden"], device="cuda")
+        for _ in range(3):
+            capi.dflash_tap_reduce(streams, rows, hc["hc"], hc["hidden"], outb)
+        torch.cuda.synchronize()
+        print(f"ncu tap done: {rows} rows", flush=True)
+        return
     if args.ncu_dense:
         m, n, k = args.ncu_dense
         gen = torch.Generator(device="cuda").manual_seed(9)
@@ -309,6 +457,8 @@ def run_ours(args):
         print(f"ncu dense done: {m} x {n} x {k}", flush=True)
         return
     w = E2E_BF16
+    if args.int4:
+        w = w.with_(name="e2e_int4", tgt_int4=True, lm_int4=True, drf_int4=True)
     if args.layers:
         from block_diffusion_speculative_gather_gb300.configs import evenly_spaced_taps
         w = w.with_(tgt_layers=args.layers,
@@ -418,9 +568,17 @@ def run_ours(args):
         prof_launch += p.gemm_launches
     capi.dflash_profile(dec.ctx, 0)
     peak, peak_src = measured_peak()
-    achieved = prof_bytes / (prof_ms / 1e3) / 1e9 if prof_ms > 0 else None
+    # The GEMM family's roofline from the graph-timed round itself (PDL
+    # intact): its algorithmic bytes per launch over the round's time split
+    # evenly across its launches.  The round also runs the attention and the
+    # row kernels, so that duration is an upper bound of the GEMMs' own and
+    # `achieved` a lower bound; it follows by hand from ms_per_step.
+    gemm_per_round = prof_launch / args.steps if args.steps else 0
+    bytes_per_round = prof_bytes / args.steps if args.steps else 0.0
+    round_s = (ms / args.steps) / 1e3
+    achieved = bytes_per_round / round_s / 1e9 if round_s > 0 else None
+    event_gbs = prof_bytes / (prof_ms / 1e3) / 1e9 if prof_ms > 0 else None
     traffic = traffic_from_profiles()
-
     # verify cost against rows (plain greedy step = 1 row, round = 16 rows)
     t1row = None
     gg = torch.cuda.CUDAGraph()
@@ -459,19 +617,24 @@ def run_ours(args):
             capi.dflash_attention_form(dec.ctx, i)] for i, m in ((0, "target"), (1, "drafter"))},
         "clocks": clocks,
         "roofline": {
-            "bound": "hbm", "kernel": "gemm_skinny_kernel (all weight-streaming GEMMs of a round)",
+            "bound": "hbm",
+            "kernel": f"gemm_skinny_kernel (the {gemm_per_round:.0f} weight-streaming GEMM launches "
+                      "of a round)",
             "achieved": round(achieved, 1) if achieved else None, "peak": peak,
             "peak_source": peak_src, "unit": "GB/s",
             "frac": round(achieved / peak, 4) if achieved else None,
             "traffic": traffic.get("dram_bytes_per_launch") if traffic else None,
-            "gemm_share_of_round": round(prof_ms / ms, 4) if ms else None,
-            "bytes_per_round": prof_bytes / args.steps,
-            "round_bound_gbs": round(prof_bytes / (ms / 1e3) / 1e9, 1) if ms else None,
-            "note": "achieved: each GEMM timed by CUDA event nodes in a captured round; the "
-                    "events break the programmatic-dependent-launch overlap, so each GEMM's "
-                    "duration also holds its start-up behind the previous kernel (the sum can "
-                    "exceed the round: gemm_share_of_round > 1) and achieved is a lower bound; "
-                    "round_bound_gbs (the GEMMs' bytes over the whole round's time) is another",
+            "traffic_source": traffic.get("summary") if traffic else
+                              "null: no ncu capture of the current GEMM kernel",
+            "bytes_per_launch": round(bytes_per_round / gemm_per_round) if gemm_per_round else None,
+            "launch_us": round(round_s * 1e6 / gemm_per_round, 3) if gemm_per_round else None,
+            "bytes_per_round": bytes_per_round,
+            "event_timed_gbs": round(event_gbs, 1) if event_gbs else None,
+            "note": "achieved = the GEMMs' algorithmic bytes per launch / (graph-timed round time "
+                    "/ GEMM launches per round), i.e. bytes_per_round / ms_per_step: the round also "
+                    "holds the attention and row kernels, so this is a lower bound of the GEMMs' "
+                    "own rate.  event_timed_gbs: each GEMM bracketed by CUDA event nodes (which "
+                    "break the dependent-launch overlap), another lower bound",
         },
     }
     if args.layers:
@@ -488,12 +651,8 @@ def run_ours(args):
         if inj16:
             result["accepted_tok_s_injected"] = inj16["accepted_tok_s"]
         result["workloads"] = measure_workloads(args.steps, args.warmup, model_for_sweep)
-    if not args.no_cpu_baseline and rank == 0 and world == 1:   # the oracle baseline: N = 1 only
-        osmp = OracleRoundSample(E2E_BF16)
-        osmp.time_for(12.0)
-        result["cpu_baseline"] = {"value": round(1.0 / osmp.round_s(), 6), "unit": "rounds/s",
-                                  "cores": cpu_cores(), "kind": "oracle",
-                                  "sample": osmp.describe()}
+    if cpu_leg is not None:                     # the oracle baseline: N = 1 only
+        result["cpu_baseline"] = cpu_leg.finish()
     if rank == 0:
         print(json.dumps(result), flush=True)
     dec.close()
@@ -908,35 +1067,44 @@ def e2e_measure(dec, w, prompt, world=1, barrier=lambda: None):
 # ----------------------------------------------------------------- reference arm
 
 def run_reference(args):
-    """The oracle arm: each step times one piece of the round sample in
-    rotation (head, fc, draft, target); the reported round time is
-    re-extrapolated from the latest time of every piece after each step."""
+    """The oracle arm: every step is one real speculative round of the e2e
+    workload by the CPU oracle (OracleRounds: drafter forward, 16-row
+    verify, acceptance, rollback, tap commit) from a synthetic 1024-position
+    state, on the host's cores (BLAS threads as the library starts them)."""
     rank, world, _ = rank_info()
     if rank != 0:
         return
     from block_diffusion_speculative_gather_gb300.configs import E2E_BF16
-    osmp = OracleRoundSample(E2E_BF16)
-    for piece in osmp.PIECES:              # every piece timed once before the steps
-        osmp.time_piece(piece)
-    rounds = []
-    for i in range(args.warmup + args.steps):
-        osmp.time_piece(osmp.PIECES[i % len(osmp.PIECES)])
-        if i >= args.warmup:
-            rounds.append(osmp.round_s())
-    mean = sum(rounds) / len(rounds)
-    v = 1.0 / mean
+    w = E2E_BF16
+    tw, dw, cfg, _ = oracle_weights(w)
+    rounds = OracleRounds(tw, dw, cfg, w.prompt_len)
+    for _ in range(args.warmup):
+        rounds.round()
+    e0 = rounds.emitted
+    c0 = os.times()
+    t = 0.0
+    for _ in range(args.steps):
+        t += rounds.round()
+    c1 = os.times()
+    busy = ((c1.user - c0.user) + (c1.system - c0.system)) / t if t > 0 else 0.0
+    v = args.steps / t
+    sample = (f"each step one real round of the e2e workload by the oracle (drafter forward "
+              f"re-projecting the tap context, 16-row verify of the 36-layer target, acceptance, "
+              f"rollback, tap commit) from a synthetic 1024-position state; fp64 numpy, "
+              f"{cpu_cores()} host cores, {busy:.1f} threads busy on average; host CPU "
+              f"{host_cpu_model()}")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "rounds/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(mean * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": round(t / args.steps * 1e3, 1), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same generators as ours)",
         "config": workload_config(
-            E2E_BF16, world,
-            timing="CPU oracle (fp64) on the host cores: each step times one piece of a layer "
-                   "sample of the round, the round extrapolated by layer count",
+            w, world,
+            timing="CPU oracle (fp64) on the host cores, one real round per step, wall clock",
             l2="not applicable (host run)"),
+        "accepted_tok_s": round((rounds.emitted - e0) / t, 6),
         "cpu_baseline": {"value": round(v, 6), "unit": "rounds/s", "cores": cpu_cores(),
-                         "kind": "oracle", "sample": osmp.describe()},
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(v, 6), "unit": "rounds/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -944,7 +1112,9 @@ def run_reference(args):
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.cpu_baseline_worker:
+        cpu_baseline_worker()
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -98,8 +98,8 @@ def _load() -> C.CDLL:
         "dflash_selftest_timeout": (C.c_int, [vp, i64, vp]),
         "dflash_adopt_kv": (C.c_int, [vp, i32, i32, i32, vp]),
         "dflash_linear_workspace_bytes": (sz, [i32, i32]),
-        "dflash_linear": (C.c_int, [vp, vp, i32, i32, vp, vp, sz, vp]),
-        "dflash_linear_noalloc": (C.c_int, [vp, vp, i32, i32, vp, vp]),
+        "dflash_linear": (C.c_int, [vp, vp, i32, i32, vp, vp, sz, vp, vp]),
+        "dflash_linear_noalloc": (C.c_int, [vp, vp, i32, i32, vp, vp, vp]),
         "dflash_profile_phases": (i32, [vp, i32, vp, i32]),
         "dflash_progress": (C.c_int, [vp, vp, vp]),
         "dflash_attention_form": (C.c_int, [vp, i32]),
@@ -284,20 +284,28 @@ def _linear_operands(w, x, y):
     return n, k
 
 
-def dflash_linear(w, x, y, workspace, stream=None):
+def dflash_linear(w, x, y, workspace, err, stream=None):
+    """y = x w^T (16 rows); err (int32[2] on the device) receives the GEMM's
+    error words after it: {0, 0}, or {1, site} when a bounded wait ran out."""
+    import torch
     n, k = _linear_operands(w, x, y)
     _need(workspace, "workspace", None, None)
-    _on_gpu(w=w, x=x, y=y, workspace=workspace)
+    _need(err, "err", (torch.int32,), (2,))
+    _on_gpu(w=w, x=x, y=y, workspace=workspace, err=err)
     check(lib.dflash_linear(_ptr(w), _ptr(x), n, k, _ptr(y), _ptr(workspace),
-                            workspace.numel() * workspace.element_size(), _stream(stream)))
+                            workspace.numel() * workspace.element_size(), _ptr(err),
+                            _stream(stream)))
 
 
-def dflash_linear_noalloc(w, x, y, stream=None):
+def dflash_linear_noalloc(w, x, y, err, stream=None):
     """y = x w^T like dflash_linear, with the library's fixed scratch instead
-    of a caller workspace (for callers that cannot allocate device memory)."""
+    of a caller workspace (for callers that cannot allocate device memory);
+    err as in dflash_linear."""
+    import torch
     n, k = _linear_operands(w, x, y)
-    _on_gpu(w=w, x=x, y=y)
-    check(lib.dflash_linear_noalloc(_ptr(w), _ptr(x), n, k, _ptr(y), _stream(stream)))
+    _need(err, "err", (torch.int32,), (2,))
+    _on_gpu(w=w, x=x, y=y, err=err)
+    check(lib.dflash_linear_noalloc(_ptr(w), _ptr(x), n, k, _ptr(y), _ptr(err), _stream(stream)))
 
 
 def dflash_profile_phases(ctx, which: int):

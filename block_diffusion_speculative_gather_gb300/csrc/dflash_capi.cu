@@ -879,6 +879,40 @@ int make_linear_maps(GemmMaps* maps, const void* w, const void* x, int n, int k)
     return r;
 }
 
+int run_linear_store(const void* w, const void* x, int n, int k, float* y, float* slots,
+                     int* counters, DevState* st, void* clear, size_t clear_bytes, int32_t* err,
+                     int sms, cudaStream_t s) {
+    GemmMaps maps;
+    int r = make_linear_maps(&maps, w, x, n, k);
+    if (r) return r;
+    GemmArgs a;
+    memset(&a, 0, sizeof a);
+    a.N = n;
+    a.K = k;
+    a.n_tiles = n / GEMM_BN;
+    a.kb = k / 64;
+    a.seg_rows[0] = n;
+    a.n_seg = 1;
+    a.out = y;
+    a.ldo = n;
+    a.slots = slots;
+    a.counters = counters;
+    a.st = st;
+    // the error words this call reports start at zero (and whatever else the
+    // caller asked to clear: the fixed scratch's tickets)
+    cudaError_t e = cudaMemsetAsync(clear, 0, clear_bytes, s);
+    if (e != cudaSuccess) return report_error(DFLASH_ERR_CUDA, "scratch clear: %s", cudaGetErrorString(e));
+    const long long units = (long long)a.n_tiles * a.kb;
+    const int ctas = sms * DFL_GEMM_CTAS_PER_SM;
+    const int grid = (int)(units < ctas ? units : ctas);
+    const int le = launch_gemm(WF_BF16, EPI_STORE, XT_BF16, maps, a, grid, s);
+    if (le) return report_error(DFLASH_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString((cudaError_t)le));
+    // the kernel's (code, site) words, after it, into the caller's err
+    e = cudaMemcpyAsync(err, &st->err, 2 * sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return report_error(DFLASH_ERR_CUDA, "error-word copy: %s", cudaGetErrorString(e));
+    return DFLASH_OK;
+}
+
 }  // namespace dfl
 
 // ====================================================================== C ABI
@@ -1786,12 +1820,12 @@ int dflash_linear_dense(const void* w, const void* x, const void* x_lo, int32_t 
 }
 
 int dflash_linear(const void* w, const void* x, int32_t n, int32_t k, float* y, void* workspace,
-                  size_t workspace_bytes, dflash_stream_t stream) {
-    if (!w || !x || !y || !workspace) return fail(DFLASH_ERR_ARG, "NULL argument");
+                  size_t workspace_bytes, int32_t* err, dflash_stream_t stream) {
+    if (!w || !x || !y || !workspace || !err) return fail(DFLASH_ERR_ARG, "NULL argument");
     const size_t need = dflash_linear_workspace_bytes(n, k);
     if (need == 0) return fail(DFLASH_ERR_ARG, "n %d k %d: n a multiple of 128, k of 64", n, k);
     if (workspace_bytes < need) return fail(DFLASH_ERR_ARG, "workspace %zu < %zu", workspace_bytes, need);
-    if (!aligned16(w) || !aligned16(x) || !aligned16(y) || !aligned16(workspace))
+    if (!aligned16(w) || !aligned16(x) || !aligned16(y) || !aligned16(workspace) || !aligned16(err))
         return fail(DFLASH_ERR_ARG, "misaligned buffer");
     if (int r0 = get_encode()) return r0;
     if (int r0 = pending_error()) return r0;
@@ -1799,32 +1833,12 @@ int dflash_linear(const void* w, const void* x, int32_t n, int32_t k, float* y, 
     CUDA_TRY(cudaGetDevice(&dev));
     CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     if (sms > 256) sms = 256;
-    GemmMaps maps;
-    memset(&maps, 0, sizeof maps);
-    int r = make_map(&maps.w[0], w, XT_BF16, k, n, GEMM_BN);
-    if (!r) r = make_map(&maps.x, x, XT_BF16, k, DFL_MAX_ROWS, DFL_MAX_ROWS);
-    if (r) return r;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    GemmArgs a;
-    memset(&a, 0, sizeof a);
-    a.N = n;
-    a.K = k;
-    a.n_tiles = n / GEMM_BN;
-    a.kb = k / 64;
-    a.seg_rows[0] = n;
-    a.n_seg = 1;
-    a.out = y;
-    a.ldo = n;
-    a.slots = reinterpret_cast<float*>(ws);
-    a.counters = reinterpret_cast<int*>(ws + align_up((size_t)MAX_SMS * 2 * GEMM_BN * DFL_MAX_ROWS * 4, 1024));
-    a.st = reinterpret_cast<DevState*>(ws + need - align_up(sizeof(DevState), 256));
-    const long long units = (long long)a.n_tiles * a.kb;
-    const int ctas = sms * DFL_GEMM_CTAS_PER_SM;
-    const int grid = (int)(units < ctas ? units : ctas);
-    const int e = launch_gemm(WF_BF16, EPI_STORE, XT_BF16, maps, a, grid,
-                              reinterpret_cast<cudaStream_t>(stream));
-    if (e) return fail(DFLASH_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString((cudaError_t)e));
-    return DFLASH_OK;
+    DevState* st = reinterpret_cast<DevState*>(ws + need - align_up(sizeof(DevState), 256));
+    return run_linear_store(
+        w, x, n, k, y, reinterpret_cast<float*>(ws),
+        reinterpret_cast<int*>(ws + align_up((size_t)MAX_SMS * 2 * GEMM_BN * DFL_MAX_ROWS * 4, 1024)),
+        st, &st->err, 2 * sizeof(int), err, sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int dflash_quantize_int4g64(const float* w, int32_t n, int32_t k, uint8_t* packed, uint16_t* scales,

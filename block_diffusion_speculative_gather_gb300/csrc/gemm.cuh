@@ -164,5 +164,13 @@ int launch_gemm(int wfmt, int epi, int xt, const GemmMaps& maps, const GemmArgs&
 // activation maps of a plain y = x w^T.
 int report_error(int code, const char* fmt, ...);
 int make_linear_maps(GemmMaps* maps, const void* w, const void* x, int n, int k);
+// The standalone y = x w^T (bf16 w [n][k], x [16][k], y fp32 [16][n]) on
+// caller-chosen scratch: clears clear_bytes at clear, launches the GEMM on
+// sms SMs with its split-K slots, tickets and state at slots / counters /
+// st, then copies the state's (code, site) error words into err (device
+// int32[2]); all on stream s.
+int run_linear_store(const void* w, const void* x, int n, int k, float* y, float* slots,
+                     int* counters, DevState* st, void* clear, size_t clear_bytes, int32_t* err,
+                     int sms, cudaStream_t s);
 
 }  // namespace dfl

@@ -12,10 +12,17 @@
 //  * n (output columns) at most LINEAR_NOALLOC_MAX_N; larger n is rejected
 //    with DFLASH_ERR_ARG before anything is launched;
 //  * every call on a device uses the same array.  Each call clears the
-//    tickets and the state word on its stream before the GEMM; the partial
+//    tickets and the state words on its stream before the GEMM; the partial
 //    tiles are always written before they are read.  Two calls that overlap
 //    on the GPU (different streams without ordering between them) race on
-//    the array and may return wrong results.
+//    the array and may return wrong results;
+//  * the kernel's bounded waits report through the caller's err words: the
+//    call copies the state's (code, site) pair there after the GEMM, so a
+//    wait that ran out (y incomplete) is seen by the caller once the stream
+//    reaches that point, although the call itself has returned DFLASH_OK;
+//  * the array's device address is looked up once per device and kept; a
+//    cudaDeviceReset (which unloads the library's module from that device)
+//    invalidates it, so the entry point must not be used after one.
 
 #include <cstring>
 #include <mutex>
@@ -77,15 +84,16 @@ int setup_device(int dev, unsigned char** addr, int* sms) {
 }  // namespace
 
 extern "C" int dflash_linear_noalloc(const void* w, const void* x, int32_t n, int32_t k, float* y,
-                                     dflash_stream_t stream) {
-    if (!w || !x || !y) return report_error(DFLASH_ERR_ARG, "NULL argument");
+                                     int32_t* err, dflash_stream_t stream) {
+    if (!w || !x || !y || !err) return report_error(DFLASH_ERR_ARG, "NULL argument");
     if (n < GEMM_BN || n % GEMM_BN || k < 64 || k % 64)
         return report_error(DFLASH_ERR_ARG, "n %d k %d: n a multiple of 128, k of 64", n, k);
     if (n > LINEAR_NOALLOC_MAX_N)
         return report_error(DFLASH_ERR_ARG,
                             "n %d exceeds %d, the most output columns the fixed scratch serves "
                             "(use dflash_linear with a workspace)", n, LINEAR_NOALLOC_MAX_N);
-    if ((reinterpret_cast<uintptr_t>(y) & 15) != 0) return report_error(DFLASH_ERR_ARG, "y misaligned");
+    if ((reinterpret_cast<uintptr_t>(y) & 15) != 0 || (reinterpret_cast<uintptr_t>(err) & 7) != 0)
+        return report_error(DFLASH_ERR_ARG, "y or err misaligned");
     const cudaError_t pending = cudaGetLastError();
     if (pending != cudaSuccess)
         return report_error(DFLASH_ERR_CUDA, "a CUDA error was pending before this call: %s",
@@ -97,32 +105,14 @@ extern "C" int dflash_linear_noalloc(const void* w, const void* x, int32_t n, in
         return report_error(DFLASH_ERR_ARG, "device %d: at most %d devices", dev, NOALLOC_MAX_DEVICES);
     unsigned char* base = nullptr;
     int sms = 0;
-    int r = setup_device(dev, &base, &sms);
+    const int r = setup_device(dev, &base, &sms);
     if (r) return r;
-    GemmMaps maps;
-    if ((r = make_linear_maps(&maps, w, x, n, k))) return r;
-
-    GemmArgs a;
-    memset(&a, 0, sizeof a);
-    a.N = n;
-    a.K = k;
-    a.n_tiles = n / GEMM_BN;
-    a.kb = k / 64;
-    a.seg_rows[0] = n;
-    a.n_seg = 1;
-    a.out = y;
-    a.ldo = n;
-    a.slots = reinterpret_cast<float*>(base);
-    a.counters = reinterpret_cast<int*>(base + NOALLOC_SLOT_BYTES);
-    a.st = reinterpret_cast<DevState*>(base + NOALLOC_SLOT_BYTES + NOALLOC_TICKET_BYTES);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // tickets and state start at zero (an earlier call may have been cut short)
-    e = cudaMemsetAsync(base + NOALLOC_SLOT_BYTES, 0, NOALLOC_TICKET_BYTES + NOALLOC_STATE_BYTES, s);
-    if (e != cudaSuccess) return report_error(DFLASH_ERR_CUDA, "scratch clear: %s", cudaGetErrorString(e));
-    const long long units = (long long)a.n_tiles * a.kb;
-    const int ctas = sms * DFL_GEMM_CTAS_PER_SM;     // <= NOALLOC_MAX_CTAS partial-tile pairs
-    const int grid = (int)(units < ctas ? units : ctas);
-    const int le = launch_gemm(WF_BF16, EPI_STORE, XT_BF16, maps, a, grid, s);
-    if (le) return report_error(DFLASH_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString((cudaError_t)le));
-    return DFLASH_OK;
+    // tickets and state start at zero on every call (an earlier call may
+    // have been cut short by a wait that ran out)
+    unsigned char* tickets = base + NOALLOC_SLOT_BYTES;
+    return run_linear_store(w, x, n, k, y, reinterpret_cast<float*>(base),
+                            reinterpret_cast<int*>(tickets),
+                            reinterpret_cast<DevState*>(tickets + NOALLOC_TICKET_BYTES), tickets,
+                            NOALLOC_TICKET_BYTES + NOALLOC_STATE_BYTES, err, sms,
+                            reinterpret_cast<cudaStream_t>(stream));
 }

@@ -8,7 +8,9 @@ Every tensor is drawn from its own counter-keyed Philox stream (key = base
 seed, a stable id of the tensor's name, chunk index), so a tensor's values do
 not depend on which other tensors were drawn or in which order, and large
 tensors are drawn in parallel chunks.  Weights are N(0, std) in fp32, rounded
-to bf16 for bf16 models; norm weights are ones; prompts are uniform ids.
+to bf16 for bf16 models; norm weights are ones, or N(1, norm_std) when a
+caller asks for it (so that a kernel which drops or swaps a norm weight
+changes the result); prompts are uniform ids.
 """
 
 from __future__ import annotations
@@ -82,25 +84,31 @@ def layer_shapes(hidden: int, n_q: int, n_kv: int, head_dim: int, ffn: int) -> D
     }
 
 
+def norm_weight(n: int, norm_std: float, seed: int, name: str) -> torch.Tensor:
+    """fp32 RMSNorm weight of width n: ones, or N(1, norm_std) keyed by name."""
+    if norm_std <= 0.0:
+        return torch.ones(n, dtype=torch.float32)
+    return torch.from_numpy(normal((n,), norm_std, seed, name) + np.float32(1.0))
+
+
 def decoder_layers(prefix: str, n_layers: int, hidden: int, n_q: int, n_kv: int,
                    head_dim: int, ffn: int, dtype: torch.dtype, std: float = 0.02,
-                   seed: int = WEIGHT_SEED) -> List[Dict[str, torch.Tensor]]:
+                   seed: int = WEIGHT_SEED, norm_std: float = 0.0) -> List[Dict[str, torch.Tensor]]:
     """Weights of n_layers decoder layers as CPU tensors.
 
     Projections are N(0, std) drawn in fp32 and cast to `dtype` (fp32 or
-    bf16); norm weights (attention/MLP input norms, q/k head norms) are fp32
-    ones.
+    bf16); norm weights (attention/MLP input norms, q/k head norms) are fp32,
+    ones or N(1, norm_std) (each its own stream).
     """
     shapes = layer_shapes(hidden, n_q, n_kv, head_dim, ffn)
+    widths = {"ln_attn": hidden, "ln_mlp": hidden, "q_norm": head_dim, "k_norm": head_dim}
     layers = []
     for l in range(n_layers):
         lw = {}
         for k in LAYER_KEYS:
             lw[k] = as_torch(normal(shapes[k], std, seed, f"{prefix}.{l}.{k}"), dtype)
-        lw["ln_attn"] = torch.ones(hidden, dtype=torch.float32)
-        lw["ln_mlp"] = torch.ones(hidden, dtype=torch.float32)
-        lw["q_norm"] = torch.ones(head_dim, dtype=torch.float32)
-        lw["k_norm"] = torch.ones(head_dim, dtype=torch.float32)
+        for k in NORM_KEYS:
+            lw[k] = norm_weight(widths[k], norm_std, seed, f"{prefix}.{l}.{k}")
         layers.append(lw)
     return layers
 
@@ -132,24 +140,25 @@ class ModelTensors:
     """Every synthetic tensor of a workload (CPU tensors).
 
     embed [vocab, H] (also the tied LM head), per-layer weights of the target
-    ("tgt") and the drafter ("drf"), fc [H, n_taps*H] and fp32 ones for the
-    final norms and the drafter's context norm.  Layers stored as INT4 (the
-    drafter's or the target's) are drawn in fp32; the quantiser of each side
-    turns them into INT4.
+    ("tgt") and the drafter ("drf"), fc [H, n_taps*H] and fp32 weights of the
+    final norms and the drafter's context norm (ones, or N(1, norm_std) when
+    norm_std > 0).  Layers stored as INT4 (the drafter's or the target's) are
+    drawn in fp32; the quantiser of each side turns them into INT4.
     """
 
-    def __init__(self, w, std: float = 0.02, seed: int = WEIGHT_SEED):
+    def __init__(self, w, std: float = 0.02, seed: int = WEIGHT_SEED, norm_std: float = 0.0):
         dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
         self.w = w
+        self.norm_std = norm_std
         self.embed = matrix("embed", w.vocab, w.hidden, dt, std, seed)
-        self.final_norm_t = torch.ones(w.hidden, dtype=torch.float32)
-        self.final_norm_d = torch.ones(w.hidden, dtype=torch.float32)
-        self.ctx_norm = torch.ones(w.hidden, dtype=torch.float32)
+        self.final_norm_t = norm_weight(w.hidden, norm_std, seed, "final_norm_tgt")
+        self.final_norm_d = norm_weight(w.hidden, norm_std, seed, "final_norm_drf")
+        self.ctx_norm = norm_weight(w.hidden, norm_std, seed, "ctx_norm")
         tdt = torch.float32 if getattr(w, "tgt_int4", False) else dt
         self.tgt = decoder_layers("tgt", w.tgt_layers, w.hidden, w.n_q, w.n_kv, w.head_dim,
-                                  w.ffn, tdt, std, seed)
+                                  w.ffn, tdt, std, seed, norm_std)
         ddt = torch.float32 if w.drf_int4 else dt
         self.drf = decoder_layers("drf", w.drf_layers, w.hidden, w.n_q, w.n_kv, w.head_dim,
-                                  w.ffn, ddt, std, seed)
+                                  w.ffn, ddt, std, seed, norm_std)
         self.fc = matrix("fc", w.hidden, w.n_taps * w.hidden, dt, std, seed) \
             if w.drf_layers else None

@@ -359,14 +359,23 @@ int dflash_quantize_int4g64(const float* w, int32_t n, int32_t k, uint8_t* packe
  * (nn.Linear layout), x bf16 [16][k] (rows the caller does not use are
  * zero), y fp32 [16][n].  n a multiple of 128, k a multiple of 64; every
  * buffer 16-byte aligned.  The workspace (dflash_linear_workspace_bytes)
- * holds the split-K partial tiles and tickets; zero-fill it before its
- * first use (every completed call leaves the tickets at zero again); calls
- * sharing a workspace must not overlap on the GPU.  The result of a row
- * depends only on that row (fixed reduction order).
+ * holds the split-K partial tiles and tickets, then a 256-byte state block;
+ * zero-fill it before its first use (every completed call leaves the
+ * tickets at zero again); calls sharing a workspace must not overlap on the
+ * GPU.  The result of a row depends only on that row (fixed reduction
+ * order).
+ * err: device int32[2].  The call clears the state's error words, and
+ * after the GEMM copies them into err on the stream: {0, 0} when the GEMM
+ * completed; {1, site} when one of its bounded waits ran out (2 s; the
+ * owner of a split tile waiting for the other parts is site 105), in which
+ * case y is incomplete and the workspace's tickets may be left nonzero --
+ * zero-fill it again before the next call.  Read err after synchronising
+ * the stream: the call itself returns DFLASH_OK once the work is enqueued.
+ * Errors (returned): ARG, CUDA.
  */
 size_t dflash_linear_workspace_bytes(int32_t n, int32_t k);
 int dflash_linear(const void* w, const void* x, int32_t n, int32_t k, float* y, void* workspace,
-                  size_t workspace_bytes, dflash_stream_t stream);
+                  size_t workspace_bytes, int32_t* err, dflash_stream_t stream);
 
 /*
  * dflash_linear without a workspace, for callers that cannot allocate
@@ -381,13 +390,18 @@ int dflash_linear(const void* w, const void* x, int32_t n, int32_t k, float* y, 
  * fixed 4 MiB + 9 KiB array in the library's device memory, held by every
  * GPU that loads the library until the process exits.  The first call on a
  * device looks up that array's device address (with the device current);
- * make that first call before any stream capture.  Every call on a device
- * shares the array: each clears the tickets it needs on its stream first,
- * but calls that overlap on the GPU (unordered streams) race and may return
- * wrong results.  The call allocates nothing.
+ * make that first call before any stream capture, and make no call on a
+ * device after a cudaDeviceReset of it (the address belongs to the module
+ * loaded before the reset).  Every call on a device shares the array: each
+ * clears the tickets and error words it needs on its stream first, but
+ * calls that overlap on the GPU (unordered streams) race and may return
+ * wrong results.  err (device int32[2], 8-byte aligned) receives the
+ * GEMM's error words as in dflash_linear: {0, 0}, or {1, site} when a
+ * bounded wait ran out and y is incomplete; read it after synchronising the
+ * stream.  The call allocates nothing.
  */
 int dflash_linear_noalloc(const void* w, const void* x, int32_t n, int32_t k, float* y,
-                          dflash_stream_t stream);
+                          int32_t* err, dflash_stream_t stream);
 
 /*
  * Dense many-row GEMM on the fifth-generation tensor cores (tcgen05, f32

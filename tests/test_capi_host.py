@@ -138,9 +138,13 @@ def test_binding_checks_standalone_operands_before_the_library(capi):
         ("err", lambda: capi.dflash_linear_dense(torch.zeros(8, 64, dtype=bf), torch.zeros(4, 64, dtype=bf),
                                                  torch.zeros(4, 8), torch.zeros(1, dtype=torch.int32))),
         ("x", lambda: capi.dflash_linear(torch.zeros(128, 64, dtype=bf), torch.zeros(8, 64, dtype=bf),
-                                         torch.zeros(16, 128), torch.zeros(64, dtype=torch.uint8))),
+                                         torch.zeros(16, 128), torch.zeros(64, dtype=torch.uint8), e())),
         ("x", lambda: capi.dflash_linear_noalloc(torch.zeros(128, 64, dtype=bf),
-                                                 torch.zeros(128, 16, dtype=bf).t(), torch.zeros(16, 128))),
+                                                 torch.zeros(128, 16, dtype=bf).t(), torch.zeros(16, 128),
+                                                 e())),
+        ("err", lambda: capi.dflash_linear_noalloc(torch.zeros(128, 64, dtype=bf),
+                                                   torch.zeros(16, 64, dtype=bf), torch.zeros(16, 128),
+                                                   torch.zeros(2, dtype=torch.int64))),
         ("scales", lambda: capi.dflash_quantize_int4g64(torch.zeros(4, 256), torch.zeros(4, 128, dtype=torch.uint8),
                                                         torch.zeros(2, 4, dtype=torch.int16))),
         ("out", lambda: capi.dflash_tap_reduce([torch.zeros(3, 4 * 64, dtype=bf)] * 2, 3, 4, 64,

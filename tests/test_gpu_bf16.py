@@ -2,11 +2,16 @@
 head_dim 128, SwiGLU 9728, vocab 151936): a 2-layer target and a 1-layer
 drafter keep the CPU oracle to seconds while every kernel runs at the full
 per-layer shape, tile count and LM-head width of the end-to-end workload.
+Every RMSNorm weight (input, MLP, q/k head, final, context) is drawn
+N(1, 0.1), so a kernel that drops or swaps a folded norm weight fails.
 
 Tolerance: logits within rel 2e-2 of the fp64 oracle (bf16 weights and bf16
-GEMM inputs against fp32 accumulation); ids bit-exact on rows whose oracle
-top-2 margin exceeds twice that; GPU speculative == GPU greedy bit-exactly;
-a 16-row verify reproduces the 1-row logits bit-for-bit.
+GEMM inputs against fp32 accumulation); ids bit-exact on every row whose
+oracle top-2 margin exceeds twice the GPU row's measured error, with a floor
+on the number of such rows taken at the accuracy these kernels reach
+(DEC_TOL); acceptance, emitted tokens and rollback exact, asserted (never
+skipped) on greedy-continuation drafts; GPU speculative == GPU greedy
+bit-exactly; a 16-row verify reproduces the 1-row logits bit-for-bit.
 """
 
 import numpy as np
@@ -21,6 +26,8 @@ from tests.oracle_inputs import ModelTensors, oracle_config, oracle_draft, oracl
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
+DEC_TOL = 1e-3     # the accuracy the decidable-row floors are taken at
+NORM_STD = 0.1
 W = E2E_BF16.with_(name="bf16_2layer", tgt_layers=2, drf_layers=1, tap_layers=(0, 1),
                    prompt_len=40, n_new=48, max_seq=256)
 
@@ -29,14 +36,18 @@ W = E2E_BF16.with_(name="bf16_2layer", tgt_layers=2, drf_layers=1, tap_layers=(0
 def qwen():
     G.build_lib()
     from block_diffusion_speculative_gather_gb300.runtime import DFlash
-    m = ModelTensors(W, std=0.02)
+    m = ModelTensors(W, std=0.02, norm_std=NORM_STD)
     tw, dw, cfg = oracle_target(m), oracle_draft(m), oracle_config(W)
     prompt = synth.uniform_ids(W.prompt_len, W.vocab)
     cache = O.KVCache(2, W.n_kv, W.head_dim)
     p_logits, p_taps = O.target_forward(tw, cfg, prompt.tolist(), 0, cache)
+    g = O.greedy(tw, cfg, prompt.tolist(), W.n_new)
+    # teacher-forced logits of every greedy step (row k predicts token k)
+    tf, _ = O.target_forward(tw, cfg, prompt.tolist() + g[:-1], 0,
+                             O.KVCache(2, W.n_kv, W.head_dim))
     dec = DFlash(W, m)
     return dict(m=m, tw=tw, dw=dw, cfg=cfg, prompt=torch.from_numpy(prompt), p_logits=p_logits,
-                p_taps=p_taps, dec=dec)
+                p_taps=p_taps, greedy=g, greedy_logits=tf[len(prompt) - 1:], dec=dec)
 
 
 def test_prefill_logits(qwen):
@@ -47,10 +58,11 @@ def test_prefill_logits(qwen):
     dec.check()
     dec.set_logits_out(None, None)
     last = (P - 1) // 16 * 16
-    err = G.rel_err_rows(vl[:P - last].cpu().numpy(), qwen["p_logits"][last:P])
-    assert err.max() < TOL, err
+    gpu = vl[:P - last].cpu().numpy()
+    dec_rows = G.check_rows("bf16_prefill", gpu, None, qwen["p_logits"][last:P], TOL, DEC_TOL)
     st = dec.stats()
-    if G.decidable(qwen["p_logits"][P - 1], TOL):
+    assert st.n == P and st.generated == 1
+    if dec_rows[-1]:
         assert st.t_n == int(np.argmax(qwen["p_logits"][P - 1]))
 
 
@@ -65,16 +77,30 @@ def test_draft_block16_matches_oracle(qwen):
     t_n = dec.stats().t_n
     ref, _ = O.draft_forward(qwen["dw"], qwen["tw"].embed, qwen["cfg"], qwen["p_taps"], t_n, P,
                              W.block)
-    err = G.rel_err_rows(dl[1:W.block].cpu().numpy(), ref[1:])
-    assert err.max() < TOL, err
-    G.check_ids(ids[:W.block - 1], ref[1:], TOL)
+    G.check_rows("bf16_draft", dl[1:W.block].cpu().numpy(), ids[:W.block - 1], ref[1:], TOL,
+                 DEC_TOL)
 
 
-def test_verify16_logits_and_accept(qwen):
+def _continuation(g, B, cut):
+    """Drafts d_1..d_{B-1} = the oracle's greedy continuation, the draft at
+    index `cut` replaced by another token (None: no mismatch)."""
+    d = list(g[1:B])
+    if cut is not None:
+        d[cut] = (d[cut] + 1) % W.vocab
+    return d
+
+
+@pytest.mark.parametrize("cut", [0, 7, None], ids=["cut0", "cut7", "all"])
+def test_verify16_logits_and_accept(qwen, cut):
+    """A 16-row verify of the oracle's greedy continuation cut at draft 0, 7 or
+    not at all: every row's logits against the oracle, and the acceptance
+    (a = cut, or 15), the emitted tokens including the bonus token and the
+    rolled-back KV length exactly as the oracle's."""
     dec, P, B = qwen["dec"], W.prompt_len, W.block
     dec.prefill(qwen["prompt"], W.n_new)
     t_n = dec.stats().t_n
-    d = synth.uniform_ids(B - 1, W.vocab, seed=9).tolist()
+    assert t_n == qwen["greedy"][0]
+    d = _continuation(qwen["greedy"], B, cut)
     vl = G.logits_buf(W.vocab)
     dec.set_logits_out(vl, None)
     toks, n = dec.verify(torch.tensor(d, dtype=torch.int32, device="cuda"))
@@ -83,13 +109,36 @@ def test_verify16_logits_and_accept(qwen):
     cache = O.KVCache(2, W.n_kv, W.head_dim)
     O.target_forward(qwen["tw"], qwen["cfg"], qwen["prompt"].tolist(), 0, cache)
     ref, _ = O.target_forward(qwen["tw"], qwen["cfg"], [t_n] + d, P, cache)
-    err = G.rel_err_rows(vl[:B].cpu().numpy(), ref)
-    assert err.max() < TOL, err
-    y = [int(np.argmax(r)) for r in ref]
-    a, emitted, _ = O.accept(d, y, -1)
-    if all(G.decidable(r, TOL) for r in ref[: a + 1]):
-        assert toks[: n.item()].tolist() == emitted
-        assert dec.stats().n == P + len(emitted)
+    gpu = vl[:B].cpu().numpy()
+    G.check_rows(f"bf16_verify_{cut}", gpu, None, ref, TOL, DEC_TOL)
+    a = G.accept_check(f"bf16_accept_{cut}", toks.cpu().tolist(), int(n.item()), dec.stats(),
+                       ref, d, gpu, TOL, P)
+    assert a == (B - 1 if cut is None else cut)
+
+
+def test_greedy_stream_matches_oracle(qwen):
+    """The GPU's plain greedy decoding (one-row verify steps) against the
+    oracle's greedy stream, each step's logits against the oracle's
+    teacher-forced row, tokens compared while decidable."""
+    dec, P = qwen["dec"], W.prompt_len
+    vl = G.logits_buf(W.vocab)
+    dec.set_logits_out(vl, None)
+    dec.prefill(qwen["prompt"], W.n_new)
+    rows = [vl[(P - 1) % 16].clone()]
+    st = dec.stats()
+    toks = [st.t_n]
+    while not st.finished and len(toks) < W.n_new:
+        t, n = dec.verify(None)
+        toks.extend(t[: int(n.item())].tolist())
+        rows.append(vl[0].clone())
+        st = dec.stats()
+    dec.check()
+    dec.set_logits_out(None, None)
+    gl = qwen["greedy_logits"]
+    floor = next((i for i, r in enumerate(gl) if not G.decidable(r, DEC_TOL)), len(gl))
+    n = G.stream_prefix("bf16_greedy_stream", toks, [r.cpu().numpy() for r in rows],
+                        qwen["greedy"], gl, TOL)
+    assert n >= floor and n > 0, (n, floor)
 
 
 def test_spec_equals_greedy_bf16(qwen):
@@ -132,9 +181,8 @@ def test_drafter_alone_ext_taps(qwen):
     dec.check()
     ref, _ = O.draft_forward(qwen["dw"], qwen["tw"].embed, qwen["cfg"], taps.float().numpy(), 123,
                              n, W.block)
-    err = G.rel_err_rows(dl[1:W.block].cpu().numpy(), ref[1:])
-    assert err.max() < TOL, err
-    G.check_ids(ids[:W.block - 1], ref[1:], TOL)
+    G.check_rows("bf16_drafter_ext_taps", dl[1:W.block].cpu().numpy(), ids[:W.block - 1],
+                 ref[1:], TOL, DEC_TOL)
     dec.close()
 
 
@@ -246,9 +294,9 @@ def test_dense_prefill_matches_chunked_and_oracle(qwen, monkeypatch):
     cache = O.KVCache(2, W.n_kv, W.head_dim)
     ref, _ = O.target_forward(qwen["tw"], qwen["cfg"], prompt.tolist(), 0, cache)
     last = (P - 1) // 16 * 16
-    err = G.rel_err_rows(lg_d.cpu().numpy(), ref[last:P])
-    assert err.max() < TOL, err
-    if G.decidable(ref[P - 1], TOL):
+    dec_rows = G.check_rows("bf16_dense_prefill", lg_d.cpu().numpy(), None, ref[last:P], TOL,
+                            DEC_TOL)
+    if dec_rows[-1]:
         assert tn_d == int(np.argmax(ref[P - 1]))
 
 

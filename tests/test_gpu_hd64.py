@@ -29,7 +29,7 @@ W = Workload(name="hd64", hidden=512, n_q=8, n_kv=4, head_dim=64, ffn=1536, voca
 @pytest.fixture(scope="module")
 def hd64():
     G.build_lib()
-    m = ModelTensors(W, std=0.05)
+    m = ModelTensors(W, std=0.05, norm_std=0.1)
     prompt = synth.uniform_ids(W.prompt_len, W.vocab, seed=21)
     tw, dw, cfg = oracle_target(m), oracle_draft(m), oracle_config(W)
     ref, _ = O.target_forward(tw, cfg, prompt.tolist(), 0, O.KVCache(2, W.n_kv, W.head_dim))
@@ -55,9 +55,9 @@ def test_hd64_prefill_logits(hd64, monkeypatch, env):
     dec, vl = _prefill(hd64, env, monkeypatch)
     P = W.prompt_len
     last = (P - 1) // 16 * 16
-    err = G.rel_err_rows(vl[:P - last].cpu().numpy(), hd64["ref"][last:P])
-    assert err.max() < TOL, err
-    if G.decidable(hd64["ref"][P - 1], TOL):
+    rows = G.check_rows(f"hd64_prefill_{env}", vl[:P - last].cpu().numpy(), None,
+                        hd64["ref"][last:P], TOL, 1e-3)
+    if rows[-1]:
         assert dec.stats().t_n == int(np.argmax(hd64["ref"][P - 1]))
     dec.close()
 

@@ -3,7 +3,9 @@ workload's format) on one Qwen3-4B-shaped layer: the library quantises the
 fp32 draws with its own kernel, the oracle with its own code (the two are
 bit-identical, see test_quantizer_bit_exact_with_oracle), and the drafter
 fed 300 external tap rows with a 64-row sliding window must give logits
-within rel 2e-2 of the oracle's dequantised fp64 drafter."""
+within rel 2e-2 of the oracle's dequantised fp64 drafter.  Norm weights are
+drawn N(1, 0.1); ids are checked on every row decidable at the GPU row's
+measured error, with a floor taken at DEC_TOL (see tests/gpu_common.py)."""
 
 import numpy as np
 import pytest
@@ -17,6 +19,8 @@ from tests.oracle_inputs import ModelTensors, oracle_config, oracle_draft
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
+DEC_TOL = 1e-3
+NORM_STD = 0.1
 W = DRAFT_INT4.with_(name="int4_1layer", drf_layers=1, n_ctx=300, window=64, max_seq=400)
 
 
@@ -25,7 +29,7 @@ def test_int4_drafter_matches_oracle(window, n_ext):
     G.build_lib()
     from block_diffusion_speculative_gather_gb300.runtime import DFlash
     w = W.with_(window=window)
-    m = ModelTensors(w)
+    m = ModelTensors(w, norm_std=NORM_STD)
     dec = DFlash(w, m)
     taps = synth.tap_rows(n_ext, w.n_taps * w.hidden)
     ext = taps.view(n_ext, w.n_taps, w.hidden).permute(1, 0, 2).contiguous()
@@ -36,9 +40,8 @@ def test_int4_drafter_matches_oracle(window, n_ext):
     dec.check()
     ref, _ = O.draft_forward(oracle_draft(m), m.embed.float().numpy(), oracle_config(w),
                              taps.float().numpy(), 777, n_ext, w.block)
-    err = G.rel_err_rows(dl[1:w.block].cpu().numpy(), ref[1:])
-    assert err.max() < TOL, err
-    G.check_ids(ids[:w.block - 1], ref[1:], TOL)
+    G.check_rows(f"int4_drafter_w{window}", dl[1:w.block].cpu().numpy(), ids[:w.block - 1],
+                 ref[1:], TOL, DEC_TOL)
     dec.close()
 
 
@@ -57,22 +60,31 @@ def int4_target():
     from block_diffusion_speculative_gather_gb300.runtime import DFlash
     from tests.oracle_inputs import oracle_target
     w = _w4()
-    m = ModelTensors(w)
-    return dict(w=w, m=m, tw=oracle_target(m), dw=oracle_draft(m), cfg=oracle_config(w),
-                prompt=torch.from_numpy(synth.uniform_ids(w.prompt_len, w.vocab)),
-                dec=DFlash(w, m))
+    m = ModelTensors(w, norm_std=NORM_STD)
+    tw, cfg = oracle_target(m), oracle_config(w)
+    prompt = synth.uniform_ids(w.prompt_len, w.vocab)
+    g = O.greedy(tw, cfg, prompt.tolist(), w.n_new)
+    tf, _ = O.target_forward(tw, cfg, prompt.tolist() + g[:-1], 0,
+                             O.KVCache(w.tgt_layers, w.n_kv, w.head_dim))
+    return dict(w=w, m=m, tw=tw, dw=oracle_draft(m), cfg=cfg, prompt=torch.from_numpy(prompt),
+                greedy=g, greedy_logits=tf[len(prompt) - 1:], dec=DFlash(w, m))
 
 
-def test_int4_target_and_lm_head_verify_match_oracle(int4_target):
+@pytest.mark.parametrize("cut", [0, 7, None], ids=["cut0", "cut7", "all"])
+def test_int4_target_and_lm_head_verify_match_oracle(int4_target, cut):
     """Target layers and the LM head in INT4 group-64 (both models 4-bit):
-    the 16-row verify's logits within rel 2e-2 of the oracle's dequantised
-    fp64 target, acceptance and rollback exact where decidable."""
+    a 16-row verify of the oracle's greedy continuation cut at draft 0, 7 or
+    not at all -- logits within rel 2e-2 of the oracle's dequantised fp64
+    target, acceptance, emitted tokens and rollback exact (asserted)."""
     T = int4_target
     w, dec, tw, cfg = T["w"], T["dec"], T["tw"], T["cfg"]
     P, B = w.prompt_len, w.block
     dec.prefill(T["prompt"], w.n_new)
     t_n = dec.stats().t_n
-    d = synth.uniform_ids(B - 1, w.vocab, seed=21).tolist()
+    assert t_n == T["greedy"][0]
+    d = list(T["greedy"][1:B])
+    if cut is not None:
+        d[cut] = (d[cut] + 1) % w.vocab
     vl = G.logits_buf(w.vocab)
     dec.set_logits_out(vl, None)
     toks, n = dec.verify(torch.tensor(d, dtype=torch.int32, device="cuda"))
@@ -81,13 +93,38 @@ def test_int4_target_and_lm_head_verify_match_oracle(int4_target):
     cache = O.KVCache(2, w.n_kv, w.head_dim)
     O.target_forward(tw, cfg, T["prompt"].tolist(), 0, cache)
     ref, _ = O.target_forward(tw, cfg, [t_n] + d, P, cache)
-    err = G.rel_err_rows(vl[:B].cpu().numpy(), ref)
-    assert err.max() < TOL, err
-    y = [int(np.argmax(r)) for r in ref]
-    a, emitted, _ = O.accept(d, y, -1)
-    if all(G.decidable(r, TOL) for r in ref[: a + 1]):
-        assert toks[: n.item()].tolist() == emitted
-        assert dec.stats().n == P + len(emitted)
+    gpu = vl[:B].cpu().numpy()
+    G.check_rows(f"int4_verify_{cut}", gpu, None, ref, TOL, DEC_TOL)
+    a = G.accept_check(f"int4_accept_{cut}", toks.cpu().tolist(), int(n.item()), dec.stats(),
+                       ref, d, gpu, TOL, P)
+    assert a == (B - 1 if cut is None else cut)
+
+
+def test_int4_greedy_stream_matches_oracle(int4_target):
+    """Plain greedy decoding of the INT4 target + INT4 LM head against the
+    oracle's greedy stream (dequantised fp64 weights), compared while
+    decidable at each step's measured error."""
+    T = int4_target
+    w, dec = T["w"], T["dec"]
+    P = w.prompt_len
+    vl = G.logits_buf(w.vocab)
+    dec.set_logits_out(vl, None)
+    dec.prefill(T["prompt"], w.n_new)
+    rows = [vl[(P - 1) % 16].clone()]
+    st = dec.stats()
+    toks = [st.t_n]
+    while not st.finished and len(toks) < w.n_new:
+        t, n = dec.verify(None)
+        toks.extend(t[: int(n.item())].tolist())
+        rows.append(vl[0].clone())
+        st = dec.stats()
+    dec.check()
+    dec.set_logits_out(None, None)
+    gl = T["greedy_logits"]
+    floor = next((i for i, r in enumerate(gl) if not G.decidable(r, DEC_TOL)), len(gl))
+    n = G.stream_prefix("int4_greedy_stream", toks, [r.cpu().numpy() for r in rows],
+                        T["greedy"], gl, TOL)
+    assert n >= floor and n > 0, (n, floor)
 
 
 def test_int4_target_draft_uses_int4_lm_head(int4_target):
@@ -105,9 +142,8 @@ def test_int4_target_draft_uses_int4_lm_head(int4_target):
     _, p_taps = O.target_forward(T["tw"], T["cfg"], T["prompt"].tolist(), 0, cache)
     ref, _ = O.draft_forward(T["dw"], T["tw"].embed, T["cfg"], p_taps, t_n, w.prompt_len, w.block,
                              lm_head=T["tw"].lm_head)
-    err = G.rel_err_rows(dl[1:w.block].cpu().numpy(), ref[1:])
-    assert err.max() < TOL, err
-    G.check_ids(ids[:w.block - 1], ref[1:], TOL)
+    G.check_rows("int4_target_draft", dl[1:w.block].cpu().numpy(), ids[:w.block - 1], ref[1:],
+                 TOL, DEC_TOL)
 
 
 def test_int4_target_spec_equals_greedy_and_batch_invariant(int4_target):
@@ -165,5 +201,4 @@ def test_int4_target_dense_prefill_matches_chunked_and_oracle(int4_target, monke
     assert err.max() < TOL / 4, err
     ref, _ = O.target_forward(T["tw"], T["cfg"], prompt.tolist(), 0, O.KVCache(2, w.n_kv, w.head_dim))
     last = (P - 1) // 16 * 16
-    err = G.rel_err_rows(lg_d.cpu().numpy(), ref[last:P])
-    assert err.max() < TOL, err
+    G.check_rows("int4_dense_prefill", lg_d.cpu().numpy(), None, ref[last:P], TOL, DEC_TOL)

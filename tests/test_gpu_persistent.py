@@ -41,7 +41,7 @@ def _make(m, persistent):
 @pytest.fixture(scope="module")
 def pair():
     G.build_lib()
-    m = ModelTensors(W, std=0.02)
+    m = ModelTensors(W, std=0.02, norm_std=0.1)
     prompt = torch.from_numpy(synth.uniform_ids(W.prompt_len, W.vocab))
     return dict(m=m, prompt=prompt, ref=_make(m, False), per=_make(m, True))
 

@@ -4,7 +4,9 @@ block 8, window 64, 32-token prompt, 64 tokens), through the C ABI.
 Tolerance: logits within rel 1e-4 of the fp64 oracle (per row, max abs
 difference over max |oracle|); token ids bit-exact wherever the oracle's
 top-2 margin exceeds twice that; GPU speculative output bit-identical to GPU
-plain greedy; acceptance lengths and rollback positions exact.
+plain greedy; acceptance lengths and rollback positions exact.  Norm
+weights are drawn N(1, 0.1); ids are checked on every row decidable at the
+GPU row's measured error, with a floor taken at DEC_TOL (tests/gpu_common.py).
 """
 
 import numpy as np
@@ -19,13 +21,14 @@ from tests.oracle_inputs import ModelTensors, oracle_config, oracle_draft, oracl
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
+DEC_TOL = 1e-5
 
 
 @pytest.fixture(scope="module", params=[0.02, 0.1], ids=["std0.02", "std0.1"])
 def tiny(request):
     G.build_lib()
     from block_diffusion_speculative_gather_gb300.runtime import DFlash
-    m = ModelTensors(TINY, std=request.param)
+    m = ModelTensors(TINY, std=request.param, norm_std=0.1)
     tw, dw, cfg = oracle_target(m), oracle_draft(m), oracle_config(TINY)
     prompt = synth.uniform_ids(TINY.prompt_len, TINY.vocab)
     cache = O.KVCache(len(tw.layers), cfg.n_kv, cfg.head_dim)
@@ -50,12 +53,12 @@ def test_prefill_logits_and_first_token(tiny):
     P = TINY.prompt_len
     last_chunk = (P - 1) // 16 * 16
     rows = P - last_chunk
-    err = G.rel_err_rows(vl[:rows].cpu().numpy(), tiny["p_logits"][last_chunk:P])
-    assert err.max() < TOL, err
+    dec_rows = G.check_rows("tiny_prefill", vl[:rows].cpu().numpy(), None,
+                            tiny["p_logits"][last_chunk:P], TOL, DEC_TOL)
     assert st.n == P and st.generated == 1 and st.ctx_len == P
     assert st.block_len == TINY.block
-    if G.decidable(tiny["p_logits"][P - 1], TOL):
-        assert st.t_n == int(np.argmax(tiny["p_logits"][P - 1]))
+    assert dec_rows[-1], "the last prompt row is not decidable"
+    assert st.t_n == int(np.argmax(tiny["p_logits"][P - 1]))
 
 
 def test_draft_matches_uncached_oracle(tiny):
@@ -71,9 +74,8 @@ def test_draft_matches_uncached_oracle(tiny):
     t_n = dec.stats().t_n
     ref_logits, ref_ids = O.draft_forward(tiny["dw"], tiny["tw"].embed, tiny["cfg"],
                                           tiny["p_taps"], t_n, P, TINY.block)
-    err = G.rel_err_rows(dl[1:TINY.block].cpu().numpy(), ref_logits[1:])
-    assert err.max() < TOL, err
-    G.check_ids(ids[:TINY.block - 1], ref_logits[1:], TOL)
+    G.check_rows("tiny_draft", dl[1:TINY.block].cpu().numpy(), ids[:TINY.block - 1],
+                 ref_logits[1:], TOL, DEC_TOL)
 
 
 @pytest.mark.parametrize("cut", [0, 3, 7])
@@ -96,17 +98,14 @@ def test_verify_accept_rollback_match_oracle(tiny, cut):
     cache = O.KVCache(len(tiny["tw"].layers), TINY.n_kv, TINY.head_dim)
     O.target_forward(tiny["tw"], tiny["cfg"], tiny["prompt"].tolist(), 0, cache)
     ref_logits, _ = O.target_forward(tiny["tw"], tiny["cfg"], [st.t_n] + d, P, cache)
-    err = G.rel_err_rows(vl[:B].cpu().numpy(), ref_logits)
-    assert err.max() < TOL, err
-    y = [int(np.argmax(r)) for r in ref_logits]
-    a, emitted, _ = O.accept(d, y, -1)
-    if all(G.decidable(r, TOL) for r in ref_logits[: a + 1]):
-        assert int(n.item()) == len(emitted)
-        assert toks[: len(emitted)].tolist() == emitted
-        assert all(t == -1 for t in toks[len(emitted):].tolist())
-        st2 = dec.stats()
-        assert st2.n == P + len(emitted) and st2.ctx_len == st2.n
-        assert st2.last_accept == a and st2.generated == 1 + len(emitted)
+    gpu = vl[:B].cpu().numpy()
+    G.check_rows(f"tiny_verify_{cut}", gpu, None, ref_logits, TOL, DEC_TOL)
+    st2 = dec.stats()
+    a = G.accept_check(f"tiny_accept_{cut}", toks.tolist(), int(n.item()), st2, ref_logits, d,
+                       gpu, TOL, P)
+    assert a == cut
+    assert all(t == -1 for t in toks[int(n.item()):].tolist())
+    assert st2.ctx_len == st2.n and st2.generated == 1 + int(n.item())
 
 
 def test_spec_equals_greedy_and_oracle(tiny):

@@ -8,6 +8,7 @@ that its one JSON line keeps the bench contract.
 """
 
 import json
+import time
 import os
 import socket
 import subprocess
@@ -68,9 +69,11 @@ def test_reference_arm_line_keeps_the_contract():
     # one step of the oracle arm on this host: the JSON line's keys, the
     # cpu_baseline describing this run and e2e equal to the line's own value
     env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    t0 = time.perf_counter()
     p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                         "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True,
-                       timeout=600)
+                       timeout=900)
+    wall = time.perf_counter() - t0
     assert p.returncode == 0, p.stderr
     lines = [l for l in p.stdout.splitlines() if l.strip()]
     assert len(lines) == 1
@@ -86,3 +89,6 @@ def test_reference_arm_line_keeps_the_contract():
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+    # every step is real timed work: the timed region fits inside the run
+    assert d["ms_per_step"] * d["steps"] / 1e3 <= wall
+    assert abs(d["value"] - 1e3 / d["ms_per_step"]) <= 1e-3 * d["value"] + 1e-6

@@ -6,9 +6,11 @@ library, shared by every call on the device.
 
 Checked through the C ABI against dflash_linear on two calls in a row (the
 second on other operands and another shape, so it runs on the scratch the
-first one left behind), within the GEMM tests' tolerance; plus the size
-limit.  This file is collected last so that a failure here comes after
-every other test has run.
+first one left behind), within the GEMM tests' tolerance, each call's error
+words {0, 0}; plus the size limit.  (The error words come from the same
+launch helper as dflash_linear's, whose timeout report test_gpu_linear.py
+makes run out.)  This file is collected last so that a failure here comes
+after every other test has run.
 """
 
 import pytest
@@ -33,8 +35,10 @@ def _with_workspace(capi, w, x):
     n, k = w.shape
     ws = torch.zeros(capi.dflash_linear_workspace_bytes(n, k), dtype=torch.uint8, device="cuda")
     y = torch.empty((16, n), dtype=torch.float32, device="cuda")
-    capi.dflash_linear(w, x, y, ws)
+    err = torch.zeros(2, dtype=torch.int32, device="cuda")
+    capi.dflash_linear(w, x, y, ws, err)
     torch.cuda.synchronize()
+    assert err.tolist() == [0, 0]
     return y
 
 
@@ -45,10 +49,12 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
         w, x = _operands(n, k, seed)
         ref = _with_workspace(capi, w, x)
         y = torch.full((16, n), float("nan"), dtype=torch.float32, device="cuda")
-        capi.dflash_linear_noalloc(w, x, y)
+        err = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+        capi.dflash_linear_noalloc(w, x, y, err)
         torch.cuda.synchronize()
-        err = float((y - ref).abs().max() / ref.abs().max())
-        assert err <= TOL, (n, k, err)
+        assert err.tolist() == [0, 0]
+        rel = float((y - ref).abs().max() / ref.abs().max())
+        assert rel <= TOL, (n, k, rel)
         assert torch.all(y[13:] == 0)
         # same kernel, grid and reduction order: in practice bit-identical
         assert torch.equal(y, ref), (n, k)
@@ -61,7 +67,8 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     w = torch.zeros((n, k), dtype=torch.bfloat16, device="cuda")
     x = torch.zeros((16, k), dtype=torch.bfloat16, device="cuda")
     y = torch.empty((16, n), dtype=torch.float32, device="cuda")
+    err = torch.zeros(2, dtype=torch.int32, device="cuda")
     with pytest.raises(capi.DFlashError) as e:
-        capi.dflash_linear_noalloc(w, x, y)
+        capi.dflash_linear_noalloc(w, x, y, err)
     assert e.value.code == -3          # DFLASH_ERR_ARG
     assert "262144" in str(e.value)
