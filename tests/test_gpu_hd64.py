@@ -81,16 +81,29 @@ def test_hd64_spec_equals_greedy_and_oracle(hd64, monkeypatch):
     gg = dec.greedy(hd64["prompt"], W.n_new)
     sp = dec.generate(hd64["prompt"], W.n_new)
     dec.check()
-    dec.close()
     assert sp == gg
-    # the oracle's greedy decoding, keeping each step's logits for the margin test
+    # the GPU greedy steps again with each step's logits, against the
+    # oracle's greedy decoding (each step's logits kept for the margin test)
+    P = W.prompt_len
+    vl = G.logits_buf(W.vocab)
+    dec.set_logits_out(vl, None)
+    dec.prefill(hd64["prompt"], W.n_new)
+    gl = [vl[(P - 1) % 16].clone()]
+    st = dec.stats()
+    while not st.finished and len(gl) < W.n_new:
+        dec.verify(None)
+        gl.append(vl[0].clone())
+        st = dec.stats()
+    dec.check()
+    dec.close()
     cache = O.KVCache(W.tgt_layers, W.n_kv, W.head_dim)
     lg, _ = O.target_forward(hd64["tw"], hd64["cfg"], hd64["prompt"].tolist(), 0, cache)
-    rows, toks, pos = [lg[-1]], [O.argmax_lowest(lg[-1])], W.prompt_len
+    rows, toks, pos = [lg[-1]], [O.argmax_lowest(lg[-1])], P
     while len(toks) < W.n_new:
         lg, _ = O.target_forward(hd64["tw"], hd64["cfg"], [toks[-1]], pos, cache)
         rows.append(lg[0])
         toks.append(O.argmax_lowest(lg[0]))
         pos += 1
-    n = G.compared_prefix(gg, toks, rows, TOL)
-    assert n >= 1
+    floor = next((i for i, r in enumerate(rows) if not G.decidable(r, 1e-3)), len(rows))
+    n = G.stream_prefix("hd64_greedy_stream", gg, [r.cpu().numpy() for r in gl], toks, rows, TOL)
+    assert n >= floor and n > 0, (n, floor)
