@@ -104,6 +104,15 @@ def _load() -> C.CDLL:
         "dflash_progress": (C.c_int, [vp, vp, vp]),
         "dflash_attention_form": (C.c_int, [vp, i32]),
         "dflash_linear_dense": (C.c_int, [vp, vp, vp, i32, i32, i32, vp, vp, vp]),
+        "dflash_batch_workspace_bytes": (sz, [C.POINTER(dflash_config), i32]),
+        "dflash_batch_init": (C.c_int, [C.POINTER(dflash_config), C.POINTER(dflash_weights), i32, vp,
+                                        vp, vp, sz, C.POINTER(vp)]),
+        "dflash_batch_context": (vp, [vp, i32]),
+        "dflash_batch_draft": (C.c_int, [vp, vp, vp]),
+        "dflash_batch_verify_accept": (C.c_int, [vp, vp, vp, vp, vp]),
+        "dflash_batch_set_logits_out": (C.c_int, [vp, vp, vp]),
+        "dflash_batch_check": (C.c_int, [vp, vp]),
+        "dflash_batch_destroy": (None, [vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -121,7 +130,10 @@ EXPORTED = ("dflash_workspace_bytes", "dflash_kv_target_bytes", "dflash_kv_draft
             "dflash_quantize_int4g64", "dflash_profile", "dflash_launch_count",
             "dflash_selftest_timeout", "dflash_adopt_kv", "dflash_linear_workspace_bytes",
             "dflash_linear", "dflash_linear_noalloc", "dflash_profile_phases",
-            "dflash_progress", "dflash_attention_form", "dflash_linear_dense")
+            "dflash_progress", "dflash_attention_form", "dflash_linear_dense",
+            "dflash_batch_workspace_bytes", "dflash_batch_init", "dflash_batch_context",
+            "dflash_batch_draft", "dflash_batch_verify_accept", "dflash_batch_set_logits_out",
+            "dflash_batch_check", "dflash_batch_destroy")
 
 
 def check(rc: int) -> None:
@@ -355,3 +367,45 @@ def dflash_linear_dense(w, x, y, err, x_lo=None, stream=None):
     _on_gpu(w=w, x=x, x_lo=x_lo, y=y, err=err)
     check(lib.dflash_linear_dense(_ptr(w), _ptr(x), _ptr(x_lo), m, n, k, _ptr(y), _ptr(err),
                                   _stream(stream)))
+
+
+# ---- several sequences in lockstep rounds
+
+def dflash_batch_workspace_bytes(cfg, S: int) -> int:
+    return lib.dflash_batch_workspace_bytes(C.byref(cfg), S)
+
+
+def dflash_batch_init(cfg, weights, S: int, kv_target, kv_draft, workspace):
+    out = C.c_void_p()
+    check(lib.dflash_batch_init(C.byref(cfg), C.byref(weights), S, _ptr(kv_target), _ptr(kv_draft),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                C.byref(out)))
+    return out.value
+
+
+def dflash_batch_context(b, s: int):
+    c = lib.dflash_batch_context(b, s)
+    if not c:
+        check(DFLASH_ERR_ARG)
+    return c
+
+
+def dflash_batch_draft(b, draft_ids, stream=None):
+    check(lib.dflash_batch_draft(b, _ptr(draft_ids), _stream(stream)))
+
+
+def dflash_batch_verify_accept(b, draft_ids, tokens_out, n_emitted, stream=None):
+    check(lib.dflash_batch_verify_accept(b, _ptr(draft_ids), _ptr(tokens_out), _ptr(n_emitted),
+                                         _stream(stream)))
+
+
+def dflash_batch_set_logits_out(b, verify_logits=None, draft_logits=None):
+    check(lib.dflash_batch_set_logits_out(b, _ptr(verify_logits), _ptr(draft_logits)))
+
+
+def dflash_batch_check(b, stream=None):
+    check(lib.dflash_batch_check(b, _stream(stream)))
+
+
+def dflash_batch_destroy(b) -> None:
+    lib.dflash_batch_destroy(b)

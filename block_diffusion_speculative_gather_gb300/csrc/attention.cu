@@ -236,10 +236,19 @@ attn_fused_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) 
     // sit at fixed positions, so they can be brought into L2 while the
     // predecessor still writes this forward's rows (L2 stays coherent with
     // those writes; the copies into shared memory come after the wait).
+    // Only the chunks the forward will read: the visible length comes from
+    // the round state read before the wait, as a hint (the state's writer
+    // may not have finished, so it may still hold the previous forward's
+    // length; a stale value only changes which chunks are prefetched, and
+    // boxes past the tensor are ignored).
     if (tid == 0 && (a.causal || a.window <= 0)) {
+        const volatile int* vs = reinterpret_cast<const volatile int*>(a.st);
+        const int hint = vs[offsetof(DevState, fwd_pos0) / 4] + vs[offsetof(DevState, fwd_T) / 4];
+        const int c_last = hint > 0 ? (hint - 1) / C : 0;
         const int np = min(f.split_chunks, 2);
         for (int i = 0; i < np; ++i) {
             const int c = sp * f.split_chunks + i;
+            if (c > c_last) break;
             const int krow = ((a.layer * 2 + 0) * a.n_kv + kh) * a.cap + c * C;
             const int vrow = ((a.layer * 2 + 1) * a.n_kv + kh) * a.cap + c * C;
 #pragma unroll
@@ -392,8 +401,14 @@ attn_tc_kernel(const __grid_constant__ AttnMaps maps, const AttnFusedArgs f) {
     const int kh = blockIdx.x, sp = blockIdx.y, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     if (tid == 0 && (a.causal || a.window <= 0)) {   // the split's chunks sit at fixed positions
+        // only chunks the forward reads (visible length from the state, a
+        // hint read before the wait, as in attn_fused_kernel)
+        const volatile int* vs = reinterpret_cast<const volatile int*>(a.st);
+        const int hint = vs[offsetof(DevState, fwd_pos0) / 4] + vs[offsetof(DevState, fwd_T) / 4];
+        const int c_last = hint > 0 ? (hint - 1) / C : 0;
 #pragma unroll
         for (int j = 0; j < NC; ++j) {
+            if (sp * NC + j > c_last) break;
             const int krow = ((a.layer * 2 + 0) * a.n_kv + kh) * a.cap + (sp * NC + j) * C;
             const int vrow = ((a.layer * 2 + 1) * a.n_kv + kh) * a.cap + (sp * NC + j) * C;
 #pragma unroll
@@ -691,6 +706,132 @@ prefill_attn_kernel(const __grid_constant__ PrefillMaps maps, const PrefillAttnA
 }
 
 template <int HD>
+__global__ void __launch_bounds__(128)
+batch_attn_kernel(const __grid_constant__ PrefillMaps maps, const BatchAttnArgs b) {
+    constexpr int C = ATTN_KEYS, HALVES = HD / 64;
+    const AttnMmaArgs& a = b.m;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int group = a.n_q / a.n_kv, qrows = group * 16;
+    uint8_t* Qs = sm;                                   // [HALVES][qrows][128 B]
+    uint8_t* KV = Qs + HALVES * qrows * 128;            // 2 x (K, V) [HALVES][64][128 B]
+    constexpr int KVB = HALVES * C * 128;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(KV + 4 * KVB);   // [0] q, [1..2] buffers
+
+    pdl_trigger();
+    pdl_wait();
+    const int kh = blockIdx.x, sq = blockIdx.y, tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    DevState* st = b.sts[sq];
+    const int T = st->fwd_T, pos0 = st->fwd_pos0;
+    const int hi = pos0 + T;
+    const int lo = (!a.causal && a.window > 0) ? max(0, pos0 - a.window) : 0;
+    const size_t ld = (size_t)a.n_q * HD;
+    auto store_row = [&](int t, int hq, int d, float v) {   // bf16 hi/lo of row 16 sq + t
+        const size_t i = (size_t)(16 * sq + t) * ld + (size_t)hq * HD + d;
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        reinterpret_cast<__nv_bfloat16*>(b.out_hi)[i] = h;
+        reinterpret_cast<__nv_bfloat16*>(b.out_lo)[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+    };
+    // rows past T (and a sequence without rows) hold zeros
+    for (int e = tid; e < 16 * group * HD; e += blockDim.x) {
+        const int t = e / (group * HD), rem = e % (group * HD);
+        if (t >= T) store_row(t, kh * group + rem / HD, rem % HD, 0.f);
+    }
+    if (T <= 0) return;
+    const int c_lo = lo / C, n_my = (hi - 1) / C - c_lo + 1;
+    const int layer_row = (sq * b.n_layers + a.layer) * 2;   // K run of this layer in the map
+
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    auto load_chunk = [&](int i) {   // chunk c_lo + i into buffer i & 1
+        uint8_t* Kb = KV + (i & 1) * 2 * KVB;
+        uint8_t* Vb = Kb + KVB;
+        const int c = c_lo + i;
+        const int krow = ((layer_row + 0) * a.n_kv + kh) * a.cap + c * C;
+        const int vrow = ((layer_row + 1) * a.n_kv + kh) * a.cap + c * C;
+        mbar_arrive_expect_tx(&bar[1 + (i & 1)], 2 * KVB);
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h) {
+            tma_load_2d(Kb + h * C * 128, &maps.kv, &bar[1 + (i & 1)], 64 * h, krow);
+            tma_load_2d(Vb + h * C * 128, &maps.kv, &bar[1 + (i & 1)], 64 * h, vrow);
+        }
+    };
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar[0], HALVES * qrows * 128);
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h)
+            tma_load_2d(Qs + h * qrows * 128, &maps.q, &bar[0], 64 * h, (sq * a.n_q + kh * group) * 16);
+        load_chunk(0);
+        if (n_my > 1) load_chunk(1);
+    }
+    bool ok = __syncthreads_and(mbar_wait_bounded(&bar[0], 0)) != 0;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    float o[HD / 8][4];
+#pragma unroll
+    for (int dt = 0; dt < HD / 8; ++dt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[dt][e] = 0.f;
+    int issued = n_my > 1 ? 2 : 1;
+    for (int i = 0; i < n_my && ok; ++i) {
+        ok = __syncthreads_and(mbar_wait_bounded(&bar[1 + (i & 1)], (uint32_t)((i >> 1) & 1))) != 0;
+        if (ok && warp < group)
+            adev::chunk_online<HD>(Qs, KV + (i & 1) * 2 * KVB, KV + (i & 1) * 2 * KVB + KVB, a, qrows,
+                                   c_lo + i, T, pos0, lo, hi, warp, lane, m, l, o);
+        __syncthreads();   // buffer i & 1 is free again
+        if (ok && tid == 0 && i + 2 < n_my) {
+            load_chunk(i + 2);
+            ++issued;
+        }
+    }
+    if (!ok) {
+        if (tid == 0) {
+            set_error(st, DERR_TIMEOUT, 230);
+            mbar_wait_bounded(&bar[0], 0, 100000000ull);
+            for (int i = 0; i < issued; ++i)
+                mbar_wait_bounded(&bar[1 + (i & 1)], (uint32_t)((i >> 1) & 1), 100000000ull);
+        }
+        return;
+    }
+    if (warp < group) {
+        const int g = lane >> 2, cq = lane & 3, hq = kh * group + warp;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int t = g + 8 * r;
+            if (t >= T) continue;
+            const float inv = 1.f / l[r];
+#pragma unroll
+            for (int dt = 0; dt < HD / 8; ++dt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) store_row(t, hq, dt * 8 + 2 * cq + e, o[dt][2 * r + e] * inv);
+        }
+    }
+}
+
+template <int HD>
+int launch_batch_hd(const CUtensorMap& q_map, const CUtensorMap& kv_map, const BatchAttnArgs& b, int S,
+                    cudaStream_t s) {
+    const int qrows = (b.m.n_q / b.m.n_kv) * 16;
+    const size_t smem = 1024 + (size_t)(HD / 64) * (qrows + 4 * ATTN_KEYS) * 128 + 3 * 8 + 64;
+    static bool set = false;
+    if (!set) {
+        const cudaError_t e = cudaFuncSetAttribute(batch_attn_kernel<HD>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return (int)e;
+        set = true;
+    }
+    PrefillMaps maps;
+    maps.q = q_map;
+    maps.kv = kv_map;
+    return (int)launch_k(batch_attn_kernel<HD>, dim3((unsigned)b.m.n_kv, (unsigned)S), dim3(128), smem, s,
+                         maps, b);
+}
+
+template <int HD>
 int launch_prefill_hd(const CUtensorMap& q_map, const CUtensorMap& kv_map, const PrefillAttnArgs& p,
                       cudaStream_t s) {
     const int qrows = (p.m.n_q / p.m.n_kv) * 16;
@@ -788,6 +929,13 @@ int launch_prefill_attention(const CUtensorMap& q_map, const CUtensorMap& kv_map
     if (p.rows < 1) return 0;
     if (p.m.head_dim == 128) return launch_prefill_hd<128>(q_map, kv_map, p, s);
     if (p.m.head_dim == 64) return launch_prefill_hd<64>(q_map, kv_map, p, s);
+    return (int)cudaErrorInvalidValue;
+}
+
+int launch_batch_attention(const CUtensorMap& q_map, const CUtensorMap& kv_map, const BatchAttnArgs& b,
+                           int S, cudaStream_t s) {
+    if (b.m.head_dim == 128) return launch_batch_hd<128>(q_map, kv_map, b, S, s);
+    if (b.m.head_dim == 64) return launch_batch_hd<64>(q_map, kv_map, b, S, s);
     return (int)cudaErrorInvalidValue;
 }
 

@@ -61,6 +61,24 @@ struct PrefillAttnArgs {
 };
 int launch_prefill_attention(const CUtensorMap& q_map, const CUtensorMap& kv_map, const PrefillAttnArgs& p,
                              cudaStream_t s);
+// Attention of a many-sequence round: sequence s's 16 rows (its forward's
+// T rows at positions pos0 .. pos0 + T - 1, from its round state) against
+// its own cache rows, causal (verify) or [window context | bidirectional
+// block] (draft).  The caches of all sequences are one map
+// [S][layers][2][n_kv][cap][hd] (f16); q rows [S][n_q][16][hd] (f16, box =
+// one kv head's q group).  One CTA per (kv head, sequence) folds every
+// visible 64-key chunk with the online softmax of the round's attention and
+// writes the normalised rows as bf16 hi/lo planes [S * 16][n_q * hd]
+// (rows past T zero).
+struct BatchAttnArgs {
+    AttnMmaArgs m;            // shapes, layer, cap, causal, window, scale
+    DevState* const* sts;     // [S] round state of each sequence
+    int n_layers;             // layers of the cache map's model
+    void* out_hi;
+    void* out_lo;
+};
+int launch_batch_attention(const CUtensorMap& q_map, const CUtensorMap& kv_map, const BatchAttnArgs& b,
+                           int S, cudaStream_t s);
 // Host: CTAs of the fused attention kernel one SM holds, for head_dim hd.
 int attention_fused_per_sm(int hd, int n_q, int n_kv, int* out);
 // Host: the same for the tcgen05 form with nc (1 or 2) chunks per split,

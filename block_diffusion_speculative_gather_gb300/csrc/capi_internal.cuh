@@ -1,0 +1,20 @@
+// Host accessors of a context for the C-ABI source files other than the one
+// that defines the context (the many-sequence round builds on contexts).
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include "../../include/dflash.h"
+#include "common.cuh"
+
+namespace dfl {
+
+DevState* ctx_state(const dflash_ctx* c);               // device round state
+const double* ctx_inv_freq(const dflash_ctx* c);        // device RoPE frequencies [head_dim/2]
+const dflash_layer* ctx_layers(const dflash_ctx* c, bool target);   // host copies
+const dflash_weights& ctx_weights(const dflash_ctx* c);
+// 2D tensor map over a row-major [rows][inner] matrix of es-byte elements.
+int encode_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es, uint64_t inner,
+               uint64_t rows, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz);
+
+}  // namespace dfl

@@ -30,6 +30,7 @@
 #include "gemm.cuh"
 #include "kernels.cuh"
 #include "round.cuh"
+#include "capi_internal.cuh"
 
 using namespace dfl;
 
@@ -877,6 +878,19 @@ int make_linear_maps(GemmMaps* maps, const void* w, const void* x, int n, int k)
     r = make_map(&maps->w[0], w, XT_BF16, k, n, GEMM_BN);
     if (!r) r = make_map(&maps->x, x, XT_BF16, k, DFL_MAX_ROWS, DFL_MAX_ROWS);
     return r;
+}
+
+DevState* ctx_state(const dflash_ctx* c) { return c->st(); }
+const double* ctx_inv_freq(const dflash_ctx* c) { return c->buf<double>(c->L.invf); }
+const dflash_layer* ctx_layers(const dflash_ctx* c, bool target) {
+    return target ? c->tgt.data() : c->drf.data();
+}
+const dflash_weights& ctx_weights(const dflash_ctx* c) { return c->w; }
+int encode_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int es, uint64_t inner,
+               uint64_t rows, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
+    int r = get_encode();
+    if (r) return r;
+    return make_map_raw(m, base, dt, es, inner, rows, box_inner, box_rows, swz);
 }
 
 int run_linear_store(const void* w, const void* x, int n, int k, float* y, float* slots,

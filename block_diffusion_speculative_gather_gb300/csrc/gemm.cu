@@ -251,14 +251,14 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
     gdev::compute_rstd<EPI>(a, s_rstd, tid);   // read after the first tile's barrier
     int stage = 0;
     uint32_t phase = 0;
-    float acc[8];
+    float acc[8], accl[8];   // hi and lo planes' accumulators, added at the tile's finish
 
     for (long long u = u0; u < u1;) {
         const int len = chunk_len(u);
         const int tile = (int)(u / a.kb), k = (int)(u % a.kb);
         if (k == 0 || u == u0) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+            for (int i = 0; i < 8; ++i) acc[i] = accl[i] = 0.f;
         }
         bool ok = false;
         if (!s_flags[0]) {
@@ -277,7 +277,7 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
             const uint8_t* Wt = Ws + (stage * CHUNK + jb) * GEMM_STAGE_W;
             const uint8_t* Xt = Xs + (stage * CHUNK + jb) * XB;
             const uint8_t* Sb = Ss + (stage * CHUNK + jb) * SB;
-            mma_kblock<WF, EPI>(Wt, Xt, Sb, a, warp, lane, acc);
+            mma_kblock<WF, EPI>(Wt, Xt, Sb, a, warp, lane, acc, accl);
             }   // k-blocks of the stage
         }
         __syncwarp();
@@ -288,7 +288,8 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
 
         if (!(k + len == a.kb || u == u1)) continue;
         if (tid == 0 && u == u1) GEMM_TS(5);
-
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += accl[i];
         finish_tile<WF, EPI>(a, tile, acc, ctile, s_flags, s_rstd, U, G, blockIdx.x, warp, lane,
                              tid);
     }

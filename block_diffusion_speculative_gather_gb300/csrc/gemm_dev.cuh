@@ -56,10 +56,14 @@ __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsig
 // Xt): swap-AB mma.sync with the weight rows as M and the 16 activation rows
 // as two n8 tiles (rows g, g + 8 of the C fragment are weight rows, columns
 // the tokens); the lo plane of a split input is multiplied by the same
-// weight fragments.  Sb: the INT4 scales of the k-block.
+// weight fragments into its own accumulators accl (four independent MMA
+// chains per warp instead of two: the chains' latency, not the tensor pipe,
+// bounds these MMAs), which the tile's finish adds to acc.  Sb: the INT4
+// scales of the k-block.
 template <int WF, int EPI>
 __device__ __forceinline__ void mma_kblock(const uint8_t* Wt, const uint8_t* Xt, const uint8_t* Sb,
-                                           const GemmArgs& a, int warp, int lane, float (&acc)[8]) {
+                                           const GemmArgs& a, int warp, int lane, float (&acc)[8],
+                                           float (&accl)[8]) {
     constexpr int XB = GemmCfg<WF>::XB;
     const int g = lane >> 2, c = lane & 3;
     if (WF == WF_INT4) {
@@ -70,7 +74,9 @@ __device__ __forceinline__ void mma_kblock(const uint8_t* Wt, const uint8_t* Xt,
         const int r0 = warp * 16 + g;
         const __nv_bfloat16* St = reinterpret_cast<const __nv_bfloat16*>(Sb);
         const __nv_bfloat162 bias = __floats2bfloat162_rn(136.f, 136.f);
-#pragma unroll
+        // one 64-k group at a time (a rolled loop: fewer live registers and
+        // a quarter of the code, which each CTA fetches cold)
+#pragma unroll 1
         for (int q = 0; q < 4; ++q) {
             const uint32_t off = swz128(r0, 2 * q + (c >> 1)) + 8 * (c & 1);
             const uint2 wa = *reinterpret_cast<const uint2*>(Wt + off);
@@ -105,7 +111,16 @@ __device__ __forceinline__ void mma_kblock(const uint8_t* Wt, const uint8_t* Xt,
                     pb[4 * m + i] = *reinterpret_cast<uint32_t*>(&vb);
                 }
             }
+            // hi and lo planes into their own accumulators, interleaved
+            uint32_t la[8], lb[8];
+            if (a.x_split) {   // lo planes: tokens g, g + 8 at rows 16 + g, 24 + g
+                *reinterpret_cast<uint4*>(&la[0]) = lds128(Xq + swz128(16 + g, 2 * c));
+                *reinterpret_cast<uint4*>(&la[4]) = lds128(Xq + swz128(16 + g, 2 * c + 1));
+                *reinterpret_cast<uint4*>(&lb[0]) = lds128(Xq + swz128(24 + g, 2 * c));
+                *reinterpret_cast<uint4*>(&lb[4]) = lds128(Xq + swz128(24 + g, 2 * c + 1));
+            }
             float g0[4] = {0.f, 0.f, 0.f, 0.f}, g1[4] = {0.f, 0.f, 0.f, 0.f};
+            float h0[4] = {0.f, 0.f, 0.f, 0.f}, h1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t A[4] = {pa[2 * j], pb[2 * j], pa[2 * j + 1], pb[2 * j + 1]};
@@ -113,19 +128,11 @@ __device__ __forceinline__ void mma_kblock(const uint8_t* Wt, const uint8_t* Xt,
                 const uint32_t B1[2] = {xb[2 * j], xb[2 * j + 1]};
                 mma_bf16_16816(g0, A, B0);
                 mma_bf16_16816(g1, A, B1);
-            }
-            if (a.x_split) {   // lo planes: tokens g, g + 8 at rows 16 + g, 24 + g
-                *reinterpret_cast<uint4*>(&xa[0]) = lds128(Xq + swz128(16 + g, 2 * c));
-                *reinterpret_cast<uint4*>(&xa[4]) = lds128(Xq + swz128(16 + g, 2 * c + 1));
-                *reinterpret_cast<uint4*>(&xb[0]) = lds128(Xq + swz128(24 + g, 2 * c));
-                *reinterpret_cast<uint4*>(&xb[4]) = lds128(Xq + swz128(24 + g, 2 * c + 1));
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t A[4] = {pa[2 * j], pb[2 * j], pa[2 * j + 1], pb[2 * j + 1]};
-                    const uint32_t B0[2] = {xa[2 * j], xa[2 * j + 1]};
-                    const uint32_t B1[2] = {xb[2 * j], xb[2 * j + 1]};
-                    mma_bf16_16816(g0, A, B0);
-                    mma_bf16_16816(g1, A, B1);
+                if (a.x_split) {
+                    const uint32_t L0[2] = {la[2 * j], la[2 * j + 1]};
+                    const uint32_t L1[2] = {lb[2 * j], lb[2 * j + 1]};
+                    mma_bf16_16816(h0, A, L0);
+                    mma_bf16_16816(h1, A, L1);
                 }
             }
             acc[0] = fmaf(sa, g0[0], acc[0]);
@@ -136,6 +143,16 @@ __device__ __forceinline__ void mma_kblock(const uint8_t* Wt, const uint8_t* Xt,
             acc[5] = fmaf(sa, g1[1], acc[5]);
             acc[6] = fmaf(sb, g1[2], acc[6]);
             acc[7] = fmaf(sb, g1[3], acc[7]);
+            if (a.x_split) {
+                accl[0] = fmaf(sa, h0[0], accl[0]);
+                accl[1] = fmaf(sa, h0[1], accl[1]);
+                accl[2] = fmaf(sb, h0[2], accl[2]);
+                accl[3] = fmaf(sb, h0[3], accl[3]);
+                accl[4] = fmaf(sa, h1[0], accl[4]);
+                accl[5] = fmaf(sa, h1[1], accl[5]);
+                accl[6] = fmaf(sb, h1[2], accl[6]);
+                accl[7] = fmaf(sb, h1[3], accl[7]);
+            }
         }
     } else if (WF == WF_BF16) {
         const int r0 = warp * 16 + g;
@@ -150,6 +167,15 @@ __device__ __forceinline__ void mma_kblock(const uint8_t* Wt, const uint8_t* Xt,
         *reinterpret_cast<uint4*>(&xb[4]) = lds128(Xt + swz128(g + 8, 2 * c + 1));
         float(&d0)[4] = *reinterpret_cast<float(*)[4]>(&acc[0]);
         float(&d1)[4] = *reinterpret_cast<float(*)[4]>(&acc[4]);
+        float(&e0)[4] = *reinterpret_cast<float(*)[4]>(&accl[0]);
+        float(&e1)[4] = *reinterpret_cast<float(*)[4]>(&accl[4]);
+        uint32_t la[8], lb[8];
+        if (a.x_split) {   // lo planes: tokens g, g + 8 at rows 16 + g, 24 + g
+            *reinterpret_cast<uint4*>(&la[0]) = lds128(Xt + swz128(16 + g, 2 * c));
+            *reinterpret_cast<uint4*>(&la[4]) = lds128(Xt + swz128(16 + g, 2 * c + 1));
+            *reinterpret_cast<uint4*>(&lb[0]) = lds128(Xt + swz128(24 + g, 2 * c));
+            *reinterpret_cast<uint4*>(&lb[4]) = lds128(Xt + swz128(24 + g, 2 * c + 1));
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const uint32_t A[4] = {ra[2 * j], rb[2 * j], ra[2 * j + 1], rb[2 * j + 1]};
@@ -157,19 +183,11 @@ __device__ __forceinline__ void mma_kblock(const uint8_t* Wt, const uint8_t* Xt,
             const uint32_t B1[2] = {xb[2 * j], xb[2 * j + 1]};
             mma_bf16_16816(d0, A, B0);
             mma_bf16_16816(d1, A, B1);
-        }
-        if (a.x_split) {   // lo planes: tokens g, g + 8 at rows 16 + g, 24 + g
-            *reinterpret_cast<uint4*>(&xa[0]) = lds128(Xt + swz128(16 + g, 2 * c));
-            *reinterpret_cast<uint4*>(&xa[4]) = lds128(Xt + swz128(16 + g, 2 * c + 1));
-            *reinterpret_cast<uint4*>(&xb[0]) = lds128(Xt + swz128(24 + g, 2 * c));
-            *reinterpret_cast<uint4*>(&xb[4]) = lds128(Xt + swz128(24 + g, 2 * c + 1));
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t A[4] = {ra[2 * j], rb[2 * j], ra[2 * j + 1], rb[2 * j + 1]};
-                const uint32_t B0[2] = {xa[2 * j], xa[2 * j + 1]};
-                const uint32_t B1[2] = {xb[2 * j], xb[2 * j + 1]};
-                mma_bf16_16816(d0, A, B0);
-                mma_bf16_16816(d1, A, B1);
+            if (a.x_split) {
+                const uint32_t L0[2] = {la[2 * j], la[2 * j + 1]};
+                const uint32_t L1[2] = {lb[2 * j], lb[2 * j + 1]};
+                mma_bf16_16816(e0, A, L0);
+                mma_bf16_16816(e1, A, L1);
             }
         }
     } else {  // WF_F32: CUDA-core FMAs, k in order

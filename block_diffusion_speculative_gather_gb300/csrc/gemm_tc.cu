@@ -1,7 +1,8 @@
 // Dense many-row GEMM on tcgen05 (see gemm_tc.cuh).
 //
 // One CTA per 128 x BN output tile (BN 256, or 128 where that balances
-// the waves over the SMs better), 128 threads.  Thread 0 is the TMA
+// the waves over the SMs better, or as the caller fixes it) and k-split,
+// 128 threads.  Thread 0 is the TMA
 // producer: a ring of k-blocks (the x tile [128][64], its low plane when
 // x_split, and the w tile [256][64], bf16 or all f16, 128-byte swizzled,
 // K-major).  Thread 32 issues tcgen05.mma (M 128, N BN, K 16, f32
@@ -13,6 +14,13 @@
 // and w rows with zeros).  Every wait is bounded; a wait that times out
 // sets the device error word, and the MMA thread still commits, so the
 // tensor memory is freed only after the MMAs it issued have finished.
+// Split-K (few rows: the many-sequence round): the k-blocks of a tile are
+// cut into `splits` contiguous ranges in split order; each split stores its
+// fp32 partial tile and the last to arrive on the tile's ticket adds all
+// partials in split order, so a row's result is the same whatever the
+// number of rows.  The argmax epilogue (the LM head of that round) keeps per
+// row the packed (orderable logit, ~column) key of its largest column and
+// folds it into the row's key with atomicMax (lowest column on ties).
 
 #include "gemm_tc.cuh"
 #include "tc_dev.cuh"
@@ -50,7 +58,11 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * DT_BM, n0 = blockIdx.y * BN;
-    const int nkb = a.K / DT_BK;
+    // this CTA's k-blocks: split z of Z takes [nkb z / Z, nkb (z + 1) / Z)
+    const int Z = a.splits > 1 ? a.splits : 1, z = blockIdx.z;
+    const int kb_lo = (int)((long long)(a.K / DT_BK) * z / Z);
+    const int nkb = (int)((long long)(a.K / DT_BK) * (z + 1) / Z) - kb_lo;
+    __shared__ int s_last;
     const int seg = n0 >= a.n_seg1 ? 2 : n0 >= a.n_seg0 ? 1 : 0;
     const int wrow = n0 - (seg == 2 ? a.n_seg1 : seg == 1 ? a.n_seg0 : 0);
 
@@ -83,13 +95,14 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
                 break;
             }
             uint8_t* st = ring + s * CFG::STAGE;
+            const int kx = (kb_lo + kb) * DT_BK;
             mbar_arrive_expect_tx(&full[s], CFG::STAGE);
-            tma_load_2d(st, &maps.x, &full[s], kb * DT_BK, a.m_off + m0);
-            if (SPLIT) tma_load_2d(st + CFG::XB, &maps.x_lo, &full[s], kb * DT_BK, a.m_off + m0);
+            tma_load_2d(st, &maps.x, &full[s], kx, a.m_off + m0);
+            if (SPLIT) tma_load_2d(st + CFG::XB, &maps.x_lo, &full[s], kx, a.m_off + m0);
 #pragma unroll
             for (int b = 0; b < BN / DT_WBOX; ++b)
                 tma_load_2d(st + (SPLIT ? 2 : 1) * CFG::XB + b * DT_WBOX * 128, &maps.w[seg], &full[s],
-                            kb * DT_BK, wrow + b * DT_WBOX);
+                            kx, wrow + b * DT_WBOX);
         }
     } else if (threadIdx.x == 32) {   // ---- MMA issuer
         constexpr uint32_t ID = F16 ? tc::idesc_f16_f32(DT_BM, BN) : tc::idesc_bf16_f32(DT_BM, BN);
@@ -120,28 +133,81 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
     ok = __syncthreads_and(ok) != 0;   // the barrier also orders the s_fail writes
     ok = ok && s_fail == 0;
     tc::fence_after_sync();
-    if (ok) {
-        const int row = m0 + 32 * warp + lane;
-        const uint32_t trow = tm + ((uint32_t)(32 * warp) << 16);
+    const int row = m0 + 32 * warp + lane;
+    const int tile = blockIdx.x * gridDim.y + blockIdx.y;
+    float* mypart = a.part + (((size_t)tile * Z + z) * DT_BM + 32 * warp + lane) * BN;
+    bool last = true;
+    if (ok && Z > 1) {
+        // publish this split's partial tile; the last split to arrive sums
+        // every partial in split order and runs the epilogue
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
             float v[32];
-            tc::ld_x32(trow + 32 * c, v);
+            tc::ld_x32(tm + ((uint32_t)(32 * warp) << 16) + 32 * c, v);
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+                __stcg(reinterpret_cast<float4*>(mypart + 32 * c + i),
+                       make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+        }
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) s_last = atomicAdd(&a.tickets[tile], 1) == Z - 1 ? 1 : 0;
+        __syncthreads();
+        last = s_last != 0;
+        if (last) {
+            __threadfence();
+            if (threadIdx.x == 0) a.tickets[tile] = 0;   // ready for the next launch
+        }
+    }
+    if (ok && last) {
+        const float* rows0 = a.part + (((size_t)tile * Z) * DT_BM + 32 * warp + lane) * BN;
+        unsigned long long best = 0ull;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            if (Z > 1) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                for (int zz = 0; zz < Z; ++zz) {   // split order: the same for every M
+                    const float* src = rows0 + (size_t)zz * DT_BM * BN + 32 * c;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 p4 = __ldcg(reinterpret_cast<const float4*>(src + i));
+                        v[i] += p4.x;
+                        v[i + 1] += p4.y;
+                        v[i + 2] += p4.z;
+                        v[i + 3] += p4.w;
+                    }
+                }
+            } else {
+                tc::ld_x32(tm + ((uint32_t)(32 * warp) << 16) + 32 * c, v);
+            }
             const int col = n0 + 32 * c;
             if (row < a.M && col < a.N) {
-                float* dst = a.y + (size_t)row * a.ldy + col;
-                if (col + 32 <= a.N) {
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                } else {
+                if (a.amax) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        if (col + i < a.N) dst[i] = v[i];
+                        if (col + i < a.N) {
+                            const unsigned long long key = argmax_key(v[i], col + i);
+                            best = key > best ? key : best;
+                        }
+                }
+                if (a.y) {
+                    float* dst = a.y + (size_t)row * a.ldy + col;
+                    if (col + 32 <= a.N) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (col + i < a.N) dst[i] = v[i];
+                    }
                 }
             }
         }
-    } else if (threadIdx.x == 0 && s_fail == 0) {
+        if (a.amax && row < a.M) atomicMax(a.amax + row, best);
+    } else if (!ok && threadIdx.x == 0 && s_fail == 0) {
         dense_error(a.err, 302);
     }
     tc::fence_before_sync();
@@ -160,7 +226,8 @@ int launch_one(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return (int)e;
         set = true;
     }
-    const dim3 grid((unsigned)((a.M + DT_BM - 1) / DT_BM), (unsigned)((a.N + BN - 1) / BN));
+    const dim3 grid((unsigned)((a.M + DT_BM - 1) / DT_BM), (unsigned)((a.N + BN - 1) / BN),
+                    (unsigned)(a.splits > 1 ? a.splits : 1));
     return (int)launch_k(gemm_dense_kernel<SPLIT, F16, BN>, grid, dim3(128), smem, s, maps, a);
 }
 
@@ -176,6 +243,8 @@ int launch_bn(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
             sms = 1;
     }
+    if (a.bn == 128) return launch_one<SPLIT, F16, 128>(maps, a, s);
+    if (a.bn == 256) return launch_one<SPLIT, F16, 256>(maps, a, s);
     const long long mt = (a.M + DT_BM - 1) / DT_BM;
     const long long w256 = (mt * ((a.N + 255) / 256) + sms - 1) / sms;
     const long long w128 = (mt * ((a.N + 127) / 128) + sms - 1) / sms;
@@ -185,11 +254,20 @@ int launch_bn(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+size_t dense_split_floats(int M, int N, int splits, int bn) {
+    return (size_t)dense_tiles(M, N, bn) * (size_t)(splits > 1 ? splits : 1) * DT_BM * bn;
+}
+
+int dense_tiles(int M, int N, int bn) { return ((M + DT_BM - 1) / DT_BM) * ((N + bn - 1) / bn); }
+
 size_t dense_smem(bool split) { return split ? DenseCfg<true, DT_BN>::SMEM : DenseCfg<false, DT_BN>::SMEM; }
 
 int launch_dense(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
-    if (a.M < 1 || a.N < 1 || a.K < DT_BK || a.K % DT_BK || a.ldy < a.N || a.ldy % 4 ||
-        a.n_seg0 % DT_BN || (a.n_seg1 < a.N && (a.n_seg1 % DT_BN || a.n_seg1 < a.n_seg0)) || a.m_off < 0)
+    if (a.M < 1 || a.N < 1 || a.K < DT_BK || a.K % DT_BK || (a.y && (a.ldy < a.N || a.ldy % 4)) ||
+        (!a.y && !a.amax) || a.n_seg0 % DT_BN ||
+        (a.n_seg1 < a.N && (a.n_seg1 % DT_BN || a.n_seg1 < a.n_seg0)) || a.m_off < 0 ||
+        (a.bn != 0 && a.bn != 128 && a.bn != 256) || a.splits > a.K / DT_BK ||
+        (a.splits > 1 && (a.bn == 0 || !a.part || !a.tickets)))
         return (int)cudaErrorInvalidValue;
     if (a.f16) return a.x_split ? launch_bn<true, true>(maps, a, s) : launch_bn<false, true>(maps, a, s);
     return a.x_split ? launch_bn<true, false>(maps, a, s) : launch_bn<false, false>(maps, a, s);

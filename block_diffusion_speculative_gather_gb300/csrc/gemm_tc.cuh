@@ -34,10 +34,26 @@ struct DenseArgs {
     int m_off;          // rows of x to skip: output row m reads x row m_off + m
     int x_split;        // 1: x = x (hi) + x_lo, two MMAs per k step
     int f16;            // 1: x and w are f16 (else bf16); both operands always share one type
-    float* y;           // [M][ldy] fp32
+    float* y;           // [M][ldy] fp32 (argmax epilogue: optional logits dump, or NULL)
     int ldy;            // a multiple of 4
     int* err;           // device [code, site]: a wait that timed out sets it (code 0 before)
+    // split-K: `splits` CTAs per output tile share its k-blocks (contiguous
+    // ranges in split order); each stores its fp32 partial tile in `part`
+    // ([tiles][splits][128][bn]) and the last to arrive on the tile's ticket
+    // adds the partials in split order 0, 1, ... (so a row's result depends
+    // on N, K and `splits`, never on M or timing) and runs the epilogue.
+    int splits;         // 1: no split
+    float* part;
+    int* tickets;       // [m tiles * n tiles], zero between launches
+    int bn;             // tile width: 0 = chosen by wave balance, else 128 or 256
+    // argmax epilogue (LM head): per row the packed key (orderable logit,
+    // ~column) of the largest column, atomicMax into amax[row]
+    unsigned long long* amax;   // NULL: the plain fp32 store
 };
+
+// Host: partial-tile floats a split launch needs, and its ticket count.
+size_t dense_split_floats(int M, int N, int splits, int bn);
+int dense_tiles(int M, int N, int bn);
 
 // Host: dynamic shared memory of the kernel (x_split or not), the launch
 // (grid ceil(M/128) x ceil(N/BN), 128 threads; BN 256, or 128 where that

@@ -264,13 +264,13 @@ __device__ __forceinline__ void gemm_phase(int epi, const GemmArgs& a, uint8_t* 
         case EPI_QKV: gdev::compute_rstd<EPI_QKV>(a, s_rstd, tid); break;
         default: break;
     }
-    float acc[8];
+    float acc[8], accl[8];   // hi and lo planes' accumulators, added at the tile's finish
     for (long long u = u0; u < u1;) {
         const int len = chunk_len(u, u1, a.kb);
         const int tile = (int)(u / a.kb), k = (int)(u % a.kb);
         if (k == 0 || u == u0) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+            for (int i = 0; i < 8; ++i) acc[i] = accl[i] = 0.f;
         }
         bool ok = false;
         if (!s_flags[0]) {
@@ -284,7 +284,7 @@ __device__ __forceinline__ void gemm_phase(int epi, const GemmArgs& a, uint8_t* 
             for (int jb = 0; jb < len; ++jb) {
                 const int slot = stage * ROUND_CHUNK + jb;
                 gdev::mma_kblock<WF_BF16, EPI_STORE>(Ws + slot * GEMM_STAGE_W, Xs + slot * RXB,
-                                                     nullptr, a, warp, lane, acc);
+                                                     nullptr, a, warp, lane, acc, accl);
             }
         }
         __syncwarp();
@@ -296,6 +296,8 @@ __device__ __forceinline__ void gemm_phase(int epi, const GemmArgs& a, uint8_t* 
         }
         u += len;
         if (!(k + len == a.kb || u == u1)) continue;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += accl[i];
         switch (epi) {
             case EPI_STORE:
                 finish_out_of_line<EPI_STORE>(a, tile, acc, ctile, s_flags, s_rstd, U, warp, lane, tid);

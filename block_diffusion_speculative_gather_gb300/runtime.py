@@ -52,6 +52,26 @@ class DFlash:
     """One generation context on one GPU."""
 
     def __init__(self, w: Workload, model, device: str = "cuda", stream=None, **cfg_over):
+        self._load(w, model, device, stream, **cfg_over)
+        kvt = capi.dflash_kv_target_bytes(self.cfg)
+        kvd = capi.dflash_kv_draft_bytes(self.cfg)
+        wsb = capi.dflash_workspace_bytes(self.cfg)
+        if wsb == 0:
+            capi.check(-1)
+        self.kv_target = torch.zeros(max(kvt, 16), dtype=torch.uint8, device=self.device)
+        self.kv_draft = torch.zeros(max(kvd, 16), dtype=torch.uint8, device=self.device)
+        self.workspace = torch.zeros(wsb, dtype=torch.uint8, device=self.device)
+        torch.cuda.synchronize(self.device)
+        self.ctx = capi.dflash_init(self.cfg, self._weights, self.kv_target, self.kv_draft,
+                                    self.workspace)
+        B = w.block
+        self.draft_ids = torch.full((max(1, B - 1),), -1, dtype=torch.int32, device=self.device)
+        self.tokens_out = torch.full((B,), -1, dtype=torch.int32, device=self.device)
+        self.n_emitted = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    def _load(self, w: Workload, model, device, stream, **cfg_over):
+        """Weights on the device (INT4 copies made by the library's
+        quantiser) and the C structs that point at them."""
         self.w = w
         self.device = torch.device(device)
         self._stream = stream      # None: the current stream at each call
@@ -71,14 +91,6 @@ class DFlash:
         self.lm_head = self.lm_scales = None
         if w.lm_int4:
             self.lm_head, self.lm_scales = self._quantize(self.embed)
-        kvt = capi.dflash_kv_target_bytes(self.cfg)
-        kvd = capi.dflash_kv_draft_bytes(self.cfg)
-        wsb = capi.dflash_workspace_bytes(self.cfg)
-        if wsb == 0:
-            capi.check(-1)
-        self.kv_target = torch.zeros(max(kvt, 16), dtype=torch.uint8, device=self.device)
-        self.kv_draft = torch.zeros(max(kvd, 16), dtype=torch.uint8, device=self.device)
-        self.workspace = torch.zeros(wsb, dtype=torch.uint8, device=self.device)
         self._layers_t = (capi.dflash_layer * max(1, len(self.tgt)))(
             *[self._layer(lw) for lw in self.tgt])
         self._layers_d = (capi.dflash_layer * max(1, len(self.drf)))(
@@ -95,12 +107,6 @@ class DFlash:
             wts.lm_head = self.lm_head.data_ptr()
             wts.lm_scales = self.lm_scales.data_ptr()
         self._weights = wts
-        torch.cuda.synchronize(self.device)
-        self.ctx = capi.dflash_init(self.cfg, wts, self.kv_target, self.kv_draft, self.workspace)
-        B = w.block
-        self.draft_ids = torch.full((max(1, B - 1),), -1, dtype=torch.int32, device=self.device)
-        self.tokens_out = torch.full((B,), -1, dtype=torch.int32, device=self.device)
-        self.n_emitted = torch.zeros(1, dtype=torch.int32, device=self.device)
 
     def _quantize(self, w: torch.Tensor):
         """INT4 group-64 (packed [n][k/2], bf16 scales [k/64][n]) of w [n][k]."""
@@ -255,3 +261,92 @@ class DFlash:
             self.close()
         except Exception:
             pass
+
+
+class DFlashBatch(DFlash):
+    """S independent sequences of one model decoded in lockstep rounds: one
+    drafter forward and one target forward over all sequences' rows per
+    round (dflash_batch_*).  Each sequence is a context of its own."""
+
+    def __init__(self, w: Workload, model, S: int, device: str = "cuda", stream=None, **cfg_over):
+        self._load(w, model, device, stream, **cfg_over)
+        self.S = S
+        kvt = capi.dflash_kv_target_bytes(self.cfg)
+        kvd = capi.dflash_kv_draft_bytes(self.cfg)
+        wsb = capi.dflash_batch_workspace_bytes(self.cfg, S)
+        if wsb == 0:
+            capi.check(-1)
+        self.kv_target = torch.zeros(max(S * kvt, 16), dtype=torch.uint8, device=self.device)
+        self.kv_draft = torch.zeros(max(S * kvd, 16), dtype=torch.uint8, device=self.device)
+        self.workspace = torch.zeros(wsb, dtype=torch.uint8, device=self.device)
+        torch.cuda.synchronize(self.device)
+        self.batch = capi.dflash_batch_init(self.cfg, self._weights, S, self.kv_target,
+                                            self.kv_draft, self.workspace)
+        self.ctxs = [capi.dflash_batch_context(self.batch, s) for s in range(S)]
+        self.ctx = None
+        B = w.block
+        self.draft_ids = torch.full((S, max(1, B - 1)), -1, dtype=torch.int32, device=self.device)
+        self.tokens_out = torch.full((S, B), -1, dtype=torch.int32, device=self.device)
+        self.n_emitted = torch.zeros(S, dtype=torch.int32, device=self.device)
+        self._prompts = [None] * S
+
+    def prefill(self, prompts, max_new):
+        """prompts: S token tensors (lengths may differ); max_new: one budget
+        or one per sequence."""
+        budgets = list(max_new) if isinstance(max_new, (list, tuple)) else [max_new] * self.S
+        for s, (p, b) in enumerate(zip(prompts, budgets)):
+            self._prompts[s] = p.to(self.device, torch.int32).contiguous()
+            capi.dflash_prefill_taps(self.ctxs[s], self._prompts[s], None, 0, 1, 0, b, self.stream)
+
+    def draft(self, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        out = self.draft_ids if out is None else out
+        capi.dflash_batch_draft(self.batch, out, self.stream)
+        return out
+
+    def verify(self, draft_ids: Optional[torch.Tensor]):
+        capi.dflash_batch_verify_accept(self.batch, draft_ids, self.tokens_out, self.n_emitted,
+                                        self.stream)
+        return self.tokens_out, self.n_emitted
+
+    def stats(self, s: int = 0) -> capi.dflash_stats_t:
+        return capi.dflash_stats(self.ctxs[s], self.stream)
+
+    def check(self):
+        capi.dflash_batch_check(self.batch, self.stream)
+
+    def set_logits_out(self, verify_logits=None, draft_logits=None):
+        capi.dflash_batch_set_logits_out(self.batch, verify_logits, draft_logits)
+
+    def rollback(self, new_len: int, token: int, s: int = 0):
+        capi.dflash_rollback(self.ctxs[s], new_len, token, self.stream)
+
+    def _loop(self, prompts, max_new, speculative: bool, draft_fn=None) -> List[List[int]]:
+        self.prefill(prompts, max_new)
+        outs = [[self.stats(s).t_n] for s in range(self.S)]
+        while True:
+            sts = [self.stats(s) for s in range(self.S)]
+            if all(st.finished for st in sts):
+                break
+            if speculative:
+                d = draft_fn(self) if draft_fn is not None else self.draft()
+            else:
+                d = None
+            toks, n = self.verify(d)
+            toks, n = toks.cpu().tolist(), n.cpu().tolist()
+            for s in range(self.S):
+                outs[s].extend(toks[s][: n[s]])
+        return outs
+
+    def generate(self, prompts, max_new, draft_fn=None) -> List[List[int]]:
+        """Speculative decoding of every sequence in lockstep rounds."""
+        return self._loop(prompts, max_new, True, draft_fn)
+
+    def greedy(self, prompts, max_new) -> List[List[int]]:
+        """Plain greedy decoding of every sequence, one batched row each step."""
+        return self._loop(prompts, max_new, False)
+
+    def close(self):
+        if getattr(self, "batch", None):
+            capi.dflash_batch_destroy(self.batch)
+            self.batch = None
+            self.ctxs = []

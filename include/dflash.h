@@ -328,6 +328,63 @@ int64_t dflash_launch_count(void);
 void dflash_destroy(dflash_ctx* ctx);
 const char* dflash_last_error(void);
 
+/* ---- several sequences in lockstep rounds ----------------------------- */
+
+/*
+ * A batch of S independent sequences (1 <= S <= 32) that share one model:
+ * each sequence is a context of its own (round state, target and draft
+ * caches, block length, budget, statistics), and a batched round runs one
+ * drafter forward and one target forward over every sequence's rows at
+ * once, so the weights stream once for all of them.  The pages verify one
+ * sequence's [1, 1 + m] rows per forward ("[RFC] DFlash", "Key
+ * Implementation Details", Phase 3) and note that the verify's cost follows
+ * its row count ("Performance"); batching sequences is this library's
+ * extension: every sequence's state moves exactly as dflash_draft_block /
+ * dflash_verify_accept would move it, and its tokens are its own
+ * single-sequence decode.  Sequence s owns rows 16 s .. 16 s + 15 of each
+ * forward; the 16 S-row GEMMs run on the dense tcgen05 GEMM (bf16 hi/lo
+ * activation planes, k-splits chosen from N and K only), so a sequence's
+ * results do not depend on S.  bf16 models only (dtype, target, drafter and
+ * the tied LM head bf16); head_dim 64 or 128.
+ *
+ * Memory (caller-owned, device): kv_target holds S consecutive target
+ * caches of dflash_kv_target_bytes(cfg) each, kv_draft S draft caches of
+ * dflash_kv_draft_bytes(cfg); workspace (dflash_batch_workspace_bytes, zero
+ * not required) holds the S contexts' workspaces and the batch's own rows.
+ * Errors: CONFIG (a configuration the batched round does not run), ARG,
+ * CUDA.
+ */
+typedef struct dflash_batch dflash_batch;
+size_t dflash_batch_workspace_bytes(const dflash_config* cfg /*host*/, int32_t S);
+int dflash_batch_init(const dflash_config* cfg /*host*/, const dflash_weights* w /*host*/, int32_t S,
+                      void* kv_target, void* kv_draft, void* workspace, size_t workspace_bytes,
+                      dflash_batch** out /*host*/);
+/* Sequence s's context, owned by the batch: start it with
+ * dflash_prefill_taps (or dflash_adopt_kv), read it with dflash_stats, roll
+ * it back with dflash_rollback, as any context; every such call must be
+ * ordered with the batch's calls on the GPU.  NULL for s outside [0, S). */
+dflash_ctx* dflash_batch_context(dflash_batch* b, int32_t s);
+/* One drafter forward over every sequence's block (its device-held block
+ * length, [t_n, MASK...] at its positions), writing draft_ids [S][block_max-1]
+ * int32 (sequence s's ids at s * (block_max - 1); entries past its block -1). */
+int dflash_batch_draft(dflash_batch* b, int32_t* draft_ids, dflash_stream_t stream);
+/* One target forward over every sequence's [t_n, d_1..d_{bl-1}] (draft_ids
+ * [S][block_max-1]; NULL: a one-row greedy step each), then per sequence the
+ * first-mismatch acceptance, KV rollback and the commit of its accepted
+ * rows' taps to its draft context: tokens_out [S][block_max] (unused -1),
+ * n_emitted [S].  Finished sequences emit 0. */
+int dflash_batch_verify_accept(dflash_batch* b, const int32_t* draft_ids, int32_t* tokens_out,
+                               int32_t* n_emitted, dflash_stream_t stream);
+/* Parity taps of the batched forwards: fp32 logits [16 S][vocab] (row
+ * 16 s + t = sequence s's forward row t; rows past its T hold padding) of
+ * every verify / draft while set; NULL switches it off. */
+int dflash_batch_set_logits_out(dflash_batch* b, float* verify_logits, float* draft_logits);
+/* Synchronises stream; reports a bounded wait of a batched GEMM that ran out
+ * (TIMEOUT) or the first sequence context whose error word is set (as
+ * dflash_check), clearing what it reports. */
+int dflash_batch_check(dflash_batch* b, dflash_stream_t stream);
+void dflash_batch_destroy(dflash_batch* b);
+
 /* ---- standalone operations ------------------------------------------- */
 
 /*
