@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--ncu-tap", type=int, default=0, metavar="ROWS",
                     help="run the hc tap reduce (4 layers, hc 4, hidden 4096) at ROWS rows, "
                          "3 launches, for an ncu capture")
+    ap.add_argument("--ncu-batch", type=int, default=0, metavar="S",
+                    help="one many-sequence round of S sequences inside NVTX range "
+                         "'dflash_batch' (with --layers: a cut target), for an ncu capture")
     ap.add_argument("--int4", action="store_true",
                     help="with --ncu-rounds: the e2e workload with every model in INT4 group-64")
     ap.add_argument("--no-e2e", action="store_true")
@@ -426,7 +429,7 @@ def run_ours(args):
     # the oracle baseline (N = 1 only): its worker prepares while the GPU runs
     cpu_leg = None
     if not (args.no_cpu_baseline or args.ncu_dense or args.ncu_prefill or args.ncu_rounds
-            or args.ncu_tap or args.layers) and rank == 0 and world == 1:
+            or args.ncu_tap or args.ncu_batch or args.layers) and rank == 0 and world == 1:
         cpu_leg = CpuBaseline()
     if world > 1:
         dist.init_process_group("nccl")
@@ -484,6 +487,24 @@ def run_ours(args):
         dec.check()
         print("ncu prefill done", flush=True)
         dec.close()
+        return
+    if args.ncu_batch:
+        from block_diffusion_speculative_gather_gb300.runtime import DFlashBatch
+        dec.close()
+        S = args.ncu_batch
+        bdec = DFlashBatch(w, model_for_sweep if model_for_sweep is not None else synth.ModelTensors(w), S)
+        prompts = [torch.from_numpy(synth.uniform_ids(w.prompt_len, w.vocab, seed=100 + i))
+                   for i in range(S)]
+        bdec.prefill(prompts, w.n_new)
+        bdec.verify(bdec.draft())
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("dflash_batch")
+        bdec.verify(bdec.draft())
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+        bdec.check()
+        print(f"ncu batch done: S={S}", flush=True)
+        bdec.close()
         return
     if args.ncu_rounds:
         dec.prefill(prompt, w.n_new)

@@ -721,26 +721,26 @@ batch_attn_kernel(const __grid_constant__ PrefillMaps maps, const BatchAttnArgs 
 
     pdl_trigger();
     pdl_wait();
-    const int kh = blockIdx.x, sq = blockIdx.y, tid = threadIdx.x;
+    const int kh = blockIdx.x, sq = blockIdx.y, z = blockIdx.z, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     DevState* st = b.sts[sq];
     const int T = st->fwd_T, pos0 = st->fwd_pos0;
     const int hi = pos0 + T;
     const int lo = (!a.causal && a.window > 0) ? max(0, pos0 - a.window) : 0;
-    const size_t ld = (size_t)a.n_q * HD;
-    auto store_row = [&](int t, int hq, int d, float v) {   // bf16 hi/lo of row 16 sq + t
-        const size_t i = (size_t)(16 * sq + t) * ld + (size_t)hq * HD + d;
-        const __nv_bfloat16 h = __float2bfloat16_rn(v);
-        reinterpret_cast<__nv_bfloat16*>(b.out_hi)[i] = h;
-        reinterpret_cast<__nv_bfloat16*>(b.out_lo)[i] = __float2bfloat16_rn(v - __bfloat162float(h));
-    };
-    // rows past T (and a sequence without rows) hold zeros
-    for (int e = tid; e < 16 * group * HD; e += blockDim.x) {
-        const int t = e / (group * HD), rem = e % (group * HD);
-        if (t >= T) store_row(t, kh * group + rem / HD, rem % HD, 0.f);
+    const int c_lo = lo / C, c_hi = (hi - 1) / C;
+    const int c0 = c_lo + z * b.split_chunks;
+    const int n_my = T > 0 ? max(0, min(b.split_chunks, c_hi + 1 - c0)) : 0;
+    // partials of this split: (max, sum, unnormalised output) per (row, q head)
+    float* pbase = b.part + ((size_t)(sq * b.splits + z) * DFL_MAX_ROWS) * a.n_q * (HD + 2);
+    if (n_my == 0) {   // nothing visible in this split: an empty partial
+        for (int e = tid; e < DFL_MAX_ROWS * group; e += blockDim.x) {
+            const int t = e / group, hq = kh * group + e % group;
+            float* pp = pbase + ((size_t)t * a.n_q + hq) * (HD + 2);
+            pp[0] = -INFINITY;
+            pp[1] = 0.f;
+        }
+        return;
     }
-    if (T <= 0) return;
-    const int c_lo = lo / C, n_my = (hi - 1) / C - c_lo + 1;
     const int layer_row = (sq * b.n_layers + a.layer) * 2;   // K run of this layer in the map
 
     if (tid == 0) {
@@ -748,10 +748,10 @@ batch_attn_kernel(const __grid_constant__ PrefillMaps maps, const BatchAttnArgs 
         fence_mbar_init();
     }
     __syncthreads();
-    auto load_chunk = [&](int i) {   // chunk c_lo + i into buffer i & 1
+    auto load_chunk = [&](int i) {   // chunk c0 + i into buffer i & 1
         uint8_t* Kb = KV + (i & 1) * 2 * KVB;
         uint8_t* Vb = Kb + KVB;
-        const int c = c_lo + i;
+        const int c = c0 + i;
         const int krow = ((layer_row + 0) * a.n_kv + kh) * a.cap + c * C;
         const int vrow = ((layer_row + 1) * a.n_kv + kh) * a.cap + c * C;
         mbar_arrive_expect_tx(&bar[1 + (i & 1)], 2 * KVB);
@@ -781,7 +781,7 @@ batch_attn_kernel(const __grid_constant__ PrefillMaps maps, const BatchAttnArgs 
         ok = __syncthreads_and(mbar_wait_bounded(&bar[1 + (i & 1)], (uint32_t)((i >> 1) & 1))) != 0;
         if (ok && warp < group)
             adev::chunk_online<HD>(Qs, KV + (i & 1) * 2 * KVB, KV + (i & 1) * 2 * KVB + KVB, a, qrows,
-                                   c_lo + i, T, pos0, lo, hi, warp, lane, m, l, o);
+                                   c0 + i, T, pos0, lo, hi, warp, lane, m, l, o);
         __syncthreads();   // buffer i & 1 is free again
         if (ok && tid == 0 && i + 2 < n_my) {
             load_chunk(i + 2);
@@ -802,13 +802,63 @@ batch_attn_kernel(const __grid_constant__ PrefillMaps maps, const BatchAttnArgs 
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int t = g + 8 * r;
-            if (t >= T) continue;
-            const float inv = 1.f / l[r];
+            float* pp = pbase + ((size_t)t * a.n_q + hq) * (HD + 2);
+            if (cq == 0) {
+                pp[0] = m[r];   // base-2 domain
+                pp[1] = l[r];
+            }
 #pragma unroll
             for (int dt = 0; dt < HD / 8; ++dt)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) store_row(t, hq, dt * 8 + 2 * cq + e, o[dt][2 * r + e] * inv);
+                for (int e = 0; e < 2; ++e) pp[2 + dt * 8 + 2 * cq + e] = o[dt][2 * r + e];
         }
+    }
+}
+
+// One warp per (sequence, row, q head): folds the splits' partials in split
+// order (base-2 maxima) and writes the normalised row as bf16 hi/lo (zero
+// for rows past the sequence's T).
+template <int HD>
+__global__ void batch_attn_combine_kernel(const BatchAttnArgs b, int S) {
+    pdl_trigger();
+    pdl_wait();
+    const AttnMmaArgs& a = b.m;
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= S * DFL_MAX_ROWS * a.n_q) return;
+    const int sq = warp / (DFL_MAX_ROWS * a.n_q), rem = warp % (DFL_MAX_ROWS * a.n_q);
+    const int t = rem / a.n_q, hq = rem % a.n_q;
+    const int T = b.sts[sq]->fwd_T;
+    const size_t ld = (size_t)a.n_q * HD;
+    const size_t obase = (size_t)(16 * sq + t) * ld + (size_t)hq * HD;
+    float out[HD / 32];
+#pragma unroll
+    for (int j = 0; j < HD / 32; ++j) out[j] = 0.f;
+    if (t < T) {
+        const size_t pstride = (size_t)DFL_MAX_ROWS * a.n_q * (HD + 2);
+        const float* p0 = b.part + ((size_t)sq * b.splits * DFL_MAX_ROWS + t) * a.n_q * (HD + 2) +
+                          (size_t)hq * (HD + 2);
+        float M = -INFINITY;
+        for (int zz = 0; zz < b.splits; ++zz) M = fmaxf(M, p0[zz * pstride]);
+        float L = 0.f;
+        for (int zz = 0; zz < b.splits; ++zz) {
+            const float mz = p0[zz * pstride];
+            const float w = mz == -INFINITY ? 0.f : exp2f(mz - M);
+            L = fmaf(p0[zz * pstride + 1], w, L);
+#pragma unroll
+            for (int j = 0; j < HD / 32; ++j)
+                out[j] = fmaf(w == 0.f ? 0.f : p0[zz * pstride + 2 + lane + 32 * j], w, out[j]);
+        }
+        const float inv = 1.f / L;
+#pragma unroll
+        for (int j = 0; j < HD / 32; ++j) out[j] *= inv;
+    }
+#pragma unroll
+    for (int j = 0; j < HD / 32; ++j) {
+        const float v = out[j];
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        reinterpret_cast<__nv_bfloat16*>(b.out_hi)[obase + lane + 32 * j] = h;
+        reinterpret_cast<__nv_bfloat16*>(b.out_lo)[obase + lane + 32 * j] =
+            __float2bfloat16_rn(v - __bfloat162float(h));
     }
 }
 
@@ -827,8 +877,12 @@ int launch_batch_hd(const CUtensorMap& q_map, const CUtensorMap& kv_map, const B
     PrefillMaps maps;
     maps.q = q_map;
     maps.kv = kv_map;
-    return (int)launch_k(batch_attn_kernel<HD>, dim3((unsigned)b.m.n_kv, (unsigned)S), dim3(128), smem, s,
-                         maps, b);
+    int e = (int)launch_k(batch_attn_kernel<HD>, dim3((unsigned)b.m.n_kv, (unsigned)S, (unsigned)b.splits),
+                          dim3(128), smem, s, maps, b);
+    if (e) return e;
+    const long long warps = (long long)S * DFL_MAX_ROWS * b.m.n_q;
+    return (int)launch_k(batch_attn_combine_kernel<HD>, dim3((unsigned)((warps * 32 + 255) / 256)), dim3(256), 0,
+                         s, b, S);
 }
 
 template <int HD>

@@ -66,14 +66,20 @@ int launch_prefill_attention(const CUtensorMap& q_map, const CUtensorMap& kv_map
 // its own cache rows, causal (verify) or [window context | bidirectional
 // block] (draft).  The caches of all sequences are one map
 // [S][layers][2][n_kv][cap][hd] (f16); q rows [S][n_q][16][hd] (f16, box =
-// one kv head's q group).  One CTA per (kv head, sequence) folds every
-// visible 64-key chunk with the online softmax of the round's attention and
-// writes the normalised rows as bf16 hi/lo planes [S * 16][n_q * hd]
-// (rows past T zero).
+// one kv head's q group).  One CTA per (kv head, sequence, split) folds its
+// split's 64-key chunks (split z: chunks c_lo + z q .. c_lo + (z + 1) q - 1,
+// counted from the first visible chunk, q fixed per model) with the online
+// softmax of the round's attention into (max, sum, output) partials
+// [S][splits][16][n_q][hd + 2]; a combine kernel folds the splits in split
+// order and writes the normalised rows as bf16 hi/lo planes
+// [S * 16][n_q * hd] (rows past T zero).
 struct BatchAttnArgs {
     AttnMmaArgs m;            // shapes, layer, cap, causal, window, scale
     DevState* const* sts;     // [S] round state of each sequence
     int n_layers;             // layers of the cache map's model
+    int split_chunks;         // q: chunks per split
+    int splits;               // splits per (kv head, sequence): grid.z
+    float* part;              // partials
     void* out_hi;
     void* out_lo;
 };

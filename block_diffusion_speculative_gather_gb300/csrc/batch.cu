@@ -321,7 +321,7 @@ struct dflash_batch {
     float* rsin = nullptr;
     unsigned long long* amax = nullptr;
     float* part = nullptr;
-    int* tickets = nullptr;
+    float* apart = nullptr;   // attention split partials
     int* err = nullptr;
     struct LayerMaps {
         DenseMaps qkv, o, gu, down, ctxkv;
@@ -335,8 +335,6 @@ struct dflash_batch {
 
 namespace {
 
-constexpr int BATCH_TICKETS = 4096;
-
 size_t up1k(size_t v) { return (v + 1023) / 1024 * 1024; }
 
 // Split count of a GEMM: about one CTA per SM over the 128-column tiles,
@@ -349,8 +347,24 @@ int splits_for(int N, int K, int sms) {
     return z > kmax ? (kmax < 1 ? 1 : kmax) : z;
 }
 
+// Attention splits of a model: at most 4 per (kv head, sequence), each of a
+// fixed number of 64-key chunks counted from the first visible chunk (from
+// the cache capacity, or the drafter's window), so a row's split boundaries
+// depend on its position only.
+void attn_splits(const dflash_config& g, bool target, int* chunks, int* splits) {
+    const int cap = (g.max_seq + 63) / 64 * 64;
+    int maxc = cap / 64;
+    if (!target && g.window > 0) {
+        const int w = (g.window + DFL_MAX_ROWS + 63) / 64 + 1;
+        if (w < maxc) maxc = w;
+    }
+    const int q = (maxc + 3) / 4;
+    *chunks = q < 1 ? 1 : q;
+    *splits = (maxc + *chunks - 1) / *chunks;
+}
+
 struct BatchLayout {
-    size_t sts, x, hi, lo, thi, tlo, y, q, rcos, rsin, amax, part, tickets, err, total;
+    size_t sts, x, hi, lo, thi, tlo, y, q, rcos, rsin, amax, part, apart, err, total;
 };
 
 BatchLayout batch_layout(const dflash_config& g, int S, int sms) {
@@ -388,7 +402,10 @@ BatchLayout batch_layout(const dflash_config& g, int S, int sms) {
     L.rsin = take(R * (size_t)(g.head_dim / 2) * 4);
     L.amax = take(R * 8);
     L.part = take(pf * 4 + 16);
-    L.tickets = take((size_t)BATCH_TICKETS * 4);
+    int ct, st, cd = 1, sd = 1;
+    attn_splits(g, true, &ct, &st);
+    if (g.drf_layers > 0) attn_splits(g, false, &cd, &sd);
+    L.apart = take((size_t)S * std::max(st, sd) * DFL_MAX_ROWS * g.n_q * (g.head_dim + 2) * 4);
     L.err = take(256);
     L.total = o;
     return L;
@@ -455,9 +472,6 @@ int dense(dflash_batch* b, const DenseMaps& m, int N, int K, int seg0, int seg1,
     d.amax = amax;
     d.splits = amax ? 1 : splits_for(N, K, b->sms);
     d.part = b->part;
-    d.tickets = b->tickets;
-    if (dense_tiles(d.M, N, 128) > BATCH_TICKETS)
-        return report_error(DFLASH_ERR_CONFIG, "GEMM %d x %d has too many tiles", d.M, N);
     const int e = launch_dense(m, d, s);
     if (e) return report_error(DFLASH_ERR_CUDA, "dense GEMM (N %d K %d): %s", N, K, cudaGetErrorString((cudaError_t)e));
     return DFLASH_OK;
@@ -508,6 +522,8 @@ int batch_layers(dflash_batch* b, bool target, cudaStream_t s) {
         at.m.scale = 1.0f / sqrtf((float)g.head_dim);
         at.sts = b->sts;
         at.n_layers = nl;
+        attn_splits(g, target, &at.split_chunks, &at.splits);
+        at.part = b->apart;
         at.out_hi = b->hi;
         at.out_lo = b->lo;
         BTRY(launch_batch_attention(b->qmap, target ? b->kvmap_t : b->kvmap_d, at, b->S, s));
@@ -655,12 +671,11 @@ int dflash_batch_init(const dflash_config* cfg, const dflash_weights* w, int32_t
     b->rsin = reinterpret_cast<float*>(bw + L.rsin);
     b->amax = reinterpret_cast<unsigned long long*>(bw + L.amax);
     b->part = reinterpret_cast<float*>(bw + L.part);
-    b->tickets = reinterpret_cast<int*>(bw + L.tickets);
+    b->apart = reinterpret_cast<float*>(bw + L.apart);
     b->err = reinterpret_cast<int*>(bw + L.err);
     std::vector<DevState*> hs(S);
     for (int s = 0; s < S; ++s) hs[s] = ctx_state(b->ctx[s]);
     if (cudaMemcpy(b->sts, hs.data(), S * sizeof(DevState*), cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMemset(bw + L.tickets, 0, (size_t)BATCH_TICKETS * 4) != cudaSuccess ||
         cudaMemset(b->err, 0, 8) != cudaSuccess)
         return bail(report_error(DFLASH_ERR_CUDA, "batch workspace set-up failed"));
     // tensor maps: GEMM inputs (hi/lo planes at the reduction width) and weights
@@ -806,7 +821,6 @@ int dflash_batch_check(dflash_batch* b, dflash_stream_t stream) {
     if (e[0]) {
         const int zero[2] = {0, 0};
         cudaMemcpy(b->err, zero, sizeof zero, cudaMemcpyHostToDevice);
-        cudaMemset(b->tickets, 0, (size_t)BATCH_TICKETS * 4);
         return report_error(e[0] == DERR_TIMEOUT ? DFLASH_ERR_TIMEOUT : DFLASH_ERR_DEVICE,
                             "batch GEMM error %d (site %d)", e[0], e[1]);
     }

@@ -77,7 +77,7 @@ int max_chunks(const dflash_config& c) { return cache_cap(c) / ATTN_CHUNK; }
 
 struct Layout {
     size_t state, x, hn, ssq, qrot, attn, act, taps, rcos, rsin, invf, amax, part, slots, counters,
-        acnt, amaps, barc, prog[3], ns[3], pf_x, pf_y, pf_chi, pf_clo, pf_w, pp_x, pp_y, pp_hi, pp_lo, pp_q,
+        acnt, amaps, barc, prog[3], ns[3], pf_x, pf_xlo, pf_y, pf_chi, pf_clo, pf_w, pp_x, pp_y, pp_hi, pp_lo, pp_q,
         pp_thi, pp_tlo, pf_rope, pp_w, total;
     int prog_n[3];
 };
@@ -170,6 +170,7 @@ Layout make_layout(const dflash_config& c) {
     if (dense_ingest_ok(c)) {   // [PF_ROWS] rows: taps bf16, GEMM out fp32, context rows hi/lo bf16
         const size_t kv = (size_t)2 * c.n_kv * c.head_dim;
         L.pf_x = take((size_t)PF_ROWS * c.n_taps * c.hidden * 2);
+        L.pf_xlo = take((size_t)PF_ROWS * c.n_taps * c.hidden * 2);   // lo plane of hc-mean taps
         L.pf_y = take((size_t)PF_ROWS * (kv > (size_t)c.hidden ? kv : (size_t)c.hidden) * 4);
         L.pf_chi = take((size_t)PF_ROWS * c.hidden * 2);
         L.pf_clo = take((size_t)PF_ROWS * c.hidden * 2);
@@ -339,6 +340,7 @@ struct dflash_ctx {
     int attn_tc[2] = {0, 0};   // tcgen05 form of the fused attention
     bool dense_ingest = false;  // window ingest on the dense tcgen05 GEMM
     DenseMaps d_fc{};           // fc over the window's tap rows
+    DenseMaps d_fc_hl{};        // the same over hi/lo tap rows (means of hc > 1 streams)
     std::vector<DenseMaps> d_kv;   // per draft layer: context K/V from the context rows
     bool dense_prefill = false;    // prompt rows before the last chunk on the dense GEMM
     struct PrefillLayer { DenseMaps qkv, o, gu, down; };
@@ -368,6 +370,16 @@ struct dflash_ctx {
     template <typename T> T* buf(size_t off) const { return reinterpret_cast<T*>(ws + off); }
     // GEMM inputs: fp32, or hi/lo bf16 planes for the bf16 models
     int act_xt() const { return cfg.dtype == DFLASH_F32 ? XT_F32 : XT_BF16S; }
+    // The input type of a GEMM whose weights have format f: fp32 for the
+    // fp32 models, one f16 plane for INT4 weights (the codes are exact in
+    // f16, and one plane halves the MMAs of the instruction-bound INT4
+    // GEMM), bf16 hi/lo planes for bf16 weights.
+    int gin_xt(int f) const {
+        if (cfg.dtype == DFLASH_F32) return XT_F32;
+        return f == DFLASH_INT4G64 ? XT_F16 : XT_BF16S;
+    }
+    int xt_model(bool target) const { return gin_xt(target ? cfg.tgt_wfmt : cfg.drf_wfmt); }
+    int xt_lm() const { return gin_xt(cfg.lm_wfmt == DFLASH_INT4G64 ? DFLASH_INT4G64 : cfg.dtype); }
     // attention operands (q, K/V caches): fp32, or fp16 for the bf16 models
     int kv_xt() const { return cfg.dtype == DFLASH_F32 ? XT_F32 : XT_F16; }
     int wf(int f) const { return f == DFLASH_F32 ? WF_F32 : f == DFLASH_INT4G64 ? WF_INT4 : WF_BF16; }
@@ -502,7 +514,7 @@ int run_gemm(dflash_ctx* c, const GemmPlan& p, const GemmArgs& a, Emit& em) {
 int build_layer_plans(dflash_ctx* c, const dflash_layer& lw, int wfmt, bool draft, LayerPlans* lp) {
     const dflash_config& g = c->cfg;
     const int H = g.hidden, qd = g.n_q * g.head_dim, kvd = g.n_kv * g.head_dim;
-    const int wf = c->wf(wfmt), xt = c->act_xt();
+    const int wf = c->wf(wfmt), xt = c->gin_xt(wfmt);
     const void* hn = c->ws + c->L.hn;
     const void* wqkv[3] = {lw.wq, lw.wk, lw.wv};
     const void* sqkv[3] = {lw.sq, lw.sk, lw.sv};
@@ -539,10 +551,11 @@ void set_norm_in(const dflash_ctx* c, GemmArgs& a, bool on) {
     a.eps = c->cfg.rms_eps;
 }
 
-// Normalised-input output of a GEMM for the next folded RMSNorm.
-void set_norm_out(const dflash_ctx* c, GemmArgs& a, const float* w_next, bool with_ssq) {
+// Normalised-input output of a GEMM for the next folded RMSNorm, in the
+// input type of the GEMM that consumes it.
+void set_norm_out(const dflash_ctx* c, GemmArgs& a, const float* w_next, bool with_ssq, int xt) {
     a.xn_out = c->ws + c->L.hn;
-    a.xn_type = c->act_xt();
+    a.xn_type = xt;
     a.w_next = w_next;
     a.ssq_out = with_ssq ? c->buf<float>(c->L.ssq) : nullptr;
 }
@@ -578,7 +591,7 @@ QkvEpi qkv_epi(const dflash_ctx* c, const dflash_layer& lw, bool target, int lay
 int run_layers(dflash_ctx* c, bool target, Emit& em) {
     const dflash_config& g = c->cfg;
     const int H = g.hidden;
-    const int xt = c->act_xt();
+    const int xt = c->xt_model(target);   // input type of this model's GEMMs
     const int nl = target ? g.tgt_layers : g.drf_layers;
     DevState* st = c->st();
     float* x = c->buf<float>(c->L.x);
@@ -652,7 +665,7 @@ int run_layers(dflash_ctx* c, bool target, Emit& em) {
         a = lp.o.args;
         a.out = x;
         a.ldo = H;
-        set_norm_out(c, a, lw.ln_mlp, true);
+        set_norm_out(c, a, lw.ln_mlp, true, xt);
         if ((r = run_gemm(c, lp.o, a, em))) return r;
         a = lp.gateup.args;
         set_norm_in(c, a, true);
@@ -664,13 +677,13 @@ int run_layers(dflash_ctx* c, bool target, Emit& em) {
         a.out = x;
         a.ldo = H;
         const float* w_next = l + 1 < nl ? (target ? c->tgt[l + 1] : c->drf[l + 1]).ln_attn : final_norm;
-        set_norm_out(c, a, w_next, true);
+        set_norm_out(c, a, w_next, true, l + 1 < nl ? xt : c->xt_lm());
         if (target && g.drf_layers > 0) {
             for (int i = 0; i < g.n_taps; ++i)
                 if (g.tap_layer[i] == l) {
                     a.tap_out = c->ws + c->L.taps + (size_t)i * H * elem_size(g.dtype);   // column i*H
                     a.ld_tap = g.n_taps * H;
-                    a.tap_type = xt;
+                    a.tap_type = c->act_xt();   // taps feed fc (bf16 weights)
                 }
         }
         if ((r = run_gemm(c, lp.down, a, em))) return r;
@@ -694,7 +707,7 @@ int run_ingest(dflash_ctx* c, Emit& em) {
     const dflash_config& g = c->cfg;
     GemmArgs a = c->fc.args;
     a.ldo = g.hidden;
-    set_norm_out(c, a, g.ctx_norm ? c->w.ctx_norm : nullptr, g.ctx_norm != 0);
+    set_norm_out(c, a, g.ctx_norm ? c->w.ctx_norm : nullptr, g.ctx_norm != 0, c->xt_model(false));
     int r = run_gemm(c, c->fc, a, em);
     if (r) return r;
     for (int l = 0; l < g.drf_layers; ++l) {
@@ -738,7 +751,7 @@ RowsArgs rows_args(dflash_ctx* c, int mode) {
                  : (g.tgt_layers ? c->tgt[0].ln_attn : nullptr);
     if (!a.w0) a.embed = nullptr;   // no model runs (drafter-alone tap staging)
     a.xn = c->ws + c->L.hn;
-    a.xn_type = c->act_xt();
+    a.xn_type = c->xt_model(!draft);   // layer 0 of the model that runs
     a.ssq = c->buf<float>(c->L.ssq);
     a.st = c->st();
     return a;
@@ -1013,11 +1026,11 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
             const void* wl[1] = {w->lm_head};
             const void* sl[1] = {w->lm_scales};
             r = plan_gemm(c, &c->lm, WF_INT4, EPI_ARGMAX, wl, re, 1, g.hidden, c->ws + L.hn,
-                          c->act_xt(), sl);
+                          c->xt_lm(), sl);
         } else {
             const void* we[1] = {w->embed};
             r = plan_gemm(c, &c->lm, c->wf(g.dtype), EPI_ARGMAX, we, re, 1, g.hidden, c->ws + L.hn,
-                          c->act_xt());
+                          c->xt_lm());
         }
     }
     if (!r && g.drf_layers > 0) {
@@ -1106,6 +1119,10 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
         const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
         r = make_map_raw(&c->d_fc.x, c->ws + L.pf_x, bf, 2, K1, PF_ROWS, DT_BK, DT_BM, sw);
         if (!r) r = make_map_raw(&c->d_fc.w[0], w->fc, bf, 2, K1, g.hidden, DT_BK, DT_WBOX, sw);
+        if (!r) {
+            c->d_fc_hl = c->d_fc;
+            r = make_map_raw(&c->d_fc_hl.x_lo, c->ws + L.pf_xlo, bf, 2, K1, PF_ROWS, DT_BK, DT_BM, sw);
+        }
         c->d_kv.resize(g.drf_layers);
         const bool q4 = g.drf_wfmt == DFLASH_INT4G64;   // f16 operands: rows and dequantised weights
         const CUtensorMapDataType xt = q4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : bf;
@@ -1374,23 +1391,30 @@ int ingest_rows(dflash_ctx* c, const DenseMaps& fcm, int x_split, int m_off, int
     return DFLASH_OK;
 }
 
-int run_dense_ingest(dflash_ctx* c, const void* ext_taps, int n_ext, int commit_lo, cudaStream_t s) {
+int run_dense_ingest(dflash_ctx* c, const void* ext_taps, int n_ext, int hc, int commit_lo, cudaStream_t s) {
     const dflash_config& g = c->cfg;
     for (int p0 = commit_lo; p0 < n_ext; p0 += PF_ROWS) {
         const int R = n_ext - p0 < PF_ROWS ? n_ext - p0 : PF_ROWS;
         TapArgs ta{};
         for (int i = 0; i < g.n_taps; ++i)
-            ta.src[i] = static_cast<const uint8_t*>(ext_taps) + ((size_t)i * n_ext + p0) * g.hidden * 2;
+            ta.src[i] = static_cast<const uint8_t*>(ext_taps) + ((size_t)i * n_ext + p0) * hc * g.hidden * 2;
         ta.n_layers = g.n_taps;
         ta.rows = R;
-        ta.hc = 1;
+        ta.hc = hc;
         ta.hidden = g.hidden;
         ta.in_type = XT_BF16;
         ta.out = c->ws + c->L.pf_x;
-        ta.out_type = XT_BF16;
         ta.out_row_stride = (long long)g.n_taps * g.hidden;
+        if (hc == 1) {
+            ta.out_type = XT_BF16;   // the tap rows themselves: exact in bf16
+        } else {
+            // the hc-stream mean carries more bits than bf16: hi/lo planes,
+            // as the round's own GEMM inputs
+            ta.out_type = XT_BF16S;
+            ta.lo_offset = (long long)((c->L.pf_xlo - c->L.pf_x) / 2);
+        }
         LAUNCH_TRY(launch_tap_reduce(ta, s));
-        if (int r = ingest_rows(c, c->d_fc, 0, 0, R, p0, s)) return r;
+        if (int r = ingest_rows(c, hc == 1 ? c->d_fc : c->d_fc_hl, hc == 1 ? 0 : 1, 0, R, p0, s)) return r;
     }
     return DFLASH_OK;
 }
@@ -1590,8 +1614,8 @@ int dflash_prefill_taps(dflash_ctx* c, const int32_t* prompt_ids, int32_t n_prom
         if (g.hidden % 8) return fail(DFLASH_ERR_CONFIG, "hidden must be a multiple of 8");
         const int commit_lo = g.window > 0 ? (n_ext > g.window ? n_ext - g.window : 0) : 0;
         const int es = elem_size(g.dtype);
-        if (c->dense_ingest && hc == 1) {
-            if ((r = run_dense_ingest(c, ext_taps, n_ext, commit_lo, s))) return r;
+        if (c->dense_ingest) {
+            if ((r = run_dense_ingest(c, ext_taps, n_ext, hc, commit_lo, s))) return r;
         } else
         for (int p0 = commit_lo / DFL_MAX_ROWS * DFL_MAX_ROWS; p0 < n_ext; p0 += DFL_MAX_ROWS) {
             const int T = n_ext - p0 < DFL_MAX_ROWS ? n_ext - p0 : DFL_MAX_ROWS;

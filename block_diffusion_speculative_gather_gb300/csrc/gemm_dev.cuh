@@ -69,11 +69,16 @@ __device__ __forceinline__ void mma_kblock(const uint8_t* Wt, const uint8_t* Xt,
     if (WF == WF_INT4) {
         // 4 scale groups of 64 k; inside group q a lane owns k 16c..16c+15
         // of rows r0 and r0+8 (two interleaved 32-bit words each) and the
-        // same 16 k of tokens g and g+8; the group's partial sums are
-        // scaled per row in fp32 and added to the accumulators.
+        // same 16 k of tokens g and g+8.  INT4 consumers take one f16
+        // activation plane (rows 0..15 of the tile): the codes are exact in
+        // f16, so a code pair becomes an f16 pair with one mask/or and one
+        // subtraction.  Each group's partial sums, in four independent
+        // chains (even / odd k-steps of both token tiles), are scaled per
+        // row by the group's bf16 scale in fp32 and added to the
+        // accumulators.
         const int r0 = warp * 16 + g;
         const __nv_bfloat16* St = reinterpret_cast<const __nv_bfloat16*>(Sb);
-        const __nv_bfloat162 bias = __floats2bfloat162_rn(136.f, 136.f);
+        const __half2 bias = __floats2half2_rn(1032.f, 1032.f);
         // one 64-k group at a time (a rolled loop: fewer live registers and
         // a quarter of the code, which each CTA fetches cold)
 #pragma unroll 1
@@ -96,28 +101,21 @@ __device__ __forceinline__ void mma_kblock(const uint8_t* Wt, const uint8_t* Xt,
             *reinterpret_cast<uint4*>(&xa[4]) = lds128(Xq + swz128(g, 2 * c + 1));
             *reinterpret_cast<uint4*>(&xb[0]) = lds128(Xq + swz128(g + 8, 2 * c));
             *reinterpret_cast<uint4*>(&xb[4]) = lds128(Xq + swz128(g + 8, 2 * c + 1));
-            // dequantise: pair p_i of a word = nibbles (i, i+4) = k (2i, 2i+1)
+            // dequantise: pair p_i of a word = nibbles (i, i+4) = k (2i, 2i+1);
+            // 0x6400 | u is the f16 1024 + u, minus 1032 the code u - 8
             uint32_t pa[8], pb[8];
             const uint32_t wordsa[2] = {wa.x, wa.y}, wordsb[2] = {wb.x, wb.y};
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    uint32_t ua = ((wordsa[m] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-                    uint32_t ub = ((wordsb[m] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-                    __nv_bfloat162 va = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&ua), bias);
-                    __nv_bfloat162 vb = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&ub), bias);
+                    uint32_t ua = ((wordsa[m] >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
+                    uint32_t ub = ((wordsb[m] >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
+                    __half2 va = __hsub2(*reinterpret_cast<__half2*>(&ua), bias);
+                    __half2 vb = __hsub2(*reinterpret_cast<__half2*>(&ub), bias);
                     pa[4 * m + i] = *reinterpret_cast<uint32_t*>(&va);
                     pb[4 * m + i] = *reinterpret_cast<uint32_t*>(&vb);
                 }
-            }
-            // hi and lo planes into their own accumulators, interleaved
-            uint32_t la[8], lb[8];
-            if (a.x_split) {   // lo planes: tokens g, g + 8 at rows 16 + g, 24 + g
-                *reinterpret_cast<uint4*>(&la[0]) = lds128(Xq + swz128(16 + g, 2 * c));
-                *reinterpret_cast<uint4*>(&la[4]) = lds128(Xq + swz128(16 + g, 2 * c + 1));
-                *reinterpret_cast<uint4*>(&lb[0]) = lds128(Xq + swz128(24 + g, 2 * c));
-                *reinterpret_cast<uint4*>(&lb[4]) = lds128(Xq + swz128(24 + g, 2 * c + 1));
             }
             float g0[4] = {0.f, 0.f, 0.f, 0.f}, g1[4] = {0.f, 0.f, 0.f, 0.f};
             float h0[4] = {0.f, 0.f, 0.f, 0.f}, h1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -126,14 +124,18 @@ __device__ __forceinline__ void mma_kblock(const uint8_t* Wt, const uint8_t* Xt,
                 const uint32_t A[4] = {pa[2 * j], pb[2 * j], pa[2 * j + 1], pb[2 * j + 1]};
                 const uint32_t B0[2] = {xa[2 * j], xa[2 * j + 1]};
                 const uint32_t B1[2] = {xb[2 * j], xb[2 * j + 1]};
-                mma_bf16_16816(g0, A, B0);
-                mma_bf16_16816(g1, A, B1);
-                if (a.x_split) {
-                    const uint32_t L0[2] = {la[2 * j], la[2 * j + 1]};
-                    const uint32_t L1[2] = {lb[2 * j], lb[2 * j + 1]};
-                    mma_bf16_16816(h0, A, L0);
-                    mma_bf16_16816(h1, A, L1);
+                if (j & 1) {
+                    mma_f16_16816(h0, A, B0);
+                    mma_f16_16816(h1, A, B1);
+                } else {
+                    mma_f16_16816(g0, A, B0);
+                    mma_f16_16816(g1, A, B1);
                 }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                g0[e] += h0[e];
+                g1[e] += h1[e];
             }
             acc[0] = fmaf(sa, g0[0], acc[0]);
             acc[1] = fmaf(sa, g0[1], acc[1]);
@@ -143,17 +145,8 @@ __device__ __forceinline__ void mma_kblock(const uint8_t* Wt, const uint8_t* Xt,
             acc[5] = fmaf(sa, g1[1], acc[5]);
             acc[6] = fmaf(sb, g1[2], acc[6]);
             acc[7] = fmaf(sb, g1[3], acc[7]);
-            if (a.x_split) {
-                accl[0] = fmaf(sa, h0[0], accl[0]);
-                accl[1] = fmaf(sa, h0[1], accl[1]);
-                accl[2] = fmaf(sb, h0[2], accl[2]);
-                accl[3] = fmaf(sb, h0[3], accl[3]);
-                accl[4] = fmaf(sa, h1[0], accl[4]);
-                accl[5] = fmaf(sa, h1[1], accl[5]);
-                accl[6] = fmaf(sb, h1[2], accl[6]);
-                accl[7] = fmaf(sb, h1[3], accl[7]);
-            }
         }
+        (void)accl;
     } else if (WF == WF_BF16) {
         const int r0 = warp * 16 + g;
         uint32_t ra[8], rb[8], xa[8], xb[8];

@@ -16,9 +16,9 @@
 // tensor memory is freed only after the MMAs it issued have finished.
 // Split-K (few rows: the many-sequence round): the k-blocks of a tile are
 // cut into `splits` contiguous ranges in split order; each split stores its
-// fp32 partial tile and the last to arrive on the tile's ticket adds all
-// partials in split order, so a row's result is the same whatever the
-// number of rows.  The argmax epilogue (the LM head of that round) keeps per
+// fp32 partial rows into its own slab, and a reduce kernel launched right
+// after adds the slabs in split order (coalesced, one pass over them), so a
+// row's result is the same whatever the number of rows.  The argmax epilogue (the LM head of that round) keeps per
 // row the packed (orderable logit, ~column) key of its largest column and
 // folds it into the row's key with atomicMax (lowest column on ties).
 
@@ -62,7 +62,6 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
     const int Z = a.splits > 1 ? a.splits : 1, z = blockIdx.z;
     const int kb_lo = (int)((long long)(a.K / DT_BK) * z / Z);
     const int nkb = (int)((long long)(a.K / DT_BK) * (z + 1) / Z) - kb_lo;
-    __shared__ int s_last;
     const int seg = n0 >= a.n_seg1 ? 2 : n0 >= a.n_seg0 ? 1 : 0;
     const int wrow = n0 - (seg == 2 ? a.n_seg1 : seg == 1 ? a.n_seg0 : 0);
 
@@ -134,12 +133,11 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
     ok = ok && s_fail == 0;
     tc::fence_after_sync();
     const int row = m0 + 32 * warp + lane;
-    const int tile = blockIdx.x * gridDim.y + blockIdx.y;
-    float* mypart = a.part + (((size_t)tile * Z + z) * DT_BM + 32 * warp + lane) * BN;
-    bool last = true;
     if (ok && Z > 1) {
-        // publish this split's partial tile; the last split to arrive sums
-        // every partial in split order and runs the epilogue
+        // split z's partial rows into slab z of part ([Z][m tiles * 128][n tiles * BN]);
+        // the reduce kernel that follows adds the slabs in split order
+        const size_t ldp = (size_t)gridDim.y * BN;
+        float* mypart = a.part + ((size_t)z * gridDim.x * DT_BM + row) * ldp + n0;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
             float v[32];
@@ -149,39 +147,14 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
                 __stcg(reinterpret_cast<float4*>(mypart + 32 * c + i),
                        make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
         }
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) s_last = atomicAdd(&a.tickets[tile], 1) == Z - 1 ? 1 : 0;
-        __syncthreads();
-        last = s_last != 0;
-        if (last) {
-            __threadfence();
-            if (threadIdx.x == 0) a.tickets[tile] = 0;   // ready for the next launch
-        }
     }
+    const bool last = Z == 1;
     if (ok && last) {
-        const float* rows0 = a.part + (((size_t)tile * Z) * DT_BM + 32 * warp + lane) * BN;
         unsigned long long best = 0ull;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
             float v[32];
-            if (Z > 1) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0.f;
-                for (int zz = 0; zz < Z; ++zz) {   // split order: the same for every M
-                    const float* src = rows0 + (size_t)zz * DT_BM * BN + 32 * c;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const float4 p4 = __ldcg(reinterpret_cast<const float4*>(src + i));
-                        v[i] += p4.x;
-                        v[i + 1] += p4.y;
-                        v[i + 2] += p4.z;
-                        v[i + 3] += p4.w;
-                    }
-                }
-            } else {
-                tc::ld_x32(tm + ((uint32_t)(32 * warp) << 16) + 32 * c, v);
-            }
+            tc::ld_x32(tm + ((uint32_t)(32 * warp) << 16) + 32 * c, v);
             const int col = n0 + 32 * c;
             if (row < a.M && col < a.N) {
                 if (a.amax) {
@@ -215,6 +188,37 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
     if (warp == 1) tc::tmem_dealloc(tm, BN);
 }
 
+// y = sum over the split slabs in split order (z = 0, 1, ...), four
+// consecutive columns per thread: coalesced, every load of a thread in
+// flight at once.
+__global__ void dense_split_reduce_kernel(const float* __restrict__ part, int Z, int M, int N,
+                                          size_t slab, size_t ldp, float* __restrict__ y, int ldy) {
+    pdl_trigger();
+    pdl_wait();
+    const long long n4 = N / 4, total = (long long)M * n4;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int row = (int)(e / n4), col = (int)(e % n4) * 4;
+        const float* src = part + (size_t)row * ldp + col;
+        float4 v[8];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int z0 = 0; z0 < Z; z0 += 8) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (z0 + j < Z) v[j] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(z0 + j) * slab));
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (z0 + j < Z) {
+                    acc.x += v[j].x;
+                    acc.y += v[j].y;
+                    acc.z += v[j].z;
+                    acc.w += v[j].w;
+                }
+        }
+        *reinterpret_cast<float4*>(y + (size_t)row * ldy + col) = acc;
+    }
+}
+
 template <bool SPLIT, bool F16, int BN>
 int launch_one(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
     constexpr size_t smem = DenseCfg<SPLIT, BN>::SMEM;
@@ -228,7 +232,14 @@ int launch_one(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
     }
     const dim3 grid((unsigned)((a.M + DT_BM - 1) / DT_BM), (unsigned)((a.N + BN - 1) / BN),
                     (unsigned)(a.splits > 1 ? a.splits : 1));
-    return (int)launch_k(gemm_dense_kernel<SPLIT, F16, BN>, grid, dim3(128), smem, s, maps, a);
+    int e = (int)launch_k(gemm_dense_kernel<SPLIT, F16, BN>, grid, dim3(128), smem, s, maps, a);
+    if (e || a.splits <= 1) return e;
+    const size_t ldp = (size_t)grid.y * BN, slab = (size_t)grid.x * DT_BM * ldp;
+    const long long items = (long long)a.M * (a.N / 4);
+    long long blocks = (items + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    return (int)launch_k(dense_split_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
+                         (const float*)a.part, a.splits, a.M, a.N, slab, ldp, a.y, a.ldy);
 }
 
 template <bool SPLIT, bool F16>
@@ -267,7 +278,7 @@ int launch_dense(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
         (!a.y && !a.amax) || a.n_seg0 % DT_BN ||
         (a.n_seg1 < a.N && (a.n_seg1 % DT_BN || a.n_seg1 < a.n_seg0)) || a.m_off < 0 ||
         (a.bn != 0 && a.bn != 128 && a.bn != 256) || a.splits > a.K / DT_BK ||
-        (a.splits > 1 && (a.bn == 0 || !a.part || !a.tickets)))
+        (a.splits > 1 && (a.bn == 0 || !a.part || !a.y || a.amax || a.N % 4)))
         return (int)cudaErrorInvalidValue;
     if (a.f16) return a.x_split ? launch_bn<true, true>(maps, a, s) : launch_bn<false, true>(maps, a, s);
     return a.x_split ? launch_bn<true, false>(maps, a, s) : launch_bn<false, false>(maps, a, s);

@@ -38,13 +38,13 @@ struct DenseArgs {
     int ldy;            // a multiple of 4
     int* err;           // device [code, site]: a wait that timed out sets it (code 0 before)
     // split-K: `splits` CTAs per output tile share its k-blocks (contiguous
-    // ranges in split order); each stores its fp32 partial tile in `part`
-    // ([tiles][splits][128][bn]) and the last to arrive on the tile's ticket
-    // adds the partials in split order 0, 1, ... (so a row's result depends
-    // on N, K and `splits`, never on M or timing) and runs the epilogue.
+    // ranges in split order); each stores its fp32 partial rows in slab z of
+    // `part` ([splits][m tiles * 128][n tiles * bn]) and a reduce kernel
+    // launched after the GEMM adds the slabs in split order 0, 1, ... into y
+    // (so a row's result depends on N, K and `splits`, never on M or
+    // timing).  Needs y, bn 128 or 256, N a multiple of 4; no argmax.
     int splits;         // 1: no split
     float* part;
-    int* tickets;       // [m tiles * n tiles], zero between launches
     int bn;             // tile width: 0 = chosen by wave balance, else 128 or 256
     // argmax epilogue (LM head): per row the packed key (orderable logit,
     // ~column) of the largest column, atomicMax into amax[row]

@@ -294,22 +294,59 @@ __device__ __forceinline__ void store_hilo(void* hi, void* lo, size_t i, float v
     reinterpret_cast<__nv_bfloat16*>(lo)[i] = __float2bfloat16_rn(v - __bfloat162float(h));
 }
 
-// One CTA of 256 threads per row; sum of squares in a fixed order.
+// One CTA of 256 threads per row; sum of squares in a fixed order.  A
+// thread holds its (up to 16) elements of the row in registers: all of its
+// loads are issued before the first use, instead of one round trip per
+// element (rows wider than 4096 take the plain loop).
 __global__ void resid_norm_kernel(ResidNormArgs a) {
     pdl_trigger();
     pdl_wait();
+    constexpr int PER = 16;
     const int r = blockIdx.x, tid = threadIdx.x;
     float* x = a.x + (size_t)r * a.hidden;
+    const float* y = a.y ? a.y + (size_t)r * a.hidden : nullptr;
     __shared__ float s_part[8];
     float ss = 0.f;
-    for (int j = tid; j < a.hidden; j += 256) {
-        float v = x[j];
-        if (a.y) {
-            v += a.y[(size_t)r * a.hidden + j];
-            x[j] = v;
+    float v[PER];
+    const bool held = a.hidden <= 256 * PER;
+    if (held) {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int j = tid + 256 * i;
+            v[i] = j < a.hidden ? x[j] : 0.f;
         }
-        if (a.tap_hi) store_hilo(a.tap_hi, a.tap_lo, (size_t)r * a.tap_ld + a.tap_col + j, v);
-        ss = fmaf(v, v, ss);
+        if (y) {
+            float w[PER];
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int j = tid + 256 * i;
+                w[i] = j < a.hidden ? y[j] : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int j = tid + 256 * i;
+                v[i] += w[i];
+                if (j < a.hidden) x[j] = v[i];
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int j = tid + 256 * i;
+            if (j < a.hidden) {
+                if (a.tap_hi) store_hilo(a.tap_hi, a.tap_lo, (size_t)r * a.tap_ld + a.tap_col + j, v[i]);
+                ss = fmaf(v[i], v[i], ss);
+            }
+        }
+    } else {
+        for (int j = tid; j < a.hidden; j += 256) {
+            float u = x[j];
+            if (y) {
+                u += y[j];
+                x[j] = u;
+            }
+            if (a.tap_hi) store_hilo(a.tap_hi, a.tap_lo, (size_t)r * a.tap_ld + a.tap_col + j, u);
+            ss = fmaf(u, u, ss);
+        }
     }
     ss = warp_sum(ss);
     if ((tid & 31) == 0) s_part[tid >> 5] = ss;
@@ -318,8 +355,16 @@ __global__ void resid_norm_kernel(ResidNormArgs a) {
 #pragma unroll
     for (int w = 0; w < 8; ++w) tot += s_part[w];
     const float rstd = 1.0f / sqrtf(tot / (float)a.hidden + a.eps);
-    for (int j = tid; j < a.hidden; j += 256)
-        store_hilo(a.hi, a.lo, (size_t)r * a.hidden + j, x[j] * a.w[j] * rstd, a.f16);
+    if (held) {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int j = tid + 256 * i;
+            if (j < a.hidden) store_hilo(a.hi, a.lo, (size_t)r * a.hidden + j, v[i] * a.w[j] * rstd, a.f16);
+        }
+    } else {
+        for (int j = tid; j < a.hidden; j += 256)
+            store_hilo(a.hi, a.lo, (size_t)r * a.hidden + j, x[j] * a.w[j] * rstd, a.f16);
+    }
 }
 
 // One warp per (row, head) over the q, k and v heads; lane l holds

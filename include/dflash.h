@@ -193,9 +193,10 @@ int dflash_init(const dflash_config* cfg /*host*/, const dflash_weights* w /*hos
  * Drafter-alone mode (tgt_layers == 0): ext_taps holds n_ext tap rows as
  *   dtype [n_taps][n_ext][hc*hidden] (hc streams per tap layer, reduced by
  *   their mean); rows are positions 0..n_ext-1 and first_token is the pending
- *   token at position n_ext.  With a bf16 or INT4 drafter and hc = 1 the
- *   window's rows are ingested on the dense tcgen05 GEMM
- *   (DFLASH_DENSE_INGEST=0 at dflash_init: 16-row chunks).
+ *   token at position n_ext.  With a bf16 or INT4 drafter the window's rows
+ *   are ingested on the dense tcgen05 GEMM, hc > 1 streams reduced to their
+ *   mean as bf16 hi/lo rows first (DFLASH_DENSE_INGEST=0 at dflash_init:
+ *   16-row chunks).
  * max_new is the generation budget (the first token counts).  Errors:
  * ARG, CAPACITY (n_prompt or n_ext + block > max_seq), STATE.
  */

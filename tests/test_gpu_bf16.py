@@ -257,6 +257,42 @@ def test_dense_ingest_matches_chunked(qwen, monkeypatch, int4):
     assert err.max() < TOL / 4, err
 
 
+def test_dense_ingest_hc4_matches_chunked_and_oracle(qwen, monkeypatch):
+    """External tap windows of hyper-connection streams (hc = 4 per tap
+    layer, 300 rows): the dense ingest reduces each layer's streams to their
+    mean as bf16 hi/lo rows and runs fc on both planes; its draft cache rows
+    match the 16-row chunks to fp16 rounding, and the next draft's logits
+    match the oracle's drafter over the oracle's hc-mean taps."""
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+    Wd = W.with_(tgt_layers=0, tap_layers=(0, 8, 17, 26, 35)[:2], max_seq=512)
+    n, hc = 300, 4
+    streams = synth.hc_streams(Wd.n_taps, n, hc, W.hidden)        # [n_taps][n][hc * H] bf16
+    out = []
+    for env in (None, "0"):
+        if env is not None:
+            monkeypatch.setenv("DFLASH_DENSE_INGEST", env)
+        dec = DFlash(Wd, qwen["m"])
+        monkeypatch.delenv("DFLASH_DENSE_INGEST", raising=False)
+        dl = G.logits_buf(W.vocab)
+        dec.set_logits_out(None, dl)
+        dec.prefill_taps(streams, hc=hc, first_token=321, max_new=32)
+        ids = dec.draft().cpu().numpy()
+        dec.check()
+        cap = (Wd.max_seq + 63) // 64 * 64
+        kv = dec.kv_draft.view(torch.float16).view(Wd.drf_layers, 2, Wd.n_kv, cap, W.head_dim)
+        out.append((kv[:, :, :, :n].float().clone(), dl[1:W.block].clone(), ids))
+        dec.close()
+    (kv_d, lg_d, ids_d), (kv_c, lg_c, _) = out
+    scale = kv_c.abs().amax(dim=-1, keepdim=True).clamp_min(1e-6)
+    assert ((kv_d - kv_c).abs() / scale).max().item() < 2.0 ** -9
+    err = G.rel_err_rows(lg_d.cpu().numpy(), lg_c.cpu().numpy())
+    assert err.max() < TOL / 4, err
+    taps = O.tap_concat([streams[i].float().numpy() for i in range(Wd.n_taps)], hc)
+    ref, _ = O.draft_forward(qwen["dw"], qwen["tw"].embed, qwen["cfg"], taps, 321, n, W.block)
+    G.check_rows("bf16_dense_ingest_hc4", lg_d.cpu().numpy(), ids_d[:W.block - 1], ref[1:], TOL,
+                 DEC_TOL)
+
+
 def test_dense_prefill_matches_chunked_and_oracle(qwen, monkeypatch):
     """The dense prompt prefill of the bf16 target (default: every prompt row
     before the last 16-row chunk through the dense tcgen05 GEMM and the

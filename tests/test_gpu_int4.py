@@ -5,7 +5,9 @@ bit-identical, see test_quantizer_bit_exact_with_oracle), and the drafter
 fed 300 external tap rows with a 64-row sliding window must give logits
 within rel 2e-2 of the oracle's dequantised fp64 drafter.  Norm weights are
 drawn N(1, 0.1); ids are checked on every row decidable at the GPU row's
-measured error, with a floor taken at DEC_TOL (see tests/gpu_common.py)."""
+measured error, with a floor taken at DEC_TOL (see tests/gpu_common.py):
+2e-3 here, because GEMMs with INT4 weights take their activations as one
+f16 plane (11 mantissa bits; bf16 weights take hi/lo bf16 planes, ~16)."""
 
 import numpy as np
 import pytest
@@ -19,7 +21,7 @@ from tests.oracle_inputs import ModelTensors, oracle_config, oracle_draft
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
-DEC_TOL = 1e-3
+DEC_TOL = 2e-3
 NORM_STD = 0.1
 W = DRAFT_INT4.with_(name="int4_1layer", drf_layers=1, n_ctx=300, window=64, max_seq=400)
 
