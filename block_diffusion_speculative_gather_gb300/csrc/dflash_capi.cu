@@ -662,31 +662,31 @@ int run_layers(dflash_ctx* c, bool target, Emit& em) {
             if (em.rec) return fail(DFLASH_ERR_CONFIG, "fp32 attention has no persistent form");
             LAUNCH_TRY(launch_attention(at, em.s));
         }
-        a = lp.o.args;
-        a.out = x;
-        a.ldo = H;
-        set_norm_out(c, a, lw.ln_mlp, true, xt);
-        if ((r = run_gemm(c, lp.o, a, em))) return r;
-        a = lp.gateup.args;
-        set_norm_in(c, a, true);
-        a.act = c->ws + c->L.act;
-        a.ld_act = g.ffn;
-        a.act_type = xt;
-        if ((r = run_gemm(c, lp.gateup, a, em))) return r;
-        a = lp.down.args;
-        a.out = x;
-        a.ldo = H;
+        GemmArgs ao = lp.o.args;
+        ao.out = x;
+        ao.ldo = H;
+        set_norm_out(c, ao, lw.ln_mlp, true, xt);
+        GemmArgs agu = lp.gateup.args;
+        set_norm_in(c, agu, true);
+        agu.act = c->ws + c->L.act;
+        agu.ld_act = g.ffn;
+        agu.act_type = xt;
+        GemmArgs ad = lp.down.args;
+        ad.out = x;
+        ad.ldo = H;
         const float* w_next = l + 1 < nl ? (target ? c->tgt[l + 1] : c->drf[l + 1]).ln_attn : final_norm;
-        set_norm_out(c, a, w_next, true, l + 1 < nl ? xt : c->xt_lm());
+        set_norm_out(c, ad, w_next, true, l + 1 < nl ? xt : c->xt_lm());
         if (target && g.drf_layers > 0) {
             for (int i = 0; i < g.n_taps; ++i)
                 if (g.tap_layer[i] == l) {
-                    a.tap_out = c->ws + c->L.taps + (size_t)i * H * elem_size(g.dtype);   // column i*H
-                    a.ld_tap = g.n_taps * H;
-                    a.tap_type = c->act_xt();   // taps feed fc (bf16 weights)
+                    ad.tap_out = c->ws + c->L.taps + (size_t)i * H * elem_size(g.dtype);   // column i*H
+                    ad.ld_tap = g.n_taps * H;
+                    ad.tap_type = c->act_xt();   // taps feed fc (bf16 weights)
                 }
         }
-        if ((r = run_gemm(c, lp.down, a, em))) return r;
+        if ((r = run_gemm(c, lp.o, ao, em))) return r;
+        if ((r = run_gemm(c, lp.gateup, agu, em))) return r;
+        if ((r = run_gemm(c, lp.down, ad, em))) return r;
     }
     return DFLASH_OK;
 }

@@ -33,10 +33,13 @@
 //    (one 32-byte run per row) and the same permutation of k is applied to
 //    both operands, so fragments come from plain 16-byte shared loads;
 //  * fp32 weights (the tiny fp32 workload) use CUDA-core FMAs in k order;
-//  * a tile whose k-range is split across CTAs is finished by the last CTA
-//    to arrive (atomic ticket, no waiting), which sums the parts in a fixed
-//    order: the result of a row never depends on how many rows the forward
-//    has, on timing, or on the other rows (batch invariance);
+//  * a tile whose k-range is split across CTAs is finished by its owner,
+//    the CTA whose range reaches the tile's first k-block (it gets there
+//    last): the others store their parts and publish them on the tile's
+//    counter without waiting, the owner waits (bounded) for them and sums
+//    the parts in CTA order: the result of a row never depends on how many
+//    rows the forward has, on timing, or on the other rows (batch
+//    invariance);
 //  * fused epilogues: store fp32, residual add (+ tap copy), SwiGLU of
 //    paired gate/up tiles, LM-head argmax with packed 64-bit atomicMax.
 //

@@ -290,10 +290,15 @@ __device__ __forceinline__ void finish_tile(const GemmArgs& a, int tile, const f
         // part goes to this CTA's slot; the tile's owner, CTA i_first (whose
         // range ends in the tile, so it reaches the tile last), is told
         // through the tile's counter and nothing here waits.
+        // The barrier orders every thread's part stores before thread 0's
+        // release add, and a release is cumulative over what was ordered
+        // before it, so the add publishes the whole part; no thread fences
+        // on its own stores (a fence per thread held all consumer warps for
+        // the stores' acknowledgement, several microseconds under the full
+        // weight stream, while the ring stalled behind them).
         float* mine = a.slots + (size_t)cta * 2 * (GEMM_BN * DFL_MAX_ROWS);
         for (int e = tid; e < GEMM_BN * DFL_MAX_ROWS; e += GEMM_CONSUMERS * 32)
             __stcg(mine + e, ctile[e]);
-        __threadfence();
         consumer_bar();
         if (tid == 0) red_release_add_s32(&a.counters[tile], 1);
         do_epi = false;
@@ -318,7 +323,8 @@ __device__ __forceinline__ void finish_tile(const GemmArgs& a, int tile, const f
         consumer_bar();
         do_epi = !aborted && s_flags[1] != 0;
         if (do_epi) {
-            __threadfence();
+            // Thread 0's acquire, then the barrier, order the parts' loads
+            // (L2, __ldcg) after their publication for every thread.
             // Each thread owns 8 consecutive elements (two float4).
             const int e0 = tid * 8;
             float4 acc0 = *reinterpret_cast<const float4*>(ctile + e0);
