@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(256) batch_rows_kernel(BatchRowsArgs b) {
 
 struct BatchQkvArgs {
     const float* y;                 // [R][(n_q + 2 n_kv) hd]: q heads, k heads, v heads
+    int y_splits;                   // > 1: y is that many split-K slabs, summed in split order
+    size_t y_slab;
     DevState* const* sts;
     int rows, n_q, n_kv, head_dim, cap, max_seq;
     const float* q_norm;
@@ -172,6 +174,24 @@ __global__ void batch_qkv_rows_kernel(BatchQkvArgs a) {
     const float* src = a.y + (size_t)r * heads * hd + (size_t)h * hd;
 #pragma unroll
     for (int m = 0; m < 4; ++m) v[m] = (m < per && t < T) ? src[lane + 32 * m] : 0.f;
+    if (a.y_splits > 1 && t < T) {
+        // every split's loads in flight at once, then the adds in split order
+        float u[7][4];
+#pragma unroll
+        for (int z = 1; z < 8; ++z)
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                u[z - 1][m] = (z < a.y_splits && m < per) ? __ldcg(src + (size_t)z * a.y_slab + lane + 32 * m) : 0.f;
+#pragma unroll
+        for (int z = 1; z < 8; ++z)
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                if (z < a.y_splits) v[m] += u[z - 1][m];
+        for (int z = 8; z < a.y_splits; ++z)
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                if (m < per) v[m] += __ldcg(src + (size_t)z * a.y_slab + lane + 32 * m);
+    }
     if (t < T && (is_q || is_k)) {
         const float* nw = is_q ? a.q_norm : a.k_norm;
         float ss = 0.f;
@@ -337,11 +357,13 @@ namespace {
 
 size_t up1k(size_t v) { return (v + 1023) / 1024 * 1024; }
 
-// Split count of a GEMM: about one CTA per SM over the 128-column tiles,
+// Split count of a GEMM: at most one CTA per SM over the 128-column tiles,
 // at most 8, at least two k-blocks per split.  Depends on N and K only.
 int splits_for(int N, int K, int sms) {
     const int tiles = (N + 127) / 128;
-    int z = (int)std::lround((double)sms / tiles);
+    // rounded down: one CTA per SM, so a count past the SMs adds a wave
+    // (rounding to nearest gave o and down 160 CTAs on 152 SMs)
+    int z = sms / tiles;
     z = z < 1 ? 1 : (z > 8 ? 8 : z);
     const int kmax = (K / DT_BK) / 2;
     return z > kmax ? (kmax < 1 ? 1 : kmax) : z;
@@ -456,8 +478,16 @@ int dense_maps(DenseMaps* m, const void* hi, const void* lo, int R, int K, const
         }                                                                                          \
     } while (0)
 
+// Where a row kernel finds a dense GEMM's output: y rows, or the split-K
+// slabs the row kernel sums itself (no reduce launch).
+struct YView {
+    const float* y;
+    int splits;
+    size_t slab;
+};
+
 int dense(dflash_batch* b, const DenseMaps& m, int N, int K, int seg0, int seg1, float* y,
-          unsigned long long* amax, cudaStream_t s) {
+          unsigned long long* amax, cudaStream_t s, YView* view = nullptr) {
     DenseArgs d{};
     d.M = b->R;
     d.N = N;
@@ -472,6 +502,16 @@ int dense(dflash_batch* b, const DenseMaps& m, int N, int K, int seg0, int seg1,
     d.amax = amax;
     d.splits = amax ? 1 : splits_for(N, K, b->sms);
     d.part = b->part;
+    if (view) {
+        size_t slab = 0, ldp = 0;
+        dense_part_layout(d.M, N, d.bn, &slab, &ldp);
+        if (d.splits > 1 && ldp == (size_t)N) {   // slab rows are y rows: the consumer sums them
+            d.keep_parts = 1;
+            *view = YView{b->part, d.splits, slab};
+        } else {
+            *view = YView{y, 1, 0};
+        }
+    }
     const int e = launch_dense(m, d, s);
     if (e) return report_error(DFLASH_ERR_CUDA, "dense GEMM (N %d K %d): %s", N, K, cudaGetErrorString((cudaError_t)e));
     return DFLASH_OK;
@@ -490,10 +530,13 @@ int batch_layers(dflash_batch* b, bool target, cudaStream_t s) {
     const int cap = (g.max_seq + 63) / 64 * 64;
     for (int l = 0; l < nl; ++l) {
         const dflash_batch::LayerMaps& M = target ? b->tl[l] : b->dl[l];
-        int r = dense(b, M.qkv, qd + 2 * kvd, H, qd, qd + kvd, b->y, nullptr, s);
+        YView yv{};
+        int r = dense(b, M.qkv, qd + 2 * kvd, H, qd, qd + kvd, b->y, nullptr, s, &yv);
         if (r) return r;
         BatchQkvArgs qa{};
-        qa.y = b->y;
+        qa.y = yv.y;
+        qa.y_splits = yv.splits;
+        qa.y_slab = yv.slab;
         qa.sts = b->sts;
         qa.rows = b->R;
         qa.n_q = g.n_q;
@@ -527,10 +570,12 @@ int batch_layers(dflash_batch* b, bool target, cudaStream_t s) {
         at.out_hi = b->hi;
         at.out_lo = b->lo;
         BTRY(launch_batch_attention(b->qmap, target ? b->kvmap_t : b->kvmap_d, at, b->S, s));
-        if ((r = dense(b, M.o, H, qd, 1 << 30, 1 << 30, b->y, nullptr, s))) return r;
+        if ((r = dense(b, M.o, H, qd, 1 << 30, 1 << 30, b->y, nullptr, s, &yv))) return r;
         ResidNormArgs rn{};
         rn.x = b->x;
-        rn.y = b->y;
+        rn.y = yv.y;
+        rn.y_splits = yv.splits;
+        rn.y_slab = yv.slab;
         rn.rows = b->R;
         rn.hidden = H;
         rn.w = lw[l].ln_mlp;
@@ -540,10 +585,12 @@ int batch_layers(dflash_batch* b, bool target, cudaStream_t s) {
         BTRY(launch_resid_norm(rn, s));
         if ((r = dense(b, M.gu, 2 * F, H, F, 1 << 30, b->y, nullptr, s))) return r;
         BTRY(launch_swiglu_rows(b->y, b->R, F, b->hi, b->lo, 0, s));
-        if ((r = dense(b, M.down, H, F, 1 << 30, 1 << 30, b->y, nullptr, s))) return r;
+        if ((r = dense(b, M.down, H, F, 1 << 30, 1 << 30, b->y, nullptr, s, &yv))) return r;
         rn = ResidNormArgs{};
         rn.x = b->x;
-        rn.y = b->y;
+        rn.y = yv.y;
+        rn.y_splits = yv.splits;
+        rn.y_slab = yv.slab;
         rn.rows = b->R;
         rn.hidden = H;
         rn.w = l + 1 < nl ? lw[l + 1].ln_attn : (target ? w.final_norm_tgt : w.final_norm_drf);

@@ -233,7 +233,7 @@ int launch_one(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
     const dim3 grid((unsigned)((a.M + DT_BM - 1) / DT_BM), (unsigned)((a.N + BN - 1) / BN),
                     (unsigned)(a.splits > 1 ? a.splits : 1));
     int e = (int)launch_k(gemm_dense_kernel<SPLIT, F16, BN>, grid, dim3(128), smem, s, maps, a);
-    if (e || a.splits <= 1) return e;
+    if (e || a.splits <= 1 || a.keep_parts) return e;
     const size_t ldp = (size_t)grid.y * BN, slab = (size_t)grid.x * DT_BM * ldp;
     const long long items = (long long)a.M * (a.N / 4);
     long long blocks = (items + 255) / 256;
@@ -271,14 +271,20 @@ size_t dense_split_floats(int M, int N, int splits, int bn) {
 
 int dense_tiles(int M, int N, int bn) { return ((M + DT_BM - 1) / DT_BM) * ((N + bn - 1) / bn); }
 
+void dense_part_layout(int M, int N, int bn, size_t* slab, size_t* ldp) {
+    *ldp = (size_t)((N + bn - 1) / bn) * bn;
+    *slab = (size_t)((M + DT_BM - 1) / DT_BM) * DT_BM * *ldp;
+}
+
 size_t dense_smem(bool split) { return split ? DenseCfg<true, DT_BN>::SMEM : DenseCfg<false, DT_BN>::SMEM; }
 
 int launch_dense(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
+    const bool kept = a.splits > 1 && a.keep_parts;
     if (a.M < 1 || a.N < 1 || a.K < DT_BK || a.K % DT_BK || (a.y && (a.ldy < a.N || a.ldy % 4)) ||
-        (!a.y && !a.amax) || a.n_seg0 % DT_BN ||
+        (!a.y && !a.amax && !kept) || a.n_seg0 % DT_BN ||
         (a.n_seg1 < a.N && (a.n_seg1 % DT_BN || a.n_seg1 < a.n_seg0)) || a.m_off < 0 ||
         (a.bn != 0 && a.bn != 128 && a.bn != 256) || a.splits > a.K / DT_BK ||
-        (a.splits > 1 && (a.bn == 0 || !a.part || !a.y || a.amax || a.N % 4)))
+        (a.splits > 1 && (a.bn == 0 || !a.part || (!a.y && !kept) || a.amax || a.N % 4)))
         return (int)cudaErrorInvalidValue;
     if (a.f16) return a.x_split ? launch_bn<true, true>(maps, a, s) : launch_bn<false, true>(maps, a, s);
     return a.x_split ? launch_bn<true, false>(maps, a, s) : launch_bn<false, false>(maps, a, s);

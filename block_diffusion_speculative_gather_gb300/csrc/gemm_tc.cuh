@@ -45,6 +45,8 @@ struct DenseArgs {
     // timing).  Needs y, bn 128 or 256, N a multiple of 4; no argmax.
     int splits;         // 1: no split
     float* part;
+    int keep_parts;     // split-K: 1 = no reduce launch; the slabs stay for
+                        // a consumer that sums them itself (y unused then)
     int bn;             // tile width: 0 = chosen by wave balance, else 128 or 256
     // argmax epilogue (LM head): per row the packed key (orderable logit,
     // ~column) of the largest column, atomicMax into amax[row]
@@ -53,6 +55,9 @@ struct DenseArgs {
 
 // Host: partial-tile floats a split launch needs, and its ticket count.
 size_t dense_split_floats(int M, int N, int splits, int bn);
+// Host: where a split launch's partial rows go: slab z of `part` starts at
+// z * slab floats, row m of a slab at m * ldp.
+void dense_part_layout(int M, int N, int bn, size_t* slab, size_t* ldp);
 int dense_tiles(int M, int N, int bn);
 
 // Host: dynamic shared memory of the kernel (x_split or not), the launch

@@ -322,6 +322,34 @@ __global__ void resid_norm_kernel(ResidNormArgs a) {
                 const int j = tid + 256 * i;
                 w[i] = j < a.hidden ? y[j] : 0.f;
             }
+            if (a.y_splits > 1) {
+                // every split's loads of 8 columns in flight at once, then
+                // the adds in split order (a split at a time cost one L2
+                // round trip per split)
+#pragma unroll
+                for (int i0 = 0; i0 < PER; i0 += 8) {
+                    float u[7][8];
+#pragma unroll
+                    for (int z = 1; z < 8; ++z)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int j = tid + 256 * (i0 + i);
+                            u[z - 1][i] = (z < a.y_splits && j < a.hidden)
+                                              ? __ldcg(y + (size_t)z * a.y_slab + j) : 0.f;
+                        }
+#pragma unroll
+                    for (int z = 1; z < 8; ++z)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (z < a.y_splits) w[i0 + i] += u[z - 1][i];
+                }
+                for (int z = 8; z < a.y_splits; ++z)
+#pragma unroll
+                    for (int i = 0; i < PER; ++i) {
+                        const int j = tid + 256 * i;
+                        if (j < a.hidden) w[i] += __ldcg(y + (size_t)z * a.y_slab + j);
+                    }
+            }
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
                 const int j = tid + 256 * i;
@@ -341,7 +369,9 @@ __global__ void resid_norm_kernel(ResidNormArgs a) {
         for (int j = tid; j < a.hidden; j += 256) {
             float u = x[j];
             if (y) {
-                u += y[j];
+                float t = y[j];
+                for (int z = 1; z < a.y_splits; ++z) t += __ldcg(y + (size_t)z * a.y_slab + j);
+                u += t;
                 x[j] = u;
             }
             if (a.tap_hi) store_hilo(a.tap_hi, a.tap_lo, (size_t)r * a.tap_ld + a.tap_col + j, u);

@@ -121,7 +121,12 @@ int launch_embed_rows(const int32_t* tokens, int rows, const void* embed, int hi
 // [rows][tap_ld] at column tap_col.
 struct ResidNormArgs {
     float* x;
-    const float* y;
+    const float* y;       // [rows][hidden], or NULL (no residual add)
+    // y_splits > 1: y holds that many split-K partial slabs of a dense GEMM
+    // (slab z at y + z * y_slab, rows of `hidden`), summed here in split
+    // order 0, 1, ... (the order of the dense GEMM's own reduce)
+    int y_splits;
+    size_t y_slab;
     int rows, hidden;
     const float* w;
     float eps;
