@@ -333,6 +333,8 @@ struct dflash_batch {
     float* x = nullptr;
     void* hi = nullptr;
     void* lo = nullptr;
+    void* ahi = nullptr;   // [R][ffn] SwiGLU output planes: the down projection's input
+    void* alo = nullptr;
     void* thi = nullptr;
     void* tlo = nullptr;
     float* y = nullptr;
@@ -386,7 +388,7 @@ void attn_splits(const dflash_config& g, bool target, int* chunks, int* splits) 
 }
 
 struct BatchLayout {
-    size_t sts, x, hi, lo, thi, tlo, y, q, rcos, rsin, amax, part, apart, err, total;
+    size_t sts, x, hi, lo, ahi, alo, thi, tlo, y, q, rcos, rsin, amax, part, apart, err, total;
 };
 
 BatchLayout batch_layout(const dflash_config& g, int S, int sms) {
@@ -416,6 +418,8 @@ BatchLayout batch_layout(const dflash_config& g, int S, int sms) {
     L.x = take(R * H * 4);
     L.hi = take(R * wmax * 2);
     L.lo = take(R * wmax * 2);
+    L.ahi = take(R * (size_t)F * 2);
+    L.alo = take(R * (size_t)F * 2);
     L.thi = take(R * (size_t)(tw ? tw : 64) * 2);
     L.tlo = take(R * (size_t)(tw ? tw : 64) * 2);
     L.y = take(R * ymax * 4);
@@ -458,14 +462,14 @@ int sm_count() {
 
 // x planes [R][K] of a GEMM input (box 128 rows x 64) and its weight maps
 int dense_maps(DenseMaps* m, const void* hi, const void* lo, int R, int K, const void* const* w, const int* rows,
-               int nseg) {
+               int nseg, int wbox = DT_WBOX) {
     memset(m, 0, sizeof *m);
     int r = encode_map(&m->x, hi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, R, DT_BK, DT_BM,
                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (!r) r = encode_map(&m->x_lo, lo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, R, DT_BK, DT_BM,
                            CU_TENSOR_MAP_SWIZZLE_128B);
     for (int i = 0; i < nseg && !r; ++i)
-        r = encode_map(&m->w[i], w[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, rows[i], DT_BK, DT_WBOX,
+        r = encode_map(&m->w[i], w[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, rows[i], DT_BK, wbox,
                        CU_TENSOR_MAP_SWIZZLE_128B);
     return r;
 }
@@ -514,6 +518,30 @@ int dense(dflash_batch* b, const DenseMaps& m, int N, int K, int seg0, int seg1,
     }
     const int e = launch_dense(m, d, s);
     if (e) return report_error(DFLASH_ERR_CUDA, "dense GEMM (N %d K %d): %s", N, K, cudaGetErrorString((cudaError_t)e));
+    return DFLASH_OK;
+}
+
+// Fused gate/up with the SwiGLU epilogue: silu(gate) * up straight into
+// the down projection's input planes (ahi / alo), 128-column tiles.
+int dense_swiglu(dflash_batch* b, const DenseMaps& m, int F, int K, cudaStream_t s) {
+    DenseArgs d{};
+    d.M = b->R;
+    d.N = 2 * F;
+    d.K = K;
+    d.n_seg0 = 1 << 30;
+    d.n_seg1 = 1 << 30;
+    d.x_split = 1;
+    d.err = b->err;
+    d.bn = 128;
+    d.splits = 1;
+    d.swiglu = 1;
+    d.up_map = 1;
+    d.up_row = 0;
+    d.act_hi = b->ahi;
+    d.act_lo = b->alo;
+    d.act_ld = F;
+    const int e = launch_dense(m, d, s);
+    if (e) return report_error(DFLASH_ERR_CUDA, "dense SwiGLU GEMM (F %d K %d): %s", F, K, cudaGetErrorString((cudaError_t)e));
     return DFLASH_OK;
 }
 
@@ -583,8 +611,7 @@ int batch_layers(dflash_batch* b, bool target, cudaStream_t s) {
         rn.hi = b->hi;
         rn.lo = b->lo;
         BTRY(launch_resid_norm(rn, s));
-        if ((r = dense(b, M.gu, 2 * F, H, F, 1 << 30, b->y, nullptr, s))) return r;
-        BTRY(launch_swiglu_rows(b->y, b->R, F, b->hi, b->lo, 0, s));
+        if ((r = dense_swiglu(b, M.gu, F, H, s))) return r;
         if ((r = dense(b, M.down, H, F, 1 << 30, 1 << 30, b->y, nullptr, s, &yv))) return r;
         rn = ResidNormArgs{};
         rn.x = b->x;
@@ -710,6 +737,8 @@ int dflash_batch_init(const dflash_config* cfg, const dflash_weights* w, int32_t
     b->x = reinterpret_cast<float*>(bw + L.x);
     b->hi = bw + L.hi;
     b->lo = bw + L.lo;
+    b->ahi = bw + L.ahi;
+    b->alo = bw + L.alo;
     b->thi = bw + L.thi;
     b->tlo = bw + L.tlo;
     b->y = reinterpret_cast<float*>(bw + L.y);
@@ -738,9 +767,10 @@ int dflash_batch_init(const dflash_config* cfg, const dflash_weights* w, int32_t
         if (!e) e = dense_maps(&M->o, b->hi, b->lo, R, qd, wo, ro, 1);
         const void* wgu[2] = {lw.w_gate, lw.w_up};
         const int rgu[2] = {F, F};
-        if (!e) e = dense_maps(&M->gu, b->hi, b->lo, R, H, wgu, rgu, 2);
+        // the SwiGLU form of the dense GEMM at 128-column tiles: 64-row weight boxes
+        if (!e) e = dense_maps(&M->gu, b->hi, b->lo, R, H, wgu, rgu, 2, DT_SWBOX);
         const void* wd[1] = {lw.w_down};
-        if (!e) e = dense_maps(&M->down, b->hi, b->lo, R, F, wd, ro, 1);
+        if (!e) e = dense_maps(&M->down, b->ahi, b->alo, R, F, wd, ro, 1);
         if (!e && draft) {
             const void* wkv[2] = {lw.wk, lw.wv};
             const int rkv[2] = {kvd, kvd};

@@ -77,7 +77,7 @@ int max_chunks(const dflash_config& c) { return cache_cap(c) / ATTN_CHUNK; }
 
 struct Layout {
     size_t state, x, hn, ssq, qrot, attn, act, taps, rcos, rsin, invf, amax, part, slots, counters,
-        acnt, amaps, barc, prog[3], ns[3], pf_x, pf_xlo, pf_y, pf_chi, pf_clo, pf_w, pp_x, pp_y, pp_hi, pp_lo, pp_q,
+        acnt, amaps, barc, prog[3], ns[3], pf_x, pf_xlo, pf_y, pf_chi, pf_clo, pf_w, pp_x, pp_y, pp_hi, pp_lo, pp_ahi, pp_alo, pp_q,
         pp_thi, pp_tlo, pf_rope, pp_w, total;
     int prog_n[3];
 };
@@ -190,6 +190,8 @@ Layout make_layout(const dflash_config& c) {
         L.pp_y = take((size_t)PF_ROWS * ywide * 4);
         L.pp_hi = take((size_t)PF_ROWS * xwide * 2);
         L.pp_lo = take((size_t)PF_ROWS * xwide * 2);
+        L.pp_ahi = take((size_t)PF_ROWS * c.ffn * 2);   // SwiGLU output planes: W_down's input
+        L.pp_alo = take((size_t)PF_ROWS * c.ffn * 2);
         L.pp_q = take((size_t)PF_ROWS * qd * 2);
         if (!L.pf_rope) L.pf_rope = take((size_t)PF_ROWS * c.head_dim * 4);
         if (c.tgt_wfmt == DFLASH_INT4G64) {   // the largest of a layer's matrices, dequantised to f16
@@ -1145,9 +1147,11 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
         const uint64_t qd = (uint64_t)g.n_q * g.head_dim, kvd = (uint64_t)g.n_kv * g.head_dim;
         const bool q4 = g.tgt_wfmt == DFLASH_INT4G64;   // f16 rows times exactly dequantised f16 weights
         const CUtensorMapDataType xt = q4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : bf;
-        auto xmaps = [&](DenseMaps& m, uint64_t width) {
-            int e = make_map_raw(&m.x, c->ws + L.pp_hi, xt, 2, width, PF_ROWS, DT_BK, DT_BM, sw);
-            if (!e) e = make_map_raw(&m.x_lo, c->ws + L.pp_lo, xt, 2, width, PF_ROWS, DT_BK, DT_BM, sw);
+        auto xmaps = [&](DenseMaps& m, uint64_t width, bool act = false) {
+            uint8_t* xh = c->ws + (act ? L.pp_ahi : L.pp_hi);
+            uint8_t* xl = c->ws + (act ? L.pp_alo : L.pp_lo);
+            int e = make_map_raw(&m.x, xh, xt, 2, width, PF_ROWS, DT_BK, DT_BM, sw);
+            if (!e) e = make_map_raw(&m.x_lo, xl, xt, 2, width, PF_ROWS, DT_BK, DT_BM, sw);
             return e;
         };
         c->d_pp.resize(g.tgt_layers);
@@ -1160,7 +1164,7 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
             if (!r) r = make_map_raw(&P.o.w[0], pw, xt, 2, qd, g.hidden, DT_BK, DT_WBOX, sw);
             if (!r) r = xmaps(P.gu, g.hidden);
             if (!r) r = make_map_raw(&P.gu.w[0], pw, xt, 2, g.hidden, 2 * (uint64_t)g.ffn, DT_BK, DT_WBOX, sw);
-            if (!r) r = xmaps(P.down, g.ffn);
+            if (!r) r = xmaps(P.down, g.ffn, true);
             if (!r) r = make_map_raw(&P.down.w[0], pw, xt, 2, g.ffn, g.hidden, DT_BK, DT_WBOX, sw);
         }
         for (int l = 0; l < g.tgt_layers && !r && !q4; ++l) {
@@ -1175,7 +1179,7 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
             if (!r) r = xmaps(P.gu, g.hidden);
             if (!r) r = make_map_raw(&P.gu.w[0], lw.w_gate, bf, 2, g.hidden, g.ffn, DT_BK, DT_WBOX, sw);
             if (!r) r = make_map_raw(&P.gu.w[1], lw.w_up, bf, 2, g.hidden, g.ffn, DT_BK, DT_WBOX, sw);
-            if (!r) r = xmaps(P.down, g.ffn);
+            if (!r) r = xmaps(P.down, g.ffn, true);
             if (!r) r = make_map_raw(&P.down.w[0], lw.w_down, bf, 2, g.ffn, g.hidden, DT_BK, DT_WBOX, sw);
         }
         if (!r)
@@ -1456,6 +1460,28 @@ int run_dense_prefill(dflash_ctx* c, const int32_t* tokens, int P, int commit_lo
         d.err = err;
         return launch_dense(m, d, s);
     };
+    // [W_gate; W_up] with the SwiGLU epilogue at 256-column tiles (128 gate
+    // rows + the matching 128 up rows, the maps' 128-row boxes), silu(gate)
+    // * up straight into W_down's input planes
+    auto dense_swiglu = [&](const DenseMaps& m, int R) {
+        DenseArgs d{};
+        d.M = R;
+        d.N = 2 * g.ffn;
+        d.K = g.hidden;
+        d.n_seg0 = 1 << 30;
+        d.n_seg1 = 1 << 30;
+        d.f16 = q4 ? 1 : 0;
+        d.x_split = 1;
+        d.err = err;
+        d.bn = 256;
+        d.swiglu = 1;
+        d.up_map = q4 ? 0 : 1;          // INT4: gate then up rows in one dequantised scratch
+        d.up_row = q4 ? g.ffn : 0;
+        d.act_hi = c->ws + c->L.pp_ahi;
+        d.act_lo = c->ws + c->L.pp_alo;
+        d.act_ld = g.ffn;
+        return launch_dense(m, d, s);
+    };
     for (int p0 = 0; p0 < P; p0 += PF_ROWS) {
         const int R = P - p0 < PF_ROWS ? P - p0 : PF_ROWS;
         LAUNCH_TRY(launch_embed_rows(tokens + p0, R, c->w.embed, g.hidden, g.vocab, x, c->st(), s));
@@ -1547,8 +1573,7 @@ int run_dense_prefill(dflash_ctx* c, const int32_t* tokens, int P, int commit_lo
                 LAUNCH_TRY(deq(lw.w_gate, lw.s_gate, g.ffn, g.hidden, 0));
                 LAUNCH_TRY(deq(lw.w_up, lw.s_up, g.ffn, g.hidden, g.ffn));
             }
-            LAUNCH_TRY(dense(PL.gu, R, 2 * g.ffn, g.hidden, g.ffn, 1 << 30));
-            LAUNCH_TRY(launch_swiglu_rows(y, R, g.ffn, hi, lo, q4 ? 1 : 0, s));
+            LAUNCH_TRY(dense_swiglu(PL.gu, R));
             if (q4) LAUNCH_TRY(deq(lw.w_down, lw.s_down, g.hidden, g.ffn, 0));
             LAUNCH_TRY(dense(PL.down, R, g.hidden, g.ffn, (g.hidden + DT_BN - 1) / DT_BN * DT_BN, 1 << 30));
         }

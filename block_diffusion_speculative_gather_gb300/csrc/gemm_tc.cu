@@ -17,12 +17,17 @@
 // Split-K (few rows: the many-sequence round): the k-blocks of a tile are
 // cut into `splits` contiguous ranges in split order; each split stores its
 // fp32 partial rows into its own slab, and a reduce kernel launched right
-// after adds the slabs in split order (coalesced, one pass over them), so a
-// row's result is the same whatever the number of rows.  The argmax epilogue (the LM head of that round) keeps per
-// row the packed (orderable logit, ~column) key of its largest column and
-// folds it into the row's key with atomicMax (lowest column on ties).
+// after adds the slabs in split order (coalesced, one pass over them) --
+// or, with keep_parts, the row kernel that consumes the output does -- so a
+// row's result is the same whatever the number of rows.  The argmax
+// epilogue (the LM head of that round) keeps per row the packed (orderable
+// logit, ~column) key of its largest column and folds it into the row's key
+// with atomicMax (lowest column on ties).  The SwiGLU form (the fused
+// gate/up projection) loads half a tile of gate rows and the matching half
+// of up rows and writes silu(gate) * up as hi/lo planes.
 
 #include "gemm_tc.cuh"
+#include "rows_dev.cuh"
 #include "tc_dev.cuh"
 
 namespace dfl {
@@ -31,6 +36,31 @@ namespace {
 
 __device__ __forceinline__ void dense_error(int* err, int site) {
     if (atomicCAS(&err[0], 0, DERR_TIMEOUT) == 0) err[1] = site;
+}
+
+// Eight consecutive values as hi/lo planes from element i (16-byte
+// aligned): the rounding of store_hilo, packed into one 16-byte store per
+// plane.
+__device__ __forceinline__ void store_hilo8(void* hi, void* lo, size_t i, const float* v, int f16) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (f16) {
+            const __half a = __float2half_rn(v[2 * q]), b = __float2half_rn(v[2 * q + 1]);
+            const __half la = __float2half_rn(v[2 * q] - __half2float(a));
+            const __half lb = __float2half_rn(v[2 * q + 1] - __half2float(b));
+            h[q] = (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
+            l[q] = (uint32_t)__half_as_ushort(la) | ((uint32_t)__half_as_ushort(lb) << 16);
+        } else {
+            const __nv_bfloat16 a = __float2bfloat16_rn(v[2 * q]), b = __float2bfloat16_rn(v[2 * q + 1]);
+            const __nv_bfloat16 la = __float2bfloat16_rn(v[2 * q] - __bfloat162float(a));
+            const __nv_bfloat16 lb = __float2bfloat16_rn(v[2 * q + 1] - __bfloat162float(b));
+            h[q] = (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+            l[q] = (uint32_t)__bfloat16_as_ushort(la) | ((uint32_t)__bfloat16_as_ushort(lb) << 16);
+        }
+    }
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(hi) + i) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(lo) + i) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 template <bool SPLIT, int BN>
@@ -98,10 +128,17 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
             mbar_arrive_expect_tx(&full[s], CFG::STAGE);
             tma_load_2d(st, &maps.x, &full[s], kx, a.m_off + m0);
             if (SPLIT) tma_load_2d(st + CFG::XB, &maps.x_lo, &full[s], kx, a.m_off + m0);
+            uint8_t* wst = st + (SPLIT ? 2 : 1) * CFG::XB;
+            if (a.swiglu) {   // BN / 2 gate rows, then the matching BN / 2 up rows
+                constexpr int HB = BN / 2;
+                const int t = n0 / BN;
+                tma_load_2d(wst, &maps.w[0], &full[s], kx, HB * t);
+                tma_load_2d(wst + HB * 128, &maps.w[a.up_map], &full[s], kx, a.up_row + HB * t);
+            } else {
 #pragma unroll
-            for (int b = 0; b < BN / DT_WBOX; ++b)
-                tma_load_2d(st + (SPLIT ? 2 : 1) * CFG::XB + b * DT_WBOX * 128, &maps.w[seg], &full[s],
-                            kx, wrow + b * DT_WBOX);
+                for (int b = 0; b < BN / DT_WBOX; ++b)
+                    tma_load_2d(wst + b * DT_WBOX * 128, &maps.w[seg], &full[s], kx, wrow + b * DT_WBOX);
+            }
         }
     } else if (threadIdx.x == 32) {   // ---- MMA issuer
         constexpr uint32_t ID = F16 ? tc::idesc_f16_f32(DT_BM, BN) : tc::idesc_bf16_f32(DT_BM, BN);
@@ -149,7 +186,25 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
         }
     }
     const bool last = Z == 1;
-    if (ok && last) {
+    if (ok && last && a.swiglu) {
+        // columns 0..BN/2-1 gate, BN/2..BN-1 up: silu(gate) * up into the
+        // hi/lo planes at columns (BN / 2) t.. of the row
+        constexpr int HB = BN / 2;
+        const int t = n0 / BN;
+#pragma unroll 1
+        for (int c = 0; c < HB / 32; ++c) {
+            float g[32], u[32];
+            tc::ld_x32(tm + ((uint32_t)(32 * warp) << 16) + 32 * c, g);
+            tc::ld_x32(tm + ((uint32_t)(32 * warp) << 16) + HB + 32 * c, u);
+            if (row < a.M) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) g[i] = swiglu(g[i], u[i]);
+                const size_t base = (size_t)row * a.act_ld + (size_t)HB * t + 32 * c;
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) store_hilo8(a.act_hi, a.act_lo, base + i, g + i, a.f16);
+            }
+        }
+    } else if (ok && last) {
         unsigned long long best = 0ull;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -280,8 +335,11 @@ size_t dense_smem(bool split) { return split ? DenseCfg<true, DT_BN>::SMEM : Den
 
 int launch_dense(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
     const bool kept = a.splits > 1 && a.keep_parts;
+    if (a.swiglu && ((a.bn != 128 && a.bn != 256) || a.splits > 1 || a.amax || a.N % a.bn || !a.act_hi || !a.act_lo ||
+                     a.act_ld % 8 || a.act_ld < a.N / 2 || a.up_map < 0 || a.up_map > 2 || a.up_row < 0))
+        return (int)cudaErrorInvalidValue;
     if (a.M < 1 || a.N < 1 || a.K < DT_BK || a.K % DT_BK || (a.y && (a.ldy < a.N || a.ldy % 4)) ||
-        (!a.y && !a.amax && !kept) || a.n_seg0 % DT_BN ||
+        (!a.y && !a.amax && !kept && !a.swiglu) || a.n_seg0 % DT_BN ||
         (a.n_seg1 < a.N && (a.n_seg1 % DT_BN || a.n_seg1 < a.n_seg0)) || a.m_off < 0 ||
         (a.bn != 0 && a.bn != 128 && a.bn != 256) || a.splits > a.K / DT_BK ||
         (a.splits > 1 && (a.bn == 0 || !a.part || (!a.y && !kept) || a.amax || a.N % 4)))

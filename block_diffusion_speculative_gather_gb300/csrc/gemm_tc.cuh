@@ -19,6 +19,7 @@ namespace dfl {
 constexpr int DT_BM = 128;   // rows of x per CTA (tensor-memory lanes)
 constexpr int DT_BN = 256;   // widest output tile (tensor-memory columns); 128 where it balances better
 constexpr int DT_WBOX = 128; // rows of one weight TMA box (a 256-column tile loads two)
+constexpr int DT_SWBOX = 64; // rows of a weight box of the SwiGLU form (gate and up halves)
 constexpr int DT_BK = 64;    // k per pipeline stage (one 128-byte swizzled row)
 
 struct DenseMaps {
@@ -51,6 +52,20 @@ struct DenseArgs {
     // argmax epilogue (LM head): per row the packed key (orderable logit,
     // ~column) of the largest column, atomicMax into amax[row]
     unsigned long long* amax;   // NULL: the plain fp32 store
+    // SwiGLU epilogue (the fused gate/up projection), tile width bn = 128
+    // or 256 fixed by the caller, h = bn / 2: output tile t holds the h gate
+    // rows h t.. of w[0] (columns 0..h-1) and the matching h up rows of
+    // w[up_map] at row up_row + h t (columns h..bn-1), each one weight box
+    // of h rows (the maps must be made with that box: DT_SWBOX rows for bn
+    // 128, DT_WBOX for 256); the epilogue writes silu(gate) * up as hi/lo
+    // planes act_hi / act_lo [M][act_ld] (f16 with f16 set, else bf16) at
+    // columns h t..  No split, no argmax; N = 2 x the SwiGLU width, a
+    // multiple of bn.
+    int swiglu;
+    int up_map, up_row;
+    void* act_hi;
+    void* act_lo;
+    int act_ld;
 };
 
 // Host: partial-tile floats a split launch needs, and its ticket count.

@@ -18,6 +18,7 @@
 // count are written as zeros, which keeps every padded GEMM column zero.
 
 #include "kernels_dev.cuh"
+#include "rows_dev.cuh"
 
 namespace dfl {
 
@@ -282,18 +283,6 @@ __global__ void embed_rows_kernel(const int32_t* tokens, int rows, const __nv_bf
         x[(size_t)r * hidden + j] = tok < 0 ? 0.f : __bfloat162float(embed[(size_t)tok * hidden + j]);
 }
 
-__device__ __forceinline__ void store_hilo(void* hi, void* lo, size_t i, float v, int f16 = 0) {
-    if (f16) {
-        const __half h = __float2half_rn(v);
-        reinterpret_cast<__half*>(hi)[i] = h;
-        reinterpret_cast<__half*>(lo)[i] = __float2half_rn(v - __half2float(h));
-        return;
-    }
-    const __nv_bfloat16 h = __float2bfloat16_rn(v);
-    reinterpret_cast<__nv_bfloat16*>(hi)[i] = h;
-    reinterpret_cast<__nv_bfloat16*>(lo)[i] = __float2bfloat16_rn(v - __bfloat162float(h));
-}
-
 // One CTA of 256 threads per row; sum of squares in a fixed order.  A
 // thread holds its (up to 16) elements of the row in registers: all of its
 // loads are issued before the first use, instead of one round trip per
@@ -495,18 +484,6 @@ __global__ void rope_rows_kernel(int pos0, int rows, int half, const double* inv
         rr = fma(-k, 2.4492935982947064e-16, rr);
         cs[e] = (float)cos(rr);
         sn[e] = (float)sin(rr);
-    }
-}
-
-__global__ void swiglu_rows_kernel(const float* y, int rows, int ffn, void* hi, void* lo, int f16) {
-    pdl_trigger();
-    pdl_wait();
-    const long long n = (long long)rows * ffn;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (long long)gridDim.x * blockDim.x) {
-        const long long r = i / ffn, j = i % ffn;
-        const float g = y[r * 2 * ffn + j], u = y[r * 2 * ffn + ffn + j];
-        store_hilo(hi, lo, (size_t)i, g / (1.f + expf(-g)) * u, f16);
     }
 }
 
@@ -800,14 +777,6 @@ int launch_rope_rows(int pos0, int rows, int half, const double* inv_freq, float
     if (blocks > 152 * 8) blocks = 152 * 8;
     return ok(launch_k(rope_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, s, pos0, rows, half, inv_freq,
                        cos_out, sin_out));
-}
-
-int launch_swiglu_rows(const float* y, int rows, int ffn, void* hi, void* lo, int f16, cudaStream_t s) {
-    if (rows < 1) return 0;
-    long long blocks = ((long long)rows * ffn + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    return ok(launch_k(swiglu_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, s, y, rows, ffn, hi, lo,
-                       f16));
 }
 
 int launch_ctx_kv_store(const CtxKvArgs& a, cudaStream_t s) {

@@ -161,9 +161,6 @@ struct QkvRowsArgs {
 };
 int launch_qkv_rows(const QkvRowsArgs& a, cudaStream_t s);
 
-// h = silu(gate) * up from y fp32 [rows][2 ffn] (gate columns, then up), as
-// bf16 hi/lo planes [rows][ffn].
-int launch_swiglu_rows(const float* y, int rows, int ffn, void* hi, void* lo, int f16, cudaStream_t s);
 
 // RoPE table of positions pos0 .. pos0 + rows - 1: cos and sin [rows][half]
 // of pos * inv_freq[i] (angle reduced and evaluated in double, rounded once
