@@ -506,6 +506,7 @@ int dense(dflash_batch* b, const DenseMaps& m, int N, int K, int seg0, int seg1,
     d.amax = amax;
     d.splits = amax ? 1 : splits_for(N, K, b->sms);
     d.part = b->part;
+    d.w_ready = 1;   // the model's weights
     if (view) {
         size_t slab = 0, ldp = 0;
         dense_part_layout(d.M, N, d.bn, &slab, &ldp);
@@ -540,6 +541,7 @@ int dense_swiglu(dflash_batch* b, const DenseMaps& m, int F, int K, cudaStream_t
     d.act_hi = b->ahi;
     d.act_lo = b->alo;
     d.act_ld = F;
+    d.w_ready = 1;
     const int e = launch_dense(m, d, s);
     if (e) return report_error(DFLASH_ERR_CUDA, "dense SwiGLU GEMM (F %d K %d): %s", F, K, cudaGetErrorString((cudaError_t)e));
     return DFLASH_OK;

@@ -1334,6 +1334,7 @@ int ingest_rows(dflash_ctx* c, const DenseMaps& fcm, int x_split, int m_off, int
     fa.y = c->buf<float>(c->L.pf_y);
     fa.ldy = g.hidden;
     fa.err = err;
+    fa.w_ready = 1;   // the model's fc weights
     LAUNCH_TRY(launch_dense(fcm, fa, s));
     CtxRowsArgs ra{};
     ra.y = fa.y;
@@ -1371,6 +1372,7 @@ int ingest_rows(dflash_ctx* c, const DenseMaps& fcm, int x_split, int m_off, int
         ka.y = c->buf<float>(c->L.pf_y);
         ka.ldy = 2 * kvr;
         ka.err = err;
+        ka.w_ready = q4 ? 0 : 1;   // INT4: dequantised into the scratch just before
         LAUNCH_TRY(launch_dense(c->d_kv[l], ka, s));
         const QkvEpi q = qkv_epi(c, c->drf[l], false, l, 0, ROWS_COMMIT);
         CtxKvArgs ca{};
@@ -1458,6 +1460,7 @@ int run_dense_prefill(dflash_ctx* c, const int32_t* tokens, int P, int commit_lo
         d.y = y;
         d.ldy = N;
         d.err = err;
+        d.w_ready = q4 ? 0 : 1;   // INT4: the previous kernel dequantised them into the scratch
         return launch_dense(m, d, s);
     };
     // [W_gate; W_up] with the SwiGLU epilogue at 256-column tiles (128 gate
@@ -1480,6 +1483,7 @@ int run_dense_prefill(dflash_ctx* c, const int32_t* tokens, int P, int commit_lo
         d.act_hi = c->ws + c->L.pp_ahi;
         d.act_lo = c->ws + c->L.pp_alo;
         d.act_ld = g.ffn;
+        d.w_ready = q4 ? 0 : 1;
         return launch_dense(m, d, s);
     };
     for (int p0 = 0; p0 < P; p0 += PF_ROWS) {

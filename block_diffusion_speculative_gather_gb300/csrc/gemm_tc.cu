@@ -107,18 +107,51 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
         tma_prefetch_desc(&maps.x);
         if (SPLIT) tma_prefetch_desc(&maps.x_lo);
         tma_prefetch_desc(&maps.w[seg]);
+        if (a.swiglu) tma_prefetch_desc(&maps.w[a.up_map]);
     }
     if (warp == 1) tc::tmem_alloc(s_tmem, BN);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tm = *s_tmem;
-    pdl_wait();   // x may come from the previous kernel
+
+    // weight tile(s) of k-block kb into its stage's w part
+    auto load_w = [&](int kb, uint8_t* wst, uint64_t* bar) {
+        const int kx = (kb_lo + kb) * DT_BK;
+        if (a.swiglu) {   // BN / 2 gate rows, then the matching BN / 2 up rows
+            constexpr int HB = BN / 2;
+            const int t = n0 / BN;
+            tma_load_2d(wst, &maps.w[0], bar, kx, HB * t);
+            tma_load_2d(wst + HB * 128, &maps.w[a.up_map], bar, kx, a.up_row + HB * t);
+        } else {
+#pragma unroll
+            for (int b = 0; b < BN / DT_WBOX; ++b)
+                tma_load_2d(wst + b * DT_WBOX * 128, &maps.w[seg], bar, kx, wrow + b * DT_WBOX);
+        }
+    };
+    const int pre = nkb < STAGES ? nkb : STAGES;
+    // weights no earlier kernel writes: the first stages' weight tiles go
+    // out before the dependency wait
+    auto first_w = [&]() {
+        for (int kb = 0; kb < pre; ++kb) {
+            mbar_arrive_expect_tx(&full[kb], CFG::STAGE);
+            load_w(kb, ring + kb * CFG::STAGE + (SPLIT ? 2 : 1) * CFG::XB, &full[kb]);
+        }
+    };
+    if (threadIdx.x == 0 && a.w_ready) first_w();
+    pdl_wait();   // x (and without w_ready the weights) may come from the previous kernel
 
     if (threadIdx.x == 0) {   // ---- TMA producer
-        for (int kb = 0; kb < nkb; ++kb) {
+        if (!a.w_ready) first_w();
+        for (int kb = 0; kb < pre; ++kb) {
+            uint8_t* st = ring + kb * CFG::STAGE;
+            const int kx = (kb_lo + kb) * DT_BK;
+            tma_load_2d(st, &maps.x, &full[kb], kx, a.m_off + m0);
+            if (SPLIT) tma_load_2d(st + CFG::XB, &maps.x_lo, &full[kb], kx, a.m_off + m0);
+        }
+        for (int kb = pre; kb < nkb; ++kb) {
             const int s = kb % STAGES;
-            if (kb >= STAGES && !mbar_wait_bounded(&empty[s], (uint32_t)((kb / STAGES - 1) & 1))) {
+            if (!mbar_wait_bounded(&empty[s], (uint32_t)((kb / STAGES - 1) & 1))) {
                 s_fail = 1;
                 dense_error(a.err, 300);
                 break;
@@ -128,17 +161,7 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
             mbar_arrive_expect_tx(&full[s], CFG::STAGE);
             tma_load_2d(st, &maps.x, &full[s], kx, a.m_off + m0);
             if (SPLIT) tma_load_2d(st + CFG::XB, &maps.x_lo, &full[s], kx, a.m_off + m0);
-            uint8_t* wst = st + (SPLIT ? 2 : 1) * CFG::XB;
-            if (a.swiglu) {   // BN / 2 gate rows, then the matching BN / 2 up rows
-                constexpr int HB = BN / 2;
-                const int t = n0 / BN;
-                tma_load_2d(wst, &maps.w[0], &full[s], kx, HB * t);
-                tma_load_2d(wst + HB * 128, &maps.w[a.up_map], &full[s], kx, a.up_row + HB * t);
-            } else {
-#pragma unroll
-                for (int b = 0; b < BN / DT_WBOX; ++b)
-                    tma_load_2d(wst + b * DT_WBOX * 128, &maps.w[seg], &full[s], kx, wrow + b * DT_WBOX);
-            }
+            load_w(kb, st + (SPLIT ? 2 : 1) * CFG::XB, &full[s]);
         }
     } else if (threadIdx.x == 32) {   // ---- MMA issuer
         constexpr uint32_t ID = F16 ? tc::idesc_f16_f32(DT_BM, BN) : tc::idesc_bf16_f32(DT_BM, BN);

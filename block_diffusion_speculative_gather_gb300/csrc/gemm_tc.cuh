@@ -63,6 +63,11 @@ struct DenseArgs {
     // multiple of bn.
     int swiglu;
     int up_map, up_row;
+    // 1: no kernel earlier in the stream writes the weights (the model's own
+    // tensors), so the first stages' weight tiles may be loaded before the
+    // dependency wait; 0 (e.g. a scratch the previous kernel dequantised
+    // into): every load waits
+    int w_ready;
     void* act_hi;
     void* act_lo;
     int act_ld;
