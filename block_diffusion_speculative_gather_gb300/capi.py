@@ -100,7 +100,6 @@ def _load() -> C.CDLL:
         "dflash_linear_workspace_bytes": (sz, [i32, i32]),
         "dflash_linear": (C.c_int, [vp, vp, i32, i32, vp, vp, sz, vp, vp]),
         "dflash_linear_noalloc": (C.c_int, [vp, vp, i32, i32, vp, vp, vp]),
-        "dflash_profile_phases": (i32, [vp, i32, vp, i32]),
         "dflash_progress": (C.c_int, [vp, vp, vp]),
         "dflash_attention_form": (C.c_int, [vp, i32]),
         "dflash_linear_dense": (C.c_int, [vp, vp, vp, i32, i32, i32, vp, vp, vp]),
@@ -129,7 +128,7 @@ EXPORTED = ("dflash_workspace_bytes", "dflash_kv_target_bytes", "dflash_kv_draft
             "dflash_destroy", "dflash_last_error", "dflash_tap_reduce",
             "dflash_quantize_int4g64", "dflash_profile", "dflash_launch_count",
             "dflash_selftest_timeout", "dflash_adopt_kv", "dflash_linear_workspace_bytes",
-            "dflash_linear", "dflash_linear_noalloc", "dflash_profile_phases",
+            "dflash_linear", "dflash_linear_noalloc",
             "dflash_progress", "dflash_attention_form", "dflash_linear_dense",
             "dflash_batch_workspace_bytes", "dflash_batch_init", "dflash_batch_context",
             "dflash_batch_draft", "dflash_batch_verify_accept", "dflash_batch_set_logits_out",
@@ -318,22 +317,6 @@ def dflash_linear_noalloc(w, x, y, err, stream=None):
     _need(err, "err", (torch.int32,), (2,))
     _on_gpu(w=w, x=x, y=y, err=err)
     check(lib.dflash_linear_noalloc(_ptr(w), _ptr(x), n, k, _ptr(y), _ptr(err), _stream(stream)))
-
-
-def dflash_profile_phases(ctx, which: int):
-    """Start times (ns) of every phase of persistent program `which` (0 draft,
-    1 verify, 2 greedy) from its last profiled launch, plus the end time;
-    [] when the program is not in use."""
-    n = lib.dflash_profile_phases(ctx, which, None, 0)
-    if n < 0:
-        check(n)
-    if n == 0:
-        return []
-    buf = (C.c_uint64 * n)()
-    rc = lib.dflash_profile_phases(ctx, which, buf, n)
-    if rc < 0:
-        check(rc)
-    return list(buf)
 
 
 def dflash_progress(ctx, out, stream=None):

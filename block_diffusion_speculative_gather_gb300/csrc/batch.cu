@@ -502,7 +502,10 @@ int dense(dflash_batch* b, const DenseMaps& m, int N, int K, int seg0, int seg1,
     d.y = y;
     d.ldy = N;
     d.err = b->err;
-    d.bn = 128;
+    // 128-column tiles, except the LM head's argmax GEMM (1187 tiles of 128
+    // at Qwen3's vocabulary, nearly 8 waves): 256 halves the tiles and with
+    // them the re-reads of the activation block
+    d.bn = amax ? 256 : 128;
     d.amax = amax;
     d.splits = amax ? 1 : splits_for(N, K, b->sms);
     d.part = b->part;

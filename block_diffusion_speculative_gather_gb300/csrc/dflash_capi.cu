@@ -29,7 +29,6 @@
 #include "common.cuh"
 #include "gemm.cuh"
 #include "kernels.cuh"
-#include "round.cuh"
 #include "capi_internal.cuh"
 
 using namespace dfl;
@@ -77,33 +76,9 @@ int max_chunks(const dflash_config& c) { return cache_cap(c) / ATTN_CHUNK; }
 
 struct Layout {
     size_t state, x, hn, ssq, qrot, attn, act, taps, rcos, rsin, invf, amax, part, slots, counters,
-        acnt, amaps, barc, prog[3], ns[3], pf_x, pf_xlo, pf_y, pf_chi, pf_clo, pf_w, pp_x, pp_y, pp_hi, pp_lo, pp_ahi, pp_alo, pp_q,
+        acnt, pf_x, pf_xlo, pf_y, pf_chi, pf_clo, pf_w, pp_x, pp_y, pp_hi, pp_lo, pp_ahi, pp_alo, pp_q,
         pp_thi, pp_tlo, pf_rope, pp_w, total;
-    int prog_n[3];
 };
-
-enum : int { PROG_DRAFT = 0, PROG_VERIFY = 1, PROG_GREEDY = 2 };
-
-// Whether a program of the persistent round kernel can serve this
-// configuration: bf16 weights in every GEMM it runs, an attention item that
-// fits the kernel's slot.
-bool round_cfg_ok(const dflash_config& g, int which) {
-    if (g.dtype != DFLASH_BF16 || (g.head_dim != 128 && g.head_dim != 64)) return false;
-    if (g.lm_wfmt != 0) return false;   // its GEMM phases are bf16 only
-    if (round_attn_bytes(g.n_q, g.n_kv, g.head_dim) > ROUND_ATTN_BYTES) return false;
-    if (which == PROG_DRAFT) return g.drf_layers > 0 && g.drf_wfmt == DFLASH_BF16;
-    return g.tgt_layers > 0 && g.tgt_wfmt == DFLASH_BF16 &&
-           (g.drf_layers == 0 || g.drf_wfmt == DFLASH_BF16);
-}
-
-// Phases of each program: row preparation, 6 per decoder layer (q/k/v,
-// attention, combine, o, gate/up, down), LM head, acceptance, and for the
-// verify programs the tap commit (fc + one k/v GEMM per draft layer).
-int program_phases(const dflash_config& g, int which) {
-    if (!round_cfg_ok(g, which)) return 0;
-    if (which == PROG_DRAFT) return 3 + 6 * g.drf_layers;
-    return 3 + 6 * g.tgt_layers + (g.drf_layers > 0 ? 1 + g.drf_layers : 0);
-}
 
 constexpr int MAX_SMS = 256 * DFL_GEMM_CTAS_PER_SM;   // GEMM CTAs (split-K slots)
 
@@ -165,8 +140,6 @@ Layout make_layout(const dflash_config& c) {
     L.slots = take((size_t)MAX_SMS * 2 * GEMM_BN * R * 4);
     L.counters = take((size_t)MAX_TILES * 4);
     L.acnt = take((size_t)2 * c.n_kv * 4);
-    L.amaps = take(2 * sizeof(AttnMaps));
-    L.barc = take(256);
     if (dense_ingest_ok(c)) {   // [PF_ROWS] rows: taps bf16, GEMM out fp32, context rows hi/lo bf16
         const size_t kv = (size_t)2 * c.n_kv * c.head_dim;
         L.pf_x = take((size_t)PF_ROWS * c.n_taps * c.hidden * 2);
@@ -203,11 +176,6 @@ Layout make_layout(const dflash_config& c) {
             L.pp_thi = take((size_t)PF_ROWS * c.n_taps * c.hidden * 2);
             L.pp_tlo = take((size_t)PF_ROWS * c.n_taps * c.hidden * 2);
         }
-    }
-    for (int i = 0; i < 3; ++i) {
-        L.prog_n[i] = program_phases(c, i);
-        L.prog[i] = take((size_t)L.prog_n[i] * sizeof(Phase));
-        L.ns[i] = take((size_t)(L.prog_n[i] + 1) * 8);
     }
     L.total = off;
     return L;
@@ -358,15 +326,6 @@ struct dflash_ctx {
     size_t ev_used = 0;
     long long prof_launches = 0;
     double prof_bytes = 0, prof_wbytes = 0;
-    // persistent round programs (draft, verify, greedy), recorded at init
-    struct Program {
-        bool on = false;
-        int n = 0;
-        size_t off = 0, ns_off = 0;       // workspace offsets: phases, phase start times
-        std::vector<double> gemm_bytes;   // per phase: algorithmic GEMM bytes (0: not a GEMM)
-        std::vector<double> gemm_wbytes;
-    } prog[3];
-    int prof_progs = 0;                   // programs launched while profiling (bit mask)
 
     DevState* st() const { return reinterpret_cast<DevState*>(ws + L.state); }
     template <typename T> T* buf(size_t off) const { return reinterpret_cast<T*>(ws + off); }
@@ -468,34 +427,12 @@ cudaError_t record_event(cudaEvent_t e, cudaStream_t s) {
                : cudaEventRecord(e, s);
 }
 
-// Where the pieces of a forward go: launched on a stream, or recorded as
-// the phases of a persistent round program.
+// Where the pieces of a forward are launched.
 struct Emit {
     cudaStream_t s = nullptr;
-    std::vector<Phase>* rec = nullptr;
-    dflash_ctx::Program* prog = nullptr;
-    int logits_slot = CS_NONE;   // recorded LM head: which launch pointer dumps logits
 };
 
-Phase& record(Emit& e, int kind, double gemm_bytes = 0.0, double gemm_wbytes = 0.0) {
-    e.rec->emplace_back();
-    Phase& ph = e.rec->back();
-    memset(&ph, 0, sizeof ph);
-    ph.kind = kind;
-    e.prog->gemm_bytes.push_back(gemm_bytes);
-    e.prog->gemm_wbytes.push_back(gemm_wbytes);
-    return ph;
-}
-
 int run_gemm(dflash_ctx* c, const GemmPlan& p, const GemmArgs& a, Emit& em) {
-    if (em.rec) {
-        Phase& ph = record(em, PH_GEMM, p.abytes, p.wbytes);
-        ph.maps = p.maps;
-        ph.g = a;
-        ph.epi = p.epi;
-        ph.logits_slot = p.epi == EPI_ARGMAX ? em.logits_slot : CS_NONE;
-        return DFLASH_OK;
-    }
     cudaStream_t s = em.s;
     const bool timed = c->prof && c->ev_used + 2 <= c->ev.size();
     if (timed) CUDA_TRY(record_event(c->ev[c->ev_used], s));
@@ -637,7 +574,7 @@ int run_layers(dflash_ctx* c, bool target, Emit& em) {
             am.scale = at.scale;
             am.part = at.part;
             am.st = st;
-            if (!em.rec && c->attn_split_chunks[target ? 0 : 1] > 0) {
+            if (c->attn_split_chunks[target ? 0 : 1] > 0) {
                 AttnFusedArgs fa{};
                 fa.m = am;
                 fa.split_chunks = c->attn_split_chunks[target ? 0 : 1];
@@ -649,19 +586,12 @@ int run_layers(dflash_ctx* c, bool target, Emit& em) {
                 fa.done = fa.arrive + g.n_kv;
                 const int e = launch_attention_fused(target ? c->amap_t : c->amap_d, fa, em.s);
                 if (e) return fail(DFLASH_ERR_CUDA, "attention launch: %s", cudaGetErrorString((cudaError_t)e));
-            } else if (em.rec) {
-                Phase& pa = record(em, PH_ATTN);
-                pa.am = am;
-                pa.target = target ? 1 : 0;
-                Phase& pc = record(em, PH_COMBINE);
-                pc.ac = at;
             } else {
                 const int e = launch_attention_mma(target ? c->amap_t : c->amap_d, am, at.max_chunks, em.s);
                 if (e) return fail(DFLASH_ERR_CUDA, "attention launch: %s", cudaGetErrorString((cudaError_t)e));
                 LAUNCH_TRY(launch_attention_combine(at, em.s));
             }
         } else {
-            if (em.rec) return fail(DFLASH_ERR_CONFIG, "fp32 attention has no persistent form");
             LAUNCH_TRY(launch_attention(at, em.s));
         }
         GemmArgs ao = lp.o.args;
@@ -770,105 +700,6 @@ AcceptArgs accept_args(dflash_ctx* c, int mode) {
     aa.eos_id = g.eos_id;
     aa.st = c->st();
     return aa;
-}
-
-// Records program `which` as phases: the same pieces the per-launch path
-// enqueues, with a grid barrier between consecutive phases.
-int record_program(dflash_ctx* c, int which, std::vector<Phase>& ph) {
-    dflash_ctx::Program& pg = c->prog[which];
-    pg.gemm_bytes.clear();
-    pg.gemm_wbytes.clear();
-    ph.clear();
-    Emit em;
-    em.rec = &ph;
-    em.prog = &pg;
-    int r;
-    if (which == PROG_DRAFT) {
-        record(em, PH_PREP).rows = rows_args(c, FWD_DRAFT);
-        if ((r = run_layers(c, false, em))) return r;
-        em.logits_slot = CS_DRAFT_LOGITS;
-        if ((r = run_lm_head(c, nullptr, em))) return r;
-        record(em, PH_ACCEPT).acc = accept_args(c, FWD_DRAFT);
-    } else {
-        const int mode = which == PROG_VERIFY ? FWD_VERIFY : FWD_GREEDY;
-        Phase& pp = record(em, PH_PREP);
-        pp.rows = rows_args(c, mode);
-        pp.tokens_slot = mode == FWD_VERIFY ? CS_DRAFT_IDS : CS_NONE;
-        if ((r = run_layers(c, true, em))) return r;
-        em.logits_slot = CS_VERIFY_LOGITS;
-        if ((r = run_lm_head(c, nullptr, em))) return r;
-        record(em, PH_ACCEPT).acc = accept_args(c, mode);
-        if (c->cfg.drf_layers > 0 && (r = run_ingest(c, em))) return r;
-    }
-    int bars = 0;
-    for (size_t i = 0; i < ph.size(); ++i) {
-        ph[i].sync_before = i > 0 ? 1 : 0;
-        bars += ph[i].sync_before;
-        ph[i].bars_before = bars;
-    }
-    return DFLASH_OK;
-}
-
-// Records and uploads every program the configuration and the device allow
-// when the persistent schedule is selected (environment DFLASH_PERSISTENT=1
-// at dflash_init; the per-launch schedule is the default).
-int setup_programs(dflash_ctx* c) {
-    const char* env = getenv("DFLASH_PERSISTENT");
-    if (!env || env[0] != '1') return DFLASH_OK;
-    int dev = 0, coop = 0, ctas = 0;
-    CUDA_TRY(cudaGetDevice(&dev));
-    CUDA_TRY(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev));
-    if (!coop) return DFLASH_OK;
-    const int e = round_max_ctas(dev, &ctas);
-    if (e) return fail(DFLASH_ERR_CUDA, "round kernel occupancy: %s", cudaGetErrorString((cudaError_t)e));
-    if (ctas < c->sms) return DFLASH_OK;
-    const AttnMaps am[2] = {c->amap_d, c->amap_t};
-    CUDA_TRY(cudaMemcpy(c->ws + c->L.amaps, am, sizeof am, cudaMemcpyHostToDevice));
-    std::vector<Phase> ph;
-    for (int w = 0; w < 3; ++w) {
-        if (c->L.prog_n[w] == 0) continue;
-        int r = record_program(c, w, ph);
-        if (r) return r;
-        if ((int)ph.size() != c->L.prog_n[w])
-            return fail(DFLASH_ERR_CONFIG, "program %d has %zu phases, %d reserved", w, ph.size(),
-                        c->L.prog_n[w]);
-        CUDA_TRY(cudaMemcpy(c->ws + c->L.prog[w], ph.data(), ph.size() * sizeof(Phase),
-                            cudaMemcpyHostToDevice));
-        dflash_ctx::Program& pg = c->prog[w];
-        pg.n = (int)ph.size();
-        pg.off = c->L.prog[w];
-        pg.ns_off = c->L.ns[w];
-        pg.on = true;
-    }
-    return DFLASH_OK;
-}
-
-// One persistent launch of program `which`.
-int run_program(dflash_ctx* c, int which, const int32_t* draft_ids, int32_t* draft_out,
-                int32_t* tokens_out, int32_t* n_emitted, cudaStream_t s) {
-    const dflash_ctx::Program& pg = c->prog[which];
-    RoundCall rc{};
-    rc.phases = reinterpret_cast<const Phase*>(c->ws + pg.off);
-    rc.n_phases = pg.n;
-    rc.head_dim = c->cfg.head_dim;
-    rc.amaps = reinterpret_cast<const AttnMaps*>(c->ws + c->L.amaps);
-    rc.bar_count = c->buf<unsigned int>(c->L.barc);
-    rc.counters = c->buf<int>(c->L.counters);
-    rc.n_counters = MAX_TILES;
-    rc.st = c->st();
-    rc.draft_ids = draft_ids;
-    rc.draft_out = draft_out;
-    rc.tokens_out = tokens_out;
-    rc.n_emitted = n_emitted;
-    rc.verify_logits = c->verify_logits;
-    rc.draft_logits = c->draft_logits;
-    if (c->prof) {
-        rc.phase_ns = c->buf<unsigned long long>(pg.ns_off);
-        c->prof_progs |= 1 << which;
-    }
-    const int e = launch_round(rc, c->sms, s);
-    if (e) return fail(DFLASH_ERR_CUDA, "round kernel launch: %s", cudaGetErrorString((cudaError_t)e));
-    return DFLASH_OK;
 }
 
 }  // namespace
@@ -1222,10 +1053,6 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
             return fail(DFLASH_ERR_CUDA, "RoPE table: %s", cudaGetErrorString(e));
         }
     }
-    if ((r = setup_programs(c))) {
-        delete c;
-        return r;
-    }
     *out = c;
     return DFLASH_OK;
 }
@@ -1248,7 +1075,6 @@ int dflash_profile(dflash_ctx* c, int32_t mode, dflash_profile_t* out) {
         c->ev_used = 0;
         c->prof_launches = 0;
         c->prof_bytes = c->prof_wbytes = 0;
-        c->prof_progs = 0;
         c->prof = true;
         return DFLASH_OK;
     }
@@ -1260,24 +1086,8 @@ int dflash_profile(dflash_ctx* c, int32_t mode, dflash_profile_t* out) {
         CUDA_TRY(cudaEventElapsedTime(&t, c->ev[i], c->ev[i + 1]));
         ms += t;
     }
-    // persistent programs: GEMM phases timed by the kernel's phase stamps
-    // (start of the phase to start of the next), read after the last launch
-    long long launches = c->prof_launches;
-    double bytes = c->prof_bytes, wbytes = c->prof_wbytes;
-    for (int w = 0; w < 3; ++w) {
-        if (!(c->prof_progs & (1 << w))) continue;
-        const dflash_ctx::Program& pg = c->prog[w];
-        std::vector<unsigned long long> ns(pg.n + 1);
-        CUDA_TRY(cudaDeviceSynchronize());
-        CUDA_TRY(cudaMemcpy(ns.data(), c->ws + pg.ns_off, ns.size() * 8, cudaMemcpyDeviceToHost));
-        for (int i = 0; i < pg.n; ++i) {
-            if (pg.gemm_bytes[i] <= 0) continue;
-            ms += (double)(ns[i + 1] - ns[i]) * 1e-6;
-            launches += 1;
-            bytes += pg.gemm_bytes[i];
-            wbytes += pg.gemm_wbytes[i];
-        }
-    }
+    const long long launches = c->prof_launches;
+    const double bytes = c->prof_bytes, wbytes = c->prof_wbytes;
     if (out) {
         out->gemm_launches = launches;
         out->gemm_ms = ms;
@@ -1285,20 +1095,6 @@ int dflash_profile(dflash_ctx* c, int32_t mode, dflash_profile_t* out) {
         out->gemm_weight_bytes = wbytes;
     }
     return DFLASH_OK;
-}
-
-int32_t dflash_profile_phases(dflash_ctx* c, int32_t which, uint64_t* ns, int32_t cap) {
-    if (!c) return fail(DFLASH_ERR_ARG, "ctx is NULL");
-    if (which < 0 || which > 2) return fail(DFLASH_ERR_ARG, "program %d", which);
-    const dflash_ctx::Program& pg = c->prog[which];
-    if (!pg.on) return 0;
-    const int n = pg.n + 1;
-    if (ns && cap > 0) {
-        CUDA_TRY(cudaDeviceSynchronize());
-        CUDA_TRY(cudaMemcpy(ns, c->ws + pg.ns_off, (size_t)(cap < n ? cap : n) * 8,
-                            cudaMemcpyDeviceToHost));
-    }
-    return n;
 }
 
 int dflash_set_logits_out(dflash_ctx* ctx, float* verify_logits, float* draft_logits) {
@@ -1698,7 +1494,6 @@ int dflash_draft_block(dflash_ctx* c, int32_t* draft_ids, dflash_stream_t stream
     if (!c->prefilled) return fail(DFLASH_ERR_STATE, "draft before prefill");
     if (!draft_ids) return fail(DFLASH_ERR_ARG, "draft_ids is NULL");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (c->prog[PROG_DRAFT].on) return run_program(c, PROG_DRAFT, nullptr, draft_ids, nullptr, nullptr, s);
     Emit em;
     em.s = s;
     LAUNCH_TRY(launch_prepare_rows(rows_args(c, FWD_DRAFT), s));
@@ -1725,8 +1520,6 @@ int dflash_verify_accept(dflash_ctx* c, const int32_t* draft_ids, int32_t* token
     if (int r0 = pending_error()) return r0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int mode = draft_ids ? FWD_VERIFY : FWD_GREEDY;
-    const int prog = draft_ids ? PROG_VERIFY : PROG_GREEDY;
-    if (c->prog[prog].on) return run_program(c, prog, draft_ids, nullptr, tokens_out, n_emitted, s);
     Emit em;
     em.s = s;
     RowsArgs ra = rows_args(c, mode);
@@ -1801,8 +1594,7 @@ int dflash_check(dflash_ctx* c, dflash_stream_t stream) {
 
 int dflash_attention_form(const dflash_ctx* c, int32_t model) {
     if (!c || (model != 0 && model != 1)) return fail(DFLASH_ERR_ARG, "NULL context or model %d", model);
-    const bool persistent = c->prog[model == 0 ? PROG_VERIFY : PROG_DRAFT].on;
-    if (c->cfg.dtype != DFLASH_BF16 || persistent || c->attn_split_chunks[model] <= 0) return 0;
+    if (c->cfg.dtype != DFLASH_BF16 || c->attn_split_chunks[model] <= 0) return 0;
     return c->attn_tc[model] ? 2 : 1;
 }
 

@@ -270,7 +270,8 @@ int dflash_progress(dflash_ctx* ctx, int32_t* out, dflash_stream_t stream);
  * the device: 2 = split-KV on the fifth-generation tensor cores (tcgen05),
  * splits of one 64-key chunk; 1 = split-KV on mma.sync tensor cores, splits
  * of several chunks; 0 = the separate partial and combine kernels (fp32
- * models, the persistent schedule).  Form 2 is opt-in: environment
+ * models, and bf16 ones whose splits do not fit the device at once).  Form
+ * 2 is opt-in: environment
  * DFLASH_ATTN_TC=1 at init (on the 16-row round it measured slower than
  * form 1).  No counterpart in the pages: an implementation choice
  * of this library.  Returns the form, or ARG for a NULL context or a model
@@ -282,17 +283,6 @@ int dflash_attention_form(const dflash_ctx* ctx, int32_t model);
  * an mbarrier nothing arrives on, gives up after limit_ns (<= 2 s) and sets
  * the device error word, so that the next dflash_check returns TIMEOUT. */
 int dflash_selftest_timeout(dflash_ctx* ctx, int64_t limit_ns, dflash_stream_t stream);
-
-/*
- * Profiling helper of the persistent round kernel: the device start times
- * (ns, %globaltimer) of every phase of program `which` (0 draft, 1 verify,
- * 2 greedy one-row step) recorded by its last launch made with profiling on
- * (dflash_profile mode 1), plus the end time: up to `cap` values into ns
- * (host).  Returns the number of values the program has (phases + 1), 0 if
- * the program is not in use, or a negative DFLASH_ERR_*.  Synchronises the
- * device.
- */
-int32_t dflash_profile_phases(dflash_ctx* ctx, int32_t which, uint64_t* ns, int32_t cap);
 
 /*
  * Parity taps: while set (non-NULL), every target LM head (verify, and the
