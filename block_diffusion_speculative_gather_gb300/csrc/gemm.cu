@@ -182,14 +182,16 @@ gemm_skinny_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
                     tma_load_2d(xdst, &maps.x, &full[stage], k * KBLK, 0);
                 }
             };
-            // The weights do not depend on earlier kernels: fill the ring with
-            // them before waiting for the predecessor (programmatic dependent
-            // launch), then add the activation tiles.
+            // The weights do not depend on earlier kernels: the first
+            // DFL_GEMM_PREWAIT stages take them before waiting for the
+            // predecessor (programmatic dependent launch), then their
+            // activation tiles follow.
+            constexpr int PRE = DFL_GEMM_PREWAIT < STAGES ? DFL_GEMM_PREWAIT : STAGES;
             long long pu[STAGES];
             int pl[STAGES];
             int npre = 0;
             long long u = u0;
-            while (u < u1 && npre < STAGES) {
+            while (u < u1 && npre < PRE) {
                 const int len = chunk_len(u);
                 pu[npre] = u;
                 pl[npre] = len;
