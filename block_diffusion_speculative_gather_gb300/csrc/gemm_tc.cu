@@ -34,6 +34,12 @@ namespace dfl {
 
 namespace {
 
+// Ring stages whose weight tiles may go out before the dependency wait
+// (build knob; only for weights no earlier kernel writes).
+#ifndef DFL_DENSE_PREWAIT
+#define DFL_DENSE_PREWAIT 8
+#endif
+
 __device__ __forceinline__ void dense_error(int* err, int site) {
     if (atomicCAS(&err[0], 0, DERR_TIMEOUT) == 0) err[1] = site;
 }
@@ -130,19 +136,20 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
         }
     };
     const int pre = nkb < STAGES ? nkb : STAGES;
-    // weights no earlier kernel writes: the first stages' weight tiles go
-    // out before the dependency wait
-    auto first_w = [&]() {
-        for (int kb = 0; kb < pre; ++kb) {
+    // weights no earlier kernel writes: the first stages' weight tiles (up
+    // to DFL_DENSE_PREWAIT of them) go out before the dependency wait
+    const int pre_w = a.w_ready ? (pre < DFL_DENSE_PREWAIT ? pre : DFL_DENSE_PREWAIT) : 0;
+    auto first_w = [&](int lo, int hi) {
+        for (int kb = lo; kb < hi; ++kb) {
             mbar_arrive_expect_tx(&full[kb], CFG::STAGE);
             load_w(kb, ring + kb * CFG::STAGE + (SPLIT ? 2 : 1) * CFG::XB, &full[kb]);
         }
     };
-    if (threadIdx.x == 0 && a.w_ready) first_w();
+    if (threadIdx.x == 0) first_w(0, pre_w);
     pdl_wait();   // x (and without w_ready the weights) may come from the previous kernel
 
     if (threadIdx.x == 0) {   // ---- TMA producer
-        if (!a.w_ready) first_w();
+        first_w(pre_w, pre);
         for (int kb = 0; kb < pre; ++kb) {
             uint8_t* st = ring + kb * CFG::STAGE;
             const int kx = (kb_lo + kb) * DT_BK;
