@@ -325,6 +325,12 @@ int launch_warps(void (*kern)(KArgs...), long long warps, cudaStream_t s, Args&&
 struct dflash_batch {
     dflash_config cfg;
     int S = 0, R = 0, sms = 0;
+    // tile width of the projections: 128 up to 8 sequences (one row tile),
+    // 256 above, so that two row tiles keep the split GEMMs in one wave; the
+    // k-split counts stay those of 128-column tiles and a tensor-core
+    // output element's sum over k does not depend on the tile width, so a
+    // sequence's results stay the same for every S
+    int bn = 128;
     std::vector<dflash_ctx*> ctx;
     uint8_t* kv_t = nullptr;
     uint8_t* kv_d = nullptr;
@@ -505,7 +511,7 @@ int dense(dflash_batch* b, const DenseMaps& m, int N, int K, int seg0, int seg1,
     // 128-column tiles, except the LM head's argmax GEMM (1187 tiles of 128
     // at Qwen3's vocabulary, nearly 8 waves): 256 halves the tiles and with
     // them the re-reads of the activation block
-    d.bn = amax ? 256 : 128;
+    d.bn = amax ? 256 : b->bn;
     d.amax = amax;
     d.splits = amax ? 1 : splits_for(N, K, b->sms);
     d.part = b->part;
@@ -526,7 +532,7 @@ int dense(dflash_batch* b, const DenseMaps& m, int N, int K, int seg0, int seg1,
 }
 
 // Fused gate/up with the SwiGLU epilogue: silu(gate) * up straight into
-// the down projection's input planes (ahi / alo), 128-column tiles.
+// the down projection's input planes (ahi / alo), at the context's tile width.
 int dense_swiglu(dflash_batch* b, const DenseMaps& m, int F, int K, cudaStream_t s) {
     DenseArgs d{};
     d.M = b->R;
@@ -536,7 +542,7 @@ int dense_swiglu(dflash_batch* b, const DenseMaps& m, int F, int K, cudaStream_t
     d.n_seg1 = 1 << 30;
     d.x_split = 1;
     d.err = b->err;
-    d.bn = 128;
+    d.bn = b->bn;
     d.splits = 1;
     d.swiglu = 1;
     d.up_map = 1;
@@ -720,6 +726,7 @@ int dflash_batch_init(const dflash_config* cfg, const dflash_weights* w, int32_t
     b->S = S;
     b->R = 16 * S;
     b->sms = sm_count();
+    b->bn = (S > 8 && g.hidden % 256 == 0) ? 256 : 128;
     b->kv_t = static_cast<uint8_t*>(kv_target);
     b->kv_d = static_cast<uint8_t*>(kv_draft);
     auto bail = [&](int r) {
@@ -772,8 +779,8 @@ int dflash_batch_init(const dflash_config* cfg, const dflash_weights* w, int32_t
         if (!e) e = dense_maps(&M->o, b->hi, b->lo, R, qd, wo, ro, 1);
         const void* wgu[2] = {lw.w_gate, lw.w_up};
         const int rgu[2] = {F, F};
-        // the SwiGLU form of the dense GEMM at 128-column tiles: 64-row weight boxes
-        if (!e) e = dense_maps(&M->gu, b->hi, b->lo, R, H, wgu, rgu, 2, DT_SWBOX);
+        // the SwiGLU form of the dense GEMM: weight boxes of half a tile
+        if (!e) e = dense_maps(&M->gu, b->hi, b->lo, R, H, wgu, rgu, 2, b->bn == 256 ? DT_WBOX : DT_SWBOX);
         const void* wd[1] = {lw.w_down};
         if (!e) e = dense_maps(&M->down, b->ahi, b->alo, R, F, wd, ro, 1);
         if (!e && draft) {

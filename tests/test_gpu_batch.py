@@ -248,3 +248,30 @@ def test_batch_sequence_independent_of_batch_size(batch):
     assert torch.equal(out[0][2], out[1][2])
     assert torch.equal(out[0][0], out[1][0])
     assert torch.equal(out[0][1], out[1][1])
+
+
+def test_batch_sequence_independent_of_tile_width(batch):
+    """Nine sequences take two row tiles, so the projections run 256-column
+    tiles (one wave of CTAs) where one to eight sequences run 128-column
+    tiles, at the same k-split counts: sequence 0's draft and verify logits
+    must still be bit-identical to its S = 1 run."""
+    from block_diffusion_speculative_gather_gb300.runtime import DFlashBatch
+    prompts = list(batch["prompts"]) + [torch.from_numpy(synth.uniform_ids(24 + 5 * i, W.vocab, seed=70 + i))
+                                        for i in range(6)]
+    budgets = _budgets() + [12] * 6
+    out = []
+    for S in (9, 1):
+        dec = DFlashBatch(W, batch["m"], S=S)
+        dec.prefill(prompts[:S], budgets[:S])
+        vl = torch.zeros((16 * S, W.vocab), dtype=torch.float32, device="cuda")
+        dl = torch.zeros((16 * S, W.vocab), dtype=torch.float32, device="cuda")
+        dec.set_logits_out(vl, dl)
+        d = dec.draft()
+        dec.verify(d)
+        dec.check()
+        dec.set_logits_out(None, None)
+        out.append((dl[:16].clone(), vl[:16].clone(), d[0].clone()))
+        dec.close()
+    assert torch.equal(out[0][2], out[1][2])
+    assert torch.equal(out[0][0], out[1][0])
+    assert torch.equal(out[0][1], out[1][1])
