@@ -377,7 +377,7 @@ int splits_for(int N, int K, int sms) {
     return z > kmax ? (kmax < 1 ? 1 : kmax) : z;
 }
 
-// Attention splits of a model: at most 4 per (kv head, sequence), each of a
+// Attention splits of a model: at most 5 per (kv head, sequence), each of a
 // fixed number of 64-key chunks counted from the first visible chunk (from
 // the cache capacity, or the drafter's window), so a row's split boundaries
 // depend on its position only.
@@ -388,7 +388,7 @@ void attn_splits(const dflash_config& g, bool target, int* chunks, int* splits) 
         const int w = (g.window + DFL_MAX_ROWS + 63) / 64 + 1;
         if (w < maxc) maxc = w;
     }
-    const int q = (maxc + 3) / 4;
+    const int q = (maxc + 4) / 5;
     *chunks = q < 1 ? 1 : q;
     *splits = (maxc + *chunks - 1) / *chunks;
 }

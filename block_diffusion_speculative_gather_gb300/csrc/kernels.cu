@@ -283,32 +283,34 @@ __global__ void embed_rows_kernel(const int32_t* tokens, int rows, const __nv_bf
         x[(size_t)r * hidden + j] = tok < 0 ? 0.f : __bfloat162float(embed[(size_t)tok * hidden + j]);
 }
 
-// One CTA of 256 threads per row; sum of squares in a fixed order.  A
-// thread holds its (up to 16) elements of the row in registers: all of its
-// loads are issued before the first use, instead of one round trip per
-// element (rows wider than 4096 take the plain loop).
-__global__ void resid_norm_kernel(ResidNormArgs a) {
+// One CTA of RN_THREADS threads per row; sum of squares in a fixed order.
+// A thread holds its (up to RN_PER) elements of the row in registers: all
+// of its loads, every split-K slab's included, are issued before the first
+// use, instead of one round trip per element or slab (rows wider than
+// RN_THREADS x RN_PER = 4096 take the plain loop).
+constexpr int RN_THREADS = 512, RN_PER = 8;
+__global__ void __launch_bounds__(RN_THREADS) resid_norm_kernel(ResidNormArgs a) {
     pdl_trigger();
     pdl_wait();
-    constexpr int PER = 16;
+    constexpr int PER = RN_PER, NT = RN_THREADS;
     const int r = blockIdx.x, tid = threadIdx.x;
     float* x = a.x + (size_t)r * a.hidden;
     const float* y = a.y ? a.y + (size_t)r * a.hidden : nullptr;
-    __shared__ float s_part[8];
+    __shared__ float s_part[NT / 32];
     float ss = 0.f;
     float v[PER];
-    const bool held = a.hidden <= 256 * PER;
+    const bool held = a.hidden <= NT * PER;
     if (held) {
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            const int j = tid + 256 * i;
+            const int j = tid + NT * i;
             v[i] = j < a.hidden ? x[j] : 0.f;
         }
         if (y) {
             float w[PER];
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
-                const int j = tid + 256 * i;
+                const int j = tid + NT * i;
                 w[i] = j < a.hidden ? y[j] : 0.f;
             }
             if (a.y_splits > 1) {
@@ -322,7 +324,7 @@ __global__ void resid_norm_kernel(ResidNormArgs a) {
                     for (int z = 1; z < 8; ++z)
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
-                            const int j = tid + 256 * (i0 + i);
+                            const int j = tid + NT * (i0 + i);
                             u[z - 1][i] = (z < a.y_splits && j < a.hidden)
                                               ? __ldcg(y + (size_t)z * a.y_slab + j) : 0.f;
                         }
@@ -335,27 +337,27 @@ __global__ void resid_norm_kernel(ResidNormArgs a) {
                 for (int z = 8; z < a.y_splits; ++z)
 #pragma unroll
                     for (int i = 0; i < PER; ++i) {
-                        const int j = tid + 256 * i;
+                        const int j = tid + NT * i;
                         if (j < a.hidden) w[i] += __ldcg(y + (size_t)z * a.y_slab + j);
                     }
             }
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
-                const int j = tid + 256 * i;
+                const int j = tid + NT * i;
                 v[i] += w[i];
                 if (j < a.hidden) x[j] = v[i];
             }
         }
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            const int j = tid + 256 * i;
+            const int j = tid + NT * i;
             if (j < a.hidden) {
                 if (a.tap_hi) store_hilo(a.tap_hi, a.tap_lo, (size_t)r * a.tap_ld + a.tap_col + j, v[i]);
                 ss = fmaf(v[i], v[i], ss);
             }
         }
     } else {
-        for (int j = tid; j < a.hidden; j += 256) {
+        for (int j = tid; j < a.hidden; j += NT) {
             float u = x[j];
             if (y) {
                 float t = y[j];
@@ -372,16 +374,16 @@ __global__ void resid_norm_kernel(ResidNormArgs a) {
     __syncthreads();
     float tot = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) tot += s_part[w];
+    for (int w = 0; w < NT / 32; ++w) tot += s_part[w];
     const float rstd = 1.0f / sqrtf(tot / (float)a.hidden + a.eps);
     if (held) {
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            const int j = tid + 256 * i;
+            const int j = tid + NT * i;
             if (j < a.hidden) store_hilo(a.hi, a.lo, (size_t)r * a.hidden + j, v[i] * a.w[j] * rstd, a.f16);
         }
     } else {
-        for (int j = tid; j < a.hidden; j += 256)
+        for (int j = tid; j < a.hidden; j += NT)
             store_hilo(a.hi, a.lo, (size_t)r * a.hidden + j, x[j] * a.w[j] * rstd, a.f16);
     }
 }
@@ -761,7 +763,7 @@ int launch_embed_rows(const int32_t* tokens, int rows, const void* embed, int hi
 
 int launch_resid_norm(const ResidNormArgs& a, cudaStream_t s) {
     if (a.rows < 1) return 0;
-    return ok(launch_k(resid_norm_kernel, dim3((unsigned)a.rows), dim3(256), 0, s, a));
+    return ok(launch_k(resid_norm_kernel, dim3((unsigned)a.rows), dim3(RN_THREADS), 0, s, a));
 }
 
 int launch_qkv_rows(const QkvRowsArgs& a, cudaStream_t s) {
