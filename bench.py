@@ -426,11 +426,12 @@ def run_ours(args):
     from block_diffusion_speculative_gather_gb300.runtime import DFlash
 
     rank, world, local = rank_info()
-    # the oracle baseline (N = 1 only): its worker prepares while the GPU runs
+    # the oracle baseline (N = 1 only): its worker prepares while the GPU
+    # workloads run, started after the end-to-end timing (its preparation
+    # loads the host, and the host-driven end-to-end loop lost ~12 % to it)
     cpu_leg = None
-    if not (args.no_cpu_baseline or args.ncu_dense or args.ncu_prefill or args.ncu_rounds
-            or args.ncu_tap or args.ncu_batch or args.layers) and rank == 0 and world == 1:
-        cpu_leg = CpuBaseline()
+    want_cpu = not (args.no_cpu_baseline or args.ncu_dense or args.ncu_prefill or args.ncu_rounds
+                    or args.ncu_tap or args.ncu_batch or args.layers) and rank == 0 and world == 1
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
@@ -663,6 +664,8 @@ def run_ours(args):
 
     if not args.no_e2e:
         result["e2e"] = e2e_measure(dec, w, prompt, world, barrier)
+    if want_cpu:
+        cpu_leg = CpuBaseline()
     del g, gp, gg            # graphs hold event nodes of this context: drop them first
     torch.cuda.synchronize()
     if not args.no_workloads and not args.layers:
