@@ -615,7 +615,6 @@ int batch_layers(dflash_batch* b, bool target, cudaStream_t s) {
         rn.y = yv.y;
         rn.y_splits = yv.splits;
         rn.y_slab = yv.slab;
-        rn.held = 1;
         rn.rows = b->R;
         rn.hidden = H;
         rn.w = lw[l].ln_mlp;
@@ -630,7 +629,6 @@ int batch_layers(dflash_batch* b, bool target, cudaStream_t s) {
         rn.y = yv.y;
         rn.y_splits = yv.splits;
         rn.y_slab = yv.slab;
-        rn.held = 1;
         rn.rows = b->R;
         rn.hidden = H;
         rn.w = l + 1 < nl ? lw[l + 1].ln_attn : (target ? w.final_norm_tgt : w.final_norm_drf);

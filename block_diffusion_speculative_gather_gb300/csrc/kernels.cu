@@ -283,27 +283,23 @@ __global__ void embed_rows_kernel(const int32_t* tokens, int rows, const __nv_bf
         x[(size_t)r * hidden + j] = tok < 0 ? 0.f : __bfloat162float(embed[(size_t)tok * hidden + j]);
 }
 
-// One CTA per row; sum of squares in a fixed order.  In the held form a
-// thread keeps its (up to PER) elements of the row in registers: all of its
-// loads, every split-K slab's included, are issued before the first use,
-// instead of one round trip per element or slab (rows wider than NT x PER
-// take the plain loop).
-// Two forms: NT = 512, PER = 8 (few rows, every row one CTA of the wave:
-// the many-sequence round) and NT = 256, PER = 0 (the plain column loop
-// at a few dozen registers, several CTAs per SM: the many rows of a
-// prefill pass).  The caller picks one per path, never by row count, so a
-// row's result does not depend on how many rows share the launch.
-template <int NT, int PER>
-__global__ void __launch_bounds__(NT) resid_norm_kernel(ResidNormArgs a) {
+// One CTA of RN_THREADS threads per row; sum of squares in a fixed order.
+// A thread holds its (up to RN_PER) elements of the row in registers: all
+// of its loads, every split-K slab's included, are issued before the first
+// use, instead of one round trip per element or slab (rows wider than
+// RN_THREADS x RN_PER = 4096 take the plain loop).
+constexpr int RN_THREADS = 512, RN_PER = 8;
+__global__ void __launch_bounds__(RN_THREADS) resid_norm_kernel(ResidNormArgs a) {
     pdl_trigger();
     pdl_wait();
+    constexpr int PER = RN_PER, NT = RN_THREADS;
     const int r = blockIdx.x, tid = threadIdx.x;
     float* x = a.x + (size_t)r * a.hidden;
     const float* y = a.y ? a.y + (size_t)r * a.hidden : nullptr;
     __shared__ float s_part[NT / 32];
     float ss = 0.f;
-    float v[PER > 0 ? PER : 1];
-    const bool held = PER > 0 && a.hidden <= NT * PER;
+    float v[PER];
+    const bool held = a.hidden <= NT * PER;
     if (held) {
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
@@ -311,7 +307,7 @@ __global__ void __launch_bounds__(NT) resid_norm_kernel(ResidNormArgs a) {
             v[i] = j < a.hidden ? x[j] : 0.f;
         }
         if (y) {
-            float w[PER > 0 ? PER : 1];
+            float w[PER];
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
                 const int j = tid + NT * i;
@@ -767,10 +763,7 @@ int launch_embed_rows(const int32_t* tokens, int rows, const void* embed, int hi
 
 int launch_resid_norm(const ResidNormArgs& a, cudaStream_t s) {
     if (a.rows < 1) return 0;
-    if (a.held)
-        return ok(launch_k(resid_norm_kernel<512, 8>, dim3((unsigned)a.rows), dim3(512), 0, s, a));
-    if (a.y_splits > 1) return (int)cudaErrorInvalidValue;   // slab sums need the held form
-    return ok(launch_k(resid_norm_kernel<256, 0>, dim3((unsigned)a.rows), dim3(256), 0, s, a));
+    return ok(launch_k(resid_norm_kernel, dim3((unsigned)a.rows), dim3(RN_THREADS), 0, s, a));
 }
 
 int launch_qkv_rows(const QkvRowsArgs& a, cudaStream_t s) {

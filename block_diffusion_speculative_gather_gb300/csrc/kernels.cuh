@@ -137,8 +137,6 @@ struct ResidNormArgs {
     long long tap_ld;
     int tap_col;
     int f16;              // 1: hi/lo planes of the norm output are f16 (taps stay bf16)
-    int held;             // 1: 512 threads holding the row in registers (few rows,
-                          // needed for y_splits > 1); 0: 256 threads looping (many rows)
 };
 int launch_resid_norm(const ResidNormArgs& a, cudaStream_t s);
 
