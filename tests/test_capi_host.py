@@ -158,3 +158,18 @@ def test_binding_checks_standalone_operands_before_the_library(capi):
         with pytest.raises(capi.DFlashError) as exc:
             call()
         assert exc.value.code == -3 and word in str(exc.value), (word, str(exc.value))
+
+
+def test_batch_workspace_guard(capi):
+    # many-sequence rounds: 1 <= S <= 32 sequences of a bf16 model
+    from block_diffusion_speculative_gather_gb300.configs import E2E_BF16
+    from block_diffusion_speculative_gather_gb300.runtime import make_config
+    cfg = make_config(E2E_BF16)
+    sizes = [capi.dflash_batch_workspace_bytes(cfg, S) for S in (1, 8, 9, 16, 32)]
+    assert all(b > 0 for b in sizes)
+    assert sizes == sorted(sizes) and len(set(sizes)) == len(sizes)   # grows with S
+    assert capi.dflash_batch_workspace_bytes(cfg, 0) == 0
+    assert capi.dflash_batch_workspace_bytes(cfg, 33) == 0
+    assert capi.dflash_batch_workspace_bytes(make_config(E2E_BF16.with_(tgt_int4=True)), 8) == 0
+    assert capi.dflash_batch_workspace_bytes(make_config(E2E_BF16.with_(drf_int4=True)), 8) == 0
+    assert capi.dflash_batch_workspace_bytes(_cfg(capi), 8) == 0      # fp32 model

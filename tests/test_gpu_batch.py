@@ -275,3 +275,38 @@ def test_batch_sequence_independent_of_tile_width(batch):
     assert torch.equal(out[0][2], out[1][2])
     assert torch.equal(out[0][0], out[1][0])
     assert torch.equal(out[0][1], out[1][1])
+
+
+def test_batch_maximum_sequences(batch):
+    """The largest batch the library takes (32 sequences: four row tiles,
+    the attention over several waves of CTAs, the largest workspace): the
+    first and the last sequence's draft and verify logits are bit-identical
+    to their own S = 1 runs."""
+    from block_diffusion_speculative_gather_gb300 import capi
+    from block_diffusion_speculative_gather_gb300.runtime import DFlashBatch
+    S = 32
+    prompts = [torch.from_numpy(synth.uniform_ids(20 + (7 * i) % 40, W.vocab, seed=200 + i)) for i in range(S)]
+    budgets = [8 + i % 5 for i in range(S)]
+
+    def run(ps, bs):
+        dec = DFlashBatch(W, batch["m"], S=len(ps))
+        dec.prefill(ps, bs)
+        n = len(ps)
+        vl = torch.zeros((16 * n, W.vocab), dtype=torch.float32, device="cuda")
+        dl = torch.zeros((16 * n, W.vocab), dtype=torch.float32, device="cuda")
+        dec.set_logits_out(vl, dl)
+        d = dec.draft()
+        dec.verify(d)
+        dec.check()
+        dec.set_logits_out(None, None)
+        dec.close()
+        return dl, vl, d
+
+    dl, vl, d = run(prompts, budgets)
+    for s in (0, S - 1):
+        dl1, vl1, d1 = run([prompts[s]], [budgets[s]])
+        assert torch.equal(d[s], d1[0]), s
+        assert torch.equal(dl[16 * s:16 * s + 16], dl1[:16]), s
+        assert torch.equal(vl[16 * s:16 * s + 16], vl1[:16]), s
+    with pytest.raises(capi.DFlashError):
+        DFlashBatch(W, batch["m"], S=S + 1)
