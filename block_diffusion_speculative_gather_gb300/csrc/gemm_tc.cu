@@ -365,7 +365,9 @@ size_t dense_smem(bool split) { return split ? DenseCfg<true, DT_BN>::SMEM : Den
 
 int launch_dense(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
     const bool kept = a.splits > 1 && a.keep_parts;
+    // the SwiGLU epilogue stores 8 plane elements (16 bytes) at a time
     if (a.swiglu && ((a.bn != 128 && a.bn != 256) || a.splits > 1 || a.amax || a.N % a.bn || !a.act_hi || !a.act_lo ||
+                     ((reinterpret_cast<uintptr_t>(a.act_hi) | reinterpret_cast<uintptr_t>(a.act_lo)) & 15) ||
                      a.act_ld % 8 || a.act_ld < a.N / 2 || a.up_map < 0 || a.up_map > 2 || a.up_row < 0))
         return (int)cudaErrorInvalidValue;
     if (a.M < 1 || a.N < 1 || a.K < DT_BK || a.K % DT_BK || (a.y && (a.ldy < a.N || a.ldy % 4)) ||
