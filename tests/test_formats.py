@@ -109,3 +109,21 @@ def test_f16_hi_lo_planes_inside_their_range():
     lo = r.astype(np.float16).astype(np.float64)
     err = np.abs(v.astype(np.float64) - hi.astype(np.float64) - lo)
     assert (err <= 2.0 ** -22 * np.abs(v.astype(np.float64)) + 2.0 ** -25).all()
+
+
+def test_int4_code_to_f16_bit_tricks():
+    """The INT4 GEMM turns codes into f16 without conversions: an even
+    nibble u in the low mantissa bits, 0x6400 | u, is the f16 1024 + u, and
+    1024 + u - 1032 = u - 8; an odd nibble left in bits 4..7, 0x6400 | 16 u,
+    is 1024 + 16 u, and (1024 + 16 u) / 16 - 72 = u - 8.  Every step is exact
+    in f16 (so one rounding, as in a fused multiply-add, changes nothing)."""
+    for u in range(16):
+        lo = np.array([0x6400 | u], dtype=np.uint16).view(np.float16)[0]
+        hi = np.array([0x6400 | (u << 4)], dtype=np.uint16).view(np.float16)[0]
+        assert float(lo) == 1024 + u
+        assert float(hi) == 1024 + 16 * u
+        assert np.float16(lo - np.float16(1032)) == u - 8
+        prod = np.float16(hi * np.float16(0.0625))      # exact: a power-of-two scale
+        assert float(prod) == 64 + u
+        assert np.float16(prod + np.float16(-72)) == u - 8
+        assert float(hi) * 0.0625 - 72 == u - 8           # the unrounded fma value
