@@ -334,8 +334,9 @@ const char* dflash_last_error(void);
  * dflash_verify_accept would move it, and its tokens are its own
  * single-sequence decode.  Sequence s owns rows 16 s .. 16 s + 15 of each
  * forward; the 16 S-row GEMMs run on the dense tcgen05 GEMM (bf16 hi/lo
- * activation planes, k-splits chosen from N and K only), so a sequence's
- * results do not depend on S.  bf16 models only (dtype, target, drafter and
+ * activation planes, k-splits chosen from N and K only, 128-column tiles up
+ * to 8 sequences and 256 above, which leaves each output's sum over k
+ * unchanged), so a sequence's results do not depend on S.  bf16 models only (dtype, target, drafter and
  * the tied LM head bf16); head_dim 64 or 128.
  *
  * Memory (caller-owned, device): kv_target holds S consecutive target
