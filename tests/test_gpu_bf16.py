@@ -186,6 +186,31 @@ def test_drafter_alone_ext_taps(qwen):
     dec.close()
 
 
+def test_drafter_window_ext_taps(qwen):
+    """Drafter with a 256-key sliding window over 700 external tap rows: the
+    window opens at key 444, inside chunk 6, so the block attention counts
+    its splits from a first visible chunk above 0 and masks the start of
+    that chunk (the fused split-KV form, checked against the oracle)."""
+    from block_diffusion_speculative_gather_gb300 import capi
+    from block_diffusion_speculative_gather_gb300.runtime import DFlash
+    Wd = W.with_(tgt_layers=0, tap_layers=(0, 8, 17, 26, 35)[:2], window=256, max_seq=1280)
+    dec = DFlash(Wd, qwen["m"])
+    assert capi.dflash_attention_form(dec.ctx, 1) == 1
+    n = 700
+    taps = synth.tap_rows(n, Wd.n_taps * W.hidden, seed=11)
+    ext = taps.view(n, Wd.n_taps, W.hidden).permute(1, 0, 2).contiguous()
+    dl = G.logits_buf(W.vocab)
+    dec.set_logits_out(None, dl)
+    dec.prefill_taps(ext, hc=1, first_token=321, max_new=32)
+    ids = dec.draft().cpu().numpy()
+    dec.check()
+    ref, _ = O.draft_forward(qwen["dw"], qwen["tw"].embed, oracle_config(Wd), taps.float().numpy(), 321,
+                             n, W.block)
+    G.check_rows("bf16_drafter_window", dl[1:W.block].cpu().numpy(), ids[:W.block - 1],
+                 ref[1:], TOL, DEC_TOL)
+    dec.close()
+
+
 @pytest.mark.parametrize("max_seq,chunks", [(256, 1), (1280, 2)], ids=["1chunk", "2chunk"])
 def test_attention_forms_agree(qwen, monkeypatch, max_seq, chunks):
     """The tcgen05 attention (DFLASH_ATTN_TC=1; splits of one chunk for a
