@@ -690,6 +690,7 @@ RowsArgs rows_args(dflash_ctx* c, int mode) {
 }
 
 
+// Arguments of the acceptance kernel common to every forward mode.
 AcceptArgs accept_args(dflash_ctx* c, int mode) {
     const dflash_config& g = c->cfg;
     AcceptArgs aa{};
@@ -1418,15 +1419,9 @@ int dflash_prefill_taps(dflash_ctx* c, const int32_t* prompt_ids, int32_t n_prom
             if ((r = run_layers(c, true, em))) return r;
             if (p0 + T == n_prompt) {
                 if ((r = run_lm_head(c, c->verify_logits, em))) return r;
-                AcceptArgs aa{};
-                aa.mode = FWD_PREFILL;
-                aa.amax = c->buf<unsigned long long>(c->L.amax);
-                aa.block_max = g.block_max;
-                aa.max_seq = g.max_seq;
-                aa.eos_id = g.eos_id;
+                AcceptArgs aa = accept_args(c, FWD_PREFILL);
                 aa.max_new = max_new;
                 aa.prompt_len = n_prompt;
-                aa.st = c->st();
                 LAUNCH_TRY(launch_accept(aa, s));
             }
             if (g.drf_layers > 0 && p0 + T > commit_lo)
@@ -1500,12 +1495,8 @@ int dflash_draft_block(dflash_ctx* c, int32_t* draft_ids, dflash_stream_t stream
     int r = run_layers(c, false, em);
     if (r) return r;
     if ((r = run_lm_head(c, c->draft_logits, em))) return r;
-    AcceptArgs aa{};
-    aa.mode = FWD_DRAFT;
-    aa.amax = c->buf<unsigned long long>(c->L.amax);
+    AcceptArgs aa = accept_args(c, FWD_DRAFT);
     aa.draft_out = draft_ids;
-    aa.block_max = g.block_max;
-    aa.st = c->st();
     LAUNCH_TRY(launch_accept(aa, s));
     return DFLASH_OK;
 }
@@ -1528,16 +1519,10 @@ int dflash_verify_accept(dflash_ctx* c, const int32_t* draft_ids, int32_t* token
     int r = run_layers(c, true, em);
     if (r) return r;
     if ((r = run_lm_head(c, c->verify_logits, em))) return r;
-    AcceptArgs aa{};
-    aa.mode = mode;
-    aa.amax = c->buf<unsigned long long>(c->L.amax);
+    AcceptArgs aa = accept_args(c, mode);
     aa.draft_ids = draft_ids;
     aa.tokens_out = tokens_out;
     aa.n_emitted = n_emitted;
-    aa.block_max = g.block_max;
-    aa.max_seq = g.max_seq;
-    aa.eos_id = g.eos_id;
-    aa.st = c->st();
     LAUNCH_TRY(launch_accept(aa, s));
     if (g.drf_layers > 0)
         if ((r = run_ingest(c, em))) return r;
