@@ -58,7 +58,9 @@ struct BatchRowsArgs {
     const __nv_bfloat16* embed;     // [vocab][hidden]
     const float* w0;                // input-norm weight of the model's first layer
     float eps;
-    const double* inv_freq;         // [head_dim / 2]
+    const float* tab_cos;           // RoPE angles of every cache position [tab_rows][head_dim / 2]
+    const float* tab_sin;
+    int tab_rows;
     float* x;                       // [R][hidden] residual
     void* hi;                       // [R][hidden] bf16: RMSNorm(x) * w0, high part
     void* lo;                       //                  ... and the rounding remainder
@@ -89,7 +91,9 @@ __global__ void __launch_bounds__(256) batch_rows_kernel(BatchRowsArgs b) {
     a.rope_cos = b.rope_cos + (size_t)sq * DFL_MAX_ROWS * half;
     a.rope_sin = b.rope_sin + (size_t)sq * DFL_MAX_ROWS * half;
     a.head_dim = b.head_dim;
-    a.inv_freq = b.inv_freq;
+    a.tab_cos = b.tab_cos;
+    a.tab_sin = b.tab_sin;
+    a.tab_rows = b.tab_rows;
     a.amax = b.amax + (size_t)sq * DFL_MAX_ROWS;
     a.st = b.sts[sq];
     kdev::prepare_row(a, t, tid, 256, sh, BlockBar());
@@ -662,7 +666,7 @@ int batch_rows(dflash_batch* b, int mode, const int32_t* tokens, bool target, cu
     ra.embed = static_cast<const __nv_bfloat16*>(ctx_weights(b->ctx[0]).embed);
     ra.w0 = ctx_layers(b->ctx[0], target)[0].ln_attn;
     ra.eps = g.rms_eps;
-    ra.inv_freq = ctx_inv_freq(b->ctx[0]);
+    rope_table(b->ctx[0], &ra.tab_cos, &ra.tab_sin, &ra.tab_rows);
     ra.x = b->x;
     ra.hi = b->hi;
     ra.lo = b->lo;

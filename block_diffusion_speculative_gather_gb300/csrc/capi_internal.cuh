@@ -10,7 +10,8 @@
 namespace dfl {
 
 DevState* ctx_state(const dflash_ctx* c);               // device round state
-const double* ctx_inv_freq(const dflash_ctx* c);        // device RoPE frequencies [head_dim/2]
+// device RoPE angles of every cache position: cos, sin [rows][head_dim/2]
+void rope_table(const dflash_ctx* c, const float** cos_tab, const float** sin_tab, int* rows);
 const dflash_layer* ctx_layers(const dflash_ctx* c, bool target);   // host copies
 const dflash_weights& ctx_weights(const dflash_ctx* c);
 // 2D tensor map over a row-major [rows][inner] matrix of es-byte elements.

@@ -75,7 +75,7 @@ int max_chunks(const dflash_config& c) { return cache_cap(c) / ATTN_CHUNK; }
 // ------------------------------------------------------------------ layout
 
 struct Layout {
-    size_t state, x, hn, ssq, qrot, attn, act, taps, rcos, rsin, invf, amax, part, slots, counters,
+    size_t state, x, hn, ssq, qrot, attn, act, taps, rcos, rsin, invf, rtab, amax, part, slots, counters,
         acnt, pf_x, pf_xlo, pf_y, pf_chi, pf_clo, pf_w, pp_x, pp_y, pp_hi, pp_lo, pp_ahi, pp_alo, pp_q,
         pp_thi, pp_tlo, pf_rope, pp_w, total;
 };
@@ -135,6 +135,8 @@ Layout make_layout(const dflash_config& c) {
     L.rcos = take(R * (c.head_dim / 2) * 4);
     L.rsin = take(R * (c.head_dim / 2) * 4);
     L.invf = take((c.head_dim / 2) * 8);
+    // RoPE angles of every cache position: cos [cap][head_dim / 2], then sin
+    L.rtab = take((size_t)2 * cache_cap(c) * (c.head_dim / 2) * 4);
     L.amax = take(R * 8);
     L.part = take((size_t)max_chunks(c) * R * c.n_q * (c.head_dim + 2) * 4);
     L.slots = take((size_t)MAX_SMS * 2 * GEMM_BN * R * 4);
@@ -676,7 +678,7 @@ RowsArgs rows_args(dflash_ctx* c, int mode) {
     a.rope_sin = c->buf<float>(c->L.rsin);
     a.head_dim = g.head_dim;
     a.rope_theta = g.rope_theta;
-    a.inv_freq = c->buf<double>(c->L.invf);
+    rope_table(c, &a.tab_cos, &a.tab_sin, &a.tab_rows);
     a.amax = c->buf<unsigned long long>(c->L.amax);
     const bool draft = mode == FWD_DRAFT;
     a.w0 = draft ? (g.drf_layers ? c->drf[0].ln_attn : nullptr)
@@ -728,7 +730,13 @@ int make_linear_maps(GemmMaps* maps, const void* w, const void* x, int n, int k)
 }
 
 DevState* ctx_state(const dflash_ctx* c) { return c->st(); }
-const double* ctx_inv_freq(const dflash_ctx* c) { return c->buf<double>(c->L.invf); }
+
+void rope_table(const dflash_ctx* c, const float** cos_tab, const float** sin_tab, int* rows) {
+    const int cap = cache_cap(c->cfg), half = c->cfg.head_dim / 2;
+    *cos_tab = c->buf<float>(c->L.rtab);
+    *sin_tab = *cos_tab + (size_t)cap * half;
+    *rows = cap;
+}
 const dflash_layer* ctx_layers(const dflash_ctx* c, bool target) {
     return target ? c->tgt.data() : c->drf.data();
 }
@@ -1049,6 +1057,15 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
         for (int i = 0; i < g.head_dim / 2; ++i)
             invf[i] = pow((double)g.rope_theta, -2.0 * (double)i / (double)g.head_dim);
         e = cudaMemcpy(c->ws + L.invf, invf.data(), invf.size() * 8, cudaMemcpyHostToDevice);
+        // the angles of every position, once: the forwards copy their rows
+        // from this table instead of evaluating cos / sin in double (slow
+        // on this part) every time
+        const int half = g.head_dim / 2, cap = cache_cap(g);
+        float* tab = c->buf<float>(L.rtab);
+        if (e == cudaSuccess)
+            e = (cudaError_t)launch_rope_rows(0, cap, half, c->buf<double>(L.invf), tab,
+                                              tab + (size_t)cap * half, nullptr);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
         if (e != cudaSuccess) {
             delete c;
             return fail(DFLASH_ERR_CUDA, "RoPE table: %s", cudaGetErrorString(e));
@@ -1116,6 +1133,26 @@ namespace {
 // one type for both operands).
 // fc over R context rows already in place (x rows m_off .. m_off + R - 1 of
 // fc's maps), then the context norm, K/V and cache rows at pos0 ...
+// RoPE angles of rows pos0 .. pos0 + R - 1 of a dense pass: the rows of the
+// position table, or (rows past it) the pass's own buffer filled now.
+int pass_rope(dflash_ctx* c, int pos0, int R, const float** rcos, const float** rsin, cudaStream_t s) {
+    const float *tc, *ts;
+    int rows;
+    rope_table(c, &tc, &ts, &rows);
+    const int half = c->cfg.head_dim / 2;
+    if (pos0 >= 0 && pos0 + R <= rows) {
+        *rcos = tc + (size_t)pos0 * half;
+        *rsin = ts + (size_t)pos0 * half;
+        return DFLASH_OK;
+    }
+    float* bc = c->buf<float>(c->L.pf_rope);
+    float* bs = bc + (size_t)PF_ROWS * half;
+    LAUNCH_TRY(launch_rope_rows(pos0, R, half, c->buf<double>(c->L.invf), bc, bs, s));
+    *rcos = bc;
+    *rsin = bs;
+    return DFLASH_OK;
+}
+
 int ingest_rows(dflash_ctx* c, const DenseMaps& fcm, int x_split, int m_off, int R, int pos0, cudaStream_t s) {
     const dflash_config& g = c->cfg;
     const int kvr = g.n_kv * g.head_dim;
@@ -1145,9 +1182,8 @@ int ingest_rows(dflash_ctx* c, const DenseMaps& fcm, int x_split, int m_off, int
     const bool q4 = g.drf_wfmt == DFLASH_INT4G64;
     ra.f16 = q4 ? 1 : 0;
     LAUNCH_TRY(launch_ctx_rows(ra, s));
-    float* rcos = c->buf<float>(c->L.pf_rope);
-    float* rsin = rcos + (size_t)PF_ROWS * (g.head_dim / 2);
-    LAUNCH_TRY(launch_rope_rows(pos0, R, g.head_dim / 2, c->buf<double>(c->L.invf), rcos, rsin, s));
+    const float *rcos, *rsin;
+    if (int e = pass_rope(c, pos0, R, &rcos, &rsin, s)) return e;
     for (int l = 0; l < g.drf_layers; ++l) {
         if (q4) {   // this layer's W_k and W_v, dequantised (exactly) to f16
             uint8_t* wq = c->ws + c->L.pf_w;
@@ -1286,9 +1322,8 @@ int run_dense_prefill(dflash_ctx* c, const int32_t* tokens, int P, int commit_lo
     for (int p0 = 0; p0 < P; p0 += PF_ROWS) {
         const int R = P - p0 < PF_ROWS ? P - p0 : PF_ROWS;
         LAUNCH_TRY(launch_embed_rows(tokens + p0, R, c->w.embed, g.hidden, g.vocab, x, c->st(), s));
-        float* rcos = c->buf<float>(c->L.pf_rope);
-        float* rsin = rcos + (size_t)PF_ROWS * (g.head_dim / 2);
-        LAUNCH_TRY(launch_rope_rows(p0, R, g.head_dim / 2, c->buf<double>(c->L.invf), rcos, rsin, s));
+        const float *rcos, *rsin;
+        if (int e = pass_rope(c, p0, R, &rcos, &rsin, s)) return e;
         for (int l = 0; l <= g.tgt_layers; ++l) {
             // residual of layer l - 1's down projection, then layer l's input norm
             // (after the last layer: the final norm, whose rows nothing reads)

@@ -17,11 +17,13 @@ struct RowsArgs {
     const void* embed;           // [vocab][hidden] (dtype)
     int embed_f32;               // 1 = fp32 embedding, 0 = bf16
     float* x;                    // fp32 [16][hidden]
-    float* rope_cos;             // [16][head_dim/2]
-    float* rope_sin;
+    float* rope_cos;             // [16][head_dim/2]: the forward rows' angles, copied from
+    float* rope_sin;             //   the position table below
     int head_dim;
     float rope_theta;
-    const double* inv_freq;      // [head_dim/2] theta^(-2i/head_dim)
+    const float* tab_cos;        // [tab_rows][head_dim/2] cos of every cache position
+    const float* tab_sin;        // [tab_rows][head_dim/2] sin
+    int tab_rows;
     unsigned long long* amax;    // [16] reset to 0
     // folded input norm of the first layer: xn = x * w0 and partial sums of x^2
     const float* w0;             // [hidden] ln_attn of layer 0 of the model that runs

@@ -90,17 +90,15 @@ __device__ __forceinline__ void prepare_row(const RowsArgs& a, int t, int tid, i
             if (lane == 0) a.ssq[b * DFL_MAX_ROWS + t] = ss;
         }
     }
-    const int half = a.head_dim / 2;
+    // the row's RoPE angles from the position table (made once at init by
+    // rope_rows_kernel: pos * theta^(-2i/d) in double, reduced with a
+    // two-part 2 pi, cos / sin in double, rounded once to fp32); a row past
+    // the table (never one the forward uses) gets the identity rotation
+    const int half = a.head_dim / 2, pos = sh[1] + t;
+    const bool in_tab = pos >= 0 && pos < a.tab_rows;
     for (int i = tid; i < half; i += nthr) {
-        // angle = pos * theta^(-2i/d) in double (the frequencies come from a
-        // table made on the host), reduced to [-pi, pi] with a two-part 2 pi,
-        // then cos / sin in double, rounded once to fp32
-        const double ang = (double)(sh[1] + t) * a.inv_freq[i];
-        const double k = rint(ang * 0.15915494309189535);          // 1 / (2 pi)
-        double r = fma(-k, 6.283185307179586, ang);                // 2 pi, high part
-        r = fma(-k, 2.4492935982947064e-16, r);                    // 2 pi, low part
-        a.rope_cos[t * half + i] = (float)cos(r);
-        a.rope_sin[t * half + i] = (float)sin(r);
+        a.rope_cos[t * half + i] = in_tab ? a.tab_cos[(size_t)pos * half + i] : 1.f;
+        a.rope_sin[t * half + i] = in_tab ? a.tab_sin[(size_t)pos * half + i] : 0.f;
     }
 }
 
