@@ -1218,7 +1218,6 @@ int ingest_rows(dflash_ctx* c, const DenseMaps& fcm, int x_split, int m_off, int
         ca.max_seq = g.max_seq;
         ca.k_norm = c->drf[l].k_norm;
         ca.eps = g.rms_eps;
-        ca.inv_freq = c->buf<double>(c->L.invf);
         ca.rope_cos = rcos;
         ca.rope_sin = rsin;
         ca.k_cache = q.k_cache;
@@ -1367,7 +1366,6 @@ int run_dense_prefill(dflash_ctx* c, const int32_t* tokens, int P, int commit_lo
             qa.q_norm = c->tgt[l].q_norm;
             qa.k_norm = c->tgt[l].k_norm;
             qa.eps = g.rms_eps;
-            qa.inv_freq = c->buf<double>(c->L.invf);
             qa.rope_cos = rcos;
             qa.rope_sin = rsin;
             qa.q_out = c->ws + c->L.pp_q;

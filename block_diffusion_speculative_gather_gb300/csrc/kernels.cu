@@ -419,17 +419,8 @@ __global__ void qkv_rows_kernel(QkvRowsArgs a) {
             cs[m] = 1.f;
             sn[m] = 0.f;
             if (m < per / 2) {
-                if (a.rope_cos) {
-                    cs[m] = a.rope_cos[(size_t)r * (hd / 2) + lane + 32 * m];
-                    sn[m] = a.rope_sin[(size_t)r * (hd / 2) + lane + 32 * m];
-                } else {
-                    const double ang = (double)pos * a.inv_freq[lane + 32 * m];
-                    const double k = rint(ang * 0.15915494309189535);
-                    double rr = fma(-k, 6.283185307179586, ang);
-                    rr = fma(-k, 2.4492935982947064e-16, rr);
-                    cs[m] = (float)cos(rr);
-                    sn[m] = (float)sin(rr);
-                }
+                cs[m] = a.rope_cos[(size_t)r * (hd / 2) + lane + 32 * m];
+                sn[m] = a.rope_sin[(size_t)r * (hd / 2) + lane + 32 * m];
             }
         }
         float o[4];
@@ -546,17 +537,8 @@ __global__ void ctx_kv_store_kernel(CtxKvArgs a) {
             cs[m] = 1.f;
             sn[m] = 0.f;
             if (m < per / 2) {
-                if (a.rope_cos) {
-                    cs[m] = a.rope_cos[(size_t)r * (hd / 2) + lane + 32 * m];
-                    sn[m] = a.rope_sin[(size_t)r * (hd / 2) + lane + 32 * m];
-                } else {
-                    const double ang = (double)pos * a.inv_freq[lane + 32 * m];
-                    const double k = rint(ang * 0.15915494309189535);
-                    double rr = fma(-k, 6.283185307179586, ang);
-                    rr = fma(-k, 2.4492935982947064e-16, rr);
-                    cs[m] = (float)cos(rr);
-                    sn[m] = (float)sin(rr);
-                }
+                cs[m] = a.rope_cos[(size_t)r * (hd / 2) + lane + 32 * m];
+                sn[m] = a.rope_sin[(size_t)r * (hd / 2) + lane + 32 * m];
             }
         }
         float o[4];

@@ -152,8 +152,7 @@ struct QkvRowsArgs {
     const float* q_norm;
     const float* k_norm;
     float eps;
-    const double* inv_freq;
-    const float* rope_cos;  // [rows][head_dim / 2] table, or NULL: from inv_freq
+    const float* rope_cos;  // [rows][head_dim / 2]: the rows of the RoPE position table
     const float* rope_sin;
     void* q_out;
     void* k_cache;
@@ -166,7 +165,8 @@ int launch_qkv_rows(const QkvRowsArgs& a, cudaStream_t s);
 
 // RoPE table of positions pos0 .. pos0 + rows - 1: cos and sin [rows][half]
 // of pos * inv_freq[i] (angle reduced and evaluated in double, rounded once
-// to fp32: the round's table), for the many-row kernels above.
+// to fp32): the position table made at init, and a dense pass's rows past
+// it.
 int launch_rope_rows(int pos0, int rows, int half, const double* inv_freq, float* cos_out, float* sin_out,
                      cudaStream_t s);
 
@@ -185,8 +185,7 @@ struct CtxKvArgs {
     int rows, pos0, n_kv, head_dim, cap, max_seq;
     const float* k_norm;    // [head_dim]
     float eps;
-    const double* inv_freq; // [head_dim / 2]
-    const float* rope_cos;  // [rows][head_dim / 2] table (launch_rope_rows), or NULL: from inv_freq
+    const float* rope_cos;  // [rows][head_dim / 2]: the rows of the RoPE position table
     const float* rope_sin;
     void* k_cache;
     void* v_cache;
