@@ -1437,9 +1437,29 @@ int dflash_prefill_taps(dflash_ctx* c, const int32_t* prompt_ids, int32_t n_prom
         if (n_prompt + 1 > g.max_seq) return fail(DFLASH_ERR_CAPACITY, "prompt of %d exceeds max_seq %d", n_prompt, g.max_seq);
         const int commit_lo = g.window > 0 ? (n_prompt > g.window ? n_prompt - g.window : 0) : 0;
         int p_first = 0;
-        if (c->dense_prefill && n_prompt > DFL_MAX_ROWS) {   // rows before the last chunk, dense
-            p_first = (n_prompt - 1) / DFL_MAX_ROWS * DFL_MAX_ROWS;
-            if ((r = run_dense_prefill(c, prompt_ids, p_first, commit_lo, s))) return r;
+        if (c->dense_prefill && n_prompt > DFL_MAX_ROWS) {
+            // every row through the dense forward (its passes also commit
+            // the taps to the drafter's context); the last chunk's residual
+            // rows then take the final norm into the round's LM head, which
+            // gives the first token, and the acceptance sets the round state
+            if ((r = run_dense_prefill(c, prompt_ids, n_prompt, commit_lo, s))) return r;
+            const int p0 = (n_prompt - 1) / DFL_MAX_ROWS * DFL_MAX_ROWS, T = n_prompt - p0;
+            const int pass0 = (n_prompt - 1) / PF_ROWS * PF_ROWS;   // first row of the last pass
+            RowsArgs ra = rows_args(c, FWD_PREFILL);
+            ra.pos0 = p0;
+            ra.T = T;
+            ra.tokens = prompt_ids;
+            ra.embed = nullptr;
+            ra.x_src = c->buf<float>(c->L.pp_x) + (size_t)(p0 - pass0) * g.hidden;
+            ra.w0 = c->w.final_norm_tgt;
+            ra.xn_type = c->xt_lm();   // the LM head's input, as the last layer writes it
+            LAUNCH_TRY(launch_prepare_rows(ra, s));
+            if ((r = run_lm_head(c, c->verify_logits, em))) return r;
+            AcceptArgs aa = accept_args(c, FWD_PREFILL);
+            aa.max_new = max_new;
+            aa.prompt_len = n_prompt;
+            LAUNCH_TRY(launch_accept(aa, s));
+            p_first = n_prompt;
         }
         for (int p0 = p_first; p0 < n_prompt; p0 += DFL_MAX_ROWS) {
             const int T = n_prompt - p0 < DFL_MAX_ROWS ? n_prompt - p0 : DFL_MAX_ROWS;

@@ -16,6 +16,8 @@ struct RowsArgs {
     const int32_t* tokens;       // PREFILL: prompt; VERIFY: draft ids; else unused
     const void* embed;           // [vocab][hidden] (dtype)
     int embed_f32;               // 1 = fp32 embedding, 0 = bf16
+    const float* x_src;          // instead of embed: the rows' residual [T][hidden] fp32
+                                 // (a dense prefill's last rows, for the final norm)
     float* x;                    // fp32 [16][hidden]
     float* rope_cos;             // [16][head_dim/2]: the forward rows' angles, copied from
     float* rope_sin;             //   the position table below

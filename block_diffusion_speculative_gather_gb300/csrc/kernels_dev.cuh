@@ -70,11 +70,14 @@ __device__ __forceinline__ void prepare_row(const RowsArgs& a, int t, int tid, i
             xr[i] = a.embed_f32 ? reinterpret_cast<const float*>(a.embed)[e]
                                 : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.embed)[e]);
         }
-    } else if (a.embed) {
+    } else if (t < T && a.x_src) {
+        for (int i = tid; i < a.hidden; i += nthr) xr[i] = a.x_src[(size_t)t * a.hidden + i];
+    } else if (a.embed || a.x_src) {
         for (int i = tid; i < a.hidden; i += nthr) xr[i] = 0.f;
     }
-    if (a.embed) {
-        // folded RMSNorm input of layer 0: xn = x * w0, per-128-column sums of x^2
+    if (a.embed || a.x_src) {
+        // folded RMSNorm input of the next matrix (layer 0's, or with x_src
+        // the final norm's): xn = x * w0, per-128-column sums of x^2
         bar();
         for (int i = tid; i < a.hidden; i += nthr)
             store_act(a.xn, a.xn_type, a.hidden, t, i, xr[i] * a.w0[i]);

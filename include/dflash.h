@@ -185,11 +185,11 @@ int dflash_init(const dflash_config* cfg /*host*/, const dflash_weights* w /*hos
  *   context window are fc-projected into the draft context ("feat: DFlash2
  *   ...": prefill stages the prompt's trailing window of tap rows), the
  *   argmax of the last row is the first generated token.  With a bf16 or
- *   INT4 target every row before the prompt's last 16-row chunk runs as a
- *   dense forward (tcgen05 GEMMs over up to 1024 rows at a time; INT4
- *   matrices dequantised exactly to f16 layer by layer; environment
- *   DFLASH_DENSE_PREFILL=0 at dflash_init runs 16-row chunks instead); the
- *   last chunk runs the round's 16-row forward.
+ *   INT4 target every prompt row runs as a dense forward (tcgen05 GEMMs
+ *   over up to 1024 rows at a time; INT4 matrices dequantised exactly to
+ *   f16 layer by layer; environment DFLASH_DENSE_PREFILL=0 at dflash_init
+ *   runs 16-row chunks instead), and the rows of the last 16-row chunk go
+ *   through the final norm into the round's LM head.
  * Drafter-alone mode (tgt_layers == 0): ext_taps holds n_ext tap rows as
  *   dtype [n_taps][n_ext][hc*hidden] (hc streams per tap layer, reduced by
  *   their mean); rows are positions 0..n_ext-1 and first_token is the pending
@@ -466,7 +466,7 @@ int dflash_linear_noalloc(const void* w, const void* x, int32_t n, int32_t k, fl
  * re-projection of the window's tap rows and each draft layer's context
  * K/V, "[RFC] DFlash", "Requested changes" 3, the persistent draft KV
  * cache) and the target's prompt prefill (every projection of the prompt
- * rows before the last 16-row chunk).  The binding checks dtypes, shapes
+ * rows).  The binding checks dtypes, shapes
  * and devices before the call.  Errors: ARG, CUDA.
  */
 int dflash_linear_dense(const void* w, const void* x, const void* x_lo, int32_t m, int32_t n, int32_t k,

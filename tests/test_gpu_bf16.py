@@ -320,12 +320,13 @@ def test_dense_ingest_hc4_matches_chunked_and_oracle(qwen, monkeypatch):
 
 def test_dense_prefill_matches_chunked_and_oracle(qwen, monkeypatch):
     """The dense prompt prefill of the bf16 target (default: every prompt row
-    before the last 16-row chunk through the dense tcgen05 GEMM and the
-    many-row causal attention, 1024 rows per pass) against 16-row forwards
-    (DFLASH_DENSE_PREFILL=0) on an 1100-token prompt (two passes, 1024 + 64
-    rows, then the last 12-row chunk): target and draft cache rows agree to
-    fp16 rounding, the last chunk's logits within the parity tolerance of
-    each other and of the oracle."""
+    through the dense tcgen05 GEMM and the many-row causal attention, 1024
+    rows per pass, then the last chunk's rows through the final norm into
+    the round's LM head) against 16-row forwards (DFLASH_DENSE_PREFILL=0)
+    on an 1100-token prompt (two passes, 1024 + 76 rows; a last chunk of
+    12 rows): target and draft cache rows agree to fp16 rounding, the last
+    chunk's logits within the parity tolerance of each other and of the
+    oracle."""
     from block_diffusion_speculative_gather_gb300.runtime import DFlash
     Wp = W.with_(max_seq=1280)
     P = 1100
@@ -361,11 +362,13 @@ def test_dense_prefill_matches_chunked_and_oracle(qwen, monkeypatch):
         assert tn_d == int(np.argmax(ref[P - 1]))
 
 
-@pytest.mark.parametrize("P", [17, 1040], ids=["one-block", "one-full-pass"])
+@pytest.mark.parametrize("P", [17, 1024, 1025, 1040],
+                         ids=["ragged-pass", "one-full-pass", "one-row-second-pass", "16-row-second-pass"])
 def test_dense_prefill_edges(qwen, monkeypatch, P):
-    """Dense prefill at its edges: 17 tokens (one 16-row dense block before a
-    1-row last chunk) and 1040 (exactly one full 1024-row pass): the last
-    chunk's logits and the first token match the 16-row forwards."""
+    """Dense prefill at its edges: 17 tokens (one 17-row pass, a last chunk
+    of one row), 1024 (exactly one full pass), 1025 (a second pass of one
+    row) and 1040 (a second pass of 16): the last chunk's logits and the
+    first token match the 16-row forwards."""
     from block_diffusion_speculative_gather_gb300.runtime import DFlash
     Wp = W.with_(max_seq=1280)
     prompt = torch.from_numpy(synth.uniform_ids(P, W.vocab, seed=13))
@@ -390,11 +393,11 @@ def test_dense_prefill_edges(qwen, monkeypatch, P):
 @pytest.mark.parametrize("int4", [False, True], ids=["bf16-drafter", "int4-drafter"])
 def test_dense_prefill_window_commit(qwen, monkeypatch, int4):
     """Dense prefill with a drafter window of 64 positions on a 300-token
-    prompt: only rows 236..299 enter the draft context — rows 236..287 from
-    the middle of the dense pass (the fc reads the tap rows from row 236 on),
-    288..299 from the last 16-row chunk.  Draft cache rows match the 16-row
-    forwards to fp16 rounding, rows before the window stay untouched, and
-    the first draft after the prefill gives the same logits."""
+    prompt: only rows 236..299 enter the draft context, from the middle of
+    the dense pass to its end (the fc reads the tap rows from row 236 on).
+    Draft cache rows match the 16-row forwards to fp16 rounding, rows before
+    the window stay untouched, and the first draft after the prefill gives
+    the same logits."""
     from block_diffusion_speculative_gather_gb300.runtime import DFlash
     Wp = W.with_(max_seq=512, window=64, drf_int4=int4)
     P, lo = 300, 300 - 64
