@@ -616,7 +616,10 @@ prefill_attn_kernel(const __grid_constant__ PrefillMaps maps, const PrefillAttnA
 
     pdl_trigger();
     pdl_wait();
-    const int kh = blockIdx.x, z = blockIdx.y, tid = threadIdx.x;
+    // row blocks in decreasing order: under the causal mask block z folds
+    // about z / 4 + 1 chunks, and the blocks that start first should be
+    // the longest ones, so that the short ones fill the tail of the launch
+    const int kh = blockIdx.x, z = gridDim.y - 1 - blockIdx.y, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int T = min(16, p.rows - 16 * z);
     if (T <= 0) return;
