@@ -72,10 +72,19 @@ int cache_cap(const dflash_config& c) { return (c.max_seq + 63) / 64 * 64; }
 
 int max_chunks(const dflash_config& c) { return cache_cap(c) / ATTN_CHUNK; }
 
+// The tap commit projects the committed context rows for every draft layer
+// in one GEMM over a copy of the layers' [W_k; W_v] (bf16 drafters of more
+// than one layer whose [W_k; W_v] fills whole 128-row tiles).
+bool ctxkv_grouped(const dflash_config& c) {
+    return c.dtype == DFLASH_BF16 && c.drf_wfmt != DFLASH_INT4G64 && c.drf_layers > 1 &&
+           (2 * c.n_kv * c.head_dim) % GEMM_BN == 0 && GEMM_BN % c.head_dim == 0;
+}
+
 // ------------------------------------------------------------------ layout
 
 struct Layout {
-    size_t state, x, hn, ssq, qrot, attn, act, taps, rcos, rsin, invf, rtab, amax, part, slots, counters,
+    size_t state, x, hn, ssq, qrot, attn, act, taps, rcos, rsin, invf, rtab, ctxkv_w, ctxkv_kn, amax, part,
+        slots, counters,
         acnt, pf_x, pf_xlo, pf_y, pf_chi, pf_clo, pf_w, pp_x, pp_y, pp_hi, pp_lo, pp_ahi, pp_alo, pp_q,
         pp_thi, pp_tlo, pf_rope, pp_w, total;
 };
@@ -137,6 +146,10 @@ Layout make_layout(const dflash_config& c) {
     L.invf = take((c.head_dim / 2) * 8);
     // RoPE angles of every cache position: cos [cap][head_dim / 2], then sin
     L.rtab = take((size_t)2 * cache_cap(c) * (c.head_dim / 2) * 4);
+    if (ctxkv_grouped(c)) {   // every draft layer's [W_k; W_v] and k-norm, one after another
+        L.ctxkv_w = take((size_t)c.drf_layers * 2 * c.n_kv * c.head_dim * c.hidden * 2);
+        L.ctxkv_kn = take((size_t)c.drf_layers * c.head_dim * 4);
+    }
     L.amax = take(R * 8);
     L.part = take((size_t)max_chunks(c) * R * c.n_q * (c.head_dim + 2) * 4);
     L.slots = take((size_t)MAX_SMS * 2 * GEMM_BN * R * 4);
@@ -304,6 +317,8 @@ struct dflash_ctx {
     int sms;
     std::vector<LayerPlans> tplan, dplan;
     GemmPlan lm, fc;
+    GemmPlan ctxkv_all;   // every draft layer's context K/V in one GEMM (when grouped)
+    bool ctxkv_group = false;
     AttnMaps amap_t{}, amap_d{};   // tensor-core attention maps (fp16 q and caches)
     // fused attention per model (0 target, 1 drafter): chunks per split and
     // splits of a launch (0: two-kernel form)
@@ -644,6 +659,15 @@ int run_ingest(dflash_ctx* c, Emit& em) {
     set_norm_out(c, a, g.ctx_norm ? c->w.ctx_norm : nullptr, g.ctx_norm != 0, c->xt_model(false));
     int r = run_gemm(c, c->fc, a, em);
     if (r) return r;
+    if (c->ctxkv_group) {
+        a = c->ctxkv_all.args;
+        set_norm_in(c, a, g.ctx_norm != 0);
+        a.qkv = qkv_epi(c, c->drf[0], false, 0, 0, ROWS_COMMIT);
+        a.qkv.group = g.drf_layers;
+        a.qkv.cache_stride = (long long)c->cache_layer_stride();
+        a.qkv.k_norm_all = c->buf<float>(c->L.ctxkv_kn);
+        return run_gemm(c, c->ctxkv_all, a, em);
+    }
     for (int l = 0; l < g.drf_layers; ++l) {
         const LayerPlans& lp = c->dplan[l];
         a = lp.ctxkv.args;
@@ -880,6 +904,28 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
         const int rfc[1] = {g.hidden};
         r = plan_gemm(c, &c->fc, c->wf(g.dtype), EPI_NORMOUT, wfc, rfc, 1, g.n_taps * g.hidden,
                       c->ws + L.taps, c->act_xt());
+    }
+    if (!r && ctxkv_grouped(g)) {
+        // the draft layers' [W_k; W_v] and k-norm weights copied one after
+        // another: the tap commit streams them in one launch (the drafter's
+        // own q/k/v GEMMs keep reading the caller's weights)
+        const size_t kvw = (size_t)g.n_kv * g.head_dim * g.hidden;   // elements of W_k (and W_v)
+        uint8_t* dst = c->ws + L.ctxkv_w;
+        for (int l = 0; l < g.drf_layers && !r; ++l) {
+            cudaError_t e = cudaMemcpy(dst + (2 * l) * kvw * 2, c->drf[l].wk, kvw * 2, cudaMemcpyDeviceToDevice);
+            if (e == cudaSuccess)
+                e = cudaMemcpy(dst + (2 * l + 1) * kvw * 2, c->drf[l].wv, kvw * 2, cudaMemcpyDeviceToDevice);
+            if (e == cudaSuccess)
+                e = cudaMemcpy(c->ws + L.ctxkv_kn + (size_t)l * g.head_dim * 4, c->drf[l].k_norm,
+                               (size_t)g.head_dim * 4, cudaMemcpyDeviceToDevice);
+            if (e != cudaSuccess) r = fail(DFLASH_ERR_CUDA, "context K/V weights: %s", cudaGetErrorString(e));
+        }
+        const void* wkv[1] = {dst};
+        const int rkv[1] = {g.drf_layers * 2 * g.n_kv * g.head_dim};
+        if (!r)
+            r = plan_gemm(c, &c->ctxkv_all, c->wf(g.drf_wfmt), EPI_QKV, wkv, rkv, 1, g.hidden, c->ws + L.hn,
+                          c->xt_model(false));
+        c->ctxkv_group = !r;
     }
     if (!r && g.dtype == DFLASH_BF16) {
         const int cap = cache_cap(g);

@@ -114,6 +114,12 @@ struct QkvEpi {
     int c_type;
     int cap, max_seq;
     int row_sel;                // rows written: ROWS_FWD (the forward's) or ROWS_COMMIT
+    // group > 1: the weights are `group` consecutive layers' [W_k; W_v]
+    // (n_q == 0), tiles in layer order; layer l's rows go to the caches at
+    // element offset l * cache_stride with k-norm weights k_norm_all + l * hd
+    int group;
+    long long cache_stride;
+    const float* k_norm_all;    // [group][hd]
 };
 
 struct GemmArgs {

@@ -417,13 +417,23 @@ __device__ __forceinline__ void finish_tile(const GemmArgs& a, int tile, const f
             const int nrows = rows_of(a.st, qe.row_sel, &r0);
             const int pos0 = a.st->fwd_pos0;
             const int hd = qe.hd, hpt = GEMM_BN / hd, per = hd / 32;
-            const int h_first = tile * hpt;
+            int tile_l = tile;               // the tile within its layer
+            const float* k_norm = qe.k_norm;
+            size_t lay_off = 0;              // cache element offset of the tile's layer
+            if (qe.group > 1) {
+                const int tpl = 2 * qe.n_kv / hpt;   // tiles per layer: [W_k; W_v]
+                const int l = tile / tpl;
+                tile_l = tile - l * tpl;
+                k_norm = qe.k_norm_all + (size_t)l * hd;
+                lay_off = (size_t)l * (size_t)qe.cache_stride;
+            }
+            const int h_first = tile_l * hpt;
             // head-norm weights of this lane (q and k), loaded once
             float qn[4], kn[4];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 qn[m] = (m < per && qe.n_q > 0) ? qe.q_norm[lane + 32 * m] : 0.f;
-                kn[m] = m < per ? qe.k_norm[lane + 32 * m] : 0.f;
+                kn[m] = m < per ? k_norm[lane + 32 * m] : 0.f;
             }
             for (int item = warp; item < DFL_MAX_ROWS * hpt; item += GEMM_CONSUMERS) {
                 const int t = item / hpt, hi = item % hpt;
@@ -478,7 +488,7 @@ __device__ __forceinline__ void finish_tile(const GemmArgs& a, int tile, const f
                 }
                 const int kh = is_k ? h - qe.n_q : h - qe.n_q - qe.n_kv;
                 void* cache = is_k ? qe.k_cache : qe.v_cache;
-                const size_t base = ((size_t)kh * qe.cap + pos) * hd;
+                const size_t base = lay_off + ((size_t)kh * qe.cap + pos) * hd;
 #pragma unroll
                 for (int m = 0; m < 4; ++m)
                     if (m < per) store_xt(cache, qe.c_type, base + lane + 32 * m, v[m]);
