@@ -76,8 +76,8 @@ int max_chunks(const dflash_config& c) { return cache_cap(c) / ATTN_CHUNK; }
 // in one GEMM over a copy of the layers' [W_k; W_v] (bf16 drafters of more
 // than one layer whose [W_k; W_v] fills whole 128-row tiles).
 bool ctxkv_grouped(const dflash_config& c) {
-    return c.dtype == DFLASH_BF16 && c.drf_wfmt != DFLASH_INT4G64 && c.drf_layers > 1 &&
-           (2 * c.n_kv * c.head_dim) % GEMM_BN == 0 && GEMM_BN % c.head_dim == 0;
+    return c.dtype == DFLASH_BF16 && c.drf_layers > 1 && (2 * c.n_kv * c.head_dim) % GEMM_BN == 0 &&
+           GEMM_BN % c.head_dim == 0;
 }
 
 // ------------------------------------------------------------------ layout
@@ -147,7 +147,12 @@ Layout make_layout(const dflash_config& c) {
     // RoPE angles of every cache position: cos [cap][head_dim / 2], then sin
     L.rtab = take((size_t)2 * cache_cap(c) * (c.head_dim / 2) * 4);
     if (ctxkv_grouped(c)) {   // every draft layer's [W_k; W_v] and k-norm, one after another
-        L.ctxkv_w = take((size_t)c.drf_layers * 2 * c.n_kv * c.head_dim * c.hidden * 2);
+        const size_t rows = (size_t)c.drf_layers * 2 * c.n_kv * c.head_dim;
+        if (c.drf_wfmt == DFLASH_INT4G64) {   // codes [rows][hidden / 2], then scales [hidden / 64][rows]
+            L.ctxkv_w = take(rows * (c.hidden / 2) + rows * (c.hidden / 64) * 2);
+        } else {
+            L.ctxkv_w = take(rows * c.hidden * 2);
+        }
         L.ctxkv_kn = take((size_t)c.drf_layers * c.head_dim * 4);
     }
     L.amax = take(R * 8);
@@ -909,22 +914,33 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
         // the draft layers' [W_k; W_v] and k-norm weights copied one after
         // another: the tap commit streams them in one launch (the drafter's
         // own q/k/v GEMMs keep reading the caller's weights)
-        const size_t kvw = (size_t)g.n_kv * g.head_dim * g.hidden;   // elements of W_k (and W_v)
+        const bool q4 = g.drf_wfmt == DFLASH_INT4G64;
+        const size_t kvd = (size_t)g.n_kv * g.head_dim, rows = (size_t)g.drf_layers * 2 * kvd;
+        const size_t rb = q4 ? g.hidden / 2 : (size_t)g.hidden * 2;   // bytes of one weight row
         uint8_t* dst = c->ws + L.ctxkv_w;
+        uint8_t* sdst = dst + rows * rb;   // INT4: scales [hidden / 64][rows] bf16
         for (int l = 0; l < g.drf_layers && !r; ++l) {
-            cudaError_t e = cudaMemcpy(dst + (2 * l) * kvw * 2, c->drf[l].wk, kvw * 2, cudaMemcpyDeviceToDevice);
-            if (e == cudaSuccess)
-                e = cudaMemcpy(dst + (2 * l + 1) * kvw * 2, c->drf[l].wv, kvw * 2, cudaMemcpyDeviceToDevice);
+            cudaError_t e = cudaSuccess;
+            const void* src[2] = {c->drf[l].wk, c->drf[l].wv};
+            const void* ssrc[2] = {c->drf[l].sk, c->drf[l].sv};
+            for (int j = 0; j < 2 && e == cudaSuccess; ++j) {
+                const size_t row0 = (2 * l + j) * kvd;
+                e = cudaMemcpy(dst + row0 * rb, src[j], kvd * rb, cudaMemcpyDeviceToDevice);
+                if (q4 && e == cudaSuccess)   // columns row0.. of every scale row
+                    e = cudaMemcpy2D(sdst + row0 * 2, rows * 2, ssrc[j], kvd * 2, kvd * 2, g.hidden / 64,
+                                     cudaMemcpyDeviceToDevice);
+            }
             if (e == cudaSuccess)
                 e = cudaMemcpy(c->ws + L.ctxkv_kn + (size_t)l * g.head_dim * 4, c->drf[l].k_norm,
                                (size_t)g.head_dim * 4, cudaMemcpyDeviceToDevice);
             if (e != cudaSuccess) r = fail(DFLASH_ERR_CUDA, "context K/V weights: %s", cudaGetErrorString(e));
         }
         const void* wkv[1] = {dst};
-        const int rkv[1] = {g.drf_layers * 2 * g.n_kv * g.head_dim};
+        const void* skv[1] = {sdst};
+        const int rkv[1] = {(int)rows};
         if (!r)
             r = plan_gemm(c, &c->ctxkv_all, c->wf(g.drf_wfmt), EPI_QKV, wkv, rkv, 1, g.hidden, c->ws + L.hn,
-                          c->xt_model(false));
+                          c->xt_model(false), q4 ? skv : nullptr);
         c->ctxkv_group = !r;
     }
     if (!r && g.dtype == DFLASH_BF16) {

@@ -164,8 +164,9 @@ size_t dflash_kv_draft_bytes(const dflash_config* cfg /*host*/);
  * config guard fires before any buffer is built), builds the TMA
  * descriptors, zeroes the workspace's counters on the legacy stream and
  * returns a context in *out (host).  Borrowed buffers must outlive it.
- * With a bf16 drafter of more than one layer it also copies every draft
- * layer's W_k, W_v and k_norm into the workspace: the tap commit projects
+ * With a bf16 model whose drafter has more than one layer it also copies
+ * every draft layer's W_k, W_v (INT4: codes and scales) and k_norm into the
+ * workspace: the tap commit projects
  * the committed context rows for all layers in one GEMM over that copy, so
  * a change to those weights after dflash_init reaches the drafter's own
  * forwards but not its context rows (make a new context instead).
