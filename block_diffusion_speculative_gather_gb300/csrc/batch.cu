@@ -272,18 +272,24 @@ struct BatchCtxKvArgs {
     const float* rope_cos;          // [R][hd / 2] (the verify's positions)
     const float* rope_sin;
     __half* cache;                  // every sequence's draft cache [S][layers][2][n_kv][cap][hd]
-    int n_layers, layer;
+    int n_layers;
+    // layers layer0 .. layer0 + nl - 1: y rows hold their K and V one layer
+    // after another, k_norm their weights [nl][hd]
+    int layer0, nl;
 };
 
-// One warp per (row, kv head, K or V): the committed rows t < fwd_commit of
-// each sequence, at positions fwd_pos0 + t: k RMSNorm and RoPE on K, both
-// into the sequence's draft cache (the round's tap-commit formulas).
+// One warp per (row, layer, kv head, K or V): the committed rows t <
+// fwd_commit of each sequence, at positions fwd_pos0 + t: k RMSNorm and
+// RoPE on K, both into the sequence's draft cache (the round's tap-commit
+// formulas).
 __global__ void batch_ctx_kv_kernel(BatchCtxKvArgs a) {
     pdl_trigger();
     pdl_wait();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (warp >= a.rows * a.n_kv * 2) return;
-    const int r = warp / (2 * a.n_kv), rem = warp % (2 * a.n_kv), sq = r >> 4, t = r & 15;
+    if (warp >= a.rows * a.nl * a.n_kv * 2) return;
+    const int per_row = a.nl * 2 * a.n_kv;
+    const int r = warp / per_row, rl = warp % per_row, li = rl / (2 * a.n_kv), rem = rl % (2 * a.n_kv);
+    const int sq = r >> 4, t = r & 15;
     DevState* st = a.sts[sq];
     if (t < st->fwd_commit_r0 || t >= st->fwd_commit_r0 + st->fwd_commit) return;
     const bool is_k = rem < a.n_kv;
@@ -294,7 +300,8 @@ __global__ void batch_ctx_kv_kernel(BatchCtxKvArgs a) {
         if (lane == 0) set_error(st, DERR_INDEX, pos);
         return;
     }
-    const float* src = a.y + (size_t)r * 2 * a.n_kv * hd + (size_t)rem * hd;
+    const float* src = a.y + (size_t)r * per_row * hd + (size_t)rl * hd;
+    const float* k_norm = a.k_norm + (size_t)li * hd;
     float v[4];
 #pragma unroll
     for (int m = 0; m < 4; ++m) v[m] = m < per ? src[lane + 32 * m] : 0.f;
@@ -305,10 +312,10 @@ __global__ void batch_ctx_kv_kernel(BatchCtxKvArgs a) {
         ss = warp_sum(ss);
         const float inv = 1.0f / sqrtf(ss / (float)hd + a.eps);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) v[m] = m < per ? v[m] * inv * a.k_norm[lane + 32 * m] : 0.f;
+        for (int m = 0; m < 4; ++m) v[m] = m < per ? v[m] * inv * k_norm[lane + 32 * m] : 0.f;
         rope_pair(v, per, a.rope_cos + (size_t)r * (hd / 2), a.rope_sin + (size_t)r * (hd / 2), lane);
     }
-    const size_t run = (((size_t)sq * a.n_layers + a.layer) * 2 + (is_k ? 0 : 1)) * a.n_kv + kh;
+    const size_t run = (((size_t)sq * a.n_layers + a.layer0 + li) * 2 + (is_k ? 0 : 1)) * a.n_kv + kh;
     __half* dst = a.cache + (run * a.cap + pos) * hd;
 #pragma unroll
     for (int m = 0; m < 4; ++m)
@@ -360,6 +367,11 @@ struct dflash_batch {
     };
     std::vector<LayerMaps> tl, dl;
     DenseMaps lm{}, fc{};
+    // the tap commit's context K/V of every draft layer in one GEMM, over the
+    // first context's copy of the layers' [W_k; W_v] (when it has one)
+    DenseMaps ctxkv_all{};
+    bool grouped_ctxkv = false;
+    const float* ctxkv_knorm = nullptr;
     CUtensorMap qmap{}, kvmap_t{}, kvmap_d{};
     float* verify_logits = nullptr;
     float* draft_logits = nullptr;
@@ -405,7 +417,9 @@ BatchLayout batch_layout(const dflash_config& g, int S, int sms) {
     const size_t R = (size_t)16 * S;
     const int H = g.hidden, qd = g.n_q * g.head_dim, kvd = g.n_kv * g.head_dim, F = g.ffn;
     const size_t wmax = (size_t)std::max(std::max(H, qd), F);
-    const size_t ymax = (size_t)std::max(std::max(qd + 2 * kvd, 2 * F), std::max(H, 2 * kvd));
+    // the grouped context K/V of the tap commit: every draft layer's K and V
+    const int kv_all = g.drf_layers * 2 * kvd;
+    const size_t ymax = (size_t)std::max(std::max(qd + 2 * kvd, 2 * F), std::max(H, kv_all));
     const int tw = g.drf_layers > 0 ? g.n_taps * H : 0;
     // partial tiles of the largest split GEMM the round runs
     size_t pf = 0;
@@ -420,6 +434,7 @@ BatchLayout batch_layout(const dflash_config& g, int S, int sms) {
     if (tw) {
         need(H, tw);
         need(2 * kvd, H);
+        need(kv_all, H);
     }
     BatchLayout L{};
     size_t o = 0;
@@ -811,6 +826,14 @@ int dflash_batch_init(const dflash_config* cfg, const dflash_weights* w, int32_t
         const int rf[1] = {H};
         r = dense_maps(&b->fc, b->thi, b->tlo, R, g.n_taps * H, wf, rf, 1);
     }
+    const void* gw = nullptr;
+    int grows = 0;
+    if (!r && g.drf_layers > 0 && ctx_grouped_ctxkv(b->ctx[0], &gw, &b->ctxkv_knorm, &grows)) {
+        const void* wk[1] = {gw};
+        const int rk[1] = {grows};
+        r = dense_maps(&b->ctxkv_all, b->hi, b->lo, R, H, wk, rk, 1);
+        b->grouped_ctxkv = !r;
+    }
     const int group_rows = (g.n_q / g.n_kv) * 16;
     if (!r)
         r = encode_map(&b->qmap, b->q, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.head_dim, (uint64_t)R * g.n_q, 64,
@@ -881,23 +904,33 @@ int dflash_batch_verify_accept(dflash_batch* b, const int32_t* draft_ids, int32_
     BTRY(launch_ctx_rows(cr, s));
     const dflash_layer* dl = ctx_layers(b->ctx[0], false);
     const int cap = (g.max_seq + 63) / 64 * 64;
+    BatchCtxKvArgs ca{};
+    ca.y = b->y;
+    ca.sts = b->sts;
+    ca.rows = b->R;
+    ca.n_kv = g.n_kv;
+    ca.head_dim = g.head_dim;
+    ca.cap = cap;
+    ca.max_seq = g.max_seq;
+    ca.eps = g.rms_eps;
+    ca.rope_cos = b->rcos;
+    ca.rope_sin = b->rsin;
+    ca.cache = reinterpret_cast<__half*>(b->kv_d);
+    ca.n_layers = g.drf_layers;
+    if (b->grouped_ctxkv) {   // every layer in one GEMM over the first context's grouped weights
+        const int kv_all = g.drf_layers * 2 * kvd;
+        if ((r = dense(b, b->ctxkv_all, kv_all, H, 1 << 30, 1 << 30, b->y, nullptr, s))) return r;
+        ca.k_norm = b->ctxkv_knorm;
+        ca.layer0 = 0;
+        ca.nl = g.drf_layers;
+        BTRY(launch_warps(batch_ctx_kv_kernel, (long long)b->R * g.drf_layers * g.n_kv * 2, s, ca));
+        return DFLASH_OK;
+    }
     for (int l = 0; l < g.drf_layers; ++l) {
         if ((r = dense(b, b->dl[l].ctxkv, 2 * kvd, H, kvd, 1 << 30, b->y, nullptr, s))) return r;
-        BatchCtxKvArgs ca{};
-        ca.y = b->y;
-        ca.sts = b->sts;
-        ca.rows = b->R;
-        ca.n_kv = g.n_kv;
-        ca.head_dim = g.head_dim;
-        ca.cap = cap;
-        ca.max_seq = g.max_seq;
         ca.k_norm = dl[l].k_norm;
-        ca.eps = g.rms_eps;
-        ca.rope_cos = b->rcos;
-        ca.rope_sin = b->rsin;
-        ca.cache = reinterpret_cast<__half*>(b->kv_d);
-        ca.n_layers = g.drf_layers;
-        ca.layer = l;
+        ca.layer0 = l;
+        ca.nl = 1;
         BTRY(launch_warps(batch_ctx_kv_kernel, (long long)b->R * g.n_kv * 2, s, ca));
     }
     return DFLASH_OK;

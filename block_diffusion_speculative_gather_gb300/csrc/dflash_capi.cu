@@ -766,6 +766,14 @@ void rope_table(const dflash_ctx* c, const float** cos_tab, const float** sin_ta
     *sin_tab = *cos_tab + (size_t)cap * half;
     *rows = cap;
 }
+bool ctx_grouped_ctxkv(const dflash_ctx* c, const void** w, const float** k_norm, int* rows) {
+    const dflash_config& g = c->cfg;
+    if (!c->ctxkv_group || g.drf_wfmt == DFLASH_INT4G64) return false;
+    *w = c->ws + c->L.ctxkv_w;
+    *k_norm = c->buf<float>(c->L.ctxkv_kn);
+    *rows = g.drf_layers * 2 * g.n_kv * g.head_dim;
+    return true;
+}
 const dflash_layer* ctx_layers(const dflash_ctx* c, bool target) {
     return target ? c->tgt.data() : c->drf.data();
 }
