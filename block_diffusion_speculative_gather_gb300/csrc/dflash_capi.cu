@@ -918,37 +918,20 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
         r = plan_gemm(c, &c->fc, c->wf(g.dtype), EPI_NORMOUT, wfc, rfc, 1, g.n_taps * g.hidden,
                       c->ws + L.taps, c->act_xt());
     }
-    if (!r && ctxkv_grouped(g)) {
+    const char* cg_env = getenv("DFLASH_CTXKV_GROUP");   // "0": one context K/V GEMM per draft layer
+    if (!r && ctxkv_grouped(g) && !(cg_env && cg_env[0] == '0')) {
         // the draft layers' [W_k; W_v] and k-norm weights copied one after
         // another: the tap commit streams them in one launch (the drafter's
         // own q/k/v GEMMs keep reading the caller's weights)
+        // (the copy itself is made after the workspace is cleared, below)
         const bool q4 = g.drf_wfmt == DFLASH_INT4G64;
-        const size_t kvd = (size_t)g.n_kv * g.head_dim, rows = (size_t)g.drf_layers * 2 * kvd;
+        const size_t rows = (size_t)g.drf_layers * 2 * g.n_kv * g.head_dim;
         const size_t rb = q4 ? g.hidden / 2 : (size_t)g.hidden * 2;   // bytes of one weight row
-        uint8_t* dst = c->ws + L.ctxkv_w;
-        uint8_t* sdst = dst + rows * rb;   // INT4: scales [hidden / 64][rows] bf16
-        for (int l = 0; l < g.drf_layers && !r; ++l) {
-            cudaError_t e = cudaSuccess;
-            const void* src[2] = {c->drf[l].wk, c->drf[l].wv};
-            const void* ssrc[2] = {c->drf[l].sk, c->drf[l].sv};
-            for (int j = 0; j < 2 && e == cudaSuccess; ++j) {
-                const size_t row0 = (2 * l + j) * kvd;
-                e = cudaMemcpy(dst + row0 * rb, src[j], kvd * rb, cudaMemcpyDeviceToDevice);
-                if (q4 && e == cudaSuccess)   // columns row0.. of every scale row
-                    e = cudaMemcpy2D(sdst + row0 * 2, rows * 2, ssrc[j], kvd * 2, kvd * 2, g.hidden / 64,
-                                     cudaMemcpyDeviceToDevice);
-            }
-            if (e == cudaSuccess)
-                e = cudaMemcpy(c->ws + L.ctxkv_kn + (size_t)l * g.head_dim * 4, c->drf[l].k_norm,
-                               (size_t)g.head_dim * 4, cudaMemcpyDeviceToDevice);
-            if (e != cudaSuccess) r = fail(DFLASH_ERR_CUDA, "context K/V weights: %s", cudaGetErrorString(e));
-        }
-        const void* wkv[1] = {dst};
-        const void* skv[1] = {sdst};
+        const void* wkv[1] = {c->ws + L.ctxkv_w};
+        const void* skv[1] = {c->ws + L.ctxkv_w + rows * rb};   // INT4: scales [hidden / 64][rows]
         const int rkv[1] = {(int)rows};
-        if (!r)
-            r = plan_gemm(c, &c->ctxkv_all, c->wf(g.drf_wfmt), EPI_QKV, wkv, rkv, 1, g.hidden, c->ws + L.hn,
-                          c->xt_model(false), q4 ? skv : nullptr);
+        r = plan_gemm(c, &c->ctxkv_all, c->wf(g.drf_wfmt), EPI_QKV, wkv, rkv, 1, g.hidden, c->ws + L.hn,
+                      c->xt_model(false), q4 ? skv : nullptr);
         c->ctxkv_group = !r;
     }
     if (!r && g.dtype == DFLASH_BF16) {
@@ -1112,6 +1095,36 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
     if (e != cudaSuccess) {
         delete c;
         return fail(DFLASH_ERR_CUDA, "workspace clear: %s", cudaGetErrorString(e));
+    }
+    if (c->ctxkv_group) {
+        // the draft layers' [W_k; W_v] (INT4: codes by rows, scales by
+        // columns) and k-norm weights, one layer after another: the tap
+        // commit streams them in one launch (the drafter's own q/k/v GEMMs
+        // keep reading the caller's weights)
+        const bool q4 = g.drf_wfmt == DFLASH_INT4G64;
+        const size_t kvd = (size_t)g.n_kv * g.head_dim, rows = (size_t)g.drf_layers * 2 * kvd;
+        const size_t rb = q4 ? g.hidden / 2 : (size_t)g.hidden * 2;   // bytes of one weight row
+        uint8_t* dst = c->ws + L.ctxkv_w;
+        uint8_t* sdst = dst + rows * rb;
+        for (int l = 0; l < g.drf_layers && e == cudaSuccess; ++l) {
+            const void* src[2] = {c->drf[l].wk, c->drf[l].wv};
+            const void* ssrc[2] = {c->drf[l].sk, c->drf[l].sv};
+            for (int j = 0; j < 2 && e == cudaSuccess; ++j) {
+                const size_t row0 = (2 * l + j) * kvd;
+                e = cudaMemcpy(dst + row0 * rb, src[j], kvd * rb, cudaMemcpyDeviceToDevice);
+                if (q4 && e == cudaSuccess)   // columns row0.. of every scale row
+                    e = cudaMemcpy2D(sdst + row0 * 2, rows * 2, ssrc[j], kvd * 2, kvd * 2, g.hidden / 64,
+                                     cudaMemcpyDeviceToDevice);
+            }
+            if (e == cudaSuccess)
+                e = cudaMemcpy(c->ws + L.ctxkv_kn + (size_t)l * g.head_dim * 4, c->drf[l].k_norm,
+                               (size_t)g.head_dim * 4, cudaMemcpyDeviceToDevice);
+        }
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) {
+            delete c;
+            return fail(DFLASH_ERR_CUDA, "context K/V weights: %s", cudaGetErrorString(e));
+        }
     }
     if (g.adaptive_block) {
         const int one = 1;

@@ -170,6 +170,8 @@ size_t dflash_kv_draft_bytes(const dflash_config* cfg /*host*/);
  * the committed context rows for all layers in one GEMM over that copy, so
  * a change to those weights after dflash_init reaches the drafter's own
  * forwards but not its context rows (make a new context instead).
+ * Environment DFLASH_CTXKV_GROUP=0 at init runs one context K/V GEMM per
+ * draft layer instead (the same rows to fp32 summation order).
  *
  * Ordering: the calls on one context must be ordered on the GPU (one stream,
  * or streams joined by events); they share the workspace.  The kernels also
