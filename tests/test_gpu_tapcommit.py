@@ -9,7 +9,11 @@ differ only in fp32 summation order, so after the same prefill and the same
 verify (the GPU's own greedy continuation as drafts: every draft accepted,
 16 rows committed) the draft cache rows of the committed positions agree to
 fp16 rounding, the prefill's rows are bit-identical, and the next draft's
-logits agree within a quarter of the parity tolerance.
+logits agree within a quarter of the parity tolerance; the grouped form's
+next draft also matches the oracle's drafter over the same context (the
+oracle target's taps of all P + 16 positions), so a tap commit that writes
+wrong context rows fails here even though speculative decoding, which
+verifies every draft, would stay lossless.
 
 Shapes: a Qwen3-4B-shaped layer (head_dim 128: one head per 128-row tile,
 16 tiles per layer), a head_dim-64 model (two heads per tile) and an INT4
@@ -22,11 +26,13 @@ import torch
 
 from block_diffusion_speculative_gather_gb300 import synth
 from block_diffusion_speculative_gather_gb300.configs import E2E_BF16, Workload
+from oracle import dflash_oracle as O
 from tests import gpu_common as G
-from tests.oracle_inputs import ModelTensors
+from tests.oracle_inputs import ModelTensors, oracle_config, oracle_draft, oracle_target
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
+DEC_TOL = {"hd128": 1e-3, "hd64": 1e-3, "int4-drafter": 2e-3}   # as in the bf16 / INT4 parity modules
 
 QWEN = E2E_BF16.with_(name="tc_qwen", tgt_layers=2, drf_layers=3, tap_layers=(0, 1), prompt_len=40,
                       n_new=48, max_seq=256)
@@ -73,17 +79,24 @@ def test_grouped_tap_commit_matches_per_layer(case, monkeypatch):
         kd = dec.kv_draft.view(torch.float16).view(W.drf_layers, 2, W.n_kv, cap, W.head_dim)
         dl = G.logits_buf(W.vocab)
         dec.set_logits_out(None, dl)
-        dec.draft()
+        ids = dec.draft().cpu().numpy()
         dec.check()
-        out.append((kd[:, :, :, :P + B].float().clone(), dl[1:B].clone()))
+        out.append((kd[:, :, :, :P + B].float().clone(), dl[1:B].clone(), ids[:B - 1].copy()))
         dec.close()
-    (kd_g, dl_g), (kd_p, dl_p) = out
+    (kd_g, dl_g, ids_g), (kd_p, dl_p, _) = out
     assert torch.equal(kd_g[:, :, :, :P], kd_p[:, :, :, :P]), "the prefill's context rows take one path"
     committed = kd_p[:, :, :, P:P + B]
     assert committed.abs().amax(dim=-1).min().item() > 0, "every committed row of every layer is written"
     assert _close_rows(kd_g[:, :, :, P:P + B], committed) < 2.0 ** -8
     err = G.rel_err_rows(dl_g.cpu().numpy(), dl_p.cpu().numpy())
     assert err.max() < TOL / 4, err
+    # the oracle's drafter over the context the commit built: the target's
+    # taps of the prompt and the 16 verified rows, the pending token gg[B]
+    tw, dw, cfg = oracle_target(m), oracle_draft(m), oracle_config(W)
+    _, taps = O.target_forward(tw, cfg, prompt.tolist() + gg[:B], 0,
+                               O.KVCache(W.tgt_layers, W.n_kv, W.head_dim))
+    ref, _ = O.draft_forward(dw, tw.embed, cfg, taps, gg[B], P + B, B)
+    G.check_rows(f"tap_commit_{case}", dl_g.cpu().numpy(), ids_g, ref[1:], TOL, DEC_TOL[case])
 
 
 def test_grouped_tap_commit_many_sequences(monkeypatch):
