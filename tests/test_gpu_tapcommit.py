@@ -102,7 +102,8 @@ def test_grouped_tap_commit_matches_per_layer(case, monkeypatch):
 def test_grouped_tap_commit_many_sequences(monkeypatch):
     """The many-sequence round's tap commit (one dense GEMM over the first
     context's copy and one cache-row launch for every layer) against its
-    per-layer form, two sequences of different prompt lengths."""
+    per-layer form, two sequences of different prompt lengths, and each
+    sequence's next draft against the oracle's drafter over its context."""
     from block_diffusion_speculative_gather_gb300.runtime import DFlashBatch
     G.build_lib()
     W = QWEN
@@ -126,11 +127,13 @@ def test_grouped_tap_commit_many_sequences(monkeypatch):
         kd = dec.kv_draft.view(torch.float16).view(2, W.drf_layers, 2, W.n_kv, cap, W.head_dim)
         dl = torch.zeros((2 * 16, W.vocab), dtype=torch.float32, device="cuda")
         dec.set_logits_out(None, dl)
-        dec.draft()
+        ids = dec.draft().cpu().numpy()
         dec.check()
-        out.append(([kd[s, :, :, :, :lens[s] + B].float().clone() for s in range(2)], dl.clone()))
+        out.append(([kd[s, :, :, :, :lens[s] + B].float().clone() for s in range(2)], dl.clone(), ids.copy(),
+                    gg))
         dec.close()
-    (kd_g, dl_g), (kd_p, dl_p) = out
+    (kd_g, dl_g, ids_g, gg), (kd_p, dl_p, _, _) = out
+    tw, dw, cfg = oracle_target(m), oracle_draft(m), oracle_config(W)
     for s, L in enumerate(lens):
         assert torch.equal(kd_g[s][..., :L, :], kd_p[s][..., :L, :])
         committed = kd_p[s][..., L:L + B, :]
@@ -139,3 +142,8 @@ def test_grouped_tap_commit_many_sequences(monkeypatch):
         rows = slice(16 * s + 1, 16 * s + B)
         err = G.rel_err_rows(dl_g[rows].cpu().numpy(), dl_p[rows].cpu().numpy())
         assert err.max() < TOL / 4, (s, err)
+        _, taps = O.target_forward(tw, cfg, prompts[s].tolist() + gg[s][:B], 0,
+                                   O.KVCache(W.tgt_layers, W.n_kv, W.head_dim))
+        ref, _ = O.draft_forward(dw, tw.embed, cfg, taps, gg[s][B], L + B, B)
+        G.check_rows(f"tap_commit_batch_{s}", dl_g[rows].cpu().numpy(), ids_g[s][:B - 1], ref[1:], TOL,
+                     DEC_TOL["hd128"])
