@@ -17,8 +17,9 @@ verifies every draft, would stay lossless.
 
 Shapes: a Qwen3-4B-shaped layer (head_dim 128: one head per 128-row tile,
 16 tiles per layer), a head_dim-64 model (two heads per tile) and an INT4
-drafter (codes copied by rows, their bf16 scales by columns); the
-many-sequence round (which reuses the first context's copy) at S = 2.
+drafter (codes copied by rows, their bf16 scales by columns), a 32-key
+drafter window that the commit slides; the many-sequence round (which
+reuses the first context's copy) at S = 2.
 """
 
 import pytest
@@ -32,7 +33,7 @@ from tests.oracle_inputs import ModelTensors, oracle_config, oracle_draft, oracl
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
-DEC_TOL = {"hd128": 1e-3, "hd64": 1e-3, "int4-drafter": 2e-3}   # as in the bf16 / INT4 parity modules
+DEC_TOL = {"hd128": 1e-3, "hd64": 1e-3, "int4-drafter": 2e-3, "hd128-window": 1e-3}   # as in the bf16 / INT4 parity modules
 
 QWEN = E2E_BF16.with_(name="tc_qwen", tgt_layers=2, drf_layers=3, tap_layers=(0, 1), prompt_len=40,
                       n_new=48, max_seq=256)
@@ -42,6 +43,9 @@ CASES = {
                      tgt_layers=2, drf_layers=3, tap_layers=(0, 1), block=16, window=0, dtype="bf16",
                      prompt_len=200, n_new=40, max_seq=512),
     "int4-drafter": QWEN.with_(name="tc_int4", drf_int4=True),
+    # a 32-key drafter window: the next draft sees prefill rows 24..39 and
+    # the committed rows 40..55
+    "hd128-window": QWEN.with_(name="tc_window", window=32),
 }
 
 
