@@ -1007,6 +1007,12 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
     }
     // window ingest on the dense tcgen05 GEMM (DFLASH_DENSE_INGEST=0 keeps
     // the 16-row chunks through the round's kernels)
+    // the tail box map of a one-segment dense weight: 160-column tiles
+    auto tail_map = [&](DenseMaps& m, const void* wt, CUtensorMapDataType dt, uint64_t k, uint64_t n) {
+        const int e = make_map_raw(&m.w_tail, wt, dt, 2, k, n, DT_BK, DT_WTAIL, CU_TENSOR_MAP_SWIZZLE_128B);
+        m.has_tail = e ? 0 : 1;
+        return e;
+    };
     const char* di_env = getenv("DFLASH_DENSE_INGEST");
     if (!r && dense_ingest_ok(g) && !(di_env && di_env[0] == '0')) {
         const uint64_t K1 = (uint64_t)g.n_taps * g.hidden, kvr = (uint64_t)g.n_kv * g.head_dim;
@@ -1014,6 +1020,7 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
         const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
         r = make_map_raw(&c->d_fc.x, c->ws + L.pf_x, bf, 2, K1, PF_ROWS, DT_BK, DT_BM, sw);
         if (!r) r = make_map_raw(&c->d_fc.w[0], w->fc, bf, 2, K1, g.hidden, DT_BK, DT_WBOX, sw);
+        if (!r) r = tail_map(c->d_fc, w->fc, bf, K1, g.hidden);
         if (!r) {
             c->d_fc_hl = c->d_fc;
             r = make_map_raw(&c->d_fc_hl.x_lo, c->ws + L.pf_xlo, bf, 2, K1, PF_ROWS, DT_BK, DT_BM, sw);
@@ -1055,10 +1062,12 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
             if (!r) r = make_map_raw(&P.qkv.w[0], pw, xt, 2, g.hidden, qd + 2 * kvd, DT_BK, DT_WBOX, sw);
             if (!r) r = xmaps(P.o, qd);
             if (!r) r = make_map_raw(&P.o.w[0], pw, xt, 2, qd, g.hidden, DT_BK, DT_WBOX, sw);
+            if (!r) r = tail_map(P.o, pw, xt, qd, g.hidden);
             if (!r) r = xmaps(P.gu, g.hidden);
             if (!r) r = make_map_raw(&P.gu.w[0], pw, xt, 2, g.hidden, 2 * (uint64_t)g.ffn, DT_BK, DT_WBOX, sw);
             if (!r) r = xmaps(P.down, g.ffn, true);
             if (!r) r = make_map_raw(&P.down.w[0], pw, xt, 2, g.ffn, g.hidden, DT_BK, DT_WBOX, sw);
+            if (!r) r = tail_map(P.down, pw, xt, g.ffn, g.hidden);
         }
         for (int l = 0; l < g.tgt_layers && !r && !q4; ++l) {
             const dflash_layer& lw = c->tgt[l];
@@ -1069,11 +1078,13 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
             if (!r) r = make_map_raw(&P.qkv.w[2], lw.wv, bf, 2, g.hidden, kvd, DT_BK, DT_WBOX, sw);
             if (!r) r = xmaps(P.o, qd);
             if (!r) r = make_map_raw(&P.o.w[0], lw.wo, bf, 2, qd, g.hidden, DT_BK, DT_WBOX, sw);
+            if (!r) r = tail_map(P.o, lw.wo, bf, qd, g.hidden);
             if (!r) r = xmaps(P.gu, g.hidden);
             if (!r) r = make_map_raw(&P.gu.w[0], lw.w_gate, bf, 2, g.hidden, g.ffn, DT_BK, DT_WBOX, sw);
             if (!r) r = make_map_raw(&P.gu.w[1], lw.w_up, bf, 2, g.hidden, g.ffn, DT_BK, DT_WBOX, sw);
             if (!r) r = xmaps(P.down, g.ffn, true);
             if (!r) r = make_map_raw(&P.down.w[0], lw.w_down, bf, 2, g.ffn, g.hidden, DT_BK, DT_WBOX, sw);
+            if (!r) r = tail_map(P.down, lw.w_down, bf, g.ffn, g.hidden);
         }
         if (!r)
             r = make_map_raw(&c->pp_qmap, c->ws + L.pp_q, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.head_dim,
@@ -1083,6 +1094,7 @@ int dflash_init(const dflash_config* cfg, const dflash_weights* w, void* kv_targ
             r = make_map_raw(&c->d_fc_pp.x, c->ws + L.pp_thi, bf, 2, K1, PF_ROWS, DT_BK, DT_BM, sw);
             if (!r) r = make_map_raw(&c->d_fc_pp.x_lo, c->ws + L.pp_tlo, bf, 2, K1, PF_ROWS, DT_BK, DT_BM, sw);
             if (!r) r = make_map_raw(&c->d_fc_pp.w[0], w->fc, bf, 2, K1, g.hidden, DT_BK, DT_WBOX, sw);
+            if (!r) r = tail_map(c->d_fc_pp, w->fc, bf, K1, g.hidden);
         }
         c->dense_prefill = !r;
     }

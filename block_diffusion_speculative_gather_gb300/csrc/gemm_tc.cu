@@ -115,7 +115,8 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
         tma_prefetch_desc(&maps.w[seg]);
         if (a.swiglu) tma_prefetch_desc(&maps.w[a.up_map]);
     }
-    if (warp == 1) tc::tmem_alloc(s_tmem, BN);
+    constexpr uint32_t TCOLS = BN <= 128 ? 128u : 256u;   // a power of two >= BN
+    if (warp == 1) tc::tmem_alloc(s_tmem, TCOLS);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -130,9 +131,12 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
             tma_load_2d(wst, &maps.w[0], bar, kx, HB * t);
             tma_load_2d(wst + HB * 128, &maps.w[a.up_map], bar, kx, a.up_row + HB * t);
         } else {
+            constexpr int NB = BN / DT_WBOX, TAIL = BN % DT_WBOX;
+            static_assert(TAIL == 0 || TAIL == DT_WTAIL, "tile width: whole weight boxes and one tail box");
 #pragma unroll
-            for (int b = 0; b < BN / DT_WBOX; ++b)
+            for (int b = 0; b < NB; ++b)
                 tma_load_2d(wst + b * DT_WBOX * 128, &maps.w[seg], bar, kx, wrow + b * DT_WBOX);
+            if (TAIL) tma_load_2d(wst + NB * DT_WBOX * 128, &maps.w_tail, bar, kx, wrow + NB * DT_WBOX);
         }
     };
     const int pre = nkb < STAGES ? nkb : STAGES;
@@ -270,7 +274,7 @@ gemm_dense_kernel(const __grid_constant__ DenseMaps maps, const DenseArgs a) {
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 1) tc::tmem_dealloc(tm, BN);
+    if (warp == 1) tc::tmem_dealloc(tm, TCOLS);
 }
 
 // y = sum over the split slabs in split order (z = 0, 1, ...), four
@@ -344,6 +348,15 @@ int launch_bn(const DenseMaps& maps, const DenseArgs& a, cudaStream_t s) {
     const long long mt = (a.M + DT_BM - 1) / DT_BM;
     const long long w256 = (mt * ((a.N + 255) / 256) + sms - 1) / sms;
     const long long w128 = (mt * ((a.N + 127) / 128) + sms - 1) / sms;
+    // a 160-column tile's stage is bound by its copies (32 KB of x planes +
+    // 20 KB of weights against 64 KB for 256 columns): about 0.8 of a
+    // 256-column one too; it wins where it takes a wave fewer than 128
+    // columns and the same as 256 (o and down over 1024 rows: 128 tiles on
+    // 152 SMs, against 160 and 80)
+    if (maps.has_tail && a.N % 160 == 0 && !a.swiglu && !a.amax && a.splits <= 1) {
+        const long long w160 = (mt * (a.N / 160) + sms - 1) / sms;
+        if (w160 * 4 < w256 * 5 && w160 <= w128) return launch_one<SPLIT, F16, 160>(maps, a, s);
+    }
     if (w128 * 4 < w256 * 5) return launch_one<SPLIT, F16, 128>(maps, a, s);
     return launch_one<SPLIT, F16, 256>(maps, a, s);
 }

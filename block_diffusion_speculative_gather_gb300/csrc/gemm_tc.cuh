@@ -20,12 +20,18 @@ constexpr int DT_BM = 128;   // rows of x per CTA (tensor-memory lanes)
 constexpr int DT_BN = 256;   // widest output tile (tensor-memory columns); 128 where it balances better
 constexpr int DT_WBOX = 128; // rows of one weight TMA box (a 256-column tile loads two)
 constexpr int DT_SWBOX = 64; // rows of a weight box of the SwiGLU form (gate and up halves)
+constexpr int DT_WTAIL = 32; // rows of the tail box of a 160-column tile (128 + 32)
 constexpr int DT_BK = 64;    // k per pipeline stage (one 128-byte swizzled row)
 
 struct DenseMaps {
     CUtensorMap x;      // [M][K] bf16, box [128 rows][64]
     CUtensorMap x_lo;   // low plane of x when x_split (same shape)
     CUtensorMap w[3];   // [N_i][K] segments concatenated along n, box [128 rows][64]
+    // w[0] again with a box of DT_WTAIL rows: the last rows of a 160-column
+    // tile (one-segment weights); has_tail = 1 when it is set, which lets
+    // the automatic tile width pick 160 columns
+    CUtensorMap w_tail;
+    int has_tail;
 };
 
 struct DenseArgs {
@@ -48,7 +54,8 @@ struct DenseArgs {
     float* part;
     int keep_parts;     // split-K: 1 = no reduce launch; the slabs stay for
                         // a consumer that sums them itself (y unused then)
-    int bn;             // tile width: 0 = chosen by wave balance, else 128 or 256
+    int bn;             // tile width: 0 = chosen by wave balance (160 too where maps.has_tail
+                        // and N is a multiple of 160), else 128 or 256
     // argmax epilogue (LM head): per row the packed key (orderable logit,
     // ~column) of the largest column, atomicMax into amax[row]
     unsigned long long* amax;   // NULL: the plain fp32 store
