@@ -632,7 +632,7 @@ def run_ours(args):
         "verify_ms_T1": round(t1row, 4),
         "round_ms_T16": round(t_max / args.steps, 4),
         "prefill": {"prompt_tokens": w.prompt_len, "ms": round(prefill_ms, 3),
-                    "path": "dense tcgen05 forward of rows before the last 16-row chunk"
+                    "path": "dense tcgen05 forward of every prompt row; the last 16-row chunk then through the final norm into the round LM head"
                             if w.prompt_len > 16 else "16-row forwards"},
         "gpu_launches": launches_per_round * args.steps,
         "attention_form": {m: {2: "tcgen05", 1: "mma.sync split-KV", 0: "partial + combine"}[
