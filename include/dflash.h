@@ -32,6 +32,11 @@
  * budget, statistics) lives in device memory, so a round needs no host
  * round-trip and the launches of a round can be captured in a CUDA graph.
  * Calls on one context must not overlap on the GPU (one stream per context).
+ * Every kernel is launched with programmatic dependent launch: it may be
+ * scheduled while its predecessor drains and waits for it only before
+ * touching memory the predecessor writes.  Environment DFLASH_PDL=0, read
+ * once when the library loads, launches every kernel plainly instead (same
+ * results; a latency study switch).
  *
  * Errors.  Every int-returning call returns DFLASH_OK (0) or a negative
  * DFLASH_ERR_* code and never aborts; dflash_last_error() gives a message
