@@ -289,7 +289,7 @@ __global__ void embed_rows_kernel(const int32_t* tokens, int rows, const __nv_bf
 // use, instead of one round trip per element or slab (rows wider than
 // RN_THREADS x RN_PER = 4096 take the plain loop).
 constexpr int RN_THREADS = 512, RN_PER = 8;
-__global__ void __launch_bounds__(RN_THREADS) resid_norm_kernel(ResidNormArgs a) {
+__device__ __forceinline__ void resid_norm_row(const ResidNormArgs& a) {
     pdl_trigger();
     pdl_wait();
     constexpr int PER = RN_PER, NT = RN_THREADS;
@@ -387,6 +387,13 @@ __global__ void __launch_bounds__(RN_THREADS) resid_norm_kernel(ResidNormArgs a)
             store_hilo(a.hi, a.lo, (size_t)r * a.hidden + j, x[j] * a.w[j] * rstd, a.f16);
     }
 }
+
+__global__ void __launch_bounds__(RN_THREADS) resid_norm_kernel(ResidNormArgs a) { resid_norm_row(a); }
+
+// The same row for the many rows of a dense pass, with the registers capped
+// so that two CTAs share an SM (at one CTA per SM the kernel waits on its
+// loads).
+__global__ void __launch_bounds__(RN_THREADS, 2) resid_norm_wide_kernel(ResidNormArgs a) { resid_norm_row(a); }
 
 // One warp per (row, head) over the q, k and v heads; lane l holds
 // elements l + 32 m (rotate-half pairs m with m + per/2 in the same lane).
@@ -745,6 +752,8 @@ int launch_embed_rows(const int32_t* tokens, int rows, const void* embed, int hi
 
 int launch_resid_norm(const ResidNormArgs& a, cudaStream_t s) {
     if (a.rows < 1) return 0;
+    if (a.rows > 512)
+        return ok(launch_k(resid_norm_wide_kernel, dim3((unsigned)a.rows), dim3(RN_THREADS), 0, s, a));
     return ok(launch_k(resid_norm_kernel, dim3((unsigned)a.rows), dim3(RN_THREADS), 0, s, a));
 }
 
